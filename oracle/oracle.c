@@ -1,0 +1,745 @@
+/*
+ * oracle.c -- plain, slow, single-threaded CPU oracle for the chunked ring
+ * allreduce with gradient-compression codecs.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg are the only callers.  The GPU library never
+ * links, includes or calls this file, and this file includes nothing from the
+ * GPU library: its enums, constants, conversions and wire formats are written
+ * out here on their own, from the definitions below.
+ *
+ * Build:  gcc -std=c11 -O2 -ffp-contract=off -fno-fast-math -fPIC -shared
+ * (no FMA contraction, no reassociation: every float operation is one IEEE
+ * binary32 operation rounded to nearest-even, in the order written).
+ *
+ * Sources (web pages, cited by title and section):
+ *  [P2] "从零实现集合通信" (collective ops from scratch, aibook lesson 76):
+ *       section "两趟实现 ring allreduce" (two-pass ring; per-rank byte and
+ *       step table: ring 2T(N-1)/N, tree T log2 N, broadcast T, allgather and
+ *       reduce_scatter T(N-1)/N), section "练习" (tree variant, byte counter).
+ *  [P4] "CCCL通信压缩库：突破LLM训练通信墙的工程实践":
+ *       §2.1 (sparse values+indices format above a sparsity threshold; block
+ *       floating point, one shared exponent per block of e.g. 128 elements,
+ *       8- or 4-bit mantissas; difference against the previous round),
+ *       §2.2 (the tensor is cut into chunks that are compressed, sent,
+ *       decompressed and reduced one after the other),
+ *       §3.3 (compression types block_fp16_to_8bit / block_fp16_to_4bit /
+ *       sparse / diff; sparsity_threshold 0.5).
+ *
+ * Readings taken where the pages are silent (each one is listed, with its
+ * reason, in the design notes of the repository):
+ *  R1  ring steps are numbered s = 1..N-1: at reduce-scatter step s rank r
+ *      sends chunk (r-s) mod N; at allgather step s it sends (r-s+1) mod N.
+ *  R3  n = ceil(T/N); chunk c = [c*n, min(T,(c+1)*n)), possibly short/empty.
+ *  R4  lossless messages carry fp32 (the accumulator type).
+ *  B1  block exponent e = floor(log2 max|x|), clamped below at -126.
+ *  B2  q = bits-2; m = clamp(rne(x * 2^(q-e)), -(2^(bits-1)-1), +(...));
+ *      decode m * 2^(e-q).
+ *  B5  planar BFP message: exps[ceil(len/128)] then mants (int8[len], or
+ *      uint8[ceil(len/2)] with element 2j in the low nibble).
+ *  B6  every reduce-scatter hop re-encodes the sender's fp32 partial; the
+ *      owner encodes its full sum once; the allgather forwards those codes
+ *      unchanged; every rank (owner included) outputs decode(codes).
+ *  S1  an element is "zero" iff its fp32 bit pattern is +0.0.
+ *  S2  sparse iff nnz < (1 - threshold) * len (in double); tie -> dense.
+ *  S3  ring messages are cut into slices of `slice` elements; each slice is
+ *      one message: 8-byte header {fmt, nnz}, then fp32 values[nnz] and
+ *      int32 slice-relative indices[nnz] ascending (sparse), or fp32[len]
+ *      (dense).
+ *  S4  sparse accumulate: acc[i] = acc[i] + v at listed positions; other
+ *      positions keep acc[i].
+ *  D1  diff: d = cur - prev (fp32); the ring runs on d.
+ *  D2  epilogue: out = base + (v / N) when a base (previous result) is given
+ *      and averaging is on; v / N with averaging only; v otherwise.
+ *  RS  reduce-scatter: the owner's output is its fp32 sum (not re-encoded).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* element types and IEEE conversions, written from the binary16 /     */
+/* bfloat16 definitions (sign, exponent, significand)                  */
+/* ------------------------------------------------------------------ */
+
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2 };
+enum { OR_CODEC_NONE = 0, OR_CODEC_BFP = 1, OR_CODEC_SPARSE = 2 };
+enum { OR_BFP_BLOCK = 128 };
+
+size_t oracle_dtype_size(int t) { return t == OR_F32 ? 4 : 2; }
+
+/* binary16 -> binary32: exact. */
+float oracle_f16_to_f32(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int ex = (h >> 10) & 0x1f;
+    int man = h & 0x3ff;
+    float v;
+    if (ex == 0)
+        v = ldexpf((float)man, -24); /* subnormal: man * 2^-24 */
+    else if (ex == 31)
+        v = man ? NAN : INFINITY;
+    else
+        v = ldexpf((float)(1024 + man), ex - 25); /* 1.man * 2^(ex-15) */
+    return sign ? -v : v;
+}
+
+/* binary32 -> binary16, round to nearest even. */
+uint16_t oracle_f32_to_f16(float x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    float a = fabsf(x);
+    if (isnan(x))
+        return sign | 0x7e00;
+    /* largest finite half is 65504; the midpoint to 65536 is 65520 and
+     * rounds to even, i.e. up, so everything from 65520 on overflows */
+    if (a >= 65520.0f)
+        return sign | 0x7c00;
+    if (a < ldexpf(1.0f, -14)) {
+        /* subnormal range: spacing 2^-24 */
+        float q = nearbyintf(ldexpf(a, 24)); /* exact scaling, then RNE */
+        return sign | (uint16_t)q;           /* q == 1024 encodes 2^-14 */
+    }
+    int E;
+    frexpf(a, &E); /* a = f * 2^E, f in [0.5, 1) */
+    int e = E - 1; /* floor(log2 a) */
+    float m = nearbyintf(ldexpf(a, 10 - e)); /* in [1024, 2048] */
+    if (m == 2048.0f) {
+        m = 1024.0f;
+        e += 1;
+    }
+    return sign | (uint16_t)((e + 15) << 10) | (uint16_t)((int)m - 1024);
+}
+
+/* bfloat16 -> binary32: the top half of the binary32 pattern. */
+float oracle_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float v;
+    memcpy(&v, &u, 4);
+    return v;
+}
+
+/* binary32 -> bfloat16, round to nearest even. */
+uint16_t oracle_f32_to_bf16(float x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    float a = fabsf(x);
+    if (isnan(x))
+        return sign | 0x7fc0;
+    if (isinf(x))
+        return sign | 0x7f80;
+    if (a < ldexpf(1.0f, -126)) {
+        /* subnormal range of bfloat16: spacing 2^-133 */
+        float q = nearbyintf(ldexpf(a, 133));
+        return sign | (uint16_t)q; /* q == 128 encodes 2^-126 */
+    }
+    int E;
+    frexpf(a, &E);
+    int e = E - 1;
+    float m = nearbyintf(ldexpf(a, 7 - e)); /* in [128, 256] */
+    if (m == 256.0f) {
+        m = 128.0f;
+        e += 1;
+    }
+    if (e > 127)
+        return sign | 0x7f80; /* rounded past the largest finite value */
+    return sign | (uint16_t)((e + 127) << 7) | (uint16_t)((int)m - 128);
+}
+
+static float load_as_f32(const void *buf, size_t i, int t)
+{
+    if (t == OR_F32)
+        return ((const float *)buf)[i];
+    if (t == OR_F16)
+        return oracle_f16_to_f32(((const uint16_t *)buf)[i]);
+    return oracle_bf16_to_f32(((const uint16_t *)buf)[i]);
+}
+
+static void store_from_f32(void *buf, size_t i, int t, float v)
+{
+    if (t == OR_F32)
+        ((float *)buf)[i] = v;
+    else if (t == OR_F16)
+        ((uint16_t *)buf)[i] = oracle_f32_to_f16(v);
+    else
+        ((uint16_t *)buf)[i] = oracle_f32_to_bf16(v);
+}
+
+/* ------------------------------------------------------------------ */
+/* block floating point  [P4 §2.1, §3.3]                                */
+/* ------------------------------------------------------------------ */
+
+/* B1: floor(log2 max|x_i|) over the block, -126 for a zero or subnormal max. */
+int oracle_bfp_block_exponent(const float *x, size_t len)
+{
+    float amax = 0.0f;
+    for (size_t i = 0; i < len; i++)
+        if (fabsf(x[i]) > amax)
+            amax = fabsf(x[i]);
+    if (amax < ldexpf(1.0f, -126))
+        return -126;
+    int E;
+    frexpf(amax, &E);
+    return E - 1;
+}
+
+static int bfp_limit(int bits) { return (1 << (bits - 1)) - 1; } /* 127 or 7 */
+
+/* B2: one element's integer code for block exponent e. */
+int oracle_bfp_code(float x, int e, int bits)
+{
+    int q = bits - 2;
+    float scaled = ldexpf(x, q - e); /* exact power-of-two scaling */
+    float r = nearbyintf(scaled);    /* round to nearest even */
+    int M = bfp_limit(bits);
+    if (r > (float)M)
+        r = (float)M;
+    if (r < -(float)M)
+        r = -(float)M;
+    return (int)r;
+}
+
+float oracle_bfp_value(int m, int e, int bits) { return ldexpf((float)m, e - (bits - 2)); }
+
+size_t oracle_bfp_bytes(size_t len, int bits)
+{
+    size_t nb = (len + OR_BFP_BLOCK - 1) / OR_BFP_BLOCK;
+    return nb + (bits == 8 ? len : (len + 1) / 2);
+}
+
+/* B5: planar encode of x[0..n) into exps[ceil(n/128)] and mants. */
+void oracle_bfp_encode(const float *x, size_t n, int bits, int8_t *exps, uint8_t *mants)
+{
+    size_t nb = (n + OR_BFP_BLOCK - 1) / OR_BFP_BLOCK;
+    if (bits == 4)
+        memset(mants, 0, (n + 1) / 2);
+    for (size_t b = 0; b < nb; b++) {
+        size_t lo = b * OR_BFP_BLOCK;
+        size_t len = n - lo < OR_BFP_BLOCK ? n - lo : OR_BFP_BLOCK;
+        int e = oracle_bfp_block_exponent(x + lo, len);
+        exps[b] = (int8_t)e;
+        for (size_t i = lo; i < lo + len; i++) {
+            int m = oracle_bfp_code(x[i], e, bits);
+            if (bits == 8) {
+                mants[i] = (uint8_t)(int8_t)m;
+            } else {
+                uint8_t nib = (uint8_t)(m & 0xf);
+                if (i % 2 == 0)
+                    mants[i / 2] |= nib;
+                else
+                    mants[i / 2] |= (uint8_t)(nib << 4);
+            }
+        }
+    }
+}
+
+static int bfp_code_at(const uint8_t *mants, size_t i, int bits)
+{
+    if (bits == 8)
+        return (int)(int8_t)mants[i];
+    int nib = (i % 2 == 0) ? (mants[i / 2] & 0xf) : (mants[i / 2] >> 4);
+    return nib >= 8 ? nib - 16 : nib; /* two's-complement 4-bit value */
+}
+
+void oracle_bfp_decode(const int8_t *exps, const uint8_t *mants, size_t n, int bits, float *out,
+                       int accumulate)
+{
+    for (size_t i = 0; i < n; i++) {
+        float v = oracle_bfp_value(bfp_code_at(mants, i, bits), exps[i / OR_BFP_BLOCK], bits);
+        out[i] = accumulate ? out[i] + v : v;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* sparse values + indices  [P4 §2.1, §3.3]                             */
+/* ------------------------------------------------------------------ */
+
+/* S1: nonzero means "bit pattern is not +0.0". */
+static int is_nonzero(float v)
+{
+    uint32_t u;
+    memcpy(&u, &v, 4);
+    return u != 0u;
+}
+
+/* S2 */
+int oracle_sparse_is_sparse(size_t nnz, size_t len, double threshold)
+{
+    return (double)nnz < (1.0 - threshold) * (double)len;
+}
+
+/* Standalone encode of x[0..n) (values kept in the input dtype t):
+ * hdr[0] = 1 sparse / 0 dense, hdr[1] = nnz.  Sparse: vals[0..nnz) and
+ * idx[0..nnz) ascending.  Dense: vals[0..n) = x. */
+void oracle_sparse_encode(const void *x, size_t n, int t, double threshold, uint32_t *hdr,
+                          void *vals, int32_t *idx)
+{
+    size_t es = oracle_dtype_size(t);
+    size_t nnz = 0;
+    for (size_t i = 0; i < n; i++)
+        if (is_nonzero(load_as_f32(x, i, t)))
+            nnz++;
+    int sparse = oracle_sparse_is_sparse(nnz, n, threshold);
+    hdr[0] = (uint32_t)sparse;
+    hdr[1] = (uint32_t)nnz;
+    if (!sparse) {
+        memcpy(vals, x, n * es);
+        return;
+    }
+    size_t k = 0;
+    for (size_t i = 0; i < n; i++) {
+        if (is_nonzero(load_as_f32(x, i, t))) {
+            memcpy((char *)vals + k * es, (const char *)x + i * es, es);
+            idx[k] = (int32_t)i;
+            k++;
+        }
+    }
+}
+
+/* Standalone decode into fp32 acc[0..n).  accumulate = 0: acc = restored
+ * message (+0.0 where the sparse message lists nothing).  accumulate = 1:
+ * acc[i] = acc[i] + v at every position the message carries (all positions
+ * for a dense message, the listed ones for a sparse message). */
+void oracle_sparse_decode(const uint32_t *hdr, const void *vals, const int32_t *idx, size_t n,
+                          int t, float *acc, int accumulate)
+{
+    if (hdr[0] == 0) {
+        for (size_t i = 0; i < n; i++) {
+            float v = load_as_f32(vals, i, t);
+            acc[i] = accumulate ? acc[i] + v : v;
+        }
+        return;
+    }
+    if (!accumulate)
+        for (size_t i = 0; i < n; i++)
+            acc[i] = 0.0f;
+    for (size_t k = 0; k < hdr[1]; k++) {
+        float v = load_as_f32(vals, k, t);
+        size_t i = (size_t)idx[k];
+        acc[i] = accumulate ? acc[i] + v : v;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* difference encoding  [P4 §2.1 "current minus previous round"]        */
+/* ------------------------------------------------------------------ */
+
+void oracle_diff_encode(const float *cur, const float *prev, float *diff, size_t n)
+{
+    for (size_t i = 0; i < n; i++)
+        diff[i] = cur[i] - prev[i];
+}
+
+/* ------------------------------------------------------------------ */
+/* ring messages: one chunk's worth of data on one edge of the ring    */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    int kind;         /* codec */
+    int bits;         /* bfp */
+    double threshold; /* sparse */
+    size_t slice;     /* sparse message slice length */
+} codec_t;
+
+typedef struct {
+    size_t len;     /* elements covered */
+    size_t bytes;   /* wire size */
+    float *f;       /* NONE: fp32 values; SPARSE: restored values (+0 if absent) */
+    uint8_t *there; /* SPARSE: 1 where the message carries a value */
+    int8_t *exps;   /* BFP */
+    uint8_t *mants; /* BFP */
+    size_t nexps;   /* BFP: ceil(len/128) */
+    size_t nmants;  /* BFP: len (8-bit) or ceil(len/2) (4-bit) */
+} message;
+
+static void msg_free(message *m)
+{
+    free(m->f);
+    free(m->there);
+    free(m->exps);
+    free(m->mants);
+    memset(m, 0, sizeof *m);
+}
+
+/* Build the message a rank sends for the fp32 data x[0..len). */
+static void msg_encode(message *m, const codec_t *cd, const float *x, size_t len)
+{
+    msg_free(m);
+    m->len = len;
+    if (cd->kind == OR_CODEC_NONE) {
+        m->f = malloc((len ? len : 1) * sizeof(float));
+        memcpy(m->f, x, len * sizeof(float));
+        m->bytes = 4 * len;
+    } else if (cd->kind == OR_CODEC_BFP) {
+        size_t nb = (len + OR_BFP_BLOCK - 1) / OR_BFP_BLOCK;
+        size_t mb = cd->bits == 8 ? len : (len + 1) / 2;
+        m->exps = malloc(nb ? nb : 1);
+        m->mants = malloc(mb ? mb : 1);
+        m->nexps = nb;
+        m->nmants = mb;
+        oracle_bfp_encode(x, len, cd->bits, m->exps, m->mants);
+        m->bytes = nb + mb;
+    } else {
+        /* S3: one message per slice; the receiver restores each slice */
+        m->f = calloc(len ? len : 1, sizeof(float));
+        m->there = calloc(len ? len : 1, 1);
+        m->bytes = 0;
+        for (size_t lo = 0; lo < len; lo += cd->slice) {
+            size_t sl = len - lo < cd->slice ? len - lo : cd->slice;
+            size_t nnz = 0;
+            for (size_t i = lo; i < lo + sl; i++)
+                nnz += is_nonzero(x[i]);
+            if (oracle_sparse_is_sparse(nnz, sl, cd->threshold)) {
+                for (size_t i = lo; i < lo + sl; i++)
+                    if (is_nonzero(x[i])) {
+                        m->f[i] = x[i];
+                        m->there[i] = 1;
+                    }
+                m->bytes += 8 + 8 * nnz;
+            } else {
+                for (size_t i = lo; i < lo + sl; i++) {
+                    m->f[i] = x[i];
+                    m->there[i] = 1;
+                }
+                m->bytes += 8 + 4 * sl;
+            }
+        }
+    }
+}
+
+static void msg_copy(message *dst, const message *src)
+{
+    msg_free(dst);
+    *dst = *src;
+    size_t len = src->len ? src->len : 1;
+    if (src->f) {
+        dst->f = malloc(len * sizeof(float));
+        memcpy(dst->f, src->f, src->len * sizeof(float));
+    }
+    if (src->there) {
+        dst->there = malloc(len);
+        memcpy(dst->there, src->there, src->len);
+    }
+    if (src->exps) {
+        dst->exps = malloc(src->nexps ? src->nexps : 1);
+        memcpy(dst->exps, src->exps, src->nexps);
+    }
+    if (src->mants) {
+        dst->mants = malloc(src->nmants ? src->nmants : 1);
+        memcpy(dst->mants, src->mants, src->nmants);
+    }
+}
+
+/* Decoded value of element i and whether the message carries it. */
+static float msg_value(const message *m, const codec_t *cd, size_t i, int *there)
+{
+    *there = 1;
+    if (cd->kind == OR_CODEC_NONE)
+        return m->f[i];
+    if (cd->kind == OR_CODEC_BFP)
+        return oracle_bfp_value(bfp_code_at(m->mants, i, cd->bits), m->exps[i / OR_BFP_BLOCK],
+                                cd->bits);
+    *there = m->there[i];
+    return m->f[i];
+}
+
+/* ------------------------------------------------------------------ */
+/* chunking  [P2 "两趟实现 ring allreduce"]                              */
+/* ------------------------------------------------------------------ */
+
+static int mod(long a, int n) { return (int)(((a % n) + n) % n); }
+
+static void chunk_range(size_t T, int N, int c, size_t *lo, size_t *len)
+{
+    size_t n = (T + (size_t)N - 1) / (size_t)N; /* R3 */
+    size_t a = (size_t)c * n;
+    size_t b = a + n;
+    if (a > T)
+        a = T;
+    if (b > T)
+        b = T;
+    *lo = a;
+    *len = b - a;
+}
+
+/* ------------------------------------------------------------------ */
+/* the two-pass ring  [P2 "两趟实现 ring allreduce"; P4 §1, §2.2]        */
+/* ------------------------------------------------------------------ */
+
+enum { OR_MODE_ALLREDUCE = 0, OR_MODE_REDUCE_SCATTER = 1 };
+
+/*
+ * Each rank r keeps a local fp32 copy of its whole buffer.  Reduce-scatter,
+ * steps s = 1..N-1: every rank r encodes its local chunk (r-s) mod N into a
+ * message for rank r+1; then every rank r decodes the message it got (chunk
+ * (r-s-1) mod N) and adds it into its local copy of that chunk.  After the
+ * last step rank r holds the full sum of chunk r.
+ * Allgather, steps s = 1..N-1: rank r sends chunk (r-s+1) mod N (for s = 1
+ * its own finished chunk, encoded once; afterwards the message it received
+ * the step before, unchanged) and rank r+1 keeps it and decodes it.
+ * Byte counters: sent[r] and recv[r+1] grow by each message's wire size.
+ *
+ * Returns 0 on success, -1 on a bad argument.
+ */
+int oracle_ring(int mode, int N, size_t T, const void *const *in, int in_t, void *const *out,
+                int out_t, int codec, int bits, double threshold, size_t slice,
+                const float *const *diff_prev, const float *diff_base, int average,
+                uint64_t *sent, uint64_t *recv)
+{
+    if (N < 1 || (codec == OR_CODEC_BFP && bits != 8 && bits != 4) || (diff_prev && in_t != OR_F32))
+        return -1;
+    if (codec == OR_CODEC_SPARSE && slice == 0)
+        return -1;
+    codec_t cd = {codec, bits, threshold, slice};
+    for (int r = 0; r < N; r++)
+        sent[r] = recv[r] = 0;
+
+    /* local working copies (D1: the ring runs on cur - prev when diffing) */
+    float **local = malloc((size_t)N * sizeof(float *));
+    for (int r = 0; r < N; r++) {
+        local[r] = malloc((T ? T : 1) * sizeof(float));
+        for (size_t i = 0; i < T; i++)
+            local[r][i] = diff_prev ? ((const float *)in[r])[i] - diff_prev[r][i]
+                                    : load_as_f32(in[r], i, in_t);
+    }
+    message *outbox = calloc((size_t)N, sizeof(message));
+
+    /* ---- pass 1: reduce-scatter ---- */
+    for (int s = 1; s <= N - 1; s++) {
+        for (int r = 0; r < N; r++) {
+            int c = mod((long)r - s, N);
+            size_t lo, len;
+            chunk_range(T, N, c, &lo, &len);
+            int dst = mod((long)r + 1, N);
+            msg_encode(&outbox[dst], &cd, local[r] + lo, len);
+            sent[r] += outbox[dst].bytes;
+            recv[dst] += outbox[dst].bytes;
+        }
+        for (int r = 0; r < N; r++) {
+            int c = mod((long)r - s - 1, N);
+            size_t lo, len;
+            chunk_range(T, N, c, &lo, &len);
+            for (size_t i = 0; i < len; i++) {
+                int there;
+                float v = msg_value(&outbox[r], &cd, i, &there);
+                if (there) /* S4 */
+                    local[r][lo + i] = local[r][lo + i] + v;
+            }
+        }
+    }
+
+    /* value each rank ends with, per element, before the epilogue */
+    float **res = malloc((size_t)N * sizeof(float *));
+    for (int r = 0; r < N; r++)
+        res[r] = malloc((T ? T : 1) * sizeof(float));
+
+    /* held[r]: the codes of the chunk rank r sends at the next allgather step */
+    message *held = calloc((size_t)N, sizeof(message));
+    int *has = calloc((size_t)N * (size_t)N, sizeof(int));
+
+    for (int r = 0; r < N; r++) {
+        size_t lo, len;
+        chunk_range(T, N, r, &lo, &len);
+        if (mode == OR_MODE_REDUCE_SCATTER || codec == OR_CODEC_NONE) {
+            for (size_t i = 0; i < len; i++)
+                res[r][lo + i] = local[r][lo + i];
+        }
+        if (mode == OR_MODE_ALLREDUCE) {
+            /* B6: the owner encodes its full sum once */
+            msg_encode(&held[r], &cd, local[r] + lo, len);
+            if (codec != OR_CODEC_NONE)
+                for (size_t i = 0; i < len; i++) {
+                    int there;
+                    float v = msg_value(&held[r], &cd, i, &there);
+                    res[r][lo + i] = there ? v : 0.0f;
+                }
+        }
+        has[r * N + r] = 1;
+    }
+
+    /* ---- pass 2: allgather ---- */
+    if (mode == OR_MODE_ALLREDUCE) {
+        for (int s = 1; s <= N - 1; s++) {
+            for (int r = 0; r < N; r++) {
+                int dst = mod((long)r + 1, N);
+                msg_copy(&outbox[dst], &held[r]);
+                sent[r] += outbox[dst].bytes;
+                recv[dst] += outbox[dst].bytes;
+            }
+            for (int r = 0; r < N; r++) {
+                int c = mod((long)r - s, N);
+                size_t lo, len;
+                chunk_range(T, N, c, &lo, &len);
+                for (size_t i = 0; i < len; i++) {
+                    int there;
+                    float v = msg_value(&outbox[r], &cd, i, &there);
+                    res[r][lo + i] = there ? v : 0.0f;
+                }
+                msg_copy(&held[r], &outbox[r]);
+                has[r * N + c] = 1;
+            }
+        }
+    }
+
+    /* ---- epilogue (D2) and output cast ---- */
+    for (int r = 0; r < N; r++) {
+        for (int c = 0; c < N; c++) {
+            if (!has[r * N + c])
+                continue; /* reduce-scatter leaves other chunks untouched */
+            size_t lo, len;
+            chunk_range(T, N, c, &lo, &len);
+            for (size_t i = lo; i < lo + len; i++) {
+                float w = res[r][i];
+                if (average)
+                    w = w / (float)N;
+                if (diff_base)
+                    w = diff_base[i] + w;
+                store_from_f32(out[r], i, out_t, w);
+            }
+        }
+    }
+
+    for (int r = 0; r < N; r++) {
+        msg_free(&outbox[r]);
+        msg_free(&held[r]);
+        free(local[r]);
+        free(res[r]);
+    }
+    free(outbox);
+    free(held);
+    free(has);
+    free(local);
+    free(res);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* allgather as its own op  [P2 table: T(N-1)/N per rank, N-1 steps]    */
+/* ------------------------------------------------------------------ */
+
+/* In place: on entry chunk r of buf[r] is rank r's contribution; on exit
+ * every buffer holds every chunk.  Element bytes are copied exactly. */
+int oracle_allgather(int N, size_t T, void *const *buf, int t, uint64_t *sent, uint64_t *recv)
+{
+    if (N < 1)
+        return -1;
+    size_t es = oracle_dtype_size(t);
+    for (int r = 0; r < N; r++)
+        sent[r] = recv[r] = 0;
+    for (int s = 1; s <= N - 1; s++) {
+        /* every rank sends first, then every rank stores what it got */
+        size_t n = (T + (size_t)N - 1) / (size_t)N;
+        char **msg = malloc((size_t)N * sizeof(char *));
+        for (int r = 0; r < N; r++) {
+            int c = mod((long)r - s + 1, N);
+            size_t lo, len;
+            chunk_range(T, N, c, &lo, &len);
+            int dst = mod((long)r + 1, N);
+            msg[dst] = malloc(n * es + 1);
+            memcpy(msg[dst], (char *)buf[r] + lo * es, len * es);
+            sent[r] += len * es;
+            recv[dst] += len * es;
+        }
+        for (int r = 0; r < N; r++) {
+            int c = mod((long)r - s, N);
+            size_t lo, len;
+            chunk_range(T, N, c, &lo, &len);
+            memcpy((char *)buf[r] + lo * es, msg[r], len * es);
+        }
+        for (int r = 0; r < N; r++)
+            free(msg[r]);
+        free(msg);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* broadcast and tree allreduce  [P2 table: broadcast T over a log2(N)  */
+/* tree; tree allreduce T log2 N, 2 log2 N steps; "练习" tree variant]  */
+/* ------------------------------------------------------------------ */
+
+static int ceil_log2(int N)
+{
+    int L = 0;
+    while ((1 << L) < N)
+        L++;
+    return L;
+}
+
+/* Binomial broadcast from root: at level k = 0..ceil(log2 N)-1 every
+ * relative rank q < 2^k with q + 2^k < N sends the whole buffer to q + 2^k
+ * (relative rank q is absolute rank (q + root) mod N). */
+int oracle_broadcast(int N, size_t T, void *const *buf, int t, int root, uint64_t *sent,
+                     uint64_t *recv)
+{
+    if (N < 1 || root < 0 || root >= N)
+        return -1;
+    size_t es = oracle_dtype_size(t);
+    for (int r = 0; r < N; r++)
+        sent[r] = recv[r] = 0;
+    int L = ceil_log2(N);
+    for (int k = 0; k < L; k++) {
+        for (int q = 0; q < (1 << k); q++) {
+            int qd = q + (1 << k);
+            if (qd >= N)
+                continue;
+            int src = (q + root) % N, dst = (qd + root) % N;
+            memcpy(buf[dst], buf[src], T * es);
+            sent[src] += T * es;
+            recv[dst] += T * es;
+        }
+    }
+    return 0;
+}
+
+/* Binomial reduce to rank 0: at level k every rank r with r mod 2^(k+1) = 0
+ * and r + 2^k < N adds rank r+2^k's partial into its own (fp32); then the
+ * binomial broadcast above from root 0.  In place, fp32 only. */
+int oracle_tree_allreduce(int N, size_t T, float *const *buf, uint64_t *sent, uint64_t *recv)
+{
+    if (N < 1)
+        return -1;
+    for (int r = 0; r < N; r++)
+        sent[r] = recv[r] = 0;
+    int L = ceil_log2(N);
+    for (int k = 0; k < L; k++) {
+        int step = 1 << k;
+        for (int r = 0; r < N; r += 2 * step) {
+            int src = r + step;
+            if (src >= N)
+                continue;
+            for (size_t i = 0; i < T; i++)
+                buf[r][i] = buf[r][i] + buf[src][i];
+            sent[src] += 4 * T;
+            recv[r] += 4 * T;
+        }
+    }
+    uint64_t *s2 = calloc((size_t)N, sizeof(uint64_t));
+    uint64_t *r2 = calloc((size_t)N, sizeof(uint64_t));
+    oracle_broadcast(N, T, (void *const *)buf, OR_F32, 0, s2, r2);
+    for (int r = 0; r < N; r++) {
+        sent[r] += s2[r];
+        recv[r] += r2[r];
+    }
+    free(s2);
+    free(r2);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* per-element dtype helpers for the Python side                       */
+/* ------------------------------------------------------------------ */
+
+void oracle_cast_to_f32(const void *x, size_t n, int t, float *out)
+{
+    for (size_t i = 0; i < n; i++)
+        out[i] = load_as_f32(x, i, t);
+}
+
+void oracle_cast_from_f32(const float *x, size_t n, int t, void *out)
+{
+    for (size_t i = 0; i < n; i++)
+        store_from_f32(out, i, t, x[i]);
+}

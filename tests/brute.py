@@ -1,0 +1,209 @@
+"""Pure-Python brute force of the ring collectives and codecs, for tiny inputs.
+
+An independent second implementation used only to pin the C oracle (N <= 4,
+T <= 64): plain Python loops, one numpy float32 scalar operation per IEEE
+binary32 add, ``math.frexp``/``math.ldexp`` for exponents and exact
+power-of-two scaling (in double, where every scaled value here is exact) and
+Python's ``round`` (round half to even) for the integer codes.  It shares no
+code with the C oracle or with the GPU library.
+
+Schedules (collective ops from scratch lesson, "two-pass ring allreduce"):
+reduce-scatter step s = 1..N-1, rank r sends chunk (r-s) mod N to r+1;
+allgather step s = 1..N-1, rank r sends chunk (r-s+1) mod N.
+"""
+from __future__ import annotations
+
+import math
+import struct
+
+import numpy as np
+
+F = np.float32
+
+
+def chunks(T, N):
+    n = -(-T // N)
+    return [(min(c * n, T), min((c + 1) * n, T)) for c in range(N)]
+
+
+def nonzero(v) -> bool:
+    return struct.pack("<f", float(v)) != b"\x00\x00\x00\x00"
+
+
+# ---------------------------------------------------------------- codecs
+
+def bfp_exponent(vals) -> int:
+    amax = max((abs(float(v)) for v in vals), default=0.0)
+    if amax < 2.0 ** -126:
+        return -126
+    _, E = math.frexp(amax)  # amax = f * 2^E, 0.5 <= f < 1
+    return E - 1
+
+
+def bfp_code(v, e, bits) -> int:
+    q, M = bits - 2, 2 ** (bits - 1) - 1
+    r = round(math.ldexp(float(v), q - e))  # half to even
+    return max(-M, min(M, r))
+
+
+def bfp_value(m, e, bits):
+    return F(math.ldexp(m, e - (bits - 2)))
+
+
+def bfp_roundtrip(vals, bits):
+    """Encode and decode a list of float32 values block by block."""
+    out, nbytes = [], 0
+    for lo in range(0, len(vals), 128):
+        blk = vals[lo:lo + 128]
+        e = bfp_exponent(blk)
+        out += [bfp_value(bfp_code(v, e, bits), e, bits) for v in blk]
+        nbytes += 1
+    nbytes += len(vals) if bits == 8 else (len(vals) + 1) // 2
+    return out, nbytes
+
+
+def sparse_roundtrip(vals, threshold, slice_len):
+    """Returns (restored values, carried flags, wire bytes) for one message."""
+    out, there, nbytes = [], [], 0
+    for lo in range(0, len(vals), slice_len):
+        sl = vals[lo:lo + slice_len]
+        nnz = sum(1 for v in sl if nonzero(v))
+        if nnz < (1.0 - threshold) * len(sl):
+            out += [v if nonzero(v) else F(0.0) for v in sl]
+            there += [nonzero(v) for v in sl]
+            nbytes += 8 + 8 * nnz
+        else:
+            out += list(sl)
+            there += [True] * len(sl)
+            nbytes += 8 + 4 * len(sl)
+    return out, there, nbytes
+
+
+# ---------------------------------------------------------------- ring
+
+def ring(xs, codec="none", bits=8, threshold=0.5, slice_len=256, mode="allreduce",
+         diff_prev=None, diff_base=None, average=False):
+    """xs: list of N lists of float32 scalars.  Returns (results, sent, recv)
+    where results[r] is a list with None at chunks rank r does not produce."""
+    N, T = len(xs), len(xs[0])
+    ch = chunks(T, N)
+    if diff_prev is not None:
+        local = [[F(xs[r][i] - diff_prev[r][i]) for i in range(T)] for r in range(N)]
+    else:
+        local = [[F(v) for v in x] for x in xs]
+    sent, recv = [0] * N, [0] * N
+
+    def encode(vals):
+        if codec == "none":
+            return list(vals), [True] * len(vals), 4 * len(vals)
+        if codec == "bfp":
+            out, nb = bfp_roundtrip(vals, bits)
+            return out, [True] * len(vals), nb
+        return sparse_roundtrip(vals, threshold, slice_len)
+
+    for s in range(1, N):
+        inbox = [None] * N
+        for r in range(N):
+            lo, hi = ch[(r - s) % N]
+            inbox[(r + 1) % N] = encode(local[r][lo:hi])
+            sent[r] += inbox[(r + 1) % N][2]
+            recv[(r + 1) % N] += inbox[(r + 1) % N][2]
+        for r in range(N):
+            lo, hi = ch[(r - s - 1) % N]
+            vals, there, _ = inbox[r]
+            for i in range(lo, hi):
+                if there[i - lo]:
+                    local[r][i] = F(local[r][i] + vals[i - lo])
+
+    res = [[None] * T for _ in range(N)]
+    held = [None] * N
+    for r in range(N):
+        lo, hi = ch[r]
+        if mode == "reduce_scatter" or codec == "none":
+            for i in range(lo, hi):
+                res[r][i] = local[r][i]
+        if mode == "allreduce":
+            held[r] = encode(local[r][lo:hi])
+            if codec != "none":
+                for i in range(lo, hi):
+                    res[r][i] = held[r][0][i - lo] if held[r][1][i - lo] else F(0.0)
+    if mode == "allreduce":
+        for s in range(1, N):
+            inbox = [None] * N
+            for r in range(N):
+                inbox[(r + 1) % N] = held[r]
+                sent[r] += held[r][2]
+                recv[(r + 1) % N] += held[r][2]
+            for r in range(N):
+                lo, hi = ch[(r - s) % N]
+                vals, there, _ = inbox[r]
+                for i in range(lo, hi):
+                    res[r][i] = vals[i - lo] if there[i - lo] else F(0.0)
+                held[r] = inbox[r]
+    for r in range(N):
+        for i in range(T):
+            if res[r][i] is None:
+                continue
+            w = res[r][i]
+            if average:
+                w = F(w / F(N))
+            if diff_base is not None:
+                w = F(diff_base[i] + w)
+            res[r][i] = w
+    return res, sent, recv
+
+
+# ---------------------------------------------------------------- tree / bcast / allgather
+
+def ceil_log2(N):
+    L = 0
+    while (1 << L) < N:
+        L += 1
+    return L
+
+
+def broadcast(bufs, root, elem_bytes):
+    N, T = len(bufs), len(bufs[0])
+    bufs = [list(b) for b in bufs]
+    sent, recv = [0] * N, [0] * N
+    for k in range(ceil_log2(N)):
+        for q in range(1 << k):
+            if q + (1 << k) < N:
+                src, dst = (q + root) % N, (q + (1 << k) + root) % N
+                bufs[dst] = list(bufs[src])
+                sent[src] += T * elem_bytes
+                recv[dst] += T * elem_bytes
+    return bufs, sent, recv
+
+
+def tree_allreduce(bufs):
+    N, T = len(bufs), len(bufs[0])
+    acc = [[F(v) for v in b] for b in bufs]
+    sent, recv = [0] * N, [0] * N
+    for k in range(ceil_log2(N)):
+        st = 1 << k
+        for r in range(0, N, 2 * st):
+            if r + st < N:
+                acc[r] = [F(a + b) for a, b in zip(acc[r], acc[r + st])]
+                sent[r + st] += 4 * T
+                recv[r] += 4 * T
+    out, s2, r2 = broadcast(acc, 0, 4)
+    return out, [a + b for a, b in zip(sent, s2)], [a + b for a, b in zip(recv, r2)]
+
+
+def allgather(bufs, elem_bytes):
+    N, T = len(bufs), len(bufs[0])
+    ch = chunks(T, N)
+    bufs = [list(b) for b in bufs]
+    sent, recv = [0] * N, [0] * N
+    for s in range(1, N):
+        msgs = [None] * N
+        for r in range(N):
+            lo, hi = ch[(r - s + 1) % N]
+            msgs[(r + 1) % N] = bufs[r][lo:hi]
+            sent[r] += (hi - lo) * elem_bytes
+            recv[(r + 1) % N] += (hi - lo) * elem_bytes
+        for r in range(N):
+            lo, hi = ch[(r - s) % N]
+            bufs[r][lo:hi] = msgs[r]
+    return bufs, sent, recv

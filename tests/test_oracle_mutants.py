@@ -1,0 +1,57 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch every one.  Each mutant is a one-line edit of oracle.c (wrong step
+index, wrong mantissa scale, ties away from zero, off-by-one exponent, wrong
+clamp, wrong threshold tie, wrong header size, reversed tree levels, swapped
+difference, wrong subnormal scaling in the fp16 conversion); the mutated copy
+is compiled into a temporary directory and the pin suite is run against it in
+a child process.  The real oracle is never modified."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+MUTANTS = {
+    "rs_send_index": ("int c = mod((long)r - s, N);", "int c = mod((long)r - s + 1, N);", 1),
+    "ag_recv_index": ("int c = mod((long)r - s, N);", "int c = mod((long)r - s + 1, N);", 2),
+    "mantissa_scale": ("int q = bits - 2;", "int q = bits - 1;", 1),
+    "ties_away": ("float r = nearbyintf(scaled);", "float r = roundf(scaled);", 1),
+    "exponent_off_by_one": ("    frexpf(amax, &E);\n    return E - 1;", "    frexpf(amax, &E);\n    return E;", 1),
+    "subnormal_exponent": ("        return -126;\n    int E;", "        return -127;\n    int E;", 1),
+    "clamp_limit": ("return (1 << (bits - 1)) - 1;", "return (1 << (bits - 1));", 1),
+    "threshold_tie": ("return (double)nnz < (1.0 - threshold)", "return (double)nnz <= (1.0 - threshold)", 1),
+    "sparse_header_bytes": ("m->bytes += 8 + 8 * nnz;", "m->bytes += 4 + 8 * nnz;", 1),
+    "tree_level_order": ("    for (int k = 0; k < L; k++) {\n        int step = 1 << k;",
+                         "    for (int k = L - 1; k >= 0; k--) {\n        int step = 1 << k;", 1),
+    "diff_sign": ("((const float *)in[r])[i] - diff_prev[r][i]", "diff_prev[r][i] - ((const float *)in[r])[i]", 1),
+    "average_by_reciprocal": ("w = w / (float)N;", "w = w * (1.0f / (float)N);", 1),
+    "f16_subnormal_scale": ("float q = nearbyintf(ldexpf(a, 24));", "float q = nearbyintf(ldexpf(a, 23));", 1),
+}
+
+
+def _mutate(src, old, new, occurrence):
+    pos = -1
+    for _ in range(occurrence):
+        pos = src.index(old, pos + 1)
+    return src[:pos] + new + src[pos + len(old):]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new, occ = MUTANTS[name]
+    src = open(SRC).read()
+    mutated = _mutate(src, old, new, occ)
+    assert mutated != src
+    c = tmp_path / "oracle_mutant.c"
+    c.write_text(mutated)
+    so = tmp_path / "liboracle_mutant.so"
+    subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                    "-shared", "-o", str(so), str(c), "-lm"], check=True)
+    env = dict(os.environ, RRA_ORACLE_LIB=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
