@@ -1,0 +1,493 @@
+#!/usr/bin/env python
+"""Benchmark of the compressed ring allreduce on one GB300 (N simulated ranks).
+
+Default workload (the one the metric is quoted on): block-FP8 compressed ring
+allreduce of one 25 MiB DDP-style fp16 gradient bucket, N = 8 simulated ranks,
+T = 13,107,200 fp16 elements per rank drawn N(0, 1e-3^2) from seed 1, fp32
+accumulation, fp16 output.  One step = one rra_ring_allreduce call (the whole
+hot path: chunking, reduce-scatter hops with fused decode + fp32 add + encode,
+owner finalise, allgather hops with decode + output cast, byte counters).
+
+Metric: algbw = T * sizeof(input element) / step time (per-rank logical
+payload, as nccl-tests count it), reported whole-job (replicas x payload /
+max-over-ranks time), plus the dominant kernel's roofline fraction against
+the measured HBM copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                  [--impl rra|reference]
+
+--impl reference times the CPU oracle on the machine's host cores instead (a
+bounded sample of the same workload per step).  With torchrun (N > 1) every
+rank runs an independent replica on its own GPU ("replicas only": the method
+simulates all ranks inside one GPU, so nothing is sharded across GPUs).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "compressed ring-allreduce algbw GB/s on 1 GB300 (N sim ranks), % of HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+CONFIG_NAMES = ("bfp8_bucket", "lossless_n4", "sparse_n16", "diloco_n8")
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of this process's GPU during the timed region."""
+
+    def __init__(self, device_index: int, period_ms: int = 50):
+        self.path = tempfile.mktemp(prefix="rra_clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(device_index), "-lms", str(period_ms)],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                    power.append(float(p[3]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- peaks / profiles
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: STREAM-style copy)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, an earlier GB300 copy measurement)"
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ring_allreduce_compressed_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(config: str):
+    """DRAM bytes per launch of the ring kernel from the committed ncu summary
+    for this workload, or None when no summary exists or the kernel sources
+    changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"ring_kernel_{config}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None, "no ncu summary"
+    m_sha = re.search(r"kernel_sources_sha:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_sha or not m_tr:
+        return None, "summary incomplete"
+    if m_sha.group(1) != kernel_sources_sha():
+        return None, "kernel changed since the ncu capture"
+    return int(m_tr.group(1)), path
+
+
+# ---------------------------------------------------------------- workloads
+
+class Workload:
+    def __init__(self, name: str, device="cuda"):
+        import ring_allreduce_compressed_gb300 as rra
+        self.rra = rra
+        self.name = name
+        self.base = None
+        if name == "bfp8_bucket":
+            c = W.CONFIGS[name]
+            self.N, self.T = c["N"], c["T"]
+            self.inputs = W.bfp_bucket(self.N, self.T, seed=c["seed"], device=device)
+            self.out_dtype = torch.float16
+            self.codec = rra.Codec("bfp", bits=8)
+            self.codec_name = "bfp8"
+            self.desc = ("block-FP8 compressed ring allreduce of one 25 MiB fp16 DDP bucket: "
+                         "N=8 simulated ranks x 13,107,200 fp16, N(0,1e-3^2) seed 1, "
+                         "128-element blocks, fp32 accumulation, fp16 output")
+        elif name == "lossless_n4":
+            c = W.CONFIGS[name]
+            self.N, self.T = c["N"], c["T"]
+            self.inputs = W.lossless(self.N, self.T, seed=c["seed"], device=device)
+            self.out_dtype = torch.float32
+            self.codec = None
+            self.codec_name = "none"
+            self.desc = "lossless fp32 ring allreduce, N=4 x 4096 fp32, N(0,1) seed 0"
+        elif name == "sparse_n16":
+            c = W.CONFIGS[name]
+            self.N, self.T = c["N"], c["T"]
+            self.inputs = W.sparse(self.N, self.T, seed=c["seed"], device=device)
+            self.out_dtype = torch.float32
+            self.codec = rra.Codec("sparse", sparsity_threshold=0.5)
+            self.codec_name = "sparse"
+            self.desc = ("sparse-format ring allreduce: N=16 x 64 Mi bf16, zero w.p. 0.6 else "
+                         "N(0,0.02^2), seed 2, threshold 0.5 per 256-element slice, fp32 out")
+        elif name == "diloco_n8":
+            c = W.CONFIGS[name]
+            self.N, self.T = c["N"], c["T"]
+            cur, prev = W.diloco(self.N, self.T, seed=c["seed"], device=device)
+            self.inputs = cur
+            # previous round's result: lossless mean of prev (setup, untimed)
+            self.base = torch.empty(self.T, dtype=torch.float32, device=device)
+            comm = rra.Comm(self.N, self.T)
+            outs = [self.base] + [torch.empty(0, device=device)] * 0
+            tmp = [torch.empty(self.T, device=device) for _ in range(self.N - 1)]
+            comm.ring_allreduce(prev, [self.base] + tmp, rra.Codec("none", average=True))
+            torch.cuda.synchronize()
+            del tmp, outs
+            comm.close()
+            self.out_dtype = torch.float32
+            self.codec = rra.Codec("bfp", bits=4, diff_prev=prev, diff_base=self.base,
+                                   average=True)
+            self.prev = prev
+            self.codec_name = "diff+bfp4"
+            self.desc = ("DiLoCo outer-step pseudo-gradient: N=8 x 10^9 fp32 deltas, "
+                         "difference against the previous round, block-FP4, averaged by 1/N, "
+                         "previous result added back; seed 3")
+        else:
+            raise ValueError(name)
+        self.in_dtype = self.inputs[0].dtype
+        self.outputs = [torch.empty(self.T, dtype=self.out_dtype, device=device)
+                        for _ in range(self.N)]
+        self.comm = rra.Comm(self.N, self.T, self.in_dtype)
+        ies = self.inputs[0].element_size()
+        oes = self.outputs[0].element_size()
+        self.payload = self.T * ies  # per-rank logical payload (algbw numerator)
+        extra_in = self.T * 4 * self.N if self.base is not None else 0  # prev streams
+        base = self.T * 4 if self.base is not None else 0
+        self.compulsory = self.N * self.T * (ies + oes) + extra_in + base
+
+    def step(self, stream=None):
+        self.comm.ring_allreduce(self.inputs, self.outputs, self.codec, stream=stream)
+
+    def l2_note(self):
+        mb = self.compulsory / 1e6
+        return (f"inputs+outputs {mb:.0f} MB per step > 129 MB L2: no flush between steps"
+                if mb > 129 else f"working set {mb:.2f} MB fits in L2 (latency-bound case)")
+
+
+# ---------------------------------------------------------------- CPU baseline (oracle)
+
+def oracle_sample_ring(wl_host, N, T, codec_name, slices_per_chunk, in_dt, out_dt, extra):
+    """Run the oracle on the first `slices_per_chunk` 256-element slices of
+    every chunk (an exact sub-problem: slices are independent).  Returns
+    (seconds, payload bytes per rank of the sample)."""
+    import oracle as O
+    n = T // N
+    m = min(n, slices_per_chunk * 256)
+    idx = np.concatenate([np.arange(c * n, c * n + m) for c in range(N)])
+    xs = [np.ascontiguousarray(x[idx]) for x in wl_host]
+    kw = {}
+    if codec_name == "bfp8":
+        kw = dict(codec="bfp", bits=8)
+    elif codec_name == "sparse":
+        kw = dict(codec="sparse", threshold=0.5)
+    elif codec_name == "diff+bfp4":
+        kw = dict(codec="bfp", bits=4, diff_prev=[np.ascontiguousarray(p[idx]) for p in extra[0]],
+                  diff_base=np.ascontiguousarray(extra[1][idx]), average=True)
+    t0 = time.perf_counter()
+    O.ring(xs, in_dt, out_dt, **kw)
+    dt = time.perf_counter() - t0
+    return dt, N * m * xs[0].itemsize
+
+
+def host_copy(t):
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+DT_NAME = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+
+
+def cpu_baseline(wl: Workload, budget_s: float = 20.0):
+    """The oracle, as it stands, single-threaded on a host core, on a bounded
+    sample of the workload sized to about `budget_s` seconds."""
+    n = wl.T // wl.N
+    hosts = [host_copy(x) for x in wl.inputs]
+    extra = None
+    if wl.base is not None:
+        extra = ([host_copy(p) for p in wl.prev], host_copy(wl.base))
+    # calibrate on a small sample, then size the measured one
+    s0 = max(1, min(n // 256, 16))
+    dt0, _ = oracle_sample_ring(hosts, wl.N, wl.T, wl.codec_name, s0, DT_NAME[wl.in_dtype],
+                                DT_NAME[wl.out_dtype], extra)
+    slices = max(1, min(-(-n // 256), int(s0 * budget_s / max(dt0, 1e-6))))
+    dt, payload = oracle_sample_ring(hosts, wl.N, wl.T, wl.codec_name, slices,
+                                     DT_NAME[wl.in_dtype], DT_NAME[wl.out_dtype], extra)
+    full = slices * 256 >= n
+    return {"value": payload / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": dt,
+            "sample": ("the full workload" if full else
+                       f"first {slices} of {-(-n // 256)} 256-element slices of every chunk "
+                       f"({slices * 256 * wl.N} of {wl.T} elements per rank; slices are "
+                       "independent, so the sample is an exact sub-problem)")}
+
+
+# ---------------------------------------------------------------- arms
+
+def run_rra(args, world, rank, local):
+    import ring_allreduce_compressed_gb300 as rra
+    rra.build()
+    wl = Workload(args.config)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    sent, recv = wl.comm.get_bytes()
+    assert wl.comm.status() == rra.RRA_OK
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    time.sleep(0.15)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        wl.step()
+        ev[k][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    status = wl.comm.status()
+    total_ms = t_start.elapsed_time(t_end)
+    kern_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    ms_step = max_over_ranks(world, total_ms / K)
+    kern_ms = max_over_ranks(world, kern_ms)
+
+    value = world * wl.payload / (ms_step * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+    achieved = wl.compulsory / (kern_ms * 1e-3) / 1e9
+    traffic, traffic_src = traffic_from_profile(args.config)
+
+    # end to end: pinned host inputs in, results out, through the public API
+    e2e = None
+    if args.config in ("bfp8_bucket", "lossless_n4") and args.e2e_steps > 0:
+        h_in = [torch.empty(wl.T, dtype=wl.in_dtype, pin_memory=True) for _ in range(wl.N)]
+        for h, d in zip(h_in, wl.inputs):
+            h.copy_(d)
+        h_out = [torch.empty(wl.T, dtype=wl.out_dtype, pin_memory=True) for _ in range(wl.N)]
+        d_in = [torch.empty_like(x) for x in wl.inputs]
+        d_out = [torch.empty_like(x) for x in wl.outputs]
+
+        def e2e_step():
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            wl.comm.ring_allreduce(d_in, d_out, wl.codec)
+            for h, d in zip(h_out, d_out):
+                h.copy_(d, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(world, a.elapsed_time(b) / args.e2e_steps)
+        ok = all(torch.equal(h_out[r].view(torch.int16 if wl.out_dtype != torch.float32 else torch.int32),
+                             wl.outputs[r].cpu().view(torch.int16 if wl.out_dtype != torch.float32 else torch.int32))
+                 for r in range(wl.N))
+        e2e = {"value": world * wl.payload / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": e2e_ms, "steps": args.e2e_steps,
+               "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in h_in),
+               "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in h_out),
+               "result_matches_device_run": ok}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, budget_s=args.cpu_budget)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{args.config}: {wl.desc}", "N": wl.N, "T": wl.T,
+                   "in_dtype": DT_NAME[wl.in_dtype], "out_dtype": DT_NAME[wl.out_dtype],
+                   "codec": wl.codec_name, "parallelism": f"replicas x{world}",
+                   "l2": wl.l2_note()},
+        "hbm_pct": 100.0 * achieved / peak,
+        "busbw": value * 2 * (wl.N - 1) / wl.N,
+        "bytes_sent_per_rank": sent[0],
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "ring_kernel", "kernel_ms": kern_ms,
+                     "bytes_per_launch": wl.compulsory,
+                     "bytes_model": "compulsory: N*T*(in+out) (+ diff prev and base)",
+                     "peak_source": peak_src, "traffic_source": traffic_src},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K,
+        "clocks": clk,
+        "status": rra.status_string(status),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+        if args.jsonl:
+            with open(args.jsonl, "a") as f:
+                f.write(json.dumps(line) + "\n")
+
+
+def run_reference(args, world, rank):
+    """The oracle timed on the host cores, one bounded sample per step."""
+    if rank != 0:
+        return
+    wl = Workload(args.config)
+    n = wl.T // wl.N
+    hosts = [host_copy(x) for x in wl.inputs]
+    extra = None
+    if wl.base is not None:
+        extra = ([host_copy(p) for p in wl.prev], host_copy(wl.base))
+    s0 = max(1, min(n // 256, 4))
+    dt0, _ = oracle_sample_ring(hosts, wl.N, wl.T, wl.codec_name, s0, DT_NAME[wl.in_dtype],
+                                DT_NAME[wl.out_dtype], extra)
+    per_step = args.ref_budget / max(1, args.steps + args.warmup)
+    slices = max(1, min(-(-n // 256), int(s0 * per_step / max(dt0, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_sample_ring(hosts, wl.N, wl.T, wl.codec_name, slices, DT_NAME[wl.in_dtype],
+                           DT_NAME[wl.out_dtype], extra)
+    tot, pay = 0.0, 0
+    for _ in range(args.steps):
+        dt, p = oracle_sample_ring(hosts, wl.N, wl.T, wl.codec_name, slices, DT_NAME[wl.in_dtype],
+                                   DT_NAME[wl.out_dtype], extra)
+        tot += dt
+        pay += p
+    value = pay / tot / 1e9
+    sample = (f"first {slices} of {-(-n // 256)} 256-element slices of every chunk per step "
+              f"({slices * 256 * wl.N} of {wl.T} elements per rank)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{args.config}: {wl.desc}", "N": wl.N, "T": wl.T,
+                       "in_dtype": DT_NAME[wl.in_dtype], "out_dtype": DT_NAME[wl.out_dtype],
+                       "codec": wl.codec_name, "parallelism": f"replicas x{world}"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["rra", "reference"], default="rra")
+    ap.add_argument("--config", choices=CONFIG_NAMES, default="bfp8_bucket")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=60.0)
+    ap.add_argument("--jsonl", default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_rra(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

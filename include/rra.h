@@ -1,0 +1,304 @@
+/*
+ * rra.h -- C ABI of a GB300 (sm_103a) library for the chunked ring
+ * allreduce coupled with gradient-compression codecs.
+ *
+ * N ranks are simulated as N buffers in the memory of ONE GPU.  A "send" is a
+ * device-side write of the (encoded) message into the receiving rank's
+ * receive slot; the receiving rank decodes it from there and accumulates in
+ * fp32.  All functions take plain pointers and sizes; the caller keeps
+ * ownership of every buffer it passes.
+ *
+ * Sources (cited by page title and section):
+ *  [ring]  "从零实现集合通信" (collective ops from scratch), section
+ *          "两趟实现 ring allreduce": tensor cut into N equal chunks, rank r
+ *          owns chunk r; reduce-scatter pass of N-1 steps (at step s rank r
+ *          sends chunk (r-s) mod N to rank r+1 and accumulates the chunk it
+ *          receives), then an allgather pass of N-1 steps; the per-rank byte
+ *          and step table (ring 2T(N-1)/N, tree T log2 N, broadcast T over a
+ *          log2(N) tree, allgather and reduce_scatter T(N-1)/N each);
+ *          section "练习" (tree variant chosen by message size, byte counter,
+ *          receive timeout instead of hanging).
+ *  [cccl]  "CCCL通信压缩库：突破LLM训练通信墙的工程实践": §2.1 sparse
+ *          values+indices when sparsity exceeds a threshold (e.g. 50%),
+ *          block floating point (one shared exponent per block of e.g. 128
+ *          elements, 8- or 4-bit mantissas), difference against the previous
+ *          round; §2.2 chunked compress -> send -> decompress -> reduce
+ *          pipeline; §3.3 compression types and sparsity_threshold 0.5.
+ *
+ * Conventions shared by every entry point:
+ *  - Device pointers are plain CUDA device addresses of the device that was
+ *    current when the communicator was created (or, for the codec
+ *    functions, the current device).  Arrays of N pointers ("in", "out",
+ *    "buf", "diff_prev") are HOST arrays; they are read during the call and
+ *    may be reused or freed as soon as it returns.
+ *  - Elements are counted, not bytes.  "count" (T) is the number of
+ *    elements of every rank's buffer.
+ *  - Chunking: n = ceil(T/N); chunk c covers elements
+ *    [c*n, min(T, (c+1)*n)); trailing chunks may be short or empty.
+ *  - All work is enqueued asynchronously on "stream" (a cudaStream_t; NULL
+ *    is the legacy default stream).  Argument errors are detected on the host
+ *    before anything is enqueued and returned as RRA_ERR_INVALID /
+ *    RRA_ERR_UNSUPPORTED; a failed launch returns RRA_ERR_CUDA.  Errors the
+ *    device detects while running (a wait that ran out of time) are latched
+ *    in the communicator and reported by rra_comm_status().
+ *  - Inputs must be finite: NaN or infinity in an input is outside the
+ *    contract (results unspecified, no fault).
+ *  - Nothing on these paths allocates memory except rra_comm_create and the
+ *    first call of rra_sparse_encode on a device (see there).
+ */
+#ifndef RRA_H
+#define RRA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Largest number of simulated ranks one communicator supports. */
+#define RRA_MAX_RANKS 64
+/* Elements per block-floating-point block ([cccl] §2.1: "e.g. 128"). */
+#define RRA_BFP_BLOCK 128
+/* Elements per ring message slice: the ring streams each chunk through the
+ * receive slots in slices of this many elements; for the sparse codec every
+ * slice is one message with its own header and its own sparse/dense choice
+ * ([cccl] §2.2: the tensor is cut into small chunks that are compressed and
+ * sent one after the other). */
+#define RRA_RING_SLICE 256
+
+typedef enum {
+    RRA_OK = 0,
+    RRA_ERR_INVALID = 1,     /* a NULL pointer, a size out of range, a bad enum */
+    RRA_ERR_UNSUPPORTED = 2, /* valid arguments, combination not provided   */
+    RRA_ERR_CUDA = 3,        /* a CUDA call or launch failed                */
+    RRA_ERR_TIMEOUT = 4,     /* a device-side wait ran past its time limit   */
+    RRA_ERR_NOMEM = 5        /* device memory allocation failed              */
+} rra_status;
+
+typedef enum { RRA_F32 = 0, RRA_F16 = 1, RRA_BF16 = 2 } rra_dtype;
+
+typedef enum {
+    RRA_CODEC_NONE = 0,   /* lossless: fp32 on the wire                      */
+    RRA_CODEC_BFP = 1,    /* block floating point, 8- or 4-bit mantissas     */
+    RRA_CODEC_SPARSE = 2  /* values + int32 indices, or dense fallback       */
+} rra_codec_kind;
+
+/*
+ * Codec of one reducing call ([cccl] §3.2/§3.3 configuration fields).
+ *  kind                what goes on the wire (above).
+ *  bits                8 or 4 (RRA_CODEC_BFP only).
+ *  sparsity_threshold  RRA_CODEC_SPARSE: a slice is sent sparse iff its
+ *                      sparsity (zeros / length) is strictly greater, i.e.
+ *                      nnz < (1 - threshold) * length; must lie in [0, 1).
+ *  diff_prev           NULL, or a host array of N device pointers to fp32
+ *                      buffers of T elements: the previous round's values.
+ *                      The ring then runs on cur - prev ([cccl] §2.1
+ *                      difference encoding); requires in_t == RRA_F32.
+ *  diff_base           NULL, or a device pointer to T fp32 values (the
+ *                      previous round's result R_prev, shared by all ranks)
+ *                      added back in the output epilogue.
+ *  average             nonzero: the reduced value is divided by N (IEEE
+ *                      division, round to nearest even) before diff_base is
+ *                      added: out = diff_base + v / N.
+ * A NULL rra_codec* means {RRA_CODEC_NONE, 0, 0, NULL, NULL, 0}.
+ */
+typedef struct {
+    rra_codec_kind kind;
+    int bits;
+    float sparsity_threshold;
+    const float *const *diff_prev;
+    const float *diff_base;
+    int average;
+} rra_codec;
+
+/* Opaque communicator: owns the device-side byte counters, the status word
+ * and the launch configuration of the N simulated ranks. */
+typedef struct rra_comm rra_comm;
+
+/*
+ * Create a communicator for nranks simulated ranks on the current device.
+ *  nranks     1..RRA_MAX_RANKS.
+ *  max_count  largest "count" any later call may pass (>= 1).
+ *  max_dtype  widest element type later calls may pass (informational; the
+ *             library keeps no per-size buffers: receive slots live in
+ *             on-chip shared memory of each launched block).
+ *  out        receives the handle.
+ * Allocates a few hundred bytes of device memory (counters, status).
+ * Errors: RRA_ERR_INVALID (bad nranks, max_count 0, NULL out, bad dtype),
+ * RRA_ERR_NOMEM, RRA_ERR_CUDA.
+ */
+rra_status rra_comm_create(int nranks, size_t max_count, rra_dtype max_dtype, rra_comm **out);
+
+/* Destroy a communicator (synchronises the device first).  NULL is a no-op. */
+rra_status rra_comm_destroy(rra_comm *comm);
+
+/*
+ * Two-pass ring allreduce ([ring] "两趟实现 ring allreduce"; [cccl] §2.1-2.2).
+ *  in[r]     device pointer to rank r's T input elements of type in_t
+ *            (with codec->diff_prev: the current round's fp32 values).
+ *  out[r]    device pointer to rank r's T output elements of type out_t.
+ *            out[r] may equal in[r] (in place); output buffers of different
+ *            ranks must not overlap, and none may overlap diff_base.
+ *  codec     NULL or a codec (above).
+ * Schedule (steps s = 1..N-1 in each pass): reduce-scatter step s, rank r
+ * sends chunk (r-s) mod N to rank r+1, which adds its own fp32 copy of that
+ * chunk to the decoded message; after N-1 steps rank r owns the full sum S_r
+ * of chunk r.  Lossless: S_r is sent as fp32.  With a codec, every hop
+ * re-encodes the sender's fp32 partial, the owner encodes S_r once, the
+ * allgather pass (step s: rank r sends chunk (r-s+1) mod N) forwards those
+ * codes unchanged, and every rank, the owner included, outputs their decoded
+ * value, so all N outputs are bit-identical.  Lossless sums follow the ring
+ * order ((x_{c+1} + x_{c+2}) + ...) + x_c exactly (fp32, round to nearest
+ * even, no FMA).  Output: cast to out_t with round to nearest even, after the
+ * optional average and diff_base epilogue.
+ * Wire formats per slice of <= RRA_RING_SLICE elements (len elements):
+ *  NONE   fp32[len]                                       4 len bytes
+ *  BFP    int8 exps[ceil(len/128)] + mantissas            ceil(len/128) + len (8-bit)
+ *                                                         or + ceil(len/2) (4-bit)
+ *  SPARSE {uint32 fmt, uint32 nnz} + fp32 vals[nnz] + int32 idx[nnz]
+ *         (slice-relative, ascending)  = 8 + 8 nnz bytes, or dense
+ *         {fmt = 0, nnz} + fp32[len] = 8 + 4 len bytes.
+ * Errors: RRA_ERR_INVALID (NULL pointers, count 0 or > max_count, bad enums,
+ * bits not 8/4, threshold outside [0,1), diff_prev with in_t != F32,
+ * out overlapping diff_base), RRA_ERR_CUDA.
+ */
+rra_status rra_ring_allreduce(rra_comm *comm, const void *const *in, void *const *out,
+                              size_t count, rra_dtype in_t, rra_dtype out_t,
+                              const rra_codec *codec, void *stream);
+
+/*
+ * Reduce-scatter: the first pass of the ring alone ([ring] table:
+ * T(N-1)/N bytes per rank, N-1 steps).  Only chunk r of out[r] is written
+ * (at its offset r*n); the rest of out[r] is left untouched.  The owner's
+ * value is its fp32 sum S_r (not re-encoded), then the same epilogue and
+ * cast as the allreduce.  Same arguments and errors as rra_ring_allreduce.
+ */
+rra_status rra_reduce_scatter(rra_comm *comm, const void *const *in, void *const *out,
+                              size_t count, rra_dtype in_t, rra_dtype out_t,
+                              const rra_codec *codec, void *stream);
+
+/*
+ * Allgather, in place ([ring] table: T(N-1)/N bytes per rank, N-1 steps):
+ * on entry chunk r of buf[r] holds rank r's contribution; on return every
+ * buf[r] holds all N chunks.  Elements are copied bit for bit, uncompressed
+ * ([cccl] §2.1: allgather and broadcast stay conservative).
+ * Errors: RRA_ERR_INVALID, RRA_ERR_CUDA.
+ */
+rra_status rra_allgather(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,
+                         void *stream);
+
+/*
+ * Broadcast from rank "root" over a binomial tree of depth ceil(log2 N)
+ * ([ring] table: T bytes per receiving rank, log2(N) tree).  At level
+ * k = 0..ceil(log2 N)-1 every relative rank q < 2^k with q + 2^k < N sends
+ * its whole buffer to q + 2^k (relative rank q = (r - root) mod N).  In
+ * place, bit-exact copies.  Errors: RRA_ERR_INVALID (root outside 0..N-1,
+ * ...), RRA_ERR_CUDA.
+ */
+rra_status rra_broadcast(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,
+                         int root, void *stream);
+
+/*
+ * Tree allreduce ([ring] table: T log2 N bytes, 2 log2 N steps; "练习":
+ * the tree variant for small messages).  Binomial reduce to rank 0 (at level
+ * k every rank r with r mod 2^(k+1) = 0 and r + 2^k < N adds rank r+2^k's
+ * fp32 partial to its own), then the binomial broadcast above from rank 0.
+ * In place; dtype must be RRA_F32 (RRA_ERR_UNSUPPORTED otherwise).
+ */
+rra_status rra_tree_allreduce(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,
+                              void *stream);
+
+/*
+ * Block-floating-point encode of x[0..n) ([cccl] §2.1, §3.3).  For each
+ * 128-element block (the last one may be short): e = floor(log2 max|x|)
+ * taken from the fp32 exponent bits (-126 for a zero or subnormal maximum),
+ * q = bits-2, m_i = clamp(rne(x_i * 2^(q-e)), -(2^(bits-1)-1), 2^(bits-1)-1).
+ *  x      device, n elements of dtype (widened to fp32 exactly).
+ *  exps   device, ceil(n/128) int8 exponents.
+ *  mants  device, n bytes (bits 8: int8 codes) or ceil(n/2) bytes (bits 4:
+ *         element 2j in the low nibble of byte j, 2j+1 in the high nibble,
+ *         two's complement; an odd tail leaves the last high nibble 0).
+ * Errors: RRA_ERR_INVALID (NULL, n 0, bits not 8/4), RRA_ERR_CUDA.
+ */
+rra_status rra_bfp_encode(const void *x, size_t n, rra_dtype dtype, int bits, int8_t *exps,
+                          uint8_t *mants, void *stream);
+
+/*
+ * Block-floating-point decode: out[i] = m_i * 2^(e-q) (exact in fp32), or,
+ * with accumulate != 0, out[i] = out[i] + m_i * 2^(e-q) (fp32, round to
+ * nearest even).  Layout as for rra_bfp_encode; out is device fp32[n].
+ */
+rra_status rra_bfp_decode(const int8_t *exps, const uint8_t *mants, size_t n, int bits,
+                          float *out, int accumulate, void *stream);
+
+/*
+ * Sparse encode of x[0..n) as ONE message ([cccl] §2.1: send only the
+ * nonzero values and their indices when the sparsity exceeds the
+ * threshold).  An element is zero iff its bit pattern, widened to fp32, is
+ * +0.0 (so -0.0 is kept and the round trip is exact).
+ *  hdr    device uint32[2]: hdr[0] = 1 (sparse) or 0 (dense), hdr[1] = nnz.
+ *  vals   device, n elements of dtype capacity.  Sparse: the nnz nonzero
+ *         values in index order.  Dense: a copy of x.
+ *  idx    device, n int32 capacity.  Sparse: the nnz indices, ascending.
+ * Sparse iff nnz < (1 - threshold) * n (evaluated in double).
+ * Uses scratch (one uint32 per 4096 elements) from a per-device workspace
+ * that the library allocates with cudaMalloc on the first call that needs
+ * more than it holds (so that first call must not be made during stream
+ * capture).  Errors: RRA_ERR_INVALID, RRA_ERR_NOMEM, RRA_ERR_CUDA.
+ */
+rra_status rra_sparse_encode(const void *x, size_t n, rra_dtype dtype, float threshold,
+                             uint32_t *hdr, void *vals, int32_t *idx, void *stream);
+
+/*
+ * Sparse decode into fp32 acc[0..n) (hdr, vals, idx as written by
+ * rra_sparse_encode; the format is read on the device).
+ *  accumulate == 0: acc = the restored message (+0.0 where a sparse message
+ *                   lists nothing).
+ *  accumulate != 0: acc[i] = acc[i] + v at every position the message
+ *                   carries (all of them when dense, the listed ones when
+ *                   sparse); other positions are left as they are.
+ */
+rra_status rra_sparse_decode(const uint32_t *hdr, const void *vals, const int32_t *idx,
+                             size_t n, rra_dtype dtype, float *acc, int accumulate,
+                             void *stream);
+
+/* Difference encoding ([cccl] §2.1): diff[i] = cur[i] - prev[i] in fp32,
+ * round to nearest even.  diff may alias cur or prev. */
+rra_status rra_diff_encode(const float *cur, const float *prev, float *diff, size_t n,
+                           void *stream);
+
+/*
+ * Byte counters of the last collective call on this communicator ([ring]
+ * "练习": per-rank byte counter): sent[r] / recv[r] = wire bytes rank r
+ * wrote into / read from receive slots, counted on the device.  Lossless
+ * ring: 2 (N-1) n * 4 bytes per rank when N divides T.  Synchronises the
+ * stream of that call.  sent, recv: HOST arrays of N entries.
+ * Errors: RRA_ERR_INVALID, RRA_ERR_CUDA, or a latched device error.
+ */
+rra_status rra_get_bytes(rra_comm *comm, uint64_t *sent, uint64_t *recv);
+
+/* Synchronise the last call's stream, return the latched device-side error
+ * (RRA_ERR_TIMEOUT, ...) or RRA_OK, and clear it. */
+rra_status rra_comm_status(rra_comm *comm);
+
+/* Time limit of every device-side wait (mailbox and copy waits), in
+ * nanoseconds; 0 restores the default (2 s).  On expiry the kernel latches
+ * RRA_ERR_TIMEOUT and returns instead of waiting further ([ring] "练习":
+ * a stuck rank raises a deadline error instead of hanging). */
+rra_status rra_set_timeout(rra_comm *comm, uint64_t ns);
+
+/* Test-only fault injection: in the next collective call, simulated rank
+ * "rank" does not publish the message it sends at ring step "step" (1-based,
+ * counted over both passes) for the first slice each block handles, so its
+ * receiver's wait runs out and the call ends with RRA_ERR_TIMEOUT.  rank < 0
+ * disables.  The setting applies to one call only. */
+rra_status rra_debug_withhold(rra_comm *comm, int rank, int step);
+
+/* Human-readable name of a status code (static string). */
+const char *rra_status_string(rra_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RRA_H */

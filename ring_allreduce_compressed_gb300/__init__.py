@@ -1,0 +1,246 @@
+"""Python binding of librra (include/rra.h): the chunked ring allreduce with
+gradient-compression codecs for N ranks simulated on one GB300 (sm_103a).
+
+This module only marshals arguments (tensor pointers, dtype codes, the
+current CUDA stream) into the C ABI; every step of every collective and codec
+runs in the library's CUDA kernels.  PyTorch supplies device memory and
+streams.  There is no CPU fallback: importing works without a GPU, but every
+call needs the built library and a CUDA device, and raises otherwise.
+
+Names follow the C ABI: ``Comm.ring_allreduce``, ``Comm.reduce_scatter``,
+``Comm.allgather``, ``Comm.broadcast``, ``Comm.tree_allreduce``,
+``bfp_encode``/``bfp_decode``, ``sparse_encode``/``sparse_decode``,
+``diff_encode``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "librra.so")
+
+RRA_OK, RRA_ERR_INVALID, RRA_ERR_UNSUPPORTED, RRA_ERR_CUDA, RRA_ERR_TIMEOUT, RRA_ERR_NOMEM = range(6)
+RRA_F32, RRA_F16, RRA_BF16 = 0, 1, 2
+CODEC_NONE, CODEC_BFP, CODEC_SPARSE = 0, 1, 2
+MAX_RANKS = 64
+BFP_BLOCK = 128
+RING_SLICE = 256
+
+_lib = None
+
+
+class RRAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)}")
+
+
+class _Codec(C.Structure):
+    _fields_ = [("kind", C.c_int), ("bits", C.c_int), ("sparsity_threshold", C.c_float),
+                ("diff_prev", C.c_void_p), ("diff_base", C.c_void_p), ("average", C.c_int)]
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile librra.so in-tree (see _compile.py)."""
+    from . import _compile
+    return _compile.build(force=force, verbose=verbose)
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"librra.so is not built ({LIB_PATH}); run "
+                               "ring_allreduce_compressed_gb300.build() first")
+        L = C.CDLL(LIB_PATH)
+        vp, sz, i32, st = C.c_void_p, C.c_size_t, C.c_int, C.c_int
+        L.rra_comm_create.argtypes = [i32, sz, i32, C.POINTER(C.c_void_p)]
+        L.rra_comm_destroy.argtypes = [vp]
+        L.rra_ring_allreduce.argtypes = [vp, vp, vp, sz, i32, i32, vp, vp]
+        L.rra_reduce_scatter.argtypes = [vp, vp, vp, sz, i32, i32, vp, vp]
+        L.rra_allgather.argtypes = [vp, vp, sz, i32, vp]
+        L.rra_broadcast.argtypes = [vp, vp, sz, i32, i32, vp]
+        L.rra_tree_allreduce.argtypes = [vp, vp, sz, i32, vp]
+        L.rra_bfp_encode.argtypes = [vp, sz, i32, i32, vp, vp, vp]
+        L.rra_bfp_decode.argtypes = [vp, vp, sz, i32, vp, i32, vp]
+        L.rra_sparse_encode.argtypes = [vp, sz, i32, C.c_float, vp, vp, vp, vp]
+        L.rra_sparse_decode.argtypes = [vp, vp, vp, sz, i32, vp, i32, vp]
+        L.rra_diff_encode.argtypes = [vp, vp, vp, sz, vp]
+        L.rra_get_bytes.argtypes = [vp, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64)]
+        L.rra_comm_status.argtypes = [vp]
+        L.rra_set_timeout.argtypes = [vp, C.c_uint64]
+        L.rra_debug_withhold.argtypes = [vp, i32, i32]
+        L.rra_status_string.argtypes = [i32]
+        L.rra_status_string.restype = C.c_char_p
+        for name in ("rra_comm_create", "rra_comm_destroy", "rra_ring_allreduce",
+                     "rra_reduce_scatter", "rra_allgather", "rra_broadcast", "rra_tree_allreduce",
+                     "rra_bfp_encode", "rra_bfp_decode", "rra_sparse_encode", "rra_sparse_decode",
+                     "rra_diff_encode", "rra_get_bytes", "rra_comm_status", "rra_set_timeout",
+                     "rra_debug_withhold"):
+            getattr(L, name).restype = st
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().rra_status_string(code).decode()
+
+
+def _check(code: int, where: str):
+    if code != RRA_OK:
+        raise RRAError(code, where)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    m = {torch.float32: RRA_F32, torch.float16: RRA_F16, torch.bfloat16: RRA_BF16}
+    if t not in m:
+        raise TypeError(f"unsupported dtype {t}")
+    return m[t]
+
+
+def _stream(stream) -> C.c_void_p:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, name):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA tensor")
+    return t.data_ptr()
+
+
+def _ptrs(ts: Sequence, name: str):
+    return (C.c_void_p * len(ts))(*[_dev(t, name) for t in ts])
+
+
+@dataclass
+class Codec:
+    """Codec of a reducing call (rra_codec).  kind: "none" | "bfp" | "sparse"."""
+    kind: str = "none"
+    bits: int = 8
+    sparsity_threshold: float = 0.5
+    diff_prev: Optional[Sequence] = None  # N fp32 tensors (previous round)
+    diff_base: Optional[object] = None    # fp32 tensor (previous result)
+    average: bool = False
+
+    def _marshal(self):
+        kinds = {"none": CODEC_NONE, "bfp": CODEC_BFP, "sparse": CODEC_SPARSE}
+        keep = []
+        c = _Codec()
+        c.kind = kinds[self.kind]
+        c.bits = int(self.bits)
+        c.sparsity_threshold = float(self.sparsity_threshold)
+        if self.diff_prev is not None:
+            arr = _ptrs(self.diff_prev, "diff_prev")
+            keep.append(arr)
+            c.diff_prev = C.cast(arr, C.c_void_p)
+        if self.diff_base is not None:
+            c.diff_base = _dev(self.diff_base, "diff_base")
+        c.average = 1 if self.average else 0
+        return c, keep
+
+
+class Comm:
+    """A communicator of ``nranks`` simulated ranks on the current device."""
+
+    def __init__(self, nranks: int, max_count: int, max_dtype=None):
+        import torch
+        code = _dtype_code(max_dtype if max_dtype is not None else torch.float32)
+        h = C.c_void_p()
+        _check(lib().rra_comm_create(nranks, max_count, code, C.byref(h)), "rra_comm_create")
+        self._h = h
+        self.nranks = nranks
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().rra_comm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _reduce(self, fn, name, inputs, outputs, codec, stream):
+        if len(inputs) != self.nranks or len(outputs) != self.nranks:
+            raise ValueError(f"{name}: need {self.nranks} inputs and outputs")
+        c, keep = (codec or Codec())._marshal()
+        _check(fn(self._h, _ptrs(inputs, "inputs"), _ptrs(outputs, "outputs"), inputs[0].numel(),
+                  _dtype_code(inputs[0].dtype), _dtype_code(outputs[0].dtype), C.byref(c),
+                  _stream(stream)), name)
+        del keep
+
+    def ring_allreduce(self, inputs, outputs, codec: Optional[Codec] = None, stream=None):
+        self._reduce(lib().rra_ring_allreduce, "rra_ring_allreduce", inputs, outputs, codec, stream)
+
+    def reduce_scatter(self, inputs, outputs, codec: Optional[Codec] = None, stream=None):
+        self._reduce(lib().rra_reduce_scatter, "rra_reduce_scatter", inputs, outputs, codec, stream)
+
+    def allgather(self, bufs, stream=None):
+        _check(lib().rra_allgather(self._h, _ptrs(bufs, "bufs"), bufs[0].numel(),
+                                   _dtype_code(bufs[0].dtype), _stream(stream)), "rra_allgather")
+
+    def broadcast(self, bufs, root: int = 0, stream=None):
+        _check(lib().rra_broadcast(self._h, _ptrs(bufs, "bufs"), bufs[0].numel(),
+                                   _dtype_code(bufs[0].dtype), root, _stream(stream)),
+               "rra_broadcast")
+
+    def tree_allreduce(self, bufs, stream=None):
+        _check(lib().rra_tree_allreduce(self._h, _ptrs(bufs, "bufs"), bufs[0].numel(),
+                                        _dtype_code(bufs[0].dtype), _stream(stream)),
+               "rra_tree_allreduce")
+
+    def get_bytes(self):
+        sent = (C.c_uint64 * self.nranks)()
+        recv = (C.c_uint64 * self.nranks)()
+        _check(lib().rra_get_bytes(self._h, sent, recv), "rra_get_bytes")
+        return list(sent), list(recv)
+
+    def status(self) -> int:
+        """Latched device-side status of the last call (cleared by reading)."""
+        return lib().rra_comm_status(self._h)
+
+    def set_timeout(self, ns: int):
+        _check(lib().rra_set_timeout(self._h, int(ns)), "rra_set_timeout")
+
+    def debug_withhold(self, rank: int, step: int):
+        _check(lib().rra_debug_withhold(self._h, rank, step), "rra_debug_withhold")
+
+
+# ---------------------------------------------------------------- codecs
+
+def bfp_encode(x, bits: int, exps, mants, stream=None):
+    _check(lib().rra_bfp_encode(_dev(x, "x"), x.numel(), _dtype_code(x.dtype), bits,
+                                _dev(exps, "exps"), _dev(mants, "mants"), _stream(stream)),
+           "rra_bfp_encode")
+
+
+def bfp_decode(exps, mants, n: int, bits: int, out, accumulate: bool = False, stream=None):
+    _check(lib().rra_bfp_decode(_dev(exps, "exps"), _dev(mants, "mants"), n, bits,
+                                _dev(out, "out"), int(accumulate), _stream(stream)),
+           "rra_bfp_decode")
+
+
+def sparse_encode(x, threshold: float, hdr, vals, idx, stream=None):
+    _check(lib().rra_sparse_encode(_dev(x, "x"), x.numel(), _dtype_code(x.dtype), threshold,
+                                   _dev(hdr, "hdr"), _dev(vals, "vals"), _dev(idx, "idx"),
+                                   _stream(stream)), "rra_sparse_encode")
+
+
+def sparse_decode(hdr, vals, idx, n: int, acc, accumulate: bool = False, stream=None):
+    _check(lib().rra_sparse_decode(_dev(hdr, "hdr"), _dev(vals, "vals"), _dev(idx, "idx"), n,
+                                   _dtype_code(vals.dtype), _dev(acc, "acc"), int(accumulate),
+                                   _stream(stream)), "rra_sparse_decode")
+
+
+def diff_encode(cur, prev, diff, stream=None):
+    _check(lib().rra_diff_encode(_dev(cur, "cur"), _dev(prev, "prev"), _dev(diff, "diff"),
+                                 cur.numel(), _stream(stream)), "rra_diff_encode")

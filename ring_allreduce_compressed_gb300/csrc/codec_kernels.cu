@@ -1,0 +1,490 @@
+// codec_kernels.cu -- standalone streaming codec kernels for sm_103a
+// ("CCCL通信压缩库" §2.1: block floating point with one shared exponent per
+// 128-element block and 8- or 4-bit mantissas; sparse values + indices when
+// the sparsity exceeds a threshold; difference against the previous round).
+// All of them are HBM-bound streams: 128-bit loads and stores where the
+// buffers allow, grid-stride loops over warp-sized tiles.
+#include "rra_device.cuh"
+#include "rra_kernels.h"
+
+namespace rra {
+
+int num_sms()
+{
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0)
+            sms = 1;
+    }
+    return sms;
+}
+
+namespace {
+
+constexpr int kThreads = 256;
+
+inline int grid_for(long long work_items, int per_block)
+{
+    long long g = (work_items + per_block - 1) / per_block;
+    long long cap = (long long)num_sms() * 16;
+    if (g > cap)
+        g = cap;
+    return (int)(g < 1 ? 1 : g);
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- BFP encode
+// One warp per 256-element tile (two 128-element blocks, one per half-warp).
+template <int IN_T, int BITS>
+__global__ void __launch_bounds__(kThreads) bfp_encode_kernel(const void *__restrict__ x, long long n,
+                                                              int8_t *__restrict__ exps,
+                                                              uint8_t *__restrict__ mants, int vec)
+{
+    constexpr int es = dtype_size(IN_T);
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (kThreads / 32);
+    const long long tiles = (n + kTile - 1) / kTile;
+    for (long long t = blockIdx.x * (long long)(kThreads / 32) + (threadIdx.x >> 5); t < tiles;
+         t += warps) {
+        const long long e0 = t * kTile + 8 * lane;
+        const int vl = (int)max(0LL, min(8LL, n - e0));
+        float v[8];
+        const char *src = reinterpret_cast<const char *>(x) + e0 * es;
+        if (vec && vl == 8)
+            load8_vec<IN_T>(src, v);
+        else
+            load8_scalar<IN_T>(src, vl, v);
+        const int e = bfp_exponent(halfwarp_absmax(v));
+        int m[8];
+        bfp_codes<BITS>(v, e, m);
+        const long long blk = (t * kTile + 128 * (lane >> 4)) / kBlock;
+        if ((lane & 15) == 0 && blk * kBlock < n)
+            exps[blk] = (int8_t)e;
+        if constexpr (BITS == 8) {
+            if (vec && vl == 8) {
+                *reinterpret_cast<uint2 *>(mants + e0) = pack8(m);
+            } else {
+                for (int i = 0; i < vl; ++i)
+                    mants[e0 + i] = (uint8_t)(int8_t)m[i];
+            }
+        } else {
+            const uint32_t u = pack4(m);
+            if (vec && vl == 8) {
+                *reinterpret_cast<uint32_t *>(mants + e0 / 2) = u;
+            } else {
+                const int nb = (vl + 1) / 2; // an odd tail keeps its high nibble 0
+                for (int b = 0; b < nb; ++b)
+                    mants[e0 / 2 + b] = (uint8_t)((u >> (8 * b)) & (2 * b + 1 < vl ? 0xffu : 0x0fu));
+            }
+        }
+    }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads) bfp_decode_kernel(const int8_t *__restrict__ exps,
+                                                              const uint8_t *__restrict__ mants,
+                                                              long long n, float *__restrict__ out,
+                                                              int accumulate, int vec)
+{
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (kThreads / 32);
+    const long long tiles = (n + kTile - 1) / kTile;
+    for (long long t = blockIdx.x * (long long)(kThreads / 32) + (threadIdx.x >> 5); t < tiles;
+         t += warps) {
+        const long long e0 = t * kTile + 8 * lane;
+        const int vl = (int)max(0LL, min(8LL, n - e0));
+        if (vl == 0)
+            continue;
+        const int e = exps[e0 / kBlock];
+        int m[8];
+        if constexpr (BITS == 8) {
+            if (vec && vl == 8) {
+                unpack8(*reinterpret_cast<const uint2 *>(mants + e0), m);
+            } else {
+                for (int i = 0; i < 8; ++i)
+                    m[i] = i < vl ? (int)(int8_t)mants[e0 + i] : 0;
+            }
+        } else {
+            uint32_t u = 0;
+            if (vec && vl == 8) {
+                u = *reinterpret_cast<const uint32_t *>(mants + e0 / 2);
+            } else {
+                for (int b = 0; b < (vl + 1) / 2; ++b)
+                    u |= (uint32_t)mants[e0 / 2 + b] << (8 * b);
+            }
+            unpack4(u, m);
+        }
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            v[i] = bfp_value<BITS>(m[i], e);
+        if (accumulate) {
+            float o[8];
+            if (vec && vl == 8)
+                load8_vec<kF32>(out + e0, o);
+            else
+                load8_scalar<kF32>(out + e0, vl, o);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[i] = __fadd_rn(o[i], v[i]);
+        }
+        store8(out + e0, kF32, v, vl, vec != 0);
+    }
+}
+
+// ---------------------------------------------------------------- sparse encode
+// Tile of 4096 elements per block: 256 threads x 16 elements (two groups of
+// 8 consecutive elements per thread).  Pass 1 counts the tile's nonzeros;
+// pass 2 (one block) turns the counts into exclusive offsets, decides the
+// format and writes the header; pass 3 writes the values and indices: a
+// thread's slot comes from a warp ballot/popc prefix and a block prefix sum
+// over the warps, plus the tile offset.
+constexpr int kSpTile = 4096;
+
+template <int IN_T>
+__device__ __forceinline__ uint32_t nz_mask8(const void *x, long long n, long long e0, int vec,
+                                             float v[8])
+{
+    constexpr int es = dtype_size(IN_T);
+    const int vl = (int)max(0LL, min(8LL, n - e0));
+    const char *src = reinterpret_cast<const char *>(x) + e0 * es;
+    if (vec && vl == 8)
+        load8_vec<IN_T>(src, v);
+    else
+        load8_scalar<IN_T>(src, vl, v);
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (i < vl && __float_as_uint(v[i]) != 0u)
+            m |= 1u << i;
+    return m;
+}
+
+template <int IN_T>
+__global__ void __launch_bounds__(kThreads) sparse_count_kernel(const void *__restrict__ x,
+                                                                long long n, uint32_t *counts,
+                                                                int vec)
+{
+    __shared__ uint32_t wsum[kThreads / 32];
+    const long long tiles = (n + kSpTile - 1) / kSpTile;
+    for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
+        uint32_t c = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float v[8];
+            const long long e0 = t * kSpTile + (long long)h * 2048 + 8 * threadIdx.x;
+            c += __popc(nz_mask8<IN_T>(x, n, e0, vec, v));
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+            c += __shfl_xor_sync(kFull, c, o);
+        if ((threadIdx.x & 31) == 0)
+            wsum[threadIdx.x >> 5] = c;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t s = 0;
+            for (int w = 0; w < kThreads / 32; ++w)
+                s += wsum[w];
+            counts[t] = s;
+        }
+        __syncthreads();
+    }
+}
+
+// Single block of 1024 threads: exclusive scan of the tile counts in place,
+// header {sparse?, nnz}.
+__global__ void __launch_bounds__(1024) sparse_scan_kernel(uint32_t *counts, long long tiles,
+                                                           long long n, double one_minus_thr,
+                                                           uint32_t *hdr)
+{
+    __shared__ unsigned long long part[1024];
+    const long long per = (tiles + 1023) / 1024;
+    const long long lo = threadIdx.x * per;
+    const long long hi = min(tiles, lo + per);
+    unsigned long long s = 0;
+    for (long long i = lo; i < hi; ++i)
+        s += counts[i];
+    part[threadIdx.x] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long run = 0;
+        for (int i = 0; i < 1024; ++i) {
+            const unsigned long long v = part[i];
+            part[i] = run;
+            run += v;
+        }
+        const bool sparse = (double)run < one_minus_thr * (double)n;
+        hdr[0] = sparse ? 1u : 0u;
+        hdr[1] = (uint32_t)run;
+    }
+    __syncthreads();
+    unsigned long long run = part[threadIdx.x];
+    for (long long i = lo; i < hi; ++i) {
+        const uint32_t v = counts[i];
+        counts[i] = (uint32_t)run;
+        run += v;
+    }
+}
+
+template <int IN_T>
+__global__ void __launch_bounds__(kThreads) sparse_emit_kernel(const void *__restrict__ x, long long n,
+                                                               const uint32_t *__restrict__ offsets,
+                                                               const uint32_t *__restrict__ hdr,
+                                                               void *__restrict__ vals,
+                                                               int32_t *__restrict__ idx, int vec)
+{
+    using E = typename Elem<IN_T>::type;
+    constexpr int es = dtype_size(IN_T);
+    __shared__ uint32_t wsum[kThreads / 32];
+    const bool sparse = hdr[0] != 0u;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long tiles = (n + kSpTile - 1) / kSpTile;
+    for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
+        if (!sparse) {
+            // dense fallback: vals = x (bit copy)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const long long e0 = t * kSpTile + (long long)h * 2048 + 8 * threadIdx.x;
+                const int vl = (int)max(0LL, min(8LL, n - e0));
+                const char *src = reinterpret_cast<const char *>(x) + e0 * es;
+                char *dst = reinterpret_cast<char *>(vals) + e0 * es;
+                if (vec && vl == 8) {
+#pragma unroll
+                    for (int b = 0; b < es / 2; ++b)
+                        reinterpret_cast<uint4 *>(dst)[b] = reinterpret_cast<const uint4 *>(src)[b];
+                } else {
+                    for (int i = 0; i < vl; ++i)
+                        reinterpret_cast<E *>(dst)[i] = reinterpret_cast<const E *>(src)[i];
+                }
+            }
+            continue;
+        }
+        float v[2][8];
+        uint32_t msk[2];
+        uint32_t mine = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const long long e0 = t * kSpTile + (long long)h * 2048 + 8 * threadIdx.x;
+            msk[h] = nz_mask8<IN_T>(x, n, e0, vec, v[h]);
+        }
+        // order of elements in the tile: half h, thread, element -> the
+        // compacted order must follow it, so scan half 0 fully before half 1
+        uint32_t base = offsets[t];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t c = __popc(msk[h]);
+            uint32_t incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o)
+                    incl += y;
+            }
+            if (lane == 31)
+                wsum[warp] = incl;
+            __syncthreads();
+            uint32_t before = 0, total = 0;
+            for (int w = 0; w < kThreads / 32; ++w) {
+                const uint32_t s = wsum[w];
+                if (w < warp)
+                    before += s;
+                total += s;
+            }
+            uint32_t pos = base + before + incl - c;
+            const long long e0 = t * kSpTile + (long long)h * 2048 + 8 * threadIdx.x;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if ((msk[h] >> i) & 1u) {
+                    if constexpr (IN_T == kF32)
+                        reinterpret_cast<float *>(vals)[pos] = v[h][i];
+                    else
+                        reinterpret_cast<E *>(vals)[pos] = reinterpret_cast<const E *>(x)[e0 + i];
+                    idx[pos] = (int32_t)(e0 + i);
+                    ++pos;
+                }
+            base += total;
+            mine += c;
+            __syncthreads();
+        }
+        (void)mine;
+    }
+}
+
+// ---------------------------------------------------------------- sparse decode
+template <int IN_T>
+__global__ void __launch_bounds__(kThreads) sparse_dense_kernel(const uint32_t *__restrict__ hdr,
+                                                                const void *__restrict__ vals,
+                                                                long long n, float *__restrict__ acc,
+                                                                int accumulate, int vec)
+{
+    constexpr int es = dtype_size(IN_T);
+    const bool sparse = hdr[0] != 0u;
+    if (sparse && accumulate)
+        return;
+    const long long groups = (n + 7) / 8;
+    for (long long gi = blockIdx.x * (long long)kThreads + threadIdx.x; gi < groups;
+         gi += (long long)gridDim.x * kThreads) {
+        const long long e0 = gi * 8;
+        const int vl = (int)min(8LL, n - e0);
+        float v[8];
+        if (sparse) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[i] = 0.0f;
+        } else {
+            const char *src = reinterpret_cast<const char *>(vals) + e0 * es;
+            if (vec && vl == 8)
+                load8_vec<IN_T>(src, v);
+            else
+                load8_scalar<IN_T>(src, vl, v);
+            if (accumulate) {
+                float o[8];
+                if (vec && vl == 8)
+                    load8_vec<kF32>(acc + e0, o);
+                else
+                    load8_scalar<kF32>(acc + e0, vl, o);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    v[i] = __fadd_rn(o[i], v[i]);
+            }
+        }
+        store8(acc + e0, kF32, v, vl, vec != 0);
+    }
+}
+
+template <int IN_T>
+__global__ void __launch_bounds__(kThreads) sparse_scatter_kernel(const uint32_t *__restrict__ hdr,
+                                                                  const void *__restrict__ vals,
+                                                                  const int32_t *__restrict__ idx,
+                                                                  long long n, float *acc,
+                                                                  int accumulate)
+{
+    using E = typename Elem<IN_T>::type;
+    if (hdr[0] == 0u)
+        return;
+    const long long nnz = min((long long)hdr[1], n); // a header never lists more than n
+    for (long long k = blockIdx.x * (long long)kThreads + threadIdx.x; k < nnz;
+         k += (long long)gridDim.x * kThreads) {
+        const long long i = idx[k];
+        if (i < 0 || i >= n)
+            continue; // malformed index: skip rather than write out of bounds
+        const float v = to_f32(reinterpret_cast<const E *>(vals)[k]);
+        acc[i] = accumulate ? __fadd_rn(acc[i], v) : v;
+    }
+}
+
+// ---------------------------------------------------------------- diff
+__global__ void __launch_bounds__(kThreads) diff_kernel(const float *cur, const float *prev,
+                                                        float *diff, long long n, int vec)
+{
+    const long long groups = (n + 7) / 8;
+    for (long long gi = blockIdx.x * (long long)kThreads + threadIdx.x; gi < groups;
+         gi += (long long)gridDim.x * kThreads) {
+        const long long e0 = gi * 8;
+        const int vl = (int)min(8LL, n - e0);
+        float a[8], b[8];
+        if (vec && vl == 8) {
+            load8_vec<kF32>(cur + e0, a);
+            load8_vec<kF32>(prev + e0, b);
+        } else {
+            load8_scalar<kF32>(cur + e0, vl, a);
+            load8_scalar<kF32>(prev + e0, vl, b);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            a[i] = __fsub_rn(a[i], b[i]);
+        store8(diff + e0, kF32, a, vl, vec != 0);
+    }
+}
+
+} // namespace
+
+// ---------------------------------------------------------------- launchers
+
+cudaError_t launch_bfp_encode(const void *x, long long n, int dtype, int bits, int8_t *exps,
+                              uint8_t *mants, cudaStream_t st)
+{
+    const int es = dtype_size(dtype);
+    const int vec = aligned16(x) && ((reinterpret_cast<uintptr_t>(mants) & 7u) == 0) ? 1 : 0;
+    (void)es;
+    const int grid = grid_for((n + kTile - 1) / kTile, kThreads / 32);
+#define RRA_ENC(T, B) bfp_encode_kernel<T, B><<<grid, kThreads, 0, st>>>(x, n, exps, mants, vec)
+    if (bits == 8) {
+        if (dtype == kF32) RRA_ENC(kF32, 8);
+        else if (dtype == kF16) RRA_ENC(kF16, 8);
+        else RRA_ENC(kBF16, 8);
+    } else {
+        if (dtype == kF32) RRA_ENC(kF32, 4);
+        else if (dtype == kF16) RRA_ENC(kF16, 4);
+        else RRA_ENC(kBF16, 4);
+    }
+#undef RRA_ENC
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bfp_decode(const int8_t *exps, const uint8_t *mants, long long n, int bits,
+                              float *out, int accumulate, cudaStream_t st)
+{
+    const int vec = aligned16(out) && ((reinterpret_cast<uintptr_t>(mants) & 7u) == 0) ? 1 : 0;
+    const int grid = grid_for((n + kTile - 1) / kTile, kThreads / 32);
+    if (bits == 8)
+        bfp_decode_kernel<8><<<grid, kThreads, 0, st>>>(exps, mants, n, out, accumulate, vec);
+    else
+        bfp_decode_kernel<4><<<grid, kThreads, 0, st>>>(exps, mants, n, out, accumulate, vec);
+    return cudaGetLastError();
+}
+
+long long sparse_encode_scratch_words(long long n) { return (n + kSpTile - 1) / kSpTile; }
+
+cudaError_t launch_sparse_encode(const void *x, long long n, int dtype, double one_minus_thr,
+                                 uint32_t *hdr, void *vals, int32_t *idx, uint32_t *scratch,
+                                 cudaStream_t st)
+{
+    const long long tiles = sparse_encode_scratch_words(n);
+    const int vec = aligned16(x) && aligned16(vals) ? 1 : 0;
+    const int grid = grid_for(tiles, 1);
+#define RRA_SP(T)                                                                              \
+    do {                                                                                       \
+        sparse_count_kernel<T><<<grid, kThreads, 0, st>>>(x, n, scratch, vec);                 \
+        sparse_scan_kernel<<<1, 1024, 0, st>>>(scratch, tiles, n, one_minus_thr, hdr);         \
+        sparse_emit_kernel<T><<<grid, kThreads, 0, st>>>(x, n, scratch, hdr, vals, idx, vec);  \
+    } while (0)
+    if (dtype == kF32) RRA_SP(kF32);
+    else if (dtype == kF16) RRA_SP(kF16);
+    else RRA_SP(kBF16);
+#undef RRA_SP
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_decode(const uint32_t *hdr, const void *vals, const int32_t *idx,
+                                 long long n, int dtype, float *acc, int accumulate,
+                                 cudaStream_t st)
+{
+    const int vec = aligned16(vals) && aligned16(acc) ? 1 : 0;
+    const int g1 = grid_for((n + 7) / 8, kThreads);
+    const int g2 = num_sms() * 4;
+#define RRA_SD(T)                                                                                  \
+    do {                                                                                           \
+        sparse_dense_kernel<T><<<g1, kThreads, 0, st>>>(hdr, vals, n, acc, accumulate, vec);       \
+        sparse_scatter_kernel<T><<<g2, kThreads, 0, st>>>(hdr, vals, idx, n, acc, accumulate);     \
+    } while (0)
+    if (dtype == kF32) RRA_SD(kF32);
+    else if (dtype == kF16) RRA_SD(kF16);
+    else RRA_SD(kBF16);
+#undef RRA_SD
+    return cudaGetLastError();
+}
+
+cudaError_t launch_diff_encode(const float *cur, const float *prev, float *diff, long long n,
+                               cudaStream_t st)
+{
+    const int vec = aligned16(cur) && aligned16(prev) && aligned16(diff) ? 1 : 0;
+    diff_kernel<<<grid_for((n + 7) / 8, kThreads), kThreads, 0, st>>>(cur, prev, diff, n, vec);
+    return cudaGetLastError();
+}
+
+} // namespace rra

@@ -1,0 +1,314 @@
+// rra_device.cuh -- device building blocks shared by the sm_103a kernels:
+// PTX wrappers (mbarrier, bulk async copy, global timer), bounded waits,
+// the per-warp tile layout, dtype conversions and the block-floating-point
+// arithmetic.
+//
+// Tile layout used everywhere: a warp handles a slice of 256 elements; lane L
+// holds elements [8L, 8L+8).  A 128-element BFP block is therefore one
+// half-warp (lanes 0-15 and 16-31).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rra {
+
+constexpr int kTile = 256;       // elements per warp slice (= RRA_RING_SLICE)
+constexpr int kEpl = 8;          // elements per lane
+constexpr int kBlock = 128;      // BFP block (= RRA_BFP_BLOCK)
+constexpr unsigned kFull = 0xffffffffu;
+
+enum Dtype { kF32 = 0, kF16 = 1, kBF16 = 2 };
+enum Status : unsigned { kStOk = 0, kStTimeout = 4 };
+
+__host__ __device__ constexpr int dtype_size(int t) { return t == kF32 ? 4 : 2; }
+
+// ---------------------------------------------------------------- PTX
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Arrive once (release at CTA scope: prior shared-memory writes of this
+// thread, and those ordered before it by a warp barrier, become visible to a
+// thread that observes the phase flip with an acquire wait).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t tx)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "r"(tx)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// One-dimensional bulk copy global -> this CTA's shared memory, completing
+// "bytes" transaction bytes on the mbarrier.  dst and src 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+                 "[%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Warp-uniform bounded wait for the phase of parity "parity" of an mbarrier.
+// Every lane waits (each gets acquire ordering).  Gives up when the time
+// limit passes or when another warp has already latched an error in *status;
+// on a time-out it latches kStTimeout.  Returns true iff every lane saw the
+// phase complete.
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                           unsigned *status)
+{
+    bool ok = mbar_try_wait(bar, parity);
+    if (!ok) {
+        const uint64_t t0 = global_ns();
+        for (uint32_t it = 1;; ++it) {
+            if (mbar_try_wait(bar, parity)) {
+                ok = true;
+                break;
+            }
+            if ((it & 15u) == 0u) {
+                if (*reinterpret_cast<volatile unsigned *>(status) != 0u)
+                    break;
+                if (global_ns() - t0 > limit_ns) {
+                    atomicCAS(status, 0u, (unsigned)kStTimeout);
+                    break;
+                }
+            }
+        }
+    }
+    return __all_sync(kFull, ok);
+}
+
+// ---------------------------------------------------------------- dtypes
+
+template <int T> struct Elem;
+template <> struct Elem<kF32> {
+    using type = float;
+};
+template <> struct Elem<kF16> {
+    using type = __half;
+};
+template <> struct Elem<kBF16> {
+    using type = __nv_bfloat16;
+};
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// 8 consecutive elements of dtype IN_T at p (16-byte aligned for 16-bit
+// types, 32-byte for fp32) widened to fp32.
+template <int IN_T> __device__ __forceinline__ void load8_vec(const void *p, float v[8])
+{
+    if constexpr (IN_T == kF32) {
+        const float4 a = reinterpret_cast<const float4 *>(p)[0];
+        const float4 b = reinterpret_cast<const float4 *>(p)[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+        using E = typename Elem<IN_T>::type;
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        const E *e = reinterpret_cast<const E *>(&u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            v[i] = to_f32(e[i]);
+    }
+}
+
+// Bounds-checked element loads (any alignment); absent elements read as 0.
+template <int IN_T>
+__device__ __forceinline__ void load8_scalar(const void *base, int valid, float v[8])
+{
+    using E = typename Elem<IN_T>::type;
+    const E *p = reinterpret_cast<const E *>(base);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v[i] = i < valid ? to_f32(p[i]) : 0.0f;
+}
+
+__device__ __forceinline__ uint16_t f32_to_16(float v, int t)
+{
+    if (t == kF16)
+        return __half_as_ushort(__float2half_rn(v));
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+// Store 8 fp32 values as out_t (round to nearest even); vectorised when the
+// destination is 16-byte aligned and all 8 are present.
+__device__ __forceinline__ void store8(void *base, int out_t, const float v[8], int valid,
+                                       bool vec)
+{
+    if (out_t == kF32) {
+        float *p = reinterpret_cast<float *>(base);
+        if (vec && valid >= 8) {
+            reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+            reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < valid)
+                    p[i] = v[i];
+        }
+    } else {
+        uint16_t h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            h[i] = f32_to_16(v[i], out_t);
+        uint16_t *p = reinterpret_cast<uint16_t *>(base);
+        if (vec && valid >= 8) {
+            uint4 u;
+            u.x = h[0] | ((uint32_t)h[1] << 16);
+            u.y = h[2] | ((uint32_t)h[3] << 16);
+            u.z = h[4] | ((uint32_t)h[5] << 16);
+            u.w = h[6] | ((uint32_t)h[7] << 16);
+            *reinterpret_cast<uint4 *>(p) = u;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < valid)
+                    p[i] = h[i];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- BFP
+
+// 2^k as an fp32 value, for k in [-149, 127] (subnormal below -126).
+__device__ __forceinline__ float pow2i(int k)
+{
+    return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(1 << (k + 149));
+}
+
+// Block exponent from the bits of the block maximum |x| (>= 0): the unbiased
+// exponent of a normal number is floor(log2); zero and subnormal maxima
+// (biased exponent 0) give the clamp value -126.
+__device__ __forceinline__ int bfp_exponent(float amax)
+{
+    const int biased = (__float_as_int(amax) >> 23) & 0xff;
+    return max(biased, 1) - 127;
+}
+
+// x * 2^k, exact whenever the product is a normal number (k <= 132 here; the
+// factor is split so that no intermediate power of two overflows).  A
+// product in the subnormal range may be rounded, but it is then below 2^-126
+// and rounds to the integer 0 either way.
+__device__ __forceinline__ float scale_pow2(float x, int k)
+{
+    if (k > 127)
+        return __fmul_rn(__fmul_rn(x, pow2i(k - 64)), pow2i(64));
+    return __fmul_rn(x, pow2i(k));
+}
+
+// Maximum |v| over the 16 lanes of this lane's half-warp.
+__device__ __forceinline__ float halfwarp_absmax(const float v[8])
+{
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        m = fmaxf(m, fabsf(v[i]));
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    return m;
+}
+
+// Integer codes of this lane's 8 elements for block exponent e.
+template <int BITS> __device__ __forceinline__ void bfp_codes(const float v[8], int e, int m[8])
+{
+    constexpr int q = BITS - 2;
+    constexpr int M = (1 << (BITS - 1)) - 1;
+    const int k = q - e;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int c = __float2int_rn(scale_pow2(v[i], k));
+        m[i] = min(max(c, -M), M);
+    }
+}
+
+template <int BITS> __device__ __forceinline__ float bfp_value(int m, int e)
+{
+    return __fmul_rn(__int2float_rn(m), pow2i(e - (BITS - 2)));
+}
+
+// Pack / unpack the lane's 8 codes: 8-bit -> uint2 (byte i = element i),
+// 4-bit -> uint32 (nibble i = element i: element 2j low, 2j+1 high).
+__device__ __forceinline__ uint2 pack8(const int m[8])
+{
+    uint2 u;
+    u.x = (m[0] & 0xff) | ((m[1] & 0xff) << 8) | ((m[2] & 0xff) << 16) | ((uint32_t)(m[3] & 0xff) << 24);
+    u.y = (m[4] & 0xff) | ((m[5] & 0xff) << 8) | ((m[6] & 0xff) << 16) | ((uint32_t)(m[7] & 0xff) << 24);
+    return u;
+}
+__device__ __forceinline__ void unpack8(uint2 u, int m[8])
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m[i] = (int)(int8_t)((u.x >> (8 * i)) & 0xff);
+        m[i + 4] = (int)(int8_t)((u.y >> (8 * i)) & 0xff);
+    }
+}
+__device__ __forceinline__ uint32_t pack4(const int m[8])
+{
+    uint32_t u = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        u |= (uint32_t)(m[i] & 0xf) << (4 * i);
+    return u;
+}
+__device__ __forceinline__ void unpack4(uint32_t u, int m[8])
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int nib = (u >> (4 * i)) & 0xf;
+        m[i] = nib >= 8 ? nib - 16 : nib;
+    }
+}
+
+// Wire bytes of one BFP message covering len elements.
+__host__ __device__ __forceinline__ uint32_t bfp_msg_bytes(int len, int bits)
+{
+    return (uint32_t)((len + kBlock - 1) / kBlock + (bits == 8 ? len : (len + 1) / 2));
+}
+
+} // namespace rra

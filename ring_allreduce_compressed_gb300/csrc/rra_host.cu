@@ -1,0 +1,575 @@
+// rra_host.cu -- the C ABI declared in include/rra.h: argument checks, the
+// communicator (device byte counters, status word, time limit, launch
+// configuration), path selection (bulk-copy fast path vs generic path) and
+// kernel launches.  No allocation happens on the collective paths.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+
+#include "rra.h"
+#include "rra_device.cuh"
+#include "rra_kernels.h"
+
+namespace rra {
+const void *ring_fn_none(int codec, int in_t, bool fast);
+const void *ring_fn_bfp(int codec, int in_t, bool fast);
+const void *ring_fn_sparse(int codec, int in_t, bool fast);
+} // namespace rra
+
+using namespace rra;
+
+struct rra_comm {
+    int N = 0;
+    int device = 0;
+    size_t max_count = 0;
+    unsigned long long *counters = nullptr; // [2 sets][sent N | recv N]
+    unsigned *status = nullptr;
+    uint64_t timeout_ns = 2000000000ull;
+    int withhold_rank = -1;
+    int withhold_step = 0;
+    unsigned gen = 0;          // counter set of the next call = gen & 1
+    int last_set = -1;         // counter set written by the last call
+    cudaStream_t last_stream = nullptr;
+    bool have_last = false;
+    int smem_optin = 0;
+    std::map<long long, int> occ; // (kernel key, smem) -> blocks per SM
+};
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+bool valid_dtype(int t) { return t == RRA_F32 || t == RRA_F16 || t == RRA_BF16; }
+size_t esize(int t) { return t == RRA_F32 ? 4 : 2; }
+bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void *a, size_t abytes, const void *b, size_t bbytes)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bbytes && y < x + abytes;
+}
+
+rra_status check_device(const rra_comm *c)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    return dev == c->device ? RRA_OK : RRA_ERR_INVALID;
+}
+
+// Counters for this call; block 0 of the launch clears the other set so the
+// next call starts from zero without a separate memset.
+void counter_sets(rra_comm *c, unsigned long long **sent, unsigned long long **recv,
+                  unsigned long long **zero)
+{
+    const int set = (int)(c->gen & 1u);
+    *sent = c->counters + (size_t)set * 2 * c->N;
+    *recv = *sent + c->N;
+    *zero = c->counters + (size_t)(set ^ 1) * 2 * c->N;
+    c->last_set = set;
+    c->gen++;
+}
+
+void note_call(rra_comm *c, cudaStream_t st)
+{
+    c->last_stream = st;
+    c->have_last = true;
+    c->withhold_rank = -1; // fault injection applies to one call only
+}
+
+int warps_for(int N) { return std::min(N, kMaxWarps); }
+
+// Mailbox depth and staging depth that fit the opt-in shared memory.
+bool pick_depths(rra_comm *c, int N, int slot_bytes, int stage_bytes, int warps, bool fast,
+                 bool sparse, int extra, int *K, int *D, int *smem)
+{
+    const int Ks[] = {2, 1};
+    const int Ds[] = {4, 3, 2, 1};
+    for (int k : Ks)
+        for (int d : Ds) {
+            if (!fast && d != Ds[0])
+                continue;
+            const Layout L = make_layout(N, k, fast ? d : 1, slot_bytes, stage_bytes, warps, fast,
+                                         sparse);
+            if (L.total + extra <= c->smem_optin) {
+                *K = k;
+                *D = fast ? d : 1;
+                *smem = L.total + extra;
+                return true;
+            }
+        }
+    return false;
+}
+
+int grid_for(rra_comm *c, long long key, const void *fn, int warps, int smem, long long items)
+{
+    const long long k = key * (1LL << 20) + smem;
+    int occ = 0;
+    auto it = c->occ.find(k);
+    if (it != c->occ.end()) {
+        occ = it->second;
+    } else {
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, warps * 32, (size_t)smem) !=
+                cudaSuccess ||
+            occ < 1)
+            occ = 1;
+        c->occ[k] = occ;
+    }
+    long long g = (long long)num_sms() * occ;
+    if (items < g)
+        g = items;
+    return (int)std::max(1LL, g);
+}
+
+const void *ring_fn(int codec, int in_t, bool fast)
+{
+    if (codec == kCodecNone)
+        return ring_fn_none(codec, in_t, fast);
+    if (codec == kCodecSparse)
+        return ring_fn_sparse(codec, in_t, fast);
+    return ring_fn_bfp(codec, in_t, fast);
+}
+
+int slot_bytes_for(int codec)
+{
+    switch (codec) {
+    case kCodecNone: return kTile * 4;
+    case kCodecBfp8: return 16 + kTile;
+    case kCodecBfp4: return 16 + kTile / 2;
+    default: return 16 + kTile * 8;
+    }
+}
+
+rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *const *out,
+                       size_t count, rra_dtype in_t, rra_dtype out_t, const rra_codec *codec,
+                       void *stream)
+{
+    if (!comm || !in || !out || count == 0 || count > comm->max_count || !valid_dtype(in_t) ||
+        !valid_dtype(out_t))
+        return RRA_ERR_INVALID;
+    rra_status s = check_device(comm);
+    if (s != RRA_OK)
+        return s;
+    const int N = comm->N;
+    rra_codec cd{};
+    cd.kind = RRA_CODEC_NONE;
+    if (codec)
+        cd = *codec;
+    int kc;
+    if (cd.kind == RRA_CODEC_NONE)
+        kc = kCodecNone;
+    else if (cd.kind == RRA_CODEC_BFP) {
+        if (cd.bits == 8)
+            kc = kCodecBfp8;
+        else if (cd.bits == 4)
+            kc = kCodecBfp4;
+        else
+            return RRA_ERR_INVALID;
+    } else if (cd.kind == RRA_CODEC_SPARSE) {
+        if (!(cd.sparsity_threshold >= 0.0f && cd.sparsity_threshold < 1.0f))
+            return RRA_ERR_INVALID;
+        kc = kCodecSparse;
+    } else {
+        return RRA_ERR_INVALID;
+    }
+    if (cd.diff_prev && in_t != RRA_F32)
+        return RRA_ERR_INVALID;
+    const size_t ib = count * esize(in_t), ob = count * esize(out_t);
+    for (int r = 0; r < N; ++r) {
+        if (!in[r] || !out[r] || (cd.diff_prev && !cd.diff_prev[r]))
+            return RRA_ERR_INVALID;
+        if (cd.diff_base && overlap(out[r], ob, cd.diff_base, count * 4))
+            return RRA_ERR_INVALID;
+        for (int q = 0; q < r; ++q)
+            if (overlap(out[r], ob, out[q], ob))
+                return RRA_ERR_INVALID;
+    }
+    (void)ib;
+
+    RingArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.N = N;
+    a.mode = mode;
+    a.in_t = in_t;
+    a.out_t = out_t;
+    a.T = (long long)count;
+    a.n = (a.T + N - 1) / N;
+    a.tiles = (a.n + kTile - 1) / kTile;
+    a.average = cd.average ? 1 : 0;
+    a.has_prev = cd.diff_prev ? 1 : 0;
+    a.base = cd.diff_base;
+    a.one_minus_thr = 1.0 - (double)cd.sparsity_threshold;
+    a.timeout_ns = comm->timeout_ns;
+    a.status = comm->status;
+    a.withhold_rank = comm->withhold_rank;
+    a.withhold_step = comm->withhold_step;
+
+    const size_t ies = esize(in_t), oes = esize(out_t);
+    bool fast = (a.n * ies) % 16 == 0 && (a.T * ies) % 16 == 0;
+    bool vec_out = (a.n * oes) % 16 == 0;
+    for (int r = 0; r < N; ++r) {
+        a.in[r] = in[r];
+        a.out[r] = out[r];
+        a.prev[r] = cd.diff_prev ? cd.diff_prev[r] : nullptr;
+        fast = fast && al16(in[r]) && (!cd.diff_prev || al16(cd.diff_prev[r]));
+        vec_out = vec_out && al16(out[r]);
+    }
+    a.vec_out = vec_out ? 1 : 0;
+    a.vec_base = (cd.diff_base && al16(cd.diff_base) && (a.n * 4) % 16 == 0) ? 1 : 0;
+
+    const int warps = warps_for(N);
+    a.slot_bytes = slot_bytes_for(kc);
+    a.stage_bytes = kTile * (int)ies * (cd.diff_prev ? 2 : 1);
+    if (cd.diff_prev)
+        a.stage_bytes = kTile * 4 * 2;
+    int smem = 0;
+    if (!pick_depths(comm, N, a.slot_bytes, a.stage_bytes, warps, fast, kc == kCodecSparse, 0,
+                     &a.K, &a.D, &smem)) {
+        fast = false;
+        if (!pick_depths(comm, N, a.slot_bytes, a.stage_bytes, warps, false, kc == kCodecSparse, 0,
+                         &a.K, &a.D, &smem))
+            return RRA_ERR_UNSUPPORTED;
+    }
+    const void *fn = ring_fn(kc, in_t, fast);
+    if (!fn)
+        return RRA_ERR_UNSUPPORTED;
+    const long long key = 1000 + kc * 100 + in_t * 10 + (fast ? 1 : 0);
+    const int grid = grid_for(comm, key, fn, warps, smem, a.tiles);
+    counter_sets(comm, &a.sent, &a.recv, &a.zero);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_ring(kc, in_t, fast, a, grid, warps, smem, st);
+    note_call(comm, st);
+    return e == cudaSuccess ? RRA_OK : RRA_ERR_CUDA;
+}
+
+rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count,
+                       rra_dtype dtype, int root, void *stream)
+{
+    if (!comm || !buf || count == 0 || count > comm->max_count || !valid_dtype(dtype))
+        return RRA_ERR_INVALID;
+    rra_status s = check_device(comm);
+    if (s != RRA_OK)
+        return s;
+    const int N = comm->N;
+    if (which == 1 && (root < 0 || root >= N))
+        return RRA_ERR_INVALID;
+    if (which == 2 && dtype != RRA_F32)
+        return RRA_ERR_UNSUPPORTED;
+    const size_t es = esize(dtype);
+    for (int r = 0; r < N; ++r) {
+        if (!buf[r])
+            return RRA_ERR_INVALID;
+        for (int q = 0; q < r; ++q)
+            if (overlap(buf[r], count * es, buf[q], count * es))
+                return RRA_ERR_INVALID;
+    }
+    CopyArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.N = N;
+    a.es = (int)es;
+    a.root = root;
+    a.T = (long long)count;
+    a.n = (a.T + N - 1) / N;
+    a.tiles = which == 0 ? (a.n + kTile - 1) / kTile : (a.T + kTile - 1) / kTile;
+    a.timeout_ns = comm->timeout_ns;
+    a.status = comm->status;
+    a.withhold_rank = comm->withhold_rank;
+    a.withhold_step = comm->withhold_step;
+    bool fast = (a.T * (long long)es) % 16 == 0 && (which != 0 || (a.n * (long long)es) % 16 == 0);
+    for (int r = 0; r < N; ++r) {
+        a.buf[r] = buf[r];
+        fast = fast && al16(buf[r]);
+    }
+    const int warps = warps_for(N);
+    a.slot_bytes = kTile * (int)es;
+    a.stage_bytes = kTile * (int)es;
+    const int extra = which == 2 ? N * kTile * 4 : 0; // tree accumulators
+    int smem = 0;
+    if (!pick_depths(comm, N, a.slot_bytes, a.stage_bytes, warps, fast, false, extra, &a.K, &a.D,
+                     &smem)) {
+        fast = false;
+        if (!pick_depths(comm, N, a.slot_bytes, a.stage_bytes, warps, false, false, extra, &a.K,
+                         &a.D, &smem))
+            return RRA_ERR_UNSUPPORTED;
+    }
+    int occ = 0;
+    const long long k = (long long)(which * 10 + (fast ? 1 : 0) + 50000) * (1LL << 20) + smem;
+    auto it = comm->occ.find(k);
+    if (it != comm->occ.end()) {
+        occ = it->second;
+    } else {
+        if (copy_kernel_attrs(which, fast, smem, warps, &occ) != cudaSuccess || occ < 1)
+            occ = 1;
+        comm->occ[k] = occ;
+    }
+    long long g = (long long)num_sms() * occ;
+    if (a.tiles < g)
+        g = a.tiles;
+    const int grid = (int)std::max(1LL, g);
+    counter_sets(comm, &a.sent, &a.recv, &a.zero);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (which == 0)
+        e = launch_allgather(fast, a, grid, warps, smem, st);
+    else if (which == 1)
+        e = launch_broadcast(fast, a, grid, warps, smem, st);
+    else
+        e = launch_tree(fast, a, grid, warps, smem, st);
+    note_call(comm, st);
+    return e == cudaSuccess ? RRA_OK : RRA_ERR_CUDA;
+}
+
+// Per-device scratch for the standalone sparse encoder (grown on demand).
+std::mutex g_ws_mu;
+std::map<int, std::pair<uint32_t *, long long>> g_ws;
+
+} // namespace
+
+namespace rra {
+cudaError_t launch_ring(int codec, int in_t, bool fast, const RingArgs &a, int grid, int warps,
+                        int smem, cudaStream_t st)
+{
+    const void *fn = ring_fn(codec, in_t, fast);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess)
+        return e;
+    void *args[] = {const_cast<RingArgs *>(&a)};
+    return cudaLaunchKernel(fn, dim3(grid), dim3(warps * 32), args, (size_t)smem, st);
+}
+} // namespace rra
+
+extern "C" {
+
+const char *rra_status_string(rra_status s)
+{
+    switch (s) {
+    case RRA_OK: return "RRA_OK";
+    case RRA_ERR_INVALID: return "RRA_ERR_INVALID";
+    case RRA_ERR_UNSUPPORTED: return "RRA_ERR_UNSUPPORTED";
+    case RRA_ERR_CUDA: return "RRA_ERR_CUDA";
+    case RRA_ERR_TIMEOUT: return "RRA_ERR_TIMEOUT";
+    case RRA_ERR_NOMEM: return "RRA_ERR_NOMEM";
+    }
+    return "RRA_ERR_UNKNOWN";
+}
+
+rra_status rra_comm_create(int nranks, size_t max_count, rra_dtype max_dtype, rra_comm **out)
+{
+    if (!out || nranks < 1 || nranks > RRA_MAX_RANKS || max_count == 0 || !valid_dtype(max_dtype))
+        return RRA_ERR_INVALID;
+    *out = nullptr;
+    rra_comm *c = new rra_comm();
+    c->N = nranks;
+    c->max_count = max_count;
+    if (cudaGetDevice(&c->device) != cudaSuccess) {
+        delete c;
+        return RRA_ERR_CUDA;
+    }
+    cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+    const size_t cbytes = sizeof(unsigned long long) * 4 * (size_t)nranks;
+    if (cudaMalloc(&c->counters, cbytes) != cudaSuccess) {
+        delete c;
+        return RRA_ERR_NOMEM;
+    }
+    if (cudaMalloc(&c->status, sizeof(unsigned)) != cudaSuccess) {
+        cudaFree(c->counters);
+        delete c;
+        return RRA_ERR_NOMEM;
+    }
+    if (cudaMemset(c->counters, 0, cbytes) != cudaSuccess ||
+        cudaMemset(c->status, 0, sizeof(unsigned)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(c->counters);
+        cudaFree(c->status);
+        delete c;
+        return RRA_ERR_CUDA;
+    }
+    *out = c;
+    return RRA_OK;
+}
+
+rra_status rra_comm_destroy(rra_comm *comm)
+{
+    if (!comm)
+        return RRA_OK;
+    cudaDeviceSynchronize();
+    cudaFree(comm->counters);
+    cudaFree(comm->status);
+    delete comm;
+    return RRA_OK;
+}
+
+rra_status rra_ring_allreduce(rra_comm *comm, const void *const *in, void *const *out,
+                              size_t count, rra_dtype in_t, rra_dtype out_t,
+                              const rra_codec *codec, void *stream)
+{
+    return ring_common(comm, kModeAllreduce, in, out, count, in_t, out_t, codec, stream);
+}
+
+rra_status rra_reduce_scatter(rra_comm *comm, const void *const *in, void *const *out,
+                              size_t count, rra_dtype in_t, rra_dtype out_t,
+                              const rra_codec *codec, void *stream)
+{
+    return ring_common(comm, kModeReduceScatter, in, out, count, in_t, out_t, codec, stream);
+}
+
+rra_status rra_allgather(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,
+                         void *stream)
+{
+    return copy_common(comm, 0, buf, count, dtype, 0, stream);
+}
+
+rra_status rra_broadcast(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,
+                         int root, void *stream)
+{
+    return copy_common(comm, 1, buf, count, dtype, root, stream);
+}
+
+rra_status rra_tree_allreduce(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,
+                              void *stream)
+{
+    return copy_common(comm, 2, buf, count, dtype, 0, stream);
+}
+
+rra_status rra_bfp_encode(const void *x, size_t n, rra_dtype dtype, int bits, int8_t *exps,
+                          uint8_t *mants, void *stream)
+{
+    if (!x || n == 0 || !exps || !mants || !valid_dtype(dtype) || (bits != 8 && bits != 4))
+        return RRA_ERR_INVALID;
+    return launch_bfp_encode(x, (long long)n, dtype, bits, exps, mants,
+                             reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RRA_OK
+               : RRA_ERR_CUDA;
+}
+
+rra_status rra_bfp_decode(const int8_t *exps, const uint8_t *mants, size_t n, int bits,
+                          float *out, int accumulate, void *stream)
+{
+    if (!exps || !mants || !out || n == 0 || (bits != 8 && bits != 4))
+        return RRA_ERR_INVALID;
+    return launch_bfp_decode(exps, mants, (long long)n, bits, out, accumulate,
+                             reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RRA_OK
+               : RRA_ERR_CUDA;
+}
+
+rra_status rra_sparse_encode(const void *x, size_t n, rra_dtype dtype, float threshold,
+                             uint32_t *hdr, void *vals, int32_t *idx, void *stream)
+{
+    if (!x || n == 0 || !hdr || !vals || !idx || !valid_dtype(dtype) ||
+        !(threshold >= 0.0f && threshold < 1.0f) || n > 0x7fffffffull)
+        return RRA_ERR_INVALID;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    const long long words = sparse_encode_scratch_words((long long)n);
+    uint32_t *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        auto &ws = g_ws[dev];
+        if (ws.second < words) {
+            if (ws.first) {
+                cudaDeviceSynchronize();
+                cudaFree(ws.first);
+                ws.first = nullptr;
+                ws.second = 0;
+            }
+            long long want = std::max(words, 1LL << 16);
+            if (cudaMalloc(&ws.first, (size_t)want * sizeof(uint32_t)) != cudaSuccess) {
+                ws.first = nullptr;
+                return RRA_ERR_NOMEM;
+            }
+            ws.second = want;
+        }
+        scratch = ws.first;
+    }
+    return launch_sparse_encode(x, (long long)n, dtype, 1.0 - (double)threshold, hdr, vals, idx,
+                                scratch, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RRA_OK
+               : RRA_ERR_CUDA;
+}
+
+rra_status rra_sparse_decode(const uint32_t *hdr, const void *vals, const int32_t *idx,
+                             size_t n, rra_dtype dtype, float *acc, int accumulate,
+                             void *stream)
+{
+    if (!hdr || !vals || !idx || !acc || n == 0 || !valid_dtype(dtype))
+        return RRA_ERR_INVALID;
+    return launch_sparse_decode(hdr, vals, idx, (long long)n, dtype, acc, accumulate,
+                                reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RRA_OK
+               : RRA_ERR_CUDA;
+}
+
+rra_status rra_diff_encode(const float *cur, const float *prev, float *diff, size_t n,
+                           void *stream)
+{
+    if (!cur || !prev || !diff || n == 0)
+        return RRA_ERR_INVALID;
+    return launch_diff_encode(cur, prev, diff, (long long)n,
+                              reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RRA_OK
+               : RRA_ERR_CUDA;
+}
+
+rra_status rra_get_bytes(rra_comm *comm, uint64_t *sent, uint64_t *recv)
+{
+    if (!comm || !sent || !recv)
+        return RRA_ERR_INVALID;
+    const int N = comm->N;
+    if (!comm->have_last) {
+        std::fill(sent, sent + N, 0);
+        std::fill(recv, recv + N, 0);
+        return RRA_OK;
+    }
+    if (cudaStreamSynchronize(comm->last_stream) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    const unsigned long long *src = comm->counters + (size_t)comm->last_set * 2 * N;
+    if (cudaMemcpy(sent, src, sizeof(uint64_t) * N, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(recv, src + N, sizeof(uint64_t) * N, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    unsigned st = 0;
+    if (cudaMemcpy(&st, comm->status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    return st ? (rra_status)st : RRA_OK;
+}
+
+rra_status rra_comm_status(rra_comm *comm)
+{
+    if (!comm)
+        return RRA_ERR_INVALID;
+    if (comm->have_last && cudaStreamSynchronize(comm->last_stream) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    unsigned st = 0;
+    if (cudaMemcpy(&st, comm->status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    if (st && cudaMemset(comm->status, 0, sizeof(unsigned)) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess)
+        return RRA_ERR_CUDA;
+    return st ? (rra_status)st : RRA_OK;
+}
+
+rra_status rra_set_timeout(rra_comm *comm, uint64_t ns)
+{
+    if (!comm)
+        return RRA_ERR_INVALID;
+    comm->timeout_ns = ns ? ns : kDefaultTimeoutNs;
+    return RRA_OK;
+}
+
+rra_status rra_debug_withhold(rra_comm *comm, int rank, int step)
+{
+    if (!comm || rank >= comm->N)
+        return RRA_ERR_INVALID;
+    comm->withhold_rank = rank < 0 ? -1 : rank;
+    comm->withhold_step = step;
+    return RRA_OK;
+}
+
+} // extern "C"

@@ -1,0 +1,137 @@
+// rra_kernels.h -- launch interface between the C ABI (rra_host.cu) and the
+// kernel translation units.  Host-side only types; no torch, no CUDA types
+// beyond cudaStream_t.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rra {
+
+constexpr int kMaxRanks = 64;
+constexpr int kMaxWarps = 16; // warps per block; ranks per warp = ceil(N / warps)
+
+enum Codec { kCodecNone = 0, kCodecBfp8 = 1, kCodecBfp4 = 2, kCodecSparse = 3 };
+enum Mode { kModeAllreduce = 0, kModeReduceScatter = 1 };
+
+// Arguments of the fused ring kernel (reduce-scatter pass, owner finalise,
+// allgather pass).  Passed by value as a __grid_constant__ parameter.
+struct RingArgs {
+    int N;          // simulated ranks
+    int mode;       // kModeAllreduce / kModeReduceScatter
+    int in_t;       // dtype of the inputs
+    int out_t;      // dtype of the outputs
+    int K;          // mailbox depth (messages in flight per ring edge)
+    int D;          // input staging depth per rank (fast path)
+    int slot_bytes; // bytes of one mailbox slot
+    int stage_bytes;
+    int average;       // divide the reduced value by N
+    int has_prev;      // difference encoding: inputs are cur, prev[] given
+    int withhold_rank; // fault injection (-1: off)
+    int withhold_step;
+    int vec_out;       // outputs allow 16-byte vector stores
+    int vec_base;      // diff_base allows 16-byte vector loads
+    long long T;       // elements per rank
+    long long n;       // chunk length ceil(T/N)
+    long long tiles;   // slices per chunk ceil(n / 256)
+    double one_minus_thr; // sparse: a slice is sparse iff nnz < one_minus_thr * len
+    unsigned long long timeout_ns;
+    unsigned long long *sent; // [N] device counters of this call
+    unsigned long long *recv; // [N]
+    unsigned long long *zero; // [2N] counters of the next call: block 0 clears them
+    unsigned *status;         // device status word
+    const float *base;        // diff_base or nullptr
+    const void *in[kMaxRanks];
+    const float *prev[kMaxRanks];
+    void *out[kMaxRanks];
+};
+
+// Arguments of the copy collectives (allgather, broadcast) and the tree.
+struct CopyArgs {
+    int N;
+    int es;    // element size in bytes (2 or 4)
+    int root;  // broadcast root
+    int K;
+    int D;
+    int slot_bytes;
+    int stage_bytes;
+    int withhold_rank;
+    int withhold_step;
+    long long T;
+    long long n;     // allgather chunk length
+    long long tiles; // slices per launch item range
+    unsigned long long timeout_ns;
+    unsigned long long *sent;
+    unsigned long long *recv;
+    unsigned long long *zero;
+    unsigned *status;
+    void *buf[kMaxRanks];
+};
+
+// Shared-memory layout of the ring / copy kernels (host and device agree).
+struct Layout {
+    int full, empty, stage_bar, rank_state, slots, stages, scratch, total;
+};
+
+__host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline Layout make_layout(int N, int K, int D, int slot_bytes,
+                                              int stage_bytes, int warps, bool fast,
+                                              bool sparse)
+{
+    Layout L;
+    int off = 0;
+    L.full = off;
+    off += N * K * 8;
+    L.empty = off;
+    off += N * K * 8;
+    L.stage_bar = off;
+    off += fast ? N * D * 8 : 0;
+    L.rank_state = off; // per rank: next staged load to issue, loads consumed, sent, recv
+    off += N * 32;
+    off = align_up(off, 128);
+    L.slots = off;
+    off += N * K * slot_bytes;
+    off = align_up(off, 128);
+    L.stages = off;
+    off += fast ? N * D * stage_bytes : 0;
+    off = align_up(off, 16);
+    L.scratch = off;
+    off += sparse ? warps * (256 * 4 + 256) : 0;
+    L.total = align_up(off, 128);
+    return L;
+}
+
+// Kernel entry points (one per translation unit family).  Each returns the
+// launch's cudaError_t.
+cudaError_t launch_ring(int codec, int in_t, bool fast, const RingArgs &a, int grid,
+                        int warps, int smem, cudaStream_t st);
+cudaError_t ring_kernel_attrs(int codec, int in_t, bool fast, int smem, int warps,
+                              int *blocks_per_sm);
+
+cudaError_t launch_allgather(bool fast, const CopyArgs &a, int grid, int warps, int smem,
+                             cudaStream_t st);
+cudaError_t launch_broadcast(bool fast, const CopyArgs &a, int grid, int warps, int smem,
+                             cudaStream_t st);
+cudaError_t launch_tree(bool fast, const CopyArgs &a, int grid, int warps, int smem,
+                        cudaStream_t st);
+cudaError_t copy_kernel_attrs(int which, bool fast, int smem, int warps, int *blocks_per_sm);
+
+// Standalone codec kernels.
+cudaError_t launch_bfp_encode(const void *x, long long n, int dtype, int bits, int8_t *exps,
+                              uint8_t *mants, cudaStream_t st);
+cudaError_t launch_bfp_decode(const int8_t *exps, const uint8_t *mants, long long n, int bits,
+                              float *out, int accumulate, cudaStream_t st);
+cudaError_t launch_sparse_encode(const void *x, long long n, int dtype, double one_minus_thr,
+                                 uint32_t *hdr, void *vals, int32_t *idx, uint32_t *scratch,
+                                 cudaStream_t st);
+long long sparse_encode_scratch_words(long long n);
+cudaError_t launch_sparse_decode(const uint32_t *hdr, const void *vals, const int32_t *idx,
+                                 long long n, int dtype, float *acc, int accumulate,
+                                 cudaStream_t st);
+cudaError_t launch_diff_encode(const float *cur, const float *prev, float *diff, long long n,
+                               cudaStream_t st);
+
+int num_sms();
+
+} // namespace rra

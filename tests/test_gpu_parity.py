@@ -1,0 +1,432 @@
+"""GPU parity: every op and codec of the CUDA path, called through the C ABI
+(Python binding), against the CPU oracle on the same seeded inputs.
+
+The bar is bit-exactness everywhere: lossless sums follow the ring's fixed
+order, the codecs round to nearest even exactly as the oracle does, byte
+counters are exact.  Sizes span several 256-element slices, ragged tails,
+chunk counts that do not divide T, the N=1 and N=2 special cases, both the
+bulk-copy fast path (16-byte aligned buffers and chunk sizes) and the generic
+path, and N up to the 64-rank maximum."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import ring_allreduce_compressed_gb300 as rra
+import workloads as W
+from gpu_util import (TORCH_DT, assert_bits_equal, cast, host, rand_f32)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    rra.build()
+    rra.lib()
+    torch.cuda.init()
+
+
+def run_ring(xs, out_dt, codec=None, mode="allreduce", outs=None):
+    N = len(xs)
+    comm = rra.Comm(N, xs[0].numel(), xs[0].dtype)
+    if outs is None:
+        outs = [torch.zeros(xs[0].numel(), dtype=TORCH_DT[out_dt], device="cuda") for _ in range(N)]
+    if mode == "allreduce":
+        comm.ring_allreduce(xs, outs, codec)
+    else:
+        comm.reduce_scatter(xs, outs, codec)
+    sent, recv = comm.get_bytes()
+    assert comm.status() == rra.RRA_OK
+    comm.close()
+    return outs, np.array(sent, np.uint64), np.array(recv, np.uint64)
+
+
+def oracle_ring(xs, in_dt, out_dt, mode="allreduce", **kw):
+    outs = None
+    if mode == "reduce_scatter":
+        outs = [np.zeros(xs[0].numel(), O.NP_DTYPES[out_dt]) for _ in xs]
+    return O.ring([host(x) for x in xs], in_dt, out_dt, mode=mode, outputs=outs, **kw)
+
+
+def compare(gpu, ref, what):
+    g_outs, g_sent, g_recv = gpu
+    r_outs, r_sent, r_recv = ref
+    for r, (g, w) in enumerate(zip(g_outs, r_outs)):
+        assert_bits_equal(host(g), w, f"{what} rank {r}")
+    assert list(g_sent) == list(r_sent), (what, g_sent, r_sent)
+    assert list(g_recv) == list(r_recv), (what, g_recv, r_recv)
+
+
+# ------------------------------------------------------------------ lossless
+
+def test_config1_lossless_all_ops():
+    """N=4, T=4096 fp32, N(0,1) seed 0: ring allreduce, reduce-scatter,
+    allgather, broadcast from rank 0 and the tree, bit-exact, with the
+    closed-form byte counter 2T(N-1)/N * 4 = 24,576 B per rank."""
+    xs = W.lossless(4, 4096, seed=0)
+    gpu = run_ring(xs, "f32")
+    ref = oracle_ring(xs, "f32", "f32")
+    compare(gpu, ref, "ring")
+    assert list(gpu[1]) == [24576] * 4
+    for r in range(1, 4):
+        assert torch.equal(gpu[0][r], gpu[0][0])
+
+    rs_out = [torch.full((4096,), 7.0, device="cuda") for _ in range(4)]
+    gpu = run_ring(xs, "f32", mode="reduce_scatter", outs=rs_out)
+    rs_ref_out = [np.full(4096, 7.0, np.float32) for _ in range(4)]
+    ref = O.ring([host(x) for x in xs], mode="reduce_scatter", outputs=rs_ref_out)
+    compare(gpu, ref, "reduce_scatter")
+
+    comm = rra.Comm(4, 4096)
+    bufs = [x.clone() for x in xs]
+    comm.allgather(bufs)
+    ref_bufs, s, r = O.allgather([host(x) for x in xs])
+    for q in range(4):
+        assert_bits_equal(host(bufs[q]), ref_bufs[q], f"allgather {q}")
+    assert comm.get_bytes() == (list(s), list(r))
+
+    bufs = [x.clone() for x in xs]
+    comm.broadcast(bufs, root=0)
+    ref_bufs, s, r = O.broadcast([host(x) for x in xs], "f32", 0)
+    for q in range(4):
+        assert_bits_equal(host(bufs[q]), ref_bufs[q], f"broadcast {q}")
+    assert comm.get_bytes() == (list(s), list(r))
+
+    bufs = [x.clone() for x in xs]
+    comm.tree_allreduce(bufs)
+    ref_bufs, s, r = O.tree_allreduce([host(x) for x in xs])
+    for q in range(4):
+        assert_bits_equal(host(bufs[q]), ref_bufs[q], f"tree {q}")
+    assert comm.get_bytes() == (list(s), list(r))
+    assert comm.status() == rra.RRA_OK
+    comm.close()
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 8, 16, 17, 33, 64])
+@pytest.mark.parametrize("T", [1, 100, 256, 1000, 4096, 70001])
+def test_lossless_ring_shapes(N, T):
+    xs = rand_f32(N, T, seed=N * 7919 + T)
+    compare(run_ring(xs, "f32"), oracle_ring(xs, "f32", "f32"), f"N={N} T={T}")
+
+
+@pytest.mark.parametrize("in_dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("out_dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("T", [4096 * 3, 5003])
+def test_lossless_dtypes(in_dt, out_dt, T):
+    xs = cast(rand_f32(4, T, seed=11), in_dt)
+    compare(run_ring(xs, out_dt), oracle_ring(xs, in_dt, out_dt), f"{in_dt}->{out_dt}")
+
+
+def test_lossless_misaligned_buffers_take_generic_path():
+    """Views starting 4 bytes into their storage are not 16-byte aligned: the
+    generic (element-wise) path must give the same bits."""
+    N, T = 4, 8192
+    base = rand_f32(N, T + 1, seed=12)
+    xs = [b[1:] for b in base]
+    outs_store = [torch.zeros(T + 1, device="cuda") for _ in range(N)]
+    outs = [o[1:] for o in outs_store]
+    comm = rra.Comm(N, T)
+    comm.ring_allreduce(xs, outs)
+    ref = O.ring([host(x) for x in xs])
+    for r in range(N):
+        assert_bits_equal(host(outs[r]), ref[0][r], f"rank {r}")
+    comm.close()
+
+
+def test_in_place_allreduce():
+    N, T = 8, 65536
+    xs = rand_f32(N, T, seed=13)
+    ref = O.ring([host(x) for x in xs])
+    comm = rra.Comm(N, T)
+    comm.ring_allreduce(xs, xs)
+    for r in range(N):
+        assert_bits_equal(host(xs[r]), ref[0][r], f"rank {r}")
+    comm.close()
+
+
+# ------------------------------------------------------------------ block floating point
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("in_dt", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("N,T", [(2, 512), (3, 1000), (8, 8 * 4096), (8, 40017), (5, 256 * 5 * 3 + 70)])
+def test_bfp_ring(bits, in_dt, N, T):
+    xs = cast(rand_f32(N, T, seed=bits * 100 + N + T, scale=1e-3), in_dt)
+    out_dt = "f16" if in_dt == "f16" else "f32"
+    codec = rra.Codec("bfp", bits=bits)
+    gpu = run_ring(xs, out_dt, codec)
+    ref = oracle_ring(xs, in_dt, out_dt, codec="bfp", bits=bits)
+    compare(gpu, ref, f"bfp{bits} {in_dt}")
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_bfp_ring_degenerate_blocks(bits):
+    """All-zero blocks, subnormal maxima, huge and tiny magnitudes in the same
+    slice, values that round to the clamp: exponents from the bits, clamp at
+    -126, codes clamped to +-(2^(bits-1)-1)."""
+    N, T = 4, 4 * 1024
+    g = torch.Generator(device="cuda")
+    g.manual_seed(99)
+    xs = []
+    for r in range(N):
+        x = torch.randn(T, generator=g, device="cuda")
+        x[:128] = 0.0
+        x[128:256] = torch.randn(128, generator=g, device="cuda") * 1e-39  # subnormal
+        x[256:384] *= 1e30
+        x[384:512] = 1.9921875 * (1 if r % 2 else -1)
+        x[512:640] *= 1e-30
+        xs.append(x)
+    codec = rra.Codec("bfp", bits=bits)
+    compare(run_ring(xs, "f32", codec), oracle_ring(xs, "f32", "f32", codec="bfp", bits=bits),
+            "degenerate")
+
+
+def test_bfp8_config2_shape_small():
+    """The headline codec on a shrunken bucket: N=8, fp16 N(0,1e-3^2), fp16 out."""
+    xs = W.bfp_bucket(8, 8 * 2048 * 8, seed=1)
+    codec = rra.Codec("bfp", bits=8)
+    gpu = run_ring(xs, "f16", codec)
+    compare(gpu, oracle_ring(xs, "f16", "f16", codec="bfp", bits=8), "cfg2 small")
+    n = xs[0].numel() // 8
+    assert all(int(s) == 14 * (n // 128 + n) for s in gpu[1])
+
+
+# ------------------------------------------------------------------ sparse
+
+@pytest.mark.parametrize("thr", [0.5, 0.2, 0.9])
+@pytest.mark.parametrize("in_dt", ["bf16", "f32", "f16"])
+@pytest.mark.parametrize("N,T", [(2, 1000), (5, 256 * 5 * 4), (16, 16 * 3000 + 5)])
+def test_sparse_ring(thr, in_dt, N, T):
+    xs = W.sparse(N, T, seed=N + T, dtype=TORCH_DT[in_dt])
+    thr32 = float(np.float32(thr))
+    out_dt = "f32"
+    codec = rra.Codec("sparse", sparsity_threshold=thr)
+    gpu = run_ring(xs, out_dt, codec)
+    ref = oracle_ring(xs, in_dt, out_dt, codec="sparse", threshold=thr32)
+    compare(gpu, ref, f"sparse thr={thr}")
+    # lossless: equals the lossless ring bit for bit (no -0.0 in the inputs)
+    compare(run_ring(xs, out_dt), (ref[0], *oracle_ring(xs, in_dt, out_dt)[1:]), "vs lossless")
+
+
+def test_sparse_ring_all_zero_and_dense():
+    N, T = 4, 4096
+    zeros = [torch.zeros(T, device="cuda") for _ in range(N)]
+    codec = rra.Codec("sparse")
+    gpu = run_ring(zeros, "f32", codec)
+    compare(gpu, oracle_ring(zeros, "f32", "f32", codec="sparse"), "zeros")
+    assert all(int(s) == 2 * (N - 1) * (T // N // 256) * 8 for s in gpu[1])  # headers only
+    dense = rand_f32(N, T, seed=5)
+    compare(run_ring(dense, "f32", codec), oracle_ring(dense, "f32", "f32", codec="sparse"), "dense")
+
+
+# ------------------------------------------------------------------ diff / average / base
+
+@pytest.mark.parametrize("codec_kind,bits", [("bfp", 4), ("bfp", 8), ("none", 8), ("sparse", 8)])
+@pytest.mark.parametrize("N,T", [(8, 8 * 1000 + 8 * 64), (3, 3000)])
+def test_diff_average_base(codec_kind, bits, N, T):
+    cur, prev = W.diloco(N, T, seed=3)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    base = torch.randn(T, generator=g, device="cuda") * 1e-4
+    codec = rra.Codec(codec_kind, bits=bits, diff_prev=prev, diff_base=base, average=True)
+    gpu = run_ring(cur, "f32", codec)
+    ref = O.ring([host(c) for c in cur], codec=codec_kind, bits=bits,
+                 diff_prev=[host(p) for p in prev], diff_base=host(base), average=True)
+    compare(gpu, ref, f"diff {codec_kind}{bits}")
+
+
+def test_average_without_base():
+    xs = rand_f32(5, 5000, seed=21)
+    codec = rra.Codec("none", average=True)
+    compare(run_ring(xs, "f32", codec), O.ring([host(x) for x in xs], average=True), "avg")
+
+
+# ------------------------------------------------------------------ reduce-scatter
+
+@pytest.mark.parametrize("codec_kind,bits,in_dt", [("none", 8, "f32"), ("bfp", 8, "f16"),
+                                                   ("bfp", 4, "f32"), ("sparse", 8, "bf16")])
+@pytest.mark.parametrize("N,T", [(4, 4096), (7, 10007), (16, 16 * 512)])
+def test_reduce_scatter(codec_kind, bits, in_dt, N, T):
+    if codec_kind == "sparse":
+        xs = W.sparse(N, T, seed=N, dtype=TORCH_DT[in_dt])
+    else:
+        xs = cast(rand_f32(N, T, seed=N + T, scale=1e-3), in_dt)
+    outs = [torch.full((T,), 3.0, device="cuda") for _ in range(N)]
+    codec = rra.Codec(codec_kind, bits=bits)
+    gpu = run_ring(xs, "f32", codec, mode="reduce_scatter", outs=outs)
+    ref_outs = [np.full(T, 3.0, np.float32) for _ in range(N)]
+    ref = O.ring([host(x) for x in xs], in_dt, "f32", codec=codec_kind, bits=bits,
+                 mode="reduce_scatter", outputs=ref_outs)
+    compare(gpu, ref, f"rs {codec_kind}")
+
+
+# ------------------------------------------------------------------ allgather / broadcast / tree
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N,T", [(1, 10), (2, 1000), (4, 4096), (7, 7 * 300 + 3), (64, 64 * 256)])
+def test_allgather(dt, N, T):
+    bufs = cast(rand_f32(N, T, seed=N + T), dt)
+    ref, s, r = O.allgather([host(b) for b in bufs], dt)
+    comm = rra.Comm(N, T, bufs[0].dtype)
+    comm.allgather(bufs)
+    for q in range(N):
+        assert_bits_equal(host(bufs[q]), ref[q], f"allgather {q}")
+    assert comm.get_bytes() == (list(s), list(r))
+    comm.close()
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 8, 13, 64])
+@pytest.mark.parametrize("root", [0, 2])
+@pytest.mark.parametrize("T", [777, 8192])
+def test_broadcast(dt, N, root, T):
+    if root >= N:
+        pytest.skip("root outside the group")
+    bufs = cast(rand_f32(N, T, seed=N * 3 + root), dt)
+    ref, s, r = O.broadcast([host(b) for b in bufs], dt, root)
+    comm = rra.Comm(N, T, bufs[0].dtype)
+    comm.broadcast(bufs, root=root)
+    for q in range(N):
+        assert_bits_equal(host(bufs[q]), ref[q], f"broadcast {q}")
+    assert comm.get_bytes() == (list(s), list(r))
+    comm.close()
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 16, 33, 64])
+@pytest.mark.parametrize("T", [300, 8192])
+def test_tree_allreduce(N, T):
+    bufs = rand_f32(N, T, seed=N * 5 + T)
+    ref, s, r = O.tree_allreduce([host(b) for b in bufs])
+    comm = rra.Comm(N, T)
+    comm.tree_allreduce(bufs)
+    for q in range(N):
+        assert_bits_equal(host(bufs[q]), ref[q], f"tree {q}")
+    assert comm.get_bytes() == (list(s), list(r))
+    comm.close()
+
+
+# ------------------------------------------------------------------ standalone codecs
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("n", [1, 127, 128, 1000, 65536 + 77])
+def test_bfp_codec(bits, dt, n):
+    x = cast(rand_f32(1, n, seed=n + bits, scale=3e-2), dt)[0]
+    nb = -(-n // 128)
+    mb = n if bits == 8 else -(-n // 2)
+    exps = torch.zeros(nb, dtype=torch.int8, device="cuda")
+    mants = torch.zeros(mb, dtype=torch.uint8, device="cuda")
+    rra.bfp_encode(x, bits, exps, mants)
+    rx = O.to_f32(host(x), dt)
+    re, rm = O.bfp_encode(rx, bits)
+    assert np.array_equal(host(exps), re) and np.array_equal(host(mants), rm)
+    out = torch.full((n,), 0.5, device="cuda")
+    rra.bfp_decode(exps, mants, n, bits, out)
+    assert_bits_equal(host(out), O.bfp_decode(re, rm, n, bits), "decode")
+    rra.bfp_decode(exps, mants, n, bits, out, accumulate=True)
+    acc = O.bfp_decode(re, rm, n, bits)
+    O.bfp_decode(re, rm, n, bits, out=acc, accumulate=True)
+    assert_bits_equal(host(out), acc, "decode accumulate")
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("p_zero,thr", [(0.6, 0.5), (0.3, 0.5), (0.5, 0.5), (0.95, 0.9)])
+@pytest.mark.parametrize("n", [1, 1000, 4096 * 3 + 11, 300000])
+def test_sparse_codec(dt, p_zero, thr, n):
+    x = W.sparse(1, n, seed=n, p_zero=p_zero, dtype=TORCH_DT[dt])[0]
+    hdr = torch.zeros(2, dtype=torch.int32, device="cuda")
+    vals = torch.zeros(n, dtype=TORCH_DT[dt], device="cuda")
+    idx = torch.full((n,), -1, dtype=torch.int32, device="cuda")
+    rra.sparse_encode(x, thr, hdr, vals, idx)
+    rh, rv, ri = O.sparse_encode(host(x), dt, float(np.float32(thr)))
+    h = host(hdr).view(np.uint32)
+    assert list(h) == list(rh)
+    k = int(rh[1]) if rh[0] else n
+    assert np.array_equal(bitsof_any(host(vals)[:k]), bitsof_any(rv))
+    if rh[0]:
+        assert np.array_equal(host(idx)[:k], ri)
+    acc = torch.full((n,), 2.0, device="cuda")
+    rra.sparse_decode(hdr, vals, idx, n, acc)
+    assert_bits_equal(host(acc), O.sparse_decode(rh, rv, ri, n, dt), "decode")
+    rra.sparse_decode(hdr, vals, idx, n, acc, accumulate=True)
+    ra = O.sparse_decode(rh, rv, ri, n, dt)
+    O.sparse_decode(rh, rv, ri, n, dt, acc=ra, accumulate=True)
+    assert_bits_equal(host(acc), ra, "decode accumulate")
+
+
+def bitsof_any(a):
+    return a.view({4: np.uint32, 2: np.uint16}[a.dtype.itemsize])
+
+
+@pytest.mark.parametrize("n", [1, 7, 4096, 100003])
+def test_diff_codec(n):
+    cur, prev = W.diloco(1, n, seed=n)
+    d = torch.empty(n, device="cuda")
+    rra.diff_encode(cur[0], prev[0], d)
+    assert_bits_equal(host(d), O.diff_encode(host(cur[0]), host(prev[0])), "diff")
+
+
+# ------------------------------------------------------------------ failure detection, determinism
+
+@pytest.mark.parametrize("op", ["ring", "allgather", "broadcast", "tree"])
+def test_withheld_message_times_out(op):
+    """A simulated rank that never publishes one message: its receiver's
+    bounded wait runs out, the launch returns, the communicator reports
+    RRA_ERR_TIMEOUT, and the next call works again."""
+    N, T = 4, 4096
+    xs = rand_f32(N, T, seed=31)
+    comm = rra.Comm(N, T)
+    comm.set_timeout(20_000_000)  # 20 ms
+    # rank 1 sends at the first step of the ring, the allgather and the tree's
+    # first reduce level; in the broadcast only the root sends at level 0
+    comm.debug_withhold(0 if op == "broadcast" else 1, 1)
+    outs = [torch.zeros(T, device="cuda") for _ in range(N)]
+    bufs = [x.clone() for x in xs]
+    if op == "ring":
+        comm.ring_allreduce(xs, outs)
+    elif op == "allgather":
+        comm.allgather(bufs)
+    elif op == "broadcast":
+        comm.broadcast(bufs, root=0)
+    else:
+        comm.tree_allreduce(bufs)
+    assert comm.status() == rra.RRA_ERR_TIMEOUT
+    assert comm.status() == rra.RRA_OK  # reading clears it
+    comm.set_timeout(0)
+    comm.ring_allreduce(xs, outs)
+    assert comm.status() == rra.RRA_OK
+    ref = O.ring([host(x) for x in xs])
+    assert_bits_equal(host(outs[2]), ref[0][2], "after recovery")
+    comm.close()
+
+
+def test_repeat_runs_bit_identical():
+    N, T = 8, 8 * 4096 + 100
+    xs = cast(rand_f32(N, T, seed=41, scale=1e-3), "f16")
+    comm = rra.Comm(N, T, torch.float16)
+    codec = rra.Codec("bfp", bits=8)
+    first = None
+    for _ in range(10):
+        outs = [torch.empty(T, dtype=torch.float16, device="cuda") for _ in range(N)]
+        comm.ring_allreduce(xs, outs, codec)
+        cur = torch.stack(outs).cpu()
+        if first is None:
+            first = cur
+        assert torch.equal(cur.view(torch.int16), first.view(torch.int16))
+    comm.close()
+
+
+def test_argument_errors_are_reported_on_the_host():
+    comm = rra.Comm(4, 1000)
+    xs = rand_f32(4, 1000, seed=1)
+    with pytest.raises(rra.RRAError):
+        comm.ring_allreduce(xs, xs, rra.Codec("bfp", bits=5))
+    with pytest.raises(rra.RRAError):
+        comm.ring_allreduce(xs, [xs[0]] * 4)  # outputs overlap
+    big = rand_f32(4, 2000, seed=1)
+    with pytest.raises(rra.RRAError):
+        comm.ring_allreduce(big, big)  # count > max_count
+    with pytest.raises(rra.RRAError):
+        comm.broadcast(xs, root=4)
+    with pytest.raises(rra.RRAError):
+        comm.tree_allreduce(cast(xs, "f16"))
+    comm.close()
