@@ -175,71 +175,70 @@ def traffic_from_profile(config: str):
 # ---------------------------------------------------------------- workloads
 
 class Workload:
-    def __init__(self, name: str, device="cuda"):
-        import ring_allreduce_compressed_gb300 as rra
-        self.rra = rra
+    """One of the configurations, resident in HBM.  With use_lib=False (the
+    reference arm) only the inputs are drawn; the CUDA library is not used."""
+
+    def __init__(self, name: str, device="cuda", use_lib: bool = True):
+        rra = None
+        if use_lib:
+            import ring_allreduce_compressed_gb300 as rra
         self.name = name
         self.base = None
+        self.prev = None
+        self.codec = None
+        c = W.CONFIGS[name]
+        self.N, self.T = c["N"], c["T"]
         if name == "bfp8_bucket":
-            c = W.CONFIGS[name]
-            self.N, self.T = c["N"], c["T"]
             self.inputs = W.bfp_bucket(self.N, self.T, seed=c["seed"], device=device)
             self.out_dtype = torch.float16
-            self.codec = rra.Codec("bfp", bits=8)
             self.codec_name = "bfp8"
             self.desc = ("block-FP8 compressed ring allreduce of one 25 MiB fp16 DDP bucket: "
                          "N=8 simulated ranks x 13,107,200 fp16, N(0,1e-3^2) seed 1, "
                          "128-element blocks, fp32 accumulation, fp16 output")
         elif name == "lossless_n4":
-            c = W.CONFIGS[name]
-            self.N, self.T = c["N"], c["T"]
             self.inputs = W.lossless(self.N, self.T, seed=c["seed"], device=device)
             self.out_dtype = torch.float32
-            self.codec = None
             self.codec_name = "none"
             self.desc = "lossless fp32 ring allreduce, N=4 x 4096 fp32, N(0,1) seed 0"
         elif name == "sparse_n16":
-            c = W.CONFIGS[name]
-            self.N, self.T = c["N"], c["T"]
             self.inputs = W.sparse(self.N, self.T, seed=c["seed"], device=device)
             self.out_dtype = torch.float32
-            self.codec = rra.Codec("sparse", sparsity_threshold=0.5)
             self.codec_name = "sparse"
             self.desc = ("sparse-format ring allreduce: N=16 x 64 Mi bf16, zero w.p. 0.6 else "
                          "N(0,0.02^2), seed 2, threshold 0.5 per 256-element slice, fp32 out")
         elif name == "diloco_n8":
-            c = W.CONFIGS[name]
-            self.N, self.T = c["N"], c["T"]
-            cur, prev = W.diloco(self.N, self.T, seed=c["seed"], device=device)
-            self.inputs = cur
-            # previous round's result: lossless mean of prev (setup, untimed)
-            self.base = torch.empty(self.T, dtype=torch.float32, device=device)
-            comm = rra.Comm(self.N, self.T)
-            outs = [self.base] + [torch.empty(0, device=device)] * 0
-            tmp = [torch.empty(self.T, device=device) for _ in range(self.N - 1)]
-            comm.ring_allreduce(prev, [self.base] + tmp, rra.Codec("none", average=True))
-            torch.cuda.synchronize()
-            del tmp, outs
-            comm.close()
+            self.inputs, self.prev = W.diloco(self.N, self.T, seed=c["seed"], device=device)
             self.out_dtype = torch.float32
-            self.codec = rra.Codec("bfp", bits=4, diff_prev=prev, diff_base=self.base,
-                                   average=True)
-            self.prev = prev
             self.codec_name = "diff+bfp4"
             self.desc = ("DiLoCo outer-step pseudo-gradient: N=8 x 10^9 fp32 deltas, "
                          "difference against the previous round, block-FP4, averaged by 1/N, "
-                         "previous result added back; seed 3")
+                         "previous result (lossless mean of prev) added back; seed 3")
         else:
             raise ValueError(name)
         self.in_dtype = self.inputs[0].dtype
-        self.outputs = [torch.empty(self.T, dtype=self.out_dtype, device=device)
-                        for _ in range(self.N)]
-        self.comm = rra.Comm(self.N, self.T, self.in_dtype)
+        if use_lib:
+            self.comm = rra.Comm(self.N, self.T, self.in_dtype)
+            if name == "bfp8_bucket":
+                self.codec = rra.Codec("bfp", bits=8)
+            elif name == "sparse_n16":
+                self.codec = rra.Codec("sparse", sparsity_threshold=0.5)
+            elif name == "diloco_n8":
+                # previous round's result: lossless mean of prev (setup, untimed);
+                # reduce-scatter writes chunk r of each output, so one buffer holds it
+                self.base = torch.empty(self.T, dtype=torch.float32, device=device)
+                self.comm.reduce_scatter(self.prev, [self.base] * self.N,
+                                         rra.Codec("none", average=True))
+                torch.cuda.synchronize()
+                self.codec = rra.Codec("bfp", bits=4, diff_prev=self.prev, diff_base=self.base,
+                                       average=True)
+            self.outputs = [torch.empty(self.T, dtype=self.out_dtype, device=device)
+                            for _ in range(self.N)]
         ies = self.inputs[0].element_size()
-        oes = self.outputs[0].element_size()
+        oes = torch.empty(0, dtype=self.out_dtype).element_size()
         self.payload = self.T * ies  # per-rank logical payload (algbw numerator)
-        extra_in = self.T * 4 * self.N if self.base is not None else 0  # prev streams
-        base = self.T * 4 if self.base is not None else 0
+        diff = self.prev is not None
+        extra_in = self.T * 4 * self.N if diff else 0  # the prev streams
+        base = self.T * 4 if diff else 0
         self.compulsory = self.N * self.T * (ies + oes) + extra_in + base
 
     def step(self, stream=None):
@@ -292,7 +291,7 @@ def cpu_baseline(wl: Workload, budget_s: float = 20.0):
     n = wl.T // wl.N
     hosts = [host_copy(x) for x in wl.inputs]
     extra = None
-    if wl.base is not None:
+    if wl.prev is not None:
         extra = ([host_copy(p) for p in wl.prev], host_copy(wl.base))
     # calibrate on a small sample, then size the measured one
     s0 = max(1, min(n // 256, 16))
@@ -427,12 +426,21 @@ def run_reference(args, world, rank):
     """The oracle timed on the host cores, one bounded sample per step."""
     if rank != 0:
         return
-    wl = Workload(args.config)
+    wl = Workload(args.config, use_lib=False)
     n = wl.T // wl.N
     hosts = [host_copy(x) for x in wl.inputs]
     extra = None
-    if wl.base is not None:
-        extra = ([host_copy(p) for p in wl.prev], host_copy(wl.base))
+    if wl.prev is not None:
+        import oracle as O
+        prev_h = [host_copy(p) for p in wl.prev]
+        # the previous result is the lossless mean of prev; the oracle computes
+        # it on the positions the samples use (the first slices of each chunk)
+        m = min(n, 1 << 20)
+        idx = np.concatenate([np.arange(c * n, c * n + m) for c in range(wl.N)])
+        mean = O.ring([np.ascontiguousarray(p[idx]) for p in prev_h], average=True)[0][0]
+        base = np.zeros(wl.T, np.float32)
+        base[idx] = mean
+        extra = (prev_h, base)
     s0 = max(1, min(n // 256, 4))
     dt0, _ = oracle_sample_ring(hosts, wl.N, wl.T, wl.codec_name, s0, DT_NAME[wl.in_dtype],
                                 DT_NAME[wl.out_dtype], extra)
@@ -464,6 +472,90 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- ring vs tree sweep
+
+def run_sweep(args, world, rank):
+    """Lossless fp32 ring vs tree allreduce over T = 256 * 4^k elements
+    (1 KiB .. 1 GiB per rank) and N in {2, 4, 8, 16, 64}, in place, values
+    U(-1,1) from seed 4 (re-seeded per case).  One JSON line per (N, T, op)
+    and a summary line per N with the measured crossover and the alpha-beta
+    link model fed by the byte counters."""
+    import ring_allreduce_compressed_gb300 as rra
+    rra.build()
+    Ns = [int(x) for x in args.sweep_n.split(",")]
+    Ts = [256 * 4 ** k for k in range(args.sweep_kmax + 1)]
+    alpha_us, beta_gbs = args.alpha_us, args.beta_gbs
+    peak, _ = hbm_peak()
+    out = []
+    for N in Ns:
+        rows = []
+        for case, T in enumerate(Ts):
+            free, _ = torch.cuda.mem_get_info()
+            if N * T * 4 * 1.1 + 2 ** 30 > free:
+                continue
+            bufs = W.uniform(N, T, seed=4 + case)
+            comm = rra.Comm(N, T)
+            res = {}
+            for op in ("ring", "tree"):
+                fn = (lambda: comm.ring_allreduce(bufs, bufs)) if op == "ring" else \
+                    (lambda: comm.tree_allreduce(bufs))
+                for _ in range(5):
+                    fn()
+                torch.cuda.synchronize()
+                reps = 20 if N * T * 4 < 2 ** 33 else 5
+                times = []
+                for _ in range(reps):
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    fn()
+                    b.record()
+                    b.synchronize()
+                    times.append(a.elapsed_time(b) * 1e3)
+                sent, recv = comm.get_bytes()
+                assert comm.status() == rra.RRA_OK
+                us = statistics.median(times)
+                res[op] = us
+                line = {"sweep": True, "op": op, "N": N, "T": T, "bytes_per_rank": T * 4,
+                        "us": us, "algbw_gbs": T * 4 / (us * 1e-6) / 1e9,
+                        "busbw_gbs": (T * 4 / (us * 1e-6) / 1e9) * (2 * (N - 1) / N
+                                                                      if op == "ring" else 1),
+                        "hbm_frac": 8 * N * T / (us * 1e-6) / 1e9 / peak,
+                        "sent_max": max(sent), "recv_max": max(recv), "reps": reps}
+                out.append(line)
+                if rank == 0:
+                    print(json.dumps(line), flush=True)
+            comm.close()
+            del bufs
+            torch.cuda.empty_cache()
+            rows.append((T, res["ring"], res["tree"]))
+        cross = None
+        for T, r_us, t_us in rows:
+            if r_us < t_us:
+                cross = T * 4
+                break
+        L = 0
+        while (1 << L) < N:
+            L += 1
+        beta = 1.0 / (beta_gbs * 1e9)  # seconds per byte
+        model = None
+        denom = 4 * beta * (L - (N - 1) / N)
+        if N > 2 and denom > 0:
+            model = (N - 1 - L) * alpha_us * 1e-6 / denom * 4  # bytes per rank
+        summ = {"sweep_summary": True, "N": N,
+                "measured_crossover_bytes": cross if cross is not None else "none in range",
+                "model": {"alpha_us": alpha_us, "beta_GBps": beta_gbs,
+                          "ring_s": "2(N-1)(alpha + beta*4T/N)", "tree_s": "2L(alpha + beta*4T)",
+                          "crossover_bytes_per_rank": model}}
+        if rank == 0:
+            print(json.dumps(summ), flush=True)
+        out.append(summ)
+    if args.jsonl and rank == 0:
+        with open(args.jsonl, "a") as f:
+            for line in out:
+                f.write(json.dumps(line) + "\n")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -476,11 +568,21 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=60.0)
     ap.add_argument("--jsonl", default=None)
+    ap.add_argument("--sweep", action="store_true",
+                    help="ring vs tree message-size sweep (lossless fp32) instead of one line")
+    ap.add_argument("--sweep-n", default="2,4,8,16,64")
+    ap.add_argument("--sweep-kmax", type=int, default=10)
+    ap.add_argument("--alpha-us", type=float, default=5.0,
+                    help="link latency of the alpha-beta model (microseconds)")
+    ap.add_argument("--beta-gbs", type=float, default=5.625,
+                    help="link bandwidth of the model, GB/s (45 Gbit/s)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_setup()
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args, world, rank)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_rra(args, world, rank, local)

@@ -288,6 +288,20 @@ rra_status rra_comm_status(rra_comm *comm);
  * a stuck rank raises a deadline error instead of hanging). */
 rra_status rra_set_timeout(rra_comm *comm, uint64_t ns);
 
+/*
+ * Launch tuning of the fused kernels (the in-kernel pipeline that replaces
+ * the pages' "chunk size" knob, CCCL §3.3: automatic by default, manual
+ * override allowed).  Each value 0 = automatic.
+ *  blocks_per_sm  resident blocks per SM to launch (1..32; clamped to what
+ *                 the occupancy calculator allows).
+ *  mailbox_depth  messages in flight per ring edge (1..8).
+ *  stage_depth    input slices each rank stages ahead with bulk copies (1..16).
+ * Depths that do not fit the shared memory are reduced automatically.
+ * Errors: RRA_ERR_INVALID for NULL or values out of range.
+ */
+rra_status rra_comm_set_tuning(rra_comm *comm, int blocks_per_sm, int mailbox_depth,
+                               int stage_depth);
+
 /* Test-only fault injection: in the next collective call, simulated rank
  * "rank" does not publish the message it sends at ring step "step" (1-based,
  * counted over both passes) for the first slice each block handles, so its

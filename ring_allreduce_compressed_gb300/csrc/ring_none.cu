@@ -1,22 +1,34 @@
 // ring_none.cu -- instantiations of the fused ring kernel for the
-// kCodecNone wire format(s); compiled as its own translation unit so
-// that the library builds in parallel.
+// kCodecNone wire format(s), every input dtype, the bulk-copy and the
+// generic input path, and the supported slice widths; its own translation unit
+// so that the library compiles in parallel.
 #include "ring_kernel.cuh"
 
 namespace rra {
 
-const void *ring_fn_none(int codec, int in_t, bool fast)
+const void *ring_fn_none(int codec, int in_t, bool fast, int groups)
 {
-    if (codec == kCodecNone) {
+    if (codec == kCodecNone && groups == 1) {
         if (in_t == kF32)
-            return fast ? (const void *)ring_kernel<kCodecNone, kF32, true>
-                        : (const void *)ring_kernel<kCodecNone, kF32, false>;
+            return fast ? (const void *)ring_kernel<kCodecNone, kF32, true, 1>
+                        : (const void *)ring_kernel<kCodecNone, kF32, false, 1>;
         if (in_t == kF16)
-            return fast ? (const void *)ring_kernel<kCodecNone, kF16, true>
-                        : (const void *)ring_kernel<kCodecNone, kF16, false>;
+            return fast ? (const void *)ring_kernel<kCodecNone, kF16, true, 1>
+                        : (const void *)ring_kernel<kCodecNone, kF16, false, 1>;
         if (in_t == kBF16)
-            return fast ? (const void *)ring_kernel<kCodecNone, kBF16, true>
-                        : (const void *)ring_kernel<kCodecNone, kBF16, false>;
+            return fast ? (const void *)ring_kernel<kCodecNone, kBF16, true, 1>
+                        : (const void *)ring_kernel<kCodecNone, kBF16, false, 1>;
+    }
+    if (codec == kCodecNone && groups == 2) {
+        if (in_t == kF32)
+            return fast ? (const void *)ring_kernel<kCodecNone, kF32, true, 2>
+                        : (const void *)ring_kernel<kCodecNone, kF32, false, 2>;
+        if (in_t == kF16)
+            return fast ? (const void *)ring_kernel<kCodecNone, kF16, true, 2>
+                        : (const void *)ring_kernel<kCodecNone, kF16, false, 2>;
+        if (in_t == kBF16)
+            return fast ? (const void *)ring_kernel<kCodecNone, kBF16, true, 2>
+                        : (const void *)ring_kernel<kCodecNone, kBF16, false, 2>;
     }
     return nullptr;
 }

@@ -60,15 +60,27 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t tx
                  : "memory");
 }
 
+#ifndef RRA_WAIT_HINT_NS
+#define RRA_WAIT_HINT_NS 0
+#endif
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
+#if RRA_WAIT_HINT_NS > 0
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity), "r"((uint32_t)RRA_WAIT_HINT_NS)
+                 : "memory");
+#else
     asm volatile("{\n\t.reg .pred p;\n\t"
                  "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
                  : "r"(smem_u32(bar)), "r"(parity)
                  : "memory");
+#endif
     return ok != 0;
 }
 
@@ -92,10 +104,15 @@ __device__ __forceinline__ uint64_t global_ns()
 }
 
 // Warp-uniform bounded wait for the phase of parity "parity" of an mbarrier.
-// Every lane waits (each gets acquire ordering).  Gives up when the time
-// limit passes or when another warp has already latched an error in *status;
-// on a time-out it latches kStTimeout.  Returns true iff every lane saw the
-// phase complete.
+// Every lane waits (each gets acquire ordering).  The common case -- the
+// neighbour publishes within microseconds -- touches nothing but the
+// mbarrier: the clock is read every 256 polls, and the device status word
+// (an error latched by another warp) only once the wait has lasted more than
+// kPollAfterNs, so no global-memory round trip sits on the critical path.
+// Gives up at the time limit (latching kStTimeout) or when another warp has
+// latched an error.  Returns true iff every lane saw the phase complete.
+constexpr uint64_t kPollAfterNs = 20000;
+
 __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
                                            unsigned *status)
 {
@@ -107,10 +124,11 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, uint6
                 ok = true;
                 break;
             }
-            if ((it & 15u) == 0u) {
-                if (*reinterpret_cast<volatile unsigned *>(status) != 0u)
+            if ((it & 255u) == 0u) {
+                const uint64_t dt = global_ns() - t0;
+                if (dt > kPollAfterNs && *reinterpret_cast<volatile unsigned *>(status) != 0u)
                     break;
-                if (global_ns() - t0 > limit_ns) {
+                if (dt > limit_ns) {
                     atomicCAS(status, 0u, (unsigned)kStTimeout);
                     break;
                 }
@@ -191,23 +209,26 @@ __device__ __forceinline__ void store8(void *base, int out_t, const float v[8], 
                     p[i] = v[i];
         }
     } else {
-        uint16_t h[8];
+        // pairs of values packed by one conversion each (round to nearest even)
+        uint32_t h[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            h[i] = f32_to_16(v[i], out_t);
+        for (int i = 0; i < 4; ++i) {
+            if (out_t == kF16) {
+                const __half2 p = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+                h[i] = *reinterpret_cast<const uint32_t *>(&p);
+            } else {
+                const __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                h[i] = *reinterpret_cast<const uint32_t *>(&p);
+            }
+        }
         uint16_t *p = reinterpret_cast<uint16_t *>(base);
         if (vec && valid >= 8) {
-            uint4 u;
-            u.x = h[0] | ((uint32_t)h[1] << 16);
-            u.y = h[2] | ((uint32_t)h[3] << 16);
-            u.z = h[4] | ((uint32_t)h[5] << 16);
-            u.w = h[6] | ((uint32_t)h[7] << 16);
-            *reinterpret_cast<uint4 *>(p) = u;
+            *reinterpret_cast<uint4 *>(p) = make_uint4(h[0], h[1], h[2], h[3]);
         } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 if (i < valid)
-                    p[i] = h[i];
+                    p[i] = (uint16_t)(h[i / 2] >> (16 * (i % 2)));
         }
     }
 }

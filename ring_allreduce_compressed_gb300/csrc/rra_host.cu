@@ -15,9 +15,9 @@
 #include "rra_kernels.h"
 
 namespace rra {
-const void *ring_fn_none(int codec, int in_t, bool fast);
-const void *ring_fn_bfp(int codec, int in_t, bool fast);
-const void *ring_fn_sparse(int codec, int in_t, bool fast);
+const void *ring_fn_none(int codec, int in_t, bool fast, int groups);
+const void *ring_fn_bfp(int codec, int in_t, bool fast, int groups);
+const void *ring_fn_sparse(int codec, int in_t, bool fast, int groups);
 } // namespace rra
 
 using namespace rra;
@@ -36,6 +36,9 @@ struct rra_comm {
     cudaStream_t last_stream = nullptr;
     bool have_last = false;
     int smem_optin = 0;
+    int tune_blocks = 0; // 0: automatic
+    int tune_K = 0;
+    int tune_D = 0;
     std::map<long long, int> occ; // (kernel key, smem) -> blocks per SM
 };
 
@@ -49,6 +52,8 @@ bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlap(const void *a, size_t abytes, const void *b, size_t bbytes)
 {
+    if (abytes == 0 || bbytes == 0)
+        return false;
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + bbytes && y < x + abytes;
 }
@@ -83,15 +88,16 @@ void note_call(rra_comm *c, cudaStream_t st)
 
 int warps_for(int N) { return std::min(N, kMaxWarps); }
 
-// Mailbox depth and staging depth that fit the opt-in shared memory.
+// Mailbox depth and staging depth that fit the opt-in shared memory: the
+// requested (or default) depths first, then smaller ones.
 bool pick_depths(rra_comm *c, int N, int slot_bytes, int stage_bytes, int warps, bool fast,
                  bool sparse, int extra, int *K, int *D, int *smem)
 {
-    const int Ks[] = {2, 1};
-    const int Ds[] = {4, 3, 2, 1};
-    for (int k : Ks)
-        for (int d : Ds) {
-            if (!fast && d != Ds[0])
+    const int k0 = c->tune_K ? c->tune_K : 2;
+    const int d0 = c->tune_D ? c->tune_D : 4;
+    for (int k = k0; k >= 1; --k)
+        for (int d = d0; d >= 1; --d) {
+            if (!fast && d != d0)
                 continue;
             const Layout L = make_layout(N, k, fast ? d : 1, slot_bytes, stage_bytes, warps, fast,
                                          sparse);
@@ -120,27 +126,30 @@ int grid_for(rra_comm *c, long long key, const void *fn, int warps, int smem, lo
             occ = 1;
         c->occ[k] = occ;
     }
+    if (c->tune_blocks)
+        occ = std::min(occ, c->tune_blocks);
     long long g = (long long)num_sms() * occ;
     if (items < g)
         g = items;
     return (int)std::max(1LL, g);
 }
 
-const void *ring_fn(int codec, int in_t, bool fast)
+const void *ring_fn(int codec, int in_t, bool fast, int groups)
 {
     if (codec == kCodecNone)
-        return ring_fn_none(codec, in_t, fast);
+        return ring_fn_none(codec, in_t, fast, groups);
     if (codec == kCodecSparse)
-        return ring_fn_sparse(codec, in_t, fast);
-    return ring_fn_bfp(codec, in_t, fast);
+        return ring_fn_sparse(codec, in_t, fast, groups);
+    return ring_fn_bfp(codec, in_t, fast, groups);
 }
 
-int slot_bytes_for(int codec)
+// Bytes of one mailbox slot for a slice of 256 * groups elements.
+int slot_bytes_for(int codec, int groups)
 {
     switch (codec) {
-    case kCodecNone: return kTile * 4;
-    case kCodecBfp8: return 16 + kTile;
-    case kCodecBfp4: return 16 + kTile / 2;
+    case kCodecNone: return kTile * 4 * groups;
+    case kCodecBfp8: return 16 + kTile * groups;
+    case kCodecBfp4: return 16 + kTile / 2 * groups;
     default: return 16 + kTile * 8;
     }
 }
@@ -179,17 +188,37 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     }
     if (cd.diff_prev && in_t != RRA_F32)
         return RRA_ERR_INVALID;
-    const size_t ib = count * esize(in_t), ob = count * esize(out_t);
+    // Region of out[r] the call writes: all of it for the allreduce, chunk r
+    // alone for the reduce-scatter (so its outputs may share one buffer).
+    const size_t oes = esize(out_t);
+    const size_t nchunk = (count + N - 1) / N;
+    auto region = [&](int r, const char **p, size_t *bytes) {
+        const char *b = static_cast<const char *>(out[r]);
+        if (mode == kModeAllreduce) {
+            *p = b;
+            *bytes = count * oes;
+            return;
+        }
+        size_t lo = std::min(count, (size_t)r * nchunk), hi = std::min(count, lo + nchunk);
+        *p = b + lo * oes;
+        *bytes = (hi - lo) * oes;
+    };
     for (int r = 0; r < N; ++r) {
         if (!in[r] || !out[r] || (cd.diff_prev && !cd.diff_prev[r]))
             return RRA_ERR_INVALID;
-        if (cd.diff_base && overlap(out[r], ob, cd.diff_base, count * 4))
+        const char *pr;
+        size_t br;
+        region(r, &pr, &br);
+        if (cd.diff_base && overlap(pr, br, cd.diff_base, count * 4))
             return RRA_ERR_INVALID;
-        for (int q = 0; q < r; ++q)
-            if (overlap(out[r], ob, out[q], ob))
+        for (int q = 0; q < r; ++q) {
+            const char *pq;
+            size_t bq;
+            region(q, &pq, &bq);
+            if (overlap(pr, br, pq, bq))
                 return RRA_ERR_INVALID;
+        }
     }
-    (void)ib;
 
     RingArgs a;
     std::memset(&a, 0, sizeof a);
@@ -209,7 +238,7 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     a.withhold_rank = comm->withhold_rank;
     a.withhold_step = comm->withhold_step;
 
-    const size_t ies = esize(in_t), oes = esize(out_t);
+    const size_t ies = esize(in_t);
     bool fast = (a.n * ies) % 16 == 0 && (a.T * ies) % 16 == 0;
     bool vec_out = (a.n * oes) % 16 == 0;
     for (int r = 0; r < N; ++r) {
@@ -223,26 +252,36 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     a.vec_base = (cd.diff_base && al16(cd.diff_base) && (a.n * 4) % 16 == 0) ? 1 : 0;
 
     const int warps = warps_for(N);
-    a.slot_bytes = slot_bytes_for(kc);
-    a.stage_bytes = kTile * (int)ies * (cd.diff_prev ? 2 : 1);
-    if (cd.diff_prev)
-        a.stage_bytes = kTile * 4 * 2;
-    int smem = 0;
-    if (!pick_depths(comm, N, a.slot_bytes, a.stage_bytes, warps, fast, kc == kCodecSparse, 0,
-                     &a.K, &a.D, &smem)) {
+    // Slice width: two groups of 8 elements per lane (512 per step) where the
+    // shared memory allows it, else one; the sparse codec's message slice is
+    // always 256 elements.
+    int groups = 0, smem = 0;
+    for (int gsel = (kc == kCodecSparse ? 1 : 2); gsel >= 1 && !groups; --gsel) {
+        a.slot_bytes = slot_bytes_for(kc, gsel);
+        a.stage_bytes = kTile * gsel * (cd.diff_prev ? 8 : (int)ies);
+        if (pick_depths(comm, N, a.slot_bytes, a.stage_bytes, warps, fast, kc == kCodecSparse, 0,
+                        &a.K, &a.D, &smem) &&
+            (gsel == 1 || a.D >= 2))
+            groups = gsel;
+    }
+    if (!groups) {
         fast = false;
+        groups = 1;
+        a.slot_bytes = slot_bytes_for(kc, 1);
+        a.stage_bytes = kTile * (cd.diff_prev ? 8 : (int)ies);
         if (!pick_depths(comm, N, a.slot_bytes, a.stage_bytes, warps, false, kc == kCodecSparse, 0,
                          &a.K, &a.D, &smem))
             return RRA_ERR_UNSUPPORTED;
     }
-    const void *fn = ring_fn(kc, in_t, fast);
+    a.tiles = (a.n + kTile * groups - 1) / (kTile * groups);
+    const void *fn = ring_fn(kc, in_t, fast, groups);
     if (!fn)
         return RRA_ERR_UNSUPPORTED;
-    const long long key = 1000 + kc * 100 + in_t * 10 + (fast ? 1 : 0);
+    const long long key = 10000 + kc * 1000 + in_t * 100 + (fast ? 10 : 0) + groups;
     const int grid = grid_for(comm, key, fn, warps, smem, a.tiles);
     counter_sets(comm, &a.sent, &a.recv, &a.zero);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_ring(kc, in_t, fast, a, grid, warps, smem, st);
+    cudaError_t e = launch_ring(fn, a, grid, warps, smem, st);
     note_call(comm, st);
     return e == cudaSuccess ? RRA_OK : RRA_ERR_CUDA;
 }
@@ -307,6 +346,8 @@ rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count
             occ = 1;
         comm->occ[k] = occ;
     }
+    if (comm->tune_blocks)
+        occ = std::min(occ, comm->tune_blocks);
     long long g = (long long)num_sms() * occ;
     if (a.tiles < g)
         g = a.tiles;
@@ -331,10 +372,9 @@ std::map<int, std::pair<uint32_t *, long long>> g_ws;
 } // namespace
 
 namespace rra {
-cudaError_t launch_ring(int codec, int in_t, bool fast, const RingArgs &a, int grid, int warps,
-                        int smem, cudaStream_t st)
+cudaError_t launch_ring(const void *fn, const RingArgs &a, int grid, int warps, int smem,
+                        cudaStream_t st)
 {
-    const void *fn = ring_fn(codec, in_t, fast);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return e;
@@ -560,6 +600,18 @@ rra_status rra_set_timeout(rra_comm *comm, uint64_t ns)
     if (!comm)
         return RRA_ERR_INVALID;
     comm->timeout_ns = ns ? ns : kDefaultTimeoutNs;
+    return RRA_OK;
+}
+
+rra_status rra_comm_set_tuning(rra_comm *comm, int blocks_per_sm, int mailbox_depth,
+                               int stage_depth)
+{
+    if (!comm || blocks_per_sm < 0 || blocks_per_sm > 32 || mailbox_depth < 0 ||
+        mailbox_depth > 8 || stage_depth < 0 || stage_depth > 16)
+        return RRA_ERR_INVALID;
+    comm->tune_blocks = blocks_per_sm;
+    comm->tune_K = mailbox_depth;
+    comm->tune_D = stage_depth;
     return RRA_OK;
 }
 

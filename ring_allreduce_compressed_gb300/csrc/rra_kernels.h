@@ -104,10 +104,8 @@ __host__ __device__ inline Layout make_layout(int N, int K, int D, int slot_byte
 
 // Kernel entry points (one per translation unit family).  Each returns the
 // launch's cudaError_t.
-cudaError_t launch_ring(int codec, int in_t, bool fast, const RingArgs &a, int grid,
-                        int warps, int smem, cudaStream_t st);
-cudaError_t ring_kernel_attrs(int codec, int in_t, bool fast, int smem, int warps,
-                              int *blocks_per_sm);
+cudaError_t launch_ring(const void *fn, const RingArgs &a, int grid, int warps, int smem,
+                        cudaStream_t st);
 
 cudaError_t launch_allgather(bool fast, const CopyArgs &a, int grid, int warps, int smem,
                              cudaStream_t st);

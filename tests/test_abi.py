@@ -1,0 +1,99 @@
+"""CPU-side checks of the boundary: the library builds for sm_103a, loads,
+exports every entry point include/rra.h declares, rejects bad arguments on the
+host before touching the device, and the oracle and the CUDA path share no
+code (neither imports, includes or links the other)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import ring_allreduce_compressed_gb300 as rra
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rra.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rra_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rra.build()
+    return rra.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ["rra_ring_allreduce", "rra_reduce_scatter", "rra_allgather", "rra_broadcast",
+                 "rra_tree_allreduce", "rra_bfp_encode", "rra_bfp_decode", "rra_sparse_encode",
+                 "rra_sparse_decode", "rra_diff_encode", "rra_get_bytes", "rra_comm_create",
+                 "rra_comm_destroy", "rra_comm_status", "rra_set_timeout"]:
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = C.CDLL(rra.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    assert rra.status_string(rra.RRA_OK) == "RRA_OK"
+    assert rra.status_string(rra.RRA_ERR_TIMEOUT) == "RRA_ERR_TIMEOUT"
+
+
+def test_host_side_argument_checks(lib):
+    """Invalid arguments are rejected before any CUDA call."""
+    L = lib
+    assert L.rra_bfp_encode(None, 10, 0, 8, None, None, None) == rra.RRA_ERR_INVALID
+    assert L.rra_bfp_encode(C.c_void_p(16), 10, 0, 5, C.c_void_p(16), C.c_void_p(16),
+                            None) == rra.RRA_ERR_INVALID
+    assert L.rra_bfp_decode(None, None, 0, 8, None, 0, None) == rra.RRA_ERR_INVALID
+    assert L.rra_sparse_encode(C.c_void_p(16), 10, 0, C.c_float(1.5), C.c_void_p(16),
+                               C.c_void_p(16), C.c_void_p(16), None) == rra.RRA_ERR_INVALID
+    assert L.rra_diff_encode(None, None, None, 4, None) == rra.RRA_ERR_INVALID
+    h = C.c_void_p()
+    assert L.rra_comm_create(0, 10, 0, C.byref(h)) == rra.RRA_ERR_INVALID
+    assert L.rra_comm_create(65, 10, 0, C.byref(h)) == rra.RRA_ERR_INVALID
+    assert L.rra_comm_create(4, 0, 0, C.byref(h)) == rra.RRA_ERR_INVALID
+    assert L.rra_ring_allreduce(None, None, None, 10, 0, 0, None, None) == rra.RRA_ERR_INVALID
+    assert L.rra_get_bytes(None, None, None) == rra.RRA_ERR_INVALID
+    assert L.rra_comm_destroy(None) == rra.RRA_OK
+
+
+def _sources(folder, exts):
+    out = []
+    for dp, _, fs in os.walk(os.path.join(ROOT, folder)):
+        if "_build" in dp or "__pycache__" in dp:
+            continue
+        out += [os.path.join(dp, f) for f in fs if f.endswith(exts)]
+    return out
+
+
+def test_oracle_and_cuda_path_share_no_code():
+    for f in _sources("oracle", (".c", ".h", ".py")):
+        text = open(f).read()
+        assert "ring_allreduce_compressed_gb300" not in text.replace(
+            "GPU library (``ring_allreduce_compressed_gb300``)", ""), f
+        assert "rra.h" not in text and "rra_device" not in text, f
+    for f in _sources("ring_allreduce_compressed_gb300", (".cu", ".cuh", ".h", ".py")):
+        text = open(f).read()
+        assert "import oracle" not in text and "oracle.h" not in text and \
+            "liboracle" not in text, f
+    wl = open(os.path.join(ROOT, "workloads", "__init__.py")).read()
+    assert "import oracle" not in wl and "ring_allreduce_compressed_gb300" not in wl
+
+
+def test_product_path_never_calls_the_oracle():
+    """Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline and
+    reference legs may touch oracle/."""
+    bench = open(os.path.join(ROOT, "bench.py")).read()
+    uses = [m.start() for m in re.finditer(r"import oracle", bench)]
+    for pos in uses:
+        fn = bench.rfind("\ndef ", 0, pos)
+        name = bench[fn + 5:bench.index("(", fn)]
+        assert name in ("oracle_sample_ring", "run_reference"), name

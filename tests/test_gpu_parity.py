@@ -259,6 +259,20 @@ def test_reduce_scatter(codec_kind, bits, in_dt, N, T):
     compare(gpu, ref, f"rs {codec_kind}")
 
 
+def test_reduce_scatter_into_one_shared_buffer():
+    """Reduce-scatter writes chunk r of out[r] only, so all ranks may point at
+    one buffer; it then holds the whole reduced vector (here the mean)."""
+    N, T = 8, 8 * 3000 + 5
+    xs = rand_f32(N, T, seed=77)
+    shared = torch.zeros(T, device="cuda")
+    comm = rra.Comm(N, T)
+    comm.reduce_scatter(xs, [shared] * N, rra.Codec("none", average=True))
+    assert comm.status() == rra.RRA_OK
+    ref = O.ring([host(x) for x in xs], average=True)[0][0]
+    assert_bits_equal(host(shared), ref, "shared")
+    comm.close()
+
+
 # ------------------------------------------------------------------ allgather / broadcast / tree
 
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
