@@ -250,6 +250,33 @@ rra_status rra_bfp_decode(const int8_t *exps, const uint8_t *mants, size_t n, in
 rra_status rra_sparse_encode(const void *x, size_t n, rra_dtype dtype, float threshold,
                              uint32_t *hdr, void *vals, int32_t *idx, void *stream);
 
+/* Largest n that rra_sparse_encode_noalloc accepts: its fixed scratch holds
+ * one 32-bit count per 4096 elements, 65536 counts (256 KiB). */
+#define RRA_NOALLOC_MAX_COUNT (65536ull * 4096ull)
+
+/*
+ * rra_sparse_encode for callers that cannot allocate device memory (the
+ * pages have no counterpart; it is a deployment variant of the sparse
+ * encoder).  Same arguments, output and errors as rra_sparse_encode, except:
+ *  - it never allocates: no cudaMalloc, cudaFree or allocating library call.
+ *    Its scratch is a fixed array inside the library (256 KiB of device
+ *    memory on every GPU that loads the library, held until the process
+ *    exits).  This suits callers that may not allocate: code recorded into a
+ *    CUDA graph while capturing, latency-critical loops, processes whose
+ *    device memory is owned by their own allocator or budgeted up front.
+ *  - n may not exceed RRA_NOALLOC_MAX_COUNT (2^28 elements); larger n returns
+ *    RRA_ERR_INVALID without doing anything (use rra_sparse_encode then).
+ *  - the first call on a device looks up the scratch array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before starting any stream capture.
+ *  - all calls share the one scratch array, and each call overwrites the
+ *    part it uses before reading it, so no clearing is needed between calls;
+ *    calls that overlap on the GPU (different streams without ordering
+ *    between them) race on the scratch and give undefined results.
+ */
+rra_status rra_sparse_encode_noalloc(const void *x, size_t n, rra_dtype dtype, float threshold,
+                                     uint32_t *hdr, void *vals, int32_t *idx, void *stream);
+
 /*
  * Sparse decode into fp32 acc[0..n) (hdr, vals, idx as written by
  * rra_sparse_encode; the format is read on the device).

@@ -241,6 +241,18 @@ def sparse_encode(x, threshold: float, hdr, vals, idx, stream=None):
                                    _stream(stream)), "rra_sparse_encode")
 
 
+def sparse_encode_noalloc(x, threshold: float, hdr, vals, idx, stream=None):
+    """rra_sparse_encode_noalloc: the sparse encoder without any device
+    allocation (fixed in-library scratch; n <= RRA_NOALLOC_MAX_COUNT), for
+    callers that cannot allocate, e.g. while a CUDA graph is being captured."""
+    f = lib().rra_sparse_encode_noalloc
+    f.argtypes = [C.c_void_p, C.c_size_t, C.c_int, C.c_float, C.c_void_p, C.c_void_p,
+                  C.c_void_p, C.c_void_p]
+    f.restype = C.c_int
+    _check(f(_dev(x, "x"), x.numel(), _dtype_code(x.dtype), threshold, _dev(hdr, "hdr"),
+             _dev(vals, "vals"), _dev(idx, "idx"), _stream(stream)), "rra_sparse_encode_noalloc")
+
+
 def sparse_decode(hdr, vals, idx, n: int, acc, accumulate: bool = False, stream=None):
     _check(lib().rra_sparse_decode(_dev(hdr, "hdr"), _dev(vals, "vals"), _dev(idx, "idx"), n,
                                    _dtype_code(vals.dtype), _dev(acc, "acc"), int(accumulate),

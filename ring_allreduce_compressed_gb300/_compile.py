@@ -20,7 +20,7 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "librra.so")
 
 SOURCES = ["rra_host.cu", "ring_none.cu", "ring_bfp.cu", "ring_sparse.cu", "copy_kernels.cu",
-           "codec_kernels.cu"]
+           "codec_kernels.cu", "noalloc.cu"]
 HEADERS = ["rra_device.cuh", "rra_kernels.h", "ring_kernel.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
