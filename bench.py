@@ -70,12 +70,20 @@ def barrier(world):
 
 
 def max_over_ranks(world, x: float) -> float:
+    """Largest value over the ranks (the slowest replica's time)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_gbs(world: int, payload_bytes: int, ms_per_step_max: float) -> float:
+    """Whole-job algbw: every replica moves its own payload per step; the job
+    takes as long as its slowest replica."""
+    return world * payload_bytes / (ms_per_step_max * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------- clocks
@@ -346,7 +354,7 @@ def run_rra(args, world, rank, local):
     ms_step = max_over_ranks(world, total_ms / K)
     kern_ms = max_over_ranks(world, kern_ms)
 
-    value = world * wl.payload / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(world, wl.payload, ms_step)
     peak, peak_src = hbm_peak()
     achieved = wl.compulsory / (kern_ms * 1e-3) / 1e9
     traffic, traffic_src = traffic_from_profile(args.config)
@@ -382,7 +390,7 @@ def run_rra(args, world, rank, local):
         ok = all(torch.equal(h_out[r].view(torch.int16 if wl.out_dtype != torch.float32 else torch.int32),
                              wl.outputs[r].cpu().view(torch.int16 if wl.out_dtype != torch.float32 else torch.int32))
                  for r in range(wl.N))
-        e2e = {"value": world * wl.payload / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        e2e = {"value": whole_job_gbs(world, wl.payload, e2e_ms), "unit": "GB/s",
                "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in h_in),
                "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in h_out),

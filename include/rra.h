@@ -321,7 +321,9 @@ rra_status rra_set_timeout(rra_comm *comm, uint64_t ns);
  * override allowed).  Each value 0 = automatic.
  *  blocks_per_sm  resident blocks per SM to launch (1..32; clamped to what
  *                 the occupancy calculator allows).
- *  mailbox_depth  messages in flight per ring edge (1..8).
+ *  mailbox_depth  messages in flight per ring edge (1..8; slices of more
+ *                 than 256 elements always use at least 2, because a rank
+ *                 frees the slot it streams from only after its own send).
  *  stage_depth    input slices each rank stages ahead with bulk copies (1..16).
  * Depths that do not fit the shared memory are reduced automatically.
  * Errors: RRA_ERR_INVALID for NULL or values out of range.

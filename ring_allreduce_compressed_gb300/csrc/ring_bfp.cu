@@ -30,6 +30,17 @@ const void *ring_fn_bfp(int codec, int in_t, bool fast, int groups)
             return fast ? (const void *)ring_kernel<kCodecBfp8, kBF16, true, 2>
                         : (const void *)ring_kernel<kCodecBfp8, kBF16, false, 2>;
     }
+    if (codec == kCodecBfp8 && groups == 4) {
+        if (in_t == kF32)
+            return fast ? (const void *)ring_kernel<kCodecBfp8, kF32, true, 4>
+                        : (const void *)ring_kernel<kCodecBfp8, kF32, false, 4>;
+        if (in_t == kF16)
+            return fast ? (const void *)ring_kernel<kCodecBfp8, kF16, true, 4>
+                        : (const void *)ring_kernel<kCodecBfp8, kF16, false, 4>;
+        if (in_t == kBF16)
+            return fast ? (const void *)ring_kernel<kCodecBfp8, kBF16, true, 4>
+                        : (const void *)ring_kernel<kCodecBfp8, kBF16, false, 4>;
+    }
     if (codec == kCodecBfp4 && groups == 1) {
         if (in_t == kF32)
             return fast ? (const void *)ring_kernel<kCodecBfp4, kF32, true, 1>
@@ -51,6 +62,17 @@ const void *ring_fn_bfp(int codec, int in_t, bool fast, int groups)
         if (in_t == kBF16)
             return fast ? (const void *)ring_kernel<kCodecBfp4, kBF16, true, 2>
                         : (const void *)ring_kernel<kCodecBfp4, kBF16, false, 2>;
+    }
+    if (codec == kCodecBfp4 && groups == 4) {
+        if (in_t == kF32)
+            return fast ? (const void *)ring_kernel<kCodecBfp4, kF32, true, 4>
+                        : (const void *)ring_kernel<kCodecBfp4, kF32, false, 4>;
+        if (in_t == kF16)
+            return fast ? (const void *)ring_kernel<kCodecBfp4, kF16, true, 4>
+                        : (const void *)ring_kernel<kCodecBfp4, kF16, false, 4>;
+        if (in_t == kBF16)
+            return fast ? (const void *)ring_kernel<kCodecBfp4, kBF16, true, 4>
+                        : (const void *)ring_kernel<kCodecBfp4, kBF16, false, 4>;
     }
     return nullptr;
 }

@@ -161,146 +161,147 @@ template <int BITS> struct BfpGroup {
 };
 
 // ---------------------------------------------------------------- wire formats
-// A Wire holds one lane's share of a message in registers.
-// All value arrays are updated in place (one array of 8G floats per lane
-// keeps the register footprint small).
-//  encode_store<DEC>: encode the lane's fp32 values v into a slot; with DEC,
-//                     v is replaced by what a receiver decodes; returns the
-//                     wire bytes.
-//  load / store:      slot <-> registers (allgather forwarding); load returns
-//                     the wire bytes.
-//  decode_add:        v = v + decoded message (positions a sparse message
-//                     does not carry keep v).
-//  values:            v = decoded values (0 where a sparse message carries none).
+// A message covers one slice of TW = 256*G elements.  The kernel streams it
+// group by group (8 elements per lane, 256 per warp): a WireCodec's per-group
+// operations move one group between registers and a slot, so only 8 values
+// per lane are live at a time however large the slice is.
+//  Reg                   one lane's share of one group of a message.
+//  load / store          group gi: slot <-> Reg (allgather forwarding).
+//  encode<DEC>           encode the lane's 8 fp32 values of group gi into the
+//                        slot; with DEC, v becomes what a receiver decodes.
+//  decode_add            v = v + decoded group (positions a sparse message
+//                        does not carry keep v).
+//  values                v = decoded group (0 where a sparse message has none).
+//  bytes(V, slot)        wire bytes of a message of V elements.
 
-template <int CODEC, int G> struct Wire;
+template <int CODEC> struct WireCodec;
 
-template <int G> struct Wire<kCodecNone, G> {
-    static constexpr int kSlot = kTile * 4 * G;
-    float f[8 * G];
+// Lossless: fp32, group gi at byte 1024*gi, lane L at 32L within the group.
+template <> struct WireCodec<kCodecNone> {
+    static constexpr bool kSliced = true; // any slice length
+    static constexpr int slot_bytes(int G) { return kTile * 4 * G; }
+    struct Reg {
+        float f[8];
+    };
+    __device__ __forceinline__ static void load(const unsigned char *slot, int gi, int lane,
+                                                Reg &m)
+    {
+        const float4 *p = reinterpret_cast<const float4 *>(slot + gi * kTile * 4) + 2 * lane;
+        const float4 a = p[0], b = p[1];
+        m.f[0] = a.x; m.f[1] = a.y; m.f[2] = a.z; m.f[3] = a.w;
+        m.f[4] = b.x; m.f[5] = b.y; m.f[6] = b.z; m.f[7] = b.w;
+    }
+    __device__ __forceinline__ static void store(unsigned char *slot, int gi, int lane,
+                                                 const Reg &m)
+    {
+        float4 *p = reinterpret_cast<float4 *>(slot + gi * kTile * 4) + 2 * lane;
+        p[0] = make_float4(m.f[0], m.f[1], m.f[2], m.f[3]);
+        p[1] = make_float4(m.f[4], m.f[5], m.f[6], m.f[7]);
+    }
     template <bool DEC>
-    __device__ __forceinline__ uint32_t encode_store(float (&v)[8 * G], int V, int lane,
-                                                     unsigned char *slot, double, unsigned char *)
+    __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int gi,
+                                                  int lane, int, double, unsigned char *)
+    {
+        float4 *p = reinterpret_cast<float4 *>(slot + gi * kTile * 4) + 2 * lane;
+        p[0] = make_float4(v[0], v[1], v[2], v[3]);
+        p[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+    __device__ __forceinline__ static void decode_add(const Reg &m, float (&v)[8], int,
+                                                      unsigned char *)
     {
 #pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-            float4 *p = reinterpret_cast<float4 *>(slot + gi * kTile * 4) + 2 * lane;
-            p[0] = make_float4(v[8 * gi + 0], v[8 * gi + 1], v[8 * gi + 2], v[8 * gi + 3]);
-            p[1] = make_float4(v[8 * gi + 4], v[8 * gi + 5], v[8 * gi + 6], v[8 * gi + 7]);
-        }
+        for (int i = 0; i < 8; ++i)
+            v[i] = __fadd_rn(v[i], m.f[i]);
+    }
+    __device__ __forceinline__ static void values(const Reg &m, float (&v)[8], int,
+                                                  unsigned char *)
+    {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            v[i] = m.f[i];
+    }
+    __device__ __forceinline__ static uint32_t bytes(int V, const unsigned char *)
+    {
         return 4u * (uint32_t)V;
-    }
-    __device__ __forceinline__ uint32_t load(const unsigned char *slot, int lane, int V)
-    {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-            const float4 *p = reinterpret_cast<const float4 *>(slot + gi * kTile * 4) + 2 * lane;
-            const float4 a = p[0], b = p[1];
-            f[8 * gi + 0] = a.x; f[8 * gi + 1] = a.y; f[8 * gi + 2] = a.z; f[8 * gi + 3] = a.w;
-            f[8 * gi + 4] = b.x; f[8 * gi + 5] = b.y; f[8 * gi + 6] = b.z; f[8 * gi + 7] = b.w;
-        }
-        return 4u * (uint32_t)V;
-    }
-    __device__ __forceinline__ void store(unsigned char *slot, int lane) const
-    {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-            float4 *p = reinterpret_cast<float4 *>(slot + gi * kTile * 4) + 2 * lane;
-            p[0] = make_float4(f[8 * gi + 0], f[8 * gi + 1], f[8 * gi + 2], f[8 * gi + 3]);
-            p[1] = make_float4(f[8 * gi + 4], f[8 * gi + 5], f[8 * gi + 6], f[8 * gi + 7]);
-        }
-    }
-    __device__ __forceinline__ void decode_add(float (&v)[8 * G], int, unsigned char *) const
-    {
-#pragma unroll
-        for (int i = 0; i < 8 * G; ++i)
-            v[i] = __fadd_rn(v[i], f[i]);
-    }
-    __device__ __forceinline__ void values(float (&v)[8 * G], int, unsigned char *) const
-    {
-#pragma unroll
-        for (int i = 0; i < 8 * G; ++i)
-            v[i] = f[i];
     }
 };
 
-// Block floating point.  Slot: 16 bytes of exponents (2G used; byte b is the
-// exponent of the slice's block b), then the mantissas in element order
+// Block floating point: 16 header bytes of exponents (byte b is the exponent
+// of the slice's 128-element block b), then the mantissas in element order
 // (group gi at 16 + gi * 256*BITS/8; lane L at 8L bytes (8-bit) or 4L bytes
 // (4-bit) within the group).
-template <int BITS, int G> struct WireBfp {
+template <int BITS> struct CodecBfp {
+    static constexpr bool kSliced = true;
     static constexpr int kMB = kTile * BITS / 8;
-    static constexpr int kSlot = 16 + kMB * G;
-    uint32_t w[G][2];
-    int e[G];
+    static constexpr int slot_bytes(int G) { return 16 + kMB * G; }
+    struct Reg {
+        uint32_t w[2];
+        int e;
+    };
+    __device__ __forceinline__ static void load(const unsigned char *slot, int gi, int lane,
+                                                Reg &m)
+    {
+        m.e = (int)(int8_t)slot[2 * gi + (lane >> 4)];
+        if constexpr (BITS == 8) {
+            const uint2 u = reinterpret_cast<const uint2 *>(slot + 16 + gi * kMB)[lane];
+            m.w[0] = u.x;
+            m.w[1] = u.y;
+        } else {
+            m.w[0] = reinterpret_cast<const uint32_t *>(slot + 16 + gi * kMB)[lane];
+            m.w[1] = 0;
+        }
+    }
+    __device__ __forceinline__ static void store(unsigned char *slot, int gi, int lane,
+                                                 const Reg &m)
+    {
+        if ((lane & 15) == 0)
+            slot[2 * gi + (lane >> 4)] = (unsigned char)(int8_t)m.e;
+        if constexpr (BITS == 8)
+            reinterpret_cast<uint2 *>(slot + 16 + gi * kMB)[lane] = make_uint2(m.w[0], m.w[1]);
+        else
+            reinterpret_cast<uint32_t *>(slot + 16 + gi * kMB)[lane] = m.w[0];
+    }
     template <bool DEC>
-    __device__ __forceinline__ uint32_t encode_store(float (&v)[8 * G], int V, int lane,
-                                                     unsigned char *slot, double, unsigned char *)
+    __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int gi,
+                                                  int lane, int, double, unsigned char *)
     {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-            BfpGroup<BITS>::encode(v + 8 * gi, e[gi], w[gi]);
-            if (DEC)
-                BfpGroup<BITS>::decode(w[gi], e[gi], v + 8 * gi);
-        }
-        store(slot, lane);
+        Reg m;
+        BfpGroup<BITS>::encode(v, m.e, m.w);
+        store(slot, gi, lane, m);
+        if (DEC)
+            BfpGroup<BITS>::decode(m.w, m.e, v);
+    }
+    __device__ __forceinline__ static void decode_add(const Reg &m, float (&v)[8], int,
+                                                      unsigned char *)
+    {
+        BfpGroup<BITS>::decode_add(m.w, m.e, v, v);
+    }
+    __device__ __forceinline__ static void values(const Reg &m, float (&v)[8], int,
+                                                  unsigned char *)
+    {
+        BfpGroup<BITS>::decode(m.w, m.e, v);
+    }
+    __device__ __forceinline__ static uint32_t bytes(int V, const unsigned char *)
+    {
         return bfp_msg_bytes(V, BITS);
-    }
-    __device__ __forceinline__ uint32_t load(const unsigned char *slot, int lane, int V)
-    {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-            e[gi] = (int)(int8_t)slot[2 * gi + (lane >> 4)];
-            if constexpr (BITS == 8) {
-                const uint2 u = reinterpret_cast<const uint2 *>(slot + 16 + gi * kMB)[lane];
-                w[gi][0] = u.x;
-                w[gi][1] = u.y;
-            } else {
-                w[gi][0] = reinterpret_cast<const uint32_t *>(slot + 16 + gi * kMB)[lane];
-                w[gi][1] = 0;
-            }
-        }
-        return bfp_msg_bytes(V, BITS);
-    }
-    __device__ __forceinline__ void store(unsigned char *slot, int lane) const
-    {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-            if ((lane & 15) == 0)
-                slot[2 * gi + (lane >> 4)] = (unsigned char)(int8_t)e[gi];
-            if constexpr (BITS == 8)
-                reinterpret_cast<uint2 *>(slot + 16 + gi * kMB)[lane] =
-                    make_uint2(w[gi][0], w[gi][1]);
-            else
-                reinterpret_cast<uint32_t *>(slot + 16 + gi * kMB)[lane] = w[gi][0];
-        }
-    }
-    __device__ __forceinline__ void decode_add(float (&v)[8 * G], int, unsigned char *) const
-    {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi)
-            BfpGroup<BITS>::decode_add(w[gi], e[gi], v + 8 * gi, v + 8 * gi);
-    }
-    __device__ __forceinline__ void values(float (&v)[8 * G], int, unsigned char *) const
-    {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi)
-            BfpGroup<BITS>::decode(w[gi], e[gi], v + 8 * gi);
     }
 };
-template <int G> struct Wire<kCodecBfp8, G> : WireBfp<8, G> {};
-template <int G> struct Wire<kCodecBfp4, G> : WireBfp<4, G> {};
+template <> struct WireCodec<kCodecBfp8> : CodecBfp<8> {};
+template <> struct WireCodec<kCodecBfp4> : CodecBfp<4> {};
 
-// Sparse values + indices (one 256-element slice per message, G = 1).
+// Sparse values + indices: one 256-element slice per message (G = 1).
 // Slot: {uint32 fmt, uint32 nnz} padded to 16 bytes, fp32 values[256],
 // int32 indices[256] (slice-relative, ascending).  Dense fallback: fmt 0,
 // values[0..len) in place.  Compaction: per-lane nonzero masks and a warp
 // inclusive scan of their popcounts give every lane's first output position.
-template <> struct Wire<kCodecSparse, 1> {
-    static constexpr int kSlot = 16 + kTile * 8;
-    uint32_t fmt, nnz;
-    float f[8];
-    int ix[8];
+template <> struct WireCodec<kCodecSparse> {
+    static constexpr bool kSliced = false; // the message is exactly one 256-element slice
+    static constexpr int slot_bytes(int) { return 16 + kTile * 8; }
+    struct Reg {
+        uint32_t fmt, nnz;
+        float f[8];
+        int ix[8];
+    };
     __device__ __forceinline__ static float *vals(unsigned char *s)
     {
         return reinterpret_cast<float *>(s + 16);
@@ -309,23 +310,64 @@ template <> struct Wire<kCodecSparse, 1> {
     {
         return reinterpret_cast<int *>(s + 16 + kTile * 4);
     }
-    __device__ __forceinline__ uint32_t bytes(int V) const
+    __device__ __forceinline__ static uint32_t bytes(int V, const unsigned char *slot)
     {
-        return V == 0 ? 0u : 8u + (fmt ? 8u * nnz : 4u * (uint32_t)V);
+        const uint2 h = *reinterpret_cast<const uint2 *>(slot);
+        return V == 0 ? 0u : 8u + (h.x ? 8u * h.y : 4u * (uint32_t)V);
     }
-    template <bool DEC>
-    __device__ __forceinline__ uint32_t encode_store(float (&acc)[8], int V, int lane,
-                                                     unsigned char *slot, double one_minus_thr,
-                                                     unsigned char *)
+    __device__ __forceinline__ static void load(const unsigned char *slot, int, int lane, Reg &m)
     {
-        // the receiver restores every value exactly (absent ones are +0.0),
-        // so the decoded values are acc itself
+        const uint2 h = *reinterpret_cast<const uint2 *>(slot);
+        m.fmt = h.x;
+        m.nnz = h.y;
+        unsigned char *s = const_cast<unsigned char *>(slot);
+        if (!m.fmt) {
+            const float4 *p = reinterpret_cast<const float4 *>(vals(s)) + 2 * lane;
+            const float4 a = p[0], b = p[1];
+            m.f[0] = a.x; m.f[1] = a.y; m.f[2] = a.z; m.f[3] = a.w;
+            m.f[4] = b.x; m.f[5] = b.y; m.f[6] = b.z; m.f[7] = b.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = lane + 32 * i;
+                if (k < (int)m.nnz) {
+                    m.f[i] = vals(s)[k];
+                    m.ix[i] = idxs(s)[k];
+                }
+            }
+        }
+    }
+    __device__ __forceinline__ static void store(unsigned char *slot, int, int lane, const Reg &m)
+    {
+        if (lane == 0)
+            *reinterpret_cast<uint2 *>(slot) = make_uint2(m.fmt, m.nnz);
+        if (!m.fmt) {
+            float4 *p = reinterpret_cast<float4 *>(vals(slot)) + 2 * lane;
+            p[0] = make_float4(m.f[0], m.f[1], m.f[2], m.f[3]);
+            p[1] = make_float4(m.f[4], m.f[5], m.f[6], m.f[7]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = lane + 32 * i;
+                if (k < (int)m.nnz) {
+                    vals(slot)[k] = m.f[i];
+                    idxs(slot)[k] = m.ix[i];
+                }
+            }
+        }
+    }
+    // the receiver restores every value exactly (absent ones are +0.0), so the
+    // decoded values are v itself: DEC changes nothing
+    template <bool DEC>
+    __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int,
+                                                  int lane, int V, double one_minus_thr,
+                                                  unsigned char *)
+    {
         uint32_t nzm = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (8 * lane + i < V && __float_as_uint(acc[i]) != 0u)
+        for (int i = 0; i < 8; ++i)
+            if (8 * lane + i < V && __float_as_uint(v[i]) != 0u)
                 nzm |= 1u << i;
-        }
         const int cnt = __popc(nzm);
         int incl = cnt;
 #pragma unroll
@@ -335,78 +377,35 @@ template <> struct Wire<kCodecSparse, 1> {
                 incl += t;
         }
         const int total = __shfl_sync(kFull, incl, 31);
-        fmt = (double)total < one_minus_thr * (double)V ? 1u : 0u;
-        nnz = (uint32_t)total;
+        const uint32_t fmt = (double)total < one_minus_thr * (double)V ? 1u : 0u;
         if (lane == 0)
-            *reinterpret_cast<uint2 *>(slot) = make_uint2(fmt, nnz);
+            *reinterpret_cast<uint2 *>(slot) = make_uint2(fmt, (uint32_t)total);
         if (fmt) {
             int pos = incl - cnt;
-            float *v = vals(slot);
+            float *vv = vals(slot);
             int *x = idxs(slot);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 if ((nzm >> i) & 1u) {
-                    v[pos] = acc[i];
+                    vv[pos] = v[i];
                     x[pos] = 8 * lane + i;
                     ++pos;
                 }
         } else {
             float4 *p = reinterpret_cast<float4 *>(vals(slot)) + 2 * lane;
-            p[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            p[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        }
-        return bytes(V);
-    }
-    __device__ __forceinline__ uint32_t load(const unsigned char *slot, int lane, int V)
-    {
-        const uint2 h = *reinterpret_cast<const uint2 *>(slot);
-        fmt = h.x;
-        nnz = h.y;
-        unsigned char *s = const_cast<unsigned char *>(slot);
-        if (!fmt) {
-            const float4 *p = reinterpret_cast<const float4 *>(vals(s)) + 2 * lane;
-            const float4 a = p[0], b = p[1];
-            f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-            f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int k = lane + 32 * i;
-                if (k < (int)nnz) {
-                    f[i] = vals(s)[k];
-                    ix[i] = idxs(s)[k];
-                }
-            }
-        }
-        return bytes(V);
-    }
-    __device__ __forceinline__ void store(unsigned char *slot, int lane) const
-    {
-        if (lane == 0)
-            *reinterpret_cast<uint2 *>(slot) = make_uint2(fmt, nnz);
-        if (!fmt) {
-            float4 *p = reinterpret_cast<float4 *>(vals(slot)) + 2 * lane;
-            p[0] = make_float4(f[0], f[1], f[2], f[3]);
-            p[1] = make_float4(f[4], f[5], f[6], f[7]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int k = lane + 32 * i;
-                if (k < (int)nnz) {
-                    vals(slot)[k] = f[i];
-                    idxs(slot)[k] = ix[i];
-                }
-            }
+            p[0] = make_float4(v[0], v[1], v[2], v[3]);
+            p[1] = make_float4(v[4], v[5], v[6], v[7]);
         }
     }
     // Sparse messages: scatter the pairs into the warp's scratch (values +
     // presence bytes), then read this lane's 8 positions.
-    __device__ __forceinline__ uint32_t gather(int lane, unsigned char *scratch, float v[8]) const
+    __device__ __forceinline__ static uint32_t gather(const Reg &m, int lane,
+                                                      unsigned char *scratch, float (&v)[8])
     {
-        if (!fmt) {
+        if (!m.fmt) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                v[i] = f[i];
+                v[i] = m.f[i];
             return 0xffu;
         }
         float *sval = reinterpret_cast<float *>(scratch);
@@ -416,9 +415,9 @@ template <> struct Wire<kCodecSparse, 1> {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int k = lane + 32 * i;
-            if (k < (int)nnz) {
-                sval[ix[i]] = f[i];
-                spres[ix[i]] = 1;
+            if (k < (int)m.nnz) {
+                sval[m.ix[i]] = m.f[i];
+                spres[m.ix[i]] = 1;
             }
         }
         __syncwarp();
@@ -435,18 +434,19 @@ template <> struct Wire<kCodecSparse, 1> {
         __syncwarp();
         return pres;
     }
-    __device__ __forceinline__ void decode_add(float (&x)[8], int lane,
-                                               unsigned char *scratch) const
+    __device__ __forceinline__ static void decode_add(const Reg &m, float (&v)[8], int lane,
+                                                      unsigned char *scratch)
     {
-        float v[8];
-        const uint32_t pres = gather(lane, scratch, v);
+        float d[8];
+        const uint32_t pres = gather(m, lane, scratch, d);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            x[i] = ((pres >> i) & 1u) ? __fadd_rn(x[i], v[i]) : x[i];
+            v[i] = ((pres >> i) & 1u) ? __fadd_rn(v[i], d[i]) : v[i];
     }
-    __device__ __forceinline__ void values(float (&v)[8], int lane, unsigned char *scratch) const
+    __device__ __forceinline__ static void values(const Reg &m, float (&v)[8], int lane,
+                                                  unsigned char *scratch)
     {
-        gather(lane, scratch, v);
+        gather(m, lane, scratch, v);
     }
 };
 
@@ -479,11 +479,29 @@ struct Fifo {
 
 // ---------------------------------------------------------------- kernel
 
+// Rare path of a wait (the phase was not complete at the first test): kept
+// out of line so that the common path stays a few instructions.
+static __device__ __noinline__ bool wait_slow(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                              unsigned *status)
+{
+    return wait_phase(bar, parity, limit_ns, status);
+}
+
+// Warp-uniform: true once every lane has observed the phase (acquire).
+__device__ __forceinline__ bool wait_ready(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                           unsigned *status)
+{
+    if (__all_sync(kFull, mbar_try_wait(bar, parity)))
+        return true;
+    return wait_slow(bar, parity, limit_ns, status);
+}
+
 template <int CODEC, int IN_T, bool FAST, int G>
 __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_constant__ RingArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    using Msg = Wire<CODEC, G>;
+    using C = WireCodec<CODEC>;
+    using Reg = typename C::Reg;
     constexpr int es = dtype_size(IN_T);
     constexpr int TW = kTile * G; // elements per rank per step
     const int N = a.N;
@@ -520,10 +538,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
     __syncthreads();
 
     const bool allred = a.mode == kModeAllreduce;
-    const int Gs = allred ? 2 * N - 1 : N; // steps per slice position
-    const int M = allred ? 2 * N - 2 : N - 1;
     const long long n = a.n, T = a.T;
-    const int out_es = dtype_size(a.out_t);
     // shortest chunk: every slice position below it is full in every chunk
     const long long min_len = T - (long long)(N - 1) * n;
 
@@ -584,181 +599,266 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
 
     Fifo rcv{0, 0}, snd{0, 0}, stg{0, 0};
     bool ok = true;
-    long long j = 0;
-    for (long long item = blockIdx.x; ok && item < a.tiles; item += gridDim.x, ++j) {
-        const long long t0 = item * TW;
-        for (int g = 1; ok && g <= Gs; ++g) {
-            const bool do_recv = g >= 2;
-            const bool do_send = g <= M;
-            const bool rs_part = g <= N;
+    long long t0 = 0;
+    const bool first_item_withhold = a.withhold_rank >= 0;
+
+    // group gi of rank r's own input for chunk c (staged on the fast path)
+    auto input_group = [&](int r, int c, int V, int gi, const unsigned char *sp,
+                           float (&v)[8]) {
+        if constexpr (FAST) {
+            load8_vec<IN_T>(sp + (gi * kTile + 8 * lane) * es, v);
+            if (a.has_prev) {
+                float p[8];
+                load8_vec<kF32>(sp + TW * 4 + (gi * kTile + 8 * lane) * 4, p);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    v[i] = __fsub_rn(v[i], p[i]);
+            }
+            if (V < TW) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (gi * kTile + 8 * lane + i >= V)
+                        v[i] = 0.0f;
+            }
+        } else {
+            const int vl = min(max(V - gi * kTile - 8 * lane, 0), 8);
+            const long long eo = (long long)c * n + t0 + gi * kTile + 8 * lane;
+            load8_scalar<IN_T>(reinterpret_cast<const char *>(a.in[r]) + eo * es, vl, v);
+            if (a.has_prev) {
+                float p[8];
+                load8_scalar<kF32>(a.prev[r] + eo, vl, p);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    v[i] = __fsub_rn(v[i], p[i]);
+            }
+        }
+    };
+    // output epilogue of group gi: average, previous-round base, cast
+    const float inv_n = ((N & (N - 1)) == 0) ? 1.0f / (float)N : 0.0f; // exact for powers of two
+    const int out_t = a.out_t;
+    auto output_group = [&](int r, int c, int V, int gi, float (&v)[8]) {
+        const long long e0 = (long long)c * n + t0 + gi * kTile + 8 * lane;
+        const int vl = V == TW ? 8 : min(max(V - gi * kTile - 8 * lane, 0), 8);
+        if (a.average) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[i] = inv_n != 0.0f ? __fmul_rn(v[i], inv_n) : __fdiv_rn(v[i], (float)N);
+        }
+        if (a.base) {
+            float bb[8];
+            if (a.vec_base && vl == 8)
+                load8_vec<kF32>(a.base + e0, bb);
+            else
+                load8_scalar<kF32>(a.base + e0, vl, bb);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[i] = __fadd_rn(bb[i], v[i]);
+        }
+        store8(reinterpret_cast<char *>(a.out[r]) + e0 * dtype_size(out_t), out_t, v, vl,
+               a.vec_out != 0);
+    };
+    auto waits_ok = [&](bool w) -> bool {
+        ok = ok && w;
+        return ok;
+    };
+    // One-group messages fit in registers: copy the message out and free its
+    // slot before waiting for the next rank's slot, so even one slot per
+    // edge cannot stall the ring.  Wider messages are streamed group by group
+    // and their slot is freed at the end of the step (two slots per edge).
+    constexpr bool kEarly = G == 1;
+    auto release_early = [&](int r, const unsigned char *rslot, uint32_t rb, Reg &m) {
+        C::load(rslot, 0, lane, m);
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(empty + r * K + rcv.slot);
+            rrecv[r] += rb;
+        }
+    };
+    // after a step that consumed a staged load: refill that stage
+    auto stage_step = [&]() {
+        if constexpr (FAST) {
+            __syncwarp();
+            if (issued == consumed + D && cur_item < a.tiles) {
+                if (lane == 0)
+                    for (int r = warp; r < N; r += W)
+                        issue_one(r, stg.slot);
+                ++issued;
+                cursor_next();
+            }
+            ++consumed;
+            stg.advance(D);
+        }
+    };
+    // publish: free the receive slot (if any), mark the sent message full
+    auto finish_step = [&](int r, int g, bool recv, bool send, uint32_t rb, uint32_t sb) {
+        __syncwarp();
+        if (lane == 0) {
+            if (recv) {
+                mbar_arrive(empty + r * K + rcv.slot);
+                rrecv[r] += rb;
+            }
+            if (send) {
+                const int dst = r + 1 == N ? 0 : r + 1;
+                if (!(first_item_withhold && r == a.withhold_rank && g == a.withhold_step &&
+                      t0 == (long long)blockIdx.x * TW))
+                    mbar_arrive(full + dst * K + snd.slot);
+                rsent[r] += sb;
+            }
+        }
+    };
+
+    for (long long item = blockIdx.x; ok && item < a.tiles; item += gridDim.x) {
+        t0 = item * TW;
+
+        // ---- reduce-scatter steps g = 1..N-1: send chunk (r-g) mod N
+        for (int g = 1; ok && g < N; ++g) {
             for (int r = warp; r < N; r += W) {
                 int c = r - g;
                 c += c < 0 ? N : 0;
-                c += c < 0 ? N : 0;
                 const int V = slice_len(c, t0);
-                const long long ebase = (long long)c * n + t0 + 8 * lane;
-
-                // ---- own input (reduce-scatter steps and the owner step)
-                float v[8 * G];
-                if (rs_part) {
-                    if constexpr (FAST) {
-                        ok = wait_phase(sbar + r * D + stg.slot, (uint32_t)stg.phase,
-                                        a.timeout_ns, a.status);
-                        if (!ok)
-                            break;
-                        const unsigned char *sp =
-                            stages + (size_t)(r * D + stg.slot) * a.stage_bytes;
-#pragma unroll
-                        for (int gi = 0; gi < G; ++gi)
-                            load8_vec<IN_T>(sp + (gi * kTile + 8 * lane) * es, v + 8 * gi);
-                        if (a.has_prev) {
-#pragma unroll
-                            for (int gi = 0; gi < G; ++gi) {
-                                float p[8];
-                                load8_vec<kF32>(sp + TW * 4 + (gi * kTile + 8 * lane) * 4, p);
-#pragma unroll
-                                for (int i = 0; i < 8; ++i)
-                                    v[8 * gi + i] = __fsub_rn(v[8 * gi + i], p[i]);
-                            }
-                        }
-                        if (V < TW) {
-#pragma unroll
-                            for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-                                for (int i = 0; i < 8; ++i)
-                                    if (gi * kTile + 8 * lane + i >= V)
-                                        v[8 * gi + i] = 0.0f;
-                        }
-                    } else {
-#pragma unroll
-                        for (int gi = 0; gi < G; ++gi) {
-                            const int vl = min(max(V - gi * kTile - 8 * lane, 0), 8);
-                            const long long eo = ebase + gi * kTile;
-                            load8_scalar<IN_T>(reinterpret_cast<const char *>(a.in[r]) + eo * es,
-                                               vl, v + 8 * gi);
-                            if (a.has_prev) {
-                                float p[8];
-                                load8_scalar<kF32>(a.prev[r] + eo, vl, p);
-#pragma unroll
-                                for (int i = 0; i < 8; ++i)
-                                    v[8 * gi + i] = __fsub_rn(v[8 * gi + i], p[i]);
-                            }
-                        }
-                    }
-                }
-
-                // ---- receive from rank r-1 (steps 2..Gs)
-                Msg w;
-                uint32_t rb = 0;
-                if (do_recv) {
-                    ok = wait_phase(full + r * K + rcv.slot, (uint32_t)rcv.phase, a.timeout_ns,
-                                    a.status);
-                    if (!ok)
-                        break;
-                    rb = w.load(slots + (size_t)(r * K + rcv.slot) * a.slot_bytes, lane, V);
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(empty + r * K + rcv.slot);
-                        rrecv[r] += rb;
-                    }
-                }
-
-                // ---- reserve the slot of rank r+1
                 const int dst = r + 1 == N ? 0 : r + 1;
-                unsigned char *dslot = nullptr;
-                if (do_send) {
-                    ok = wait_phase(empty + dst * K + snd.slot, (uint32_t)(snd.phase ^ 1),
-                                    a.timeout_ns, a.status);
-                    if (!ok)
-                        break;
-                    dslot = slots + (size_t)(dst * K + snd.slot) * a.slot_bytes;
+                if (FAST && !waits_ok(wait_ready(sbar + r * D + stg.slot, (uint32_t)stg.phase,
+                                                 a.timeout_ns, a.status)))
+                    break;
+                if (g >= 2 && !waits_ok(wait_ready(full + r * K + rcv.slot, (uint32_t)rcv.phase,
+                                                   a.timeout_ns, a.status)))
+                    break;
+                const unsigned char *sp = stages + (size_t)(r * D + stg.slot) * a.stage_bytes;
+                const unsigned char *rslot = slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
+                uint32_t rb = 0;
+                Reg m0;
+                if (g >= 2) {
+                    rb = C::bytes(V, rslot);
+                    if (kEarly)
+                        release_early(r, rslot, rb, m0);
                 }
-
-                // ---- compute (in place in v)
-                bool do_out = false;
-                uint32_t sb = 0;
-                if (rs_part) {
-                    if (do_recv)
-                        w.decode_add(v, lane, scratch);
-                    Msg ws;
-                    if (g < N) {
-                        sb = ws.template encode_store<false>(v, V, lane, dslot, a.one_minus_thr,
-                                                             scratch);
-                    } else {
-                        do_out = true;
-                        if (allred) {
-                            // N = 1 has no allgather step: encode into the rank's
-                            // own (otherwise unused) mailbox slot for its output
-                            unsigned char *es_slot =
-                                dslot ? dslot : slots + (size_t)(r * K) * a.slot_bytes;
-                            sb = ws.template encode_store<true>(v, V, lane, es_slot,
-                                                                a.one_minus_thr, scratch);
-                            if (!dslot)
-                                sb = 0;
-                        }
-                    }
-                } else {
-                    w.values(v, lane, scratch);
-                    do_out = true;
-                    if (do_send) { // allgather: forward the received codes unchanged
-                        w.store(dslot, lane);
-                        sb = rb;
-                    }
-                }
-                if (do_send) {
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (!(r == a.withhold_rank && g == a.withhold_step && j == 0))
-                            mbar_arrive(full + dst * K + snd.slot);
-                        rsent[r] += sb;
-                    }
-                }
-
-                // ---- output epilogue: average, previous-round base, cast
-                if (do_out) {
+                if (!waits_ok(wait_ready(empty + dst * K + snd.slot, (uint32_t)(snd.phase ^ 1),
+                                         a.timeout_ns, a.status)))
+                    break;
+                unsigned char *dslot = slots + (size_t)(dst * K + snd.slot) * a.slot_bytes;
 #pragma unroll
-                    for (int gi = 0; gi < G; ++gi) {
-                        const int vl = min(max(V - gi * kTile - 8 * lane, 0), 8);
-                        const long long eo = ebase + gi * kTile;
-                        float wv[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            wv[i] = a.average ? __fdiv_rn(v[8 * gi + i], (float)N)
-                                              : v[8 * gi + i];
-                        if (a.base) {
-                            float bb[8];
-                            if (a.vec_base && vl == 8)
-                                load8_vec<kF32>(a.base + eo, bb);
-                            else
-                                load8_scalar<kF32>(a.base + eo, vl, bb);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                wv[i] = __fadd_rn(bb[i], wv[i]);
-                        }
-                        store8(reinterpret_cast<char *>(a.out[r]) + eo * out_es, a.out_t, wv,
-                               vl, a.vec_out != 0);
+                for (int gi = 0; gi < G; ++gi) {
+                    float v[8];
+                    input_group(r, c, V, gi, sp, v);
+                    if (g >= 2) {
+                        Reg m;
+                        if (kEarly)
+                            m = m0;
+                        else
+                            C::load(rslot, gi, lane, m);
+                        C::decode_add(m, v, lane, scratch);
                     }
+                    C::template encode<false>(v, dslot, gi, lane, V, a.one_minus_thr, scratch);
                 }
+                __syncwarp();
+                finish_step(r, g, g >= 2 && !kEarly, true, rb, C::bytes(V, dslot));
             }
             if (!ok)
                 break;
-            // ---- refill the consumed stage and advance the shared counters
-            if (FAST && rs_part) {
-                __syncwarp();
-                if (issued == consumed + D && cur_item < a.tiles) {
-                    if (lane == 0)
-                        for (int r = warp; r < N; r += W)
-                            issue_one(r, stg.slot);
-                    ++issued;
-                    cursor_next();
-                }
-                ++consumed;
-                stg.advance(D);
-            }
-            if (do_recv)
+            stage_step();
+            if (g >= 2)
                 rcv.advance(K);
-            if (do_send)
-                snd.advance(K);
+            snd.advance(K);
+        }
+        if (!ok)
+            break;
+
+        // ---- owner step g = N: chunk r; allreduce encodes the full sum once
+        for (int r = warp; r < N; r += W) {
+            const int V = slice_len(r, t0);
+            const int dst = r + 1 == N ? 0 : r + 1;
+            const bool recv = N > 1, send = allred && N > 1;
+            if (FAST && !waits_ok(wait_ready(sbar + r * D + stg.slot, (uint32_t)stg.phase,
+                                             a.timeout_ns, a.status)))
+                break;
+            if (recv && !waits_ok(wait_ready(full + r * K + rcv.slot, (uint32_t)rcv.phase,
+                                             a.timeout_ns, a.status)))
+                break;
+            const unsigned char *sp = stages + (size_t)(r * D + stg.slot) * a.stage_bytes;
+            const unsigned char *rslot = slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
+            const uint32_t rb = recv ? C::bytes(V, rslot) : 0u;
+            Reg m0;
+            if (kEarly && recv)
+                release_early(r, rslot, rb, m0);
+            if (send && !waits_ok(wait_ready(empty + dst * K + snd.slot,
+                                             (uint32_t)(snd.phase ^ 1), a.timeout_ns, a.status)))
+                break;
+            // N = 1 has no allgather step: encode into the rank's own (unused) slot
+            unsigned char *dslot = send ? slots + (size_t)(dst * K + snd.slot) * a.slot_bytes
+                                        : slots + (size_t)(r * K) * a.slot_bytes;
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+                float v[8];
+                input_group(r, r, V, gi, sp, v);
+                if (recv) {
+                    Reg m;
+                    if (kEarly)
+                        m = m0;
+                    else
+                        C::load(rslot, gi, lane, m);
+                    C::decode_add(m, v, lane, scratch);
+                }
+                if (allred)
+                    C::template encode<true>(v, dslot, gi, lane, V, a.one_minus_thr, scratch);
+                output_group(r, r, V, gi, v);
+            }
+            __syncwarp();
+            finish_step(r, N, recv && !kEarly, send, rb, send ? C::bytes(V, dslot) : 0u);
+        }
+        if (!ok)
+            break;
+        stage_step();
+        if (N > 1)
+            rcv.advance(K);
+        if (allred && N > 1)
+            snd.advance(K);
+
+        // ---- allgather steps g = N+1..2N-1: output chunk (r-g) mod N, forward its codes
+        if (allred) {
+            for (int g = N + 1; ok && g <= 2 * N - 1; ++g) {
+                const bool fwd = g < 2 * N - 1;
+                for (int r = warp; r < N; r += W) {
+                    int c = r - g;
+                    c += c < 0 ? N : 0;
+                    c += c < 0 ? N : 0;
+                    const int V = slice_len(c, t0);
+                    const int dst = r + 1 == N ? 0 : r + 1;
+                    if (!waits_ok(wait_ready(full + r * K + rcv.slot, (uint32_t)rcv.phase,
+                                             a.timeout_ns, a.status)))
+                        break;
+                    const unsigned char *rslot =
+                        slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
+                    const uint32_t rb = C::bytes(V, rslot);
+                    Reg m0;
+                    if (kEarly)
+                        release_early(r, rslot, rb, m0);
+                    if (fwd && !waits_ok(wait_ready(empty + dst * K + snd.slot,
+                                                    (uint32_t)(snd.phase ^ 1), a.timeout_ns,
+                                                    a.status)))
+                        break;
+                    unsigned char *dslot = slots + (size_t)(dst * K + snd.slot) * a.slot_bytes;
+#pragma unroll
+                    for (int gi = 0; gi < G; ++gi) {
+                        Reg m;
+                        if (kEarly)
+                            m = m0;
+                        else
+                            C::load(rslot, gi, lane, m);
+                        if (fwd)
+                            C::store(dslot, gi, lane, m);
+                        float v[8];
+                        C::values(m, v, lane, scratch);
+                        output_group(r, c, V, gi, v);
+                    }
+                    __syncwarp();
+                    finish_step(r, g, !kEarly, fwd, rb, rb);
+                }
+                if (!ok)
+                    break;
+                rcv.advance(K);
+                if (fwd)
+                    snd.advance(K);
+            }
         }
     }
 

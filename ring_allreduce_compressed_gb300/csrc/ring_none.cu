@@ -30,6 +30,17 @@ const void *ring_fn_none(int codec, int in_t, bool fast, int groups)
             return fast ? (const void *)ring_kernel<kCodecNone, kBF16, true, 2>
                         : (const void *)ring_kernel<kCodecNone, kBF16, false, 2>;
     }
+    if (codec == kCodecNone && groups == 4) {
+        if (in_t == kF32)
+            return fast ? (const void *)ring_kernel<kCodecNone, kF32, true, 4>
+                        : (const void *)ring_kernel<kCodecNone, kF32, false, 4>;
+        if (in_t == kF16)
+            return fast ? (const void *)ring_kernel<kCodecNone, kF16, true, 4>
+                        : (const void *)ring_kernel<kCodecNone, kF16, false, 4>;
+        if (in_t == kBF16)
+            return fast ? (const void *)ring_kernel<kCodecNone, kBF16, true, 4>
+                        : (const void *)ring_kernel<kCodecNone, kBF16, false, 4>;
+    }
     return nullptr;
 }
 

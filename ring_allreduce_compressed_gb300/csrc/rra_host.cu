@@ -36,6 +36,7 @@ struct rra_comm {
     cudaStream_t last_stream = nullptr;
     bool have_last = false;
     int smem_optin = 0;
+    int smem_per_sm = 0;
     int tune_blocks = 0; // 0: automatic
     int tune_K = 0;
     int tune_D = 0;
@@ -154,6 +155,47 @@ int slot_bytes_for(int codec, int groups)
     }
 }
 
+// Slice width (groups of 8 elements per lane) and staging depth: wider
+// slices amortise each step's handshakes over more elements; the first
+// candidate that leaves room for three resident blocks per SM wins, else
+// the first that fits at all.
+struct LaunchShape {
+    int groups, K, D, smem;
+    bool fast;
+};
+
+bool pick_shape(rra_comm *c, int N, int kc, int ies, bool diff, bool fast, int warps,
+                LaunchShape *out)
+{
+    static const int kGD[][2] = {{4, 2}, {4, 1}, {2, 4}, {2, 2}, {1, 4}, {1, 2}, {1, 1}};
+    const bool sparse = kc == kCodecSparse;
+    for (int pass = 0; pass < 2; ++pass) {
+        for (const auto &gd : kGD) {
+            const int G = gd[0];
+            int D = c->tune_D ? c->tune_D : gd[1];
+            if (sparse && G != 1)
+                continue;
+            if (!fast)
+                D = 1;
+            const int slot = slot_bytes_for(kc, G);
+            const int stage = kTile * G * (diff ? 8 : ies);
+            // wider messages need two slots per ring edge: a rank frees the
+            // slot it streams from only after its own send of the same step,
+            // so with one slot every rank would wait for its successor
+            for (int K = c->tune_K ? c->tune_K : 2; K >= (G == 1 ? 1 : 2); --K) {
+                const Layout L = make_layout(N, K, D, slot, stage, warps, fast, sparse);
+                const int need = pass == 0 ? 3 * (L.total + 1024) : L.total;
+                const int have = pass == 0 ? c->smem_per_sm : c->smem_optin;
+                if (need <= have && L.total <= c->smem_optin) {
+                    *out = LaunchShape{G, K, D, L.total, fast};
+                    return true;
+                }
+            }
+        }
+    }
+    return false;
+}
+
 rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *const *out,
                        size_t count, rra_dtype in_t, rra_dtype out_t, const rra_codec *codec,
                        void *stream)
@@ -252,27 +294,17 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     a.vec_base = (cd.diff_base && al16(cd.diff_base) && (a.n * 4) % 16 == 0) ? 1 : 0;
 
     const int warps = warps_for(N);
-    // Slice width: two groups of 8 elements per lane (512 per step) where the
-    // shared memory allows it, else one; the sparse codec's message slice is
-    // always 256 elements.
-    int groups = 0, smem = 0;
-    for (int gsel = (kc == kCodecSparse ? 1 : 2); gsel >= 1 && !groups; --gsel) {
-        a.slot_bytes = slot_bytes_for(kc, gsel);
-        a.stage_bytes = kTile * gsel * (cd.diff_prev ? 8 : (int)ies);
-        if (pick_depths(comm, N, a.slot_bytes, a.stage_bytes, warps, fast, kc == kCodecSparse, 0,
-                        &a.K, &a.D, &smem) &&
-            (gsel == 1 || a.D >= 2))
-            groups = gsel;
-    }
-    if (!groups) {
+    LaunchShape sh;
+    if (!pick_shape(comm, N, kc, (int)ies, cd.diff_prev != nullptr, fast, warps, &sh)) {
         fast = false;
-        groups = 1;
-        a.slot_bytes = slot_bytes_for(kc, 1);
-        a.stage_bytes = kTile * (cd.diff_prev ? 8 : (int)ies);
-        if (!pick_depths(comm, N, a.slot_bytes, a.stage_bytes, warps, false, kc == kCodecSparse, 0,
-                         &a.K, &a.D, &smem))
+        if (!pick_shape(comm, N, kc, (int)ies, cd.diff_prev != nullptr, false, warps, &sh))
             return RRA_ERR_UNSUPPORTED;
     }
+    const int groups = sh.groups, smem = sh.smem;
+    a.K = sh.K;
+    a.D = sh.D;
+    a.slot_bytes = slot_bytes_for(kc, groups);
+    a.stage_bytes = kTile * groups * (cd.diff_prev ? 8 : (int)ies);
     a.tiles = (a.n + kTile * groups - 1) / (kTile * groups);
     const void *fn = ring_fn(kc, in_t, fast, groups);
     if (!fn)
@@ -411,6 +443,7 @@ rra_status rra_comm_create(int nranks, size_t max_count, rra_dtype max_dtype, rr
         return RRA_ERR_CUDA;
     }
     cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+    cudaDeviceGetAttribute(&c->smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, c->device);
     const size_t cbytes = sizeof(unsigned long long) * 4 * (size_t)nranks;
     if (cudaMalloc(&c->counters, cbytes) != cudaSuccess) {
         delete c;
