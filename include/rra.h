@@ -325,11 +325,13 @@ rra_status rra_set_timeout(rra_comm *comm, uint64_t ns);
  *                 than 256 elements always use at least 2, because a rank
  *                 frees the slot it streams from only after its own send).
  *  stage_depth    input slices each rank stages ahead with bulk copies (1..16).
- * Depths that do not fit the shared memory are reduced automatically.
- * Errors: RRA_ERR_INVALID for NULL or values out of range.
+ *  slice_groups   elements per ring message in units of 256 (1, 2, 4 or 8;
+ *                 the sparse codec always uses 1).
+ * Depths and widths that do not fit the shared memory are reduced
+ * automatically.  Errors: RRA_ERR_INVALID for NULL or values out of range.
  */
 rra_status rra_comm_set_tuning(rra_comm *comm, int blocks_per_sm, int mailbox_depth,
-                               int stage_depth);
+                               int stage_depth, int slice_groups);
 
 /* Test-only fault injection: in the next collective call, simulated rank
  * "rank" does not publish the message it sends at ring step "step" (1-based,

@@ -74,7 +74,7 @@ def lib():
         L.rra_comm_status.argtypes = [vp]
         L.rra_set_timeout.argtypes = [vp, C.c_uint64]
         L.rra_debug_withhold.argtypes = [vp, i32, i32]
-        L.rra_comm_set_tuning.argtypes = [vp, i32, i32, i32]
+        L.rra_comm_set_tuning.argtypes = [vp, i32, i32, i32, i32]
         L.rra_status_string.argtypes = [i32]
         L.rra_status_string.restype = C.c_char_p
         for name in ("rra_comm_create", "rra_comm_destroy", "rra_ring_allreduce",
@@ -212,10 +212,11 @@ class Comm:
     def set_timeout(self, ns: int):
         _check(lib().rra_set_timeout(self._h, int(ns)), "rra_set_timeout")
 
-    def set_tuning(self, blocks_per_sm: int = 0, mailbox_depth: int = 0, stage_depth: int = 0):
+    def set_tuning(self, blocks_per_sm: int = 0, mailbox_depth: int = 0, stage_depth: int = 0,
+                   slice_groups: int = 0):
         """Launch tuning of the fused kernels (0 = automatic)."""
-        _check(lib().rra_comm_set_tuning(self._h, blocks_per_sm, mailbox_depth, stage_depth),
-               "rra_comm_set_tuning")
+        _check(lib().rra_comm_set_tuning(self._h, blocks_per_sm, mailbox_depth, stage_depth,
+                                         slice_groups), "rra_comm_set_tuning")
 
     def debug_withhold(self, rank: int, step: int):
         _check(lib().rra_debug_withhold(self._h, rank, step), "rra_debug_withhold")

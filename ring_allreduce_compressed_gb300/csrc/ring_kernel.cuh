@@ -62,13 +62,17 @@ template <int BITS> struct BfpGroup {
     // w[0..1] = 8 bytes (BITS 8) or w[0] = 8 nibbles (BITS 4).
     __device__ __forceinline__ static void encode(const float v[8], int &e, uint32_t w[2])
     {
-        float amax = 0.0f;
+        float lmax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            amax = fmaxf(amax, fabsf(v[i]));
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+            lmax = fmaxf(lmax, fabsf(v[i]));
+        // half-warp maximum: non-negative floats order like their bit patterns,
+        // so two warp-wide unsigned max reductions (one per half) give it
+        const unsigned lane = threadIdx.x & 31u;
+        const unsigned bits = __float_as_uint(lmax);
+        const unsigned lo = __reduce_max_sync(kFull, lane < 16 ? bits : 0u);
+        const unsigned hi = __reduce_max_sync(kFull, lane < 16 ? 0u : bits);
+        const float amax = __uint_as_float(lane < 16 ? lo : hi);
         e = bfp_exponent(amax);
         int k = q - e;
         float x[8];
@@ -84,7 +88,7 @@ template <int BITS> struct BfpGroup {
             for (int i = 0; i < 8; ++i)
                 x[i] = v[i];
         }
-        const float s = pow2i(k);
+        const float s = __int_as_float((k + 127) << 23); // k in [q-127, 127]: a normal 2^k
         float t[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -496,7 +500,9 @@ __device__ __forceinline__ bool wait_ready(uint64_t *bar, uint32_t parity, uint6
     return wait_slow(bar, parity, limit_ns, status);
 }
 
-template <int CODEC, int IN_T, bool FAST, int G>
+// ONE: every warp plays exactly one rank (N <= warps per block), so rank
+// indices, addresses and byte counts stay in registers across the loops.
+template <int CODEC, int IN_T, bool FAST, int G, bool ONE>
 __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_constant__ RingArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -539,6 +545,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
 
     const bool allred = a.mode == kModeAllreduce;
     const long long n = a.n, T = a.T;
+    const int rstride = ONE ? N : W; // rank loop stride: one iteration when ONE
+    unsigned long long my_sent = 0, my_recv = 0; // ONE: this warp's rank's bytes
     // shortest chunk: every slice position below it is full in every chunk
     const long long min_len = T - (long long)(N - 1) * n;
 
@@ -589,7 +597,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
     if constexpr (FAST) {
         while (issued < D && cur_item < a.tiles) {
             if (lane == 0)
-                for (int r = warp; r < N; r += W)
+                for (int r = warp; r < N; r += rstride)
                     issue_one(r, (int)issued);
             ++issued;
             cursor_next();
@@ -636,8 +644,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
     // output epilogue of group gi: average, previous-round base, cast
     const float inv_n = ((N & (N - 1)) == 0) ? 1.0f / (float)N : 0.0f; // exact for powers of two
     const int out_t = a.out_t;
+    const bool plain_out = !a.average && !a.base && a.vec_out;
     auto output_group = [&](int r, int c, int V, int gi, float (&v)[8]) {
         const long long e0 = (long long)c * n + t0 + gi * kTile + 8 * lane;
+        if (plain_out && V == TW) { // full slice, no epilogue arithmetic: vector store
+            store8(reinterpret_cast<char *>(a.out[r]) + e0 * dtype_size(out_t), out_t, v, 8,
+                   true);
+            return;
+        }
         const int vl = V == TW ? 8 : min(max(V - gi * kTile - 8 * lane, 0), 8);
         if (a.average) {
 #pragma unroll
@@ -668,10 +682,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
     constexpr bool kEarly = G == 1;
     auto release_early = [&](int r, const unsigned char *rslot, uint32_t rb, Reg &m) {
         C::load(rslot, 0, lane, m);
+        if (ONE)
+            my_recv += rb;
         __syncwarp();
         if (lane == 0) {
             mbar_arrive(empty + r * K + rcv.slot);
-            rrecv[r] += rb;
+            if (!ONE)
+                rrecv[r] += rb;
         }
     };
     // after a step that consumed a staged load: refill that stage
@@ -680,7 +697,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
             __syncwarp();
             if (issued == consumed + D && cur_item < a.tiles) {
                 if (lane == 0)
-                    for (int r = warp; r < N; r += W)
+                    for (int r = warp; r < N; r += rstride)
                         issue_one(r, stg.slot);
                 ++issued;
                 cursor_next();
@@ -691,18 +708,24 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
     };
     // publish: free the receive slot (if any), mark the sent message full
     auto finish_step = [&](int r, int g, bool recv, bool send, uint32_t rb, uint32_t sb) {
+        if (ONE) {
+            my_recv += recv ? rb : 0u;
+            my_sent += send ? sb : 0u;
+        }
         __syncwarp();
         if (lane == 0) {
             if (recv) {
                 mbar_arrive(empty + r * K + rcv.slot);
-                rrecv[r] += rb;
+                if (!ONE)
+                    rrecv[r] += rb;
             }
             if (send) {
                 const int dst = r + 1 == N ? 0 : r + 1;
                 if (!(first_item_withhold && r == a.withhold_rank && g == a.withhold_step &&
                       t0 == (long long)blockIdx.x * TW))
                     mbar_arrive(full + dst * K + snd.slot);
-                rsent[r] += sb;
+                if (!ONE)
+                    rsent[r] += sb;
             }
         }
     };
@@ -712,7 +735,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
 
         // ---- reduce-scatter steps g = 1..N-1: send chunk (r-g) mod N
         for (int g = 1; ok && g < N; ++g) {
-            for (int r = warp; r < N; r += W) {
+            for (int r = warp; r < N; r += rstride) {
                 int c = r - g;
                 c += c < 0 ? N : 0;
                 const int V = slice_len(c, t0);
@@ -764,7 +787,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
             break;
 
         // ---- owner step g = N: chunk r; allreduce encodes the full sum once
-        for (int r = warp; r < N; r += W) {
+        for (int r = warp; r < N; r += rstride) {
             const int V = slice_len(r, t0);
             const int dst = r + 1 == N ? 0 : r + 1;
             const bool recv = N > 1, send = allred && N > 1;
@@ -817,7 +840,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
         if (allred) {
             for (int g = N + 1; ok && g <= 2 * N - 1; ++g) {
                 const bool fwd = g < 2 * N - 1;
-                for (int r = warp; r < N; r += W) {
+                for (int r = warp; r < N; r += rstride) {
                     int c = r - g;
                     c += c < 0 ? N : 0;
                     c += c < 0 ? N : 0;
@@ -870,13 +893,23 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
                 drain_phase(sbar + r * D + (int)(L % D), (uint32_t)((L / D) & 1), a.timeout_ns);
     }
     // ---- per-rank byte counters
-    if (lane == 0)
-        for (int r = warp; r < N; r += W) {
-            if (rsent[r])
-                atomicAdd(a.sent + r, rsent[r]);
-            if (rrecv[r])
-                atomicAdd(a.recv + r, rrecv[r]);
+    if (lane == 0) {
+        if (ONE) {
+            if (warp < N) {
+                if (my_sent)
+                    atomicAdd(a.sent + warp, my_sent);
+                if (my_recv)
+                    atomicAdd(a.recv + warp, my_recv);
+            }
+        } else {
+            for (int r = warp; r < N; r += W) {
+                if (rsent[r])
+                    atomicAdd(a.sent + r, rsent[r]);
+                if (rrecv[r])
+                    atomicAdd(a.recv + r, rrecv[r]);
+            }
         }
+    }
 }
 
 } // namespace rra

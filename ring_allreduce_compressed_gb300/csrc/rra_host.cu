@@ -15,9 +15,10 @@
 #include "rra_kernels.h"
 
 namespace rra {
-const void *ring_fn_none(int codec, int in_t, bool fast, int groups);
-const void *ring_fn_bfp(int codec, int in_t, bool fast, int groups);
-const void *ring_fn_sparse(int codec, int in_t, bool fast, int groups);
+const void *ring_fn_none(int codec, int in_t, bool fast, int groups, bool one);
+const void *ring_fn_bfp8(int codec, int in_t, bool fast, int groups, bool one);
+const void *ring_fn_bfp4(int codec, int in_t, bool fast, int groups, bool one);
+const void *ring_fn_sparse(int codec, int in_t, bool fast, int groups, bool one);
 } // namespace rra
 
 using namespace rra;
@@ -40,6 +41,7 @@ struct rra_comm {
     int tune_blocks = 0; // 0: automatic
     int tune_K = 0;
     int tune_D = 0;
+    int tune_G = 0;
     std::map<long long, int> occ; // (kernel key, smem) -> blocks per SM
 };
 
@@ -135,13 +137,15 @@ int grid_for(rra_comm *c, long long key, const void *fn, int warps, int smem, lo
     return (int)std::max(1LL, g);
 }
 
-const void *ring_fn(int codec, int in_t, bool fast, int groups)
+const void *ring_fn(int codec, int in_t, bool fast, int groups, bool one)
 {
     if (codec == kCodecNone)
-        return ring_fn_none(codec, in_t, fast, groups);
+        return ring_fn_none(codec, in_t, fast, groups, one);
     if (codec == kCodecSparse)
-        return ring_fn_sparse(codec, in_t, fast, groups);
-    return ring_fn_bfp(codec, in_t, fast, groups);
+        return ring_fn_sparse(codec, in_t, fast, groups, one);
+    if (codec == kCodecBfp8)
+        return ring_fn_bfp8(codec, in_t, fast, groups, one);
+    return ring_fn_bfp4(codec, in_t, fast, groups, one);
 }
 
 // Bytes of one mailbox slot for a slice of 256 * groups elements.
@@ -167,11 +171,16 @@ struct LaunchShape {
 bool pick_shape(rra_comm *c, int N, int kc, int ies, bool diff, bool fast, int warps,
                 LaunchShape *out)
 {
-    static const int kGD[][2] = {{4, 2}, {4, 1}, {2, 4}, {2, 2}, {1, 4}, {1, 2}, {1, 1}};
+    static const int kGD[][2] = {{8, 2}, {8, 1}, {4, 2}, {4, 1}, {2, 4},
+                                 {2, 2}, {1, 4}, {1, 2}, {1, 1}};
     const bool sparse = kc == kCodecSparse;
-    for (int pass = 0; pass < 2; ++pass) {
+    // a requested slice width is tried first on its own; passes 2 and 3 are
+    // the automatic choice
+    for (int pass = c->tune_G && !sparse ? 0 : 2; pass < 4; ++pass) {
         for (const auto &gd : kGD) {
             const int G = gd[0];
+            if (pass < 2 && G != c->tune_G)
+                continue;
             int D = c->tune_D ? c->tune_D : gd[1];
             if (sparse && G != 1)
                 continue;
@@ -184,8 +193,9 @@ bool pick_shape(rra_comm *c, int N, int kc, int ies, bool diff, bool fast, int w
             // so with one slot every rank would wait for its successor
             for (int K = c->tune_K ? c->tune_K : 2; K >= (G == 1 ? 1 : 2); --K) {
                 const Layout L = make_layout(N, K, D, slot, stage, warps, fast, sparse);
-                const int need = pass == 0 ? 3 * (L.total + 1024) : L.total;
-                const int have = pass == 0 ? c->smem_per_sm : c->smem_optin;
+                const bool three = pass % 2 == 0; // leave room for three blocks per SM
+                const int need = three ? 3 * (L.total + 1024) : L.total;
+                const int have = three ? c->smem_per_sm : c->smem_optin;
                 if (need <= have && L.total <= c->smem_optin) {
                     *out = LaunchShape{G, K, D, L.total, fast};
                     return true;
@@ -306,10 +316,12 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     a.slot_bytes = slot_bytes_for(kc, groups);
     a.stage_bytes = kTile * groups * (cd.diff_prev ? 8 : (int)ies);
     a.tiles = (a.n + kTile * groups - 1) / (kTile * groups);
-    const void *fn = ring_fn(kc, in_t, fast, groups);
+    const bool one = warps == N; // every warp plays exactly one rank
+    const void *fn = ring_fn(kc, in_t, fast, groups, one);
     if (!fn)
         return RRA_ERR_UNSUPPORTED;
-    const long long key = 10000 + kc * 1000 + in_t * 100 + (fast ? 10 : 0) + groups;
+    const long long key = 100000 + kc * 10000 + in_t * 1000 + (fast ? 100 : 0) +
+                          (one ? 10 : 0) + groups;
     const int grid = grid_for(comm, key, fn, warps, smem, a.tiles);
     counter_sets(comm, &a.sent, &a.recv, &a.zero);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -637,14 +649,17 @@ rra_status rra_set_timeout(rra_comm *comm, uint64_t ns)
 }
 
 rra_status rra_comm_set_tuning(rra_comm *comm, int blocks_per_sm, int mailbox_depth,
-                               int stage_depth)
+                               int stage_depth, int slice_groups)
 {
     if (!comm || blocks_per_sm < 0 || blocks_per_sm > 32 || mailbox_depth < 0 ||
-        mailbox_depth > 8 || stage_depth < 0 || stage_depth > 16)
+        mailbox_depth > 8 || stage_depth < 0 || stage_depth > 16 ||
+        !(slice_groups == 0 || slice_groups == 1 || slice_groups == 2 || slice_groups == 4 ||
+          slice_groups == 8))
         return RRA_ERR_INVALID;
     comm->tune_blocks = blocks_per_sm;
     comm->tune_K = mailbox_depth;
     comm->tune_D = stage_depth;
+    comm->tune_G = slice_groups;
     return RRA_OK;
 }
 
