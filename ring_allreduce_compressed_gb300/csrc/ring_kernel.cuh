@@ -90,9 +90,13 @@ template <int BITS> struct BfpGroup {
         }
         const float s = __int_as_float((k + 127) << 23); // k in [q-127, 127]: a normal 2^k
         float t[8];
+        const float2 s2 = make_float2(s, s), c2 = make_float2(kMagic, kMagic);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            t[i] = __fmaf_rn(x[i], s, kMagic);
+        for (int i = 0; i < 8; i += 2) { // paired fp32 fma: two IEEE fmas per instruction
+            const float2 r = __ffma2_rn(make_float2(x[i], x[i + 1]), s2, c2);
+            t[i] = r.x;
+            t[i + 1] = r.y;
+        }
         if (__fmul_rn(ax, s) >= (float)M + 0.5f) { // some value rounds past the clamp
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -119,48 +123,64 @@ template <int BITS> struct BfpGroup {
         }
     }
 
-    // m_i as exact floats.
-    __device__ __forceinline__ static void codes(const uint32_t w[2], float mf[8])
+    // m_i as exact floats, in pairs (element 2j in .x, 2j+1 in .y).
+    __device__ __forceinline__ static void codes(const uint32_t w[2], float2 mf[4])
     {
         constexpr float off = kMagic + (float)(1 << (BITS - 1));
+        const float2 off2 = make_float2(-off, -off);
         if constexpr (BITS == 8) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const uint32_t x = w[h] ^ 0x80808080u;
-                mf[4 * h + 0] = __uint_as_float(__byte_perm(x, kMagicBits, 0x7640)) - off;
-                mf[4 * h + 1] = __uint_as_float(__byte_perm(x, kMagicBits, 0x7641)) - off;
-                mf[4 * h + 2] = __uint_as_float(__byte_perm(x, kMagicBits, 0x7642)) - off;
-                mf[4 * h + 3] = __uint_as_float(__byte_perm(x, kMagicBits, 0x7643)) - off;
+                mf[2 * h + 0] = __fadd2_rn(
+                    make_float2(__uint_as_float(__byte_perm(x, kMagicBits, 0x7640)),
+                                __uint_as_float(__byte_perm(x, kMagicBits, 0x7641))),
+                    off2);
+                mf[2 * h + 1] = __fadd2_rn(
+                    make_float2(__uint_as_float(__byte_perm(x, kMagicBits, 0x7642)),
+                                __uint_as_float(__byte_perm(x, kMagicBits, 0x7643))),
+                    off2);
             }
         } else {
             const uint32_t x = w[0] ^ 0x88888888u;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                mf[i] = __uint_as_float(((x >> (4 * i)) & 0xfu) | kMagicBits) - off;
+            for (int j = 0; j < 4; ++j)
+                mf[j] = __fadd2_rn(
+                    make_float2(__uint_as_float(((x >> (8 * j)) & 0xfu) | kMagicBits),
+                                __uint_as_float(((x >> (8 * j + 4)) & 0xfu) | kMagicBits)),
+                    off2);
         }
     }
 
     // Decoded values m_i * 2^(e-q) (exact).
     __device__ __forceinline__ static void decode(const uint32_t w[2], int e, float out[8])
     {
-        float mf[8];
+        float2 mf[4];
         codes(w, mf);
         const float s = pow2i(e - q);
+        const float2 s2 = make_float2(s, s);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            out[i] = __fmul_rn(mf[i], s);
+        for (int j = 0; j < 4; ++j) {
+            const float2 r = __fmul2_rn(mf[j], s2);
+            out[2 * j] = r.x;
+            out[2 * j + 1] = r.y;
+        }
     }
 
     // acc_i = x_i + m_i * 2^(e-q) with one rounding (the product is exact).
     __device__ __forceinline__ static void decode_add(const uint32_t w[2], int e, const float x[8],
                                                       float acc[8])
     {
-        float mf[8];
+        float2 mf[4];
         codes(w, mf);
         const float s = pow2i(e - q);
+        const float2 s2 = make_float2(s, s);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            acc[i] = __fmaf_rn(mf[i], s, x[i]);
+        for (int j = 0; j < 4; ++j) {
+            const float2 r = __ffma2_rn(mf[j], s2, make_float2(x[2 * j], x[2 * j + 1]));
+            acc[2 * j] = r.x;
+            acc[2 * j + 1] = r.y;
+        }
     }
 };
 
@@ -214,8 +234,12 @@ template <> struct WireCodec<kCodecNone> {
                                                       unsigned char *)
     {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            v[i] = __fadd_rn(v[i], m.f[i]);
+        for (int i = 0; i < 8; i += 2) {
+            const float2 r =
+                __fadd2_rn(make_float2(v[i], v[i + 1]), make_float2(m.f[i], m.f[i + 1]));
+            v[i] = r.x;
+            v[i + 1] = r.y;
+        }
     }
     __device__ __forceinline__ static void values(const Reg &m, float (&v)[8], int,
                                                   unsigned char *)
