@@ -152,11 +152,16 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, an earlier GB300 copy measurement)"
 
 
+# the files the ring kernels are compiled from (host-side launch code excluded)
+RING_KERNEL_SOURCES = ("ring_kernel.cuh", "rra_device.cuh", "rra_kernels.h", "ring_none.cu",
+                       "ring_bfp8.cu", "ring_bfp4.cu", "ring_sparse.cu")
+
+
 def kernel_sources_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ring_allreduce_compressed_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name in RING_KERNEL_SOURCES:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -510,18 +515,43 @@ def run_sweep(args, world, rank):
                 for _ in range(5):
                     fn()
                 torch.cuda.synchronize()
-                reps = 20 if N * T * 4 < 2 ** 33 else 5
-                times = []
-                for _ in range(reps):
-                    a = torch.cuda.Event(enable_timing=True)
-                    b = torch.cuda.Event(enable_timing=True)
-                    a.record()
-                    fn()
-                    b.record()
-                    b.synchronize()
-                    times.append(a.elapsed_time(b) * 1e3)
                 sent, recv = comm.get_bytes()
                 assert comm.status() == rra.RRA_OK
+                reps = 20 if N * T * 4 < 2 ** 33 else 5
+                times = []
+                if N * T * 4 <= 2 ** 26:
+                    # small messages: replay a CUDA graph of 20 back-to-back calls
+                    # so that the host's launch cost is not part of the time
+                    graph = torch.cuda.CUDAGraph()
+                    s = torch.cuda.Stream()
+                    s.wait_stream(torch.cuda.current_stream())
+                    with torch.cuda.stream(s):
+                        with torch.cuda.graph(graph, stream=s):
+                            for _ in range(20):
+                                fn()
+                    torch.cuda.current_stream().wait_stream(s)
+                    graph.replay()
+                    torch.cuda.synchronize()
+                    for _ in range(reps):
+                        a = torch.cuda.Event(enable_timing=True)
+                        b = torch.cuda.Event(enable_timing=True)
+                        a.record()
+                        graph.replay()
+                        b.record()
+                        b.synchronize()
+                        times.append(a.elapsed_time(b) * 1e3 / 20)
+                    del graph
+                    assert comm.status() == rra.RRA_OK
+                else:
+                    for _ in range(reps):
+                        a = torch.cuda.Event(enable_timing=True)
+                        b = torch.cuda.Event(enable_timing=True)
+                        a.record()
+                        fn()
+                        b.record()
+                        b.synchronize()
+                        times.append(a.elapsed_time(b) * 1e3)
+                    assert comm.status() == rra.RRA_OK
                 us = statistics.median(times)
                 res[op] = us
                 line = {"sweep": True, "op": op, "N": N, "T": T, "bytes_per_rank": T * 4,
