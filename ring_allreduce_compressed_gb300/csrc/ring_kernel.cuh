@@ -208,7 +208,7 @@ template <> struct WireCodec<kCodecNone> {
         float f[8];
     };
     __device__ __forceinline__ static void load(const unsigned char *slot, int gi, int lane,
-                                                Reg &m)
+                                                unsigned char *, Reg &m)
     {
         const float4 *p = reinterpret_cast<const float4 *>(slot + gi * kTile * 4) + 2 * lane;
         const float4 a = p[0], b = p[1];
@@ -224,7 +224,8 @@ template <> struct WireCodec<kCodecNone> {
     }
     template <bool DEC>
     __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int gi,
-                                                  int lane, int, double, unsigned char *)
+                                                  int lane, int, const RingArgs &,
+                                                  unsigned char *)
     {
         float4 *p = reinterpret_cast<float4 *>(slot + gi * kTile * 4) + 2 * lane;
         p[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -267,7 +268,7 @@ template <int BITS> struct CodecBfp {
         int e;
     };
     __device__ __forceinline__ static void load(const unsigned char *slot, int gi, int lane,
-                                                Reg &m)
+                                                unsigned char *, Reg &m)
     {
         m.e = (int)(int8_t)slot[2 * gi + (lane >> 4)];
         if constexpr (BITS == 8) {
@@ -291,7 +292,8 @@ template <int BITS> struct CodecBfp {
     }
     template <bool DEC>
     __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int gi,
-                                                  int lane, int, double, unsigned char *)
+                                                  int lane, int, const RingArgs &,
+                                                  unsigned char *)
     {
         Reg m;
         BfpGroup<BITS>::encode(v, m.e, m.w);
@@ -320,15 +322,17 @@ template <> struct WireCodec<kCodecBfp4> : CodecBfp<4> {};
 // Sparse values + indices: one 256-element slice per message (G = 1).
 // Slot: {uint32 fmt, uint32 nnz} padded to 16 bytes, fp32 values[256],
 // int32 indices[256] (slice-relative, ascending).  Dense fallback: fmt 0,
-// values[0..len) in place.  Compaction: per-lane nonzero masks and a warp
+// values[0..len) in place.  Compaction: per-lane presence masks and a warp
 // inclusive scan of their popcounts give every lane's first output position.
+// A received message is held in registers in its decoded form: the lane's 8
+// values (+0.0 where the message has none) and a presence mask, from which
+// the identical message can be written again when it is forwarded.
 template <> struct WireCodec<kCodecSparse> {
     static constexpr bool kSliced = false; // the message is exactly one 256-element slice
     static constexpr int slot_bytes(int) { return 16 + kTile * 8; }
     struct Reg {
-        uint32_t fmt, nnz;
+        uint32_t fmt, nnz, pres;
         float f[8];
-        int ix[8];
     };
     __device__ __forceinline__ static float *vals(unsigned char *s)
     {
@@ -343,69 +347,13 @@ template <> struct WireCodec<kCodecSparse> {
         const uint2 h = *reinterpret_cast<const uint2 *>(slot);
         return V == 0 ? 0u : 8u + (h.x ? 8u * h.y : 4u * (uint32_t)V);
     }
-    __device__ __forceinline__ static void load(const unsigned char *slot, int, int lane, Reg &m)
+    // Write the message whose lane values are v and whose present positions
+    // are the bits of nzm: sparse (ascending indices) when fmt is set, dense
+    // otherwise.  Warp-collective.
+    __device__ __forceinline__ static void emit(unsigned char *slot, int lane, const float (&v)[8],
+                                                uint32_t nzm, uint32_t fmt, int cnt, int incl,
+                                                int total)
     {
-        const uint2 h = *reinterpret_cast<const uint2 *>(slot);
-        m.fmt = h.x;
-        m.nnz = h.y;
-        unsigned char *s = const_cast<unsigned char *>(slot);
-        if (!m.fmt) {
-            const float4 *p = reinterpret_cast<const float4 *>(vals(s)) + 2 * lane;
-            const float4 a = p[0], b = p[1];
-            m.f[0] = a.x; m.f[1] = a.y; m.f[2] = a.z; m.f[3] = a.w;
-            m.f[4] = b.x; m.f[5] = b.y; m.f[6] = b.z; m.f[7] = b.w;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int k = lane + 32 * i;
-                if (k < (int)m.nnz) {
-                    m.f[i] = vals(s)[k];
-                    m.ix[i] = idxs(s)[k];
-                }
-            }
-        }
-    }
-    __device__ __forceinline__ static void store(unsigned char *slot, int, int lane, const Reg &m)
-    {
-        if (lane == 0)
-            *reinterpret_cast<uint2 *>(slot) = make_uint2(m.fmt, m.nnz);
-        if (!m.fmt) {
-            float4 *p = reinterpret_cast<float4 *>(vals(slot)) + 2 * lane;
-            p[0] = make_float4(m.f[0], m.f[1], m.f[2], m.f[3]);
-            p[1] = make_float4(m.f[4], m.f[5], m.f[6], m.f[7]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int k = lane + 32 * i;
-                if (k < (int)m.nnz) {
-                    vals(slot)[k] = m.f[i];
-                    idxs(slot)[k] = m.ix[i];
-                }
-            }
-        }
-    }
-    // the receiver restores every value exactly (absent ones are +0.0), so the
-    // decoded values are v itself: DEC changes nothing
-    template <bool DEC>
-    __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int,
-                                                  int lane, int V, double one_minus_thr,
-                                                  unsigned char *)
-    {
-        uint32_t nzm = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (8 * lane + i < V && __float_as_uint(v[i]) != 0u)
-                nzm |= 1u << i;
-        const int cnt = __popc(nzm);
-        int incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o)
-                incl += t;
-        }
-        const int total = __shfl_sync(kFull, incl, 31);
-        const uint32_t fmt = (double)total < one_minus_thr * (double)V ? 1u : 0u;
         if (lane == 0)
             *reinterpret_cast<uint2 *>(slot) = make_uint2(fmt, (uint32_t)total);
         if (fmt) {
@@ -425,56 +373,108 @@ template <> struct WireCodec<kCodecSparse> {
             p[1] = make_float4(v[4], v[5], v[6], v[7]);
         }
     }
-    // Sparse messages: scatter the pairs into the warp's scratch (values +
-    // presence bytes), then read this lane's 8 positions.
-    __device__ __forceinline__ static uint32_t gather(const Reg &m, int lane,
-                                                      unsigned char *scratch, float (&v)[8])
+    __device__ __forceinline__ static int warp_incl_scan(int lane, int cnt)
     {
-        if (!m.fmt) {
+        int incl = cnt;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                v[i] = m.f[i];
-            return 0xffu;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o)
+                incl += t;
         }
+        return incl;
+    }
+    // Read a message into its decoded register form.  Sparse messages are
+    // scattered into the warp's scratch (values + presence bytes) and read
+    // back at the lane's 8 positions.  Warp-collective.
+    __device__ __forceinline__ static void load(const unsigned char *slot, int, int lane,
+                                                unsigned char *scratch, Reg &m)
+    {
+        const uint2 h = *reinterpret_cast<const uint2 *>(slot);
+        m.fmt = h.x;
+        m.nnz = h.y;
+        unsigned char *s = const_cast<unsigned char *>(slot);
+        if (!m.fmt) {
+            const float4 *p = reinterpret_cast<const float4 *>(vals(s)) + 2 * lane;
+            const float4 a = p[0], b = p[1];
+            m.f[0] = a.x; m.f[1] = a.y; m.f[2] = a.z; m.f[3] = a.w;
+            m.f[4] = b.x; m.f[5] = b.y; m.f[6] = b.z; m.f[7] = b.w;
+            m.pres = 0xffu;
+            return;
+        }
+        const int nnz = min((int)h.y, kTile);
         float *sval = reinterpret_cast<float *>(scratch);
         unsigned char *spres = scratch + kTile * 4;
         *reinterpret_cast<uint2 *>(spres + 8 * lane) = make_uint2(0u, 0u);
         __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int k = lane + 32 * i;
-            if (k < (int)m.nnz) {
-                sval[m.ix[i]] = m.f[i];
-                spres[m.ix[i]] = 1;
-            }
+        for (int k = lane; k < nnz; k += 32) {
+            const int ix = idxs(s)[k];
+            sval[ix] = vals(s)[k];
+            spres[ix] = 1;
         }
         __syncwarp();
+        const uint2 pb = *reinterpret_cast<const uint2 *>(spres + 8 * lane);
+        const float4 *sv = reinterpret_cast<const float4 *>(sval) + 2 * lane;
+        const float4 a = sv[0], b = sv[1];
+        const float t[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         uint32_t pres = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            if (spres[8 * lane + i]) {
-                pres |= 1u << i;
-                v[i] = sval[8 * lane + i];
-            } else {
-                v[i] = 0.0f;
-            }
+            const uint32_t byte = ((i < 4 ? pb.x : pb.y) >> (8 * (i & 3))) & 0xffu;
+            pres |= (byte ? 1u : 0u) << i;
+            m.f[i] = byte ? t[i] : 0.0f;
         }
+        m.pres = pres;
         __syncwarp();
-        return pres;
     }
-    __device__ __forceinline__ static void decode_add(const Reg &m, float (&v)[8], int lane,
-                                                      unsigned char *scratch)
+    // Forward a received message unchanged: the same format, count, values
+    // and ascending indices.  Warp-collective.
+    __device__ __forceinline__ static void store(unsigned char *slot, int, int lane, const Reg &m)
     {
-        float d[8];
-        const uint32_t pres = gather(m, lane, scratch, d);
+        if (!m.fmt) {
+            emit(slot, lane, m.f, 0xffu, 0u, 0, 0, (int)m.nnz);
+            return;
+        }
+        const int cnt = __popc(m.pres);
+        const int incl = warp_incl_scan(lane, cnt);
+        const int total = __shfl_sync(kFull, incl, 31);
+        emit(slot, lane, m.f, m.pres, 1u, cnt, incl, total);
+    }
+    // The header of a dense message also carries its nonzero count.  The
+    // receiver restores every value exactly (absent ones are +0.0), so
+    // the decoded values are v itself: DEC changes nothing.
+    template <bool DEC>
+    __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int,
+                                                  int lane, int V, const RingArgs &a,
+                                                  unsigned char *)
+    {
+        uint32_t nzm = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            v[i] = ((pres >> i) & 1u) ? __fadd_rn(v[i], d[i]) : v[i];
+            if (8 * lane + i < V && __float_as_uint(v[i]) != 0u)
+                nzm |= 1u << i;
+        const int cnt = __popc(nzm);
+        const int incl = warp_incl_scan(lane, cnt);
+        const int total = __shfl_sync(kFull, incl, 31);
+        // full slices compare with the precomputed integer limit; a ragged
+        // slice evaluates nnz < (1 - threshold) * len in double
+        const uint32_t fmt = V == kTile ? (total < a.sp_full_lim ? 1u : 0u)
+                                        : ((double)total < a.one_minus_thr * (double)V ? 1u : 0u);
+        emit(slot, lane, v, nzm, fmt, cnt, incl, total);
     }
-    __device__ __forceinline__ static void values(const Reg &m, float (&v)[8], int lane,
-                                                  unsigned char *scratch)
+    __device__ __forceinline__ static void decode_add(const Reg &m, float (&v)[8], int,
+                                                      unsigned char *)
     {
-        gather(m, lane, scratch, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            v[i] = ((m.pres >> i) & 1u) ? __fadd_rn(v[i], m.f[i]) : v[i];
+    }
+    __device__ __forceinline__ static void values(const Reg &m, float (&v)[8], int,
+                                                  unsigned char *)
+    {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            v[i] = m.f[i];
     }
 };
 
@@ -524,11 +524,17 @@ __device__ __forceinline__ bool wait_ready(uint64_t *bar, uint32_t parity, uint6
     return wait_slow(bar, parity, limit_ns, status);
 }
 
-// ONE: every warp plays exactly one rank (N <= warps per block), so rank
-// indices, addresses and byte counts stay in registers across the loops.
-template <int CODEC, int IN_T, bool FAST, int G, bool ONE>
-__global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_constant__ RingArgs a)
+// MODE kRanksShared: a warp may play several ranks (N > warps per block).
+// MODE kRankPerWarp8 / kRankPerWarp16: every warp plays exactly one rank, so
+// rank indices, addresses and byte counts stay in registers across the
+// loops; blocks of at most 8 warps get up to 80 registers a thread (three
+// blocks per SM), blocks of up to 16 warps 64 (two blocks per SM).
+template <int CODEC, int IN_T, bool FAST, int G, int MODE>
+__global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 32,
+                                  MODE == kRankPerWarp8 ? 3 : 2)
+    ring_kernel(const __grid_constant__ RingArgs a)
 {
+    constexpr bool ONE = MODE != kRanksShared;
     extern __shared__ __align__(128) unsigned char smem[];
     using C = WireCodec<CODEC>;
     using Reg = typename C::Reg;
@@ -705,7 +711,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
     // and their slot is freed at the end of the step (two slots per edge).
     constexpr bool kEarly = G == 1;
     auto release_early = [&](int r, const unsigned char *rslot, uint32_t rb, Reg &m) {
-        C::load(rslot, 0, lane, m);
+        C::load(rslot, 0, lane, scratch, m);
         if (ONE)
             my_recv += rb;
         __syncwarp();
@@ -783,7 +789,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
                                          a.timeout_ns, a.status)))
                     break;
                 unsigned char *dslot = slots + (size_t)(dst * K + snd.slot) * a.slot_bytes;
-#pragma unroll
+#pragma unroll 1
                 for (int gi = 0; gi < G; ++gi) {
                     float v[8];
                     input_group(r, c, V, gi, sp, v);
@@ -792,10 +798,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
                         if (kEarly)
                             m = m0;
                         else
-                            C::load(rslot, gi, lane, m);
+                            C::load(rslot, gi, lane, scratch, m);
                         C::decode_add(m, v, lane, scratch);
                     }
-                    C::template encode<false>(v, dslot, gi, lane, V, a.one_minus_thr, scratch);
+                    C::template encode<false>(v, dslot, gi, lane, V, a, scratch);
                 }
                 __syncwarp();
                 finish_step(r, g, g >= 2 && !kEarly, true, rb, C::bytes(V, dslot));
@@ -833,7 +839,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
             // N = 1 has no allgather step: encode into the rank's own (unused) slot
             unsigned char *dslot = send ? slots + (size_t)(dst * K + snd.slot) * a.slot_bytes
                                         : slots + (size_t)(r * K) * a.slot_bytes;
-#pragma unroll
+#pragma unroll 1
             for (int gi = 0; gi < G; ++gi) {
                 float v[8];
                 input_group(r, r, V, gi, sp, v);
@@ -842,11 +848,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
                     if (kEarly)
                         m = m0;
                     else
-                        C::load(rslot, gi, lane, m);
+                        C::load(rslot, gi, lane, scratch, m);
                     C::decode_add(m, v, lane, scratch);
                 }
                 if (allred)
-                    C::template encode<true>(v, dslot, gi, lane, V, a.one_minus_thr, scratch);
+                    C::template encode<true>(v, dslot, gi, lane, V, a, scratch);
                 output_group(r, r, V, gi, v);
             }
             __syncwarp();
@@ -884,13 +890,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
                                                     a.status)))
                         break;
                     unsigned char *dslot = slots + (size_t)(dst * K + snd.slot) * a.slot_bytes;
-#pragma unroll
+#pragma unroll 1
                     for (int gi = 0; gi < G; ++gi) {
                         Reg m;
                         if (kEarly)
                             m = m0;
                         else
-                            C::load(rslot, gi, lane, m);
+                            C::load(rslot, gi, lane, scratch, m);
                         if (fwd)
                             C::store(dslot, gi, lane, m);
                         float v[8];
@@ -933,6 +939,28 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 2) ring_kernel(const __grid_co
                     atomicAdd(a.recv + r, rrecv[r]);
             }
         }
+    }
+}
+
+// Kernel for one (codec, input dtype, slice width): the generic path, or the
+// staged path in the given MODE.
+template <int CODEC, int IN_T, int G> const void *ring_variant(bool fast, int mode)
+{
+    if (!fast)
+        return (const void *)ring_kernel<CODEC, IN_T, false, G, kRanksShared>;
+    switch (mode) {
+    case kRankPerWarp8: return (const void *)ring_kernel<CODEC, IN_T, true, G, kRankPerWarp8>;
+    case kRankPerWarp16: return (const void *)ring_kernel<CODEC, IN_T, true, G, kRankPerWarp16>;
+    default: return (const void *)ring_kernel<CODEC, IN_T, true, G, kRanksShared>;
+    }
+}
+template <int CODEC, int G> const void *ring_variant(int in_t, bool fast, int mode)
+{
+    switch (in_t) {
+    case kF32: return ring_variant<CODEC, kF32, G>(fast, mode);
+    case kF16: return ring_variant<CODEC, kF16, G>(fast, mode);
+    case kBF16: return ring_variant<CODEC, kBF16, G>(fast, mode);
+    default: return nullptr;
     }
 }
 

@@ -15,10 +15,10 @@
 #include "rra_kernels.h"
 
 namespace rra {
-const void *ring_fn_none(int codec, int in_t, bool fast, int groups, bool one);
-const void *ring_fn_bfp8(int codec, int in_t, bool fast, int groups, bool one);
-const void *ring_fn_bfp4(int codec, int in_t, bool fast, int groups, bool one);
-const void *ring_fn_sparse(int codec, int in_t, bool fast, int groups, bool one);
+const void *ring_fn_none(int in_t, bool fast, int groups, int rmap);
+const void *ring_fn_bfp8(int in_t, bool fast, int groups, int rmap);
+const void *ring_fn_bfp4(int in_t, bool fast, int groups, int rmap);
+const void *ring_fn_sparse(int in_t, bool fast, int groups, int rmap);
 } // namespace rra
 
 using namespace rra;
@@ -137,15 +137,15 @@ int grid_for(rra_comm *c, long long key, const void *fn, int warps, int smem, lo
     return (int)std::max(1LL, g);
 }
 
-const void *ring_fn(int codec, int in_t, bool fast, int groups, bool one)
+const void *ring_fn(int codec, int in_t, bool fast, int groups, int rmap)
 {
     if (codec == kCodecNone)
-        return ring_fn_none(codec, in_t, fast, groups, one);
+        return ring_fn_none(in_t, fast, groups, rmap);
     if (codec == kCodecSparse)
-        return ring_fn_sparse(codec, in_t, fast, groups, one);
+        return ring_fn_sparse(in_t, fast, groups, rmap);
     if (codec == kCodecBfp8)
-        return ring_fn_bfp8(codec, in_t, fast, groups, one);
-    return ring_fn_bfp4(codec, in_t, fast, groups, one);
+        return ring_fn_bfp8(in_t, fast, groups, rmap);
+    return ring_fn_bfp4(in_t, fast, groups, rmap);
 }
 
 // Bytes of one mailbox slot for a slice of 256 * groups elements.
@@ -168,9 +168,10 @@ struct LaunchShape {
     bool fast;
 };
 
-bool pick_shape(rra_comm *c, int N, int kc, int ies, bool diff, bool fast, int warps,
-                LaunchShape *out)
+bool pick_shape(rra_comm *c, int N, long long n, int kc, int ies, bool diff, bool fast,
+                int warps, LaunchShape *out)
 {
+    const int sms = num_sms();
     static const int kGD[][2] = {{8, 2}, {8, 1}, {4, 2}, {4, 1}, {2, 4},
                                  {2, 2}, {1, 4}, {1, 2}, {1, 1}};
     const bool sparse = kc == kCodecSparse;
@@ -183,6 +184,10 @@ bool pick_shape(rra_comm *c, int N, int kc, int ies, bool diff, bool fast, int w
                 continue;
             int D = c->tune_D ? c->tune_D : gd[1];
             if (sparse && G != 1)
+                continue;
+            // a short chunk is cut into narrower slices while a wider one
+            // would leave SMs without a slice position to work on
+            if (pass >= 2 && G > 1 && (n + (long long)kTile * G - 1) / ((long long)kTile * G) < sms)
                 continue;
             if (!fast)
                 D = 1;
@@ -285,6 +290,10 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     a.has_prev = cd.diff_prev ? 1 : 0;
     a.base = cd.diff_base;
     a.one_minus_thr = 1.0 - (double)cd.sparsity_threshold;
+    // the same test for a full slice as an integer limit: nnz < lim
+    a.sp_full_lim = 0;
+    while (a.sp_full_lim <= kTile && (double)a.sp_full_lim < a.one_minus_thr * (double)kTile)
+        ++a.sp_full_lim;
     a.timeout_ns = comm->timeout_ns;
     a.status = comm->status;
     a.withhold_rank = comm->withhold_rank;
@@ -305,9 +314,9 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
 
     const int warps = warps_for(N);
     LaunchShape sh;
-    if (!pick_shape(comm, N, kc, (int)ies, cd.diff_prev != nullptr, fast, warps, &sh)) {
+    if (!pick_shape(comm, N, a.n, kc, (int)ies, cd.diff_prev != nullptr, fast, warps, &sh)) {
         fast = false;
-        if (!pick_shape(comm, N, kc, (int)ies, cd.diff_prev != nullptr, false, warps, &sh))
+        if (!pick_shape(comm, N, a.n, kc, (int)ies, cd.diff_prev != nullptr, false, warps, &sh))
             return RRA_ERR_UNSUPPORTED;
     }
     const int groups = sh.groups, smem = sh.smem;
@@ -316,12 +325,13 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     a.slot_bytes = slot_bytes_for(kc, groups);
     a.stage_bytes = kTile * groups * (cd.diff_prev ? 8 : (int)ies);
     a.tiles = (a.n + kTile * groups - 1) / (kTile * groups);
-    const bool one = warps == N; // every warp plays exactly one rank
-    const void *fn = ring_fn(kc, in_t, fast, groups, one);
+    // every warp plays exactly one rank when N fits the block
+    const int rmap = warps != N ? kRanksShared : (warps <= 8 ? kRankPerWarp8 : kRankPerWarp16);
+    const void *fn = ring_fn(kc, in_t, fast, groups, rmap);
     if (!fn)
         return RRA_ERR_UNSUPPORTED;
-    const long long key = 100000 + kc * 10000 + in_t * 1000 + (fast ? 100 : 0) +
-                          (one ? 10 : 0) + groups;
+    const long long key = 100000 + kc * 10000 + in_t * 1000 + (fast ? 100 : 0) + rmap * 10 +
+                          groups;
     const int grid = grid_for(comm, key, fn, warps, smem, a.tiles);
     counter_sets(comm, &a.sent, &a.recv, &a.zero);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -416,10 +426,31 @@ std::map<int, std::pair<uint32_t *, long long>> g_ws;
 } // namespace
 
 namespace rra {
+// Largest dynamic shared memory already allowed for each kernel (per device),
+// so the attribute is set once per kernel rather than on every launch.
+static std::mutex g_attr_mu;
+static std::map<std::pair<int, const void *>, int> g_attr_smem;
+
+static cudaError_t allow_smem(const void *fn, int smem)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    int &have = g_attr_smem[{dev, fn}];
+    if (smem <= have)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        have = smem;
+    return e;
+}
+
 cudaError_t launch_ring(const void *fn, const RingArgs &a, int grid, int warps, int smem,
                         cudaStream_t st)
 {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = allow_smem(fn, smem);
     if (e != cudaSuccess)
         return e;
     void *args[] = {const_cast<RingArgs *>(&a)};

@@ -13,6 +13,8 @@ constexpr int kMaxWarps = 16; // warps per block; ranks per warp = ceil(N / warp
 
 enum Codec { kCodecNone = 0, kCodecBfp8 = 1, kCodecBfp4 = 2, kCodecSparse = 3 };
 enum Mode { kModeAllreduce = 0, kModeReduceScatter = 1 };
+// How simulated ranks map onto the warps of a ring kernel block.
+enum RankMap { kRanksShared = 0, kRankPerWarp8 = 1, kRankPerWarp16 = 2 };
 
 // Arguments of the fused ring kernel (reduce-scatter pass, owner finalise,
 // allgather pass).  Passed by value as a __grid_constant__ parameter.
@@ -35,6 +37,7 @@ struct RingArgs {
     long long n;       // chunk length ceil(T/N)
     long long tiles;   // slices per chunk ceil(n / 256)
     double one_minus_thr; // sparse: a slice is sparse iff nnz < one_minus_thr * len
+    int sp_full_lim;      // sparse: a full 256-element slice is sparse iff nnz < sp_full_lim
     unsigned long long timeout_ns;
     unsigned long long *sent; // [N] device counters of this call
     unsigned long long *recv; // [N]
