@@ -550,10 +550,13 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     ring_kernel(const __grid_constant__ RingArgs a)
 {
     constexpr bool ONE = MODE != kRanksShared;
+    // kF32Diff: fp32 inputs cur with a second stream prev, encoded as cur - prev
+    constexpr bool PREV = IN_T == kF32Diff;
+    constexpr int LT = PREV ? kF32 : IN_T; // element type of the input buffers
     extern __shared__ __align__(128) unsigned char smem[];
     using C = WireCodec<CODEC>;
     using Reg = typename C::Reg;
-    constexpr int es = dtype_size(IN_T);
+    constexpr int es = dtype_size(LT);
     constexpr int TW = kTile * G; // elements per rank per step
     const int N = a.N;
     const int W = blockDim.x >> 5;
@@ -607,24 +610,35 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
 
     // ---- staged input loads.  All ranks consume loads in the same order
     // (slice iteration, step 1..N), so one cursor gives the next load to
-    // issue for every rank; "issued" and "consumed" count loads per rank.
-    long long cur_item = blockIdx.x; // slice position of the next load to issue
-    int cur_g = 1;                   // its step
-    long long issued = 0, consumed = 0;
+    // issue for every rank; "inflight" counts loads issued and not consumed.
+    int cur_item = blockIdx.x; // slice position of the next load to issue
+    int cur_g = 1;             // its step
+    int inflight = 0;          // loads issued and not yet consumed, per rank
+    const int tiles = (int)a.tiles;
     auto issue_one = [&](int r, int d) { // lane 0: load (cur_item, cur_g) of rank r into stage d
         int c = r - cur_g;
         c += c < 0 ? N : 0;
-        const long long t0 = cur_item * TW;
+        const long long t0 = (long long)cur_item * TW;
         const uint32_t bytes = (uint32_t)slice_len(c, t0) * es;
         uint64_t *bar = sbar + r * D + d;
         unsigned char *dst = stages + (size_t)(r * D + d) * a.stage_bytes;
+        if (bytes < (uint32_t)(TW * es)) {
+            // a short slice: zero the rest of the stage (both streams), so
+            // that the consumer reads +0.0 past the end without a test per
+            // group; these stores precede the arrive that publishes the stage
+            for (uint32_t o = bytes; o < (uint32_t)(TW * es); o += 4) {
+                *reinterpret_cast<uint32_t *>(dst + o) = 0u;
+                if constexpr (PREV)
+                    *reinterpret_cast<uint32_t *>(dst + TW * 4 + o) = 0u;
+            }
+        }
         if (bytes == 0) {
             mbar_arrive(bar);
             return;
         }
         const long long eo = (long long)c * n + t0;
         const char *src = reinterpret_cast<const char *>(a.in[r]) + eo * es;
-        if (a.has_prev) {
+        if constexpr (PREV) {
             mbar_arrive_expect_tx(bar, 2 * bytes);
             bulk_g2s(dst, src, bytes, bar);
             bulk_g2s(dst + TW * 4, a.prev[r] + eo, bytes, bar);
@@ -640,11 +654,11 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
         }
     };
     if constexpr (FAST) {
-        while (issued < D && cur_item < a.tiles) {
+        while (inflight < D && cur_item < tiles) {
             if (lane == 0)
                 for (int r = warp; r < N; r += rstride)
-                    issue_one(r, (int)issued);
-            ++issued;
+                    issue_one(r, inflight);
+            ++inflight;
             cursor_next();
         }
         __syncwarp();
@@ -654,30 +668,26 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     bool ok = true;
     long long t0 = 0;
     const bool first_item_withhold = a.withhold_rank >= 0;
+    int withhold_g = 0; // step whose send is withheld in this slice (0: none)
 
     // group gi of rank r's own input for chunk c (staged on the fast path)
     auto input_group = [&](int r, int c, int V, int gi, const unsigned char *sp,
                            float (&v)[8]) {
         if constexpr (FAST) {
-            load8_vec<IN_T>(sp + (gi * kTile + 8 * lane) * es, v);
-            if (a.has_prev) {
+            // the stage is zero past the slice's end (see issue_one)
+            load8_vec<LT>(sp + (gi * kTile + 8 * lane) * es, v);
+            if constexpr (PREV) {
                 float p[8];
                 load8_vec<kF32>(sp + TW * 4 + (gi * kTile + 8 * lane) * 4, p);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     v[i] = __fsub_rn(v[i], p[i]);
             }
-            if (V < TW) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (gi * kTile + 8 * lane + i >= V)
-                        v[i] = 0.0f;
-            }
         } else {
             const int vl = min(max(V - gi * kTile - 8 * lane, 0), 8);
             const long long eo = (long long)c * n + t0 + gi * kTile + 8 * lane;
-            load8_scalar<IN_T>(reinterpret_cast<const char *>(a.in[r]) + eo * es, vl, v);
-            if (a.has_prev) {
+            load8_scalar<LT>(reinterpret_cast<const char *>(a.in[r]) + eo * es, vl, v);
+            if constexpr (PREV) {
                 float p[8];
                 load8_scalar<kF32>(a.prev[r] + eo, vl, p);
 #pragma unroll
@@ -689,12 +699,12 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     // output epilogue of group gi: average, previous-round base, cast
     const float inv_n = ((N & (N - 1)) == 0) ? 1.0f / (float)N : 0.0f; // exact for powers of two
     const int out_t = a.out_t;
+    const int osz = dtype_size(out_t);
     const bool plain_out = !a.average && !a.base && a.vec_out;
     auto output_group = [&](int r, int c, int V, int gi, float (&v)[8]) {
         const long long e0 = (long long)c * n + t0 + gi * kTile + 8 * lane;
         if (plain_out && V == TW) { // full slice, no epilogue arithmetic: vector store
-            store8(reinterpret_cast<char *>(a.out[r]) + e0 * dtype_size(out_t), out_t, v, 8,
-                   true);
+            store8_full(reinterpret_cast<char *>(a.out[r]) + e0 * osz, out_t, v);
             return;
         }
         const int vl = V == TW ? 8 : min(max(V - gi * kTile - 8 * lane, 0), 8);
@@ -713,8 +723,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
             for (int i = 0; i < 8; ++i)
                 v[i] = __fadd_rn(bb[i], v[i]);
         }
-        store8(reinterpret_cast<char *>(a.out[r]) + e0 * dtype_size(out_t), out_t, v, vl,
-               a.vec_out != 0);
+        store8(reinterpret_cast<char *>(a.out[r]) + e0 * osz, out_t, v, vl, a.vec_out != 0);
     };
     auto waits_ok = [&](bool w) -> bool {
         ok = ok && w;
@@ -740,14 +749,14 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     auto stage_step = [&]() {
         if constexpr (FAST) {
             __syncwarp();
-            if (issued == consumed + D && cur_item < a.tiles) {
+            if (inflight == D && cur_item < tiles) { // refill the stage just consumed
                 if (lane == 0)
                     for (int r = warp; r < N; r += rstride)
                         issue_one(r, stg.slot);
-                ++issued;
                 cursor_next();
+            } else {
+                --inflight;
             }
-            ++consumed;
             stg.advance(D);
         }
     };
@@ -766,8 +775,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
             }
             if (send) {
                 const int dst = r + 1 == N ? 0 : r + 1;
-                if (!(first_item_withhold && r == a.withhold_rank && g == a.withhold_step &&
-                      t0 == (long long)blockIdx.x * TW))
+                if (!(r == a.withhold_rank && g == withhold_g))
                     mbar_arrive(full + dst * K + snd.slot);
                 if (!ONE)
                     rsent[r] += sb;
@@ -775,8 +783,10 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
         }
     };
 
-    for (long long item = blockIdx.x; ok && item < a.tiles; item += gridDim.x) {
-        t0 = item * TW;
+    for (int item = blockIdx.x; ok && item < tiles; item += gridDim.x) {
+        t0 = (long long)item * TW;
+        // the fault-injection test withholds one send in each block's first slice
+        withhold_g = first_item_withhold && item == (int)blockIdx.x ? a.withhold_step : 0;
 
         // ---- reduce-scatter steps g = 1..N-1: send chunk (r-g) mod N
         for (int g = 1; ok && g < N; ++g) {
@@ -933,9 +943,14 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     // ---- drain this warp's staged copies that are still in flight
     if constexpr (FAST) {
         __syncwarp();
-        for (int r = warp; r < N; r += W)
-            for (long long L = consumed; L < issued; ++L)
-                drain_phase(sbar + r * D + (int)(L % D), (uint32_t)((L / D) & 1), a.timeout_ns);
+        // the loads in flight occupy the stages from stg on, in order
+        for (int r = warp; r < N; r += W) {
+            Fifo d = stg;
+            for (int L = 0; L < inflight; ++L) {
+                drain_phase(sbar + r * D + d.slot, (uint32_t)d.phase, a.timeout_ns);
+                d.advance(D);
+            }
+        }
     }
     // ---- per-rank byte counters
     if (lane == 0) {
@@ -975,6 +990,7 @@ template <int CODEC, int G> const void *ring_variant(int in_t, bool fast, int mo
     case kF32: return ring_variant<CODEC, kF32, G>(fast, mode);
     case kF16: return ring_variant<CODEC, kF16, G>(fast, mode);
     case kBF16: return ring_variant<CODEC, kBF16, G>(fast, mode);
+    case kF32Diff: return ring_variant<CODEC, kF32Diff, G>(fast, mode);
     default: return nullptr;
     }
 }

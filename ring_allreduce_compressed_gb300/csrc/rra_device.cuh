@@ -21,9 +21,12 @@ constexpr int kBlock = 128;      // BFP block (= RRA_BFP_BLOCK)
 constexpr unsigned kFull = 0xffffffffu;
 
 enum Dtype { kF32 = 0, kF16 = 1, kBF16 = 2 };
+// Ring kernel input kind: fp32 inputs cur together with a second fp32 stream
+// prev, sent as the difference cur - prev.
+constexpr int kF32Diff = 3;
 enum Status : unsigned { kStOk = 0, kStTimeout = 4 };
 
-__host__ __device__ constexpr int dtype_size(int t) { return t == kF32 ? 4 : 2; }
+__host__ __device__ constexpr int dtype_size(int t) { return t == kF32 || t == kF32Diff ? 4 : 2; }
 
 // ---------------------------------------------------------------- PTX
 
@@ -192,8 +195,24 @@ __device__ __forceinline__ uint16_t f32_to_16(float v, int t)
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
+// 8 fp32 values as 4 packed pairs of 16-bit out_t (round to nearest even).
+template <int OUT_T> __device__ __forceinline__ void pack16x8(const float v[8], uint32_t h[4])
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (OUT_T == kF16) {
+            const __half2 p = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+            h[i] = *reinterpret_cast<const uint32_t *>(&p);
+        } else {
+            const __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            h[i] = *reinterpret_cast<const uint32_t *>(&p);
+        }
+    }
+}
+
 // Store 8 fp32 values as out_t (round to nearest even); vectorised when the
-// destination is 16-byte aligned and all 8 are present.
+// destination is 16-byte aligned and all 8 are present.  Each output type
+// has its own straight-line path, so a runtime out_t costs one branch.
 __device__ __forceinline__ void store8(void *base, int out_t, const float v[8], int valid,
                                        bool vec)
 {
@@ -208,29 +227,38 @@ __device__ __forceinline__ void store8(void *base, int out_t, const float v[8], 
                 if (i < valid)
                     p[i] = v[i];
         }
-    } else {
-        // pairs of values packed by one conversion each (round to nearest even)
-        uint32_t h[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (out_t == kF16) {
-                const __half2 p = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
-                h[i] = *reinterpret_cast<const uint32_t *>(&p);
-            } else {
-                const __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                h[i] = *reinterpret_cast<const uint32_t *>(&p);
-            }
-        }
-        uint16_t *p = reinterpret_cast<uint16_t *>(base);
-        if (vec && valid >= 8) {
-            *reinterpret_cast<uint4 *>(p) = make_uint4(h[0], h[1], h[2], h[3]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (i < valid)
-                    p[i] = (uint16_t)(h[i / 2] >> (16 * (i % 2)));
-        }
+        return;
     }
+    uint32_t h[4];
+    if (out_t == kF16)
+        pack16x8<kF16>(v, h);
+    else
+        pack16x8<kBF16>(v, h);
+    uint16_t *p = reinterpret_cast<uint16_t *>(base);
+    if (vec && valid >= 8) {
+        *reinterpret_cast<uint4 *>(p) = make_uint4(h[0], h[1], h[2], h[3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < valid)
+                p[i] = (uint16_t)(h[i / 2] >> (16 * (i % 2)));
+    }
+}
+
+// Full, aligned group of 8: a 16-byte (or two) vector store of out_t.
+__device__ __forceinline__ void store8_full(void *p, int out_t, const float v[8])
+{
+    if (out_t == kF32) {
+        reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        return;
+    }
+    uint32_t h[4];
+    if (out_t == kF16)
+        pack16x8<kF16>(v, h);
+    else
+        pack16x8<kBF16>(v, h);
+    *reinterpret_cast<uint4 *>(p) = make_uint4(h[0], h[1], h[2], h[3]);
 }
 
 // ---------------------------------------------------------------- BFP

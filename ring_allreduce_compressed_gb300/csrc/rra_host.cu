@@ -327,10 +327,11 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     a.tiles = (a.n + kTile * groups - 1) / (kTile * groups);
     // every warp plays exactly one rank when N fits the block
     const int rmap = warps != N ? kRanksShared : (warps <= 8 ? kRankPerWarp8 : kRankPerWarp16);
-    const void *fn = ring_fn(kc, in_t, fast, groups, rmap);
+    const int kin = cd.diff_prev ? kF32Diff : (int)in_t; // kernel input kind
+    const void *fn = ring_fn(kc, kin, fast, groups, rmap);
     if (!fn)
         return RRA_ERR_UNSUPPORTED;
-    const long long key = 100000 + kc * 10000 + in_t * 1000 + (fast ? 100 : 0) + rmap * 10 +
+    const long long key = 100000 + kc * 10000 + kin * 1000 + (fast ? 100 : 0) + rmap * 10 +
                           groups;
     const int grid = grid_for(comm, key, fn, warps, smem, a.tiles);
     counter_sets(comm, &a.sent, &a.recv, &a.zero);
