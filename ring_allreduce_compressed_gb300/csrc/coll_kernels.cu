@@ -1,0 +1,745 @@
+// coll_kernels.cu -- ring allgather, binomial broadcast and tree allreduce for
+// N simulated ranks on one sm_103a GPU ("从零实现集合通信": per-rank byte/step
+// table -- allgather T(N-1)/N in N-1 steps, broadcast T over a log2(N) tree,
+// tree allreduce T log2 N in 2 log2 N steps; "练习": the tree variant).
+//
+// Same machinery as the fused ring (ring_kernel.cuh).  A block runs the
+// collective for one slice position (TW = 256*G elements) at a time and
+// strides over slice positions; simulated rank r is warp r mod W.  Every edge
+// of the communication graph is a FIFO of K slots in shared memory owned by
+// its receiver, with a "full" and an "empty" mbarrier per slot and bounded
+// waits.  Data a rank reads from its own buffer is staged with bulk async
+// copies on the fast path (16-byte aligned buffers and slice boundaries).
+//
+//  allgather   ring edges r -> r+1; step g = 1..N, chunk (r - g + 1) mod N:
+//              g = 1 sends the rank's own chunk, g >= 2 stores the received
+//              chunk into the rank's buffer and forwards it while g < N.
+//  broadcast   binomial tree from the root: relative rank q = (r - root) mod N
+//              receives at level floor(log2 q) from q - 2^level and forwards
+//              at every later level k with q + 2^k < N, from its receive slot.
+//  tree        fp32.  Each rank accumulates in its staged slice: at reduce
+//              level k, r with r mod 2^(k+1) = 2^k sends to r - 2^k, which
+//              adds (receiver's partial + sender's partial, round to nearest
+//              even); then the binomial broadcast of rank 0's sum.
+// Each tree/broadcast edge carries one message per slice position, so one
+// FIFO position per block serves all of them; ring edges carry N-1 messages
+// per slice position, one per step.  Within a level, a warp does all of its
+// ranks' sends before any of their receives, so a warp that plays both ends
+// of an edge (N > 16) never waits on itself.
+#include "rra_device.cuh"
+#include "rra_kernels.h"
+
+namespace rra {
+
+namespace {
+
+// One lane's 8 consecutive elements of ES bytes each (16 or 32 bytes).
+template <int ES> struct Vec8 {
+    uint4 u[ES / 2];
+    __device__ __forceinline__ void load(const void *p)
+    {
+#pragma unroll
+        for (int i = 0; i < ES / 2; ++i)
+            u[i] = reinterpret_cast<const uint4 *>(p)[i];
+    }
+    __device__ __forceinline__ void store(void *p) const
+    {
+#pragma unroll
+        for (int i = 0; i < ES / 2; ++i)
+            reinterpret_cast<uint4 *>(p)[i] = u[i];
+    }
+    // the first `valid` elements at p (any alignment); the rest read as zero
+    __device__ __forceinline__ void load_elems(const void *p, int valid)
+    {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if constexpr (ES == 4)
+                reinterpret_cast<uint32_t *>(u)[i] =
+                    i < valid ? reinterpret_cast<const uint32_t *>(p)[i] : 0u;
+            else
+                reinterpret_cast<uint16_t *>(u)[i] =
+                    i < valid ? reinterpret_cast<const uint16_t *>(p)[i] : (uint16_t)0;
+        }
+    }
+    __device__ __forceinline__ void store_elems(void *p, int valid) const
+    {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < valid) {
+                if constexpr (ES == 4)
+                    reinterpret_cast<uint32_t *>(p)[i] = reinterpret_cast<const uint32_t *>(u)[i];
+                else
+                    reinterpret_cast<uint16_t *>(p)[i] = reinterpret_cast<const uint16_t *>(u)[i];
+            }
+    }
+};
+
+// Shared-memory carve-up of a collective kernel (host and device agree via
+// coll_layout in rra_kernels.h).
+struct CollSmem {
+    uint64_t *full, *empty, *sbar;
+    unsigned long long *rsent, *rrecv;
+    unsigned char *slots, *stages;
+};
+
+__device__ __forceinline__ CollSmem coll_carve(unsigned char *smem, const CopyArgs &a, int edges,
+                                               int stagers, bool fast)
+{
+    const CollLayout L =
+        coll_layout(a.N, edges, a.K, stagers, a.D, a.slot_bytes, a.stage_bytes, fast);
+    CollSmem s;
+    s.full = reinterpret_cast<uint64_t *>(smem + L.full);
+    s.empty = reinterpret_cast<uint64_t *>(smem + L.empty);
+    s.sbar = reinterpret_cast<uint64_t *>(smem + L.stage_bar);
+    s.rsent = reinterpret_cast<unsigned long long *>(smem + L.counters);
+    s.rrecv = s.rsent + a.N;
+    s.slots = smem + L.slots;
+    s.stages = smem + L.stages;
+    return s;
+}
+
+__device__ __forceinline__ void coll_init(const CollSmem &s, const CopyArgs &a, int edges,
+                                          int stagers, bool fast)
+{
+    for (int i = threadIdx.x; i < edges * a.K; i += blockDim.x) {
+        mbar_init(s.full + i, 1);
+        mbar_init(s.empty + i, 1);
+    }
+    if (fast)
+        for (int i = threadIdx.x; i < stagers * a.D; i += blockDim.x)
+            mbar_init(s.sbar + i, 1);
+    for (int i = threadIdx.x; i < a.N; i += blockDim.x) {
+        s.rsent[i] = 0;
+        s.rrecv[i] = 0;
+    }
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < 2 * a.N; i += blockDim.x)
+            a.zero[i] = 0ull;
+    mbar_fence_init();
+    __syncthreads();
+}
+
+// Per-rank byte counters: in registers when every warp plays one rank, in
+// shared memory otherwise; added to the device counters once per block.
+template <bool ONE> struct Bytes {
+    unsigned long long sent = 0, recv = 0;
+    __device__ __forceinline__ void add_sent(const CollSmem &s, int r, unsigned long long b)
+    {
+        if (ONE)
+            sent += b;
+        else
+            s.rsent[r] += b;
+    }
+    __device__ __forceinline__ void add_recv(const CollSmem &s, int r, unsigned long long b)
+    {
+        if (ONE)
+            recv += b;
+        else
+            s.rrecv[r] += b;
+    }
+    __device__ __forceinline__ void flush(const CollSmem &s, const CopyArgs &a, int warp, int W)
+    {
+        if ((threadIdx.x & 31) != 0)
+            return;
+        if (ONE) {
+            if (warp < a.N) {
+                if (sent)
+                    atomicAdd(a.sent + warp, sent);
+                if (recv)
+                    atomicAdd(a.recv + warp, recv);
+            }
+        } else {
+            for (int r = warp; r < a.N; r += W) {
+                if (s.rsent[r])
+                    atomicAdd(a.sent + r, s.rsent[r]);
+                if (s.rrecv[r])
+                    atomicAdd(a.recv + r, s.rrecv[r]);
+            }
+        }
+    }
+};
+
+__device__ __forceinline__ int clamp_len(long long v, int w)
+{
+    return (int)(v < 0 ? 0 : (v > w ? w : v));
+}
+
+} // namespace
+
+// ---------------------------------------------------------------- allgather
+template <int ES, bool FAST, int G, bool ONE>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) allgather_kernel(const __grid_constant__ CopyArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int TW = kTile * G;
+    const int N = a.N, W = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int K = a.K, D = a.D;
+    const CollSmem s = coll_carve(smem, a, N, N, FAST);
+    coll_init(s, a, N, N, FAST);
+    const long long n = a.n, T = a.T;
+    const int rstride = ONE ? N : W;
+    const int tiles = (int)a.tiles;
+    const long long min_len = T - (long long)(N - 1) * n; // shortest chunk
+    auto slice_len = [&](int c, long long t0) -> int {
+        if (t0 + TW <= min_len)
+            return TW;
+        long long lo = (long long)c * n, hi = lo + n;
+        lo = lo < T ? lo : T;
+        hi = hi < T ? hi : T;
+        return clamp_len(hi - lo - t0, TW);
+    };
+    // staged loads: each rank's own chunk, one slice per slice position
+    int cur_item = blockIdx.x, inflight = 0;
+    auto issue = [&](int r, int d) { // lane 0
+        const long long t0 = (long long)cur_item * TW;
+        const uint32_t bytes = (uint32_t)slice_len(r, t0) * ES;
+        uint64_t *bar = s.sbar + r * D + d;
+        if (bytes == 0) {
+            mbar_arrive(bar);
+            return;
+        }
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(s.stages + (size_t)(r * D + d) * a.stage_bytes,
+                 reinterpret_cast<const char *>(a.buf[r]) + ((long long)r * n + t0) * ES, bytes,
+                 bar);
+    };
+    if constexpr (FAST) {
+        while (inflight < D && cur_item < tiles) {
+            if (lane == 0)
+                for (int r = warp; r < N; r += rstride)
+                    issue(r, inflight);
+            ++inflight;
+            cur_item += gridDim.x;
+        }
+        __syncwarp();
+    }
+    Bytes<ONE> by;
+    Fifo rcv{0, 0}, snd{0, 0}, stg{0, 0};
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < tiles; item += gridDim.x) {
+        const long long t0 = (long long)item * TW;
+        const bool first = item == (int)blockIdx.x;
+        for (int g = 1; ok && g <= N; ++g) {
+            const bool fwd = g < N;
+            for (int r = warp; r < N; r += rstride) {
+                int c = r - g + 1;
+                c += c < 0 ? N : 0;
+                const int V = slice_len(c, t0);
+                const int dst = r + 1 == N ? 0 : r + 1;
+                const unsigned char *src;
+                if (g == 1) {
+                    if (FAST) {
+                        if (!(ok = wait_ready(s.sbar + r * D + stg.slot, (uint32_t)stg.phase,
+                                              a.timeout_ns, a.status)))
+                            break;
+                        src = s.stages + (size_t)(r * D + stg.slot) * a.stage_bytes;
+                    } else {
+                        src = reinterpret_cast<const unsigned char *>(a.buf[r]) +
+                              ((long long)r * n + t0) * ES;
+                    }
+                } else {
+                    if (!(ok = wait_ready(s.full + r * K + rcv.slot, (uint32_t)rcv.phase,
+                                          a.timeout_ns, a.status)))
+                        break;
+                    src = s.slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
+                }
+                if (fwd && !(ok = wait_ready(s.empty + dst * K + snd.slot,
+                                             (uint32_t)(snd.phase ^ 1), a.timeout_ns, a.status)))
+                    break;
+                unsigned char *dslot = s.slots + (size_t)(dst * K + snd.slot) * a.slot_bytes;
+                char *mine = reinterpret_cast<char *>(a.buf[r]) + ((long long)c * n + t0) * ES;
+                const bool global_src = !FAST && g == 1;
+#pragma unroll 1
+                for (int gi = 0; gi < G; ++gi) {
+                    const int e = gi * kTile + 8 * lane;
+                    const int vl = min(max(V - e, 0), 8);
+                    if (gi * kTile >= V)
+                        break;
+                    Vec8<ES> v;
+                    if (global_src)
+                        v.load_elems(src + (size_t)e * ES, vl);
+                    else
+                        v.load(src + (size_t)e * ES);
+                    if (g >= 2) {
+                        if (FAST && vl == 8)
+                            v.store(mine + (size_t)e * ES);
+                        else
+                            v.store_elems(mine + (size_t)e * ES, vl);
+                    }
+                    if (fwd)
+                        v.store(dslot + (size_t)e * ES);
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    if (g >= 2) {
+                        mbar_arrive(s.empty + r * K + rcv.slot);
+                        by.add_recv(s, r, (unsigned long long)V * ES);
+                    }
+                    if (fwd) {
+                        if (!(first && r == a.withhold_rank && g == a.withhold_step))
+                            mbar_arrive(s.full + dst * K + snd.slot);
+                        by.add_sent(s, r, (unsigned long long)V * ES);
+                    }
+                }
+            }
+            if (!ok)
+                break;
+            if (FAST && g == 1) { // the own-chunk stage is consumed: refill it
+                __syncwarp();
+                if (inflight == D && cur_item < tiles) {
+                    if (lane == 0)
+                        for (int r = warp; r < N; r += rstride)
+                            issue(r, stg.slot);
+                    cur_item += gridDim.x;
+                } else {
+                    --inflight;
+                }
+                stg.advance(D);
+            }
+            if (g >= 2)
+                rcv.advance(K);
+            if (fwd)
+                snd.advance(K);
+        }
+    }
+    if constexpr (FAST) {
+        __syncwarp();
+        for (int r = warp; r < N; r += W) {
+            Fifo d = stg;
+            for (int L = 0; L < inflight; ++L) {
+                drain_phase(s.sbar + r * D + d.slot, (uint32_t)d.phase, a.timeout_ns);
+                d.advance(D);
+            }
+        }
+    }
+    by.flush(s, a, warp, W);
+}
+
+// ---------------------------------------------------------------- broadcast
+template <int ES, bool FAST, int G, bool ONE>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) broadcast_kernel(const __grid_constant__ CopyArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int TW = kTile * G;
+    const int N = a.N, W = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int K = a.K, D = a.D;
+    // edge q (the slot FIFO of rank q) receives from q's parent; one stager
+    const CollSmem s = coll_carve(smem, a, N, 1, FAST);
+    coll_init(s, a, N, 1, FAST);
+    const long long T = a.T;
+    const int rstride = ONE ? N : W;
+    const int tiles = (int)a.tiles;
+    const int root = a.root;
+    int L = 0;
+    while ((1 << L) < N)
+        ++L;
+    // last level at which relative rank q forwards (-1: never)
+    auto last_send = [&](int q) -> int {
+        const int k0 = q > 0 ? 32 - __clz(q) : 0;
+        int last = -1;
+        for (int k = k0; k < L; ++k)
+            if (q + (1 << k) < N)
+                last = k;
+        return last;
+    };
+    const bool root_warp = root % W == warp;
+    int cur_item = blockIdx.x, inflight = 0;
+    auto issue = [&](int d) { // lane 0 of the root's warp
+        const long long t0 = (long long)cur_item * TW;
+        const uint32_t bytes = (uint32_t)clamp_len(T - t0, TW) * ES;
+        uint64_t *bar = s.sbar + d;
+        if (bytes == 0) {
+            mbar_arrive(bar);
+            return;
+        }
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(s.stages + (size_t)d * a.stage_bytes,
+                 reinterpret_cast<const char *>(a.buf[root]) + t0 * ES, bytes, bar);
+    };
+    if constexpr (FAST) {
+        while (inflight < D && cur_item < tiles) {
+            if (lane == 0 && root_warp)
+                issue(inflight);
+            ++inflight;
+            cur_item += gridDim.x;
+        }
+        __syncwarp();
+    }
+    Bytes<ONE> by;
+    Fifo e{0, 0}, stg{0, 0};
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < tiles; item += gridDim.x) {
+        const long long t0 = (long long)item * TW;
+        const bool first = item == (int)blockIdx.x;
+        const int V = clamp_len(T - t0, TW);
+        const unsigned long long mb = (unsigned long long)V * ES;
+        if (FAST && root_warp &&
+            !(ok = wait_ready(s.sbar + stg.slot, (uint32_t)stg.phase, a.timeout_ns, a.status)))
+            break;
+        const unsigned char *root_src =
+            FAST ? s.stages + (size_t)stg.slot * a.stage_bytes
+                 : reinterpret_cast<const unsigned char *>(a.buf[root]) + t0 * ES;
+        for (int k = 0; ok && k < L; ++k) {
+            // senders at level k: relative q < 2^k with q + 2^k < N
+            for (int r = warp; r < N; r += rstride) {
+                int q = r - root;
+                q += q < 0 ? N : 0;
+                if (!(q < (1 << k) && q + (1 << k) < N))
+                    continue;
+                int child = r + (1 << k);
+                child -= child >= N ? N : 0;
+                if (!(ok = wait_ready(s.empty + child * K + e.slot, (uint32_t)(e.phase ^ 1),
+                                      a.timeout_ns, a.status)))
+                    break;
+                const unsigned char *src =
+                    q == 0 ? root_src : s.slots + (size_t)(r * K + e.slot) * a.slot_bytes;
+                unsigned char *dslot = s.slots + (size_t)(child * K + e.slot) * a.slot_bytes;
+                const bool global_src = !FAST && q == 0;
+#pragma unroll 1
+                for (int gi = 0; gi < G; ++gi) {
+                    const int el = gi * kTile + 8 * lane;
+                    if (gi * kTile >= V)
+                        break;
+                    Vec8<ES> v;
+                    if (global_src)
+                        v.load_elems(src + (size_t)el * ES, min(max(V - el, 0), 8));
+                    else
+                        v.load(src + (size_t)el * ES);
+                    v.store(dslot + (size_t)el * ES);
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    if (!(first && r == a.withhold_rank && k + 1 == a.withhold_step))
+                        mbar_arrive(s.full + child * K + e.slot);
+                    by.add_sent(s, r, mb);
+                    if (q > 0 && k == last_send(q)) // done forwarding: free the slot
+                        mbar_arrive(s.empty + r * K + e.slot);
+                }
+            }
+            if (!ok)
+                break;
+            // receivers at level k: relative q in [2^k, 2^(k+1))
+            for (int r = warp; r < N; r += rstride) {
+                int q = r - root;
+                q += q < 0 ? N : 0;
+                if (!(q >= (1 << k) && q < (2 << k)))
+                    continue;
+                if (!(ok = wait_ready(s.full + r * K + e.slot, (uint32_t)e.phase, a.timeout_ns,
+                                      a.status)))
+                    break;
+                const unsigned char *rslot = s.slots + (size_t)(r * K + e.slot) * a.slot_bytes;
+                char *mine = reinterpret_cast<char *>(a.buf[r]) + t0 * ES;
+#pragma unroll 1
+                for (int gi = 0; gi < G; ++gi) {
+                    const int el = gi * kTile + 8 * lane;
+                    if (gi * kTile >= V)
+                        break;
+                    const int vl = min(max(V - el, 0), 8);
+                    Vec8<ES> v;
+                    v.load(rslot + (size_t)el * ES);
+                    if (FAST && vl == 8)
+                        v.store(mine + (size_t)el * ES);
+                    else
+                        v.store_elems(mine + (size_t)el * ES, vl);
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    by.add_recv(s, r, mb);
+                    if (last_send(q) < 0) // a leaf frees its slot at once
+                        mbar_arrive(s.empty + r * K + e.slot);
+                }
+            }
+        }
+        if (!ok)
+            break;
+        if (FAST) { // the root's stage is consumed: refill it
+            __syncwarp();
+            if (inflight == D && cur_item < tiles) {
+                if (lane == 0 && root_warp)
+                    issue(stg.slot);
+                cur_item += gridDim.x;
+            } else {
+                --inflight;
+            }
+            stg.advance(D);
+        }
+        e.advance(K);
+    }
+    if constexpr (FAST) {
+        __syncwarp();
+        if (root_warp) {
+            Fifo d = stg;
+            for (int i = 0; i < inflight; ++i) {
+                drain_phase(s.sbar + d.slot, (uint32_t)d.phase, a.timeout_ns);
+                d.advance(D);
+            }
+        }
+    }
+    by.flush(s, a, warp, W);
+}
+
+// ---------------------------------------------------------------- tree allreduce
+template <bool FAST, int G, bool ONE>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) tree_kernel(const __grid_constant__ CopyArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int TW = kTile * G;
+    const int N = a.N, W = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int K = a.K, D = a.D;
+    // edge q: reduce messages from child q to its parent; edge N + q:
+    // broadcast messages into rank q.  Every rank stages (and accumulates in)
+    // its own slice; the generic path has one stage that it fills itself.
+    const CollSmem s = coll_carve(smem, a, 2 * N, N, true);
+    coll_init(s, a, 2 * N, N, FAST);
+    const long long T = a.T;
+    const int rstride = ONE ? N : W;
+    const int tiles = (int)a.tiles;
+    int L = 0;
+    while ((1 << L) < N)
+        ++L;
+    int cur_item = blockIdx.x, inflight = 0;
+    auto issue = [&](int r, int d) { // lane 0
+        const long long t0 = (long long)cur_item * TW;
+        const uint32_t bytes = (uint32_t)clamp_len(T - t0, TW) * 4;
+        uint64_t *bar = s.sbar + r * D + d;
+        if (bytes == 0) {
+            mbar_arrive(bar);
+            return;
+        }
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(s.stages + (size_t)(r * D + d) * a.stage_bytes,
+                 reinterpret_cast<const float *>(a.buf[r]) + t0, bytes, bar);
+    };
+    if constexpr (FAST) {
+        while (inflight < D && cur_item < tiles) {
+            if (lane == 0)
+                for (int r = warp; r < N; r += rstride)
+                    issue(r, inflight);
+            ++inflight;
+            cur_item += gridDim.x;
+        }
+        __syncwarp();
+    }
+    Bytes<ONE> by;
+    Fifo e{0, 0}, stg{0, 0};
+    bool ok = true;
+    auto acc_of = [&](int r) -> float * {
+        return reinterpret_cast<float *>(s.stages + (size_t)(r * D + stg.slot) * a.stage_bytes);
+    };
+    for (int item = blockIdx.x; ok && item < tiles; item += gridDim.x) {
+        const long long t0 = (long long)item * TW;
+        const bool first = item == (int)blockIdx.x;
+        const int V = clamp_len(T - t0, TW);
+        const int ng = (V + kTile - 1) / kTile;
+        const unsigned long long mb = 4ull * (unsigned long long)V;
+        // every rank's slice in its accumulator
+        for (int r = warp; r < N; r += rstride) {
+            if (FAST) {
+                if (!(ok = wait_ready(s.sbar + r * D + stg.slot, (uint32_t)stg.phase,
+                                      a.timeout_ns, a.status)))
+                    break;
+            } else {
+                float *acc = acc_of(r);
+                const float *src = reinterpret_cast<const float *>(a.buf[r]) + t0;
+#pragma unroll 1
+                for (int gi = 0; gi < ng; ++gi) {
+                    const int el = gi * kTile + 8 * lane;
+                    float x[8];
+                    load8_scalar<kF32>(src + el, min(max(V - el, 0), 8), x);
+                    reinterpret_cast<float4 *>(acc + el)[0] = make_float4(x[0], x[1], x[2], x[3]);
+                    reinterpret_cast<float4 *>(acc + el)[1] = make_float4(x[4], x[5], x[6], x[7]);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok)
+            break;
+        // copy rank r's accumulator into the slot FIFO of edge `edge`
+        auto send = [&](int r, int edge, int step) -> bool {
+            if (!wait_ready(s.empty + edge * K + e.slot, (uint32_t)(e.phase ^ 1), a.timeout_ns,
+                            a.status))
+                return false;
+            const float *acc = acc_of(r);
+            float *dst = reinterpret_cast<float *>(s.slots + (size_t)(edge * K + e.slot) * a.slot_bytes);
+#pragma unroll 1
+            for (int gi = 0; gi < ng; ++gi) {
+                const int el = gi * kTile + 8 * lane;
+                reinterpret_cast<float4 *>(dst + el)[0] = reinterpret_cast<const float4 *>(acc + el)[0];
+                reinterpret_cast<float4 *>(dst + el)[1] = reinterpret_cast<const float4 *>(acc + el)[1];
+            }
+            __syncwarp();
+            if (lane == 0) {
+                if (!(first && r == a.withhold_rank && step == a.withhold_step))
+                    mbar_arrive(s.full + edge * K + e.slot);
+                by.add_sent(s, r, mb);
+            }
+            return true;
+        };
+        // ---- binomial reduce to rank 0
+        for (int k = 0; ok && k < L; ++k) {
+            for (int r = warp; r < N; r += rstride) // senders first
+                if ((r & ((2 << k) - 1)) == (1 << k) && !(ok = send(r, r, k + 1)))
+                    break;
+            if (!ok)
+                break;
+            for (int r = warp; r < N; r += rstride) { // then receivers: acc_r + acc_child
+                if ((r & ((2 << k) - 1)) != 0 || r + (1 << k) >= N)
+                    continue;
+                const int child = r + (1 << k);
+                if (!(ok = wait_ready(s.full + child * K + e.slot, (uint32_t)e.phase,
+                                      a.timeout_ns, a.status)))
+                    break;
+                float *acc = acc_of(r);
+                const float *msg =
+                    reinterpret_cast<const float *>(s.slots + (size_t)(child * K + e.slot) * a.slot_bytes);
+#pragma unroll 1
+                for (int gi = 0; gi < ng; ++gi) {
+                    const int el = gi * kTile + 8 * lane;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float4 m = reinterpret_cast<const float4 *>(msg + el)[h];
+                        float4 x = reinterpret_cast<float4 *>(acc + el)[h];
+                        const float2 lo = __fadd2_rn(make_float2(x.x, x.y), make_float2(m.x, m.y));
+                        const float2 hi = __fadd2_rn(make_float2(x.z, x.w), make_float2(m.z, m.w));
+                        reinterpret_cast<float4 *>(acc + el)[h] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(s.empty + child * K + e.slot);
+                    by.add_recv(s, r, mb);
+                }
+            }
+        }
+        if (!ok)
+            break;
+        // ---- rank 0 holds the sum: its output, then the binomial broadcast
+        auto store_out = [&](int r) {
+            const float *acc = acc_of(r);
+            float *out = reinterpret_cast<float *>(a.buf[r]) + t0;
+#pragma unroll 1
+            for (int gi = 0; gi < ng; ++gi) {
+                const int el = gi * kTile + 8 * lane;
+                float x[8];
+                load8_vec<kF32>(acc + el, x);
+                store8(out + el, kF32, x, min(max(V - el, 0), 8), FAST);
+            }
+        };
+        if (warp == 0)
+            store_out(0);
+        for (int k = 0; ok && k < L; ++k) {
+            for (int r = warp; r < N; r += rstride) // senders: r < 2^k
+                if (r < (1 << k) && r + (1 << k) < N && !(ok = send(r, N + r + (1 << k), L + k + 1)))
+                    break;
+            if (!ok)
+                break;
+            for (int r = warp; r < N; r += rstride) { // receivers: r in [2^k, 2^(k+1))
+                if (!(r >= (1 << k) && r < (2 << k)))
+                    continue;
+                if (!(ok = wait_ready(s.full + (N + r) * K + e.slot, (uint32_t)e.phase,
+                                      a.timeout_ns, a.status)))
+                    break;
+                float *acc = acc_of(r);
+                const float *msg =
+                    reinterpret_cast<const float *>(s.slots + (size_t)((N + r) * K + e.slot) * a.slot_bytes);
+#pragma unroll 1
+                for (int gi = 0; gi < ng; ++gi) {
+                    const int el = gi * kTile + 8 * lane;
+                    reinterpret_cast<float4 *>(acc + el)[0] = reinterpret_cast<const float4 *>(msg + el)[0];
+                    reinterpret_cast<float4 *>(acc + el)[1] = reinterpret_cast<const float4 *>(msg + el)[1];
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(s.empty + (N + r) * K + e.slot);
+                    by.add_recv(s, r, mb);
+                }
+                store_out(r);
+            }
+        }
+        if (!ok)
+            break;
+        if (FAST) { // every rank is done with its accumulator: refill the stage
+            __syncwarp();
+            if (inflight == D && cur_item < tiles) {
+                if (lane == 0)
+                    for (int r = warp; r < N; r += rstride)
+                        issue(r, stg.slot);
+                cur_item += gridDim.x;
+            } else {
+                --inflight;
+            }
+            stg.advance(D);
+        } else {
+            __syncwarp();
+        }
+        e.advance(K);
+    }
+    if constexpr (FAST) {
+        __syncwarp();
+        for (int r = warp; r < N; r += W) {
+            Fifo d = stg;
+            for (int i = 0; i < inflight; ++i) {
+                drain_phase(s.sbar + r * D + d.slot, (uint32_t)d.phase, a.timeout_ns);
+                d.advance(D);
+            }
+        }
+    }
+    by.flush(s, a, warp, W);
+}
+
+// ---------------------------------------------------------------- launchers
+
+namespace {
+
+template <int ES, int G> const void *ag_fn(bool fast, bool one)
+{
+    if (fast)
+        return one ? (const void *)allgather_kernel<ES, true, G, true>
+                   : (const void *)allgather_kernel<ES, true, G, false>;
+    return one ? (const void *)allgather_kernel<ES, false, G, true>
+               : (const void *)allgather_kernel<ES, false, G, false>;
+}
+template <int ES, int G> const void *bc_fn(bool fast, bool one)
+{
+    if (fast)
+        return one ? (const void *)broadcast_kernel<ES, true, G, true>
+                   : (const void *)broadcast_kernel<ES, true, G, false>;
+    return one ? (const void *)broadcast_kernel<ES, false, G, true>
+               : (const void *)broadcast_kernel<ES, false, G, false>;
+}
+template <int G> const void *tr_fn(bool fast, bool one)
+{
+    if (fast)
+        return one ? (const void *)tree_kernel<true, G, true> : (const void *)tree_kernel<true, G, false>;
+    return one ? (const void *)tree_kernel<false, G, true> : (const void *)tree_kernel<false, G, false>;
+}
+
+template <int ES> const void *coll_fn_es(int which, int groups, bool fast, bool one)
+{
+    switch (which * 10 + groups) {
+    case 1: return ag_fn<ES, 1>(fast, one);
+    case 2: return ag_fn<ES, 2>(fast, one);
+    case 4: return ag_fn<ES, 4>(fast, one);
+    case 11: return bc_fn<ES, 1>(fast, one);
+    case 12: return bc_fn<ES, 2>(fast, one);
+    case 14: return bc_fn<ES, 4>(fast, one);
+    default: return nullptr;
+    }
+}
+
+} // namespace
+
+const void *coll_fn(int which, int es, int groups, bool fast, bool one)
+{
+    if (which == 2) {
+        switch (groups) {
+        case 1: return tr_fn<1>(fast, one);
+        case 2: return tr_fn<2>(fast, one);
+        case 4: return tr_fn<4>(fast, one);
+        default: return nullptr;
+        }
+    }
+    return es == 4 ? coll_fn_es<4>(which, groups, fast, one) : coll_fn_es<2>(which, groups, fast, one);
+}
+
+} // namespace rra

@@ -141,6 +141,50 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, uint6
     return __all_sync(kFull, ok);
 }
 
+// ---------------------------------------------------------------- mailbox helpers
+
+// Bounded wait used only to drain this warp's own bulk copies before exit:
+// it ignores the status word (copies in flight must land before the block's
+// shared memory is released) and gives up only at the time limit.
+__device__ __forceinline__ void drain_phase(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > limit_ns)
+            break;
+}
+
+// A (slot, phase) position in a FIFO of depth n, advanced without division.
+struct Fifo {
+    int slot, phase;
+    __device__ __forceinline__ void advance(int n)
+    {
+        if (++slot == n) {
+            slot = 0;
+            phase ^= 1;
+        }
+    }
+};
+
+// Rare path of a wait (the phase was not complete at the first test): kept
+// out of line so that the common path stays a few instructions.
+static __device__ __noinline__ bool wait_slow(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                              unsigned *status)
+{
+    return wait_phase(bar, parity, limit_ns, status);
+}
+
+// Warp-uniform: true once every lane has observed the phase (acquire).
+__device__ __forceinline__ bool wait_ready(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                           unsigned *status)
+{
+    if (__all_sync(kFull, mbar_try_wait(bar, parity)))
+        return true;
+    return wait_slow(bar, parity, limit_ns, status);
+}
+
 // ---------------------------------------------------------------- dtypes
 
 template <int T> struct Elem;

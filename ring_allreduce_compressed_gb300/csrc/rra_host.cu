@@ -91,29 +91,6 @@ void note_call(rra_comm *c, cudaStream_t st)
 
 int warps_for(int N) { return std::min(N, kMaxWarps); }
 
-// Mailbox depth and staging depth that fit the opt-in shared memory: the
-// requested (or default) depths first, then smaller ones.
-bool pick_depths(rra_comm *c, int N, int slot_bytes, int stage_bytes, int warps, bool fast,
-                 bool sparse, int extra, int *K, int *D, int *smem)
-{
-    const int k0 = c->tune_K ? c->tune_K : 2;
-    const int d0 = c->tune_D ? c->tune_D : 4;
-    for (int k = k0; k >= 1; --k)
-        for (int d = d0; d >= 1; --d) {
-            if (!fast && d != d0)
-                continue;
-            const Layout L = make_layout(N, k, fast ? d : 1, slot_bytes, stage_bytes, warps, fast,
-                                         sparse);
-            if (L.total + extra <= c->smem_optin) {
-                *K = k;
-                *D = fast ? d : 1;
-                *smem = L.total + extra;
-                return true;
-            }
-        }
-    return false;
-}
-
 int grid_for(rra_comm *c, long long key, const void *fn, int warps, int smem, long long items)
 {
     const long long k = key * (1LL << 20) + smem;
@@ -369,7 +346,6 @@ rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count
     a.root = root;
     a.T = (long long)count;
     a.n = (a.T + N - 1) / N;
-    a.tiles = which == 0 ? (a.n + kTile - 1) / kTile : (a.T + kTile - 1) / kTile;
     a.timeout_ns = comm->timeout_ns;
     a.status = comm->status;
     a.withhold_rank = comm->withhold_rank;
@@ -380,42 +356,57 @@ rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count
         fast = fast && al16(buf[r]);
     }
     const int warps = warps_for(N);
-    a.slot_bytes = kTile * (int)es;
-    a.stage_bytes = kTile * (int)es;
-    const int extra = which == 2 ? N * kTile * 4 : 0; // tree accumulators
-    int smem = 0;
-    if (!pick_depths(comm, N, a.slot_bytes, a.stage_bytes, warps, fast, false, extra, &a.K, &a.D,
-                     &smem)) {
-        fast = false;
-        if (!pick_depths(comm, N, a.slot_bytes, a.stage_bytes, warps, false, false, extra, &a.K,
-                         &a.D, &smem))
-            return RRA_ERR_UNSUPPORTED;
+    const bool one = warps == N;
+    // allgather: ring edges, every rank stages its chunk; broadcast: one edge
+    // into each rank, the root stages; tree: a reduce and a broadcast edge into
+    // each rank, every rank stages (and accumulates in) its slice
+    const int edges = which == 2 ? 2 * N : N;
+    const int stagers = which == 1 ? 1 : N;
+    const long long range = which == 0 ? a.n : a.T; // elements per rank walked in slices
+    const int sms = num_sms();
+    // widest slice that leaves every SM work and room for three, two or one
+    // blocks per SM; ring edges need two slots (a rank holds its slot while it
+    // forwards), tree edges can make do with one
+    int G = 0, smem = 0;
+    static const int kG[] = {4, 2, 1};
+    for (int pass = 0; pass < 3 && !G; ++pass) {
+        const int per_sm = 3 - pass;
+        for (int g : kG) {
+            if (comm->tune_G && g != comm->tune_G)
+                continue;
+            if (!comm->tune_G && g > 1 && (range + (long long)kTile * g - 1) / ((long long)kTile * g) < sms)
+                continue;
+            const int bytes = kTile * g * (int)es;
+            bool found = false;
+            for (int K = comm->tune_K ? comm->tune_K : 2; K >= (which == 0 ? 2 : 1) && !found; --K)
+                for (int D = fast ? (comm->tune_D ? comm->tune_D : 2) : 1; D >= 1 && !found; --D) {
+                    const CollLayout L =
+                        coll_layout(N, edges, K, stagers, D, bytes, bytes, fast || which == 2);
+                    if (per_sm * (L.total + 1024) <= comm->smem_per_sm &&
+                        L.total <= comm->smem_optin) {
+                        G = g;
+                        a.K = K;
+                        a.D = D;
+                        smem = L.total;
+                        found = true;
+                    }
+                }
+            if (G)
+                break;
+        }
     }
-    int occ = 0;
-    const long long k = (long long)(which * 10 + (fast ? 1 : 0) + 50000) * (1LL << 20) + smem;
-    auto it = comm->occ.find(k);
-    if (it != comm->occ.end()) {
-        occ = it->second;
-    } else {
-        if (copy_kernel_attrs(which, fast, smem, warps, &occ) != cudaSuccess || occ < 1)
-            occ = 1;
-        comm->occ[k] = occ;
-    }
-    if (comm->tune_blocks)
-        occ = std::min(occ, comm->tune_blocks);
-    long long g = (long long)num_sms() * occ;
-    if (a.tiles < g)
-        g = a.tiles;
-    const int grid = (int)std::max(1LL, g);
+    if (!G)
+        return RRA_ERR_UNSUPPORTED;
+    a.slot_bytes = a.stage_bytes = kTile * G * (int)es;
+    a.tiles = (range + (long long)kTile * G - 1) / ((long long)kTile * G);
+    const void *fn = coll_fn(which, (int)es, G, fast, one);
+    if (!fn)
+        return RRA_ERR_UNSUPPORTED;
+    const long long key = 50000 + which * 1000 + (int)es * 100 + G * 10 + (fast ? 2 : 0) + (one ? 1 : 0);
+    const int grid = grid_for(comm, key, fn, warps, smem, a.tiles);
     counter_sets(comm, &a.sent, &a.recv, &a.zero);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (which == 0)
-        e = launch_allgather(fast, a, grid, warps, smem, st);
-    else if (which == 1)
-        e = launch_broadcast(fast, a, grid, warps, smem, st);
-    else
-        e = launch_tree(fast, a, grid, warps, smem, st);
+    const cudaError_t e = launch_coll(fn, a, grid, warps, smem, st);
     note_call(comm, st);
     return e == cudaSuccess ? RRA_OK : RRA_ERR_CUDA;
 }
@@ -446,6 +437,16 @@ static cudaError_t allow_smem(const void *fn, int smem)
     if (e == cudaSuccess)
         have = smem;
     return e;
+}
+
+cudaError_t launch_coll(const void *fn, const CopyArgs &a, int grid, int warps, int smem,
+                        cudaStream_t st)
+{
+    cudaError_t e = allow_smem(fn, smem);
+    if (e != cudaSuccess)
+        return e;
+    void *args[] = {const_cast<CopyArgs *>(&a)};
+    return cudaLaunchKernel(fn, dim3(grid), dim3(warps * 32), args, (size_t)smem, st);
 }
 
 cudaError_t launch_ring(const void *fn, const RingArgs &a, int grid, int warps, int smem,

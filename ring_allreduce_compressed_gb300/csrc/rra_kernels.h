@@ -105,18 +105,47 @@ __host__ __device__ inline Layout make_layout(int N, int K, int D, int slot_byte
     return L;
 }
 
+// Shared-memory layout of the allgather / broadcast / tree kernels: `edges`
+// slot FIFOs of K slots (full and empty barrier each), D stages for each of
+// `stagers` ranks, per-rank byte counters.
+struct CollLayout {
+    int full, empty, stage_bar, counters, slots, stages, total;
+};
+
+__host__ __device__ inline CollLayout coll_layout(int N, int edges, int K, int stagers, int D,
+                                                  int slot_bytes, int stage_bytes, bool stage)
+{
+    CollLayout L;
+    int off = 0;
+    L.full = off;
+    off += edges * K * 8;
+    L.empty = off;
+    off += edges * K * 8;
+    L.stage_bar = off;
+    off += stagers * D * 8;
+    L.counters = off;
+    off += N * 16;
+    off = align_up(off, 128);
+    L.slots = off;
+    off += edges * K * slot_bytes;
+    off = align_up(off, 128);
+    L.stages = off;
+    off += stage ? stagers * D * stage_bytes : 0;
+    L.total = align_up(off, 128);
+    return L;
+}
+
 // Kernel entry points (one per translation unit family).  Each returns the
 // launch's cudaError_t.
 cudaError_t launch_ring(const void *fn, const RingArgs &a, int grid, int warps, int smem,
                         cudaStream_t st);
 
-cudaError_t launch_allgather(bool fast, const CopyArgs &a, int grid, int warps, int smem,
-                             cudaStream_t st);
-cudaError_t launch_broadcast(bool fast, const CopyArgs &a, int grid, int warps, int smem,
-                             cudaStream_t st);
-cudaError_t launch_tree(bool fast, const CopyArgs &a, int grid, int warps, int smem,
+// Allgather (which 0), broadcast (1) or tree allreduce (2) kernel for
+// element size es, slice width 256 * groups, staged or generic path, one rank
+// per warp or several; nullptr if not instantiated.
+const void *coll_fn(int which, int es, int groups, bool fast, bool one);
+cudaError_t launch_coll(const void *fn, const CopyArgs &a, int grid, int warps, int smem,
                         cudaStream_t st);
-cudaError_t copy_kernel_attrs(int which, bool fast, int smem, int warps, int *blocks_per_sm);
 
 // Standalone codec kernels.
 cudaError_t launch_bfp_encode(const void *x, long long n, int dtype, int bits, int8_t *exps,
