@@ -333,6 +333,65 @@ rra_status rra_set_timeout(rra_comm *comm, uint64_t ns);
 rra_status rra_comm_set_tuning(rra_comm *comm, int blocks_per_sm, int mailbox_depth,
                                int stage_depth, int slice_groups);
 
+/* The launch shape of the last ring call (rra_ring_allreduce,
+ * rra_reduce_scatter, rra_allreduce_auto's ring leg): resident blocks per SM,
+ * mailbox slots per ring edge, staging depth, 256-element groups per slice.
+ * Errors: RRA_ERR_INVALID for NULL arguments. */
+rra_status rra_comm_last_shape(rra_comm *comm, int *blocks_per_sm, int *mailbox_depth,
+                               int *stage_depth, int *slice_groups);
+
+/*
+ * Measured launch-shape tuning of the ring allreduce (the pages' pipeline
+ * chunk size, CCCL §2.2 and §3.3, which suggest 1-4 MB pieces and leave the
+ * choice to the workload).  Runs the allreduce described by the arguments
+ * (same meaning as rra_ring_allreduce) once per candidate shape -- slice
+ * widths 8, 4, 2, 1 x 256 elements, staging depths 1-4, 2-4 or all
+ * resident blocks per SM -- times each on `stream` with CUDA events, and
+ * remembers the fastest for this communicator and this call's (codec, input
+ * kind, output dtype, alignment, count).  Later ring allreduce calls with
+ * the same key use it, unless rra_comm_set_tuning set a manual shape.  The
+ * final call runs with the chosen shape, so `out` holds its result on
+ * return.  Results are bit-identical for every shape; only time differs.
+ * Synchronous: it waits on events, so it must not be called while `stream`
+ * is being captured (RRA_ERR_INVALID).  Errors: as rra_ring_allreduce;
+ * a device time-out in any candidate is returned and nothing is stored.
+ */
+rra_status rra_autotune(rra_comm *comm, const void *const *in, void *const *out, size_t count,
+                        rra_dtype in_t, rra_dtype out_t, const rra_codec *codec, void *stream);
+
+/* Size-based choice between ring and tree ([ring] section "真实世界中的生产模式":
+ * pick ring or tree by message size, from measurement; section "练习": add
+ * the tree variant, switch by size and measure the crossover).  The default
+ * crossover is the one measured on GB300 for N = 2..64: the ring is never
+ * slower than the tree from 4 MiB per rank on. */
+#define RRA_DEFAULT_CROSSOVER (4ull << 20)
+#define RRA_ALGO_RING 0
+#define RRA_ALGO_TREE 1
+
+/* In-place allreduce of buf[r][0..count) that runs rra_tree_allreduce when
+ * count * sizeof(dtype) is below the communicator's crossover and dtype is
+ * fp32 (the tree sums fp32 only), otherwise the lossless rra_ring_allreduce
+ * in place.  The two algorithms add in different orders, so their results
+ * may differ in the last bits; *algorithm (if not NULL) reports which ran
+ * (RRA_ALGO_RING / RRA_ALGO_TREE).  Errors: as the chosen operation. */
+rra_status rra_allreduce_auto(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,
+                              void *stream, int *algorithm);
+
+/* Crossover of rra_allreduce_auto in bytes per rank (0 restores
+ * RRA_DEFAULT_CROSSOVER).  Errors: RRA_ERR_INVALID for NULL. */
+rra_status rra_set_crossover(rra_comm *comm, size_t bytes_per_rank);
+rra_status rra_get_crossover(rra_comm *comm, size_t *bytes_per_rank);
+
+/* Measure the crossover on this GPU: times the in-place ring and tree
+ * allreduce of buf at 256 * 4^k fp32 elements per rank (k = 0, 1, ..., up
+ * to count) and sets the communicator's crossover to the smallest measured
+ * size from which on the ring is never slower (one byte above the largest
+ * size if the tree always wins).  buf's contents are overwritten.  fp32
+ * only.  Synchronous; not during a stream capture (RRA_ERR_INVALID).  The
+ * result is also stored in *bytes_per_rank if not NULL. */
+rra_status rra_autotune_crossover(rra_comm *comm, void *const *buf, size_t count,
+                                  rra_dtype dtype, void *stream, size_t *bytes_per_rank);
+
 /* Test-only fault injection: in the next collective call, simulated rank
  * "rank" does not publish the message it sends at ring step "step" (1-based,
  * counted over both passes) for the first slice each block handles, so its

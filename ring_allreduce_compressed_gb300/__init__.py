@@ -23,6 +23,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "librra.so")
 
 RRA_OK, RRA_ERR_INVALID, RRA_ERR_UNSUPPORTED, RRA_ERR_CUDA, RRA_ERR_TIMEOUT, RRA_ERR_NOMEM = range(6)
+RRA_ALGO_RING, RRA_ALGO_TREE = 0, 1
+RRA_DEFAULT_CROSSOVER = 4 << 20
 RRA_F32, RRA_F16, RRA_BF16 = 0, 1, 2
 CODEC_NONE, CODEC_BFP, CODEC_SPARSE = 0, 1, 2
 MAX_RANKS = 64
@@ -75,13 +77,21 @@ def lib():
         L.rra_set_timeout.argtypes = [vp, C.c_uint64]
         L.rra_debug_withhold.argtypes = [vp, i32, i32]
         L.rra_comm_set_tuning.argtypes = [vp, i32, i32, i32, i32]
+        L.rra_comm_last_shape.argtypes = [vp] + [C.POINTER(C.c_int)] * 4
+        L.rra_autotune.argtypes = [vp, vp, vp, sz, i32, i32, vp, vp]
+        L.rra_allreduce_auto.argtypes = [vp, vp, sz, i32, vp, C.POINTER(C.c_int)]
+        L.rra_set_crossover.argtypes = [vp, sz]
+        L.rra_get_crossover.argtypes = [vp, C.POINTER(C.c_size_t)]
+        L.rra_autotune_crossover.argtypes = [vp, vp, sz, i32, vp, C.POINTER(C.c_size_t)]
         L.rra_status_string.argtypes = [i32]
         L.rra_status_string.restype = C.c_char_p
         for name in ("rra_comm_create", "rra_comm_destroy", "rra_ring_allreduce",
                      "rra_reduce_scatter", "rra_allgather", "rra_broadcast", "rra_tree_allreduce",
                      "rra_bfp_encode", "rra_bfp_decode", "rra_sparse_encode", "rra_sparse_decode",
                      "rra_diff_encode", "rra_get_bytes", "rra_comm_status", "rra_set_timeout",
-                     "rra_debug_withhold", "rra_comm_set_tuning"):
+                     "rra_debug_withhold", "rra_comm_set_tuning", "rra_comm_last_shape",
+                     "rra_autotune", "rra_allreduce_auto", "rra_set_crossover",
+                     "rra_get_crossover", "rra_autotune_crossover"):
             getattr(L, name).restype = st
         _lib = L
     return _lib
@@ -217,6 +227,46 @@ class Comm:
         """Launch tuning of the fused kernels (0 = automatic)."""
         _check(lib().rra_comm_set_tuning(self._h, blocks_per_sm, mailbox_depth, stage_depth,
                                          slice_groups), "rra_comm_set_tuning")
+
+    def last_shape(self):
+        """(blocks per SM, mailbox depth, staging depth, slice groups) of the
+        last ring launch."""
+        v = [C.c_int() for _ in range(4)]
+        _check(lib().rra_comm_last_shape(self._h, *[C.byref(x) for x in v]),
+               "rra_comm_last_shape")
+        return tuple(x.value for x in v)
+
+    def autotune(self, inputs, outputs, codec: Optional[Codec] = None, stream=None):
+        """Time the ring allreduce of these arguments in every candidate
+        launch shape and keep the fastest for later calls with the same
+        codec, dtypes and count (rra_autotune); returns that shape."""
+        self._reduce(lib().rra_autotune, "rra_autotune", inputs, outputs, codec, stream)
+        return self.last_shape()
+
+    def allreduce_auto(self, bufs, stream=None) -> int:
+        """In-place allreduce, tree below the crossover (fp32), ring above;
+        returns RRA_ALGO_RING or RRA_ALGO_TREE."""
+        algo = C.c_int(-1)
+        _check(lib().rra_allreduce_auto(self._h, _ptrs(bufs, "bufs"), bufs[0].numel(),
+                                        _dtype_code(bufs[0].dtype), _stream(stream),
+                                        C.byref(algo)), "rra_allreduce_auto")
+        return algo.value
+
+    def set_crossover(self, bytes_per_rank: int = 0):
+        _check(lib().rra_set_crossover(self._h, int(bytes_per_rank)), "rra_set_crossover")
+
+    def crossover(self) -> int:
+        v = C.c_size_t()
+        _check(lib().rra_get_crossover(self._h, C.byref(v)), "rra_get_crossover")
+        return v.value
+
+    def autotune_crossover(self, bufs, stream=None) -> int:
+        """Measure the ring/tree crossover on bufs (overwritten); returns it."""
+        v = C.c_size_t()
+        _check(lib().rra_autotune_crossover(self._h, _ptrs(bufs, "bufs"), bufs[0].numel(),
+                                            _dtype_code(bufs[0].dtype), _stream(stream),
+                                            C.byref(v)), "rra_autotune_crossover")
+        return v.value
 
     def debug_withhold(self, rank: int, step: int):
         _check(lib().rra_debug_withhold(self._h, rank, step), "rra_debug_withhold")

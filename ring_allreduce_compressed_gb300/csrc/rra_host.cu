@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <array>
+#include <vector>
 #include <cstdint>
 #include <cstring>
 #include <map>
@@ -38,10 +40,12 @@ struct rra_comm {
     bool have_last = false;
     int smem_optin = 0;
     int smem_per_sm = 0;
-    int tune_blocks = 0; // 0: automatic
-    int tune_K = 0;
-    int tune_D = 0;
-    int tune_G = 0;
+    rra::Tune tune;      // manual tuning (rra_comm_set_tuning); zeros: automatic
+    // measured best ring shapes (rra_autotune), by (op, codec, input kind,
+    // output dtype, staged path, count)
+    std::map<std::array<long long, 6>, rra::Tune> tuned;
+    rra::Tune last{};      // shape of the last ring launch (blocks = blocks per SM)
+    size_t crossover = 0;  // rra_allreduce_auto: tree below this many bytes per rank
     std::map<long long, int> occ; // (kernel key, smem) -> blocks per SM
 };
 
@@ -91,7 +95,29 @@ void note_call(rra_comm *c, cudaStream_t st)
 
 int warps_for(int N) { return std::min(N, kMaxWarps); }
 
-int grid_for(rra_comm *c, long long key, const void *fn, int warps, int smem, long long items)
+// Largest dynamic shared memory already allowed for each kernel (per device),
+// so the attribute is set once per kernel rather than on every launch.
+std::mutex g_attr_mu;
+std::map<std::pair<int, const void *>, int> g_attr_smem;
+
+cudaError_t allow_smem(const void *fn, int smem)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    int &have = g_attr_smem[{dev, fn}];
+    if (smem <= have)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        have = smem;
+    return e;
+}
+
+int grid_for(rra_comm *c, long long key, const void *fn, int warps, int smem, long long items,
+             int blocks_cap = 0, int *per_sm = nullptr)
 {
     const long long k = key * (1LL << 20) + smem;
     int occ = 0;
@@ -99,15 +125,18 @@ int grid_for(rra_comm *c, long long key, const void *fn, int warps, int smem, lo
     if (it != c->occ.end()) {
         occ = it->second;
     } else {
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        // raise (never lower) the kernel's shared-memory limit before asking
+        allow_smem(fn, smem);
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, warps * 32, (size_t)smem) !=
                 cudaSuccess ||
             occ < 1)
             occ = 1;
         c->occ[k] = occ;
     }
-    if (c->tune_blocks)
-        occ = std::min(occ, c->tune_blocks);
+    if (blocks_cap)
+        occ = std::min(occ, blocks_cap);
+    if (per_sm)
+        *per_sm = occ;
     long long g = (long long)num_sms() * occ;
     if (items < g)
         g = items;
@@ -145,8 +174,8 @@ struct LaunchShape {
     bool fast;
 };
 
-bool pick_shape(rra_comm *c, int N, long long n, int kc, int ies, bool diff, bool fast,
-                int warps, LaunchShape *out)
+bool pick_shape(rra_comm *c, const Tune &t, int N, long long n, int kc, int ies, bool diff,
+                bool fast, int warps, LaunchShape *out)
 {
     const int sms = num_sms();
     static const int kGD[][2] = {{8, 2}, {8, 1}, {4, 2}, {4, 1}, {2, 4},
@@ -154,12 +183,12 @@ bool pick_shape(rra_comm *c, int N, long long n, int kc, int ies, bool diff, boo
     const bool sparse = kc == kCodecSparse;
     // a requested slice width is tried first on its own; passes 2 and 3 are
     // the automatic choice
-    for (int pass = c->tune_G && !sparse ? 0 : 2; pass < 4; ++pass) {
+    for (int pass = t.G && !sparse ? 0 : 2; pass < 4; ++pass) {
         for (const auto &gd : kGD) {
             const int G = gd[0];
-            if (pass < 2 && G != c->tune_G)
+            if (pass < 2 && G != t.G)
                 continue;
-            int D = c->tune_D ? c->tune_D : gd[1];
+            int D = t.D ? t.D : gd[1];
             if (sparse && G != 1)
                 continue;
             // a short chunk is cut into narrower slices while a wider one
@@ -173,7 +202,7 @@ bool pick_shape(rra_comm *c, int N, long long n, int kc, int ies, bool diff, boo
             // wider messages need two slots per ring edge: a rank frees the
             // slot it streams from only after its own send of the same step,
             // so with one slot every rank would wait for its successor
-            for (int K = c->tune_K ? c->tune_K : 2; K >= (G == 1 ? 1 : 2); --K) {
+            for (int K = t.K ? t.K : 2; K >= (G == 1 ? 1 : 2); --K) {
                 const Layout L = make_layout(N, K, D, slot, stage, warps, fast, sparse);
                 const bool three = pass % 2 == 0; // leave room for three blocks per SM
                 const int need = three ? 3 * (L.total + 1024) : L.total;
@@ -188,9 +217,12 @@ bool pick_shape(rra_comm *c, int N, long long n, int kc, int ies, bool diff, boo
     return false;
 }
 
+// force: an explicit launch shape (autotuning); otherwise the manual tuning,
+// else a measured shape for this call's key, else the automatic choice.
 rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *const *out,
                        size_t count, rra_dtype in_t, rra_dtype out_t, const rra_codec *codec,
-                       void *stream)
+                       void *stream, const Tune *force = nullptr,
+                       std::array<long long, 6> *key_out = nullptr)
 {
     if (!comm || !in || !out || count == 0 || count > comm->max_count || !valid_dtype(in_t) ||
         !valid_dtype(out_t))
@@ -290,10 +322,23 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     a.vec_base = (cd.diff_base && al16(cd.diff_base) && (a.n * 4) % 16 == 0) ? 1 : 0;
 
     const int warps = warps_for(N);
+    const int kin = cd.diff_prev ? kF32Diff : (int)in_t; // kernel input kind
+    const std::array<long long, 6> tkey = {mode, kc, kin, (long long)out_t, fast ? 1 : 0,
+                                           (long long)count};
+    if (key_out)
+        *key_out = tkey;
+    Tune t = comm->tune;
+    if (force) {
+        t = *force;
+    } else if (!t.any()) {
+        const auto it = comm->tuned.find(tkey);
+        if (it != comm->tuned.end())
+            t = it->second;
+    }
     LaunchShape sh;
-    if (!pick_shape(comm, N, a.n, kc, (int)ies, cd.diff_prev != nullptr, fast, warps, &sh)) {
+    if (!pick_shape(comm, t, N, a.n, kc, (int)ies, cd.diff_prev != nullptr, fast, warps, &sh)) {
         fast = false;
-        if (!pick_shape(comm, N, a.n, kc, (int)ies, cd.diff_prev != nullptr, false, warps, &sh))
+        if (!pick_shape(comm, t, N, a.n, kc, (int)ies, cd.diff_prev != nullptr, false, warps, &sh))
             return RRA_ERR_UNSUPPORTED;
     }
     const int groups = sh.groups, smem = sh.smem;
@@ -304,13 +349,14 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     a.tiles = (a.n + kTile * groups - 1) / (kTile * groups);
     // every warp plays exactly one rank when N fits the block
     const int rmap = warps != N ? kRanksShared : (warps <= 8 ? kRankPerWarp8 : kRankPerWarp16);
-    const int kin = cd.diff_prev ? kF32Diff : (int)in_t; // kernel input kind
     const void *fn = ring_fn(kc, kin, fast, groups, rmap);
     if (!fn)
         return RRA_ERR_UNSUPPORTED;
     const long long key = 100000 + kc * 10000 + kin * 1000 + (fast ? 100 : 0) + rmap * 10 +
                           groups;
-    const int grid = grid_for(comm, key, fn, warps, smem, a.tiles);
+    int per_sm = 0;
+    const int grid = grid_for(comm, key, fn, warps, smem, a.tiles, t.blocks, &per_sm);
+    comm->last = Tune{per_sm, a.K, a.D, groups};
     counter_sets(comm, &a.sent, &a.recv, &a.zero);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = launch_ring(fn, a, grid, warps, smem, st);
@@ -372,14 +418,14 @@ rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count
     for (int pass = 0; pass < 3 && !G; ++pass) {
         const int per_sm = 3 - pass;
         for (int g : kG) {
-            if (comm->tune_G && g != comm->tune_G)
+            if (comm->tune.G && g != comm->tune.G)
                 continue;
-            if (!comm->tune_G && g > 1 && (range + (long long)kTile * g - 1) / ((long long)kTile * g) < sms)
+            if (!comm->tune.G && g > 1 && (range + (long long)kTile * g - 1) / ((long long)kTile * g) < sms)
                 continue;
             const int bytes = kTile * g * (int)es;
             bool found = false;
-            for (int K = comm->tune_K ? comm->tune_K : 2; K >= (which == 0 ? 2 : 1) && !found; --K)
-                for (int D = fast ? (comm->tune_D ? comm->tune_D : 2) : 1; D >= 1 && !found; --D) {
+            for (int K = comm->tune.K ? comm->tune.K : 2; K >= (which == 0 ? 2 : 1) && !found; --K)
+                for (int D = fast ? (comm->tune.D ? comm->tune.D : 2) : 1; D >= 1 && !found; --D) {
                     const CollLayout L =
                         coll_layout(N, edges, K, stagers, D, bytes, bytes, fast || which == 2);
                     if (per_sm * (L.total + 1024) <= comm->smem_per_sm &&
@@ -403,7 +449,7 @@ rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count
     if (!fn)
         return RRA_ERR_UNSUPPORTED;
     const long long key = 50000 + which * 1000 + (int)es * 100 + G * 10 + (fast ? 2 : 0) + (one ? 1 : 0);
-    const int grid = grid_for(comm, key, fn, warps, smem, a.tiles);
+    const int grid = grid_for(comm, key, fn, warps, smem, a.tiles, comm->tune.blocks);
     counter_sets(comm, &a.sent, &a.recv, &a.zero);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const cudaError_t e = launch_coll(fn, a, grid, warps, smem, st);
@@ -418,27 +464,6 @@ std::map<int, std::pair<uint32_t *, long long>> g_ws;
 } // namespace
 
 namespace rra {
-// Largest dynamic shared memory already allowed for each kernel (per device),
-// so the attribute is set once per kernel rather than on every launch.
-static std::mutex g_attr_mu;
-static std::map<std::pair<int, const void *>, int> g_attr_smem;
-
-static cudaError_t allow_smem(const void *fn, int smem)
-{
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    std::lock_guard<std::mutex> lk(g_attr_mu);
-    int &have = g_attr_smem[{dev, fn}];
-    if (smem <= have)
-        return cudaSuccess;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)
-        have = smem;
-    return e;
-}
-
 cudaError_t launch_coll(const void *fn, const CopyArgs &a, int grid, int warps, int smem,
                         cudaStream_t st)
 {
@@ -689,10 +714,10 @@ rra_status rra_comm_set_tuning(rra_comm *comm, int blocks_per_sm, int mailbox_de
         !(slice_groups == 0 || slice_groups == 1 || slice_groups == 2 || slice_groups == 4 ||
           slice_groups == 8))
         return RRA_ERR_INVALID;
-    comm->tune_blocks = blocks_per_sm;
-    comm->tune_K = mailbox_depth;
-    comm->tune_D = stage_depth;
-    comm->tune_G = slice_groups;
+    comm->tune.blocks = blocks_per_sm;
+    comm->tune.K = mailbox_depth;
+    comm->tune.D = stage_depth;
+    comm->tune.G = slice_groups;
     return RRA_OK;
 }
 
@@ -702,6 +727,206 @@ rra_status rra_debug_withhold(rra_comm *comm, int rank, int step)
         return RRA_ERR_INVALID;
     comm->withhold_rank = rank < 0 ? -1 : rank;
     comm->withhold_step = step;
+    return RRA_OK;
+}
+
+rra_status rra_comm_last_shape(rra_comm *comm, int *blocks_per_sm, int *mailbox_depth,
+                               int *stage_depth, int *slice_groups)
+{
+    if (!comm || !blocks_per_sm || !mailbox_depth || !stage_depth || !slice_groups)
+        return RRA_ERR_INVALID;
+    *blocks_per_sm = comm->last.blocks;
+    *mailbox_depth = comm->last.K;
+    *stage_depth = comm->last.D;
+    *slice_groups = comm->last.G;
+    return RRA_OK;
+}
+
+rra_status rra_autotune(rra_comm *comm, const void *const *in, void *const *out, size_t count,
+                        rra_dtype in_t, rra_dtype out_t, const rra_codec *codec, void *stream)
+{
+    if (!comm)
+        return RRA_ERR_INVALID;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone)
+        return RRA_ERR_INVALID; // it waits on events: not inside a capture
+    // the automatic shape first: checks the arguments, warms up, gives the key
+    std::array<long long, 6> key{};
+    const Tune autoshape{};
+    rra_status s = ring_common(comm, kModeAllreduce, in, out, count, in_t, out_t, codec, stream,
+                               &autoshape, &key);
+    if (s != RRA_OK)
+        return s;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        if (e0)
+            cudaEventDestroy(e0);
+        return RRA_ERR_CUDA;
+    }
+    // best of a few calls of one shape (fewer for long calls)
+    auto time_shape = [&](const Tune &t, float *best_ms) -> rra_status {
+        *best_ms = 1e30f;
+        for (int rep = 0; rep < 4; ++rep) {
+            if (cudaEventRecord(e0, st) != cudaSuccess)
+                return RRA_ERR_CUDA;
+            const rra_status r =
+                ring_common(comm, kModeAllreduce, in, out, count, in_t, out_t, codec, stream, &t);
+            if (r != RRA_OK)
+                return r;
+            float ms = 0.0f;
+            if (cudaEventRecord(e1, st) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+                cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess)
+                return RRA_ERR_CUDA;
+            if (rep > 0) // the first call of a shape warms it up
+                *best_ms = std::min(*best_ms, ms);
+            if (rep >= 2 && ms > 2.0f)
+                break;
+        }
+        return RRA_OK;
+    };
+    Tune best{};
+    float best_ms = 1e30f;
+    std::vector<std::array<int, 4>> seen;
+    static const int kG[] = {8, 4, 2, 1}, kD[] = {1, 2, 3, 4}, kB[] = {0, 2, 3, 4};
+    for (int G : kG)
+        for (int D : kD)
+            for (int B : kB) {
+                if (s != RRA_OK)
+                    break;
+                const Tune cand{B, 0, D, G};
+                float ms = 0.0f;
+                s = time_shape(cand, &ms);
+                if (s == RRA_ERR_UNSUPPORTED) { // this shape does not fit: skip it
+                    s = RRA_OK;
+                    continue;
+                }
+                if (s != RRA_OK)
+                    break;
+                // different requests can land on the same launch shape
+                const std::array<int, 4> got = {comm->last.blocks, comm->last.K, comm->last.D,
+                                                comm->last.G};
+                if (std::find(seen.begin(), seen.end(), got) != seen.end())
+                    continue;
+                seen.push_back(got);
+                if (ms < best_ms) {
+                    best_ms = ms;
+                    best = Tune{got[0], got[1], got[2], got[3]};
+                }
+            }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (s != RRA_OK)
+        return s;
+    // a candidate that timed out latches the status word: report it, keep nothing
+    s = rra_comm_status(comm);
+    if (s != RRA_OK)
+        return s;
+    comm->tuned[key] = best;
+    // leave the outputs of a call with the chosen shape
+    return ring_common(comm, kModeAllreduce, in, out, count, in_t, out_t, codec, stream);
+}
+
+rra_status rra_set_crossover(rra_comm *comm, size_t bytes_per_rank)
+{
+    if (!comm)
+        return RRA_ERR_INVALID;
+    comm->crossover = bytes_per_rank;
+    return RRA_OK;
+}
+
+rra_status rra_get_crossover(rra_comm *comm, size_t *bytes_per_rank)
+{
+    if (!comm || !bytes_per_rank)
+        return RRA_ERR_INVALID;
+    *bytes_per_rank = comm->crossover ? comm->crossover : RRA_DEFAULT_CROSSOVER;
+    return RRA_OK;
+}
+
+rra_status rra_allreduce_auto(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,
+                              void *stream, int *algorithm)
+{
+    if (!comm || !buf || !valid_dtype(dtype))
+        return RRA_ERR_INVALID;
+    const size_t cross = comm->crossover ? comm->crossover : RRA_DEFAULT_CROSSOVER;
+    // the tree sums fp32 only; other dtypes always take the ring
+    const bool tree = dtype == RRA_F32 && count * esize(dtype) < cross;
+    if (algorithm)
+        *algorithm = tree ? RRA_ALGO_TREE : RRA_ALGO_RING;
+    if (tree)
+        return copy_common(comm, 2, buf, count, dtype, 0, stream);
+    return ring_common(comm, kModeAllreduce, reinterpret_cast<const void *const *>(buf), buf,
+                       count, dtype, dtype, nullptr, stream);
+}
+
+rra_status rra_autotune_crossover(rra_comm *comm, void *const *buf, size_t count,
+                                  rra_dtype dtype, void *stream, size_t *bytes_per_rank)
+{
+    if (!comm || !buf || dtype != RRA_F32 || count == 0 || count > comm->max_count)
+        return RRA_ERR_INVALID;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone)
+        return RRA_ERR_INVALID;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        if (e0)
+            cudaEventDestroy(e0);
+        return RRA_ERR_CUDA;
+    }
+    rra_status s = RRA_OK;
+    auto time_op = [&](bool tree, size_t n, float *best_ms) -> rra_status {
+        *best_ms = 1e30f;
+        for (int rep = 0; rep < 4; ++rep) {
+            if (cudaEventRecord(e0, st) != cudaSuccess)
+                return RRA_ERR_CUDA;
+            const rra_status r =
+                tree ? copy_common(comm, 2, buf, n, dtype, 0, stream)
+                     : ring_common(comm, kModeAllreduce, reinterpret_cast<const void *const *>(buf),
+                                   buf, n, dtype, dtype, nullptr, stream);
+            if (r != RRA_OK)
+                return r;
+            float ms = 0.0f;
+            if (cudaEventRecord(e1, st) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+                cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess)
+                return RRA_ERR_CUDA;
+            if (rep > 0)
+                *best_ms = std::min(*best_ms, ms);
+        }
+        return RRA_OK;
+    };
+    // sizes 1 KiB * 4^k per rank up to count: the crossover is the smallest
+    // measured size from which on the ring is never slower than the tree
+    std::vector<std::pair<size_t, bool>> ring_wins;
+    for (size_t n = 256; s == RRA_OK; n = n * 4 > count && n < count ? count : n * 4) {
+        float tr = 0.0f, tt = 0.0f;
+        s = time_op(false, n, &tr);
+        if (s == RRA_OK)
+            s = time_op(true, n, &tt);
+        if (s == RRA_OK)
+            ring_wins.push_back({n * 4, tr <= tt});
+        if (n >= count)
+            break;
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (s == RRA_OK)
+        s = rra_comm_status(comm);
+    if (s != RRA_OK)
+        return s;
+    size_t cross = ring_wins.back().second ? ring_wins.back().first : ring_wins.back().first + 1;
+    for (size_t i = ring_wins.size(); i-- > 0;) {
+        if (!ring_wins[i].second)
+            break;
+        cross = ring_wins[i].first;
+    }
+    comm->crossover = cross;
+    if (bytes_per_rank)
+        *bytes_per_rank = cross;
     return RRA_OK;
 }
 

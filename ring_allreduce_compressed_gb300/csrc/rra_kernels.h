@@ -13,6 +13,13 @@ constexpr int kMaxWarps = 16; // warps per block; ranks per warp = ceil(N / warp
 
 enum Codec { kCodecNone = 0, kCodecBfp8 = 1, kCodecBfp4 = 2, kCodecSparse = 3 };
 enum Mode { kModeAllreduce = 0, kModeReduceScatter = 1 };
+
+// Launch shape of a ring kernel: blocks per SM, mailbox slots per edge,
+// staging depth, 256-element groups per slice.  Zero fields: automatic.
+struct Tune {
+    int blocks = 0, K = 0, D = 0, G = 0;
+    bool any() const { return blocks || K || D || G; }
+};
 // How simulated ranks map onto the warps of a ring kernel block.
 enum RankMap { kRanksShared = 0, kRankPerWarp8 = 1, kRankPerWarp16 = 2 };
 

@@ -63,6 +63,23 @@ def test_host_side_argument_checks(lib):
     assert L.rra_ring_allreduce(None, None, None, 10, 0, 0, None, None) == rra.RRA_ERR_INVALID
     assert L.rra_get_bytes(None, None, None) == rra.RRA_ERR_INVALID
     assert L.rra_comm_destroy(None) == rra.RRA_OK
+    assert L.rra_comm_last_shape(None, None, None, None, None) == rra.RRA_ERR_INVALID
+    assert L.rra_autotune(None, None, None, 10, 0, 0, None, None) == rra.RRA_ERR_INVALID
+    assert L.rra_allreduce_auto(None, None, 10, 0, None, None) == rra.RRA_ERR_INVALID
+    assert L.rra_set_crossover(None, 0) == rra.RRA_ERR_INVALID
+    assert L.rra_get_crossover(None, None) == rra.RRA_ERR_INVALID
+    assert L.rra_autotune_crossover(None, None, 10, 0, None, None) == rra.RRA_ERR_INVALID
+
+
+def test_header_constants_match_the_binding():
+    text = open(HEADER).read()
+    consts = dict(re.findall(r"#define (RRA_[A-Z_]+) \(?([0-9a-fx]+)", text))
+    assert int(consts["RRA_ALGO_RING"]) == rra.RRA_ALGO_RING
+    assert int(consts["RRA_ALGO_TREE"]) == rra.RRA_ALGO_TREE
+    m = re.search(r"#define RRA_DEFAULT_CROSSOVER \((\d+)ull << (\d+)\)", text)
+    assert int(m.group(1)) << int(m.group(2)) == rra.RRA_DEFAULT_CROSSOVER
+    assert int(consts["RRA_RING_SLICE"]) == rra.RING_SLICE
+    assert int(consts["RRA_BFP_BLOCK"]) == rra.BFP_BLOCK
 
 
 def _sources(folder, exts):
