@@ -217,13 +217,12 @@ template <int CODEC> struct WireCodec;
 
 // Lossless: fp32, group gi at byte 1024*gi, lane L at 32L within the group.
 template <> struct WireCodec<kCodecNone> {
-    static constexpr bool kSliced = true; // any slice length
     static constexpr int slot_bytes(int G) { return kTile * 4 * G; }
     struct Reg {
         float f[8];
     };
     __device__ __forceinline__ static void load(const unsigned char *slot, int gi, int lane,
-                                                unsigned char *, Reg &m)
+                                                unsigned char *, const RingArgs &, Reg &m)
     {
         const float4 *p = reinterpret_cast<const float4 *>(slot + gi * kTile * 4) + 2 * lane;
         const float4 a = p[0], b = p[1];
@@ -231,7 +230,7 @@ template <> struct WireCodec<kCodecNone> {
         m.f[4] = b.x; m.f[5] = b.y; m.f[6] = b.z; m.f[7] = b.w;
     }
     __device__ __forceinline__ static void store(unsigned char *slot, int gi, int lane,
-                                                 const Reg &m)
+                                                 const Reg &m, const RingArgs &)
     {
         float4 *p = reinterpret_cast<float4 *>(slot + gi * kTile * 4) + 2 * lane;
         p[0] = make_float4(m.f[0], m.f[1], m.f[2], m.f[3]);
@@ -264,7 +263,8 @@ template <> struct WireCodec<kCodecNone> {
         for (int i = 0; i < 8; ++i)
             v[i] = m.f[i];
     }
-    __device__ __forceinline__ static uint32_t bytes(int V, const unsigned char *)
+    __device__ __forceinline__ static uint32_t bytes(int V, const unsigned char *,
+                                                     const RingArgs &)
     {
         return 4u * (uint32_t)V;
     }
@@ -275,7 +275,6 @@ template <> struct WireCodec<kCodecNone> {
 // (group gi at 16 + gi * 256*BITS/8; lane L at 8L bytes (8-bit) or 4L bytes
 // (4-bit) within the group).
 template <int BITS> struct CodecBfp {
-    static constexpr bool kSliced = true;
     static constexpr int kMB = kTile * BITS / 8;
     static constexpr int slot_bytes(int G) { return 16 + kMB * G; }
     struct Reg {
@@ -283,7 +282,7 @@ template <int BITS> struct CodecBfp {
         int e;
     };
     __device__ __forceinline__ static void load(const unsigned char *slot, int gi, int lane,
-                                                unsigned char *, Reg &m)
+                                                unsigned char *, const RingArgs &, Reg &m)
     {
         m.e = (int)(int8_t)slot[2 * gi + (lane >> 4)];
         if constexpr (BITS == 8) {
@@ -296,7 +295,7 @@ template <int BITS> struct CodecBfp {
         }
     }
     __device__ __forceinline__ static void store(unsigned char *slot, int gi, int lane,
-                                                 const Reg &m)
+                                                 const Reg &m, const RingArgs &)
     {
         if ((lane & 15) == 0)
             slot[2 * gi + (lane >> 4)] = (unsigned char)(int8_t)m.e;
@@ -312,7 +311,12 @@ template <int BITS> struct CodecBfp {
     {
         Reg m;
         BfpGroup<BITS>::encode(v, m.e, m.w);
-        store(slot, gi, lane, m);
+        if ((lane & 15) == 0)
+            slot[2 * gi + (lane >> 4)] = (unsigned char)(int8_t)m.e;
+        if constexpr (BITS == 8)
+            reinterpret_cast<uint2 *>(slot + 16 + gi * kMB)[lane] = make_uint2(m.w[0], m.w[1]);
+        else
+            reinterpret_cast<uint32_t *>(slot + 16 + gi * kMB)[lane] = m.w[0];
         if (DEC)
             BfpGroup<BITS>::decode(m.w, m.e, v);
     }
@@ -326,7 +330,8 @@ template <int BITS> struct CodecBfp {
     {
         BfpGroup<BITS>::decode(m.w, m.e, v);
     }
-    __device__ __forceinline__ static uint32_t bytes(int V, const unsigned char *)
+    __device__ __forceinline__ static uint32_t bytes(int V, const unsigned char *,
+                                                     const RingArgs &)
     {
         return bfp_msg_bytes(V, BITS);
     }
@@ -334,47 +339,65 @@ template <int BITS> struct CodecBfp {
 template <> struct WireCodec<kCodecBfp8> : CodecBfp<8> {};
 template <> struct WireCodec<kCodecBfp4> : CodecBfp<4> {};
 
-// Sparse values + indices: one 256-element slice per message (G = 1).
-// Slot: {uint32 fmt, uint32 nnz} padded to 16 bytes, fp32 values[256],
-// int32 indices[256] (slice-relative, ascending).  Dense fallback: fmt 0,
+// Sparse values + indices.  Every 256-element group of a slice is its own
+// sub-message (reading: one sparse/dense decision per 256 elements), so a
+// slice of G groups carries G sub-messages of a.sp_sub bytes each:
+// {uint32 fmt, uint32 nnz} padded to 16 bytes, fp32 values, then (sparse
+// form) int32 indices, slice-relative and ascending, from byte 16 + 4*icap.
+// A group is sent sparse only with nnz < a.sp_full_lim, so icap =
+// a.sp_icap = lim - 1 pairs always fit; the dense fallback (fmt 0) holds
 // values[0..len) in place.  Compaction: per-lane presence masks and a warp
 // inclusive scan of their popcounts give every lane's first output position.
-// A received message is held in registers in its decoded form: the lane's 8
+// A received group is held in registers in its decoded form: the lane's 8
 // values (+0.0 where the message has none) and a presence mask, from which
-// the identical message can be written again when it is forwarded.
+// the identical sub-message can be written again when it is forwarded.
 template <> struct WireCodec<kCodecSparse> {
-    static constexpr bool kSliced = false; // the message is exactly one 256-element slice
-    static constexpr int slot_bytes(int) { return 16 + kTile * 8; }
     struct Reg {
         uint32_t fmt, nnz, pres;
         float f[8];
     };
+    __device__ __forceinline__ static unsigned char *sub(const unsigned char *slot, int gi,
+                                                         const RingArgs &a)
+    {
+        return const_cast<unsigned char *>(slot) + gi * a.sp_sub;
+    }
     __device__ __forceinline__ static float *vals(unsigned char *s)
     {
         return reinterpret_cast<float *>(s + 16);
     }
-    __device__ __forceinline__ static int *idxs(unsigned char *s)
+    __device__ __forceinline__ static int *idxs(unsigned char *s, const RingArgs &a)
     {
-        return reinterpret_cast<int *>(s + 16 + kTile * 4);
+        return reinterpret_cast<int *>(s + 16 + 4 * a.sp_icap);
     }
-    __device__ __forceinline__ static uint32_t bytes(int V, const unsigned char *slot)
+    // elements of group gi in a slice of V
+    __device__ __forceinline__ static int group_len(int V, int gi)
     {
-        const uint2 h = *reinterpret_cast<const uint2 *>(slot);
-        return V == 0 ? 0u : 8u + (h.x ? 8u * h.y : 4u * (uint32_t)V);
+        return min(max(V - gi * kTile, 0), kTile);
     }
-    // Write the message whose lane values are v and whose present positions
-    // are the bits of nzm: sparse (ascending indices) when fmt is set, dense
-    // otherwise.  Warp-collective.
-    __device__ __forceinline__ static void emit(unsigned char *slot, int lane, const float (&v)[8],
+    // wire bytes of the sub-messages of a slice of V elements
+    __device__ __forceinline__ static uint32_t bytes(int V, const unsigned char *slot,
+                                                     const RingArgs &a)
+    {
+        uint32_t b = 0;
+        for (int gi = 0; gi * kTile < V; ++gi) {
+            const uint2 h = *reinterpret_cast<const uint2 *>(sub(slot, gi, a));
+            b += 8u + (h.x ? 8u * h.y : 4u * (uint32_t)group_len(V, gi));
+        }
+        return b;
+    }
+    // Write the sub-message whose lane values are v and whose present
+    // positions are the bits of nzm: sparse (ascending indices) when fmt is
+    // set, dense otherwise.  Warp-collective.
+    __device__ __forceinline__ static void emit(unsigned char *s, int lane, const float (&v)[8],
                                                 uint32_t nzm, uint32_t fmt, int cnt, int incl,
-                                                int total)
+                                                int total, const RingArgs &a)
     {
         if (lane == 0)
-            *reinterpret_cast<uint2 *>(slot) = make_uint2(fmt, (uint32_t)total);
+            *reinterpret_cast<uint2 *>(s) = make_uint2(fmt, (uint32_t)total);
         if (fmt) {
             int pos = incl - cnt;
-            float *vv = vals(slot);
-            int *x = idxs(slot);
+            float *vv = vals(s);
+            int *x = idxs(s, a);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 if ((nzm >> i) & 1u) {
@@ -383,7 +406,7 @@ template <> struct WireCodec<kCodecSparse> {
                     ++pos;
                 }
         } else {
-            float4 *p = reinterpret_cast<float4 *>(vals(slot)) + 2 * lane;
+            float4 *p = reinterpret_cast<float4 *>(vals(s)) + 2 * lane;
             p[0] = make_float4(v[0], v[1], v[2], v[3]);
             p[1] = make_float4(v[4], v[5], v[6], v[7]);
         }
@@ -399,39 +422,41 @@ template <> struct WireCodec<kCodecSparse> {
         }
         return incl;
     }
-    // Read a message into its decoded register form.  Sparse messages are
-    // scattered into the warp's scratch (values + presence bytes) and read
-    // back at the lane's 8 positions.  Warp-collective.
-    __device__ __forceinline__ static void load(const unsigned char *slot, int, int lane,
-                                                unsigned char *scratch, Reg &m)
+    // Read sub-message gi into its decoded register form.  Sparse groups
+    // are scattered into the warp's scratch (values + presence bytes) and
+    // read back at the lane's 8 positions.  Warp-collective.
+    __device__ __forceinline__ static void load(const unsigned char *slot, int gi, int lane,
+                                                unsigned char *scratch, const RingArgs &a,
+                                                Reg &m)
     {
-        const uint2 h = *reinterpret_cast<const uint2 *>(slot);
+        unsigned char *s = sub(slot, gi, a);
+        const uint2 h = *reinterpret_cast<const uint2 *>(s);
         m.fmt = h.x;
         m.nnz = h.y;
-        unsigned char *s = const_cast<unsigned char *>(slot);
         if (!m.fmt) {
             const float4 *p = reinterpret_cast<const float4 *>(vals(s)) + 2 * lane;
-            const float4 a = p[0], b = p[1];
-            m.f[0] = a.x; m.f[1] = a.y; m.f[2] = a.z; m.f[3] = a.w;
-            m.f[4] = b.x; m.f[5] = b.y; m.f[6] = b.z; m.f[7] = b.w;
+            const float4 x = p[0], y = p[1];
+            m.f[0] = x.x; m.f[1] = x.y; m.f[2] = x.z; m.f[3] = x.w;
+            m.f[4] = y.x; m.f[5] = y.y; m.f[6] = y.z; m.f[7] = y.w;
             m.pres = 0xffu;
             return;
         }
-        const int nnz = min((int)h.y, kTile);
+        const int nnz = min((int)h.y, a.sp_icap);
         float *sval = reinterpret_cast<float *>(scratch);
         unsigned char *spres = scratch + kTile * 4;
         *reinterpret_cast<uint2 *>(spres + 8 * lane) = make_uint2(0u, 0u);
         __syncwarp();
+        const int *ix_in = idxs(s, a);
         for (int k = lane; k < nnz; k += 32) {
-            const int ix = idxs(s)[k];
+            const int ix = ix_in[k] & (kTile - 1); // in range for any slot contents
             sval[ix] = vals(s)[k];
             spres[ix] = 1;
         }
         __syncwarp();
         const uint2 pb = *reinterpret_cast<const uint2 *>(spres + 8 * lane);
         const float4 *sv = reinterpret_cast<const float4 *>(sval) + 2 * lane;
-        const float4 a = sv[0], b = sv[1];
-        const float t[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        const float4 x = sv[0], y = sv[1];
+        const float t[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
         uint32_t pres = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -442,40 +467,43 @@ template <> struct WireCodec<kCodecSparse> {
         m.pres = pres;
         __syncwarp();
     }
-    // Forward a received message unchanged: the same format, count, values
+    // Forward a received group unchanged: the same format, count, values
     // and ascending indices.  Warp-collective.
-    __device__ __forceinline__ static void store(unsigned char *slot, int, int lane, const Reg &m)
+    __device__ __forceinline__ static void store(unsigned char *slot, int gi, int lane,
+                                                 const Reg &m, const RingArgs &a)
     {
+        unsigned char *s = sub(slot, gi, a);
         if (!m.fmt) {
-            emit(slot, lane, m.f, 0xffu, 0u, 0, 0, (int)m.nnz);
+            emit(s, lane, m.f, 0xffu, 0u, 0, 0, (int)m.nnz, a);
             return;
         }
         const int cnt = __popc(m.pres);
         const int incl = warp_incl_scan(lane, cnt);
         const int total = __shfl_sync(kFull, incl, 31);
-        emit(slot, lane, m.f, m.pres, 1u, cnt, incl, total);
+        emit(s, lane, m.f, m.pres, 1u, cnt, incl, total, a);
     }
-    // The header of a dense message also carries its nonzero count.  The
-    // receiver restores every value exactly (absent ones are +0.0), so
-    // the decoded values are v itself: DEC changes nothing.
+    // The header of a dense group also carries its nonzero count.  The
+    // receiver restores every value exactly (absent ones are +0.0), so the
+    // decoded values are v itself: DEC changes nothing.
     template <bool DEC>
-    __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int,
+    __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int gi,
                                                   int lane, int V, const RingArgs &a,
                                                   unsigned char *)
     {
+        const int Vg = group_len(V, gi);
         uint32_t nzm = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            if (8 * lane + i < V && __float_as_uint(v[i]) != 0u)
+            if (8 * lane + i < Vg && __float_as_uint(v[i]) != 0u)
                 nzm |= 1u << i;
         const int cnt = __popc(nzm);
         const int incl = warp_incl_scan(lane, cnt);
         const int total = __shfl_sync(kFull, incl, 31);
-        // full slices compare with the precomputed integer limit; a ragged
-        // slice evaluates nnz < (1 - threshold) * len in double
-        const uint32_t fmt = V == kTile ? (total < a.sp_full_lim ? 1u : 0u)
-                                        : ((double)total < a.one_minus_thr * (double)V ? 1u : 0u);
-        emit(slot, lane, v, nzm, fmt, cnt, incl, total);
+        // full groups compare with the precomputed integer limit; a ragged
+        // group evaluates nnz < (1 - threshold) * len in double
+        const uint32_t fmt = Vg == kTile ? (total < a.sp_full_lim ? 1u : 0u)
+                                         : ((double)total < a.one_minus_thr * (double)Vg ? 1u : 0u);
+        emit(sub(slot, gi, a), lane, v, nzm, fmt, cnt, incl, total, a);
     }
     __device__ __forceinline__ static void decode_add(const Reg &m, float (&v)[8], int,
                                                       unsigned char *)
@@ -691,7 +719,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     // and their slot is freed at the end of the step (two slots per edge).
     constexpr bool kEarly = G == 1;
     auto release_early = [&](int r, const unsigned char *rslot, uint32_t rb, Reg &m) {
-        C::load(rslot, 0, lane, scratch, m);
+        C::load(rslot, 0, lane, scratch, a, m);
         if (ONE)
             my_recv += rb;
         __syncwarp();
@@ -762,7 +790,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                 uint32_t rb = 0;
                 Reg m0;
                 if (g >= 2) {
-                    rb = C::bytes(V, rslot);
+                    rb = C::bytes(V, rslot, a);
                     if (kEarly)
                         release_early(r, rslot, rb, m0);
                 }
@@ -779,13 +807,13 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                         if (kEarly)
                             m = m0;
                         else
-                            C::load(rslot, gi, lane, scratch, m);
+                            C::load(rslot, gi, lane, scratch, a, m);
                         C::decode_add(m, v, lane, scratch);
                     }
                     C::template encode<false>(v, dslot, gi, lane, V, a, scratch);
                 }
                 __syncwarp();
-                finish_step(r, g, g >= 2 && !kEarly, true, rb, C::bytes(V, dslot));
+                finish_step(r, g, g >= 2 && !kEarly, true, rb, C::bytes(V, dslot, a));
             }
             if (!ok)
                 break;
@@ -810,7 +838,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                 break;
             const unsigned char *sp = stages + (size_t)(r * D + stg.slot) * a.stage_bytes;
             const unsigned char *rslot = slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
-            const uint32_t rb = recv ? C::bytes(V, rslot) : 0u;
+            const uint32_t rb = recv ? C::bytes(V, rslot, a) : 0u;
             Reg m0;
             if (kEarly && recv)
                 release_early(r, rslot, rb, m0);
@@ -829,7 +857,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     if (kEarly)
                         m = m0;
                     else
-                        C::load(rslot, gi, lane, scratch, m);
+                        C::load(rslot, gi, lane, scratch, a, m);
                     C::decode_add(m, v, lane, scratch);
                 }
                 if (allred)
@@ -837,7 +865,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                 output_group(r, r, V, gi, v);
             }
             __syncwarp();
-            finish_step(r, N, recv && !kEarly, send, rb, send ? C::bytes(V, dslot) : 0u);
+            finish_step(r, N, recv && !kEarly, send, rb, send ? C::bytes(V, dslot, a) : 0u);
         }
         if (!ok)
             break;
@@ -862,7 +890,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                         break;
                     const unsigned char *rslot =
                         slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
-                    const uint32_t rb = C::bytes(V, rslot);
+                    const uint32_t rb = C::bytes(V, rslot, a);
                     Reg m0;
                     if (kEarly)
                         release_early(r, rslot, rb, m0);
@@ -877,9 +905,9 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                         if (kEarly)
                             m = m0;
                         else
-                            C::load(rslot, gi, lane, scratch, m);
+                            C::load(rslot, gi, lane, scratch, a, m);
                         if (fwd)
-                            C::store(dslot, gi, lane, m);
+                            C::store(dslot, gi, lane, m, a);
                         float v[8];
                         C::values(m, v, lane, scratch);
                         output_group(r, c, V, gi, v);

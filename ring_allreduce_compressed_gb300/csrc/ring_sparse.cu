@@ -10,6 +10,8 @@ const void *ring_fn_sparse(int in_t, bool fast, int groups, int mode)
 {
     switch (groups) {
     case 1: return ring_variant<kCodecSparse, 1>(in_t, fast, mode);
+    case 2: return ring_variant<kCodecSparse, 2>(in_t, fast, mode);
+    case 4: return ring_variant<kCodecSparse, 4>(in_t, fast, mode);
     default: return nullptr;
     }
 }

@@ -154,59 +154,68 @@ const void *ring_fn(int codec, int in_t, bool fast, int groups, int rmap)
     return ring_fn_bfp4(in_t, fast, groups, rmap);
 }
 
+// Sparse group sub-message: a 16-byte header, fp32 values, then the indices
+// of a sparse group.  A group goes sparse only with nnz < lim, so at most
+// lim - 1 pairs; the dense form holds 256 values.
+int sparse_icap(int lim) { return std::max(lim - 1, 0); }
+int sparse_sub_bytes(int lim) { return align_up(16 + std::max(kTile * 4, 8 * sparse_icap(lim)), 16); }
+
 // Bytes of one mailbox slot for a slice of 256 * groups elements.
-int slot_bytes_for(int codec, int groups)
+int slot_bytes_for(int codec, int groups, int sparse_lim)
 {
     switch (codec) {
     case kCodecNone: return kTile * 4 * groups;
     case kCodecBfp8: return 16 + kTile * groups;
     case kCodecBfp4: return 16 + kTile / 2 * groups;
-    default: return 16 + kTile * 8;
+    default: return sparse_sub_bytes(sparse_lim) * groups;
     }
 }
 
 // Slice width (groups of 8 elements per lane) and staging depth: wider
 // slices amortise each step's handshakes over more elements; the first
-// candidate that leaves room for three resident blocks per SM wins, else
-// the first that fits at all.
+// candidate that leaves room for about 24 resident warps per SM wins (three
+// blocks of up to 8 warps, two wider ones), else the first that fits at all.
 struct LaunchShape {
     int groups, K, D, smem;
     bool fast;
 };
 
 bool pick_shape(rra_comm *c, const Tune &t, int N, long long n, int kc, int ies, bool diff,
-                bool fast, int warps, LaunchShape *out)
+                bool fast, int warps, int sparse_lim, LaunchShape *out)
 {
     const int sms = num_sms();
     static const int kGD[][2] = {{8, 2}, {8, 1}, {4, 2}, {4, 1}, {2, 4},
-                                 {2, 2}, {1, 4}, {1, 2}, {1, 1}};
+                                 {2, 2}, {2, 1}, {1, 4}, {1, 2}, {1, 1}};
+    // resident blocks to leave room for: about 24 warps per SM (three blocks
+    // of up to 8 warps, two of 12 to 16)
+    const int want = warps >= 12 ? 2 : 3;
     const bool sparse = kc == kCodecSparse;
     // a requested slice width is tried first on its own; passes 2 and 3 are
     // the automatic choice
-    for (int pass = t.G && !sparse ? 0 : 2; pass < 4; ++pass) {
+    for (int pass = t.G ? 0 : 2; pass < 4; ++pass) {
         for (const auto &gd : kGD) {
             const int G = gd[0];
             if (pass < 2 && G != t.G)
                 continue;
-            int D = t.D ? t.D : gd[1];
-            if (sparse && G != 1)
+            if (sparse && G > 4) // sparse slices of 1, 2 or 4 groups are instantiated
                 continue;
+            int D = t.D ? t.D : gd[1];
             // a short chunk is cut into narrower slices while a wider one
             // would leave SMs without a slice position to work on
             if (pass >= 2 && G > 1 && (n + (long long)kTile * G - 1) / ((long long)kTile * G) < sms)
                 continue;
             if (!fast)
                 D = 1;
-            const int slot = slot_bytes_for(kc, G);
+            const int slot = slot_bytes_for(kc, G, sparse_lim);
             const int stage = kTile * G * (diff ? 8 : ies);
             // wider messages need two slots per ring edge: a rank frees the
             // slot it streams from only after its own send of the same step,
             // so with one slot every rank would wait for its successor
             for (int K = t.K ? t.K : 2; K >= (G == 1 ? 1 : 2); --K) {
                 const Layout L = make_layout(N, K, D, slot, stage, warps, fast, sparse);
-                const bool three = pass % 2 == 0; // leave room for three blocks per SM
-                const int need = three ? 3 * (L.total + 1024) : L.total;
-                const int have = three ? c->smem_per_sm : c->smem_optin;
+                const bool several = pass % 2 == 0; // leave room for `want` blocks per SM
+                const int need = several ? want * (L.total + 1024) : L.total;
+                const int have = several ? c->smem_per_sm : c->smem_optin;
                 if (need <= have && L.total <= c->smem_optin) {
                     *out = LaunchShape{G, K, D, L.total, fast};
                     return true;
@@ -303,6 +312,8 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     a.sp_full_lim = 0;
     while (a.sp_full_lim <= kTile && (double)a.sp_full_lim < a.one_minus_thr * (double)kTile)
         ++a.sp_full_lim;
+    a.sp_icap = sparse_icap(a.sp_full_lim);
+    a.sp_sub = sparse_sub_bytes(a.sp_full_lim);
     a.timeout_ns = comm->timeout_ns;
     a.status = comm->status;
     a.withhold_rank = comm->withhold_rank;
@@ -336,15 +347,17 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
             t = it->second;
     }
     LaunchShape sh;
-    if (!pick_shape(comm, t, N, a.n, kc, (int)ies, cd.diff_prev != nullptr, fast, warps, &sh)) {
+    if (!pick_shape(comm, t, N, a.n, kc, (int)ies, cd.diff_prev != nullptr, fast, warps,
+                    a.sp_full_lim, &sh)) {
         fast = false;
-        if (!pick_shape(comm, t, N, a.n, kc, (int)ies, cd.diff_prev != nullptr, false, warps, &sh))
+        if (!pick_shape(comm, t, N, a.n, kc, (int)ies, cd.diff_prev != nullptr, false, warps,
+                        a.sp_full_lim, &sh))
             return RRA_ERR_UNSUPPORTED;
     }
     const int groups = sh.groups, smem = sh.smem;
     a.K = sh.K;
     a.D = sh.D;
-    a.slot_bytes = slot_bytes_for(kc, groups);
+    a.slot_bytes = slot_bytes_for(kc, groups, a.sp_full_lim);
     a.stage_bytes = kTile * groups * (cd.diff_prev ? 8 : (int)ies);
     a.tiles = (a.n + kTile * groups - 1) / (kTile * groups);
     // every warp plays exactly one rank when N fits the block

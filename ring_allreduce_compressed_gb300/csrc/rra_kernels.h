@@ -45,6 +45,8 @@ struct RingArgs {
     long long tiles;   // slices per chunk ceil(n / 256)
     double one_minus_thr; // sparse: a slice is sparse iff nnz < one_minus_thr * len
     int sp_full_lim;      // sparse: a full 256-element slice is sparse iff nnz < sp_full_lim
+    int sp_icap;          // sparse: most (value, index) pairs of a sparse group = lim - 1
+    int sp_sub;           // sparse: bytes of one group's sub-message in a slot
     unsigned long long timeout_ns;
     unsigned long long *sent; // [N] device counters of this call
     unsigned long long *recv; // [N]

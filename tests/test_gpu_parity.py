@@ -444,3 +444,38 @@ def test_argument_errors_are_reported_on_the_host():
     with pytest.raises(rra.RRAError):
         comm.tree_allreduce(cast(xs, "f16"))
     comm.close()
+
+
+# ------------------------------------------------------------------ forced launch shapes
+
+@pytest.mark.parametrize("codec_kind,bits,in_dt", [("none", 8, "f32"), ("bfp", 8, "f16"),
+                                                   ("bfp", 4, "bf16"), ("sparse", 8, "bf16")])
+@pytest.mark.parametrize("N,T", [(8, 8 * 2048 * 3 + 8 * 700 + 3), (5, 5 * 1300 + 2),
+                                 (20, 20 * 1024 + 7)])
+def test_forced_launch_shapes(codec_kind, bits, in_dt, N, T):
+    """Every slice width (1, 2, 4, 8 groups of 256), staging depth and block
+    count gives the oracle's bits and byte counts: the shape changes only how
+    the work is cut, never what is computed.  Covers multi-group sparse
+    slices (one sub-message per group) and ranks shared by a warp (N=20)."""
+    if codec_kind == "sparse":
+        xs = W.sparse(N, T, seed=N + T, dtype=TORCH_DT[in_dt])
+    else:
+        xs = cast(rand_f32(N, T, seed=N + T, scale=1e-3), in_dt)
+    codec = rra.Codec(codec_kind, bits=bits)
+    ref = oracle_ring(xs, in_dt, "f32", codec=codec_kind, bits=bits)
+    comm = rra.Comm(N, T, xs[0].dtype)
+    for G in (1, 2, 4, 8):
+        for D, blocks in ((1, 0), (3, 1)):
+            comm.set_tuning(blocks, 0, D, G)
+            outs = [torch.zeros(T, device="cuda") for _ in range(N)]
+            comm.ring_allreduce(xs, outs, codec)
+            sent, recv = comm.get_bytes()
+            assert comm.status() == rra.RRA_OK
+            got_G = comm.last_shape()[3]
+            # a width that does not fit the shared memory falls back to a narrower one;
+            # with one stage and at most 8 ranks every instantiated width fits
+            if N <= 8 and D == 1 and not (codec_kind == "sparse" and G == 8):
+                assert got_G == G, (G, got_G)
+            compare((outs, np.array(sent, np.uint64), np.array(recv, np.uint64)), ref,
+                    f"{codec_kind}{bits} G={G} D={D} blocks={blocks}")
+    comm.close()
