@@ -191,7 +191,7 @@ class Workload:
     """One of the configurations, resident in HBM.  With use_lib=False (the
     reference arm) only the inputs are drawn; the CUDA library is not used."""
 
-    def __init__(self, name: str, device="cuda", use_lib: bool = True):
+    def __init__(self, name: str, device="cuda", use_lib: bool = True, scale: int = 1):
         rra = None
         if use_lib:
             import ring_allreduce_compressed_gb300 as rra
@@ -200,7 +200,9 @@ class Workload:
         self.prev = None
         self.codec = None
         c = W.CONFIGS[name]
-        self.N, self.T = c["N"], c["T"]
+        # scale > 1: the same workload with T / scale elements per rank (a
+        # small case for profiler captures; never a bench line of the metric)
+        self.N, self.T = c["N"], c["T"] // scale
         if name == "bfp8_bucket":
             self.inputs = W.bfp_bucket(self.N, self.T, seed=c["seed"], device=device)
             self.out_dtype = torch.float16
@@ -327,7 +329,7 @@ def cpu_baseline(wl: Workload, budget_s: float = 20.0):
 def run_rra(args, world, rank, local):
     import ring_allreduce_compressed_gb300 as rra
     rra.build()
-    wl = Workload(args.config)
+    wl = Workload(args.config, scale=args.scale)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         wl.step()
@@ -409,7 +411,7 @@ def run_rra(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{args.config}: {wl.desc}", "N": wl.N, "T": wl.T,
+        "config": {"workload": f"{args.config}: {wl.desc}" + (f" [T / {args.scale}]" if getattr(args, "scale", 1) > 1 else ""), "N": wl.N, "T": wl.T,
                    "in_dtype": DT_NAME[wl.in_dtype], "out_dtype": DT_NAME[wl.out_dtype],
                    "codec": wl.codec_name, "parallelism": f"replicas x{world}",
                    "l2": wl.l2_note()},
@@ -601,6 +603,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["rra", "reference"], default="rra")
     ap.add_argument("--config", choices=CONFIG_NAMES, default="bfp8_bucket")
+    ap.add_argument("--scale", type=int, default=1,
+                    help="run the workload with T / scale elements per rank: a small case for "
+                         "ncu captures, reported with its own T (not the metric's workload)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
