@@ -67,6 +67,9 @@ def lib():
             L.oracle_ring.argtypes = [i32, i32, sz, vp, i32, vp, i32, i32, i32, C.c_double, sz,
                                       vp, vp, i32, u64p, u64p]
             L.oracle_ring.restype = i32
+            L.oracle_ring_ef.argtypes = [i32, i32, sz, vp, i32, vp, i32, i32, i32, C.c_double,
+                                         sz, vp, vp, i32, vp, u64p, u64p]
+            L.oracle_ring_ef.restype = i32
             L.oracle_allgather.argtypes = [i32, sz, vp, i32, u64p, u64p]
             L.oracle_broadcast.argtypes = [i32, sz, vp, i32, i32, u64p, u64p]
             L.oracle_tree_allreduce.argtypes = [i32, sz, vp, u64p, u64p]
@@ -126,12 +129,14 @@ def _counters(N):
 
 def ring(inputs, in_dtype="f32", out_dtype="f32", codec="none", bits=8, threshold=0.5,
          slice=RING_SLICE, diff_prev=None, diff_base=None, average=False,
-         mode="allreduce", outputs=None):
+         mode="allreduce", outputs=None, residual=None):
     """Two-pass ring allreduce (mode="allreduce") or its first pass alone
     (mode="reduce_scatter") over N host arrays.  Returns (outputs, sent, recv).
 
     For reduce_scatter only chunk r of outputs[r] is written; pass ``outputs``
-    to control what the other chunks hold (default: zeros)."""
+    to control what the other chunks hold (default: zeros).  ``residual``:
+    N float32 arrays of T error-feedback residuals (BFP only), updated in
+    place."""
     N = len(inputs)
     T = inputs[0].size
     _check(inputs, T, in_dtype)
@@ -146,12 +151,17 @@ def ring(inputs, in_dtype="f32", out_dtype="f32", codec="none", bits=8, threshol
     if diff_base is not None:
         _check([diff_base], T, "f32")
         db = _ptr(diff_base)
+    rp = None
+    if residual is not None:
+        _check(residual, T, "f32")
+        rp = _ptrs(residual)
     sent, recv = _counters(N)
-    rc = lib().oracle_ring({"allreduce": 0, "reduce_scatter": 1}[mode], N, T, _ptrs(inputs),
-                           DTYPES[in_dtype], _ptrs(outputs), DTYPES[out_dtype], CODECS[codec],
-                           bits, float(threshold), slice,
-                           C.cast(dp, C.c_void_p) if dp is not None else None, db,
-                           int(bool(average)), sent, recv)
+    rc = lib().oracle_ring_ef({"allreduce": 0, "reduce_scatter": 1}[mode], N, T, _ptrs(inputs),
+                              DTYPES[in_dtype], _ptrs(outputs), DTYPES[out_dtype], CODECS[codec],
+                              bits, float(threshold), slice,
+                              C.cast(dp, C.c_void_p) if dp is not None else None, db,
+                              int(bool(average)), C.cast(rp, C.c_void_p) if rp is not None else None,
+                              sent, recv)
     if rc != 0:
         raise ValueError("oracle_ring: bad arguments")
     return outputs, np.array(sent[:], np.uint64), np.array(recv[:], np.uint64)

@@ -52,6 +52,11 @@
  *  D2  epilogue: out = base + (v / N) when a base (previous result) is given
  *      and averaging is on; v / N with averaging only; v otherwise.
  *  RS  reduce-scatter: the owner's output is its fp32 sum (not re-encoded).
+ *  EF  error feedback ([P4] §5, future directions), BFP only: each rank
+ *      keeps an fp32 residual e_r[T]; whatever value v it encodes (its
+ *      reduce-scatter messages, and as owner its chunk's full sum) is encoded
+ *      as u = v + e, after which e = u - decode(Q(u)).  Every element of
+ *      e_r is updated exactly once per allreduce.
  */
 #include <math.h>
 #include <stdint.h>
@@ -483,12 +488,32 @@ enum { OR_MODE_ALLREDUCE = 0, OR_MODE_REDUCE_SCATTER = 1 };
  *
  * Returns 0 on success, -1 on a bad argument.
  */
-int oracle_ring(int mode, int N, size_t T, const void *const *in, int in_t, void *const *out,
-                int out_t, int codec, int bits, double threshold, size_t slice,
-                const float *const *diff_prev, const float *diff_base, int average,
-                uint64_t *sent, uint64_t *recv)
+/* Encode n fp32 values v into m with error feedback ("CCCL通信压缩库" §5,
+ * future directions: the precision a compression loses in one round is
+ * carried into the next round).  The value encoded is u = v + e (fp32); the
+ * residual becomes e = u - decode(Q(u)).  e is updated in place. */
+static void msg_encode_ef(message *m, const codec_t *cd, const float *v, float *e, size_t n)
+{
+    float *u = malloc((n ? n : 1) * sizeof(float));
+    for (size_t i = 0; i < n; i++)
+        u[i] = v[i] + e[i];
+    msg_encode(m, cd, u, n);
+    for (size_t i = 0; i < n; i++) {
+        int there;
+        const float d = msg_value(m, cd, i, &there);
+        e[i] = u[i] - (there ? d : 0.0f);
+    }
+    free(u);
+}
+
+int oracle_ring_ef(int mode, int N, size_t T, const void *const *in, int in_t, void *const *out,
+                   int out_t, int codec, int bits, double threshold, size_t slice,
+                   const float *const *diff_prev, const float *diff_base, int average,
+                   float *const *resid, uint64_t *sent, uint64_t *recv)
 {
     if (N < 1 || (codec == OR_CODEC_BFP && bits != 8 && bits != 4) || (diff_prev && in_t != OR_F32))
+        return -1;
+    if (resid && codec != OR_CODEC_BFP) /* only a lossy codec has an error to feed back */
         return -1;
     if (codec == OR_CODEC_SPARSE && slice == 0)
         return -1;
@@ -513,7 +538,10 @@ int oracle_ring(int mode, int N, size_t T, const void *const *in, int in_t, void
             size_t lo, len;
             chunk_range(T, N, c, &lo, &len);
             int dst = mod((long)r + 1, N);
-            msg_encode(&outbox[dst], &cd, local[r] + lo, len);
+            if (resid) /* every message a rank encodes takes its residual */
+                msg_encode_ef(&outbox[dst], &cd, local[r] + lo, resid[r] + lo, len);
+            else
+                msg_encode(&outbox[dst], &cd, local[r] + lo, len);
             sent[r] += outbox[dst].bytes;
             recv[dst] += outbox[dst].bytes;
         }
@@ -548,7 +576,10 @@ int oracle_ring(int mode, int N, size_t T, const void *const *in, int in_t, void
         }
         if (mode == OR_MODE_ALLREDUCE) {
             /* B6: the owner encodes its full sum once */
-            msg_encode(&held[r], &cd, local[r] + lo, len);
+            if (resid)
+                msg_encode_ef(&held[r], &cd, local[r] + lo, resid[r] + lo, len);
+            else
+                msg_encode(&held[r], &cd, local[r] + lo, len);
             if (codec != OR_CODEC_NONE)
                 for (size_t i = 0; i < len; i++) {
                     int there;
@@ -613,6 +644,15 @@ int oracle_ring(int mode, int N, size_t T, const void *const *in, int in_t, void
     free(local);
     free(res);
     return 0;
+}
+
+int oracle_ring(int mode, int N, size_t T, const void *const *in, int in_t, void *const *out,
+                int out_t, int codec, int bits, double threshold, size_t slice,
+                const float *const *diff_prev, const float *diff_base, int average,
+                uint64_t *sent, uint64_t *recv)
+{
+    return oracle_ring_ef(mode, N, T, in, in_t, out, out_t, codec, bits, threshold, slice,
+                          diff_prev, diff_base, average, NULL, sent, recv);
 }
 
 /* ------------------------------------------------------------------ */

@@ -82,9 +82,11 @@ def sparse_roundtrip(vals, threshold, slice_len):
 # ---------------------------------------------------------------- ring
 
 def ring(xs, codec="none", bits=8, threshold=0.5, slice_len=256, mode="allreduce",
-         diff_prev=None, diff_base=None, average=False):
+         diff_prev=None, diff_base=None, average=False, residual=None):
     """xs: list of N lists of float32 scalars.  Returns (results, sent, recv)
-    where results[r] is a list with None at chunks rank r does not produce."""
+    where results[r] is a list with None at chunks rank r does not produce.
+    residual: N lists of float32 error-feedback residuals, updated in place
+    (a rank encodes u = v + e and keeps e = u - decoded)."""
     N, T = len(xs), len(xs[0])
     ch = chunks(T, N)
     if diff_prev is not None:
@@ -101,11 +103,20 @@ def ring(xs, codec="none", bits=8, threshold=0.5, slice_len=256, mode="allreduce
             return out, [True] * len(vals), nb
         return sparse_roundtrip(vals, threshold, slice_len)
 
+    def encode_at(r, lo, hi, vals):
+        if residual is None:
+            return encode(vals)
+        u = [F(v + residual[r][lo + k]) for k, v in enumerate(vals)]
+        msg = encode(u)
+        for k in range(hi - lo):
+            residual[r][lo + k] = F(u[k] - (msg[0][k] if msg[1][k] else F(0.0)))
+        return msg
+
     for s in range(1, N):
         inbox = [None] * N
         for r in range(N):
             lo, hi = ch[(r - s) % N]
-            inbox[(r + 1) % N] = encode(local[r][lo:hi])
+            inbox[(r + 1) % N] = encode_at(r, lo, hi, local[r][lo:hi])
             sent[r] += inbox[(r + 1) % N][2]
             recv[(r + 1) % N] += inbox[(r + 1) % N][2]
         for r in range(N):
@@ -123,7 +134,7 @@ def ring(xs, codec="none", bits=8, threshold=0.5, slice_len=256, mode="allreduce
             for i in range(lo, hi):
                 res[r][i] = local[r][i]
         if mode == "allreduce":
-            held[r] = encode(local[r][lo:hi])
+            held[r] = encode_at(r, lo, hi, local[r][lo:hi])
             if codec != "none":
                 for i in range(lo, hi):
                     res[r][i] = held[r][0][i - lo] if held[r][1][i - lo] else F(0.0)

@@ -491,3 +491,77 @@ def test_sparse_ring_keeps_minus_zero_of_own_input():
     assert struct.pack("<f", float(ls[1][2])) == struct.pack("<f", 0.0)
     ref, _, _ = brute.ring([list(x) for x in xs], codec="sparse", slice_len=4, mode="reduce_scatter")
     assert struct.pack("<f", float(ref[1][2])) == struct.pack("<f", -0.0)
+
+
+# --------------------------------------------------------------- error feedback
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("mode", ["allreduce", "reduce_scatter"])
+@pytest.mark.parametrize("N,T", [(1, 10), (2, 64), (3, 50), (4, 17)])
+def test_error_feedback_brute_force(bits, mode, N, T):
+    """Two rounds with carried residuals against the independent brute force:
+    outputs, byte counts and every residual bit for bit."""
+    rng = np.random.default_rng(N * 100 + T + bits)
+    res_o = [(rng.standard_normal(T) * 1e-5).astype(np.float32) for _ in range(N)]
+    res_b = [list(r.copy()) for r in res_o]
+    for rnd in range(2):
+        xs = [(rng.standard_normal(T) * 1e-3).astype(np.float32) for _ in range(N)]
+        outs = [np.zeros(T, np.float32) for _ in range(N)]
+        outs, sent, recv = O.ring(xs, codec="bfp", bits=bits, mode=mode, outputs=outs,
+                                  residual=res_o)
+        ref, bs, br = brute.ring([list(x) for x in xs], codec="bfp", bits=bits, mode=mode,
+                                 residual=res_b)
+        for r in range(N):
+            want = np.array([0.0 if v is None else v for v in ref[r]], np.float32)
+            assert np.array_equal(bits32(outs[r]), bits32(want)), (rnd, r)
+            assert np.array_equal(bits32(res_o[r]), bits32(np.array(res_b[r], np.float32))), (rnd, r)
+        assert list(sent) == bs and list(recv) == br
+
+
+def test_error_feedback_zero_residual_first_round_is_the_plain_ring():
+    rng = np.random.default_rng(4)
+    N, T = 4, 700
+    xs = [(rng.standard_normal(T) * 1e-3).astype(np.float32) for _ in range(N)]
+    res = [np.zeros(T, np.float32) for _ in range(N)]
+    with_ef = O.ring(xs, codec="bfp", bits=4, residual=res)
+    plain = O.ring(xs, codec="bfp", bits=4)
+    for r in range(N):
+        assert np.array_equal(bits32(with_ef[0][r]), bits32(plain[0][r]))
+    assert any(np.any(e != 0) for e in res)  # BFP4 loses something, so residuals are set
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_error_feedback_conserves_the_total(bits):
+    """Over K rounds, everything sent and not yet delivered sits in the
+    residuals.  Each chunk's result D = sum_r x_r + sum_r (e_old - e_new), up
+    to fp32 rounding of the sums.  So sum_k D_k + sum_r e_r(K) equals
+    sum_k sum_r x_{r,k}, and the error of sum_k D_k stays bounded instead of
+    growing with K as it does without feedback."""
+    rng = np.random.default_rng(11 + bits)
+    N, T, K = 4, 1024, 24
+    res = [np.zeros(T, np.float32) for _ in range(N)]
+    tot_in = np.zeros(T)
+    tot_ef = np.zeros(T)
+    tot_plain = np.zeros(T)
+    mag = 0.0
+    for _ in range(K):
+        xs = [(rng.standard_normal(T) * 1e-3).astype(np.float32) for _ in range(N)]
+        tot_in += np.sum([x.astype(np.float64) for x in xs], axis=0)
+        mag += np.sum([np.abs(x.astype(np.float64)) for x in xs], axis=0)
+        tot_ef += O.ring(xs, codec="bfp", bits=bits, residual=res)[0][0]
+        tot_plain += O.ring(xs, codec="bfp", bits=bits)[0][0]
+    left = np.sum([e.astype(np.float64) for e in res], axis=0)
+    # fp32 rounding of the adds along the chain: a few ulps of the magnitudes involved
+    bound = 4 * N * 2.0 ** -24 * (mag + K * np.max([np.abs(e) for e in res]))
+    assert np.all(np.abs(tot_ef + left - tot_in) <= bound + 1e-12)
+    drift_ef = np.abs(tot_ef - tot_in).mean()
+    drift_plain = np.abs(tot_plain - tot_in).mean()
+    assert drift_ef < drift_plain / 2, (drift_ef, drift_plain)
+
+
+def test_error_feedback_needs_a_lossy_codec():
+    xs = [np.ones(16, np.float32)] * 2
+    res = [np.zeros(16, np.float32)] * 2
+    for codec in ("none", "sparse"):
+        with pytest.raises(ValueError):
+            O.ring(xs, codec=codec, residual=res)
