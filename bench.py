@@ -154,7 +154,8 @@ def hbm_peak():
 
 # the files the ring kernels are compiled from (host-side launch code excluded)
 RING_KERNEL_SOURCES = ("ring_kernel.cuh", "rra_device.cuh", "rra_kernels.h", "ring_none.cu",
-                       "ring_bfp8.cu", "ring_bfp4.cu", "ring_sparse.cu")
+                       "ring_bfp8.cu", "ring_bfp4.cu", "ring_bfp8_ef.cu", "ring_bfp4_ef.cu",
+                       "ring_sparse.cu")
 
 
 def kernel_sources_sha() -> str:

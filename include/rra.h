@@ -101,7 +101,19 @@ typedef enum {
  *  average             nonzero: the reduced value is divided by N (IEEE
  *                      division, round to nearest even) before diff_base is
  *                      added: out = diff_base + v / N.
- * A NULL rra_codec* means {RRA_CODEC_NONE, 0, 0, NULL, NULL, 0}.
+ *  residual            NULL, or a host array of N device pointers to fp32
+ *                      buffers of T elements: per-rank error-feedback
+ *                      residuals, read and updated in place ([cccl] §5,
+ *                      future directions: the precision a compression loses
+ *                      is carried into the next round).  Every value rank r
+ *                      encodes -- its reduce-scatter messages and, as owner,
+ *                      its chunk's sum -- is encoded as u = v + e_r, and
+ *                      e_r = u - decode(codes) is stored back; each element
+ *                      is updated once per call.  RRA_CODEC_BFP only (the
+ *                      other codecs lose nothing); start from zeros.  The
+ *                      buffers must not overlap each other or any input,
+ *                      output, diff_prev or diff_base buffer.
+ * A NULL rra_codec* means {RRA_CODEC_NONE, 0, 0, NULL, NULL, 0, NULL}.
  */
 typedef struct {
     rra_codec_kind kind;
@@ -110,6 +122,7 @@ typedef struct {
     const float *const *diff_prev;
     const float *diff_base;
     int average;
+    float *const *residual;
 } rra_codec;
 
 /* Opaque communicator: owns the device-side byte counters, the status word

@@ -42,7 +42,8 @@ class RRAError(RuntimeError):
 
 class _Codec(C.Structure):
     _fields_ = [("kind", C.c_int), ("bits", C.c_int), ("sparsity_threshold", C.c_float),
-                ("diff_prev", C.c_void_p), ("diff_base", C.c_void_p), ("average", C.c_int)]
+                ("diff_prev", C.c_void_p), ("diff_base", C.c_void_p), ("average", C.c_int),
+                ("residual", C.c_void_p)]
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -140,6 +141,7 @@ class Codec:
     diff_prev: Optional[Sequence] = None  # N fp32 tensors (previous round)
     diff_base: Optional[object] = None    # fp32 tensor (previous result)
     average: bool = False
+    residual: Optional[Sequence] = None   # N fp32 tensors: error-feedback residuals (BFP)
 
     def _marshal(self):
         kinds = {"none": CODEC_NONE, "bfp": CODEC_BFP, "sparse": CODEC_SPARSE}
@@ -155,6 +157,10 @@ class Codec:
         if self.diff_base is not None:
             c.diff_base = _dev(self.diff_base, "diff_base")
         c.average = 1 if self.average else 0
+        if self.residual is not None:
+            arr = _ptrs(self.residual, "residual")
+            keep.append(arr)
+            c.residual = C.cast(arr, C.c_void_p)
         return c, keep
 
 

@@ -528,7 +528,9 @@ template <> struct WireCodec<kCodecSparse> {
 // rank indices, addresses and byte counts stay in registers across the
 // loops; blocks of at most 8 warps get up to 80 registers a thread (three
 // blocks per SM), blocks of up to 16 warps 64 (two blocks per SM).
-template <int CODEC, int IN_T, bool FAST, int G, int MODE>
+// EF: error feedback -- every value a rank encodes takes its residual first,
+// and the residual keeps what the encoding lost (BFP instantiations only).
+template <int CODEC, int IN_T, bool FAST, int G, int MODE, bool EF>
 __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 32,
                                   MODE == kRankPerWarp8 ? 3 : 2)
     ring_kernel(const __grid_constant__ RingArgs a)
@@ -709,6 +711,35 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
         }
         store8(reinterpret_cast<char *>(a.out[r]) + e0 * osz, out_t, v, vl, a.vec_out != 0);
     };
+    // error feedback of group gi: encode u = v + e into the slot, store
+    // e = u - decoded and leave the decoded values in v
+    auto encode_ef = [&](int r, int c, int V, int gi, float (&v)[8], unsigned char *dslot) {
+        const long long e0 = (long long)c * n + t0 + gi * kTile + 8 * lane;
+        const int vl = min(max(V - gi * kTile - 8 * lane, 0), 8);
+        float *ep = a.resid[r] + e0;
+        float e[8];
+        if (a.vec_resid && vl == 8)
+            load8_vec<kF32>(ep, e);
+        else
+            load8_scalar<kF32>(ep, vl, e);
+        float u[8];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            const float2 s2 = __fadd2_rn(make_float2(v[i], v[i + 1]), make_float2(e[i], e[i + 1]));
+            u[i] = s2.x;
+            u[i + 1] = s2.y;
+            v[i] = s2.x;
+            v[i + 1] = s2.y;
+        }
+        C::template encode<true>(v, dslot, gi, lane, V, a, scratch);
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            const float2 d2 = __fadd2_rn(make_float2(u[i], u[i + 1]), make_float2(-v[i], -v[i + 1]));
+            e[i] = d2.x;
+            e[i + 1] = d2.y;
+        }
+        store8(ep, kF32, e, vl, a.vec_resid != 0);
+    };
     auto waits_ok = [&](bool w) -> bool {
         ok = ok && w;
         return ok;
@@ -810,7 +841,10 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                             C::load(rslot, gi, lane, scratch, a, m);
                         C::decode_add(m, v, lane, scratch);
                     }
-                    C::template encode<false>(v, dslot, gi, lane, V, a, scratch);
+                    if constexpr (EF)
+                        encode_ef(r, c, V, gi, v, dslot);
+                    else
+                        C::template encode<false>(v, dslot, gi, lane, V, a, scratch);
                 }
                 __syncwarp();
                 finish_step(r, g, g >= 2 && !kEarly, true, rb, C::bytes(V, dslot, a));
@@ -860,8 +894,12 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                         C::load(rslot, gi, lane, scratch, a, m);
                     C::decode_add(m, v, lane, scratch);
                 }
-                if (allred)
-                    C::template encode<true>(v, dslot, gi, lane, V, a, scratch);
+                if (allred) {
+                    if constexpr (EF)
+                        encode_ef(r, r, V, gi, v, dslot);
+                    else
+                        C::template encode<true>(v, dslot, gi, lane, V, a, scratch);
+                }
                 output_group(r, r, V, gi, v);
             }
             __syncwarp();
@@ -958,23 +996,23 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
 
 // Kernel for one (codec, input dtype, slice width): the generic path, or the
 // staged path in the given MODE.
-template <int CODEC, int IN_T, int G> const void *ring_variant(bool fast, int mode)
+template <int CODEC, int IN_T, int G, bool EF> const void *ring_variant(bool fast, int mode)
 {
     if (!fast)
-        return (const void *)ring_kernel<CODEC, IN_T, false, G, kRanksShared>;
+        return (const void *)ring_kernel<CODEC, IN_T, false, G, kRanksShared, EF>;
     switch (mode) {
-    case kRankPerWarp8: return (const void *)ring_kernel<CODEC, IN_T, true, G, kRankPerWarp8>;
-    case kRankPerWarp16: return (const void *)ring_kernel<CODEC, IN_T, true, G, kRankPerWarp16>;
-    default: return (const void *)ring_kernel<CODEC, IN_T, true, G, kRanksShared>;
+    case kRankPerWarp8: return (const void *)ring_kernel<CODEC, IN_T, true, G, kRankPerWarp8, EF>;
+    case kRankPerWarp16: return (const void *)ring_kernel<CODEC, IN_T, true, G, kRankPerWarp16, EF>;
+    default: return (const void *)ring_kernel<CODEC, IN_T, true, G, kRanksShared, EF>;
     }
 }
-template <int CODEC, int G> const void *ring_variant(int in_t, bool fast, int mode)
+template <int CODEC, int G, bool EF = false> const void *ring_variant(int in_t, bool fast, int mode)
 {
     switch (in_t) {
-    case kF32: return ring_variant<CODEC, kF32, G>(fast, mode);
-    case kF16: return ring_variant<CODEC, kF16, G>(fast, mode);
-    case kBF16: return ring_variant<CODEC, kBF16, G>(fast, mode);
-    case kF32Diff: return ring_variant<CODEC, kF32Diff, G>(fast, mode);
+    case kF32: return ring_variant<CODEC, kF32, G, EF>(fast, mode);
+    case kF16: return ring_variant<CODEC, kF16, G, EF>(fast, mode);
+    case kBF16: return ring_variant<CODEC, kBF16, G, EF>(fast, mode);
+    case kF32Diff: return ring_variant<CODEC, kF32Diff, G, EF>(fast, mode);
     default: return nullptr;
     }
 }

@@ -21,6 +21,8 @@ const void *ring_fn_none(int in_t, bool fast, int groups, int rmap);
 const void *ring_fn_bfp8(int in_t, bool fast, int groups, int rmap);
 const void *ring_fn_bfp4(int in_t, bool fast, int groups, int rmap);
 const void *ring_fn_sparse(int in_t, bool fast, int groups, int rmap);
+const void *ring_fn_bfp8_ef(int in_t, bool fast, int groups, int rmap);
+const void *ring_fn_bfp4_ef(int in_t, bool fast, int groups, int rmap);
 } // namespace rra
 
 using namespace rra;
@@ -143,8 +145,12 @@ int grid_for(rra_comm *c, long long key, const void *fn, int warps, int smem, lo
     return (int)std::max(1LL, g);
 }
 
-const void *ring_fn(int codec, int in_t, bool fast, int groups, int rmap)
+const void *ring_fn(int codec, int in_t, bool fast, int groups, int rmap, bool ef)
 {
+    if (ef)
+        return codec == kCodecBfp8 ? ring_fn_bfp8_ef(in_t, fast, groups, rmap)
+               : codec == kCodecBfp4 ? ring_fn_bfp4_ef(in_t, fast, groups, rmap)
+                                     : nullptr;
     if (codec == kCodecNone)
         return ring_fn_none(in_t, fast, groups, rmap);
     if (codec == kCodecSparse)
@@ -263,6 +269,10 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     }
     if (cd.diff_prev && in_t != RRA_F32)
         return RRA_ERR_INVALID;
+    // error feedback: only a lossy codec has an error to carry
+    const bool ef = cd.residual != nullptr;
+    if (ef && kc != kCodecBfp8 && kc != kCodecBfp4)
+        return RRA_ERR_UNSUPPORTED;
     // Region of out[r] the call writes: all of it for the allreduce, chunk r
     // alone for the reduce-scatter (so its outputs may share one buffer).
     const size_t oes = esize(out_t);
@@ -292,6 +302,25 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
             region(q, &pq, &bq);
             if (overlap(pr, br, pq, bq))
                 return RRA_ERR_INVALID;
+        }
+    }
+    // residuals are read and written: they may share no byte with any
+    // buffer of the call, nor with each other
+    if (ef) {
+        const size_t rb = count * 4, ib = count * esize(in_t);
+        for (int r = 0; r < N; ++r) {
+            const void *e = cd.residual[r];
+            if (!e || (cd.diff_base && overlap(e, rb, cd.diff_base, rb)))
+                return RRA_ERR_INVALID;
+            for (int q = 0; q < N; ++q) {
+                const char *pq;
+                size_t bq;
+                region(q, &pq, &bq);
+                if (overlap(e, rb, pq, bq) || overlap(e, rb, in[q], ib) ||
+                    (cd.diff_prev && overlap(e, rb, cd.diff_prev[q], rb)) ||
+                    (q < r && overlap(e, rb, cd.residual[q], rb)))
+                    return RRA_ERR_INVALID;
+            }
         }
     }
 
@@ -331,11 +360,17 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     }
     a.vec_out = vec_out ? 1 : 0;
     a.vec_base = (cd.diff_base && al16(cd.diff_base) && (a.n * 4) % 16 == 0) ? 1 : 0;
+    bool vec_resid = ef && (a.n * 4) % 16 == 0;
+    for (int r = 0; ef && r < N; ++r) {
+        a.resid[r] = cd.residual[r];
+        vec_resid = vec_resid && al16(cd.residual[r]);
+    }
+    a.vec_resid = vec_resid ? 1 : 0;
 
     const int warps = warps_for(N);
     const int kin = cd.diff_prev ? kF32Diff : (int)in_t; // kernel input kind
-    const std::array<long long, 6> tkey = {mode, kc, kin, (long long)out_t, fast ? 1 : 0,
-                                           (long long)count};
+    const std::array<long long, 6> tkey = {mode, kc + (ef ? 100 : 0), kin, (long long)out_t,
+                                           fast ? 1 : 0, (long long)count};
     if (key_out)
         *key_out = tkey;
     Tune t = comm->tune;
@@ -362,11 +397,11 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     a.tiles = (a.n + kTile * groups - 1) / (kTile * groups);
     // every warp plays exactly one rank when N fits the block
     const int rmap = warps != N ? kRanksShared : (warps <= 8 ? kRankPerWarp8 : kRankPerWarp16);
-    const void *fn = ring_fn(kc, kin, fast, groups, rmap);
+    const void *fn = ring_fn(kc, kin, fast, groups, rmap, ef);
     if (!fn)
         return RRA_ERR_UNSUPPORTED;
-    const long long key = 100000 + kc * 10000 + kin * 1000 + (fast ? 100 : 0) + rmap * 10 +
-                          groups;
+    const long long key = (ef ? 1000000 : 0) + 100000 + kc * 10000 + kin * 1000 +
+                          (fast ? 100 : 0) + rmap * 10 + groups;
     int per_sm = 0;
     const int grid = grid_for(comm, key, fn, warps, smem, a.tiles, t.blocks, &per_sm);
     comm->last = Tune{per_sm, a.K, a.D, groups};

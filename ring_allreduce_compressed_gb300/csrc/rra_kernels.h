@@ -40,6 +40,7 @@ struct RingArgs {
     int withhold_step;
     int vec_out;       // outputs allow 16-byte vector stores
     int vec_base;      // diff_base allows 16-byte vector loads
+    int vec_resid;     // error-feedback residuals allow 16-byte vector access
     long long T;       // elements per rank
     long long n;       // chunk length ceil(T/N)
     long long tiles;   // slices per chunk ceil(n / 256)
@@ -55,6 +56,7 @@ struct RingArgs {
     const float *base;        // diff_base or nullptr
     const void *in[kMaxRanks];
     const float *prev[kMaxRanks];
+    float *resid[kMaxRanks]; // error-feedback residuals (kernels instantiated with EF)
     void *out[kMaxRanks];
 };
 
