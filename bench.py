@@ -192,7 +192,8 @@ class Workload:
     """One of the configurations, resident in HBM.  With use_lib=False (the
     reference arm) only the inputs are drawn; the CUDA library is not used."""
 
-    def __init__(self, name: str, device="cuda", use_lib: bool = True, scale: int = 1):
+    def __init__(self, name: str, device="cuda", use_lib: bool = True, scale: int = 1,
+                 ef: bool = False):
         rra = None
         if use_lib:
             import ring_allreduce_compressed_gb300 as rra
@@ -232,6 +233,14 @@ class Workload:
         else:
             raise ValueError(name)
         self.in_dtype = self.inputs[0].dtype
+        # error feedback (BFP workloads): one fp32 residual per rank, from zero
+        self.ef = ef
+        if ef:
+            if self.codec_name not in ("bfp8", "diff+bfp4"):
+                raise SystemExit(f"--ef needs a BFP workload, not {name}")
+            self.residual = [torch.zeros(self.T, dtype=torch.float32, device=device)
+                             for _ in range(self.N)]
+            self.desc += "; with error feedback (an fp32 residual per rank, read and written)"
         if use_lib:
             self.comm = rra.Comm(self.N, self.T, self.in_dtype)
             if name == "bfp8_bucket":
@@ -247,6 +256,8 @@ class Workload:
                 torch.cuda.synchronize()
                 self.codec = rra.Codec("bfp", bits=4, diff_prev=self.prev, diff_base=self.base,
                                        average=True)
+            if ef:
+                self.codec.residual = self.residual
             self.outputs = [torch.empty(self.T, dtype=self.out_dtype, device=device)
                             for _ in range(self.N)]
         ies = self.inputs[0].element_size()
@@ -255,7 +266,8 @@ class Workload:
         diff = self.prev is not None
         extra_in = self.T * 4 * self.N if diff else 0  # the prev streams
         base = self.T * 4 if diff else 0
-        self.compulsory = self.N * self.T * (ies + oes) + extra_in + base
+        self.compulsory = (self.N * self.T * (ies + oes) + extra_in + base +
+                           (self.N * self.T * 8 if ef else 0))  # residual read + write
 
     def step(self, stream=None):
         self.comm.ring_allreduce(self.inputs, self.outputs, self.codec, stream=stream)
@@ -268,7 +280,8 @@ class Workload:
 
 # ---------------------------------------------------------------- CPU baseline (oracle)
 
-def oracle_sample_ring(wl_host, N, T, codec_name, slices_per_chunk, in_dt, out_dt, extra):
+def oracle_sample_ring(wl_host, N, T, codec_name, slices_per_chunk, in_dt, out_dt, extra,
+                       ef=False):
     """Run the oracle on the first `slices_per_chunk` 256-element slices of
     every chunk (an exact sub-problem: slices are independent).  Returns
     (seconds, payload bytes per rank of the sample)."""
@@ -285,6 +298,8 @@ def oracle_sample_ring(wl_host, N, T, codec_name, slices_per_chunk, in_dt, out_d
     elif codec_name == "diff+bfp4":
         kw = dict(codec="bfp", bits=4, diff_prev=[np.ascontiguousarray(p[idx]) for p in extra[0]],
                   diff_base=np.ascontiguousarray(extra[1][idx]), average=True)
+    if ef:
+        kw["residual"] = [np.zeros(xs[0].size, np.float32) for _ in range(N)]
     t0 = time.perf_counter()
     O.ring(xs, in_dt, out_dt, **kw)
     dt = time.perf_counter() - t0
@@ -312,10 +327,10 @@ def cpu_baseline(wl: Workload, budget_s: float = 20.0):
     # calibrate on a small sample, then size the measured one
     s0 = max(1, min(n // 256, 16))
     dt0, _ = oracle_sample_ring(hosts, wl.N, wl.T, wl.codec_name, s0, DT_NAME[wl.in_dtype],
-                                DT_NAME[wl.out_dtype], extra)
+                                DT_NAME[wl.out_dtype], extra, wl.ef)
     slices = max(1, min(-(-n // 256), int(s0 * budget_s / max(dt0, 1e-6))))
     dt, payload = oracle_sample_ring(hosts, wl.N, wl.T, wl.codec_name, slices,
-                                     DT_NAME[wl.in_dtype], DT_NAME[wl.out_dtype], extra)
+                                     DT_NAME[wl.in_dtype], DT_NAME[wl.out_dtype], extra, wl.ef)
     full = slices * 256 >= n
     return {"value": payload / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "seconds": dt,
@@ -330,7 +345,7 @@ def cpu_baseline(wl: Workload, budget_s: float = 20.0):
 def run_rra(args, world, rank, local):
     import ring_allreduce_compressed_gb300 as rra
     rra.build()
-    wl = Workload(args.config, scale=args.scale)
+    wl = Workload(args.config, scale=args.scale, ef=args.ef)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         wl.step()
@@ -442,7 +457,7 @@ def run_reference(args, world, rank):
     """The oracle timed on the host cores, one bounded sample per step."""
     if rank != 0:
         return
-    wl = Workload(args.config, use_lib=False)
+    wl = Workload(args.config, use_lib=False, ef=args.ef)
     n = wl.T // wl.N
     hosts = [host_copy(x) for x in wl.inputs]
     extra = None
@@ -459,16 +474,16 @@ def run_reference(args, world, rank):
         extra = (prev_h, base)
     s0 = max(1, min(n // 256, 4))
     dt0, _ = oracle_sample_ring(hosts, wl.N, wl.T, wl.codec_name, s0, DT_NAME[wl.in_dtype],
-                                DT_NAME[wl.out_dtype], extra)
+                                DT_NAME[wl.out_dtype], extra, wl.ef)
     per_step = args.ref_budget / max(1, args.steps + args.warmup)
     slices = max(1, min(-(-n // 256), int(s0 * per_step / max(dt0, 1e-6))))
     for _ in range(args.warmup):
         oracle_sample_ring(hosts, wl.N, wl.T, wl.codec_name, slices, DT_NAME[wl.in_dtype],
-                           DT_NAME[wl.out_dtype], extra)
+                           DT_NAME[wl.out_dtype], extra, wl.ef)
     tot, pay = 0.0, 0
     for _ in range(args.steps):
         dt, p = oracle_sample_ring(hosts, wl.N, wl.T, wl.codec_name, slices, DT_NAME[wl.in_dtype],
-                                   DT_NAME[wl.out_dtype], extra)
+                                   DT_NAME[wl.out_dtype], extra, wl.ef)
         tot += dt
         pay += p
     value = pay / tot / 1e9
@@ -597,6 +612,46 @@ def run_sweep(args, world, rank):
                 f.write(json.dumps(line) + "\n")
 
 
+def run_drift(args):
+    """Error-feedback drift study: K rounds of the DiLoCo composition (difference
+    against the previous round, BFP4, average, base).  Every round draws new
+    deltas.  The K compressed results, with and without error feedback, are
+    summed and compared with the sum of the lossless ring's results.  Feedback
+    keeps what compression lost in the residuals and re-sends it, so its
+    accumulated error should stay bounded, while the plain codec's error grows
+    with K."""
+    import ring_allreduce_compressed_gb300 as rra
+    c = W.CONFIGS["diloco_n8"]
+    N, T = c["N"], c["T"] // max(1, args.scale)
+    comm = rra.Comm(N, T)
+    base = torch.zeros(T, device="cuda")
+    res = [torch.zeros(T, device="cuda") for _ in range(N)]
+    out_l = [torch.empty(T, device="cuda") for _ in range(N)]
+    out_p = [torch.empty(T, device="cuda") for _ in range(N)]
+    out_e = [torch.empty(T, device="cuda") for _ in range(N)]
+    acc = {k: torch.zeros(T, dtype=torch.float64, device="cuda") for k in ("lossless", "plain", "ef")}
+    rows = []
+    for k in range(args.drift_rounds):
+        cur, prev = W.diloco(N, T, seed=1000 + k)
+        comm.ring_allreduce(cur, out_l, rra.Codec("none", diff_prev=prev, diff_base=base,
+                                                   average=True))
+        comm.ring_allreduce(cur, out_p, rra.Codec("bfp", bits=4, diff_prev=prev,
+                                                   diff_base=base, average=True))
+        comm.ring_allreduce(cur, out_e, rra.Codec("bfp", bits=4, diff_prev=prev, diff_base=base,
+                                                   average=True, residual=res))
+        assert comm.status() == rra.RRA_OK
+        acc["lossless"] += out_l[0].double()
+        acc["plain"] += out_p[0].double()
+        acc["ef"] += out_e[0].double()
+        scale = acc["lossless"].pow(2).mean().sqrt().item()
+        row = {"round": k + 1,
+               "rms_rel_err_plain": (acc["plain"] - acc["lossless"]).pow(2).mean().sqrt().item() / scale,
+               "rms_rel_err_ef": (acc["ef"] - acc["lossless"]).pow(2).mean().sqrt().item() / scale}
+        rows.append(row)
+    print(json.dumps({"drift_study": True, "N": N, "T": T, "codec": "diff+bfp4, average",
+                      "rounds": rows}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -604,6 +659,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["rra", "reference"], default="rra")
     ap.add_argument("--config", choices=CONFIG_NAMES, default="bfp8_bucket")
+    ap.add_argument("--ef", action="store_true",
+                    help="BFP workloads: with error feedback (an fp32 residual per rank)")
+    ap.add_argument("--drift-rounds", type=int, default=0,
+                    help="error-feedback drift study: K DiLoCo rounds (T / --scale per rank), "
+                         "compressed with and without feedback against the lossless ring")
     ap.add_argument("--scale", type=int, default=1,
                     help="run the workload with T / scale elements per rank: a small case for "
                          "ncu captures, reported with its own T (not the metric's workload)")
@@ -624,6 +684,9 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_setup()
+    if args.drift_rounds:
+        run_drift(args)
+        return
     if args.sweep:
         run_sweep(args, world, rank)
     elif args.impl == "reference":
