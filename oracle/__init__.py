@@ -71,6 +71,8 @@ def lib():
                                          sz, vp, vp, i32, vp, u64p, u64p]
             L.oracle_ring_ef.restype = i32
             L.oracle_allgather.argtypes = [i32, sz, vp, i32, u64p, u64p]
+            L.oracle_codec_stats.argtypes = [i32, sz, vp, i32, u64p]
+            L.oracle_codec_stats.restype = i32
             L.oracle_broadcast.argtypes = [i32, sz, vp, i32, i32, u64p, u64p]
             L.oracle_tree_allreduce.argtypes = [i32, sz, vp, u64p, u64p]
             for f in (L.oracle_allgather, L.oracle_broadcast, L.oracle_tree_allreduce):
@@ -165,6 +167,19 @@ def ring(inputs, in_dtype="f32", out_dtype="f32", codec="none", bits=8, threshol
     if rc != 0:
         raise ValueError("oracle_ring: bad arguments")
     return outputs, np.array(sent[:], np.uint64), np.array(recv[:], np.uint64)
+
+
+def codec_stats(bufs, dtype="f32"):
+    """Statistics of N input buffers for the adaptive codec choice:
+    [elements, nonzero (fp32 bits not +0.0), nonzero flushed to code 0 by
+    BFP4, nonzero flushed to code 0 by BFP8], with 128-element blocks cut
+    from each ring chunk's start."""
+    N, T = len(bufs), bufs[0].size
+    _check(bufs, T, dtype)
+    st = (C.c_uint64 * 4)()
+    if lib().oracle_codec_stats(N, T, _ptrs(bufs), DTYPES[dtype], st) != 0:
+        raise ValueError("oracle_codec_stats: bad arguments")
+    return np.array(st[:], np.uint64)
 
 
 def allgather(bufs, dtype="f32"):

@@ -783,3 +783,51 @@ void oracle_cast_from_f32(const float *x, size_t n, int t, void *out)
     for (size_t i = 0; i < n; i++)
         store_from_f32(out, i, t, x[i]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* codec statistics for the adaptive choice  [P4 §5 future directions:       */
+/* watch sparsity and value distribution, switch compression accordingly]    */
+/* ------------------------------------------------------------------------ */
+
+/* Over the N input buffers of T elements (each cut into chunks of ceil(T/N)
+ * and each chunk into 128-element BFP blocks from its start, as the ring's
+ * first hop encodes them):
+ *   stats[0] = N * T                      elements
+ *   stats[1] = elements whose fp32 bits are not +0.0
+ *   stats[2] = of those, the ones whose BFP4 code is 0 (|x| <= 2^(e-3))
+ *   stats[3] = of those, the ones whose BFP8 code is 0 (|x| <= 2^(e-7))
+ * A code rounds to 0 exactly when |x| * 2^(q-e) <= 1/2 (ties to even), with
+ * e the block exponent and q = bits - 2. */
+int oracle_codec_stats(int N, size_t T, const void *const *in, int in_t, uint64_t *stats)
+{
+    if (N < 1)
+        return -1;
+    for (int k = 0; k < 4; k++)
+        stats[k] = 0;
+    float *blk = malloc(OR_BFP_BLOCK * sizeof(float));
+    for (int r = 0; r < N; r++)
+        for (int c = 0; c < N; c++) {
+            size_t lo, len;
+            chunk_range(T, N, c, &lo, &len);
+            for (size_t b = 0; b < len; b += OR_BFP_BLOCK) {
+                const size_t m = len - b < OR_BFP_BLOCK ? len - b : OR_BFP_BLOCK;
+                for (size_t i = 0; i < m; i++)
+                    blk[i] = load_as_f32(in[r], lo + b + i, in_t);
+                const int e = oracle_bfp_block_exponent(blk, m);
+                for (size_t i = 0; i < m; i++) {
+                    uint32_t u;
+                    memcpy(&u, &blk[i], 4);
+                    stats[0]++;
+                    if (u == 0u)
+                        continue;
+                    stats[1]++;
+                    if (fabsf(blk[i]) <= ldexpf(1.0f, e - 3))
+                        stats[2]++;
+                    if (fabsf(blk[i]) <= ldexpf(1.0f, e - 7))
+                        stats[3]++;
+                }
+            }
+        }
+    free(blk);
+    return 0;
+}

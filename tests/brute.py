@@ -218,3 +218,28 @@ def allgather(bufs, elem_bytes):
             lo, hi = ch[(r - s) % N]
             bufs[r][lo:hi] = msgs[r]
     return bufs, sent, recv
+
+
+# ---------------------------------------------------------------- codec statistics
+
+def codec_stats(xs):
+    """[elements, nonzero, flushed by BFP4, flushed by BFP8] over N lists of
+    float32 scalars: 128-element blocks from each ring chunk's start; a
+    nonzero element (bits not +0.0) is flushed when its code rounds to 0,
+    i.e. when |x| * 2^(q - e) <= 1/2."""
+    N, T = len(xs), len(xs[0])
+    st = [0, 0, 0, 0]
+    for x in xs:
+        for lo, hi in chunks(T, N):
+            for b in range(lo, hi, 128):
+                blk = [F(v) for v in x[b:min(b + 128, hi)]]
+                e = bfp_exponent(blk)
+                for v in blk:
+                    st[0] += 1
+                    if not nonzero(v):
+                        continue
+                    st[1] += 1
+                    for k, bits in ((2, 4), (3, 8)):
+                        if bfp_code(v, e, bits) == 0:
+                            st[k] += 1
+    return st

@@ -3,7 +3,7 @@ catch every one.  Each mutant is a one-line edit of oracle.c (wrong step
 index, wrong mantissa scale, ties away from zero, off-by-one exponent, wrong
 clamp, wrong threshold tie, wrong header size, reversed tree levels, swapped
 difference, wrong subnormal scaling in the fp16 conversion, error-feedback sign,
-owner without error feedback); the mutated copy
+owner without error feedback, flush tie in the codec statistics); the mutated copy
 is compiled into a temporary directory and the pin suite is run against it in
 a child process.  The real oracle is never modified."""
 import os
@@ -31,6 +31,7 @@ MUTANTS = {
     "average_by_reciprocal": ("w = w / (float)N;", "w = w * (1.0f / (float)N);", 1),
     "f16_subnormal_scale": ("float q = nearbyintf(ldexpf(a, 24));", "float q = nearbyintf(ldexpf(a, 23));", 1),
     "ef_residual_sign": ("e[i] = u[i] - (there ? d : 0.0f);", "e[i] = (there ? d : 0.0f) - u[i];", 1),
+    "stats_flush_tie": ("if (fabsf(blk[i]) <= ldexpf(1.0f, e - 7))", "if (fabsf(blk[i]) < ldexpf(1.0f, e - 7))", 1),
     "ef_owner_skipped": ("            if (resid)\n                msg_encode_ef(&held[r]",
                          "            if (0)\n                msg_encode_ef(&held[r]", 1),
 }

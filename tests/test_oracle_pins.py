@@ -565,3 +565,46 @@ def test_error_feedback_needs_a_lossy_codec():
     for codec in ("none", "sparse"):
         with pytest.raises(ValueError):
             O.ring(xs, codec=codec, residual=res)
+
+
+# --------------------------------------------------------------- codec statistics
+
+def test_codec_stats_closed_form():
+    """One block with maximum 1.0 (e = 0): BFP8 rounds |x| <= 2^-7 to code 0
+    (1/128 is the tie and goes to even 0; 1/127 does not), BFP4 rounds
+    |x| <= 2^-3 to 0.  +0.0 is not counted as nonzero; -0.0 is, and flushes."""
+    x = np.array([1.0, 1 / 128, 1 / 127, 0.125, 0.13, 0.0, -0.0], np.float32)
+    st = O.codec_stats([x])
+    assert list(st) == [7, 6, 4, 2]
+
+
+def test_codec_stats_blocks_start_at_chunk_starts():
+    """Blocks are cut from each ring chunk's start, so the same values give
+    different counts for different N when a block straddles a chunk edge."""
+    T = 256
+    x = np.full(T, 1e-3, np.float32)
+    x[0] = 1.0  # a large value only in the first 128 elements of the buffer
+    st1 = O.codec_stats([x])  # one chunk: the block of x[0] holds 127 small values
+    assert list(st1) == [T, T, 127, 127]
+    xs = [x.copy(), x.copy(), x.copy()]
+    st3 = O.codec_stats(xs)  # chunks of 86: only x[0]'s block (86 values) sees 1.0
+    assert list(st3) == [3 * T, 3 * T, 3 * 85, 3 * 85]
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N,T", [(1, 300), (2, 257), (3, 1000), (5, 64)])
+def test_codec_stats_brute_force(dt, N, T):
+    rng = np.random.default_rng(N * 31 + T)
+    xs = []
+    for _ in range(N):
+        x = (rng.standard_normal(T) * 10.0 ** rng.integers(-6, 2, T)).astype(np.float32)
+        x[rng.random(T) < 0.3] = 0.0
+        x[rng.random(T) < 0.02] = -0.0
+        xs.append(x)
+    if dt != "f32":
+        hs = [O.from_f32(x, dt) for x in xs]
+        vals = [O.to_f32(h, dt) for h in hs]
+    else:
+        hs, vals = xs, xs
+    st = O.codec_stats(hs, dt)
+    assert list(st) == brute.codec_stats([list(v) for v in vals])
