@@ -405,6 +405,41 @@ rra_status rra_get_crossover(rra_comm *comm, size_t *bytes_per_rank);
 rra_status rra_autotune_crossover(rra_comm *comm, void *const *buf, size_t count,
                                   rra_dtype dtype, void *stream, size_t *bytes_per_rank);
 
+/*
+ * Adaptive codec choice ([cccl] §5, future directions: watch the gradients'
+ * statistics -- sparsity, value distribution -- and switch the compression
+ * to match, instead of one static threshold).
+ *
+ * Statistics of the N input buffers in[r][0..count): every ring chunk of
+ * every buffer is cut into 128-element blocks from its start, as the ring's
+ * first hop encodes them.
+ *  elements      N * count.
+ *  nonzero       elements whose fp32 value is not +0.0 (-0.0 counts).
+ *  bfp4_flushed  nonzero elements whose BFP4 code would be 0
+ *                (|x| <= 2^(e-3), e the block exponent).
+ *  bfp8_flushed  the same for BFP8 (|x| <= 2^(e-7)).
+ */
+typedef struct {
+    uint64_t elements, nonzero, bfp4_flushed, bfp8_flushed;
+} rra_codec_stats;
+
+/* Measure the statistics (one read of every input on `stream`, then a
+ * synchronous read-back: not inside a stream capture, RRA_ERR_INVALID).
+ * Errors: RRA_ERR_INVALID (NULL, count 0 or above max_count, bad dtype),
+ * RRA_ERR_CUDA. */
+rra_status rra_codec_measure(rra_comm *comm, const void *const *in, size_t count,
+                             rra_dtype dtype, rra_codec_stats *out, void *stream);
+
+/* Measure, then fill *codec (every other field zero/NULL) by this rule:
+ * RRA_CODEC_SPARSE with `sparsity_threshold` when the share of zero elements
+ * exceeds it; else BFP4 when it flushes at most `max_flushed_fraction` of
+ * the nonzero elements to code 0; else BFP8.  *stats (if not NULL) receives
+ * the measurement.  Errors: RRA_ERR_INVALID for a threshold outside [0, 1) or
+ * a fraction outside [0, 1]; otherwise as rra_codec_measure. */
+rra_status rra_codec_advise(rra_comm *comm, const void *const *in, size_t count, rra_dtype dtype,
+                            float sparsity_threshold, float max_flushed_fraction,
+                            rra_codec *codec, rra_codec_stats *stats, void *stream);
+
 /* Test-only fault injection: in the next collective call, simulated rank
  * "rank" does not publish the message it sends at ring step "step" (1-based,
  * counted over both passes) for the first slice each block handles, so its

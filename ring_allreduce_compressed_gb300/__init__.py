@@ -46,6 +46,11 @@ class _Codec(C.Structure):
                 ("residual", C.c_void_p)]
 
 
+class _Stats(C.Structure):
+    _fields_ = [("elements", C.c_uint64), ("nonzero", C.c_uint64),
+                ("bfp4_flushed", C.c_uint64), ("bfp8_flushed", C.c_uint64)]
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile librra.so in-tree (see _compile.py)."""
     from . import _compile
@@ -84,6 +89,9 @@ def lib():
         L.rra_set_crossover.argtypes = [vp, sz]
         L.rra_get_crossover.argtypes = [vp, C.POINTER(C.c_size_t)]
         L.rra_autotune_crossover.argtypes = [vp, vp, sz, i32, vp, C.POINTER(C.c_size_t)]
+        L.rra_codec_measure.argtypes = [vp, vp, sz, i32, C.POINTER(_Stats), vp]
+        L.rra_codec_advise.argtypes = [vp, vp, sz, i32, C.c_float, C.c_float,
+                                       C.POINTER(_Codec), C.POINTER(_Stats), vp]
         L.rra_status_string.argtypes = [i32]
         L.rra_status_string.restype = C.c_char_p
         for name in ("rra_comm_create", "rra_comm_destroy", "rra_ring_allreduce",
@@ -92,7 +100,8 @@ def lib():
                      "rra_diff_encode", "rra_get_bytes", "rra_comm_status", "rra_set_timeout",
                      "rra_debug_withhold", "rra_comm_set_tuning", "rra_comm_last_shape",
                      "rra_autotune", "rra_allreduce_auto", "rra_set_crossover",
-                     "rra_get_crossover", "rra_autotune_crossover"):
+                     "rra_get_crossover", "rra_autotune_crossover", "rra_codec_measure",
+                     "rra_codec_advise"):
             getattr(L, name).restype = st
         _lib = L
     return _lib
@@ -273,6 +282,29 @@ class Comm:
                                             _dtype_code(bufs[0].dtype), _stream(stream),
                                             C.byref(v)), "rra_autotune_crossover")
         return v.value
+
+    def codec_stats(self, inputs, stream=None) -> dict:
+        """rra_codec_measure: elements, nonzero, and the nonzero elements BFP4
+        and BFP8 would round to code 0, over the N inputs."""
+        st = _Stats()
+        _check(lib().rra_codec_measure(self._h, _ptrs(inputs, "inputs"), inputs[0].numel(),
+                                       _dtype_code(inputs[0].dtype), C.byref(st), _stream(stream)),
+               "rra_codec_measure")
+        return {k: int(getattr(st, k)) for k, _ in _Stats._fields_}
+
+    def advise_codec(self, inputs, sparsity_threshold: float = 0.5,
+                     max_flushed_fraction: float = 0.01, stream=None):
+        """rra_codec_advise: (Codec, stats) -- sparse above the sparsity
+        threshold, else BFP4 if it flushes at most the given share of the
+        nonzero values to code 0, else BFP8."""
+        st, c = _Stats(), _Codec()
+        _check(lib().rra_codec_advise(self._h, _ptrs(inputs, "inputs"), inputs[0].numel(),
+                                      _dtype_code(inputs[0].dtype), float(sparsity_threshold),
+                                      float(max_flushed_fraction), C.byref(c), C.byref(st),
+                                      _stream(stream)), "rra_codec_advise")
+        kind = {CODEC_NONE: "none", CODEC_BFP: "bfp", CODEC_SPARSE: "sparse"}[c.kind]
+        return (Codec(kind, bits=c.bits, sparsity_threshold=c.sparsity_threshold),
+                {k: int(getattr(st, k)) for k, _ in _Stats._fields_})
 
     def debug_withhold(self, rank: int, step: int):
         _check(lib().rra_debug_withhold(self._h, rank, step), "rra_debug_withhold")

@@ -401,9 +401,96 @@ __global__ void __launch_bounds__(kThreads) diff_kernel(const float *cur, const 
     }
 }
 
+// ---------------------------------------------------------------- codec statistics
+// One warp per 128-element BFP block (4 elements a lane).  Blocks are cut
+// from the start of each ring chunk of every rank's buffer, as the ring's
+// first hop encodes them.  A nonzero element (fp32 bits not +0.0) is flushed
+// by a BFP code of q = bits - 2 fraction bits when it rounds to code 0, that
+// is when |x| <= 2^(e - q - 1) for the block exponent e.
+
+// 2^k as an fp32 value for k in [-149, 127] (subnormal below -126).
+__device__ __forceinline__ float pow2_exact(int k)
+{
+    return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(1 << (k + 149));
+}
+
+template <int IN_T>
+__global__ void __launch_bounds__(kThreads) codec_stats_kernel(const __grid_constant__ StatsArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const long long nb = (a.n + kBlock - 1) / kBlock; // blocks of a full chunk
+    const long long total = (long long)a.N * a.N * nb;
+    const long long wid = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    uint32_t cnt_nz = 0, cnt_f4 = 0, cnt_f8 = 0;
+    unsigned long long cnt_el = 0;
+    for (long long g = wid; g < total; g += nw) {
+        const int r = (int)(g / ((long long)a.N * nb));
+        const long long rem = g - (long long)r * a.N * nb;
+        const int c = (int)(rem / nb);
+        const long long b = rem - (long long)c * nb;
+        const long long lo = min(a.T, (long long)c * a.n), hi = min(a.T, lo + a.n);
+        const long long e0 = lo + b * kBlock;
+        if (e0 >= hi)
+            continue; // a short chunk has fewer blocks
+        const long long e1 = min(hi, e0 + kBlock);
+        float v[4];
+        unsigned mx = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const long long e = e0 + lane * 4 + i;
+            v[i] = e < e1 ? to_f32(reinterpret_cast<const typename Elem<IN_T>::type *>(a.in[r])[e])
+                          : 0.0f;
+            mx = max(mx, __float_as_uint(v[i]) & 0x7fffffffu);
+        }
+        mx = __reduce_max_sync(kFull, mx);
+        const int e = max((int)(mx >> 23), 1) - 127;
+        const float t4 = pow2_exact(e - 3), t8 = pow2_exact(e - 7);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (e0 + lane * 4 + i >= e1)
+                continue;
+            if (__float_as_uint(v[i]) == 0u)
+                continue;
+            ++cnt_nz;
+            cnt_f4 += fabsf(v[i]) <= t4 ? 1u : 0u;
+            cnt_f8 += fabsf(v[i]) <= t8 ? 1u : 0u;
+        }
+        if (lane == 0)
+            cnt_el += (unsigned long long)(e1 - e0);
+    }
+    cnt_nz = __reduce_add_sync(kFull, cnt_nz);
+    cnt_f4 = __reduce_add_sync(kFull, cnt_f4);
+    cnt_f8 = __reduce_add_sync(kFull, cnt_f8);
+    if (lane == 0) {
+        if (cnt_el)
+            atomicAdd(a.stats + 0, cnt_el);
+        if (cnt_nz)
+            atomicAdd(a.stats + 1, (unsigned long long)cnt_nz);
+        if (cnt_f4)
+            atomicAdd(a.stats + 2, (unsigned long long)cnt_f4);
+        if (cnt_f8)
+            atomicAdd(a.stats + 3, (unsigned long long)cnt_f8);
+    }
+}
+
 } // namespace
 
 // ---------------------------------------------------------------- launchers
+
+cudaError_t launch_codec_stats(const StatsArgs &a, int dtype, cudaStream_t st)
+{
+    const long long nb = (a.n + kBlock - 1) / kBlock;
+    const long long warps = (long long)a.N * a.N * nb;
+    const int grid = grid_for((warps + kThreads / 32 - 1) / (kThreads / 32), kThreads / 32);
+    if (dtype == kF32)
+        codec_stats_kernel<kF32><<<grid, kThreads, 0, st>>>(a);
+    else if (dtype == kF16)
+        codec_stats_kernel<kF16><<<grid, kThreads, 0, st>>>(a);
+    else
+        codec_stats_kernel<kBF16><<<grid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_bfp_encode(const void *x, long long n, int dtype, int bits, int8_t *exps,
                               uint8_t *mants, cudaStream_t st)

@@ -48,6 +48,7 @@ struct rra_comm {
     std::map<std::array<long long, 6>, rra::Tune> tuned;
     rra::Tune last{};      // shape of the last ring launch (blocks = blocks per SM)
     size_t crossover = 0;  // rra_allreduce_auto: tree below this many bytes per rank
+    unsigned long long *stats = nullptr; // [4] codec statistics (inside `counters`)
     std::map<long long, int> occ; // (kernel key, smem) -> blocks per SM
 };
 
@@ -562,7 +563,8 @@ rra_status rra_comm_create(int nranks, size_t max_count, rra_dtype max_dtype, rr
     }
     cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
     cudaDeviceGetAttribute(&c->smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, c->device);
-    const size_t cbytes = sizeof(unsigned long long) * 4 * (size_t)nranks;
+    // two counter sets (sent and recv per rank), then 4 codec statistics
+    const size_t cbytes = sizeof(unsigned long long) * (4 * (size_t)nranks + 4);
     if (cudaMalloc(&c->counters, cbytes) != cudaSuccess) {
         delete c;
         return RRA_ERR_NOMEM;
@@ -572,6 +574,7 @@ rra_status rra_comm_create(int nranks, size_t max_count, rra_dtype max_dtype, rr
         delete c;
         return RRA_ERR_NOMEM;
     }
+    c->stats = c->counters + 4 * (size_t)nranks;
     if (cudaMemset(c->counters, 0, cbytes) != cudaSuccess ||
         cudaMemset(c->status, 0, sizeof(unsigned)) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
@@ -975,6 +978,76 @@ rra_status rra_autotune_crossover(rra_comm *comm, void *const *buf, size_t count
     comm->crossover = cross;
     if (bytes_per_rank)
         *bytes_per_rank = cross;
+    return RRA_OK;
+}
+
+rra_status rra_codec_measure(rra_comm *comm, const void *const *in, size_t count,
+                             rra_dtype dtype, rra_codec_stats *out, void *stream)
+{
+    if (!comm || !in || !out || count == 0 || count > comm->max_count || !valid_dtype(dtype))
+        return RRA_ERR_INVALID;
+    rra_status s = check_device(comm);
+    if (s != RRA_OK)
+        return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone)
+        return RRA_ERR_INVALID; // it reads the result back on the host
+    StatsArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.N = comm->N;
+    a.T = (long long)count;
+    a.n = (a.T + a.N - 1) / a.N;
+    a.stats = comm->stats;
+    for (int r = 0; r < comm->N; ++r) {
+        if (!in[r])
+            return RRA_ERR_INVALID;
+        a.in[r] = in[r];
+    }
+    unsigned long long h[4];
+    if (cudaMemsetAsync(comm->stats, 0, sizeof h, st) != cudaSuccess ||
+        launch_codec_stats(a, dtype, st) != cudaSuccess ||
+        cudaMemcpyAsync(h, comm->stats, sizeof h, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    out->elements = h[0];
+    out->nonzero = h[1];
+    out->bfp4_flushed = h[2];
+    out->bfp8_flushed = h[3];
+    return RRA_OK;
+}
+
+rra_status rra_codec_advise(rra_comm *comm, const void *const *in, size_t count, rra_dtype dtype,
+                            float sparsity_threshold, float max_flushed_fraction,
+                            rra_codec *codec, rra_codec_stats *stats, void *stream)
+{
+    if (!codec || !(sparsity_threshold >= 0.0f && sparsity_threshold < 1.0f) ||
+        !(max_flushed_fraction >= 0.0f && max_flushed_fraction <= 1.0f))
+        return RRA_ERR_INVALID;
+    rra_codec_stats st{};
+    const rra_status s = rra_codec_measure(comm, in, count, dtype, &st, stream);
+    if (s != RRA_OK)
+        return s;
+    if (stats)
+        *stats = st;
+    std::memset(codec, 0, sizeof *codec);
+    codec->sparsity_threshold = sparsity_threshold;
+    // sparse when the zeros exceed the threshold (the sparse codec still
+    // decides per group); else the narrowest BFP that flushes at most the
+    // allowed share of the nonzero values to code 0
+    const double zeros = (double)(st.elements - st.nonzero);
+    if (st.elements && zeros > (double)sparsity_threshold * (double)st.elements) {
+        codec->kind = RRA_CODEC_SPARSE;
+        codec->bits = 8;
+    } else if ((double)st.bfp4_flushed <= (double)max_flushed_fraction * (double)st.nonzero) {
+        codec->kind = RRA_CODEC_BFP;
+        codec->bits = 4;
+    } else {
+        codec->kind = RRA_CODEC_BFP;
+        codec->bits = 8;
+    }
     return RRA_OK;
 }
 

@@ -173,6 +173,16 @@ cudaError_t launch_sparse_decode(const uint32_t *hdr, const void *vals, const in
 cudaError_t launch_diff_encode(const float *cur, const float *prev, float *diff, long long n,
                                cudaStream_t st);
 
+// Codec statistics over the N input buffers: stats[0..3] = elements, nonzero,
+// flushed by BFP4, flushed by BFP8 (added to; the caller clears them).
+struct StatsArgs {
+    int N;
+    long long T, n;
+    unsigned long long *stats;
+    const void *in[kMaxRanks];
+};
+cudaError_t launch_codec_stats(const StatsArgs &a, int dtype, cudaStream_t st);
+
 int num_sms();
 
 } // namespace rra

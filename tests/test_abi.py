@@ -69,6 +69,9 @@ def test_host_side_argument_checks(lib):
     assert L.rra_set_crossover(None, 0) == rra.RRA_ERR_INVALID
     assert L.rra_get_crossover(None, None) == rra.RRA_ERR_INVALID
     assert L.rra_autotune_crossover(None, None, 10, 0, None, None) == rra.RRA_ERR_INVALID
+    assert L.rra_codec_measure(None, None, 10, 0, None, None) == rra.RRA_ERR_INVALID
+    assert L.rra_codec_advise(None, None, 10, 0, C.c_float(0.5), C.c_float(0.01), None, None,
+                              None) == rra.RRA_ERR_INVALID
 
 
 def test_header_constants_match_the_binding():
