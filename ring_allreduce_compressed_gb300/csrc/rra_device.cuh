@@ -63,27 +63,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t tx
                  : "memory");
 }
 
-#ifndef RRA_WAIT_HINT_NS
-#define RRA_WAIT_HINT_NS 0
-#endif
+// One test of an mbarrier phase (acquire on success); it may block for a
+// short, hardware-chosen time before returning false.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
-#if RRA_WAIT_HINT_NS > 0
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(smem_u32(bar)), "r"(parity), "r"((uint32_t)RRA_WAIT_HINT_NS)
-                 : "memory");
-#else
     asm volatile("{\n\t.reg .pred p;\n\t"
                  "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
                  : "r"(smem_u32(bar)), "r"(parity)
                  : "memory");
-#endif
     return ok != 0;
 }
 
