@@ -152,19 +152,23 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, an earlier GB300 copy measurement)"
 
 
-# the files the ring kernels are compiled from (host-side launch code excluded)
-RING_KERNEL_SOURCES = ("ring_kernel.cuh", "rra_device.cuh", "rra_kernels.h", "ring_none.cu",
-                       "ring_bfp8.cu", "ring_bfp4.cu", "ring_bfp8_ef.cu", "ring_bfp4_ef.cu",
-                       "ring_sparse.cu")
+# The files each workload's ring kernel is compiled from (host-side launch
+# code excluded): a change to another codec's files leaves its summary valid.
+RING_KERNEL_COMMON = ("ring_kernel.cuh", "rra_device.cuh", "rra_kernels.h")
+RING_KERNEL_SOURCES = {
+    "bfp8_bucket": ("ring_bfp8.cu", "ring_bfp8_ef.cu"),
+    "diloco_n8": ("ring_bfp4.cu", "ring_bfp4_ef.cu"),
+    "sparse_n16": ("ring_sparse.cu", "wire_sparse.cuh"),
+    "lossless_n4": ("ring_none.cu",),
+}
 
 
-def kernel_sources_sha() -> str:
+def kernel_sources_sha(config: str = "bfp8_bucket") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ring_allreduce_compressed_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name in RING_KERNEL_SOURCES:
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in sorted(RING_KERNEL_COMMON + RING_KERNEL_SOURCES[config]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -181,7 +185,7 @@ def traffic_from_profile(config: str):
     m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
     if not m_sha or not m_tr:
         return None, "summary incomplete"
-    if m_sha.group(1) != kernel_sources_sha():
+    if m_sha.group(1) != kernel_sources_sha(config):
         return None, "kernel changed since the ncu capture"
     return int(m_tr.group(1)), path
 

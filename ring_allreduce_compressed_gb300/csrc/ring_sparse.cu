@@ -3,6 +3,7 @@
 // rank-to-warp mapping, and the generic path; its own translation unit so
 // that the library compiles in parallel.
 #include "ring_kernel.cuh"
+#include "wire_sparse.cuh"
 
 namespace rra {
 
