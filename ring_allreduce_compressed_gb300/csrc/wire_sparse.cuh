@@ -148,8 +148,7 @@ template <> struct WireCodec<kCodecSparse> {
         }
         const int cnt = __popc(m.pres);
         const int incl = warp_incl_scan(lane, cnt);
-        const int total = __shfl_sync(kFull, incl, 31);
-        emit(s, lane, m.f, m.pres, 1u, cnt, incl, total, a);
+        emit(s, lane, m.f, m.pres, 1u, cnt, incl, (int)m.nnz, a);
     }
     // The header of a dense group also carries its nonzero count.  The
     // receiver restores every value exactly (absent ones are +0.0), so the
@@ -166,17 +165,28 @@ template <> struct WireCodec<kCodecSparse> {
             if (8 * lane + i < Vg && __float_as_uint(v[i]) != 0u)
                 nzm |= 1u << i;
         const int cnt = __popc(nzm);
-        const int incl = warp_incl_scan(lane, cnt);
-        const int total = __shfl_sync(kFull, incl, 31);
+        const int total = (int)__reduce_add_sync(kFull, (unsigned)cnt);
         // full groups compare with the precomputed integer limit; a ragged
         // group evaluates nnz < (1 - threshold) * len in double
         const uint32_t fmt = Vg == kTile ? (total < a.sp_full_lim ? 1u : 0u)
                                          : ((double)total < a.one_minus_thr * (double)Vg ? 1u : 0u);
+        // only a sparse group needs every lane's output position
+        const int incl = fmt ? warp_incl_scan(lane, cnt) : 0;
         emit(sub(slot, gi, a), lane, v, nzm, fmt, cnt, incl, total, a);
     }
     __device__ __forceinline__ static void decode_add(const Reg &m, float (&v)[8], int,
                                                       unsigned char *)
     {
+        if (m.pres == 0xffu) { // every position present (always so for a dense group)
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                const float2 r = __fadd2_rn(make_float2(v[i], v[i + 1]),
+                                            make_float2(m.f[i], m.f[i + 1]));
+                v[i] = r.x;
+                v[i + 1] = r.y;
+            }
+            return;
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             v[i] = ((m.pres >> i) & 1u) ? __fadd_rn(v[i], m.f[i]) : v[i];
