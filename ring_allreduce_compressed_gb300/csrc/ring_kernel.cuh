@@ -337,6 +337,38 @@ template <int BITS> struct CodecBfp {
     }
 };
 template <> struct WireCodec<kCodecBfp8> : CodecBfp<8> {};
+
+// fp16 outputs straight from BFP8 offset codes.  A byte permute places an
+// offset code b = m + 128 under the high byte 0x64 of an fp16 word: the half
+// H = 1024 + b.  With s = 2^(e-q) and c = -1152 * s both fp16 numbers,
+// fma(H, s, c) = (H - 1152) * s = m * 2^(e-q) exactly before its one
+// rounding, so the result is the exact decoded value rounded once to fp16 --
+// the same bits as rounding the fp32 decode to fp16.  s is an fp16 number for
+// e - q in [-24, 15] and c for e - q in [-31, 5]; elsewhere the fp32 decode
+// is used.  The table entry of block exponent e (index e + 128) holds the
+// half2 words (s, s) and (c, c), or zero outside that range.
+__device__ __forceinline__ uint2 bfp8_f16_entry(int e)
+{
+    const int k = e - BfpGroup<8>::q;
+    if (k < -24 || k > 5)
+        return make_uint2(0u, 0u);
+    const uint32_t s = k >= -14 ? (uint32_t)(k + 15) << 10 : 1u << (k + 24);
+    const uint32_t c = 0x8000u | ((uint32_t)(k + 25) << 10) | 0x80u; // -1.125 * 2^(k+10)
+    return make_uint2(s | s << 16, c | c << 16);
+}
+
+// h[j] = fp16 pair (element 2j, 2j+1) of one lane's 8 codes; sc from the table.
+__device__ __forceinline__ void bfp8_decode_f16(const uint32_t w[2], uint2 sc, uint32_t h[4])
+{
+    const __half2 s2 = *reinterpret_cast<const __half2 *>(&sc.x);
+    const __half2 c2 = *reinterpret_cast<const __half2 *>(&sc.y);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t hw = __byte_perm(w[j >> 1], 0x64646464u, (j & 1) ? 0x4342 : 0x4140);
+        const __half2 r = __hfma2(*reinterpret_cast<const __half2 *>(&hw), s2, c2);
+        h[j] = *reinterpret_cast<const uint32_t *>(&r);
+    }
+}
 template <> struct WireCodec<kCodecBfp4> : CodecBfp<4> {};
 
 // ---------------------------------------------------------------- kernel
@@ -371,8 +403,10 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int K = a.K, D = a.D;
-    const Layout Lo =
-        make_layout(N, K, D, a.slot_bytes, a.stage_bytes, W, FAST, CODEC == kCodecSparse);
+    // BFP8 allgather steps write fp16 outputs straight from the codes
+    constexpr bool kDirect16 = CODEC == kCodecBfp8;
+    const Layout Lo = make_layout(N, K, D, a.slot_bytes, a.stage_bytes, W, FAST,
+                                  CODEC == kCodecSparse, kDirect16);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lo.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + Lo.empty);
     uint64_t *sbar = reinterpret_cast<uint64_t *>(smem + Lo.stage_bar);
@@ -396,6 +430,10 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < 2 * N; i += blockDim.x)
             a.zero[i] = 0ull;
+    const uint2 *lut = reinterpret_cast<const uint2 *>(smem + Lo.lut);
+    if constexpr (kDirect16)
+        for (int i = threadIdx.x; i < 256; i += blockDim.x)
+            reinterpret_cast<uint2 *>(smem + Lo.lut)[i] = bfp8_f16_entry(i - 128);
     mbar_fence_init();
     __syncthreads();
 
@@ -510,6 +548,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     const int out_t = a.out_t;
     const int osz = dtype_size(out_t);
     const bool plain_out = !a.average && !a.base && a.vec_out;
+    const bool direct16 = kDirect16 && plain_out && out_t == kF16;
     auto output_group = [&](int r, int c, int V, int gi, float (&v)[8]) {
         const long long e0 = (long long)c * n + t0 + gi * kTile + 8 * lane;
         if (plain_out && V == TW) { // full slice, no epilogue arithmetic: vector store
@@ -773,18 +812,51 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                         break;
                     }
                     unsigned char *dslot = slots + (size_t)(dst * K + snd.slot) * a.slot_bytes;
+                    bool done = false;
+                    if constexpr (kDirect16) {
+                        // a full slice of plain fp16 outputs: codes straight to fp16
+                        if (direct16 && V == TW) {
+                            uint4 *op = reinterpret_cast<uint4 *>(
+                                            reinterpret_cast<__half *>(a.out[r]) +
+                                            (long long)c * n + t0) +
+                                        lane;
+#pragma unroll
+                            for (int gi = 0; gi < G; ++gi) {
+                                Reg m;
+                                if (kEarly)
+                                    m = m0;
+                                else
+                                    C::load(rslot, gi, lane, scratch, a, m);
+                                if (fwd)
+                                    C::store(dslot, gi, lane, m, a);
+                                uint32_t h[4];
+                                const uint2 sc = lut[m.e + 128]; // m.e is a signed byte
+                                if (sc.x != 0u) {
+                                    bfp8_decode_f16(m.w, sc, h);
+                                } else {
+                                    float v[8];
+                                    C::values(m, v, lane, scratch);
+                                    pack16x8<kF16>(v, h);
+                                }
+                                op[gi * (kTile / 8)] = make_uint4(h[0], h[1], h[2], h[3]);
+                            }
+                            done = true;
+                        }
+                    }
+                    if (!done) {
 #pragma unroll 1
-                    for (int gi = 0; gi < G; ++gi) {
-                        Reg m;
-                        if (kEarly)
-                            m = m0;
-                        else
-                            C::load(rslot, gi, lane, scratch, a, m);
-                        if (fwd)
-                            C::store(dslot, gi, lane, m, a);
-                        float v[8];
-                        C::values(m, v, lane, scratch);
-                        output_group(r, c, V, gi, v);
+                        for (int gi = 0; gi < G; ++gi) {
+                            Reg m;
+                            if (kEarly)
+                                m = m0;
+                            else
+                                C::load(rslot, gi, lane, scratch, a, m);
+                            if (fwd)
+                                C::store(dslot, gi, lane, m, a);
+                            float v[8];
+                            C::values(m, v, lane, scratch);
+                            output_group(r, c, V, gi, v);
+                        }
                     }
                     __syncwarp();
                     finish_step(r, g, !kEarly, fwd, rb, rb);

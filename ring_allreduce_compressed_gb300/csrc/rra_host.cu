@@ -219,7 +219,8 @@ bool pick_shape(rra_comm *c, const Tune &t, int N, long long n, int kc, int ies,
             // slot it streams from only after its own send of the same step,
             // so with one slot every rank would wait for its successor
             for (int K = t.K ? t.K : 2; K >= (G == 1 ? 1 : 2); --K) {
-                const Layout L = make_layout(N, K, D, slot, stage, warps, fast, sparse);
+                const Layout L =
+                    make_layout(N, K, D, slot, stage, warps, fast, sparse, kc == kCodecBfp8);
                 const bool several = pass % 2 == 0; // leave room for `want` blocks per SM
                 const int need = several ? want * (L.total + 1024) : L.total;
                 const int have = several ? c->smem_per_sm : c->smem_optin;

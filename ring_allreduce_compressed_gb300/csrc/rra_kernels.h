@@ -84,14 +84,14 @@ struct CopyArgs {
 
 // Shared-memory layout of the ring / copy kernels (host and device agree).
 struct Layout {
-    int full, empty, stage_bar, rank_state, slots, stages, scratch, total;
+    int full, empty, stage_bar, rank_state, slots, stages, scratch, lut, total;
 };
 
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 __host__ __device__ inline Layout make_layout(int N, int K, int D, int slot_bytes,
                                               int stage_bytes, int warps, bool fast,
-                                              bool sparse)
+                                              bool sparse, bool lut)
 {
     Layout L;
     int off = 0;
@@ -112,6 +112,9 @@ __host__ __device__ inline Layout make_layout(int N, int K, int D, int slot_byte
     off = align_up(off, 16);
     L.scratch = off;
     off += sparse ? warps * (256 * 4 + 256) : 0;
+    off = align_up(off, 16);
+    L.lut = off; // BFP8: 256 entries of 8 bytes (the fp16 output table)
+    off += lut ? 256 * 8 : 0;
     L.total = align_up(off, 128);
     return L;
 }

@@ -190,6 +190,39 @@ def test_bfp8_config2_shape_small():
     assert all(int(s) == 14 * (n // 128 + n) for s in gpu[1])
 
 
+@pytest.mark.parametrize("in_dt", ["f32", "f16"])
+@pytest.mark.parametrize("G", [0, 1, 2, 8])
+def test_bfp8_f16_outputs_across_exponents(in_dt, G):
+    """fp16 outputs of BFP8 codes for block exponents from far below the fp16
+    subnormals to past the fp16 maximum.  Where 2^(e-q) and the offset term
+    are fp16 numbers the allgather writes fp16 straight from the codes, else
+    it rounds the fp32 decode; both must give the oracle's bits (the exact
+    decoded value rounded once to fp16), on full slices and the ragged tail,
+    for every slice width."""
+    N, T = 8, 8 * 2048 * 6 + 8 * 40
+    g = torch.Generator(device="cuda")
+    g.manual_seed(70 + G)
+    lo, hi = (-48, 21) if in_dt == "f32" else (-30, 13)
+    nb = -(-T // 128)
+    j = (torch.arange(nb, device="cuda") * 7) % (hi - lo + 1) + lo
+    scale = torch.pow(2.0, j.float()).repeat_interleave(128)[:T]
+    xs = cast([torch.randn(T, generator=g, device="cuda") * scale for _ in range(N)], in_dt)
+    comm = rra.Comm(N, T, xs[0].dtype)
+    if G:
+        comm.set_tuning(0, 0, 0, G)
+    outs = [torch.zeros(T, dtype=torch.float16, device="cuda") for _ in range(N)]
+    codec = rra.Codec("bfp", bits=8)
+    comm.ring_allreduce(xs, outs, codec)
+    assert comm.status() == rra.RRA_OK
+    if G:
+        assert comm.last_shape()[3] == G
+    sent, recv = comm.get_bytes()
+    comm.close()
+    ref = oracle_ring(xs, in_dt, "f16", codec="bfp", bits=8)
+    compare((outs, np.array(sent, np.uint64), np.array(recv, np.uint64)), ref,
+            f"bfp8 {in_dt}->f16 G={G}")
+
+
 # ------------------------------------------------------------------ sparse
 
 @pytest.mark.parametrize("thr", [0.5, 0.2, 0.9])
