@@ -304,12 +304,10 @@ template <int BITS> struct CodecBfp {
         else
             reinterpret_cast<uint32_t *>(slot + 16 + gi * kMB)[lane] = m.w[0];
     }
-    template <bool DEC>
-    __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int gi,
-                                                  int lane, int, const RingArgs &,
-                                                  unsigned char *)
+    // encode group gi into the slot and return its codes
+    __device__ __forceinline__ static void encode_reg(const float (&v)[8], unsigned char *slot,
+                                                      int gi, int lane, Reg &m)
     {
-        Reg m;
         BfpGroup<BITS>::encode(v, m.e, m.w);
         if ((lane & 15) == 0)
             slot[2 * gi + (lane >> 4)] = (unsigned char)(int8_t)m.e;
@@ -317,6 +315,14 @@ template <int BITS> struct CodecBfp {
             reinterpret_cast<uint2 *>(slot + 16 + gi * kMB)[lane] = make_uint2(m.w[0], m.w[1]);
         else
             reinterpret_cast<uint32_t *>(slot + 16 + gi * kMB)[lane] = m.w[0];
+    }
+    template <bool DEC>
+    __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int gi,
+                                                  int lane, int, const RingArgs &,
+                                                  unsigned char *)
+    {
+        Reg m;
+        encode_reg(v, slot, gi, lane, m);
         if (DEC)
             BfpGroup<BITS>::decode(m.w, m.e, v);
     }
@@ -376,8 +382,9 @@ template <> struct WireCodec<kCodecBfp4> : CodecBfp<4> {};
 // MODE kRanksShared: a warp may play several ranks (N > warps per block).
 // MODE kRankPerWarp8 / kRankPerWarp16: every warp plays exactly one rank, so
 // rank indices, addresses and byte counts stay in registers across the
-// loops; blocks of at most 8 warps get up to 80 registers a thread (three
-// blocks per SM), blocks of up to 16 warps 64 (two blocks per SM).
+// loops (each rank loop runs exactly once: the host launches W = N warps);
+// blocks of at most 8 warps get up to 80 registers a thread (three blocks per
+// SM), blocks of up to 16 warps 64 (two blocks per SM).
 // EF: error feedback -- every value a rank encodes takes its residual first,
 // and the residual keeps what the encoding lost (BFP instantiations only).
 template <int CODEC, int IN_T, bool FAST, int G, int MODE, bool EF>
@@ -395,8 +402,9 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     constexpr int es = dtype_size(LT);
     constexpr int TW = kTile * G; // elements per rank per step
     // The reduce-scatter group loop of the BFP codecs is unrolled (measured
-    // faster: more independent work between the block reductions); the other
-    // loops stay rolled to keep the code within the instruction cache.
+    // faster: more independent work between the block reductions), and so is
+    // the BFP8 allgather loop that writes fp16 straight from the codes; the
+    // other loops stay rolled to keep the code within the instruction cache.
     constexpr int kUnrollRS = (CODEC == kCodecBfp8 || CODEC == kCodecBfp4) ? G : 1;
     const int N = a.N;
     const int W = blockDim.x >> 5;
@@ -460,16 +468,18 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     // issue for every rank; "inflight" counts loads issued and not consumed.
     int cur_item = blockIdx.x; // slice position of the next load to issue
     int cur_g = 1;             // its step
+    // that slice position is full in every chunk
+    bool cur_full = (long long)cur_item * TW + TW <= min_len;
     int inflight = 0;          // loads issued and not yet consumed, per rank
     const int tiles = (int)a.tiles;
     auto issue_one = [&](int r, int d) { // lane 0: load (cur_item, cur_g) of rank r into stage d
         int c = r - cur_g;
         c += c < 0 ? N : 0;
         const long long t0 = (long long)cur_item * TW;
-        const uint32_t bytes = (uint32_t)slice_len(c, t0) * es;
+        const uint32_t bytes = cur_full ? (uint32_t)(TW * es) : (uint32_t)slice_len(c, t0) * es;
         uint64_t *bar = sbar + r * D + d;
         unsigned char *dst = stages + (size_t)(r * D + d) * a.stage_bytes;
-        if (bytes < (uint32_t)(TW * es)) {
+        if (!cur_full && bytes < (uint32_t)(TW * es)) {
             // a short slice: zero the rest of the stage (both streams), so
             // that the consumer reads +0.0 past the end without a test per
             // group; these stores precede the arrive that publishes the stage
@@ -479,7 +489,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     *reinterpret_cast<uint32_t *>(dst + TW * 4 + o) = 0u;
             }
         }
-        if (bytes == 0) {
+        if (!cur_full && bytes == 0) {
             mbar_arrive(bar);
             return;
         }
@@ -498,6 +508,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
         if (++cur_g > N) {
             cur_g = 1;
             cur_item += gridDim.x;
+            cur_full = (long long)cur_item * TW + TW <= min_len;
         }
     };
     if constexpr (FAST) {
@@ -648,7 +659,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
             }
             if (send) {
                 const int dst = r + 1 == N ? 0 : r + 1;
-                if (!(r == a.withhold_rank && g == withhold_g))
+                if (!((ONE || r == a.withhold_rank) && g == withhold_g))
                     mbar_arrive(full + dst * K + snd.slot);
                 if (!ONE)
                     rsent[r] += sb;
@@ -660,11 +671,14 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
         t0 = (long long)item * TW;
         const bool item_full = t0 + TW <= min_len;
         // the fault-injection test withholds one send in each block's first slice
-        withhold_g = first_item_withhold && item == (int)blockIdx.x ? a.withhold_step : 0;
+        withhold_g = first_item_withhold && item == (int)blockIdx.x &&
+                             (!ONE || warp == a.withhold_rank)
+                         ? a.withhold_step
+                         : 0;
 
         // ---- reduce-scatter steps g = 1..N-1: send chunk (r-g) mod N
         for (int g = 1; ok && g < N; ++g) {
-            for (int r = warp; r < N; r += rstride) {
+            for (int r = warp; ONE || r < N; r += rstride) {
                 int c = r - g;
                 c += c < 0 ? N : 0;
                 const int V = slice_len(c, t0, item_full);
@@ -711,8 +725,11 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     else
                         C::template encode<false>(v, dslot, gi, lane, V, a, scratch);
                 }
-                __syncwarp();
+                if constexpr (CODEC == kCodecSparse)
+                    __syncwarp(); // bytes() reads the group headers of all lanes
                 finish_step(r, g, g >= 2 && !kEarly, true, rb, C::bytes(V, dslot, a));
+                if (ONE)
+                    break;
             }
             if (!ok)
                 break;
@@ -725,7 +742,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
             break;
 
         // ---- owner step g = N: chunk r; allreduce encodes the full sum once
-        for (int r = warp; r < N; r += rstride) {
+        for (int r = warp; ONE || r < N; r += rstride) {
             const int V = slice_len(r, t0, item_full);
             const int dst = r + 1 == N ? 0 : r + 1;
             const bool recv = N > 1, send = allred && N > 1;
@@ -753,8 +770,43 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
             // N = 1 has no allgather step: encode into the rank's own (unused) slot
             unsigned char *dslot = send ? slots + (size_t)(dst * K + snd.slot) * a.slot_bytes
                                         : slots + (size_t)(r * K) * a.slot_bytes;
+            bool done = false;
+            if constexpr (kDirect16 && !EF) {
+                // a full slice of plain fp16 outputs: encode the sum, send the
+                // codes and write fp16 straight from them (a rolled loop: the
+                // unrolled one measured slower, its code too large for the
+                // instruction cache next to the unrolled loops)
+                if (direct16 && send && V == TW) {
+                    uint4 *op = reinterpret_cast<uint4 *>(
+                                    reinterpret_cast<__half *>(a.out[r]) + (long long)r * n + t0) +
+                                lane;
 #pragma unroll 1
-            for (int gi = 0; gi < G; ++gi) {
+                    for (int gi = 0; gi < G; ++gi) {
+                        float v[8];
+                        input_group(r, r, V, gi, sp, v);
+                        Reg m;
+                        if (kEarly)
+                            m = m0;
+                        else
+                            C::load(rslot, gi, lane, scratch, a, m);
+                        C::decode_add(m, v, lane, scratch);
+                        Reg w;
+                        C::encode_reg(v, dslot, gi, lane, w);
+                        uint32_t h[4];
+                        const uint2 sc = lut[w.e + 128];
+                        if (sc.x != 0u) {
+                            bfp8_decode_f16(w.w, sc, h);
+                        } else {
+                            C::values(w, v, lane, scratch);
+                            pack16x8<kF16>(v, h);
+                        }
+                        op[gi * (kTile / 8)] = make_uint4(h[0], h[1], h[2], h[3]);
+                    }
+                    done = true;
+                }
+            }
+#pragma unroll 1
+            for (int gi = 0; !done && gi < G; ++gi) {
                 float v[8];
                 input_group(r, r, V, gi, sp, v);
                 if (recv) {
@@ -773,8 +825,11 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                 }
                 output_group(r, r, V, gi, v);
             }
-            __syncwarp();
+            if constexpr (CODEC == kCodecSparse)
+                __syncwarp();
             finish_step(r, N, recv && !kEarly, send, rb, send ? C::bytes(V, dslot, a) : 0u);
+            if (ONE)
+                break;
         }
         if (!ok)
             break;
@@ -788,7 +843,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
         if (allred) {
             for (int g = N + 1; ok && g <= 2 * N - 1; ++g) {
                 const bool fwd = g < 2 * N - 1;
-                for (int r = warp; r < N; r += rstride) {
+                for (int r = warp; ONE || r < N; r += rstride) {
                     int c = r - g;
                     c += c < 0 ? N : 0;
                     c += c < 0 ? N : 0;
@@ -860,6 +915,8 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     }
                     __syncwarp();
                     finish_step(r, g, !kEarly, fwd, rb, rb);
+                    if (ONE)
+                        break;
                 }
                 if (!ok)
                     break;
