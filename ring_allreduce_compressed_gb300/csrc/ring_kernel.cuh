@@ -208,15 +208,21 @@ template <int BITS> struct BfpGroup {
 //  load / store          group gi: slot <-> Reg (allgather forwarding).
 //  encode<DEC>           encode the lane's 8 fp32 values of group gi into the
 //                        slot; with DEC, v becomes what a receiver decodes.
+//                        Returns the group's wire bytes where they depend on
+//                        the data (kVarBytes), else 0.
 //  decode_add            v = v + decoded group (positions a sparse message
 //                        does not carry keep v).
 //  values                v = decoded group (0 where a sparse message has none).
 //  bytes(V, slot)        wire bytes of a message of V elements.
+//  kVarBytes             the wire bytes depend on the data; the kernel then
+//                        sums group_bytes(m, V, gi) of the groups it loads and
+//                        the returns of encode rather than re-reading headers.
 
 template <int CODEC> struct WireCodec;
 
 // Lossless: fp32, group gi at byte 1024*gi, lane L at 32L within the group.
 template <> struct WireCodec<kCodecNone> {
+    static constexpr bool kVarBytes = false;
     static constexpr int slot_bytes(int G) { return kTile * 4 * G; }
     struct Reg {
         float f[8];
@@ -237,13 +243,14 @@ template <> struct WireCodec<kCodecNone> {
         p[1] = make_float4(m.f[4], m.f[5], m.f[6], m.f[7]);
     }
     template <bool DEC>
-    __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int gi,
-                                                  int lane, int, const RingArgs &,
-                                                  unsigned char *)
+    __device__ __forceinline__ static uint32_t encode(float (&v)[8], unsigned char *slot, int gi,
+                                                      int lane, int, const RingArgs &,
+                                                      unsigned char *)
     {
         float4 *p = reinterpret_cast<float4 *>(slot + gi * kTile * 4) + 2 * lane;
         p[0] = make_float4(v[0], v[1], v[2], v[3]);
         p[1] = make_float4(v[4], v[5], v[6], v[7]);
+        return 0u;
     }
     __device__ __forceinline__ static void decode_add(const Reg &m, float (&v)[8], int,
                                                       unsigned char *)
@@ -275,6 +282,7 @@ template <> struct WireCodec<kCodecNone> {
 // (group gi at 16 + gi * 256*BITS/8; lane L at 8L bytes (8-bit) or 4L bytes
 // (4-bit) within the group).
 template <int BITS> struct CodecBfp {
+    static constexpr bool kVarBytes = false;
     static constexpr int kMB = kTile * BITS / 8;
     static constexpr int slot_bytes(int G) { return 16 + kMB * G; }
     struct Reg {
@@ -317,14 +325,15 @@ template <int BITS> struct CodecBfp {
             reinterpret_cast<uint32_t *>(slot + 16 + gi * kMB)[lane] = m.w[0];
     }
     template <bool DEC>
-    __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int gi,
-                                                  int lane, int, const RingArgs &,
-                                                  unsigned char *)
+    __device__ __forceinline__ static uint32_t encode(float (&v)[8], unsigned char *slot, int gi,
+                                                      int lane, int, const RingArgs &,
+                                                      unsigned char *)
     {
         Reg m;
         encode_reg(v, slot, gi, lane, m);
         if (DEC)
             BfpGroup<BITS>::decode(m.w, m.e, v);
+        return 0u;
     }
     __device__ __forceinline__ static void decode_add(const Reg &m, float (&v)[8], int,
                                                       unsigned char *)
@@ -401,11 +410,13 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     using Reg = typename C::Reg;
     constexpr int es = dtype_size(LT);
     constexpr int TW = kTile * G; // elements per rank per step
-    // The reduce-scatter group loop of the BFP codecs is unrolled (measured
-    // faster: more independent work between the block reductions), and so is
-    // the BFP8 allgather loop that writes fp16 straight from the codes; the
+    // The reduce-scatter group loop of the lossy codecs is unrolled (measured
+    // faster: more independent work between the warp reductions), and so are
+    // the BFP8 allgather loop that writes fp16 straight from the codes and the
+    // allgather loop of the sparse codec (slices of at most 4 groups); the
     // other loops stay rolled to keep the code within the instruction cache.
-    constexpr int kUnrollRS = (CODEC == kCodecBfp8 || CODEC == kCodecBfp4) ? G : 1;
+    constexpr int kUnrollRS = CODEC != kCodecNone ? G : 1;
+    constexpr int kUnrollAG = CODEC == kCodecSparse ? G : 1;
     const int N = a.N;
     const int W = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5;
@@ -695,9 +706,11 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                 }
                 const unsigned char *sp = stages + (size_t)(r * D + stg.slot) * a.stage_bytes;
                 const unsigned char *rslot = slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
-                uint32_t rb = 0;
+                // wire bytes received and sent (data-dependent sizes are
+                // summed group by group below)
+                uint32_t rb = 0, sb = 0;
                 Reg m0;
-                if (g >= 2) {
+                if (g >= 2 && (kEarly || !C::kVarBytes)) {
                     rb = C::bytes(V, rslot, a);
                     if (kEarly)
                         release_early(r, rslot, rb, m0);
@@ -714,20 +727,23 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     input_group(r, c, V, gi, sp, v);
                     if (g >= 2) {
                         Reg m;
-                        if (kEarly)
+                        if (kEarly) {
                             m = m0;
-                        else
+                        } else {
                             C::load(rslot, gi, lane, scratch, a, m);
+                            if constexpr (C::kVarBytes)
+                                rb += C::group_bytes(m, V, gi);
+                        }
                         C::decode_add(m, v, lane, scratch);
                     }
                     if constexpr (EF)
                         encode_ef(r, c, V, gi, v, dslot);
                     else
-                        C::template encode<false>(v, dslot, gi, lane, V, a, scratch);
+                        sb += C::template encode<false>(v, dslot, gi, lane, V, a, scratch);
                 }
-                if constexpr (CODEC == kCodecSparse)
-                    __syncwarp(); // bytes() reads the group headers of all lanes
-                finish_step(r, g, g >= 2 && !kEarly, true, rb, C::bytes(V, dslot, a));
+                if constexpr (!C::kVarBytes)
+                    sb = C::bytes(V, dslot, a);
+                finish_step(r, g, g >= 2 && !kEarly, true, rb, sb);
                 if (ONE)
                     break;
             }
@@ -758,7 +774,8 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
             }
             const unsigned char *sp = stages + (size_t)(r * D + stg.slot) * a.stage_bytes;
             const unsigned char *rslot = slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
-            const uint32_t rb = recv ? C::bytes(V, rslot, a) : 0u;
+            uint32_t rb = recv && (kEarly || !C::kVarBytes) ? C::bytes(V, rslot, a) : 0u;
+            uint32_t sb = 0;
             Reg m0;
             if (kEarly && recv)
                 release_early(r, rslot, rb, m0);
@@ -811,23 +828,26 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                 input_group(r, r, V, gi, sp, v);
                 if (recv) {
                     Reg m;
-                    if (kEarly)
+                    if (kEarly) {
                         m = m0;
-                    else
+                    } else {
                         C::load(rslot, gi, lane, scratch, a, m);
+                        if constexpr (C::kVarBytes)
+                            rb += C::group_bytes(m, V, gi);
+                    }
                     C::decode_add(m, v, lane, scratch);
                 }
                 if (allred) {
                     if constexpr (EF)
                         encode_ef(r, r, V, gi, v, dslot);
                     else
-                        C::template encode<true>(v, dslot, gi, lane, V, a, scratch);
+                        sb += C::template encode<true>(v, dslot, gi, lane, V, a, scratch);
                 }
                 output_group(r, r, V, gi, v);
             }
-            if constexpr (CODEC == kCodecSparse)
-                __syncwarp();
-            finish_step(r, N, recv && !kEarly, send, rb, send ? C::bytes(V, dslot, a) : 0u);
+            if constexpr (!C::kVarBytes)
+                sb = C::bytes(V, dslot, a);
+            finish_step(r, N, recv && !kEarly, send, rb, send ? sb : 0u);
             if (ONE)
                 break;
         }
@@ -856,7 +876,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     }
                     const unsigned char *rslot =
                         slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
-                    const uint32_t rb = C::bytes(V, rslot, a);
+                    uint32_t rb = (kEarly || !C::kVarBytes) ? C::bytes(V, rslot, a) : 0u;
                     Reg m0;
                     if (kEarly)
                         release_early(r, rslot, rb, m0);
@@ -899,13 +919,16 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                         }
                     }
                     if (!done) {
-#pragma unroll 1
+#pragma unroll kUnrollAG
                         for (int gi = 0; gi < G; ++gi) {
                             Reg m;
-                            if (kEarly)
+                            if (kEarly) {
                                 m = m0;
-                            else
+                            } else {
                                 C::load(rslot, gi, lane, scratch, a, m);
+                                if constexpr (C::kVarBytes)
+                                    rb += C::group_bytes(m, V, gi);
+                            }
                             if (fwd)
                                 C::store(dslot, gi, lane, m, a);
                             float v[8];

@@ -21,6 +21,7 @@ namespace rra {
 // values (+0.0 where the message has none) and a presence mask, from which
 // the identical sub-message can be written again when it is forwarded.
 template <> struct WireCodec<kCodecSparse> {
+    static constexpr bool kVarBytes = true;
     struct Reg {
         uint32_t fmt, nnz, pres;
         float f[8];
@@ -43,6 +44,13 @@ template <> struct WireCodec<kCodecSparse> {
     {
         return min(max(V - gi * kTile, 0), kTile);
     }
+    // wire bytes of one sub-message: the 8-byte header, then nnz (value,
+    // index) pairs (sparse) or the group's values (dense); an empty group
+    // past the slice's end sends nothing
+    __device__ __forceinline__ static uint32_t sub_bytes(uint32_t fmt, uint32_t nnz, int len)
+    {
+        return len > 0 ? 8u + (fmt ? 8u * nnz : 4u * (uint32_t)len) : 0u;
+    }
     // wire bytes of the sub-messages of a slice of V elements
     __device__ __forceinline__ static uint32_t bytes(int V, const unsigned char *slot,
                                                      const RingArgs &a)
@@ -50,9 +58,14 @@ template <> struct WireCodec<kCodecSparse> {
         uint32_t b = 0;
         for (int gi = 0; gi * kTile < V; ++gi) {
             const uint2 h = *reinterpret_cast<const uint2 *>(sub(slot, gi, a));
-            b += 8u + (h.x ? 8u * h.y : 4u * (uint32_t)group_len(V, gi));
+            b += sub_bytes(h.x, h.y, group_len(V, gi));
         }
         return b;
+    }
+    // wire bytes of a loaded group gi of a slice of V elements
+    __device__ __forceinline__ static uint32_t group_bytes(const Reg &m, int V, int gi)
+    {
+        return sub_bytes(m.fmt, m.nnz, group_len(V, gi));
     }
     // Write the sub-message whose lane values are v and whose present
     // positions are the bits of nzm: sparse (ascending indices) when fmt is
@@ -154,16 +167,22 @@ template <> struct WireCodec<kCodecSparse> {
     // receiver restores every value exactly (absent ones are +0.0), so the
     // decoded values are v itself: DEC changes nothing.
     template <bool DEC>
-    __device__ __forceinline__ static void encode(float (&v)[8], unsigned char *slot, int gi,
-                                                  int lane, int V, const RingArgs &a,
-                                                  unsigned char *)
+    __device__ __forceinline__ static uint32_t encode(float (&v)[8], unsigned char *slot, int gi,
+                                                      int lane, int V, const RingArgs &a,
+                                                      unsigned char *)
     {
         const int Vg = group_len(V, gi);
         uint32_t nzm = 0;
+        if (Vg == kTile) { // a full group: every lane's 8 positions are inside it
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (8 * lane + i < Vg && __float_as_uint(v[i]) != 0u)
-                nzm |= 1u << i;
+            for (int i = 0; i < 8; ++i)
+                nzm |= (__float_as_uint(v[i]) != 0u ? 1u : 0u) << i;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (8 * lane + i < Vg && __float_as_uint(v[i]) != 0u)
+                    nzm |= 1u << i;
+        }
         const int cnt = __popc(nzm);
         const int total = (int)__reduce_add_sync(kFull, (unsigned)cnt);
         // full groups compare with the precomputed integer limit; a ragged
@@ -173,6 +192,7 @@ template <> struct WireCodec<kCodecSparse> {
         // only a sparse group needs every lane's output position
         const int incl = fmt ? warp_incl_scan(lane, cnt) : 0;
         emit(sub(slot, gi, a), lane, v, nzm, fmt, cnt, incl, total, a);
+        return sub_bytes(fmt, (uint32_t)total, Vg);
     }
     __device__ __forceinline__ static void decode_add(const Reg &m, float (&v)[8], int,
                                                       unsigned char *)
