@@ -640,10 +640,29 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                 rrecv[r] += rb;
         }
     };
-    // after a step that consumed a staged load: refill that stage
+    // Common case of a step's waits: every barrier it needs has already
+    // completed, seen with one test each and one warp vote.  Otherwise the
+    // step waits for them one by one (bounded).  A completed phase stays
+    // complete until this rank acts on that barrier again, so the tests are
+    // exact.  One-group messages free their receive slot before the send
+    // wait, so they always take the one-by-one order.
+    auto all_ready = [&](bool stage, bool recv, bool send, int r, int dst) -> bool {
+        if constexpr (kEarly)
+            return false;
+        bool t = true;
+        if (FAST && stage)
+            t = mbar_try_wait(sbar + r * D + stg.slot, (uint32_t)stg.phase);
+        if (recv)
+            t &= mbar_try_wait(full + r * K + rcv.slot, (uint32_t)rcv.phase);
+        if (send)
+            t &= mbar_try_wait(empty + dst * K + snd.slot, (uint32_t)(snd.phase ^ 1));
+        return __all_sync(kFull, t);
+    };
+    // after a step that consumed a staged load: refill that stage (the warp
+    // barrier of the step's finish_step orders every lane's reads of the
+    // stage before lane 0 issues the copy that overwrites it)
     auto stage_step = [&]() {
         if constexpr (FAST) {
-            __syncwarp();
             if (inflight == D && cur_item < tiles) { // refill the stage just consumed
                 if (lane == 0)
                     for (int r = warp; r < N; r += rstride)
@@ -694,13 +713,16 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                 c += c < 0 ? N : 0;
                 const int V = slice_len(c, t0, item_full);
                 const int dst = r + 1 == N ? 0 : r + 1;
-                if (FAST && !wait_ready(sbar + r * D + stg.slot, (uint32_t)stg.phase,
-        a.timeout_ns, a.status)) {
+                const bool pre = all_ready(true, g >= 2, true, r, dst);
+                if (!pre && FAST &&
+                    !wait_ready(sbar + r * D + stg.slot, (uint32_t)stg.phase, a.timeout_ns,
+                                a.status)) {
                     ok = false;
                     break;
                 }
-                if (g >= 2 && !wait_ready(full + r * K + rcv.slot, (uint32_t)rcv.phase,
-        a.timeout_ns, a.status)) {
+                if (!pre && g >= 2 &&
+                    !wait_ready(full + r * K + rcv.slot, (uint32_t)rcv.phase, a.timeout_ns,
+                                a.status)) {
                     ok = false;
                     break;
                 }
@@ -715,8 +737,8 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     if (kEarly)
                         release_early(r, rslot, rb, m0);
                 }
-                if (!wait_ready(empty + dst * K + snd.slot, (uint32_t)(snd.phase ^ 1),
-        a.timeout_ns, a.status)) {
+                if (!pre && !wait_ready(empty + dst * K + snd.slot, (uint32_t)(snd.phase ^ 1),
+                                        a.timeout_ns, a.status)) {
                     ok = false;
                     break;
                 }
@@ -762,13 +784,16 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
             const int V = slice_len(r, t0, item_full);
             const int dst = r + 1 == N ? 0 : r + 1;
             const bool recv = N > 1, send = allred && N > 1;
-            if (FAST && !wait_ready(sbar + r * D + stg.slot, (uint32_t)stg.phase,
-        a.timeout_ns, a.status)) {
+            const bool pre = all_ready(true, recv, send, r, dst);
+            if (!pre && FAST &&
+                !wait_ready(sbar + r * D + stg.slot, (uint32_t)stg.phase, a.timeout_ns,
+                            a.status)) {
                 ok = false;
                 break;
             }
-            if (recv && !wait_ready(full + r * K + rcv.slot, (uint32_t)rcv.phase,
-        a.timeout_ns, a.status)) {
+            if (!pre && recv &&
+                !wait_ready(full + r * K + rcv.slot, (uint32_t)rcv.phase, a.timeout_ns,
+                            a.status)) {
                 ok = false;
                 break;
             }
@@ -779,8 +804,9 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
             Reg m0;
             if (kEarly && recv)
                 release_early(r, rslot, rb, m0);
-            if (send && !wait_ready(empty + dst * K + snd.slot,
-                                             (uint32_t)(snd.phase ^ 1), a.timeout_ns, a.status)) {
+            if (!pre && send &&
+                !wait_ready(empty + dst * K + snd.slot, (uint32_t)(snd.phase ^ 1), a.timeout_ns,
+                            a.status)) {
                 ok = false;
                 break;
             }
@@ -869,8 +895,9 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     c += c < 0 ? N : 0;
                     const int V = slice_len(c, t0, item_full);
                     const int dst = r + 1 == N ? 0 : r + 1;
-                    if (!wait_ready(full + r * K + rcv.slot, (uint32_t)rcv.phase,
-        a.timeout_ns, a.status)) {
+                    const bool pre = all_ready(false, true, fwd, r, dst);
+                    if (!pre && !wait_ready(full + r * K + rcv.slot, (uint32_t)rcv.phase,
+                                            a.timeout_ns, a.status)) {
                         ok = false;
                         break;
                     }
@@ -880,9 +907,9 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     Reg m0;
                     if (kEarly)
                         release_early(r, rslot, rb, m0);
-                    if (fwd && !wait_ready(empty + dst * K + snd.slot,
-                                                    (uint32_t)(snd.phase ^ 1), a.timeout_ns,
-                                                    a.status)) {
+                    if (!pre && fwd &&
+                        !wait_ready(empty + dst * K + snd.slot, (uint32_t)(snd.phase ^ 1),
+                                    a.timeout_ns, a.status)) {
                         ok = false;
                         break;
                     }
