@@ -71,6 +71,9 @@ def lib():
                                          sz, vp, vp, i32, vp, u64p, u64p]
             L.oracle_ring_ef.restype = i32
             L.oracle_allgather.argtypes = [i32, sz, vp, i32, u64p, u64p]
+            L.oracle_allgather_codec.argtypes = [i32, sz, vp, i32, i32, i32, C.c_double, sz,
+                                                 u64p, u64p]
+            L.oracle_allgather_codec.restype = i32
             L.oracle_codec_stats.argtypes = [i32, sz, vp, i32, u64p]
             L.oracle_codec_stats.restype = i32
             L.oracle_broadcast.argtypes = [i32, sz, vp, i32, i32, u64p, u64p]
@@ -188,6 +191,18 @@ def allgather(bufs, dtype="f32"):
     _check(bufs, T, dtype)
     sent, recv = _counters(N)
     assert lib().oracle_allgather(N, T, _ptrs(bufs), DTYPES[dtype], sent, recv) == 0
+    return bufs, np.array(sent[:], np.uint64), np.array(recv[:], np.uint64)
+
+
+def allgather_codec(bufs, dtype="f32", codec="bfp", bits=8, threshold=0.5, slice=RING_SLICE):
+    """In-place compressed allgather (reading AG): chunk r of bufs[r] is rank
+    r's contribution; every buffer ends with decode(codes) of every chunk."""
+    N, T = len(bufs), bufs[0].size
+    _check(bufs, T, dtype)
+    sent, recv = _counters(N)
+    if lib().oracle_allgather_codec(N, T, _ptrs(bufs), DTYPES[dtype], CODECS[codec], bits,
+                                    float(threshold), slice, sent, recv) != 0:
+        raise ValueError("oracle_allgather_codec: bad arguments")
     return bufs, np.array(sent[:], np.uint64), np.array(recv[:], np.uint64)
 
 

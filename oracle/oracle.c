@@ -52,6 +52,14 @@
  *  D2  epilogue: out = base + (v / N) when a base (previous result) is given
  *      and averaging is on; v / N with averaging only; v otherwise.
  *  RS  reduce-scatter: the owner's output is its fp32 sum (not re-encoded).
+ *  AG  compressed allgather ([P4] §2.1, operator-aware layer: allgather
+ *      and broadcast take lossless compression or a higher-precision lossy
+ *      one; §3.3: low-precision compression for all_gather after
+ *      all_reduce): the owner of chunk c encodes its own elements of chunk c
+ *      (widened to fp32) once, as one ring message; the allgather steps of
+ *      R1 forward those codes unchanged; every rank, the owner included,
+ *      stores decode(codes) in the buffer's dtype (RNE), so all buffers end
+ *      identical.  Sparse codes restore every element exactly.
  *  EF  error feedback ([P4] §5, future directions), BFP only: each rank
  *      keeps an fp32 residual e_r[T]; whatever value v it encodes (its
  *      reduce-scatter messages, and as owner its chunk's full sum) is encoded
@@ -692,6 +700,71 @@ int oracle_allgather(int N, size_t T, void *const *buf, int t, uint64_t *sent, u
             free(msg[r]);
         free(msg);
     }
+    return 0;
+}
+
+/* Compressed allgather (reading AG), in place: chunk r of buf[r] is rank
+ * r's contribution; codec BFP (bits 8 or 4) or sparse (threshold, slices of
+ * `slice` elements).  Rank r sends at allgather step s the codes of chunk
+ * (r - s + 1) mod N, so it forwards every chunk but chunk r + 1; the byte
+ * counters add the message bytes. */
+int oracle_allgather_codec(int N, size_t T, void *const *buf, int t, int codec, int bits,
+                           double threshold, size_t slice, uint64_t *sent, uint64_t *recv)
+{
+    if (N < 1 || (codec != OR_CODEC_BFP && codec != OR_CODEC_SPARSE) ||
+        (codec == OR_CODEC_BFP && bits != 8 && bits != 4) ||
+        (codec == OR_CODEC_SPARSE && slice == 0))
+        return -1;
+    codec_t cd = {codec, bits, threshold, slice};
+    for (int r = 0; r < N; r++)
+        sent[r] = recv[r] = 0;
+    /* held[r]: the codes rank r sends at the next step; first its own chunk */
+    message *held = calloc((size_t)N, sizeof(message));
+    message *inbox = calloc((size_t)N, sizeof(message));
+    float *x = malloc((T ? T : 1) * sizeof(float));
+    for (int r = 0; r < N; r++) {
+        size_t lo, len;
+        chunk_range(T, N, r, &lo, &len);
+        for (size_t i = 0; i < len; i++)
+            x[i] = load_as_f32(buf[r], lo + i, t);
+        msg_encode(&held[r], &cd, x, len);
+    }
+    /* the owner's own chunk becomes the decoded codes as well */
+    for (int r = 0; r < N; r++) {
+        size_t lo, len;
+        chunk_range(T, N, r, &lo, &len);
+        for (size_t i = 0; i < len; i++) {
+            int there;
+            float v = msg_value(&held[r], &cd, i, &there);
+            store_from_f32(buf[r], lo + i, t, there ? v : 0.0f);
+        }
+    }
+    for (int s = 1; s <= N - 1; s++) {
+        for (int r = 0; r < N; r++) {
+            int dst = mod((long)r + 1, N);
+            msg_copy(&inbox[dst], &held[r]);
+            sent[r] += inbox[dst].bytes;
+            recv[dst] += inbox[dst].bytes;
+        }
+        for (int r = 0; r < N; r++) {
+            int c = mod((long)r - s, N); /* the chunk rank r receives at step s */
+            size_t lo, len;
+            chunk_range(T, N, c, &lo, &len);
+            for (size_t i = 0; i < len; i++) {
+                int there;
+                float v = msg_value(&inbox[r], &cd, i, &there);
+                store_from_f32(buf[r], lo + i, t, there ? v : 0.0f);
+            }
+            msg_copy(&held[r], &inbox[r]);
+        }
+    }
+    for (int r = 0; r < N; r++) {
+        msg_free(&held[r]);
+        msg_free(&inbox[r]);
+    }
+    free(held);
+    free(inbox);
+    free(x);
     return 0;
 }
 

@@ -220,6 +220,41 @@ def allgather(bufs, elem_bytes):
     return bufs, sent, recv
 
 
+def allgather_codec(xs, codec="bfp", bits=8, threshold=0.5, slice_len=256):
+    """Compressed allgather of N lists of float32 scalars: the owner of chunk
+    c encodes its own elements once, the codes travel the ring unchanged, and
+    every rank (owner included) holds the decoded chunk.  Returns (results,
+    sent, recv)."""
+    N, T = len(xs), len(xs[0])
+    ch = chunks(T, N)
+    held = []
+    for r in range(N):
+        lo, hi = ch[r]
+        vals = [F(v) for v in xs[r][lo:hi]]
+        if codec == "bfp":
+            out, nb = bfp_roundtrip(vals, bits)
+        else:
+            out, _, nb = sparse_roundtrip(vals, threshold, slice_len)
+        held.append((out, nb))
+    res = [[F(v) for v in x] for x in xs]
+    for r in range(N):
+        lo, hi = ch[r]
+        res[r][lo:hi] = held[r][0]
+    sent, recv = [0] * N, [0] * N
+    cur = held
+    for s in range(1, N):
+        nxt = [None] * N
+        for r in range(N):
+            nxt[(r + 1) % N] = cur[r]
+            sent[r] += cur[r][1]
+            recv[(r + 1) % N] += cur[r][1]
+        for r in range(N):
+            lo, hi = ch[(r - s) % N]
+            res[r][lo:hi] = nxt[r][0]
+        cur = nxt
+    return res, sent, recv
+
+
 # ---------------------------------------------------------------- codec statistics
 
 def codec_stats(xs):

@@ -200,6 +200,88 @@ def test_allgather(N, T, dt):
         assert np.array_equal(np.array(ref[r]), out[r].view(np.uint32 if es == 4 else np.uint16))
 
 
+# --------------------------------------------------------------- compressed allgather
+# Reading AG: the owner encodes its chunk once, the codes travel the ring
+# unchanged, every rank (owner included) stores the decoded chunk.
+
+@pytest.mark.parametrize("codec,bits", [("bfp", 8), ("bfp", 4), ("sparse", 8)])
+@pytest.mark.parametrize("N,T", [(1, 10), (2, 64), (3, 50), (4, 64), (4, 17)])
+def test_allgather_codec_brute_force(codec, bits, N, T):
+    rng = np.random.default_rng(N * 31 + T)
+    xs = [(rng.standard_normal(T) * (rng.random(T) < 0.3)).astype(np.float32) for _ in range(N)]
+    out, sent, recv = O.allgather_codec([x.copy() for x in xs], "f32", codec, bits)
+    ref, bs, br = brute.allgather_codec([list(x) for x in xs], codec, bits)
+    for r in range(N):
+        assert np.array_equal(out[r].view(np.uint32), np.array(ref[r], np.float32).view(np.uint32))
+    assert list(sent) == bs and list(recv) == br
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_allgather_codec_is_the_chunk_codec_everywhere(bits, dt):
+    """Every buffer ends with, for each chunk c, the standalone codec's round
+    trip of the owner's chunk c, cast to the buffer's dtype; the byte counts
+    are the message sizes of the N - 1 chunks each rank forwards (all but
+    chunk r + 1)."""
+    N, T = 5, 5 * 300 + 7
+    rng = np.random.default_rng(bits + len(dt))
+    bufs = [O.from_f32((rng.standard_normal(T) * 1e-2).astype(np.float32), dt) for _ in range(N)]
+    n = -(-T // N)
+    lims = [(min(c * n, T), min((c + 1) * n, T)) for c in range(N)]
+    want, msg = [], []
+    for c, (lo, hi) in enumerate(lims):
+        x = O.to_f32(bufs[c][lo:hi], dt)
+        exps, mants = O.bfp_encode(x, bits)
+        want.append(O.from_f32(O.bfp_decode(exps, mants, hi - lo, bits), dt))
+        msg.append(O.bfp_bytes(hi - lo, bits))
+    out, sent, recv = O.allgather_codec([b.copy() for b in bufs], dt, "bfp", bits)
+    for r in range(N):
+        for c, (lo, hi) in enumerate(lims):
+            assert np.array_equal(out[r][lo:hi], want[c]), (r, c)
+        assert int(sent[r]) == sum(msg) - msg[(r + 1) % N]
+        assert int(recv[r]) == sum(msg) - msg[r]
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("N,T", [(2, 512), (4, 4096), (5, 1001)])
+def test_allgather_codec_is_the_allreduce_second_pass(bits, N, T):
+    """The compressed allreduce is its reduce-scatter followed by this
+    allgather of the owners' fp32 sums: outputs and byte counts add up."""
+    rng = np.random.default_rng(N + T + bits)
+    xs = [rng.standard_normal(T).astype(np.float32) for _ in range(N)]
+    ar, s_ar, r_ar = O.ring([x.copy() for x in xs], codec="bfp", bits=bits)
+    rs_out = [np.zeros(T, np.float32) for _ in range(N)]
+    rs, s_rs, r_rs = O.ring([x.copy() for x in xs], codec="bfp", bits=bits,
+                            mode="reduce_scatter", outputs=rs_out)
+    out, s_ag, r_ag = O.allgather_codec(rs, "f32", "bfp", bits)
+    for r in range(N):
+        assert np.array_equal(out[r].view(np.uint32), ar[r].view(np.uint32))
+    assert list(s_ar) == [a + b for a, b in zip(s_rs, s_ag)]
+    assert list(r_ar) == [a + b for a, b in zip(r_rs, r_ag)]
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_sparse_allgather_is_an_exact_copy(dt):
+    """Sparse codes restore every element, -0.0 included: the buffers equal the
+    lossless allgather's, while the bytes are the sparse messages' (fp32
+    values and int32 indices, so fewer than fp32 elements would take)."""
+    N, T = 4, 4 * 700
+    rng = np.random.default_rng(5)
+    vals = rng.standard_normal(T).astype(np.float32)
+    vals[rng.random(T) < 0.7] = 0.0
+    vals[::97] = -0.0
+    bufs = [O.from_f32(np.roll(vals, 13 * r), dt) for r in range(N)]
+    out, sent, _ = O.allgather_codec([b.copy() for b in bufs], dt, "sparse")
+    ref, _, _ = O.allgather([b.copy() for b in bufs], dt)
+    for r in range(N):
+        assert np.array_equal(out[r].view(np.uint8), ref[r].view(np.uint8))
+    n = T // N
+    msg = [brute.sparse_roundtrip(list(O.to_f32(bufs[c][c * n:(c + 1) * n], dt)), 0.5, 256)[2]
+           for c in range(N)]
+    assert [int(x) for x in sent] == [sum(msg) - msg[(r + 1) % N] for r in range(N)]
+    assert all(int(x) < 4 * n * (N - 1) for x in sent)
+
+
 # --------------------------------------------------------------- broadcast / tree
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 13])
