@@ -45,7 +45,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "compressed ring-allreduce algbw GB/s on 1 GB300 (N sim ranks), % of HBM peak"
 FALLBACK_HBM_GBS = 6800.0
-CONFIG_NAMES = ("bfp8_bucket", "lossless_n4", "sparse_n16", "diloco_n8")
+CONFIG_NAMES = ("bfp8_bucket", "lossless_n4", "sparse_n16", "diloco_n8", "bfp8_allgather")
 
 
 # ---------------------------------------------------------------- distributed
@@ -159,6 +159,7 @@ RING_KERNEL_SOURCES = {
     "bfp8_bucket": ("ring_bfp8.cu", "ring_bfp8_ef.cu"),
     "diloco_n8": ("ring_bfp4.cu", "ring_bfp4_ef.cu"),
     "sparse_n16": ("ring_sparse.cu", "wire_sparse.cuh"),
+    "bfp8_allgather": ("ring_bfp8.cu",),
     "lossless_n4": ("ring_none.cu",),
 }
 
@@ -216,6 +217,15 @@ class Workload:
             self.desc = ("block-FP8 compressed ring allreduce of one 25 MiB fp16 DDP bucket: "
                          "N=8 simulated ranks x 13,107,200 fp16, N(0,1e-3^2) seed 1, "
                          "128-element blocks, fp32 accumulation, fp16 output")
+        elif name == "bfp8_allgather":
+            self.inputs = W.bfp_bucket(self.N, self.T, seed=c["seed"], device=device)
+            self.out_dtype = torch.float16
+            self.codec_name = "bfp8-allgather"
+            self.desc = ("block-FP8 compressed allgather, in place (parameters gathered as in "
+                         "ZeRO/FSDP): N=8 simulated ranks x 13,107,200 fp16, N(0,1e-3^2) seed 1; "
+                         "each owner encodes its chunk once, every rank stores the decoded "
+                         "chunks.  Decoding then re-encoding gives the same codes, so every "
+                         "step does the same work on the buffers the previous step left")
         elif name == "lossless_n4":
             self.inputs = W.lossless(self.N, self.T, seed=c["seed"], device=device)
             self.out_dtype = torch.float32
@@ -247,7 +257,7 @@ class Workload:
             self.desc += "; with error feedback (an fp32 residual per rank, read and written)"
         if use_lib:
             self.comm = rra.Comm(self.N, self.T, self.in_dtype)
-            if name == "bfp8_bucket":
+            if name in ("bfp8_bucket", "bfp8_allgather"):
                 self.codec = rra.Codec("bfp", bits=8)
             elif name == "sparse_n16":
                 self.codec = rra.Codec("sparse", sparsity_threshold=0.5)
@@ -272,8 +282,14 @@ class Workload:
         base = self.T * 4 if diff else 0
         self.compulsory = (self.N * self.T * (ies + oes) + extra_in + base +
                            (self.N * self.T * 8 if ef else 0))  # residual read + write
+        if name == "bfp8_allgather":  # each rank reads its own chunk, writes its buffer
+            n = -(-self.T // self.N)
+            self.compulsory = self.N * (n * ies + self.T * oes)
 
     def step(self, stream=None):
+        if self.name == "bfp8_allgather":
+            self.comm.allgather(self.inputs, self.codec, stream=stream)
+            return
         self.comm.ring_allreduce(self.inputs, self.outputs, self.codec, stream=stream)
 
     def l2_note(self):
@@ -285,14 +301,15 @@ class Workload:
 # ---------------------------------------------------------------- CPU baseline (oracle)
 
 def oracle_sample_ring(wl_host, N, T, codec_name, slices_per_chunk, in_dt, out_dt, extra,
-                       ef=False):
-    """Run the oracle on the first `slices_per_chunk` 256-element slices of
-    every chunk (an exact sub-problem: slices are independent).  Returns
-    (seconds, payload bytes per rank of the sample)."""
+                       ef=False, first_slice=0):
+    """Run the oracle on `slices_per_chunk` 256-element slices of every chunk,
+    from slice `first_slice` on (an exact sub-problem: slices are
+    independent).  Returns (seconds, payload bytes per rank of the sample)."""
     import oracle as O
     n = T // N
-    m = min(n, slices_per_chunk * 256)
-    idx = np.concatenate([np.arange(c * n, c * n + m) for c in range(N)])
+    lo = min(n, first_slice * 256)
+    m = min(n - lo, slices_per_chunk * 256)
+    idx = np.concatenate([np.arange(c * n + lo, c * n + lo + m) for c in range(N)])
     xs = [np.ascontiguousarray(x[idx]) for x in wl_host]
     kw = {}
     if codec_name == "bfp8":
@@ -305,7 +322,10 @@ def oracle_sample_ring(wl_host, N, T, codec_name, slices_per_chunk, in_dt, out_d
     if ef:
         kw["residual"] = [np.zeros(xs[0].size, np.float32) for _ in range(N)]
     t0 = time.perf_counter()
-    O.ring(xs, in_dt, out_dt, **kw)
+    if codec_name == "bfp8-allgather":
+        O.allgather_codec(xs, in_dt, "bfp", 8)
+    else:
+        O.ring(xs, in_dt, out_dt, **kw)
     dt = time.perf_counter() - t0
     return dt, N * m * xs[0].itemsize
 
@@ -336,8 +356,28 @@ def cpu_baseline(wl: Workload, budget_s: float = 20.0):
     dt, payload = oracle_sample_ring(hosts, wl.N, wl.T, wl.codec_name, slices,
                                      DT_NAME[wl.in_dtype], DT_NAME[wl.out_dtype], extra, wl.ef)
     full = slices * 256 >= n
+    # the same sample on every host core: contiguous groups of slices, each an
+    # exact sub-problem, one oracle call per thread (the C oracle runs outside
+    # the interpreter lock)
+    threads = max(1, min(os.cpu_count() or 1, slices))
+    per = -(-slices // threads)
+    groups = [(g0, min(per, slices - g0)) for g0 in range(0, slices, per)]
+
+    def one(group):
+        return oracle_sample_ring(hosts, wl.N, wl.T, wl.codec_name, group[1],
+                                  DT_NAME[wl.in_dtype], DT_NAME[wl.out_dtype], extra, wl.ef,
+                                  first_slice=group[0])[1]
+
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=len(groups)) as ex:
+        t0 = time.perf_counter()
+        moved = sum(ex.map(one, groups))
+        dt_all = time.perf_counter() - t0
+    assert moved == payload
     return {"value": payload / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "seconds": dt,
+            "all_cores": {"value": payload / dt_all / 1e9, "cores": len(groups),
+                          "seconds": dt_all, "split": "contiguous slice groups, one thread each"},
             "sample": ("the full workload" if full else
                        f"first {slices} of {-(-n // 256)} 256-element slices of every chunk "
                        f"({slices * 256 * wl.N} of {wl.T} elements per rank; slices are "

@@ -202,6 +202,25 @@ rra_status rra_allgather(rra_comm *comm, void *const *buf, size_t count, rra_dty
                          void *stream);
 
 /*
+ * Compressed allgather, in place ([cccl] §2.1, the operator-aware layer:
+ * allgather and broadcast take lossless compression or a higher-precision
+ * lossy one; §3.3: low-precision compression for all_gather once all_reduce
+ * runs compressed).  On entry chunk r of buf[r] (dtype f32, f16 or bf16) is
+ * rank r's contribution.  Its owner encodes it once -- BFP (codec->bits 8
+ * or 4, lossy) or sparse values + indices (codec->sparsity_threshold;
+ * lossless) -- the codes travel the ring of the allgather pass unchanged
+ * (N-1 steps), and every rank, the owner included, stores the decoded chunk
+ * in dtype (round to nearest even), so all buffers end identical.  Sparse
+ * codes restore every element bit for bit.  Byte counters: the messages
+ * each rank forwards (all chunks but chunk r+1) and receives.
+ * codec NULL or RRA_CODEC_NONE: rra_allgather (a plain copy).
+ * Errors: RRA_ERR_INVALID (as rra_allgather; diff_prev, diff_base, average
+ * or residual set; a bad codec), RRA_ERR_CUDA.
+ */
+rra_status rra_allgather_codec(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,
+                               const rra_codec *codec, void *stream);
+
+/*
  * Broadcast from rank "root" over a binomial tree of depth ceil(log2 N)
  * ([ring] table: T bytes per receiving rank, log2(N) tree).  At level
  * k = 0..ceil(log2 N)-1 every relative rank q < 2^k with q + 2^k < N sends

@@ -71,6 +71,7 @@ def lib():
         L.rra_ring_allreduce.argtypes = [vp, vp, vp, sz, i32, i32, vp, vp]
         L.rra_reduce_scatter.argtypes = [vp, vp, vp, sz, i32, i32, vp, vp]
         L.rra_allgather.argtypes = [vp, vp, sz, i32, vp]
+        L.rra_allgather_codec.argtypes = [vp, vp, sz, i32, vp, vp]
         L.rra_broadcast.argtypes = [vp, vp, sz, i32, i32, vp]
         L.rra_tree_allreduce.argtypes = [vp, vp, sz, i32, vp]
         L.rra_bfp_encode.argtypes = [vp, sz, i32, i32, vp, vp, vp]
@@ -95,7 +96,8 @@ def lib():
         L.rra_status_string.argtypes = [i32]
         L.rra_status_string.restype = C.c_char_p
         for name in ("rra_comm_create", "rra_comm_destroy", "rra_ring_allreduce",
-                     "rra_reduce_scatter", "rra_allgather", "rra_broadcast", "rra_tree_allreduce",
+                     "rra_reduce_scatter", "rra_allgather", "rra_allgather_codec", "rra_broadcast",
+                     "rra_tree_allreduce",
                      "rra_bfp_encode", "rra_bfp_decode", "rra_sparse_encode", "rra_sparse_decode",
                      "rra_diff_encode", "rra_get_bytes", "rra_comm_status", "rra_set_timeout",
                      "rra_debug_withhold", "rra_comm_set_tuning", "rra_comm_last_shape",
@@ -210,9 +212,19 @@ class Comm:
     def reduce_scatter(self, inputs, outputs, codec: Optional[Codec] = None, stream=None):
         self._reduce(lib().rra_reduce_scatter, "rra_reduce_scatter", inputs, outputs, codec, stream)
 
-    def allgather(self, bufs, stream=None):
-        _check(lib().rra_allgather(self._h, _ptrs(bufs, "bufs"), bufs[0].numel(),
-                                   _dtype_code(bufs[0].dtype), _stream(stream)), "rra_allgather")
+    def allgather(self, bufs, codec: Optional[Codec] = None, stream=None):
+        """In-place allgather; with a BFP or sparse codec every chunk travels
+        as its owner's codes and every rank stores the decoded chunk."""
+        if codec is None:
+            _check(lib().rra_allgather(self._h, _ptrs(bufs, "bufs"), bufs[0].numel(),
+                                       _dtype_code(bufs[0].dtype), _stream(stream)),
+                   "rra_allgather")
+            return
+        c, keep = codec._marshal()
+        _check(lib().rra_allgather_codec(self._h, _ptrs(bufs, "bufs"), bufs[0].numel(),
+                                         _dtype_code(bufs[0].dtype), C.byref(c),
+                                         _stream(stream)), "rra_allgather_codec")
+        del keep
 
     def broadcast(self, bufs, root: int = 0, stream=None):
         _check(lib().rra_broadcast(self._h, _ptrs(bufs, "bufs"), bufs[0].numel(),

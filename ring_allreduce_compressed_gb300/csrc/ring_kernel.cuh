@@ -28,6 +28,9 @@
 //   g = N+1..2N-2  allgather step g-N+1: receive codes of chunk c, output
 //                  their decoded value, forward the same codes.
 //   g = 2N-1       receive the last chunk (c = r+1), output, no send.
+// The allgather alone (compressed allgather) skips steps 1..N-1: at g = N the
+// owner encodes its own input chunk r, outputs its decoded value and sends
+// the codes, and steps N+1..2N-1 run as above.
 // Input slices are staged into shared memory with one-dimensional bulk async
 // copies (cp.async.bulk + mbarrier transaction counts), D loads ahead per
 // rank, on the fast path (16-byte aligned buffers and chunk sizes); the
@@ -457,6 +460,8 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     __syncthreads();
 
     const bool allred = a.mode == kModeAllreduce;
+    const bool agonly = a.mode == kModeAllgather; // the allgather pass alone
+    const bool gather = allred || agonly;         // an allgather pass follows the owner
     const long long n = a.n, T = a.T;
     const int rstride = ONE ? N : W; // rank loop stride: one iteration when ONE
     unsigned long long my_sent = 0, my_recv = 0; // ONE: this warp's rank's bytes
@@ -478,7 +483,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     // (slice iteration, step 1..N), so one cursor gives the next load to
     // issue for every rank; "inflight" counts loads issued and not consumed.
     int cur_item = blockIdx.x; // slice position of the next load to issue
-    int cur_g = 1;             // its step
+    int cur_g = agonly ? N : 1; // its step (the allgather alone loads at the owner step only)
     // that slice position is full in every chunk
     bool cur_full = (long long)cur_item * TW + TW <= min_len;
     int inflight = 0;          // loads issued and not yet consumed, per rank
@@ -517,7 +522,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     };
     auto cursor_next = [&]() {
         if (++cur_g > N) {
-            cur_g = 1;
+            cur_g = agonly ? N : 1;
             cur_item += gridDim.x;
             cur_full = (long long)cur_item * TW + TW <= min_len;
         }
@@ -707,7 +712,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                          : 0;
 
         // ---- reduce-scatter steps g = 1..N-1: send chunk (r-g) mod N
-        for (int g = 1; ok && g < N; ++g) {
+        for (int g = 1; ok && !agonly && g < N; ++g) {
             for (int r = warp; ONE || r < N; r += rstride) {
                 int c = r - g;
                 c += c < 0 ? N : 0;
@@ -783,7 +788,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
         for (int r = warp; ONE || r < N; r += rstride) {
             const int V = slice_len(r, t0, item_full);
             const int dst = r + 1 == N ? 0 : r + 1;
-            const bool recv = N > 1, send = allred && N > 1;
+            const bool recv = N > 1 && !agonly, send = gather && N > 1;
             const bool pre = all_ready(true, recv, send, r, dst);
             if (!pre && FAST &&
                 !wait_ready(sbar + r * D + stg.slot, (uint32_t)stg.phase, a.timeout_ns,
@@ -819,7 +824,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                 // codes and write fp16 straight from them (a rolled loop: the
                 // unrolled one measured slower, its code too large for the
                 // instruction cache next to the unrolled loops)
-                if (direct16 && send && V == TW) {
+                if (direct16 && send && recv && V == TW) {
                     uint4 *op = reinterpret_cast<uint4 *>(
                                     reinterpret_cast<__half *>(a.out[r]) + (long long)r * n + t0) +
                                 lane;
@@ -863,7 +868,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     }
                     C::decode_add(m, v, lane, scratch);
                 }
-                if (allred) {
+                if (gather) {
                     if constexpr (EF)
                         encode_ef(r, r, V, gi, v, dslot);
                     else
@@ -880,13 +885,13 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
         if (!ok)
             break;
         stage_step();
-        if (N > 1)
+        if (N > 1 && !agonly)
             rcv.advance(K);
-        if (allred && N > 1)
+        if (gather && N > 1)
             snd.advance(K);
 
         // ---- allgather steps g = N+1..2N-1: output chunk (r-g) mod N, forward its codes
-        if (allred) {
+        if (gather) {
             for (int g = N + 1; ok && g <= 2 * N - 1; ++g) {
                 const bool fwd = g < 2 * N - 1;
                 for (int r = warp; ONE || r < N; r += rstride) {

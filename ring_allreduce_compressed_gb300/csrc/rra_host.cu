@@ -275,13 +275,14 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     const bool ef = cd.residual != nullptr;
     if (ef && kc != kCodecBfp8 && kc != kCodecBfp4)
         return RRA_ERR_UNSUPPORTED;
-    // Region of out[r] the call writes: all of it for the allreduce, chunk r
-    // alone for the reduce-scatter (so its outputs may share one buffer).
+    // Region of out[r] the call writes: all of it for the allreduce and the
+    // allgather, chunk r alone for the reduce-scatter (so its outputs may
+    // share one buffer).
     const size_t oes = esize(out_t);
     const size_t nchunk = (count + N - 1) / N;
     auto region = [&](int r, const char **p, size_t *bytes) {
         const char *b = static_cast<const char *>(out[r]);
-        if (mode == kModeAllreduce) {
+        if (mode != kModeReduceScatter) {
             *p = b;
             *bytes = count * oes;
             return;
@@ -617,6 +618,22 @@ rra_status rra_allgather(rra_comm *comm, void *const *buf, size_t count, rra_dty
                          void *stream)
 {
     return copy_common(comm, 0, buf, count, dtype, 0, stream);
+}
+
+rra_status rra_allgather_codec(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,
+                               const rra_codec *codec, void *stream)
+{
+    if (!codec || codec->kind == RRA_CODEC_NONE) {
+        if (codec && (codec->diff_prev || codec->diff_base || codec->average || codec->residual))
+            return RRA_ERR_INVALID;
+        return rra_allgather(comm, buf, count, dtype, stream);
+    }
+    // the allgather moves each owner's own elements: no difference stream,
+    // base, averaging or residual applies
+    if (codec->diff_prev || codec->diff_base || codec->average || codec->residual)
+        return RRA_ERR_INVALID;
+    return ring_common(comm, kModeAllgather, reinterpret_cast<const void *const *>(buf), buf,
+                       count, dtype, dtype, codec, stream);
 }
 
 rra_status rra_broadcast(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,

@@ -12,7 +12,7 @@ constexpr int kMaxRanks = 64;
 constexpr int kMaxWarps = 16; // warps per block; ranks per warp = ceil(N / warps)
 
 enum Codec { kCodecNone = 0, kCodecBfp8 = 1, kCodecBfp4 = 2, kCodecSparse = 3 };
-enum Mode { kModeAllreduce = 0, kModeReduceScatter = 1 };
+enum Mode { kModeAllreduce = 0, kModeReduceScatter = 1, kModeAllgather = 2 };
 
 // Launch shape of a ring kernel: blocks per SM, mailbox slots per edge,
 // staging depth, 256-element groups per slice.  Zero fields: automatic.
@@ -27,7 +27,7 @@ enum RankMap { kRanksShared = 0, kRankPerWarp8 = 1, kRankPerWarp16 = 2 };
 // allgather pass).  Passed by value as a __grid_constant__ parameter.
 struct RingArgs {
     int N;          // simulated ranks
-    int mode;       // kModeAllreduce / kModeReduceScatter
+    int mode;       // kModeAllreduce / kModeReduceScatter / kModeAllgather
     int in_t;       // dtype of the inputs
     int out_t;      // dtype of the outputs
     int K;          // mailbox depth (messages in flight per ring edge)

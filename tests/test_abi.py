@@ -72,6 +72,11 @@ def test_host_side_argument_checks(lib):
     assert L.rra_codec_measure(None, None, 10, 0, None, None) == rra.RRA_ERR_INVALID
     assert L.rra_codec_advise(None, None, 10, 0, C.c_float(0.5), C.c_float(0.01), None, None,
                               None) == rra.RRA_ERR_INVALID
+    assert L.rra_allgather_codec(None, None, 10, 0, None, None) == rra.RRA_ERR_INVALID
+    bfp, keep = rra.Codec("bfp", bits=8)._marshal()
+    assert L.rra_allgather_codec(None, None, 10, 0, C.byref(bfp), None) == rra.RRA_ERR_INVALID
+    avg, keep2 = rra.Codec("bfp", bits=8, average=True)._marshal()
+    assert L.rra_allgather_codec(None, None, 10, 0, C.byref(avg), None) == rra.RRA_ERR_INVALID
 
 
 def test_header_constants_match_the_binding():

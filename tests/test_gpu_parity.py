@@ -321,6 +321,103 @@ def test_allgather(dt, N, T):
     comm.close()
 
 
+def _allgather_inputs(N, T, dt, codec, seed):
+    xs = rand_f32(N, T, seed=seed, scale=1e-2)
+    if codec == "sparse":  # mostly +0.0, with some -0.0 kept as values
+        g = torch.Generator(device="cuda")
+        g.manual_seed(seed + 1)
+        keep = torch.rand(N, T, generator=g, device="cuda") < 0.3
+        xs = [torch.where(keep[r], x, torch.zeros_like(x)) for r, x in enumerate(xs)]
+        for x in xs:
+            x[5::211] = -0.0
+    return cast(xs, dt)
+
+
+@pytest.mark.parametrize("codec,bits", [("bfp", 8), ("bfp", 4), ("sparse", 8)])
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N,T", [(1, 300), (2, 512), (3, 1000), (8, 8 * 2048 * 5 + 8 * 24),
+                                 (5, 256 * 5 * 3 + 70), (16, 16 * 1024 * 3)])
+def test_allgather_codec(codec, bits, dt, N, T):
+    """Compressed allgather: every buffer holds every owner's decoded chunk,
+    bit for bit as the oracle; byte counters exact (full slices, a ragged
+    tail, chunk sizes that are and are not 16-byte multiples)."""
+    bufs = _allgather_inputs(N, T, dt, codec, seed=N * 101 + T + bits)
+    ref, s, r = O.allgather_codec([host(b) for b in bufs], dt, codec, bits)
+    comm = rra.Comm(N, T, bufs[0].dtype)
+    c = rra.Codec("bfp", bits=bits) if codec == "bfp" else rra.Codec("sparse", sparsity_threshold=0.5)
+    comm.allgather(bufs, codec=c)
+    assert comm.status() == rra.RRA_OK
+    for q in range(N):
+        assert_bits_equal(host(bufs[q]), ref[q], f"allgather {codec}{bits} {dt} rank {q}")
+    assert comm.get_bytes() == (list(s), list(r))
+    comm.close()
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_allgather_codec_launch_shapes(G):
+    """Every slice width gives the same bits (fp16 BFP8: the direct fp16 path
+    on full slices, the fp32 decode on the ragged tail)."""
+    N, T = 8, 8 * 2048 * 7 + 8 * 56
+    bufs = _allgather_inputs(N, T, "f16", "bfp", seed=G)
+    ref, s, r = O.allgather_codec([host(b) for b in bufs], "f16", "bfp", 8)
+    comm = rra.Comm(N, T, torch.float16)
+    comm.set_tuning(0, 0, 0, G)
+    comm.allgather(bufs, codec=rra.Codec("bfp", bits=8))
+    assert comm.status() == rra.RRA_OK and comm.last_shape()[3] == G
+    for q in range(N):
+        assert_bits_equal(host(bufs[q]), ref[q], f"G={G} rank {q}")
+    assert comm.get_bytes() == (list(s), list(r))
+    comm.close()
+
+
+def test_sparse_allgather_equals_the_plain_allgather():
+    """Sparse codes restore every element: the same bits as the uncompressed
+    allgather, including -0.0, with fewer bytes on the wire for fp32."""
+    N, T = 8, 8 * 4096
+    bufs = _allgather_inputs(N, T, "f32", "sparse", seed=3)
+    plain = [b.clone() for b in bufs]
+    comm = rra.Comm(N, T)
+    comm.allgather(plain)
+    _, plain_bytes = comm.get_bytes()
+    comm.allgather(bufs, codec=rra.Codec("sparse", sparsity_threshold=0.5))
+    _, sparse_bytes = comm.get_bytes()
+    for q in range(N):
+        assert_bits_equal(host(bufs[q]), host(plain[q]), f"rank {q}")
+    assert all(a < b for a, b in zip(sparse_bytes, plain_bytes))
+    comm.close()
+
+
+def test_allgather_codec_after_allreduce_on_one_comm():
+    """The allreduce, the compressed allgather and the allreduce again on one
+    communicator: each keeps its own launch-shape key and result."""
+    N, T = 4, 4 * 2048 * 3
+    xs = rand_f32(N, T, seed=8)
+    codec = rra.Codec("bfp", bits=8)
+    comm = rra.Comm(N, T)
+    outs = [torch.zeros(T, device="cuda") for _ in range(N)]
+    ref_ar = oracle_ring(xs, "f32", "f32", codec="bfp", bits=8)[0]
+    comm.ring_allreduce(xs, outs, codec)
+    bufs = [x.clone() for x in xs]
+    ref_ag = O.allgather_codec([host(b) for b in bufs], "f32", "bfp", 8)[0]
+    comm.allgather(bufs, codec=codec)
+    comm.ring_allreduce(xs, outs, codec)
+    assert comm.status() == rra.RRA_OK
+    for q in range(N):
+        assert_bits_equal(host(outs[q]), ref_ar[q], f"allreduce {q}")
+        assert_bits_equal(host(bufs[q]), ref_ag[q], f"allgather {q}")
+    comm.close()
+
+
+def test_allgather_codec_argument_errors():
+    N, T = 4, 1024
+    comm = rra.Comm(N, T)
+    bufs = rand_f32(N, T, seed=1)
+    for bad in (rra.Codec("bfp", bits=8, average=True), rra.Codec("bfp", bits=5)):
+        with pytest.raises(RuntimeError):
+            comm.allgather(bufs, codec=bad)
+    comm.close()
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("N", [1, 2, 3, 5, 8, 13, 64])
 @pytest.mark.parametrize("root", [0, 2])

@@ -25,6 +25,8 @@ CONFIGS = {
     "bfp8_bucket": dict(N=8, T=13_107_200, dtype="f16", seed=1),
     "sparse_n16": dict(N=16, T=64 * 2 ** 20, dtype="bf16", seed=2),
     "diloco_n8": dict(N=8, T=10 ** 9, dtype="f32", seed=3),
+    # the bucket's tensors as parameters gathered compressed (allgather alone)
+    "bfp8_allgather": dict(N=8, T=13_107_200, dtype="f16", seed=1),
 }
 SWEEP_N = (2, 4, 8, 16, 64)
 SWEEP_T = tuple(256 * 4 ** k for k in range(11))  # 1 KiB .. 1 GiB of fp32
