@@ -77,6 +77,8 @@ def lib():
             L.oracle_codec_stats.argtypes = [i32, sz, vp, i32, u64p]
             L.oracle_codec_stats.restype = i32
             L.oracle_broadcast.argtypes = [i32, sz, vp, i32, i32, u64p, u64p]
+            L.oracle_broadcast_codec.argtypes = [i32, sz, vp, i32, i32, i32, u64p, u64p]
+            L.oracle_broadcast_codec.restype = i32
             L.oracle_tree_allreduce.argtypes = [i32, sz, vp, u64p, u64p]
             for f in (L.oracle_allgather, L.oracle_broadcast, L.oracle_tree_allreduce):
                 f.restype = i32
@@ -212,6 +214,18 @@ def broadcast(bufs, dtype="f32", root=0):
     sent, recv = _counters(N)
     if lib().oracle_broadcast(N, T, _ptrs(bufs), DTYPES[dtype], root, sent, recv) != 0:
         raise ValueError("oracle_broadcast: bad arguments")
+    return bufs, np.array(sent[:], np.uint64), np.array(recv[:], np.uint64)
+
+
+def broadcast_codec(bufs, dtype="f32", root=0, bits=8):
+    """In-place BFP-compressed broadcast (reading AB): every buffer ends with
+    the decoded codes of the root's buffer."""
+    N, T = len(bufs), bufs[0].size
+    _check(bufs, T, dtype)
+    sent, recv = _counters(N)
+    if lib().oracle_broadcast_codec(N, T, _ptrs(bufs), DTYPES[dtype], root, bits, sent,
+                                    recv) != 0:
+        raise ValueError("oracle_broadcast_codec: bad arguments")
     return bufs, np.array(sent[:], np.uint64), np.array(recv[:], np.uint64)
 
 

@@ -60,6 +60,11 @@
  *      R1 forward those codes unchanged; every rank, the owner included,
  *      stores decode(codes) in the buffer's dtype (RNE), so all buffers end
  *      identical.  Sparse codes restore every element exactly.
+ *  AB  compressed broadcast (the same layer of [P4] §2.1 and §3.3), BFP:
+ *      the root encodes its whole buffer (widened to fp32) once, as one
+ *      message with blocks of 128 from the buffer start; every edge of the
+ *      binomial tree carries those codes unchanged; every rank, the root
+ *      included, stores decode(codes) in the buffer's dtype (RNE).
  *  EF  error feedback ([P4] §5, future directions), BFP only: each rank
  *      keeps an fp32 residual e_r[T]; whatever value v it encodes (its
  *      reduce-scatter messages, and as owner its chunk's full sum) is encoded
@@ -804,6 +809,44 @@ int oracle_broadcast(int N, size_t T, void *const *buf, int t, int root, uint64_
             recv[dst] += T * es;
         }
     }
+    return 0;
+}
+
+/* Compressed broadcast (reading AB): the root's codes travel the binomial
+ * tree above; every rank, the root included, stores the decoded buffer.
+ * BFP only (bits 8 or 4); every edge carries the whole message. */
+int oracle_broadcast_codec(int N, size_t T, void *const *buf, int t, int root, int bits,
+                           uint64_t *sent, uint64_t *recv)
+{
+    if (N < 1 || root < 0 || root >= N || (bits != 8 && bits != 4))
+        return -1;
+    codec_t cd = {OR_CODEC_BFP, bits, 0.0, 0};
+    for (int r = 0; r < N; r++)
+        sent[r] = recv[r] = 0;
+    float *x = malloc((T ? T : 1) * sizeof(float));
+    for (size_t i = 0; i < T; i++)
+        x[i] = load_as_f32(buf[root], i, t);
+    message m;
+    memset(&m, 0, sizeof m);
+    msg_encode(&m, &cd, x, T);
+    int L = ceil_log2(N);
+    for (int k = 0; k < L; k++) {
+        for (int q = 0; q < (1 << k); q++) {
+            int qd = q + (1 << k);
+            if (qd >= N)
+                continue;
+            sent[(q + root) % N] += m.bytes;
+            recv[(qd + root) % N] += m.bytes;
+        }
+    }
+    for (int r = 0; r < N; r++)
+        for (size_t i = 0; i < T; i++) {
+            int there;
+            float v = msg_value(&m, &cd, i, &there);
+            store_from_f32(buf[r], i, t, there ? v : 0.0f);
+        }
+    msg_free(&m);
+    free(x);
     return 0;
 }
 

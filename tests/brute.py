@@ -187,6 +187,21 @@ def broadcast(bufs, root, elem_bytes):
     return bufs, sent, recv
 
 
+def broadcast_codec(bufs, root, bits):
+    """BFP-compressed broadcast of N lists of float32 scalars: the root's
+    buffer is encoded once (blocks from its start), every tree edge carries
+    the codes, every rank holds the decoded buffer."""
+    N, T = len(bufs), len(bufs[0])
+    out, nb = bfp_roundtrip([F(v) for v in bufs[root]], bits)
+    sent, recv = [0] * N, [0] * N
+    for k in range(ceil_log2(N)):
+        for q in range(1 << k):
+            if q + (1 << k) < N:
+                sent[(q + root) % N] += nb
+                recv[(q + (1 << k) + root) % N] += nb
+    return [list(out) for _ in range(N)], sent, recv
+
+
 def tree_allreduce(bufs):
     N, T = len(bufs), len(bufs[0])
     acc = [[F(v) for v in b] for b in bufs]

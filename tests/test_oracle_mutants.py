@@ -4,7 +4,8 @@ index, wrong mantissa scale, ties away from zero, off-by-one exponent, wrong
 clamp, wrong threshold tie, wrong header size, reversed tree levels, swapped
 difference, wrong subnormal scaling in the fp16 conversion, error-feedback sign,
 owner without error feedback, flush tie in the codec statistics, wrong chunk or an
-owner that keeps its input in the compressed allgather); the mutated copy
+owner that keeps its input in the compressed allgather, a root that keeps its input
+in the compressed broadcast); the mutated copy
 is compiled into a temporary directory and the pin suite is run against it in
 a child process.  The real oracle is never modified."""
 import os
@@ -36,6 +37,8 @@ MUTANTS = {
     "ef_owner_skipped": ("            if (resid)\n                msg_encode_ef(&held[r]",
                          "            if (0)\n                msg_encode_ef(&held[r]", 1),
     "agc_recv_index": ("int c = mod((long)r - s, N);", "int c = mod((long)r - s + 1, N);", 4),
+    "bcc_root_keeps_input": ("    for (int r = 0; r < N; r++)\n        for (size_t i = 0; i < T; i++) {\n            int there;",
+                             "    for (int r = 0; r < N; r++)\n        for (size_t i = 0; i < T * (r != root); i++) {\n            int there;", 1),
     "agc_owner_keeps_input": ("/* the owner's own chunk becomes the decoded codes as well */\n    for (int r = 0; r < N; r++) {",
                               "/* the owner's own chunk becomes the decoded codes as well */\n    for (int r = 0; r < 0; r++) {", 1),
 }

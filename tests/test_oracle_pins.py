@@ -282,6 +282,40 @@ def test_sparse_allgather_is_an_exact_copy(dt):
     assert all(int(x) < 4 * n * (N - 1) for x in sent)
 
 
+# Reading AB: the root's BFP codes travel the binomial tree unchanged.
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("N,root", [(1, 0), (2, 1), (3, 0), (5, 2), (4, 3)])
+@pytest.mark.parametrize("T", [1, 37, 64, 130])
+def test_broadcast_codec_brute_force(bits, N, root, T):
+    rng = np.random.default_rng(N * 7 + root + T)
+    xs = [rng.standard_normal(T).astype(np.float32) for _ in range(N)]
+    out, sent, recv = O.broadcast_codec([x.copy() for x in xs], "f32", root, bits)
+    ref, bs, br = brute.broadcast_codec([list(x) for x in xs], root, bits)
+    for r in range(N):
+        assert np.array_equal(out[r].view(np.uint32), np.array(ref[r], np.float32).view(np.uint32))
+    assert list(sent) == bs and list(recv) == br
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_broadcast_codec_is_the_codec_round_trip_everywhere(bits, dt):
+    """Every buffer, the root's included, holds the standalone codec's round
+    trip of the root's buffer in its dtype; the root sends ceil(log2 N)
+    messages of the codec's size, every other rank receives one."""
+    N, T, root = 8, 1000, 3
+    rng = np.random.default_rng(bits)
+    bufs = [O.from_f32((rng.standard_normal(T) * 1e-3).astype(np.float32), dt) for _ in range(N)]
+    exps, mants = O.bfp_encode(O.to_f32(bufs[root], dt), bits)
+    want = O.from_f32(O.bfp_decode(exps, mants, T, bits), dt)
+    out, sent, recv = O.broadcast_codec([b.copy() for b in bufs], dt, root, bits)
+    msg = O.bfp_bytes(T, bits)
+    for r in range(N):
+        assert np.array_equal(out[r], want)
+    assert int(sent[root]) == 3 * msg and int(sum(sent)) == (N - 1) * msg
+    assert [int(x) for x in recv] == [0 if r == root else msg for r in range(N)]
+
+
 # --------------------------------------------------------------- broadcast / tree
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 13])
