@@ -45,7 +45,8 @@ import workloads as W  # noqa: E402
 
 METRIC = "compressed ring-allreduce algbw GB/s on 1 GB300 (N sim ranks), % of HBM peak"
 FALLBACK_HBM_GBS = 6800.0
-CONFIG_NAMES = ("bfp8_bucket", "lossless_n4", "sparse_n16", "diloco_n8", "bfp8_allgather")
+CONFIG_NAMES = ("bfp8_bucket", "lossless_n4", "sparse_n16", "diloco_n8", "bfp8_allgather",
+                "bfp8_broadcast")
 
 
 # ---------------------------------------------------------------- distributed
@@ -160,6 +161,7 @@ RING_KERNEL_SOURCES = {
     "diloco_n8": ("ring_bfp4.cu", "ring_bfp4_ef.cu"),
     "sparse_n16": ("ring_sparse.cu", "wire_sparse.cuh"),
     "bfp8_allgather": ("ring_bfp8.cu",),
+    "bfp8_broadcast": ("coll_kernels.cu",),
     "lossless_n4": ("ring_none.cu",),
 }
 
@@ -173,11 +175,16 @@ def kernel_sources_sha(config: str = "bfp8_bucket") -> str:
     return h.hexdigest()[:16]
 
 
+# the kernel each workload times (the ring kernel unless named here)
+KERNEL_OF = {"bfp8_broadcast": "broadcast_bfp_kernel"}
+
+
 def traffic_from_profile(config: str):
-    """DRAM bytes per launch of the ring kernel from the committed ncu summary
-    for this workload, or None when no summary exists or the kernel sources
+    """DRAM bytes per launch of the workload's kernel from the committed ncu
+    summary for it, or None when no summary exists or the kernel sources
     changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"ring_kernel_{config}.md")
+    kernel = KERNEL_OF.get(config, "ring_kernel")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{config}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -226,6 +233,15 @@ class Workload:
                          "each owner encodes its chunk once, every rank stores the decoded "
                          "chunks.  Decoding then re-encoding gives the same codes, so every "
                          "step does the same work on the buffers the previous step left")
+        elif name == "bfp8_broadcast":
+            self.inputs = W.bfp_bucket(self.N, self.T, seed=c["seed"], device=device)
+            self.out_dtype = torch.float16
+            self.codec_name = "bfp8-broadcast"
+            self.desc = ("block-FP8 compressed broadcast from rank 0 over the binomial tree, in "
+                         "place: N=8 simulated ranks x 13,107,200 fp16, N(0,1e-3^2) seed 1; the "
+                         "root encodes once, every rank stores the decoded buffer.  Decoding "
+                         "then re-encoding gives the same codes, so every step does the same "
+                         "work")
         elif name == "lossless_n4":
             self.inputs = W.lossless(self.N, self.T, seed=c["seed"], device=device)
             self.out_dtype = torch.float32
@@ -257,7 +273,7 @@ class Workload:
             self.desc += "; with error feedback (an fp32 residual per rank, read and written)"
         if use_lib:
             self.comm = rra.Comm(self.N, self.T, self.in_dtype)
-            if name in ("bfp8_bucket", "bfp8_allgather"):
+            if name in ("bfp8_bucket", "bfp8_allgather", "bfp8_broadcast"):
                 self.codec = rra.Codec("bfp", bits=8)
             elif name == "sparse_n16":
                 self.codec = rra.Codec("sparse", sparsity_threshold=0.5)
@@ -285,10 +301,15 @@ class Workload:
         if name == "bfp8_allgather":  # each rank reads its own chunk, writes its buffer
             n = -(-self.T // self.N)
             self.compulsory = self.N * (n * ies + self.T * oes)
+        if name == "bfp8_broadcast":  # the root reads its buffer, every rank writes its own
+            self.compulsory = self.T * ies + self.N * self.T * oes
 
     def step(self, stream=None):
         if self.name == "bfp8_allgather":
             self.comm.allgather(self.inputs, self.codec, stream=stream)
+            return
+        if self.name == "bfp8_broadcast":
+            self.comm.broadcast(self.inputs, 0, self.codec, stream=stream)
             return
         self.comm.ring_allreduce(self.inputs, self.outputs, self.codec, stream=stream)
 
@@ -324,6 +345,8 @@ def oracle_sample_ring(wl_host, N, T, codec_name, slices_per_chunk, in_dt, out_d
     t0 = time.perf_counter()
     if codec_name == "bfp8-allgather":
         O.allgather_codec(xs, in_dt, "bfp", 8)
+    elif codec_name == "bfp8-broadcast":
+        O.broadcast_codec(xs, in_dt, 0, 8)
     else:
         O.ring(xs, in_dt, out_dt, **kw)
     dt = time.perf_counter() - t0
@@ -514,7 +537,7 @@ def run_rra(args, world, rank, local):
         "bytes_sent_per_rank": sent[0],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "ring_kernel", "kernel_ms": kern_ms,
+                     "kernel": KERNEL_OF.get(args.config, "ring_kernel"), "kernel_ms": kern_ms,
                      "bytes_per_launch": wl.compulsory,
                      "bytes_model": "compulsory: N*T*(in+out) (+ diff prev and base)",
                      "peak_source": peak_src, "traffic_source": traffic_src},

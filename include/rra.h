@@ -232,6 +232,24 @@ rra_status rra_broadcast(rra_comm *comm, void *const *buf, size_t count, rra_dty
                          int root, void *stream);
 
 /*
+ * Compressed broadcast over the same binomial tree ([cccl] §2.1, the
+ * operator-aware layer: broadcast takes a higher-precision lossy
+ * compression; §3.3: low-precision compression for broadcast once
+ * all_reduce runs compressed).  The root encodes its buffer once as block
+ * floating point (codec->bits 8 or 4; 128-element blocks from the buffer
+ * start), every tree edge carries those codes unchanged, and every rank,
+ * the root included, stores the decoded buffer in dtype (round to nearest
+ * even), so all buffers end identical.  Byte counters: the message
+ * (ceil(count/128) exponent bytes + the codes) once per tree edge.
+ * codec NULL or RRA_CODEC_NONE: rra_broadcast (a plain copy).
+ * Errors: RRA_ERR_INVALID (as rra_broadcast; diff_prev, diff_base, average or
+ * residual set; bits other than 8 or 4), RRA_ERR_UNSUPPORTED (the sparse
+ * codec), RRA_ERR_CUDA.
+ */
+rra_status rra_broadcast_codec(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,
+                               int root, const rra_codec *codec, void *stream);
+
+/*
  * Tree allreduce ([ring] table: T log2 N bytes, 2 log2 N steps; "练习":
  * the tree variant for small messages).  Binomial reduce to rank 0 (at level
  * k every rank r with r mod 2^(k+1) = 0 and r + 2^k < N adds rank r+2^k's

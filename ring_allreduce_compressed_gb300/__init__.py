@@ -73,6 +73,7 @@ def lib():
         L.rra_allgather.argtypes = [vp, vp, sz, i32, vp]
         L.rra_allgather_codec.argtypes = [vp, vp, sz, i32, vp, vp]
         L.rra_broadcast.argtypes = [vp, vp, sz, i32, i32, vp]
+        L.rra_broadcast_codec.argtypes = [vp, vp, sz, i32, i32, vp, vp]
         L.rra_tree_allreduce.argtypes = [vp, vp, sz, i32, vp]
         L.rra_bfp_encode.argtypes = [vp, sz, i32, i32, vp, vp, vp]
         L.rra_bfp_decode.argtypes = [vp, vp, sz, i32, vp, i32, vp]
@@ -97,6 +98,7 @@ def lib():
         L.rra_status_string.restype = C.c_char_p
         for name in ("rra_comm_create", "rra_comm_destroy", "rra_ring_allreduce",
                      "rra_reduce_scatter", "rra_allgather", "rra_allgather_codec", "rra_broadcast",
+                     "rra_broadcast_codec",
                      "rra_tree_allreduce",
                      "rra_bfp_encode", "rra_bfp_decode", "rra_sparse_encode", "rra_sparse_decode",
                      "rra_diff_encode", "rra_get_bytes", "rra_comm_status", "rra_set_timeout",
@@ -226,10 +228,20 @@ class Comm:
                                          _stream(stream)), "rra_allgather_codec")
         del keep
 
-    def broadcast(self, bufs, root: int = 0, stream=None):
-        _check(lib().rra_broadcast(self._h, _ptrs(bufs, "bufs"), bufs[0].numel(),
-                                   _dtype_code(bufs[0].dtype), root, _stream(stream)),
-               "rra_broadcast")
+    def broadcast(self, bufs, root: int = 0, codec: Optional[Codec] = None, stream=None):
+        """In-place broadcast from root; with a BFP codec the root's codes
+        travel the tree and every rank (root included) stores the decoded
+        buffer."""
+        if codec is None:
+            _check(lib().rra_broadcast(self._h, _ptrs(bufs, "bufs"), bufs[0].numel(),
+                                       _dtype_code(bufs[0].dtype), root, _stream(stream)),
+                   "rra_broadcast")
+            return
+        c, keep = codec._marshal()
+        _check(lib().rra_broadcast_codec(self._h, _ptrs(bufs, "bufs"), bufs[0].numel(),
+                                         _dtype_code(bufs[0].dtype), root, C.byref(c),
+                                         _stream(stream)), "rra_broadcast_codec")
+        del keep
 
     def tree_allreduce(self, bufs, stream=None):
         _check(lib().rra_tree_allreduce(self._h, _ptrs(bufs, "bufs"), bufs[0].numel(),

@@ -26,6 +26,12 @@
 // per slice position, one per step.  Within a level, a warp does all of its
 // ranks' sends before any of their receives, so a warp that plays both ends
 // of an edge (N > 16) never waits on itself.
+//  broadcast   (BFP) the same tree carrying the root's block-floating-point
+//              codes: the root encodes each slice once into its own slot
+//              (its edge has no sender) and stores the decoded values in its
+//              buffer; forwarders copy codes slot to slot; receivers store
+//              the decoded values.
+#include "ring_kernel.cuh" // BfpGroup: the BFP arithmetic of the ring
 #include "rra_device.cuh"
 #include "rra_kernels.h"
 
@@ -478,6 +484,237 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) broadcast_kernel(const __gr
     by.flush(s, a, warp, W);
 }
 
+// ---------------------------------------------------------------- BFP broadcast
+// Message of one slice in a slot: 16 exponent bytes (byte b: block b), then
+// the codes of group gi at 16 + gi * 256*BITS/8, lane L at 8L (BITS 8) or 4L
+// (BITS 4) bytes within the group -- the layout of the ring's BFP messages.
+template <int BITS> struct BfpSlot {
+    static constexpr int kMB = kTile * BITS / 8;
+    __device__ __forceinline__ static void put(unsigned char *slot, int gi, int lane, int e,
+                                               const uint32_t w[2])
+    {
+        if ((lane & 15) == 0)
+            slot[2 * gi + (lane >> 4)] = (unsigned char)(int8_t)e;
+        if constexpr (BITS == 8)
+            reinterpret_cast<uint2 *>(slot + 16 + gi * kMB)[lane] = make_uint2(w[0], w[1]);
+        else
+            reinterpret_cast<uint32_t *>(slot + 16 + gi * kMB)[lane] = w[0];
+    }
+    __device__ __forceinline__ static void get(const unsigned char *slot, int gi, int lane, int &e,
+                                               uint32_t w[2])
+    {
+        e = (int)(int8_t)slot[2 * gi + (lane >> 4)];
+        if constexpr (BITS == 8) {
+            const uint2 u = reinterpret_cast<const uint2 *>(slot + 16 + gi * kMB)[lane];
+            w[0] = u.x;
+            w[1] = u.y;
+        } else {
+            w[0] = reinterpret_cast<const uint32_t *>(slot + 16 + gi * kMB)[lane];
+            w[1] = 0;
+        }
+    }
+};
+
+// 8 elements of dtype dt at p widened to fp32; the first `valid` are read,
+// the rest are +0.0 (vec: 16-byte aligned, all 8 present)
+__device__ __forceinline__ void load8_dt(const void *p, int dt, int valid, bool vec, float v[8])
+{
+    if (dt == kF32) {
+        if (vec && valid == 8)
+            load8_vec<kF32>(p, v);
+        else
+            load8_scalar<kF32>(p, valid, v);
+    } else if (dt == kF16) {
+        if (vec && valid == 8)
+            load8_vec<kF16>(p, v);
+        else
+            load8_scalar<kF16>(p, valid, v);
+    } else {
+        if (vec && valid == 8)
+            load8_vec<kBF16>(p, v);
+        else
+            load8_scalar<kBF16>(p, valid, v);
+    }
+}
+
+template <int BITS, bool FAST, int G, bool ONE>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1)
+    broadcast_bfp_kernel(const __grid_constant__ CopyArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    using BG = BfpGroup<BITS>;
+    using SL = BfpSlot<BITS>;
+    constexpr int TW = kTile * G;
+    const int N = a.N, W = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int K = a.K, D = a.D, dt = a.dt, es = a.es;
+    const CollSmem s = coll_carve(smem, a, N, 1, FAST);
+    coll_init(s, a, N, 1, FAST);
+    const long long T = a.T;
+    const int rstride = ONE ? N : W;
+    const int tiles = (int)a.tiles;
+    const int root = a.root;
+    int L = 0;
+    while ((1 << L) < N)
+        ++L;
+    auto last_send = [&](int q) -> int { // last level at which q forwards (-1: never)
+        const int k0 = q > 0 ? 32 - __clz(q) : 0;
+        int last = -1;
+        for (int k = k0; k < L; ++k)
+            if (q + (1 << k) < N)
+                last = k;
+        return last;
+    };
+    const bool root_warp = root % W == warp;
+    int cur_item = blockIdx.x, inflight = 0;
+    auto issue = [&](int d) { // lane 0 of the root's warp
+        const long long t0 = (long long)cur_item * TW;
+        const uint32_t bytes = (uint32_t)clamp_len(T - t0, TW) * es;
+        uint64_t *bar = s.sbar + d;
+        if (bytes == 0) {
+            mbar_arrive(bar);
+            return;
+        }
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(s.stages + (size_t)d * a.stage_bytes,
+                 reinterpret_cast<const char *>(a.buf[root]) + t0 * es, bytes, bar);
+    };
+    if constexpr (FAST) {
+        while (inflight < D && cur_item < tiles) {
+            if (lane == 0 && root_warp)
+                issue(inflight);
+            ++inflight;
+            cur_item += gridDim.x;
+        }
+        __syncwarp();
+    }
+    Bytes<ONE> by;
+    Fifo e{0, 0}, stg{0, 0};
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < tiles; item += gridDim.x) {
+        const long long t0 = (long long)item * TW;
+        const bool first = item == (int)blockIdx.x;
+        const int V = clamp_len(T - t0, TW);
+        const unsigned long long mb = bfp_msg_bytes(V, BITS);
+        // the root encodes the slice into its own slot and stores its decoded values
+        if (root_warp) {
+            if (FAST &&
+                !(ok = wait_ready(s.sbar + stg.slot, (uint32_t)stg.phase, a.timeout_ns, a.status)))
+                break;
+            const unsigned char *src =
+                FAST ? s.stages + (size_t)stg.slot * a.stage_bytes
+                     : reinterpret_cast<const unsigned char *>(a.buf[root]) + t0 * es;
+            unsigned char *own = s.slots + (size_t)(root * K + e.slot) * a.slot_bytes;
+            char *mine = reinterpret_cast<char *>(a.buf[root]) + t0 * es;
+#pragma unroll 1
+            for (int gi = 0; gi < G; ++gi) {
+                if (gi * kTile >= V)
+                    break;
+                const int el = gi * kTile + 8 * lane;
+                const int vl = min(max(V - el, 0), 8);
+                float v[8];
+                load8_dt(src + (size_t)el * es, dt, vl, FAST, v); // +0.0 past the end
+                int ex;
+                uint32_t w[2];
+                BG::encode(v, ex, w);
+                SL::put(own, gi, lane, ex, w);
+                BG::decode(w, ex, v);
+                store8(mine + (size_t)el * es, dt, v, vl, FAST);
+            }
+            __syncwarp();
+        }
+        for (int k = 0; ok && k < L; ++k) {
+            // senders at level k: relative q < 2^k with q + 2^k < N
+            for (int r = warp; r < N; r += rstride) {
+                int q = r - root;
+                q += q < 0 ? N : 0;
+                if (!(q < (1 << k) && q + (1 << k) < N))
+                    continue;
+                int child = r + (1 << k);
+                child -= child >= N ? N : 0;
+                if (!(ok = wait_ready(s.empty + child * K + e.slot, (uint32_t)(e.phase ^ 1),
+                                      a.timeout_ns, a.status)))
+                    break;
+                const unsigned char *src = s.slots + (size_t)(r * K + e.slot) * a.slot_bytes;
+                unsigned char *dslot = s.slots + (size_t)(child * K + e.slot) * a.slot_bytes;
+#pragma unroll 1
+                for (int gi = 0; gi < G; ++gi) {
+                    if (gi * kTile >= V)
+                        break;
+                    int ex;
+                    uint32_t w[2];
+                    SL::get(src, gi, lane, ex, w);
+                    SL::put(dslot, gi, lane, ex, w);
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    if (!(first && r == a.withhold_rank && k + 1 == a.withhold_step))
+                        mbar_arrive(s.full + child * K + e.slot);
+                    by.add_sent(s, r, mb);
+                    if (q > 0 && k == last_send(q)) // done forwarding: free the slot
+                        mbar_arrive(s.empty + r * K + e.slot);
+                }
+            }
+            if (!ok)
+                break;
+            // receivers at level k: relative q in [2^k, 2^(k+1))
+            for (int r = warp; r < N; r += rstride) {
+                int q = r - root;
+                q += q < 0 ? N : 0;
+                if (!(q >= (1 << k) && q < (2 << k)))
+                    continue;
+                if (!(ok = wait_ready(s.full + r * K + e.slot, (uint32_t)e.phase, a.timeout_ns,
+                                      a.status)))
+                    break;
+                const unsigned char *rslot = s.slots + (size_t)(r * K + e.slot) * a.slot_bytes;
+                char *mine = reinterpret_cast<char *>(a.buf[r]) + t0 * es;
+#pragma unroll 1
+                for (int gi = 0; gi < G; ++gi) {
+                    if (gi * kTile >= V)
+                        break;
+                    const int el = gi * kTile + 8 * lane;
+                    int ex;
+                    uint32_t w[2];
+                    SL::get(rslot, gi, lane, ex, w);
+                    float v[8];
+                    BG::decode(w, ex, v);
+                    store8(mine + (size_t)el * es, dt, v, min(max(V - el, 0), 8), FAST);
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    by.add_recv(s, r, mb);
+                    if (last_send(q) < 0) // a leaf frees its slot at once
+                        mbar_arrive(s.empty + r * K + e.slot);
+                }
+            }
+        }
+        if (!ok)
+            break;
+        if (FAST) { // the root's stage is consumed: refill it
+            __syncwarp();
+            if (inflight == D && cur_item < tiles) {
+                if (lane == 0 && root_warp)
+                    issue(stg.slot);
+                cur_item += gridDim.x;
+            } else {
+                --inflight;
+            }
+            stg.advance(D);
+        }
+        e.advance(K);
+    }
+    if constexpr (FAST) {
+        __syncwarp();
+        if (root_warp) {
+            Fifo d = stg;
+            for (int i = 0; i < inflight; ++i) {
+                drain_phase(s.sbar + d.slot, (uint32_t)d.phase, a.timeout_ns);
+                d.advance(D);
+            }
+        }
+    }
+    by.flush(s, a, warp, W);
+}
+
 // ---------------------------------------------------------------- tree allreduce
 template <bool FAST, int G, bool ONE>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) tree_kernel(const __grid_constant__ CopyArgs a)
@@ -728,6 +965,28 @@ template <int ES> const void *coll_fn_es(int which, int groups, bool fast, bool 
 }
 
 } // namespace
+
+template <int BITS, int G> const void *bb_fn(bool fast, bool one)
+{
+    if (fast)
+        return one ? (const void *)broadcast_bfp_kernel<BITS, true, G, true>
+                   : (const void *)broadcast_bfp_kernel<BITS, true, G, false>;
+    return one ? (const void *)broadcast_bfp_kernel<BITS, false, G, true>
+               : (const void *)broadcast_bfp_kernel<BITS, false, G, false>;
+}
+
+const void *bcast_bfp_fn(int bits, int groups, bool fast, bool one)
+{
+    switch (bits * 10 + groups) {
+    case 81: return bb_fn<8, 1>(fast, one);
+    case 82: return bb_fn<8, 2>(fast, one);
+    case 84: return bb_fn<8, 4>(fast, one);
+    case 41: return bb_fn<4, 1>(fast, one);
+    case 42: return bb_fn<4, 2>(fast, one);
+    case 44: return bb_fn<4, 4>(fast, one);
+    default: return nullptr;
+    }
+}
 
 const void *coll_fn(int which, int es, int groups, bool fast, bool one)
 {

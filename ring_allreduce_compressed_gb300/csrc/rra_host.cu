@@ -415,8 +415,10 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     return e == cudaSuccess ? RRA_OK : RRA_ERR_CUDA;
 }
 
+// which: 0 allgather, 1 broadcast, 2 tree allreduce; bits 8 or 4: the
+// broadcast carries the root's BFP codes (0: plain copies)
 rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count,
-                       rra_dtype dtype, int root, void *stream)
+                       rra_dtype dtype, int root, void *stream, int bits = 0)
 {
     if (!comm || !buf || count == 0 || count > comm->max_count || !valid_dtype(dtype))
         return RRA_ERR_INVALID;
@@ -447,6 +449,8 @@ rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count
     a.status = comm->status;
     a.withhold_rank = comm->withhold_rank;
     a.withhold_step = comm->withhold_step;
+    a.bits = bits;
+    a.dt = (int)dtype;
     bool fast = (a.T * (long long)es) % 16 == 0 && (which != 0 || (a.n * (long long)es) % 16 == 0);
     for (int r = 0; r < N; ++r) {
         a.buf[r] = buf[r];
@@ -474,11 +478,12 @@ rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count
             if (!comm->tune.G && g > 1 && (range + (long long)kTile * g - 1) / ((long long)kTile * g) < sms)
                 continue;
             const int bytes = kTile * g * (int)es;
+            const int slot = bits ? 16 + kTile * g * bits / 8 : bytes; // BFP: codes
             bool found = false;
             for (int K = comm->tune.K ? comm->tune.K : 2; K >= (which == 0 ? 2 : 1) && !found; --K)
                 for (int D = fast ? (comm->tune.D ? comm->tune.D : 2) : 1; D >= 1 && !found; --D) {
                     const CollLayout L =
-                        coll_layout(N, edges, K, stagers, D, bytes, bytes, fast || which == 2);
+                        coll_layout(N, edges, K, stagers, D, slot, bytes, fast || which == 2);
                     if (per_sm * (L.total + 1024) <= comm->smem_per_sm &&
                         L.total <= comm->smem_optin) {
                         G = g;
@@ -495,11 +500,14 @@ rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count
     if (!G)
         return RRA_ERR_UNSUPPORTED;
     a.slot_bytes = a.stage_bytes = kTile * G * (int)es;
+    if (bits)
+        a.slot_bytes = 16 + kTile * G * bits / 8;
     a.tiles = (range + (long long)kTile * G - 1) / ((long long)kTile * G);
-    const void *fn = coll_fn(which, (int)es, G, fast, one);
+    const void *fn = bits ? bcast_bfp_fn(bits, G, fast, one) : coll_fn(which, (int)es, G, fast, one);
     if (!fn)
         return RRA_ERR_UNSUPPORTED;
-    const long long key = 50000 + which * 1000 + (int)es * 100 + G * 10 + (fast ? 2 : 0) + (one ? 1 : 0);
+    const long long key = 50000 + bits * 10000 + which * 1000 + (int)es * 100 + G * 10 +
+                          (fast ? 2 : 0) + (one ? 1 : 0);
     const int grid = grid_for(comm, key, fn, warps, smem, a.tiles, comm->tune.blocks);
     counter_sets(comm, &a.sent, &a.recv, &a.zero);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -640,6 +648,20 @@ rra_status rra_broadcast(rra_comm *comm, void *const *buf, size_t count, rra_dty
                          int root, void *stream)
 {
     return copy_common(comm, 1, buf, count, dtype, root, stream);
+}
+
+rra_status rra_broadcast_codec(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,
+                               int root, const rra_codec *codec, void *stream)
+{
+    if (codec && (codec->diff_prev || codec->diff_base || codec->average || codec->residual))
+        return RRA_ERR_INVALID;
+    if (!codec || codec->kind == RRA_CODEC_NONE)
+        return rra_broadcast(comm, buf, count, dtype, root, stream);
+    if (codec->kind == RRA_CODEC_SPARSE)
+        return RRA_ERR_UNSUPPORTED;
+    if (codec->kind != RRA_CODEC_BFP || (codec->bits != 8 && codec->bits != 4))
+        return RRA_ERR_INVALID;
+    return copy_common(comm, 1, buf, count, dtype, root, stream, codec->bits);
 }
 
 rra_status rra_tree_allreduce(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,

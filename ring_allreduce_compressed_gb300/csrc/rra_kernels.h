@@ -71,6 +71,8 @@ struct CopyArgs {
     int stage_bytes;
     int withhold_rank;
     int withhold_step;
+    int bits;        // BFP broadcast: code width (8 or 4); 0 for plain copies
+    int dt;          // BFP broadcast: element dtype (kF32 / kF16 / kBF16)
     long long T;
     long long n;     // allgather chunk length
     long long tiles; // slices per launch item range
@@ -158,6 +160,8 @@ cudaError_t launch_ring(const void *fn, const RingArgs &a, int grid, int warps, 
 // element size es, slice width 256 * groups, staged or generic path, one rank
 // per warp or several; nullptr if not instantiated.
 const void *coll_fn(int which, int es, int groups, bool fast, bool one);
+// BFP-compressed broadcast (bits 8 or 4); the element dtype is a kernel argument
+const void *bcast_bfp_fn(int bits, int groups, bool fast, bool one);
 cudaError_t launch_coll(const void *fn, const CopyArgs &a, int grid, int warps, int smem,
                         cudaStream_t st);
 

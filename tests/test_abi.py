@@ -77,6 +77,11 @@ def test_host_side_argument_checks(lib):
     assert L.rra_allgather_codec(None, None, 10, 0, C.byref(bfp), None) == rra.RRA_ERR_INVALID
     avg, keep2 = rra.Codec("bfp", bits=8, average=True)._marshal()
     assert L.rra_allgather_codec(None, None, 10, 0, C.byref(avg), None) == rra.RRA_ERR_INVALID
+    assert L.rra_broadcast_codec(None, None, 10, 0, 0, None, None) == rra.RRA_ERR_INVALID
+    assert L.rra_broadcast_codec(None, None, 10, 0, 0, C.byref(bfp), None) == rra.RRA_ERR_INVALID
+    assert L.rra_broadcast_codec(None, None, 10, 0, 0, C.byref(avg), None) == rra.RRA_ERR_INVALID
+    sp, keep3 = rra.Codec("sparse", sparsity_threshold=0.5)._marshal()
+    assert L.rra_broadcast_codec(None, None, 10, 0, 0, C.byref(sp), None) == rra.RRA_ERR_UNSUPPORTED
 
 
 def test_header_constants_match_the_binding():

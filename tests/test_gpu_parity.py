@@ -435,6 +435,76 @@ def test_broadcast(dt, N, root, T):
     comm.close()
 
 
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N,root", [(1, 0), (2, 1), (5, 2), (8, 3), (16, 0), (33, 7)])
+@pytest.mark.parametrize("T", [777, 8192, 3 * 4096 + 128 * 5 + 3])
+def test_broadcast_codec(bits, dt, N, root, T):
+    """BFP-compressed broadcast: every buffer, the root's included, holds the
+    decoded codes of the root's buffer, bit for bit as the oracle; byte
+    counters exact (fast and generic paths, one rank per warp and several)."""
+    bufs = cast(rand_f32(N, T, seed=N * 13 + root + T + bits, scale=1e-2), dt)
+    ref, s, r = O.broadcast_codec([host(b) for b in bufs], dt, root, bits)
+    comm = rra.Comm(N, T, bufs[0].dtype)
+    comm.broadcast(bufs, root=root, codec=rra.Codec("bfp", bits=bits))
+    assert comm.status() == rra.RRA_OK
+    for q in range(N):
+        assert_bits_equal(host(bufs[q]), ref[q], f"bfp{bits} {dt} broadcast rank {q}")
+    assert comm.get_bytes() == (list(s), list(r))
+    comm.close()
+
+
+@pytest.mark.parametrize("G", [1, 2, 4])
+def test_broadcast_codec_slice_widths_and_blocks(G):
+    """Every slice width, and blocks that are all zero, subnormal, huge or
+    round to the clamp, give the oracle's bits."""
+    N, T, root = 8, 4096 * 6 + 256 + 40, 5
+    g = torch.Generator(device="cuda")
+    g.manual_seed(G)
+    bufs = [torch.randn(T, generator=g, device="cuda") for _ in range(N)]
+    x = bufs[root]
+    x[:128] = 0.0
+    x[128:256] = torch.randn(128, generator=g, device="cuda") * 1e-39
+    x[256:384] *= 1e30
+    x[384:512] = 1.9921875
+    ref, s, r = O.broadcast_codec([host(b) for b in bufs], "f32", root, 8)
+    comm = rra.Comm(N, T)
+    comm.set_tuning(0, 0, 0, G)
+    comm.broadcast(bufs, root=root, codec=rra.Codec("bfp", bits=8))
+    assert comm.status() == rra.RRA_OK
+    for q in range(N):
+        assert_bits_equal(host(bufs[q]), ref[q], f"G={G} rank {q}")
+    assert comm.get_bytes() == (list(s), list(r))
+    comm.close()
+
+
+def test_broadcast_codec_misaligned_takes_generic_path():
+    N, T, root = 4, 5000, 1
+    store = cast(rand_f32(N, T + 1, seed=4, scale=1e-2), "f16")
+    bufs = [b[1:] for b in store]
+    ref, s, r = O.broadcast_codec([host(b) for b in bufs], "f16", root, 8)
+    comm = rra.Comm(N, T, torch.float16)
+    comm.broadcast(bufs, root=root, codec=rra.Codec("bfp", bits=8))
+    assert comm.status() == rra.RRA_OK
+    for q in range(N):
+        assert_bits_equal(host(bufs[q]), ref[q], f"rank {q}")
+    comm.close()
+
+
+def test_broadcast_codec_argument_errors():
+    N, T = 4, 1024
+    comm = rra.Comm(N, T)
+    bufs = rand_f32(N, T, seed=1)
+    for bad, code in ((rra.Codec("sparse", sparsity_threshold=0.5), rra.RRA_ERR_UNSUPPORTED),
+                      (rra.Codec("bfp", bits=6), rra.RRA_ERR_INVALID)):
+        with pytest.raises(rra.RRAError) as ei:
+            comm.broadcast(bufs, root=0, codec=bad)
+        assert ei.value.code == code
+    with pytest.raises(rra.RRAError):
+        comm.broadcast(bufs, root=N, codec=rra.Codec("bfp", bits=8))
+    comm.close()
+
+
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 16, 33, 64])
 @pytest.mark.parametrize("T", [300, 8192])
 def test_tree_allreduce(N, T):

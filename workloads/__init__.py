@@ -27,6 +27,8 @@ CONFIGS = {
     "diloco_n8": dict(N=8, T=10 ** 9, dtype="f32", seed=3),
     # the bucket's tensors as parameters gathered compressed (allgather alone)
     "bfp8_allgather": dict(N=8, T=13_107_200, dtype="f16", seed=1),
+    # the same tensors broadcast compressed from rank 0 (binomial tree)
+    "bfp8_broadcast": dict(N=8, T=13_107_200, dtype="f16", seed=1),
 }
 SWEEP_N = (2, 4, 8, 16, 64)
 SWEEP_T = tuple(256 * 4 ** k for k in range(11))  # 1 KiB .. 1 GiB of fp32
