@@ -76,6 +76,8 @@ def lib():
             L.oracle_allgather_codec.restype = i32
             L.oracle_codec_stats.argtypes = [i32, sz, vp, i32, u64p]
             L.oracle_codec_stats.restype = i32
+            L.oracle_codec_stats_op.argtypes = [i32, i32, i32, sz, vp, i32, u64p]
+            L.oracle_codec_stats_op.restype = i32
             L.oracle_broadcast.argtypes = [i32, sz, vp, i32, i32, u64p, u64p]
             L.oracle_broadcast_codec.argtypes = [i32, sz, vp, i32, i32, i32, u64p, u64p]
             L.oracle_broadcast_codec.restype = i32
@@ -184,6 +186,21 @@ def codec_stats(bufs, dtype="f32"):
     st = (C.c_uint64 * 4)()
     if lib().oracle_codec_stats(N, T, _ptrs(bufs), DTYPES[dtype], st) != 0:
         raise ValueError("oracle_codec_stats: bad arguments")
+    return np.array(st[:], np.uint64)
+
+
+OPS = {"allreduce": 0, "allgather": 1, "broadcast": 2}
+
+
+def codec_stats_op(bufs, dtype="f32", op="allreduce", root=0):
+    """Statistics of what an operation encodes (reading F4op): the allreduce
+    every chunk of every buffer, the compressed allgather chunk r of buffer
+    r, the compressed broadcast the root's buffer (blocks from its start)."""
+    N, T = len(bufs), bufs[0].size
+    _check(bufs, T, dtype)
+    st = (C.c_uint64 * 4)()
+    if lib().oracle_codec_stats_op(OPS[op], root, N, T, _ptrs(bufs), DTYPES[dtype], st) != 0:
+        raise ValueError("oracle_codec_stats_op: bad arguments")
     return np.array(st[:], np.uint64)
 
 

@@ -60,6 +60,10 @@
  *      R1 forward those codes unchanged; every rank, the owner included,
  *      stores decode(codes) in the buffer's dtype (RNE), so all buffers end
  *      identical.  Sparse codes restore every element exactly.
+ *  F4op  what each operation encodes, for its statistics: the allreduce
+ *      every chunk of every buffer; the compressed allgather chunk r of
+ *      buffer r; the compressed broadcast the root's buffer, blocks from its
+ *      start.
  *  AB  compressed broadcast (the same layer of [P4] §2.1 and §3.3), BFP:
  *      the root encodes its whole buffer (widened to fp32) once, as one
  *      message with blocks of 128 from the buffer start; every edge of the
@@ -914,36 +918,62 @@ void oracle_cast_from_f32(const float *x, size_t n, int t, void *out)
  *   stats[3] = of those, the ones whose BFP8 code is 0 (|x| <= 2^(e-7))
  * A code rounds to 0 exactly when |x| * 2^(q-e) <= 1/2 (ties to even), with
  * e the block exponent and q = bits - 2. */
+/* adds the statistics of buf[lo, lo + len), cut into blocks from lo */
+static void stats_range(const void *buf, size_t lo, size_t len, int in_t, float *blk,
+                        uint64_t *stats)
+{
+    for (size_t b = 0; b < len; b += OR_BFP_BLOCK) {
+        const size_t m = len - b < OR_BFP_BLOCK ? len - b : OR_BFP_BLOCK;
+        for (size_t i = 0; i < m; i++)
+            blk[i] = load_as_f32(buf, lo + b + i, in_t);
+        const int e = oracle_bfp_block_exponent(blk, m);
+        for (size_t i = 0; i < m; i++) {
+            uint32_t u;
+            memcpy(&u, &blk[i], 4);
+            stats[0]++;
+            if (u == 0u)
+                continue;
+            stats[1]++;
+            if (fabsf(blk[i]) <= ldexpf(1.0f, e - 3))
+                stats[2]++;
+            if (fabsf(blk[i]) <= ldexpf(1.0f, e - 7))
+                stats[3]++;
+        }
+    }
+}
+
+int oracle_codec_stats_op(int op, int root, int N, size_t T, const void *const *in, int in_t,
+                          uint64_t *stats);
+
 int oracle_codec_stats(int N, size_t T, const void *const *in, int in_t, uint64_t *stats)
 {
-    if (N < 1)
+    return oracle_codec_stats_op(0, 0, N, T, in, in_t, stats);
+}
+
+/* The statistics of what an operation encodes (reading F4-op): op 0, the
+ * allreduce's first hop: every chunk of every buffer; op 1, the compressed
+ * allgather: chunk r of buffer r only (the rest is overwritten); op 2, the
+ * compressed broadcast: the root's whole buffer, blocks from its start. */
+int oracle_codec_stats_op(int op, int root, int N, size_t T, const void *const *in, int in_t,
+                          uint64_t *stats)
+{
+    if (N < 1 || op < 0 || op > 2 || (op == 2 && (root < 0 || root >= N)))
         return -1;
     for (int k = 0; k < 4; k++)
         stats[k] = 0;
     float *blk = malloc(OR_BFP_BLOCK * sizeof(float));
-    for (int r = 0; r < N; r++)
-        for (int c = 0; c < N; c++) {
-            size_t lo, len;
-            chunk_range(T, N, c, &lo, &len);
-            for (size_t b = 0; b < len; b += OR_BFP_BLOCK) {
-                const size_t m = len - b < OR_BFP_BLOCK ? len - b : OR_BFP_BLOCK;
-                for (size_t i = 0; i < m; i++)
-                    blk[i] = load_as_f32(in[r], lo + b + i, in_t);
-                const int e = oracle_bfp_block_exponent(blk, m);
-                for (size_t i = 0; i < m; i++) {
-                    uint32_t u;
-                    memcpy(&u, &blk[i], 4);
-                    stats[0]++;
-                    if (u == 0u)
-                        continue;
-                    stats[1]++;
-                    if (fabsf(blk[i]) <= ldexpf(1.0f, e - 3))
-                        stats[2]++;
-                    if (fabsf(blk[i]) <= ldexpf(1.0f, e - 7))
-                        stats[3]++;
-                }
+    if (op == 2) {
+        stats_range(in[root], 0, T, in_t, blk, stats);
+    } else {
+        for (int r = 0; r < N; r++)
+            for (int c = 0; c < N; c++) {
+                if (op == 1 && c != r)
+                    continue;
+                size_t lo, len;
+                chunk_range(T, N, c, &lo, &len);
+                stats_range(in[r], lo, len, in_t, blk, stats);
             }
-        }
+    }
     free(blk);
     return 0;
 }

@@ -316,6 +316,45 @@ def test_broadcast_codec_is_the_codec_round_trip_everywhere(bits, dt):
     assert [int(x) for x in recv] == [0 if r == root else msg for r in range(N)]
 
 
+# Reading F4op: the statistics of what each operation encodes.
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_codec_stats_per_operation(dt):
+    """The allgather counts chunk r of buffer r alone, the broadcast the
+    root's buffer with blocks from its start: each equals the statistics of
+    those elements as a one-rank problem; the allreduce's are the sum over
+    every (buffer, chunk)."""
+    N, T, root = 5, 5 * 300 + 77, 2
+    rng = np.random.default_rng(len(dt))
+    bufs = []
+    for r in range(N):
+        x = (rng.standard_normal(T) * 10.0 ** rng.integers(-4, 2, T)).astype(np.float32)
+        x[rng.random(T) < 0.3] = 0.0
+        bufs.append(O.from_f32(x, dt))
+    n = -(-T // N)
+    own = [bufs[r][min(r * n, T):min((r + 1) * n, T)] for r in range(N)]
+    want_ag = sum(O.codec_stats([np.ascontiguousarray(o)], dt) for o in own)
+    assert list(O.codec_stats_op(bufs, dt, "allgather")) == list(want_ag)
+    assert list(O.codec_stats_op(bufs, dt, "broadcast", root)) == list(O.codec_stats([bufs[root]], dt))
+    assert list(O.codec_stats_op(bufs, dt, "allreduce")) == list(O.codec_stats(bufs, dt))
+    # the allreduce counts every buffer over every chunk: N times T elements
+    assert int(O.codec_stats_op(bufs, dt, "allreduce")[0]) == N * T
+
+
+def test_codec_stats_per_operation_brute_force():
+    N, T, root = 3, 40, 1
+    rng = np.random.default_rng(2)
+    xs = [(rng.standard_normal(T) * (rng.random(T) < 0.6)).astype(np.float32) for _ in range(N)]
+    n = -(-T // N)
+    ag = [0, 0, 0, 0]
+    for r in range(N):
+        piece = list(xs[r][min(r * n, T):min((r + 1) * n, T)])
+        ag = [a + b for a, b in zip(ag, brute.codec_stats([piece]))]
+    assert list(O.codec_stats_op([x.copy() for x in xs], "f32", "allgather")) == ag
+    assert list(O.codec_stats_op([x.copy() for x in xs], "f32", "broadcast", root)) == \
+        brute.codec_stats([list(xs[root])])
+
+
 # --------------------------------------------------------------- broadcast / tree
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 13])
