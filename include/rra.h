@@ -477,6 +477,35 @@ rra_status rra_codec_advise(rra_comm *comm, const void *const *in, size_t count,
                             float sparsity_threshold, float max_flushed_fraction,
                             rra_codec *codec, rra_codec_stats *stats, void *stream);
 
+/*
+ * Operator-aware choice ([cccl] §2.1, third layer: the allreduce may
+ * compress boldly, since the reduction averages the errors out; allgather
+ * and broadcast carry parameters and whole tensors and take lossless or
+ * higher-precision lossy compression, or none).  op: RRA_OP_ALLREDUCE,
+ * RRA_OP_ALLGATHER or RRA_OP_BROADCAST; root: the broadcast root (ignored
+ * otherwise).
+ * rra_codec_measure_op measures what that operation encodes: the allreduce
+ * every chunk of every buffer (as rra_codec_measure); the compressed
+ * allgather chunk r of in[r] alone; the compressed broadcast in[root] alone,
+ * blocks from its start.
+ * rra_codec_advise_op: RRA_OP_ALLREDUCE is rra_codec_advise.  Otherwise,
+ * RRA_CODEC_SPARSE for the allgather when the share of zero elements exceeds
+ * `sparsity_threshold` (lossless); else, when `allow_lossy` is nonzero and
+ * BFP8 flushes at most `max_flushed_fraction` of the nonzero elements to
+ * code 0, BFP8; else RRA_CODEC_NONE.  BFP4 is never advised for these ops.
+ * Errors: RRA_ERR_INVALID (an unknown op, a root outside 0..N-1 for the
+ * broadcast, or as rra_codec_advise / rra_codec_measure), RRA_ERR_CUDA.
+ */
+#define RRA_OP_ALLREDUCE 0
+#define RRA_OP_ALLGATHER 1
+#define RRA_OP_BROADCAST 2
+rra_status rra_codec_measure_op(rra_comm *comm, int op, int root, const void *const *in,
+                                size_t count, rra_dtype dtype, rra_codec_stats *out, void *stream);
+rra_status rra_codec_advise_op(rra_comm *comm, int op, int root, const void *const *in,
+                               size_t count, rra_dtype dtype, float sparsity_threshold,
+                               float max_flushed_fraction, int allow_lossy, rra_codec *codec,
+                               rra_codec_stats *stats, void *stream);
+
 /* Test-only fault injection: in the next collective call, simulated rank
  * "rank" does not publish the message it sends at ring step "step" (1-based,
  * counted over both passes) for the first slice each block handles, so its

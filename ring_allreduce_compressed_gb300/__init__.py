@@ -24,6 +24,8 @@ LIB_PATH = os.path.join(_PKG, "lib", "librra.so")
 
 RRA_OK, RRA_ERR_INVALID, RRA_ERR_UNSUPPORTED, RRA_ERR_CUDA, RRA_ERR_TIMEOUT, RRA_ERR_NOMEM = range(6)
 RRA_ALGO_RING, RRA_ALGO_TREE = 0, 1
+# operations for the operator-aware codec choice (rra_codec_*_op)
+RRA_OP_ALLREDUCE, RRA_OP_ALLGATHER, RRA_OP_BROADCAST = 0, 1, 2
 RRA_DEFAULT_CROSSOVER = 4 << 20
 RRA_F32, RRA_F16, RRA_BF16 = 0, 1, 2
 CODEC_NONE, CODEC_BFP, CODEC_SPARSE = 0, 1, 2
@@ -92,6 +94,9 @@ def lib():
         L.rra_get_crossover.argtypes = [vp, C.POINTER(C.c_size_t)]
         L.rra_autotune_crossover.argtypes = [vp, vp, sz, i32, vp, C.POINTER(C.c_size_t)]
         L.rra_codec_measure.argtypes = [vp, vp, sz, i32, C.POINTER(_Stats), vp]
+        L.rra_codec_measure_op.argtypes = [vp, i32, i32, vp, sz, i32, C.POINTER(_Stats), vp]
+        L.rra_codec_advise_op.argtypes = [vp, i32, i32, vp, sz, i32, C.c_float, C.c_float, i32,
+                                          C.POINTER(_Codec), C.POINTER(_Stats), vp]
         L.rra_codec_advise.argtypes = [vp, vp, sz, i32, C.c_float, C.c_float,
                                        C.POINTER(_Codec), C.POINTER(_Stats), vp]
         L.rra_status_string.argtypes = [i32]
@@ -105,7 +110,7 @@ def lib():
                      "rra_debug_withhold", "rra_comm_set_tuning", "rra_comm_last_shape",
                      "rra_autotune", "rra_allreduce_auto", "rra_set_crossover",
                      "rra_get_crossover", "rra_autotune_crossover", "rra_codec_measure",
-                     "rra_codec_advise"):
+                     "rra_codec_advise", "rra_codec_measure_op", "rra_codec_advise_op"):
             getattr(L, name).restype = st
         _lib = L
     return _lib
@@ -307,13 +312,20 @@ class Comm:
                                             C.byref(v)), "rra_autotune_crossover")
         return v.value
 
-    def codec_stats(self, inputs, stream=None) -> dict:
+    def codec_stats(self, inputs, op: int = None, root: int = 0, stream=None) -> dict:
         """rra_codec_measure: elements, nonzero, and the nonzero elements BFP4
-        and BFP8 would round to code 0, over the N inputs."""
+        and BFP8 would round to code 0, over the N inputs; with an op
+        (RRA_OP_*), rra_codec_measure_op: over what that operation encodes."""
         st = _Stats()
-        _check(lib().rra_codec_measure(self._h, _ptrs(inputs, "inputs"), inputs[0].numel(),
-                                       _dtype_code(inputs[0].dtype), C.byref(st), _stream(stream)),
-               "rra_codec_measure")
+        if op is None:
+            _check(lib().rra_codec_measure(self._h, _ptrs(inputs, "inputs"), inputs[0].numel(),
+                                           _dtype_code(inputs[0].dtype), C.byref(st),
+                                           _stream(stream)), "rra_codec_measure")
+        else:
+            _check(lib().rra_codec_measure_op(self._h, op, root, _ptrs(inputs, "inputs"),
+                                              inputs[0].numel(), _dtype_code(inputs[0].dtype),
+                                              C.byref(st), _stream(stream)),
+                   "rra_codec_measure_op")
         return {k: int(getattr(st, k)) for k, _ in _Stats._fields_}
 
     def advise_codec(self, inputs, sparsity_threshold: float = 0.5,
@@ -326,6 +338,24 @@ class Comm:
                                       _dtype_code(inputs[0].dtype), float(sparsity_threshold),
                                       float(max_flushed_fraction), C.byref(c), C.byref(st),
                                       _stream(stream)), "rra_codec_advise")
+        kind = {CODEC_NONE: "none", CODEC_BFP: "bfp", CODEC_SPARSE: "sparse"}[c.kind]
+        return (Codec(kind, bits=c.bits, sparsity_threshold=c.sparsity_threshold),
+                {k: int(getattr(st, k)) for k, _ in _Stats._fields_})
+
+    def advise_codec_op(self, op: int, inputs, root: int = 0, sparsity_threshold: float = 0.5,
+                        max_flushed_fraction: float = 0.01, allow_lossy: bool = True,
+                        stream=None):
+        """rra_codec_advise_op: (Codec, stats) for the allreduce (as
+        advise_codec), the compressed allgather (sparse if sparse enough,
+        else BFP8 when allowed and harmless enough, else none) or the
+        compressed broadcast (BFP8 when allowed and harmless enough, else
+        none)."""
+        st, c = _Stats(), _Codec()
+        _check(lib().rra_codec_advise_op(self._h, op, root, _ptrs(inputs, "inputs"),
+                                         inputs[0].numel(), _dtype_code(inputs[0].dtype),
+                                         float(sparsity_threshold), float(max_flushed_fraction),
+                                         1 if allow_lossy else 0, C.byref(c), C.byref(st),
+                                         _stream(stream)), "rra_codec_advise_op")
         kind = {CODEC_NONE: "none", CODEC_BFP: "bfp", CODEC_SPARSE: "sparse"}[c.kind]
         return (Codec(kind, bits=c.bits, sparsity_threshold=c.sparsity_threshold),
                 {k: int(getattr(st, k)) for k, _ in _Stats._fields_})

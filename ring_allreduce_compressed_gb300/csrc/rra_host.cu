@@ -1021,10 +1021,12 @@ rra_status rra_autotune_crossover(rra_comm *comm, void *const *buf, size_t count
     return RRA_OK;
 }
 
-rra_status rra_codec_measure(rra_comm *comm, const void *const *in, size_t count,
-                             rra_dtype dtype, rra_codec_stats *out, void *stream)
+rra_status rra_codec_measure_op(rra_comm *comm, int op, int root, const void *const *in,
+                                size_t count, rra_dtype dtype, rra_codec_stats *out, void *stream)
 {
-    if (!comm || !in || !out || count == 0 || count > comm->max_count || !valid_dtype(dtype))
+    if (!comm || !in || !out || count == 0 || count > comm->max_count || !valid_dtype(dtype) ||
+        op < RRA_OP_ALLREDUCE || op > RRA_OP_BROADCAST ||
+        (op == RRA_OP_BROADCAST && (root < 0 || root >= comm->N)))
         return RRA_ERR_INVALID;
     rra_status s = check_device(comm);
     if (s != RRA_OK)
@@ -1035,20 +1037,44 @@ rra_status rra_codec_measure(rra_comm *comm, const void *const *in, size_t count
         return RRA_ERR_CUDA;
     if (cs != cudaStreamCaptureStatusNone)
         return RRA_ERR_INVALID; // it reads the result back on the host
-    StatsArgs a;
-    std::memset(&a, 0, sizeof a);
-    a.N = comm->N;
-    a.T = (long long)count;
-    a.n = (a.T + a.N - 1) / a.N;
-    a.stats = comm->stats;
-    for (int r = 0; r < comm->N; ++r) {
+    for (int r = 0; r < comm->N; ++r)
         if (!in[r])
             return RRA_ERR_INVALID;
-        a.in[r] = in[r];
-    }
+    const int N = comm->N;
+    const long long T = (long long)count, n = (T + N - 1) / N;
+    const size_t es = esize(dtype);
     unsigned long long h[4];
-    if (cudaMemsetAsync(comm->stats, 0, sizeof h, st) != cudaSuccess ||
-        launch_codec_stats(a, dtype, st) != cudaSuccess ||
+    if (cudaMemsetAsync(comm->stats, 0, sizeof h, st) != cudaSuccess)
+        return RRA_ERR_CUDA;
+    // the statistics kernel counts every chunk of every buffer it is given;
+    // the allgather's owner chunks and the broadcast's root buffer are each
+    // given as a one-buffer, one-chunk problem
+    auto run = [&](int nb, long long t, const void *const *bufs) -> bool {
+        StatsArgs a;
+        std::memset(&a, 0, sizeof a);
+        a.N = nb;
+        a.T = t;
+        a.n = (t + nb - 1) / nb;
+        a.stats = comm->stats;
+        for (int r = 0; r < nb; ++r)
+            a.in[r] = bufs[r];
+        return launch_codec_stats(a, dtype, st) == cudaSuccess;
+    };
+    bool ok = true;
+    if (op == RRA_OP_ALLREDUCE) {
+        ok = run(N, T, in);
+    } else if (op == RRA_OP_BROADCAST) {
+        ok = run(1, T, in + root);
+    } else {
+        for (int r = 0; r < N && ok; ++r) {
+            const long long lo = std::min(T, r * n), hi = std::min(T, lo + n);
+            if (hi > lo) {
+                const void *p = static_cast<const char *>(in[r]) + lo * (long long)es;
+                ok = run(1, hi - lo, &p);
+            }
+        }
+    }
+    if (!ok ||
         cudaMemcpyAsync(h, comm->stats, sizeof h, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
         return RRA_ERR_CUDA;
@@ -1057,6 +1083,12 @@ rra_status rra_codec_measure(rra_comm *comm, const void *const *in, size_t count
     out->bfp4_flushed = h[2];
     out->bfp8_flushed = h[3];
     return RRA_OK;
+}
+
+rra_status rra_codec_measure(rra_comm *comm, const void *const *in, size_t count,
+                             rra_dtype dtype, rra_codec_stats *out, void *stream)
+{
+    return rra_codec_measure_op(comm, RRA_OP_ALLREDUCE, 0, in, count, dtype, out, stream);
 }
 
 rra_status rra_codec_advise(rra_comm *comm, const void *const *in, size_t count, rra_dtype dtype,
@@ -1085,6 +1117,43 @@ rra_status rra_codec_advise(rra_comm *comm, const void *const *in, size_t count,
         codec->kind = RRA_CODEC_BFP;
         codec->bits = 4;
     } else {
+        codec->kind = RRA_CODEC_BFP;
+        codec->bits = 8;
+    }
+    return RRA_OK;
+}
+
+rra_status rra_codec_advise_op(rra_comm *comm, int op, int root, const void *const *in,
+                               size_t count, rra_dtype dtype, float sparsity_threshold,
+                               float max_flushed_fraction, int allow_lossy, rra_codec *codec,
+                               rra_codec_stats *stats, void *stream)
+{
+    if (op == RRA_OP_ALLREDUCE)
+        return rra_codec_advise(comm, in, count, dtype, sparsity_threshold,
+                                max_flushed_fraction, codec, stats, stream);
+    if (!codec || !(sparsity_threshold >= 0.0f && sparsity_threshold < 1.0f) ||
+        !(max_flushed_fraction >= 0.0f && max_flushed_fraction <= 1.0f))
+        return RRA_ERR_INVALID;
+    rra_codec_stats st{};
+    const rra_status s =
+        rra_codec_measure_op(comm, op, root, in, count, dtype, &st, stream);
+    if (s != RRA_OK)
+        return s;
+    if (stats)
+        *stats = st;
+    std::memset(codec, 0, sizeof *codec);
+    codec->sparsity_threshold = sparsity_threshold;
+    codec->kind = RRA_CODEC_NONE;
+    // conservative: lossless sparse codes first (allgather only), then the
+    // higher-precision lossy width, and only when it is allowed and flushes
+    // at most the given share of the nonzero values; else no compression
+    const double zeros = (double)(st.elements - st.nonzero);
+    if (op == RRA_OP_ALLGATHER && st.elements &&
+        zeros > (double)sparsity_threshold * (double)st.elements) {
+        codec->kind = RRA_CODEC_SPARSE;
+        codec->bits = 8;
+    } else if (allow_lossy &&
+               (double)st.bfp8_flushed <= (double)max_flushed_fraction * (double)st.nonzero) {
         codec->kind = RRA_CODEC_BFP;
         codec->bits = 8;
     }

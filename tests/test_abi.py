@@ -82,6 +82,9 @@ def test_host_side_argument_checks(lib):
     assert L.rra_broadcast_codec(None, None, 10, 0, 0, C.byref(avg), None) == rra.RRA_ERR_INVALID
     sp, keep3 = rra.Codec("sparse", sparsity_threshold=0.5)._marshal()
     assert L.rra_broadcast_codec(None, None, 10, 0, 0, C.byref(sp), None) == rra.RRA_ERR_UNSUPPORTED
+    assert L.rra_codec_measure_op(None, 1, 0, None, 10, 0, None, None) == rra.RRA_ERR_INVALID
+    assert L.rra_codec_advise_op(None, 2, 0, None, 10, 0, C.c_float(0.5), C.c_float(0.01), 1,
+                                 None, None, None) == rra.RRA_ERR_INVALID
 
 
 def test_header_constants_match_the_binding():
@@ -89,6 +92,8 @@ def test_header_constants_match_the_binding():
     consts = dict(re.findall(r"#define (RRA_[A-Z_]+) \(?([0-9a-fx]+)", text))
     assert int(consts["RRA_ALGO_RING"]) == rra.RRA_ALGO_RING
     assert int(consts["RRA_ALGO_TREE"]) == rra.RRA_ALGO_TREE
+    for name in ("RRA_OP_ALLREDUCE", "RRA_OP_ALLGATHER", "RRA_OP_BROADCAST"):
+        assert int(consts[name]) == getattr(rra, name)
     m = re.search(r"#define RRA_DEFAULT_CROSSOVER \((\d+)ull << (\d+)\)", text)
     assert int(m.group(1)) << int(m.group(2)) == rra.RRA_DEFAULT_CROSSOVER
     assert int(consts["RRA_RING_SLICE"]) == rra.RING_SLICE

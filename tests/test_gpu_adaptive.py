@@ -79,3 +79,64 @@ def test_advised_codec_runs_the_ring():
     for r in range(N):
         assert np.array_equal(host(outs[r]).view(np.uint32), ref[r].view(np.uint32))
     comm.close()
+
+
+# ---------------------------------------------------------------- operator-aware choice
+
+@pytest.mark.parametrize("op", ["allgather", "broadcast"])
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N,T", [(1, 300), (3, 1000), (8, 8 * 1000 + 3), (20, 20 * 130 + 11)])
+def test_codec_stats_per_operation_match_the_oracle(op, dt, N, T):
+    """What the compressed allgather (each owner's chunk) and broadcast (the
+    root's buffer) encode, counted exactly as the oracle counts it."""
+    xs = _mixed(N, T, seed=N + T + len(op), dt=dt)
+    root = (N - 1) // 2
+    comm = rra.Comm(N, T, xs[0].dtype)
+    code = {"allgather": rra.RRA_OP_ALLGATHER, "broadcast": rra.RRA_OP_BROADCAST}[op]
+    got = comm.codec_stats(xs, op=code, root=root)
+    want = O.codec_stats_op([host(x) for x in xs], dt, op, root)
+    assert [got[k] for k in ("elements", "nonzero", "bfp4_flushed", "bfp8_flushed")] == \
+        [int(v) for v in want]
+    comm.close()
+
+
+def test_operator_aware_advice():
+    """Allgather and broadcast take lossless sparse codes (allgather only),
+    else BFP8 when lossy codes are allowed and flush little, else nothing;
+    BFP4 is never advised for them.  The allreduce keeps its own rule."""
+    N, T = 8, 8 * 4096
+    comm = rra.Comm(N, T)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    sparse = [torch.where(torch.rand(T, generator=g, device="cuda") < 0.2,
+                          torch.randn(T, generator=g, device="cuda"), torch.zeros(T, device="cuda"))
+              for _ in range(N)]
+    smooth = [torch.randn(T, generator=g, device="cuda") for _ in range(N)]
+    c, st = comm.advise_codec_op(rra.RRA_OP_ALLGATHER, sparse)
+    assert c.kind == "sparse" and st["elements"] == T  # N owner chunks of T / N
+    c, _ = comm.advise_codec_op(rra.RRA_OP_BROADCAST, sparse, root=3)
+    assert c.kind in ("bfp", "none") and (c.kind == "none" or c.bits == 8)
+    c, st = comm.advise_codec_op(rra.RRA_OP_ALLGATHER, smooth)
+    flushed8 = st["bfp8_flushed"] <= 0.01 * st["nonzero"]
+    assert (c.kind, c.bits) == (("bfp", 8) if flushed8 else ("none", 0))
+    c, _ = comm.advise_codec_op(rra.RRA_OP_ALLGATHER, smooth, allow_lossy=False)
+    assert c.kind == "none"
+    c, st = comm.advise_codec_op(rra.RRA_OP_BROADCAST, smooth, root=0, max_flushed_fraction=1.0)
+    assert (c.kind, c.bits) == ("bfp", 8) and st["elements"] == T
+    c, _ = comm.advise_codec_op(rra.RRA_OP_BROADCAST, smooth, root=0, max_flushed_fraction=0.0)
+    assert c.kind == ("bfp" if st["bfp8_flushed"] == 0 else "none")
+    c_ar, _ = comm.advise_codec_op(rra.RRA_OP_ALLREDUCE, smooth)
+    c_ref, _ = comm.advise_codec(smooth)
+    assert (c_ar.kind, c_ar.bits) == (c_ref.kind, c_ref.bits)
+    # the advised codec runs the compressed allgather unchanged
+    bufs = [x.clone() for x in sparse]
+    c, _ = comm.advise_codec_op(rra.RRA_OP_ALLGATHER, bufs)
+    ref = O.allgather_codec([host(b) for b in bufs], "f32", c.kind, c.bits)[0]
+    comm.allgather(bufs, codec=c)
+    for q in range(N):
+        assert np.array_equal(host(bufs[q]).view(np.uint32), ref[q].view(np.uint32))
+    with pytest.raises(rra.RRAError):
+        comm.advise_codec_op(rra.RRA_OP_BROADCAST, smooth, root=N)
+    with pytest.raises(rra.RRAError):
+        comm.advise_codec_op(7, smooth)
+    comm.close()
