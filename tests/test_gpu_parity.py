@@ -581,7 +581,8 @@ def test_diff_codec(n):
 
 # ------------------------------------------------------------------ failure detection, determinism
 
-@pytest.mark.parametrize("op", ["ring", "allgather", "broadcast", "tree"])
+@pytest.mark.parametrize("op", ["ring", "allgather", "broadcast", "tree", "allgather_codec",
+                                "broadcast_codec"])
 def test_withheld_message_times_out(op):
     """A simulated rank that never publishes one message: its receiver's
     bounded wait runs out, the launch returns, the communicator reports
@@ -591,16 +592,22 @@ def test_withheld_message_times_out(op):
     comm = rra.Comm(N, T)
     comm.set_timeout(20_000_000)  # 20 ms
     # rank 1 sends at the first step of the ring, the allgather and the tree's
-    # first reduce level; in the broadcast only the root sends at level 0
-    comm.debug_withhold(0 if op == "broadcast" else 1, 1)
+    # first reduce level; in the broadcasts only the root sends at level 0;
+    # the compressed allgather's first send is the owner's, at ring step N
+    comm.debug_withhold(0 if op.startswith("broadcast") else 1, N if op == "allgather_codec" else 1)
     outs = [torch.zeros(T, device="cuda") for _ in range(N)]
     bufs = [x.clone() for x in xs]
+    bfp8 = rra.Codec("bfp", bits=8)
     if op == "ring":
         comm.ring_allreduce(xs, outs)
     elif op == "allgather":
         comm.allgather(bufs)
     elif op == "broadcast":
         comm.broadcast(bufs, root=0)
+    elif op == "allgather_codec":
+        comm.allgather(bufs, codec=bfp8)
+    elif op == "broadcast_codec":
+        comm.broadcast(bufs, root=0, codec=bfp8)
     else:
         comm.tree_allreduce(bufs)
     assert comm.status() == rra.RRA_ERR_TIMEOUT
