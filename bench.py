@@ -440,7 +440,9 @@ def run_rra(args, world, rank, local):
     clk = clocks.stop()
     status = wl.comm.status()
     total_ms = t_start.elapsed_time(t_end)
-    kern_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = sum(step_ms) / K
+    kern_ms_median = max_over_ranks(world, statistics.median(step_ms))
     ms_step = max_over_ranks(world, total_ms / K)
     kern_ms = max_over_ranks(world, kern_ms)
 
@@ -539,6 +541,12 @@ def run_rra(args, world, rank, local):
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": KERNEL_OF.get(args.config, "ring_kernel"), "kernel_ms": kern_ms,
                      "bytes_per_launch": wl.compulsory,
+                     "kernel_ms_median": kern_ms_median,
+                     # the slot-materialised model: every wire byte written to a
+                     # slot and read back once, beside the compulsory bytes (the
+                     # slots live in shared memory here, so this can exceed 1)
+                     "bytes_alg_slots": wl.compulsory + 2 * sum(sent),
+                     "frac_alg_slots": (wl.compulsory + 2 * sum(sent)) / (kern_ms * 1e-3) / 1e9 / peak,
                      "bytes_model": "compulsory: N*T*(in+out) (+ diff prev and base)",
                      "peak_source": peak_src, "traffic_source": traffic_src},
         "cpu_baseline": cpu,
