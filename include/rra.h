@@ -509,8 +509,10 @@ rra_status rra_codec_advise_op(rra_comm *comm, int op, int root, const void *con
 /* Test-only fault injection: in the next collective call, simulated rank
  * "rank" does not publish the message it sends at ring step "step" (1-based,
  * counted over both passes; the compressed allgather sends first at step N,
- * the owner's) -- or, in a broadcast or the tree, at level "step" (1-based)
- * -- for the first slice each block handles, so its receiver's wait runs out
+ * the owner's) -- or, in the plain broadcast or the tree, at level "step"
+ * (1-based); in the compressed broadcast, where a rank publishes once for
+ * all its children, any step >= 1 -- for the first slice each block
+ * handles, so its receiver's wait runs out
  * and the call ends with RRA_ERR_TIMEOUT.  rank < 0 disables.  The setting
  * applies to one call only. */
 rra_status rra_debug_withhold(rra_comm *comm, int rank, int step);

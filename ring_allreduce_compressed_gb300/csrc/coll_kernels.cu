@@ -27,10 +27,12 @@
 // ranks' sends before any of their receives, so a warp that plays both ends
 // of an edge (N > 16) never waits on itself.
 //  broadcast   (BFP) the same tree carrying the root's block-floating-point
-//              codes: the root encodes each slice once into its own slot
-//              (its edge has no sender) and stores the decoded values in its
-//              buffer; forwarders copy codes slot to slot; receivers store
-//              the decoded values.
+//              codes, each edge copied by its receiver: the root encodes
+//              each slice once into its own slot and stores the decoded
+//              values; every other rank copies its parent's codes into its
+//              own slot (if it has children) and stores the decoded values;
+//              a slot is freed when all of its rank's children have copied
+//              it (an mbarrier counting the children).
 #include "ring_kernel.cuh" // BfpGroup: the BFP arithmetic of the ring
 #include "rra_device.cuh"
 #include "rra_kernels.h"
@@ -104,12 +106,14 @@ __device__ __forceinline__ CollSmem coll_carve(unsigned char *smem, const CopyAr
     return s;
 }
 
+// empty_count(edge): arrivals that free a slot of that edge (1 by default)
+template <class EmptyCount>
 __device__ __forceinline__ void coll_init(const CollSmem &s, const CopyArgs &a, int edges,
-                                          int stagers, bool fast)
+                                          int stagers, bool fast, EmptyCount empty_count)
 {
     for (int i = threadIdx.x; i < edges * a.K; i += blockDim.x) {
         mbar_init(s.full + i, 1);
-        mbar_init(s.empty + i, 1);
+        mbar_init(s.empty + i, (uint32_t)empty_count(i / a.K));
     }
     if (fast)
         for (int i = threadIdx.x; i < stagers * a.D; i += blockDim.x)
@@ -123,6 +127,12 @@ __device__ __forceinline__ void coll_init(const CollSmem &s, const CopyArgs &a, 
             a.zero[i] = 0ull;
     mbar_fence_init();
     __syncthreads();
+}
+
+__device__ __forceinline__ void coll_init(const CollSmem &s, const CopyArgs &a, int edges,
+                                          int stagers, bool fast)
+{
+    coll_init(s, a, edges, stagers, fast, [](int) { return 1; });
 }
 
 // Per-rank byte counters: in registers when every warp plays one rank, in
@@ -547,23 +557,27 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     constexpr int TW = kTile * G;
     const int N = a.N, W = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int K = a.K, D = a.D, dt = a.dt, es = a.es;
-    const CollSmem s = coll_carve(smem, a, N, 1, FAST);
-    coll_init(s, a, N, 1, FAST);
-    const long long T = a.T;
-    const int rstride = ONE ? N : W;
-    const int tiles = (int)a.tiles;
     const int root = a.root;
     int L = 0;
     while ((1 << L) < N)
         ++L;
-    auto last_send = [&](int q) -> int { // last level at which q forwards (-1: never)
-        const int k0 = q > 0 ? 32 - __clz(q) : 0;
-        int last = -1;
-        for (int k = k0; k < L; ++k)
-            if (q + (1 << k) < N)
-                last = k;
-        return last;
+    // relative rank q: parent q - 2^floor(log2 q); children q + 2^k for every
+    // k with 2^k > q and q + 2^k < N
+    auto children = [&](int q) -> int {
+        int c = 0;
+        for (int k = q > 0 ? 32 - __clz(q) : 0; k < L; ++k)
+            c += q + (1 << k) < N ? 1 : 0;
+        return c;
     };
+    auto rel = [&](int r) -> int {
+        const int q = r - root;
+        return q < 0 ? q + N : q;
+    };
+    // a rank's slot is freed once every child has copied the message out
+    const CollSmem s = coll_carve(smem, a, N, 1, FAST);
+    coll_init(s, a, N, 1, FAST, [&](int r) { return max(children(rel(r)), 1); });
+    const long long T = a.T;
+    const int tiles = (int)a.tiles;
     const bool root_warp = root % W == warp;
     int cur_item = blockIdx.x, inflight = 0;
     auto issue = [&](int d) { // lane 0 of the root's warp
@@ -595,95 +609,77 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         const bool first = item == (int)blockIdx.x;
         const int V = clamp_len(T - t0, TW);
         const unsigned long long mb = bfp_msg_bytes(V, BITS);
-        // the root encodes the slice into its own slot and stores its decoded values
-        if (root_warp) {
-            if (FAST &&
-                !(ok = wait_ready(s.sbar + stg.slot, (uint32_t)stg.phase, a.timeout_ns, a.status)))
+        // a warp plays its ranks in increasing relative rank, so a parent it
+        // plays always publishes before a child it plays waits for it
+        for (int q = ONE ? rel(warp) : 0; ok && q < N; q += ONE ? N : 1) {
+            int r = q + root;
+            r -= r >= N ? N : 0;
+            if (!ONE && r % W != warp)
+                continue;
+            const int nch = children(q);
+            unsigned char *own = s.slots + (size_t)(r * K + e.slot) * a.slot_bytes;
+            char *mine = reinterpret_cast<char *>(a.buf[r]) + t0 * es;
+            // a rank with children first waits until they have all copied the
+            // message that last used this slot
+            if (nch > 0 && !(ok = wait_ready(s.empty + r * K + e.slot, (uint32_t)(e.phase ^ 1),
+                                             a.timeout_ns, a.status)))
                 break;
-            const unsigned char *src =
-                FAST ? s.stages + (size_t)stg.slot * a.stage_bytes
-                     : reinterpret_cast<const unsigned char *>(a.buf[root]) + t0 * es;
-            unsigned char *own = s.slots + (size_t)(root * K + e.slot) * a.slot_bytes;
-            char *mine = reinterpret_cast<char *>(a.buf[root]) + t0 * es;
-#pragma unroll 1
-            for (int gi = 0; gi < G; ++gi) {
-                if (gi * kTile >= V)
+            int p = 0; // absolute rank of the parent
+            if (q == 0) {
+                if (FAST && !(ok = wait_ready(s.sbar + stg.slot, (uint32_t)stg.phase,
+                                              a.timeout_ns, a.status)))
                     break;
-                const int el = gi * kTile + 8 * lane;
-                const int vl = min(max(V - el, 0), 8);
-                float v[8];
-                load8_dt(src + (size_t)el * es, dt, vl, FAST, v); // +0.0 past the end
-                int ex;
-                uint32_t w[2];
-                BG::encode(v, ex, w);
-                SL::put(own, gi, lane, ex, w);
-                BG::decode(w, ex, v);
-                store8(mine + (size_t)el * es, dt, v, vl, FAST);
-            }
-            __syncwarp();
-        }
-        for (int k = 0; ok && k < L; ++k) {
-            // senders at level k: relative q < 2^k with q + 2^k < N
-            for (int r = warp; r < N; r += rstride) {
-                int q = r - root;
-                q += q < 0 ? N : 0;
-                if (!(q < (1 << k) && q + (1 << k) < N))
-                    continue;
-                int child = r + (1 << k);
-                child -= child >= N ? N : 0;
-                if (!(ok = wait_ready(s.empty + child * K + e.slot, (uint32_t)(e.phase ^ 1),
-                                      a.timeout_ns, a.status)))
-                    break;
-                const unsigned char *src = s.slots + (size_t)(r * K + e.slot) * a.slot_bytes;
-                unsigned char *dslot = s.slots + (size_t)(child * K + e.slot) * a.slot_bytes;
+                const unsigned char *src =
+                    FAST ? s.stages + (size_t)stg.slot * a.stage_bytes
+                         : reinterpret_cast<const unsigned char *>(a.buf[root]) + t0 * es;
 #pragma unroll 1
-                for (int gi = 0; gi < G; ++gi) {
+                for (int gi = 0; gi < G; ++gi) { // encode once, keep the decoded values
                     if (gi * kTile >= V)
                         break;
+                    const int el = gi * kTile + 8 * lane;
+                    const int vl = min(max(V - el, 0), 8);
+                    float v[8];
+                    load8_dt(src + (size_t)el * es, dt, vl, FAST, v); // +0.0 past the end
                     int ex;
                     uint32_t w[2];
-                    SL::get(src, gi, lane, ex, w);
-                    SL::put(dslot, gi, lane, ex, w);
+                    BG::encode(v, ex, w);
+                    SL::put(own, gi, lane, ex, w);
+                    BG::decode(w, ex, v);
+                    store8(mine + (size_t)el * es, dt, v, vl, FAST);
                 }
-                __syncwarp();
-                if (lane == 0) {
-                    if (!(first && r == a.withhold_rank && k + 1 == a.withhold_step))
-                        mbar_arrive(s.full + child * K + e.slot);
-                    by.add_sent(s, r, mb);
-                    if (q > 0 && k == last_send(q)) // done forwarding: free the slot
-                        mbar_arrive(s.empty + r * K + e.slot);
-                }
-            }
-            if (!ok)
-                break;
-            // receivers at level k: relative q in [2^k, 2^(k+1))
-            for (int r = warp; r < N; r += rstride) {
-                int q = r - root;
-                q += q < 0 ? N : 0;
-                if (!(q >= (1 << k) && q < (2 << k)))
-                    continue;
-                if (!(ok = wait_ready(s.full + r * K + e.slot, (uint32_t)e.phase, a.timeout_ns,
+            } else {
+                p = q - (1 << (31 - __clz(q))) + root;
+                p -= p >= N ? N : 0;
+                if (!(ok = wait_ready(s.full + p * K + e.slot, (uint32_t)e.phase, a.timeout_ns,
                                       a.status)))
                     break;
-                const unsigned char *rslot = s.slots + (size_t)(r * K + e.slot) * a.slot_bytes;
-                char *mine = reinterpret_cast<char *>(a.buf[r]) + t0 * es;
+                const unsigned char *pslot = s.slots + (size_t)(p * K + e.slot) * a.slot_bytes;
 #pragma unroll 1
-                for (int gi = 0; gi < G; ++gi) {
+                for (int gi = 0; gi < G; ++gi) { // copy the parent's codes, store decoded
                     if (gi * kTile >= V)
                         break;
                     const int el = gi * kTile + 8 * lane;
                     int ex;
                     uint32_t w[2];
-                    SL::get(rslot, gi, lane, ex, w);
+                    SL::get(pslot, gi, lane, ex, w);
+                    if (nch > 0)
+                        SL::put(own, gi, lane, ex, w);
                     float v[8];
                     BG::decode(w, ex, v);
                     store8(mine + (size_t)el * es, dt, v, min(max(V - el, 0), 8), FAST);
                 }
-                __syncwarp();
-                if (lane == 0) {
+            }
+            __syncwarp();
+            if (lane == 0) {
+                if (q > 0) {
+                    mbar_arrive(s.empty + p * K + e.slot); // done with the parent's slot
                     by.add_recv(s, r, mb);
-                    if (last_send(q) < 0) // a leaf frees its slot at once
-                        mbar_arrive(s.empty + r * K + e.slot);
+                }
+                if (nch > 0) {
+                    // fault injection: a withheld rank never publishes its message
+                    if (!(first && r == a.withhold_rank && a.withhold_step >= 1))
+                        mbar_arrive(s.full + r * K + e.slot);
+                    by.add_sent(s, r, mb * (unsigned long long)nch);
                 }
             }
         }
