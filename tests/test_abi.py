@@ -132,3 +132,22 @@ def test_product_path_never_calls_the_oracle():
         fn = bench.rfind("\ndef ", 0, pos)
         name = bench[fn + 5:bench.index("(", fn)]
         assert name in ("oracle_sample_ring", "run_reference"), name
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/rra.h is a C ABI: it compiles as strict C99 and as C++, and a C
+    translation unit can name every entry point it declares."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    src = tmp_path / "use_rra.c"
+    refs = "\n".join(f"    (void)&{n};" for n in declared_functions())
+    src.write_text('#include "rra.h"\nvoid use_all(void)\n{\n' + refs + "\n}\n")
+    for lang in (["-x", "c", "-std=c99", "-pedantic-errors"], ["-x", "c++", "-std=c++17"]):
+        r = subprocess.run([gcc, *lang, "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
+                            "-I", cuda_inc, "-c", str(src), "-o", str(tmp_path / "u.o")],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
