@@ -336,7 +336,8 @@ def _allgather_inputs(N, T, dt, codec, seed):
 @pytest.mark.parametrize("codec,bits", [("bfp", 8), ("bfp", 4), ("sparse", 8)])
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("N,T", [(1, 300), (2, 512), (3, 1000), (8, 8 * 2048 * 5 + 8 * 24),
-                                 (5, 256 * 5 * 3 + 70), (16, 16 * 1024 * 3)])
+                                 (5, 256 * 5 * 3 + 70), (16, 16 * 1024 * 3), (33, 33 * 512 + 7),
+                                 (64, 64 * 256 * 2)])
 def test_allgather_codec(codec, bits, dt, N, T):
     """Compressed allgather: every buffer holds every owner's decoded chunk,
     bit for bit as the oracle; byte counters exact (full slices, a ragged
