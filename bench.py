@@ -447,6 +447,37 @@ def run_rra(args, world, rank, local):
     kern_ms = max_over_ranks(world, kern_ms)
 
     value = whole_job_gbs(world, wl.payload, ms_step)
+
+    # latency-bound workloads: one call's device time without the host's
+    # launch cost, from CUDA-graph replays of back-to-back calls (outside the
+    # timed region above)
+    latency = None
+    if wl.compulsory <= 2 ** 26:
+        calls, reps = 20, 20
+        graph = torch.cuda.CUDAGraph()
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            with torch.cuda.graph(graph, stream=gs):
+                for _ in range(calls):
+                    wl.step()
+        stream.wait_stream(gs)
+        graph.replay()
+        torch.cuda.synchronize()
+        per_call = []
+        for _ in range(reps):
+            a_ev = torch.cuda.Event(enable_timing=True)
+            b_ev = torch.cuda.Event(enable_timing=True)
+            a_ev.record()
+            graph.replay()
+            b_ev.record()
+            b_ev.synchronize()
+            per_call.append(a_ev.elapsed_time(b_ev) * 1e3 / calls)
+        del graph
+        assert wl.comm.status() == rra.RRA_OK
+        latency = {"graph_us_per_call": statistics.median(per_call), "calls_per_graph": calls,
+                   "replays": reps, "note": "median over CUDA-graph replays of back-to-back "
+                   "calls; excludes the host launch cost that the per-step events include"}
     peak, peak_src = hbm_peak()
     achieved = wl.compulsory / (kern_ms * 1e-3) / 1e9
     traffic, traffic_src = traffic_from_profile(args.config)
@@ -551,6 +582,7 @@ def run_rra(args, world, rank, local):
                      "peak_source": peak_src, "traffic_source": traffic_src},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "latency": latency,
         "gpu_launches": K,
         "clocks": clk,
         "status": rra.status_string(status),
