@@ -376,7 +376,7 @@ rra_status rra_set_timeout(rra_comm *comm, uint64_t ns);
  *                 frees the slot it streams from only after its own send).
  *  stage_depth    input slices each rank stages ahead with bulk copies (1..16).
  *  slice_groups   elements per ring message in units of 256 (1, 2, 4 or 8;
- *                 the sparse codec always uses 1).
+ *                 the sparse codec uses 1, 2 or 4).
  * Depths and widths that do not fit the shared memory are reduced
  * automatically.  Errors: RRA_ERR_INVALID for NULL or values out of range.
  */
