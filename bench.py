@@ -646,6 +646,80 @@ def run_reference(args, world, rank):
 
 # ---------------------------------------------------------------- ring vs tree sweep
 
+def run_codecs(args, world, rank):
+    """The standalone codec entry points on 2^28 elements, each timed with CUDA
+    events (median of 10 after 3 warm-ups) against its compulsory bytes: the
+    input read once and the output written once (the sparse encoder reads its
+    input twice: a count pass and an emit pass)."""
+    import ring_allreduce_compressed_gb300 as rra
+    rra.build()
+    if rank != 0:
+        return
+    peak, peak_src = hbm_peak()
+    n = 1 << 28
+    g = torch.Generator(device="cuda")
+    g.manual_seed(6)
+    x16 = (torch.randn(n, generator=g, device="cuda") * 1e-3).half()
+    xs = torch.randn(n, generator=g, device="cuda")
+    xs[torch.rand(n, generator=g, device="cuda") < 0.6] = 0.0
+    xb = xs.bfloat16()
+    del xs
+    nb = -(-n // 128)
+    exps = torch.empty(nb, dtype=torch.int8, device="cuda")
+    mants = torch.empty(n, dtype=torch.uint8, device="cuda")
+    out32 = torch.zeros(n, device="cuda")
+    hdr = torch.empty(2, dtype=torch.int32, device="cuda")
+    vals = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty(n, dtype=torch.int32, device="cuda")
+    rra.sparse_encode(xb, 0.5, hdr, vals, idx)
+    torch.cuda.synchronize()
+    fmt, nnz = [int(v) for v in hdr.cpu()]
+    cur = torch.randn(n, generator=g, device="cuda")
+    prev = torch.randn(n, generator=g, device="cuda")
+    diff = torch.empty(n, device="cuda")
+
+    def bfp_bytes(bits):
+        return nb + (n if bits == 8 else n // 2)
+
+    cases = [
+        ("bfp8_encode f16", lambda: rra.bfp_encode(x16, 8, exps, mants), 2 * n + bfp_bytes(8)),
+        ("bfp4_encode f16", lambda: rra.bfp_encode(x16, 4, exps, mants), 2 * n + bfp_bytes(4)),
+        ("bfp8_decode -> f32", lambda: rra.bfp_decode(exps, mants, n, 8, out32), bfp_bytes(8) + 4 * n),
+        ("bfp8_decode accumulate f32", lambda: rra.bfp_decode(exps, mants, n, 8, out32, True),
+         bfp_bytes(8) + 8 * n),
+        ("sparse_encode bf16 (60 % zeros)", lambda: rra.sparse_encode(xb, 0.5, hdr, vals, idx),
+         2 * n + (6 * nnz if fmt else 2 * n)),
+        ("sparse_decode -> f32", lambda: rra.sparse_decode(hdr, vals, idx, n, out32),
+         (6 * nnz if fmt else 2 * n) + 4 * n),
+        ("diff_encode f32", lambda: rra.diff_encode(cur, prev, diff), 12 * n),
+    ]
+    out = []
+    for name, fn, nbytes in cases:
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(10):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b) * 1e3)
+        us = statistics.median(times)
+        line = {"codec_bench": True, "op": name, "n": n, "us": us, "bytes": nbytes,
+                "gbs": nbytes / (us * 1e-6) / 1e9,
+                "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peak, "peak_source": peak_src,
+                "sparse_format": "sparse" if fmt else "dense", "nnz": nnz}
+        out.append(line)
+        print(json.dumps(line), flush=True)
+    if args.jsonl:
+        with open(args.jsonl, "a") as f:
+            for line in out:
+                f.write(json.dumps(line) + "\n")
+
+
 def run_sweep(args, world, rank):
     """Lossless fp32 ring vs tree allreduce over T = 256 * 4^k elements
     (1 KiB .. 1 GiB per rank) and N in {2, 4, 8, 16, 64}, in place, values
@@ -815,6 +889,8 @@ def main():
     ap.add_argument("--jsonl", default=None)
     ap.add_argument("--sweep", action="store_true",
                     help="ring vs tree message-size sweep (lossless fp32) instead of one line")
+    ap.add_argument("--codecs", action="store_true",
+                    help="time the standalone codec entry points instead of one line")
     ap.add_argument("--sweep-n", default="2,4,8,16,64")
     ap.add_argument("--sweep-kmax", type=int, default=10)
     ap.add_argument("--alpha-us", type=float, default=5.0,
@@ -830,6 +906,8 @@ def main():
         return
     if args.sweep:
         run_sweep(args, world, rank)
+    elif args.codecs:
+        run_codecs(args, world, rank)
     elif args.impl == "reference":
         run_reference(args, world, rank)
     else:

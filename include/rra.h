@@ -329,7 +329,12 @@ rra_status rra_sparse_encode_noalloc(const void *x, size_t n, rra_dtype dtype, f
 
 /*
  * Sparse decode into fp32 acc[0..n) (hdr, vals, idx as written by
- * rra_sparse_encode; the format is read on the device).
+ * rra_sparse_encode: indices ascending; the format is read on the device).
+ * A sparse message without accumulation is restored in one pass over acc,
+ * 4096 elements at a time, using a per-device scratch of n/4096 + 1 words
+ * that the library allocates on first use and grows as needed (decodes that
+ * overlap on the GPU share it); an index out of order or outside [0, n) is
+ * ignored.
  *  accumulate == 0: acc = the restored message (+0.0 where a sparse message
  *                   lists nothing).
  *  accumulate != 0: acc[i] = acc[i] + v at every position the message

@@ -6,6 +6,9 @@
 // buffers allow, grid-stride loops over warp-sized tiles.
 #include "rra_device.cuh"
 #include "rra_kernels.h"
+#include <algorithm>
+#include <map>
+#include <mutex>
 
 namespace rra {
 
@@ -142,25 +145,51 @@ __global__ void __launch_bounds__(kThreads) bfp_decode_kernel(const int8_t *__re
 // pass 2 (one block) turns the counts into exclusive offsets, decides the
 // format and writes the header; pass 3 writes the values and indices: a
 // thread's slot comes from a warp ballot/popc prefix and a block prefix sum
-// over the warps, plus the tile offset.
+// over the warps; the tile's compacted run is staged in shared memory and
+// leaves in consecutive stores at the tile's offset.
 constexpr int kSpTile = 4096;
 
+// Nonzero mask of the 8 elements at e0 (bit i: element e0+i is not +0.0),
+// from the elements' own bits, which are also returned (a 16-bit element
+// zero-extended): an fp16 or bf16 element widens to +0.0 exactly when its 16
+// bits are zero, so no conversion is needed.
 template <int IN_T>
-__device__ __forceinline__ uint32_t nz_mask8(const void *x, long long n, long long e0, int vec,
-                                             float v[8])
+__device__ __forceinline__ uint32_t nz_mask8_bits(const void *x, long long n, long long e0,
+                                                  int vec, uint32_t w[8])
 {
-    constexpr int es = dtype_size(IN_T);
     const int vl = (int)max(0LL, min(8LL, n - e0));
-    const char *src = reinterpret_cast<const char *>(x) + e0 * es;
-    if (vec && vl == 8)
-        load8_vec<IN_T>(src, v);
-    else
-        load8_scalar<IN_T>(src, vl, v);
+    if constexpr (IN_T == kF32) {
+        const uint32_t *p = reinterpret_cast<const uint32_t *>(x) + e0;
+        if (vec && vl == 8) {
+            const uint4 a = reinterpret_cast<const uint4 *>(p)[0];
+            const uint4 b = reinterpret_cast<const uint4 *>(p)[1];
+            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+            w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                w[i] = i < vl ? p[i] : 0u;
+        }
+    } else {
+        const uint16_t *p = reinterpret_cast<const uint16_t *>(x) + e0;
+        if (vec && vl == 8) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(p);
+            const uint32_t h[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                w[2 * i] = h[i] & 0xffffu;
+                w[2 * i + 1] = h[i] >> 16;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                w[i] = i < vl ? (uint32_t)p[i] : 0u;
+        }
+    }
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-        if (i < vl && __float_as_uint(v[i]) != 0u)
-            m |= 1u << i;
+        m |= (w[i] != 0u ? 1u : 0u) << i;
     return m;
 }
 
@@ -175,9 +204,9 @@ __global__ void __launch_bounds__(kThreads) sparse_count_kernel(const void *__re
         uint32_t c = 0;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            float v[8];
+            uint32_t w[8];
             const long long e0 = t * kSpTile + (long long)h * 2048 + 8 * threadIdx.x;
-            c += __popc(nz_mask8<IN_T>(x, n, e0, vec, v));
+            c += __popc(nz_mask8_bits<IN_T>(x, n, e0, vec, w));
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1)
@@ -196,34 +225,71 @@ __global__ void __launch_bounds__(kThreads) sparse_count_kernel(const void *__re
 }
 
 // Single block of 1024 threads: exclusive scan of the tile counts in place,
-// header {sparse?, nnz}.
+// header {sparse?, nnz}.  Each thread owns a contiguous run of counts, read
+// in batches of 8 independent loads; the runs' totals are scanned with warp
+// shuffles and one shared-memory pass over the 32 warp totals.
 __global__ void __launch_bounds__(1024) sparse_scan_kernel(uint32_t *counts, long long tiles,
                                                            long long n, double one_minus_thr,
                                                            uint32_t *hdr)
 {
-    __shared__ unsigned long long part[1024];
+    __shared__ unsigned long long wsum[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const long long per = (tiles + 1023) / 1024;
-    const long long lo = threadIdx.x * per;
+    const long long lo = min(tiles, (long long)threadIdx.x * per);
     const long long hi = min(tiles, lo + per);
     unsigned long long s = 0;
-    for (long long i = lo; i < hi; ++i)
+    long long i = lo;
+    for (; i + 8 <= hi; i += 8) {
+        uint32_t v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            v[j] = counts[i + j];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            s += v[j];
+    }
+    for (; i < hi; ++i)
         s += counts[i];
-    part[threadIdx.x] = s;
+    unsigned long long incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o)
+            incl += t;
+    }
+    if (lane == 31)
+        wsum[warp] = incl;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned long long run = 0;
-        for (int i = 0; i < 1024; ++i) {
-            const unsigned long long v = part[i];
-            part[i] = run;
-            run += v;
+    if (warp == 0) {
+        unsigned long long w = wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long t = __shfl_up_sync(kFull, w, o);
+            if (lane >= o)
+                w += t;
         }
-        const bool sparse = (double)run < one_minus_thr * (double)n;
-        hdr[0] = sparse ? 1u : 0u;
-        hdr[1] = (uint32_t)run;
+        wsum[lane] = w; // inclusive totals of warps 0..lane
     }
     __syncthreads();
-    unsigned long long run = part[threadIdx.x];
-    for (long long i = lo; i < hi; ++i) {
+    if (threadIdx.x == 0) {
+        const unsigned long long total = wsum[31];
+        hdr[0] = (double)total < one_minus_thr * (double)n ? 1u : 0u;
+        hdr[1] = (uint32_t)total;
+    }
+    unsigned long long run = (warp > 0 ? wsum[warp - 1] : 0ull) + incl - s;
+    i = lo;
+    for (; i + 8 <= hi; i += 8) {
+        uint32_t v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            v[j] = counts[i + j];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            counts[i + j] = (uint32_t)run;
+            run += v[j];
+        }
+    }
+    for (; i < hi; ++i) {
         const uint32_t v = counts[i];
         counts[i] = (uint32_t)run;
         run += v;
@@ -240,6 +306,8 @@ __global__ void __launch_bounds__(kThreads) sparse_emit_kernel(const void *__res
     using E = typename Elem<IN_T>::type;
     constexpr int es = dtype_size(IN_T);
     __shared__ uint32_t wsum[kThreads / 32];
+    __shared__ uint32_t sval[kSpTile]; // bits of the compacted values of one tile
+    __shared__ uint16_t sidx[kSpTile]; // their positions in the tile
     const bool sparse = hdr[0] != 0u;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const long long tiles = (n + kSpTile - 1) / kSpTile;
@@ -263,17 +331,17 @@ __global__ void __launch_bounds__(kThreads) sparse_emit_kernel(const void *__res
             }
             continue;
         }
-        float v[2][8];
-        uint32_t msk[2];
-        uint32_t mine = 0;
+        // compacted values and indices of the tile, staged so that they
+        // leave in consecutive, coalesced stores
+        uint32_t bits[2][8], msk[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const long long e0 = t * kSpTile + (long long)h * 2048 + 8 * threadIdx.x;
-            msk[h] = nz_mask8<IN_T>(x, n, e0, vec, v[h]);
+            msk[h] = nz_mask8_bits<IN_T>(x, n, e0, vec, bits[h]);
         }
         // order of elements in the tile: half h, thread, element -> the
         // compacted order must follow it, so scan half 0 fully before half 1
-        uint32_t base = offsets[t];
+        uint32_t local = 0; // compacted elements of the tile before this half
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const uint32_t c = __popc(msk[h]);
@@ -294,27 +362,34 @@ __global__ void __launch_bounds__(kThreads) sparse_emit_kernel(const void *__res
                     before += s;
                 total += s;
             }
-            uint32_t pos = base + before + incl - c;
-            const long long e0 = t * kSpTile + (long long)h * 2048 + 8 * threadIdx.x;
+            uint32_t pos = local + before + incl - c;
+            const int e0 = h * 2048 + 8 * (int)threadIdx.x; // within the tile
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 if ((msk[h] >> i) & 1u) {
-                    if constexpr (IN_T == kF32)
-                        reinterpret_cast<float *>(vals)[pos] = v[h][i];
-                    else
-                        reinterpret_cast<E *>(vals)[pos] = reinterpret_cast<const E *>(x)[e0 + i];
-                    idx[pos] = (int32_t)(e0 + i);
+                    sval[pos] = bits[h][i]; // the input's own bits
+                    sidx[pos] = (uint16_t)(e0 + i);
                     ++pos;
                 }
-            base += total;
-            mine += c;
-            __syncthreads();
+            local += total;
+            __syncthreads(); // wsum is reused by the next half
         }
-        (void)mine;
+        // the tile's compacted run, written with consecutive threads
+        const uint32_t base = offsets[t];
+        const long long t0 = t * kSpTile;
+        for (uint32_t k = threadIdx.x; k < local; k += kThreads) {
+            if constexpr (IN_T == kF32)
+                reinterpret_cast<uint32_t *>(vals)[base + k] = sval[k];
+            else
+                reinterpret_cast<uint16_t *>(vals)[base + k] = (uint16_t)sval[k];
+            idx[base + k] = (int32_t)(t0 + sidx[k]);
+        }
+        __syncthreads(); // the staging arrays are reused by the next tile
     }
 }
 
 // ---------------------------------------------------------------- sparse decode
+// Dense message: a streaming copy (or add) of the values into acc.
 template <int IN_T>
 __global__ void __launch_bounds__(kThreads) sparse_dense_kernel(const uint32_t *__restrict__ hdr,
                                                                 const void *__restrict__ vals,
@@ -323,7 +398,7 @@ __global__ void __launch_bounds__(kThreads) sparse_dense_kernel(const uint32_t *
 {
     constexpr int es = dtype_size(IN_T);
     const bool sparse = hdr[0] != 0u;
-    if (sparse && accumulate)
+    if (sparse) // sparse_fill_kernel or sparse_scatter_kernel restores it
         return;
     const long long groups = (n + 7) / 8;
     for (long long gi = blockIdx.x * (long long)kThreads + threadIdx.x; gi < groups;
@@ -331,31 +406,98 @@ __global__ void __launch_bounds__(kThreads) sparse_dense_kernel(const uint32_t *
         const long long e0 = gi * 8;
         const int vl = (int)min(8LL, n - e0);
         float v[8];
-        if (sparse) {
+        const char *src = reinterpret_cast<const char *>(vals) + e0 * es;
+        if (vec && vl == 8)
+            load8_vec<IN_T>(src, v);
+        else
+            load8_scalar<IN_T>(src, vl, v);
+        if (accumulate) {
+            float o[8];
+            if (vec && vl == 8)
+                load8_vec<kF32>(acc + e0, o);
+            else
+                load8_scalar<kF32>(acc + e0, vl, o);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                v[i] = 0.0f;
-        } else {
-            const char *src = reinterpret_cast<const char *>(vals) + e0 * es;
-            if (vec && vl == 8)
-                load8_vec<IN_T>(src, v);
-            else
-                load8_scalar<IN_T>(src, vl, v);
-            if (accumulate) {
-                float o[8];
-                if (vec && vl == 8)
-                    load8_vec<kF32>(acc + e0, o);
-                else
-                    load8_scalar<kF32>(acc + e0, vl, o);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    v[i] = __fadd_rn(o[i], v[i]);
-            }
+                v[i] = __fadd_rn(o[i], v[i]);
         }
         store8(acc + e0, kF32, v, vl, vec != 0);
     }
 }
 
+// Sparse message, accumulate == 0: one pass over acc in 4096-element tiles.
+// First the position in the (ascending) index list where each tile starts,
+// one binary search per tile; then every tile is built in shared memory
+// (+0.0, then its values, read with consecutive threads) and written once.
+// An index outside its tile (out of order, or outside [0, n)) is never
+// written.
+__global__ void __launch_bounds__(kThreads) sparse_tile_starts_kernel(
+    const uint32_t *__restrict__ hdr, const int32_t *__restrict__ idx, long long n,
+    uint32_t *__restrict__ start, int accumulate)
+{
+    if (hdr[0] == 0u || accumulate)
+        return;
+    const long long nnz = min((long long)hdr[1], n); // a header never lists more than n
+    const long long tiles = (n + kSpTile - 1) / kSpTile;
+    for (long long t = blockIdx.x * (long long)kThreads + threadIdx.x; t <= tiles;
+         t += (long long)gridDim.x * kThreads) {
+        long long lo = 0, hi = nnz;
+        if (t == tiles) {
+            lo = nnz;
+        } else {
+            const long long target = t * kSpTile;
+            while (lo < hi) {
+                const long long mid = (lo + hi) >> 1;
+                if ((long long)idx[mid] < target)
+                    lo = mid + 1;
+                else
+                    hi = mid;
+            }
+        }
+        start[t] = (uint32_t)lo;
+    }
+}
+
+template <int IN_T>
+__global__ void __launch_bounds__(kThreads) sparse_fill_kernel(const uint32_t *__restrict__ hdr,
+                                                               const void *__restrict__ vals,
+                                                               const int32_t *__restrict__ idx,
+                                                               const uint32_t *__restrict__ start,
+                                                               long long n, float *acc,
+                                                               int accumulate, int vec)
+{
+    using E = typename Elem<IN_T>::type;
+    __shared__ __align__(16) float tile[kSpTile];
+    if (hdr[0] == 0u || accumulate)
+        return;
+    const long long tiles = (n + kSpTile - 1) / kSpTile;
+    for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const long long t0 = t * kSpTile, t1 = min(n, t0 + kSpTile);
+        for (int i = threadIdx.x; i < kSpTile; i += kThreads)
+            tile[i] = 0.0f;
+        __syncthreads();
+        const long long kb = start[t], ke = start[t + 1];
+#pragma unroll 4
+        for (long long k = kb + threadIdx.x; k < ke; k += kThreads) {
+            const long long i = idx[k];
+            if (i >= t0 && i < t1)
+                tile[i - t0] = to_f32(reinterpret_cast<const E *>(vals)[k]);
+        }
+        __syncthreads();
+        const int len = (int)(t1 - t0);
+        if (vec && len == kSpTile) {
+            float4 *dst = reinterpret_cast<float4 *>(acc + t0);
+            for (int j = threadIdx.x; j < kSpTile / 4; j += kThreads)
+                dst[j] = reinterpret_cast<const float4 *>(tile)[j];
+        } else {
+            for (int j = threadIdx.x; j < len; j += kThreads)
+                acc[t0 + j] = tile[j];
+        }
+        __syncthreads(); // the tile is rebuilt for the next position
+    }
+}
+
+// Sparse message, accumulate != 0: acc[i] += v at the listed positions.
 template <int IN_T>
 __global__ void __launch_bounds__(kThreads) sparse_scatter_kernel(const uint32_t *__restrict__ hdr,
                                                                   const void *__restrict__ vals,
@@ -364,7 +506,7 @@ __global__ void __launch_bounds__(kThreads) sparse_scatter_kernel(const uint32_t
                                                                   int accumulate)
 {
     using E = typename Elem<IN_T>::type;
-    if (hdr[0] == 0u)
+    if (hdr[0] == 0u || !accumulate)
         return;
     const long long nnz = min((long long)hdr[1], n); // a header never lists more than n
     for (long long k = blockIdx.x * (long long)kThreads + threadIdx.x; k < nnz;
@@ -547,16 +689,53 @@ cudaError_t launch_sparse_encode(const void *x, long long n, int dtype, double o
     return cudaGetLastError();
 }
 
+// Per-device scratch of the decoder: where each tile's values start
+// (grown on demand; decodes that overlap on the GPU share it).
+std::mutex g_dec_mu;
+std::map<int, std::pair<uint32_t *, long long>> g_dec_ws;
+
 cudaError_t launch_sparse_decode(const uint32_t *hdr, const void *vals, const int32_t *idx,
                                  long long n, int dtype, float *acc, int accumulate,
                                  cudaStream_t st)
 {
+    const long long words = (n + kSpTile - 1) / kSpTile + 1;
+    uint32_t *scratch = nullptr;
+    {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess)
+            return e;
+        std::lock_guard<std::mutex> lk(g_dec_mu);
+        auto &ws = g_dec_ws[dev];
+        if (ws.second < words) {
+            if (ws.first) {
+                cudaDeviceSynchronize(); // a decode in flight may still read it
+                cudaFree(ws.first);
+                ws.first = nullptr;
+                ws.second = 0;
+            }
+            const long long want = std::max(words, 1LL << 12);
+            e = cudaMalloc(&ws.first, (size_t)want * sizeof(uint32_t));
+            if (e != cudaSuccess) {
+                ws.first = nullptr;
+                return e;
+            }
+            ws.second = want;
+        }
+        scratch = ws.first;
+    }
     const int vec = aligned16(vals) && aligned16(acc) ? 1 : 0;
     const int g1 = grid_for((n + 7) / 8, kThreads);
     const int g2 = num_sms() * 4;
+    const long long tiles = (n + kSpTile - 1) / kSpTile;
+    const int gs = (int)std::min<long long>((tiles + 1 + kThreads - 1) / kThreads, 65535);
+    const int gf = (int)std::min<long long>(tiles, (long long)num_sms() * 8);
 #define RRA_SD(T)                                                                                  \
     do {                                                                                           \
         sparse_dense_kernel<T><<<g1, kThreads, 0, st>>>(hdr, vals, n, acc, accumulate, vec);       \
+        sparse_tile_starts_kernel<<<gs, kThreads, 0, st>>>(hdr, idx, n, scratch, accumulate);      \
+        sparse_fill_kernel<T><<<gf, kThreads, 0, st>>>(hdr, vals, idx, scratch, n, acc,            \
+                                                       accumulate, vec);                           \
         sparse_scatter_kernel<T><<<g2, kThreads, 0, st>>>(hdr, vals, idx, n, acc, accumulate);     \
     } while (0)
     if (dtype == kF32) RRA_SD(kF32);

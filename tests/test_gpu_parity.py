@@ -568,6 +568,30 @@ def test_sparse_codec(dt, p_zero, thr, n):
     assert_bits_equal(host(acc), ra, "decode accumulate")
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_sparse_codec_many_tiles(dt, offset):
+    """Long inputs: every block of the encoder and the one-pass decoder walks
+    several 4096-element tiles; the decoded view may start off 16-byte
+    alignment (element-wise stores)."""
+    n = (1 << 24) + 333
+    x = W.sparse(1, n, seed=77, p_zero=0.6, dtype=TORCH_DT[dt])[0]
+    hdr = torch.zeros(2, dtype=torch.int32, device="cuda")
+    vals = torch.zeros(n, dtype=TORCH_DT[dt], device="cuda")
+    idx = torch.zeros(n, dtype=torch.int32, device="cuda")
+    rra.sparse_encode(x, 0.5, hdr, vals, idx)
+    rh, rv, ri = O.sparse_encode(host(x), dt, 0.5)
+    assert list(host(hdr).view(np.uint32)) == list(rh) and rh[0] == 1
+    k = int(rh[1])
+    assert np.array_equal(bitsof_any(host(vals)[:k]), bitsof_any(rv))
+    assert np.array_equal(host(idx)[:k], ri)
+    store = torch.full((n + offset,), 3.0, device="cuda")
+    acc = store[offset:]
+    rra.sparse_decode(hdr, vals, idx, n, acc)
+    assert_bits_equal(host(acc), O.sparse_decode(rh, rv, ri, n, dt), "decode")
+    assert float(store[0]) == 3.0 or offset == 0
+
+
 def bitsof_any(a):
     return a.view({4: np.uint32, 2: np.uint16}[a.dtype.itemsize])
 
