@@ -63,6 +63,18 @@ def test_bf16_conversion_matches_torch():
     assert np.array_equal(bits32(back), bits32((ours.astype(np.uint32) << 16).view(np.float32)))
 
 
+def test_scalar_casts_match_library_routines():
+    """The scalar fp32 -> fp16 / bf16 helpers agree with numpy's and torch's
+    round-to-nearest-even conversions, ties and overflow included."""
+    vals = [0.0, -0.0, 1.0, 65504.0, 65520.0, 2.0 ** -25, 3 * 2.0 ** -26, 1.00390625,
+            1.01171875, -3.3895314e38, 1e-40, 0.1, -7.3e-5]
+    for v in vals:
+        f = np.float32(v)
+        assert O.f32_to_f16_bits(float(f)) == int(np.array(f).astype(np.float16).view(np.uint16))
+        want = torch.tensor([f]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)[0]
+        assert O.f32_to_bf16_bits(float(f)) == int(want)
+
+
 # --------------------------------------------------------------- lossless ring
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4])
@@ -433,6 +445,10 @@ def test_bfp_golden_codes(case):
     dec = O.bfp_decode(exps, mants, len(xs), bits)
     for m, d in zip(codes, dec):
         assert d == np.float32(math.ldexp(m, e - (bits - 2)))
+    # the per-element helpers give the same codes and values one at a time
+    for v, m in zip(xs, codes):
+        assert O.bfp_code(np.float32(v), e, bits) == m
+        assert O.bfp_value(m, e, bits) == math.ldexp(m, e - (bits - 2))
 
 
 def test_bfp4_nibble_packing_by_hand():
