@@ -355,7 +355,8 @@ rra_status rra_diff_encode(const float *cur, const float *prev, float *diff, siz
  * "练习": per-rank byte counter): sent[r] / recv[r] = wire bytes rank r
  * wrote into / read from receive slots, counted on the device.  Lossless
  * ring: 2 (N-1) n * 4 bytes per rank when N divides T.  Synchronises the
- * stream of that call.  sent, recv: HOST arrays of N entries.
+ * stream of that call.  sent, recv: HOST arrays of N entries.  A call that
+ * returned an error did not launch and does not count as the last call.
  * Errors: RRA_ERR_INVALID, RRA_ERR_CUDA, or a latched device error.
  */
 rra_status rra_get_bytes(rra_comm *comm, uint64_t *sent, uint64_t *recv);

@@ -89,6 +89,15 @@ void counter_sets(rra_comm *c, unsigned long long **sent, unsigned long long **r
     c->gen++;
 }
 
+// A launch that failed cleared nothing and counted nothing: step back to the
+// previous call's set, so the next call still starts from a cleared set and
+// rra_get_bytes still reports the last launched call.
+void undo_counter_sets(rra_comm *c, int prev_set)
+{
+    c->gen--;
+    c->last_set = prev_set;
+}
+
 void note_call(rra_comm *c, cudaStream_t st)
 {
     c->last_stream = st;
@@ -408,11 +417,15 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     int per_sm = 0;
     const int grid = grid_for(comm, key, fn, warps, smem, a.tiles, t.blocks, &per_sm);
     comm->last = Tune{per_sm, a.K, a.D, groups};
+    const int prev_set = comm->last_set;
     counter_sets(comm, &a.sent, &a.recv, &a.zero);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_ring(fn, a, grid, warps, smem, st);
+    if (launch_ring(fn, a, grid, warps, smem, st) != cudaSuccess) {
+        undo_counter_sets(comm, prev_set);
+        return RRA_ERR_CUDA;
+    }
     note_call(comm, st);
-    return e == cudaSuccess ? RRA_OK : RRA_ERR_CUDA;
+    return RRA_OK;
 }
 
 // which: 0 allgather, 1 broadcast, 2 tree allreduce; bits 8 or 4: the
@@ -509,11 +522,15 @@ rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count
     const long long key = 50000 + bits * 10000 + which * 1000 + (int)es * 100 + G * 10 +
                           (fast ? 2 : 0) + (one ? 1 : 0);
     const int grid = grid_for(comm, key, fn, warps, smem, a.tiles, comm->tune.blocks);
+    const int prev_set = comm->last_set;
     counter_sets(comm, &a.sent, &a.recv, &a.zero);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = launch_coll(fn, a, grid, warps, smem, st);
+    if (launch_coll(fn, a, grid, warps, smem, st) != cudaSuccess) {
+        undo_counter_sets(comm, prev_set);
+        return RRA_ERR_CUDA;
+    }
     note_call(comm, st);
-    return e == cudaSuccess ? RRA_OK : RRA_ERR_CUDA;
+    return RRA_OK;
 }
 
 // Per-device scratch for the standalone sparse encoder (grown on demand).
