@@ -292,10 +292,12 @@ rra_status rra_bfp_decode(const int8_t *exps, const uint8_t *mants, size_t n, in
  *         values in index order.  Dense: a copy of x.
  *  idx    device, n int32 capacity.  Sparse: the nnz indices, ascending.
  * Sparse iff nnz < (1 - threshold) * n (evaluated in double).
- * Uses scratch (one uint32 per 4096 elements) from a per-device workspace
- * that the library allocates with cudaMalloc on the first call that needs
- * more than it holds (so that first call must not be made during stream
- * capture).  Errors: RRA_ERR_INVALID, RRA_ERR_NOMEM, RRA_ERR_CUDA.
+ * Uses scratch (one uint32 per 4096 elements) from a workspace per device
+ * and stream that the library allocates with cudaMalloc on the first call
+ * that needs more than it holds (so that first call must not be made during
+ * stream capture).  Encodes on different streams may overlap: each stream
+ * has its own workspace.  Errors: RRA_ERR_INVALID, RRA_ERR_NOMEM,
+ * RRA_ERR_CUDA.
  */
 rra_status rra_sparse_encode(const void *x, size_t n, rra_dtype dtype, float threshold,
                              uint32_t *hdr, void *vals, int32_t *idx, void *stream);
@@ -331,10 +333,11 @@ rra_status rra_sparse_encode_noalloc(const void *x, size_t n, rra_dtype dtype, f
  * Sparse decode into fp32 acc[0..n) (hdr, vals, idx as written by
  * rra_sparse_encode: indices ascending; the format is read on the device).
  * A sparse message without accumulation is restored in one pass over acc,
- * 4096 elements at a time, using a per-device scratch of n/4096 + 1 words
- * that the library allocates on first use and grows as needed (decodes that
- * overlap on the GPU share it); an index out of order or outside [0, n) is
- * ignored.
+ * 4096 elements at a time, using a scratch of n/4096 + 1 words per device
+ * and stream that the library allocates on first use and grows as needed
+ * (so the first call on a stream, or the first with a larger n, must not be
+ * made during stream capture; decodes on different streams may overlap);
+ * an index out of order or outside [0, n) is ignored.
  *  accumulate == 0: acc = the restored message (+0.0 where a sparse message
  *                   lists nothing).
  *  accumulate != 0: acc[i] = acc[i] + v at every position the message

@@ -689,41 +689,40 @@ cudaError_t launch_sparse_encode(const void *x, long long n, int dtype, double o
     return cudaGetLastError();
 }
 
-// Per-device scratch of the decoder: where each tile's values start
-// (grown on demand; decodes that overlap on the GPU share it).
+// Scratch of the decoder, one per (device, stream): where each tile's values
+// start.  Grown on demand; decodes on different streams never share one, and
+// the lock is held until the launches are queued, so no growth by another
+// thread frees a buffer under a launch.
 std::mutex g_dec_mu;
-std::map<int, std::pair<uint32_t *, long long>> g_dec_ws;
+std::map<std::pair<int, cudaStream_t>, std::pair<uint32_t *, long long>> g_dec_ws;
 
 cudaError_t launch_sparse_decode(const uint32_t *hdr, const void *vals, const int32_t *idx,
                                  long long n, int dtype, float *acc, int accumulate,
                                  cudaStream_t st)
 {
     const long long words = (n + kSpTile - 1) / kSpTile + 1;
-    uint32_t *scratch = nullptr;
-    {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess)
-            return e;
-        std::lock_guard<std::mutex> lk(g_dec_mu);
-        auto &ws = g_dec_ws[dev];
-        if (ws.second < words) {
-            if (ws.first) {
-                cudaDeviceSynchronize(); // a decode in flight may still read it
-                cudaFree(ws.first);
-                ws.first = nullptr;
-                ws.second = 0;
-            }
-            const long long want = std::max(words, 1LL << 12);
-            e = cudaMalloc(&ws.first, (size_t)want * sizeof(uint32_t));
-            if (e != cudaSuccess) {
-                ws.first = nullptr;
-                return e;
-            }
-            ws.second = want;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lk(g_dec_mu);
+    auto &ws = g_dec_ws[{dev, st}];
+    if (ws.second < words) {
+        if (ws.first) {
+            cudaDeviceSynchronize(); // a decode in flight may still read it
+            cudaFree(ws.first);
+            ws.first = nullptr;
+            ws.second = 0;
         }
-        scratch = ws.first;
+        const long long want = std::max(words, 1LL << 12);
+        e = cudaMalloc(&ws.first, (size_t)want * sizeof(uint32_t));
+        if (e != cudaSuccess) {
+            ws.first = nullptr;
+            return e;
+        }
+        ws.second = want;
     }
+    uint32_t *const scratch = ws.first;
     const int vec = aligned16(vals) && aligned16(acc) ? 1 : 0;
     const int g1 = grid_for((n + 7) / 8, kThreads);
     const int g2 = num_sms() * 4;

@@ -533,9 +533,12 @@ rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count
     return RRA_OK;
 }
 
-// Per-device scratch for the standalone sparse encoder (grown on demand).
+// Scratch of the standalone sparse encoder, one per (device, stream), grown
+// on demand.  Encodes on different streams never share one, and the lock is
+// held until the launches are queued, so no growth by another thread frees a
+// buffer under a launch.
 std::mutex g_ws_mu;
-std::map<int, std::pair<uint32_t *, long long>> g_ws;
+std::map<std::pair<int, cudaStream_t>, std::pair<uint32_t *, long long>> g_ws;
 
 } // namespace
 
@@ -719,28 +722,25 @@ rra_status rra_sparse_encode(const void *x, size_t n, rra_dtype dtype, float thr
     if (cudaGetDevice(&dev) != cudaSuccess)
         return RRA_ERR_CUDA;
     const long long words = sparse_encode_scratch_words((long long)n);
-    uint32_t *scratch = nullptr;
-    {
-        std::lock_guard<std::mutex> lk(g_ws_mu);
-        auto &ws = g_ws[dev];
-        if (ws.second < words) {
-            if (ws.first) {
-                cudaDeviceSynchronize();
-                cudaFree(ws.first);
-                ws.first = nullptr;
-                ws.second = 0;
-            }
-            long long want = std::max(words, 1LL << 16);
-            if (cudaMalloc(&ws.first, (size_t)want * sizeof(uint32_t)) != cudaSuccess) {
-                ws.first = nullptr;
-                return RRA_ERR_NOMEM;
-            }
-            ws.second = want;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    auto &ws = g_ws[{dev, st}];
+    if (ws.second < words) {
+        if (ws.first) {
+            cudaDeviceSynchronize(); // an encode in flight may still use it
+            cudaFree(ws.first);
+            ws.first = nullptr;
+            ws.second = 0;
         }
-        scratch = ws.first;
+        long long want = std::max(words, 1LL << 16);
+        if (cudaMalloc(&ws.first, (size_t)want * sizeof(uint32_t)) != cudaSuccess) {
+            ws.first = nullptr;
+            return RRA_ERR_NOMEM;
+        }
+        ws.second = want;
     }
     return launch_sparse_encode(x, (long long)n, dtype, 1.0 - (double)threshold, hdr, vals, idx,
-                                scratch, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+                                ws.first, st) == cudaSuccess
                ? RRA_OK
                : RRA_ERR_CUDA;
 }

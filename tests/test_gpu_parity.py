@@ -592,6 +592,35 @@ def test_sparse_codec_many_tiles(dt, offset):
     assert float(store[0]) == 3.0 or offset == 0
 
 
+def test_sparse_codec_concurrent_streams():
+    """Encodes and decodes queued on two streams without ordering between
+    them: each stream has its own scratch, so both results match the oracle."""
+    sizes = [(1 << 22) + 5, (1 << 21) + 4099]
+    xs = [W.sparse(1, n, seed=90 + i, p_zero=0.7, dtype=torch.float32)[0]
+          for i, n in enumerate(sizes)]
+    streams = [torch.cuda.Stream() for _ in sizes]
+    outs = []
+    for x, n in zip(xs, sizes):
+        outs.append((torch.zeros(2, dtype=torch.int32, device="cuda"),
+                     torch.zeros(n, device="cuda"),
+                     torch.zeros(n, dtype=torch.int32, device="cuda"),
+                     torch.full((n,), 5.0, device="cuda")))
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for x, st, (hdr, vals, idx, _) in zip(xs, streams, outs):
+            rra.sparse_encode(x, 0.5, hdr, vals, idx, stream=st)
+        for n, st, (hdr, vals, idx, acc) in zip(sizes, streams, outs):
+            rra.sparse_decode(hdr, vals, idx, n, acc, stream=st)
+    torch.cuda.synchronize()
+    for x, n, (hdr, vals, idx, acc) in zip(xs, sizes, outs):
+        rh, rv, ri = O.sparse_encode(host(x), "f32", 0.5)
+        assert list(host(hdr).view(np.uint32)) == list(rh) and rh[0] == 1
+        k = int(rh[1])
+        assert np.array_equal(host(vals)[:k].view(np.uint32), rv.view(np.uint32))
+        assert np.array_equal(host(idx)[:k], ri)
+        assert_bits_equal(host(acc), O.sparse_decode(rh, rv, ri, n, "f32"), "decode")
+
+
 def bitsof_any(a):
     return a.view({4: np.uint32, 2: np.uint16}[a.dtype.itemsize])
 
