@@ -77,8 +77,24 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* Allocation that ends the process with a message instead of returning NULL:
+ * the oracle is a test program, and running out of host memory is fatal to
+ * it.  Zero-byte requests get one byte, so a pointer is never NULL. */
+static void *xcalloc(size_t count, size_t size)
+{
+    void *p = calloc(count ? count : 1, size ? size : 1);
+    if (!p) {
+        fprintf(stderr, "oracle: out of host memory (%zu x %zu bytes)\n", count, size);
+        abort();
+    }
+    return p;
+}
+
+static void *xmalloc(size_t bytes) { return xcalloc(bytes, 1); }
 
 /* ------------------------------------------------------------------ */
 /* element types and IEEE conversions, written from the binary16 /     */
@@ -391,22 +407,22 @@ static void msg_encode(message *m, const codec_t *cd, const float *x, size_t len
     msg_free(m);
     m->len = len;
     if (cd->kind == OR_CODEC_NONE) {
-        m->f = malloc((len ? len : 1) * sizeof(float));
+        m->f = xmalloc((len ? len : 1) * sizeof(float));
         memcpy(m->f, x, len * sizeof(float));
         m->bytes = 4 * len;
     } else if (cd->kind == OR_CODEC_BFP) {
         size_t nb = (len + OR_BFP_BLOCK - 1) / OR_BFP_BLOCK;
         size_t mb = cd->bits == 8 ? len : (len + 1) / 2;
-        m->exps = malloc(nb ? nb : 1);
-        m->mants = malloc(mb ? mb : 1);
+        m->exps = xmalloc(nb ? nb : 1);
+        m->mants = xmalloc(mb ? mb : 1);
         m->nexps = nb;
         m->nmants = mb;
         oracle_bfp_encode(x, len, cd->bits, m->exps, m->mants);
         m->bytes = nb + mb;
     } else {
         /* S3: one message per slice; the receiver restores each slice */
-        m->f = calloc(len ? len : 1, sizeof(float));
-        m->there = calloc(len ? len : 1, 1);
+        m->f = xcalloc(len ? len : 1, sizeof(float));
+        m->there = xcalloc(len ? len : 1, 1);
         m->bytes = 0;
         for (size_t lo = 0; lo < len; lo += cd->slice) {
             size_t sl = len - lo < cd->slice ? len - lo : cd->slice;
@@ -437,19 +453,19 @@ static void msg_copy(message *dst, const message *src)
     *dst = *src;
     size_t len = src->len ? src->len : 1;
     if (src->f) {
-        dst->f = malloc(len * sizeof(float));
+        dst->f = xmalloc(len * sizeof(float));
         memcpy(dst->f, src->f, src->len * sizeof(float));
     }
     if (src->there) {
-        dst->there = malloc(len);
+        dst->there = xmalloc(len);
         memcpy(dst->there, src->there, src->len);
     }
     if (src->exps) {
-        dst->exps = malloc(src->nexps ? src->nexps : 1);
+        dst->exps = xmalloc(src->nexps ? src->nexps : 1);
         memcpy(dst->exps, src->exps, src->nexps);
     }
     if (src->mants) {
-        dst->mants = malloc(src->nmants ? src->nmants : 1);
+        dst->mants = xmalloc(src->nmants ? src->nmants : 1);
         memcpy(dst->mants, src->mants, src->nmants);
     }
 }
@@ -511,7 +527,7 @@ enum { OR_MODE_ALLREDUCE = 0, OR_MODE_REDUCE_SCATTER = 1 };
  * residual becomes e = u - decode(Q(u)).  e is updated in place. */
 static void msg_encode_ef(message *m, const codec_t *cd, const float *v, float *e, size_t n)
 {
-    float *u = malloc((n ? n : 1) * sizeof(float));
+    float *u = xmalloc((n ? n : 1) * sizeof(float));
     for (size_t i = 0; i < n; i++)
         u[i] = v[i] + e[i];
     msg_encode(m, cd, u, n);
@@ -539,14 +555,14 @@ int oracle_ring_ef(int mode, int N, size_t T, const void *const *in, int in_t, v
         sent[r] = recv[r] = 0;
 
     /* local working copies (D1: the ring runs on cur - prev when diffing) */
-    float **local = malloc((size_t)N * sizeof(float *));
+    float **local = xmalloc((size_t)N * sizeof(float *));
     for (int r = 0; r < N; r++) {
-        local[r] = malloc((T ? T : 1) * sizeof(float));
+        local[r] = xmalloc((T ? T : 1) * sizeof(float));
         for (size_t i = 0; i < T; i++)
             local[r][i] = diff_prev ? ((const float *)in[r])[i] - diff_prev[r][i]
                                     : load_as_f32(in[r], i, in_t);
     }
-    message *outbox = calloc((size_t)N, sizeof(message));
+    message *outbox = xcalloc((size_t)N, sizeof(message));
 
     /* ---- pass 1: reduce-scatter ---- */
     for (int s = 1; s <= N - 1; s++) {
@@ -576,13 +592,13 @@ int oracle_ring_ef(int mode, int N, size_t T, const void *const *in, int in_t, v
     }
 
     /* value each rank ends with, per element, before the epilogue */
-    float **res = malloc((size_t)N * sizeof(float *));
+    float **res = xmalloc((size_t)N * sizeof(float *));
     for (int r = 0; r < N; r++)
-        res[r] = malloc((T ? T : 1) * sizeof(float));
+        res[r] = xmalloc((T ? T : 1) * sizeof(float));
 
     /* held[r]: the codes of the chunk rank r sends at the next allgather step */
-    message *held = calloc((size_t)N, sizeof(message));
-    int *has = calloc((size_t)N * (size_t)N, sizeof(int));
+    message *held = xcalloc((size_t)N, sizeof(message));
+    int *has = xcalloc((size_t)N * (size_t)N, sizeof(int));
 
     for (int r = 0; r < N; r++) {
         size_t lo, len;
@@ -688,13 +704,13 @@ int oracle_allgather(int N, size_t T, void *const *buf, int t, uint64_t *sent, u
     for (int s = 1; s <= N - 1; s++) {
         /* every rank sends first, then every rank stores what it got */
         size_t n = (T + (size_t)N - 1) / (size_t)N;
-        char **msg = malloc((size_t)N * sizeof(char *));
+        char **msg = xmalloc((size_t)N * sizeof(char *));
         for (int r = 0; r < N; r++) {
             int c = mod((long)r - s + 1, N);
             size_t lo, len;
             chunk_range(T, N, c, &lo, &len);
             int dst = mod((long)r + 1, N);
-            msg[dst] = malloc(n * es + 1);
+            msg[dst] = xmalloc(n * es + 1);
             memcpy(msg[dst], (char *)buf[r] + lo * es, len * es);
             sent[r] += len * es;
             recv[dst] += len * es;
@@ -728,9 +744,9 @@ int oracle_allgather_codec(int N, size_t T, void *const *buf, int t, int codec, 
     for (int r = 0; r < N; r++)
         sent[r] = recv[r] = 0;
     /* held[r]: the codes rank r sends at the next step; first its own chunk */
-    message *held = calloc((size_t)N, sizeof(message));
-    message *inbox = calloc((size_t)N, sizeof(message));
-    float *x = malloc((T ? T : 1) * sizeof(float));
+    message *held = xcalloc((size_t)N, sizeof(message));
+    message *inbox = xcalloc((size_t)N, sizeof(message));
+    float *x = xmalloc((T ? T : 1) * sizeof(float));
     for (int r = 0; r < N; r++) {
         size_t lo, len;
         chunk_range(T, N, r, &lo, &len);
@@ -827,7 +843,7 @@ int oracle_broadcast_codec(int N, size_t T, void *const *buf, int t, int root, i
     codec_t cd = {OR_CODEC_BFP, bits, 0.0, 0};
     for (int r = 0; r < N; r++)
         sent[r] = recv[r] = 0;
-    float *x = malloc((T ? T : 1) * sizeof(float));
+    float *x = xmalloc((T ? T : 1) * sizeof(float));
     for (size_t i = 0; i < T; i++)
         x[i] = load_as_f32(buf[root], i, t);
     message m;
@@ -876,8 +892,8 @@ int oracle_tree_allreduce(int N, size_t T, float *const *buf, uint64_t *sent, ui
             recv[r] += 4 * T;
         }
     }
-    uint64_t *s2 = calloc((size_t)N, sizeof(uint64_t));
-    uint64_t *r2 = calloc((size_t)N, sizeof(uint64_t));
+    uint64_t *s2 = xcalloc((size_t)N, sizeof(uint64_t));
+    uint64_t *r2 = xcalloc((size_t)N, sizeof(uint64_t));
     oracle_broadcast(N, T, (void *const *)buf, OR_F32, 0, s2, r2);
     for (int r = 0; r < N; r++) {
         sent[r] += s2[r];
@@ -961,7 +977,7 @@ int oracle_codec_stats_op(int op, int root, int N, size_t T, const void *const *
         return -1;
     for (int k = 0; k < 4; k++)
         stats[k] = 0;
-    float *blk = malloc(OR_BFP_BLOCK * sizeof(float));
+    float *blk = xmalloc(OR_BFP_BLOCK * sizeof(float));
     if (op == 2) {
         stats_range(in[root], 0, T, in_t, blk, stats);
     } else {
