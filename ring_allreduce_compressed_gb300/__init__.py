@@ -80,6 +80,7 @@ def lib():
         L.rra_bfp_encode.argtypes = [vp, sz, i32, i32, vp, vp, vp]
         L.rra_bfp_decode.argtypes = [vp, vp, sz, i32, vp, i32, vp]
         L.rra_sparse_encode.argtypes = [vp, sz, i32, C.c_float, vp, vp, vp, vp]
+        L.rra_sparse_encode_noalloc.argtypes = [vp, sz, i32, C.c_float, vp, vp, vp, vp]
         L.rra_sparse_decode.argtypes = [vp, vp, vp, sz, i32, vp, i32, vp]
         L.rra_diff_encode.argtypes = [vp, vp, vp, sz, vp]
         L.rra_get_bytes.argtypes = [vp, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64)]
@@ -105,7 +106,8 @@ def lib():
                      "rra_reduce_scatter", "rra_allgather", "rra_allgather_codec", "rra_broadcast",
                      "rra_broadcast_codec",
                      "rra_tree_allreduce",
-                     "rra_bfp_encode", "rra_bfp_decode", "rra_sparse_encode", "rra_sparse_decode",
+                     "rra_bfp_encode", "rra_bfp_decode", "rra_sparse_encode",
+                     "rra_sparse_encode_noalloc", "rra_sparse_decode",
                      "rra_diff_encode", "rra_get_bytes", "rra_comm_status", "rra_set_timeout",
                      "rra_debug_withhold", "rra_comm_set_tuning", "rra_comm_last_shape",
                      "rra_autotune", "rra_allreduce_auto", "rra_set_crossover",
@@ -388,12 +390,10 @@ def sparse_encode_noalloc(x, threshold: float, hdr, vals, idx, stream=None):
     """rra_sparse_encode_noalloc: the sparse encoder without any device
     allocation (fixed in-library scratch; n <= RRA_NOALLOC_MAX_COUNT), for
     callers that cannot allocate, e.g. while a CUDA graph is being captured."""
-    f = lib().rra_sparse_encode_noalloc
-    f.argtypes = [C.c_void_p, C.c_size_t, C.c_int, C.c_float, C.c_void_p, C.c_void_p,
-                  C.c_void_p, C.c_void_p]
-    f.restype = C.c_int
-    _check(f(_dev(x, "x"), x.numel(), _dtype_code(x.dtype), threshold, _dev(hdr, "hdr"),
-             _dev(vals, "vals"), _dev(idx, "idx"), _stream(stream)), "rra_sparse_encode_noalloc")
+    _check(lib().rra_sparse_encode_noalloc(_dev(x, "x"), x.numel(), _dtype_code(x.dtype),
+                                           threshold, _dev(hdr, "hdr"), _dev(vals, "vals"),
+                                           _dev(idx, "idx"), _stream(stream)),
+           "rra_sparse_encode_noalloc")
 
 
 def sparse_decode(hdr, vals, idx, n: int, acc, accumulate: bool = False, stream=None):

@@ -41,6 +41,27 @@ def test_library_exports_every_declared_symbol(lib):
     assert not missing, missing
 
 
+def declared_arity():
+    """Parameter count of every function include/rra.h declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(rra_[a-z_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_declares_every_signature(lib):
+    """The binding gives ctypes each entry point's full signature (a missing
+    argtypes would pass 64-bit pointers and sizes as C int)."""
+    arity = declared_arity()
+    assert set(arity) == set(declared_functions())
+    for name, n in arity.items():
+        f = getattr(lib, name)
+        assert f.argtypes is not None and len(f.argtypes) == n, name
+        assert f.restype is (C.c_char_p if name == "rra_status_string" else C.c_int), name
+
+
 def test_status_strings(lib):
     assert rra.status_string(rra.RRA_OK) == "RRA_OK"
     assert rra.status_string(rra.RRA_ERR_TIMEOUT) == "RRA_ERR_TIMEOUT"
