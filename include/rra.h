@@ -138,6 +138,13 @@ typedef struct rra_comm rra_comm;
  *             on-chip shared memory of each launched block).
  *  out        receives the handle.
  * Allocates a few hundred bytes of device memory (counters, status).
+ * Threads: one communicator serves one host thread at a time (its launch
+ * caches, counter sets and last-call record have no lock); separate
+ * communicators may be driven from separate threads.  Calls on one
+ * communicator must also run in order on the GPU: each launch clears the
+ * byte counters of the next call, so two calls on different streams need
+ * an ordering between them (an event, or one stream) to count correctly.
+ * rra_get_bytes and rra_comm_status wait on the stream of the last call.
  * Errors: RRA_ERR_INVALID (bad nranks, max_count 0, NULL out, bad dtype),
  * RRA_ERR_NOMEM, RRA_ERR_CUDA.
  */
