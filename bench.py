@@ -805,14 +805,7 @@ def run_sweep(args, world, rank):
             if r_us < t_us:
                 cross = T * 4
                 break
-        L = 0
-        while (1 << L) < N:
-            L += 1
-        beta = 1.0 / (beta_gbs * 1e9)  # seconds per byte
-        model = None
-        denom = 4 * beta * (L - (N - 1) / N)
-        if N > 2 and denom > 0:
-            model = (N - 1 - L) * alpha_us * 1e-6 / denom * 4  # bytes per rank
+        model = alpha_beta_crossover(N, alpha_us, beta_gbs)
         summ = {"sweep_summary": True, "N": N,
                 "measured_crossover_bytes": cross if cross is not None else "none in range",
                 "model": {"alpha_us": alpha_us, "beta_GBps": beta_gbs,
@@ -825,6 +818,26 @@ def run_sweep(args, world, rank):
         with open(args.jsonl, "a") as f:
             for line in out:
                 f.write(json.dumps(line) + "\n")
+
+
+def alpha_beta_times(N: int, nbytes: float, alpha_us: float, beta_gbs: float):
+    """Link-model times (seconds) of the ring and the binomial tree for
+    nbytes per rank: the ring takes 2(N-1) steps of nbytes/N, the tree
+    2*ceil(log2 N) steps of the whole buffer, each step alpha + bytes/beta."""
+    L = max(N - 1, 0).bit_length()
+    a, b = alpha_us * 1e-6, 1.0 / (beta_gbs * 1e9)
+    return 2 * (N - 1) * (a + b * nbytes / N), 2 * L * (a + b * nbytes)
+
+
+def alpha_beta_crossover(N: int, alpha_us: float, beta_gbs: float):
+    """Bytes per rank at which the modelled ring and tree times are equal
+    (the ring is faster above it), or None when one is never faster (N <= 2:
+    the two schedules coincide)."""
+    L = max(N - 1, 0).bit_length()
+    slope = L - (N - 1) / N  # extra bytes/beta per byte the tree pays
+    if N <= 2 or slope <= 0:
+        return None
+    return (N - 1 - L) * alpha_us * 1e-6 * beta_gbs * 1e9 / slope
 
 
 def run_drift(args):
