@@ -43,8 +43,9 @@
  *    in the communicator and reported by rra_comm_status().
  *  - Inputs must be finite: NaN or infinity in an input is outside the
  *    contract (results unspecified, no fault).
- *  - Nothing on these paths allocates memory except rra_comm_create and the
- *    first call of rra_sparse_encode on a device (see there).
+ *  - Nothing on these paths allocates memory except rra_comm_create, and
+ *    rra_sparse_encode / rra_sparse_decode when a stream's scratch is
+ *    smaller than the call needs (its first call, or a larger n; see there).
  */
 #ifndef RRA_H
 #define RRA_H
