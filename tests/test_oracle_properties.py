@@ -5,7 +5,8 @@ force or a closed form -- never against the oracle itself.  No GPU is needed.
 Sources: "从零实现集合通信", "两趟实现 ring allreduce" (the two-pass schedule and
 its 2T(N-1)/N bytes per rank); "CCCL通信压缩库" §2.1 (block floating point with
 a shared exponent per block, sparse values + indices above a threshold) and
-its operator-aware layer (compressed allgather)."""
+its operator-aware layer (compressed allgather and broadcast) and its
+error feedback (§5: carry what one round's compression lost into the next)."""
 import math
 
 import numpy as np
@@ -113,6 +114,40 @@ def test_compressed_allgather_is_each_chunks_round_trip(N, T, seed, bits):
             assert np.array_equal(out[r][lo:hi].view(np.uint32),
                                   np.array(want, np.float32).view(np.uint32))
     assert [int(s) for s in sent] == [sum(msg) - msg[(r + 1) % N] for r in range(N)]
+
+
+@SETTINGS
+@given(N=st.integers(1, 9), T=st.integers(1, 600), pick=st.integers(0, 2 ** 20),
+       seed=st.integers(0, 2 ** 31 - 1), bits=st.sampled_from([8, 4]))
+def test_compressed_broadcast_is_the_roots_round_trip(N, T, pick, seed, bits):
+    """Every buffer, the root's included, ends with the BFP round trip of the
+    root's buffer; each non-root rank receives one message, and the root
+    sends one to each of its ceil(log2 N) children in the binomial tree."""
+    root = pick % N
+    xs = O_rand(N, T, seed)
+    out, sent, recv = O.broadcast_codec([x.copy() for x in xs], "f32", root, bits)
+    want, nb = brute.bfp_roundtrip([np.float32(v) for v in xs[root]], bits)
+    for r in range(N):
+        assert np.array_equal(out[r].view(np.uint32), np.array(want, np.float32).view(np.uint32))
+    assert [int(v) for v in recv] == [0 if r == root else nb for r in range(N)]
+    assert int(sum(sent)) == (N - 1) * nb
+    assert int(sent[root]) == brute.ceil_log2(N) * nb
+
+
+@SETTINGS
+@given(N=st.integers(1, 4), T=st.integers(1, 300), seed=st.integers(0, 2 ** 31 - 1),
+       bits=st.sampled_from([8, 4]))
+def test_error_feedback_from_zero_residual_is_the_plain_ring(N, T, seed, bits):
+    """With every residual zero, adding it changes no code (v + 0 only turns
+    -0.0 into +0.0, which encodes the same), so the first round of error
+    feedback delivers exactly the plain compressed ring's result."""
+    xs = O_rand(N, T, seed)
+    res = [np.zeros(T, np.float32) for _ in range(N)]
+    ef, s_ef, _ = O.ring([x.copy() for x in xs], codec="bfp", bits=bits, residual=res)
+    plain, s_plain, _ = O.ring([x.copy() for x in xs], codec="bfp", bits=bits)
+    for r in range(N):
+        assert np.array_equal(ef[r].view(np.uint32), plain[r].view(np.uint32))
+    assert list(s_ef) == list(s_plain)
 
 
 def O_rand(N, T, seed):
