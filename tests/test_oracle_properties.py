@@ -150,6 +150,37 @@ def test_error_feedback_from_zero_residual_is_the_plain_ring(N, T, seed, bits):
     assert list(s_ef) == list(s_plain)
 
 
+@SETTINGS
+@given(N=st.integers(1, 9), T=st.integers(1, 80), seed=st.integers(0, 2 ** 31 - 1))
+def test_tree_allreduce_equals_brute_force(N, T, seed):
+    """The binomial-tree allreduce (reduce to rank 0, then broadcast) against
+    the brute force: every buffer bit for bit, and the per-rank byte counts."""
+    xs = O_rand(N, T, seed)
+    out, sent, recv = O.tree_allreduce([x.copy() for x in xs])
+    ref, bs, br = brute.tree_allreduce([list(x) for x in xs])
+    for r in range(N):
+        assert np.array_equal(out[r].view(np.uint32), np.array(ref[r], np.float32).view(np.uint32))
+    assert [int(v) for v in sent] == bs and [int(v) for v in recv] == br
+
+
+@SETTINGS
+@given(N=st.integers(1, 5), T=st.integers(1, 64), seed=st.integers(0, 2 ** 31 - 1),
+       codec=st.sampled_from(["none", "bfp8", "sparse"]))
+def test_reduce_scatter_equals_brute_force(N, T, seed, codec):
+    """The first pass alone: chunk r of rank r's output against the brute
+    force, and the byte counts of N-1 steps."""
+    xs = O_rand(N, T, seed)
+    kind, bits = ("bfp", 8) if codec == "bfp8" else (codec, 8)
+    outs, sent, recv = O.ring([x.copy() for x in xs], codec=kind, bits=bits,
+                              mode="reduce_scatter")
+    ref, bs, br = brute.ring([list(x) for x in xs], codec=kind, bits=bits,
+                             mode="reduce_scatter")
+    for r, (lo, hi) in enumerate(brute.chunks(T, N)):
+        want = np.array(ref[r][lo:hi], np.float32)
+        assert np.array_equal(outs[r][lo:hi].view(np.uint32), want.view(np.uint32))
+    assert list(sent) == bs and list(recv) == br
+
+
 def O_rand(N, T, seed):
     rng = np.random.default_rng(seed)
     xs = []
