@@ -181,6 +181,27 @@ def test_reduce_scatter_equals_brute_force(N, T, seed, codec):
     assert list(sent) == bs and list(recv) == br
 
 
+@SETTINGS
+@given(N=st.integers(1, 5), T=st.integers(1, 300), seed=st.integers(0, 2 ** 31 - 1),
+       bits=st.sampled_from([8, 4]), average=st.booleans())
+def test_difference_ring_equals_brute_force(N, T, seed, bits, average):
+    """The ring on cur - prev with the base added back (and the average
+    taken) against the brute force, on every rank."""
+    rng = np.random.default_rng(seed)
+    prev = [(rng.standard_normal(T) * 1e-4).astype(np.float32) for _ in range(N)]
+    cur = [(p + (rng.standard_normal(T) * 1e-5).astype(np.float32)).astype(np.float32)
+           for p in prev]
+    base = (rng.standard_normal(T) * 1e-4).astype(np.float32)
+    outs, sent, _ = O.ring([c.copy() for c in cur], codec="bfp", bits=bits, diff_prev=prev,
+                           diff_base=base, average=average)
+    ref, bs, _ = brute.ring([list(c) for c in cur], codec="bfp", bits=bits,
+                            diff_prev=[list(p) for p in prev], diff_base=list(base),
+                            average=average)
+    for r in range(N):
+        assert np.array_equal(outs[r].view(np.uint32), np.array(ref[r], np.float32).view(np.uint32))
+    assert list(sent) == bs
+
+
 def O_rand(N, T, seed):
     rng = np.random.default_rng(seed)
     xs = []
