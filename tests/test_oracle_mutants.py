@@ -5,7 +5,8 @@ clamp, wrong threshold tie, wrong header size, reversed tree levels, swapped
 difference, wrong subnormal scaling in the fp16 conversion, error-feedback sign,
 owner without error feedback, flush tie in the codec statistics, wrong chunk or an
 owner that keeps its input in the compressed allgather, a root that keeps its input
-in the compressed broadcast); the mutated copy
+in the compressed broadcast, a dropped base or average in the difference epilogue,
+swapped or unsigned BFP4 nibbles); the mutated copy
 is compiled into a temporary directory and the pin suite is run against it in
 a child process.  The real oracle is never modified."""
 import os
@@ -39,6 +40,13 @@ MUTANTS = {
     "agc_recv_index": ("int c = mod((long)r - s, N);", "int c = mod((long)r - s + 1, N);", 4),
     "bcc_root_keeps_input": ("    for (int r = 0; r < N; r++)\n        for (size_t i = 0; i < T; i++) {\n            int there;",
                              "    for (int r = 0; r < N; r++)\n        for (size_t i = 0; i < T * (r != root); i++) {\n            int there;", 1),
+    "base_dropped": ("                if (diff_base)\n                    w = diff_base[i] + w;",
+                     "                if (0)\n                    w = diff_base[i] + w;", 1),
+    "average_dropped": ("                if (average)\n                    w = w / (float)N;",
+                        "                if (0)\n                    w = w / (float)N;", 1),
+    "nibble_order": ("                if (i % 2 == 0)\n                    mants[i / 2] |= nib;",
+                     "                if (i % 2 == 1)\n                    mants[i / 2] |= nib;", 1),
+    "nibble_unsigned": ("return nib >= 8 ? nib - 16 : nib;", "return nib;", 1),
     "agc_owner_keeps_input": ("/* the owner's own chunk becomes the decoded codes as well */\n    for (int r = 0; r < N; r++) {",
                               "/* the owner's own chunk becomes the decoded codes as well */\n    for (int r = 0; r < 0; r++) {", 1),
 }
