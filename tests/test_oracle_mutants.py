@@ -6,7 +6,7 @@ difference, wrong subnormal scaling in the fp16 conversion, error-feedback sign,
 owner without error feedback, flush tie in the codec statistics, wrong chunk or an
 owner that keeps its input in the compressed allgather, a root that keeps its input
 in the compressed broadcast, a dropped base or average in the difference epilogue,
-swapped or unsigned BFP4 nibbles); the mutated copy
+swapped or unsigned BFP4 nibbles, -0.0 taken for a zero); the mutated copy
 is compiled into a temporary directory and the pin suite is run against it in
 a child process.  The real oracle is never modified."""
 import os
@@ -47,6 +47,8 @@ MUTANTS = {
     "nibble_order": ("                if (i % 2 == 0)\n                    mants[i / 2] |= nib;",
                      "                if (i % 2 == 1)\n                    mants[i / 2] |= nib;", 1),
     "nibble_unsigned": ("return nib >= 8 ? nib - 16 : nib;", "return nib;", 1),
+    "minus_zero_is_zero": ("    memcpy(&u, &v, 4);\n    return u != 0u;",
+                           "    memcpy(&u, &v, 4);\n    return (u << 1) != 0u;", 1),
     "agc_owner_keeps_input": ("/* the owner's own chunk becomes the decoded codes as well */\n    for (int r = 0; r < N; r++) {",
                               "/* the owner's own chunk becomes the decoded codes as well */\n    for (int r = 0; r < 0; r++) {", 1),
 }
