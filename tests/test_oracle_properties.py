@@ -202,11 +202,36 @@ def test_difference_ring_equals_brute_force(N, T, seed, bits, average):
     assert list(sent) == bs
 
 
-def O_rand(N, T, seed):
+@SETTINGS
+@given(N=st.integers(1, 5), T=st.integers(1, 700), seed=st.integers(0, 2 ** 31 - 1),
+       op=st.sampled_from(["allreduce", "allgather", "broadcast"]), pick=st.integers(0, 99))
+def test_codec_statistics_equal_brute_force(N, T, seed, op, pick):
+    """The statistics behind the adaptive codec choice, per operation,
+    against the brute force over exactly the elements that operation
+    encodes (all chunks of all buffers; chunk r of buffer r; the root's
+    buffer as one message)."""
+    xs = O_rand(N, T, seed, tiny=True)
+    root = pick % N
+    got = [int(v) for v in O.codec_stats_op([x.copy() for x in xs], "f32", op, root)]
+    if op == "allreduce":
+        want = brute.codec_stats([list(x) for x in xs])
+    elif op == "broadcast":
+        want = brute.codec_stats([list(xs[root])])
+    else:
+        want = [0, 0, 0, 0]
+        for r, (lo, hi) in enumerate(brute.chunks(T, N)):
+            part = brute.codec_stats([list(xs[r][lo:hi])]) if hi > lo else [0, 0, 0, 0]
+            want = [a + b for a, b in zip(want, part)]
+    assert got == want
+
+
+def O_rand(N, T, seed, tiny=False):
     rng = np.random.default_rng(seed)
     xs = []
     for _ in range(N):
-        x = rng.standard_normal(T) * 10.0 ** rng.integers(-3, 3, T).astype(np.float64)
+        # tiny: magnitudes over 12 decades, so that blocks flush small elements
+        span = 6 if tiny else 3
+        x = rng.standard_normal(T) * 10.0 ** rng.integers(-span, span, T).astype(np.float64)
         x[rng.random(T) < 0.3] = 0.0
         xs.append(x.astype(np.float32))
     return xs
