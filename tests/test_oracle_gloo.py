@@ -1,10 +1,11 @@
-"""Pin the lossless oracle against torch.distributed's gloo allreduce, the
-check the collective ops lesson itself prescribes ("用 gloo 来验证": compare
-each primitive with gloo at the same world size on the same tensor, fail above
-float32 epsilon).  gloo sums in its own order, so the comparison allows the
-recursive-summation bound (N-1) u sum|x| on each element; gloo's broadcast
-and allgather are exact and are compared bit for bit.  World sizes 2 and 4,
-CPU processes, 127.0.0.1 rendezvous."""
+"""Pin the lossless oracle against torch.distributed's gloo collectives, the
+check the collective-ops lesson ("从零实现集合通信") itself suggests: run each
+primitive through gloo at the same world size on the same tensor and fail
+above float32 epsilon.  gloo sums in its own order, so the comparison allows
+the recursive-summation bound (N-1) u sum|x| on each element.  gloo's
+broadcast and allgather are exact and are compared bit for bit, and so is the
+compressed allgather against gloo gathering each chunk's BFP8 round trip.
+World sizes 2 and 4, CPU processes, 127.0.0.1 rendezvous."""
 import math
 import os
 import socket
@@ -15,6 +16,7 @@ import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
+import brute
 import oracle as O
 
 U = 2.0 ** -24
@@ -39,7 +41,12 @@ def _worker(rank, world, port, xs, q):
     parts = [torch.empty(xs[0].size // world, dtype=torch.float32) for _ in range(world)]
     n = xs[0].size // world
     dist.all_gather(parts, torch.from_numpy(xs[rank][rank * n:(rank + 1) * n].copy()))
-    q.put((rank, t.numpy(), b.numpy(), torch.cat(parts).numpy()))
+    # compressed allgather: each rank's chunk goes through the BFP8 round trip
+    # (the brute force's restatement of the codec) before gloo gathers it
+    rt, _ = brute.bfp_roundtrip([np.float32(v) for v in xs[rank][rank * n:(rank + 1) * n]], 8)
+    cparts = [torch.empty(n, dtype=torch.float32) for _ in range(world)]
+    dist.all_gather(cparts, torch.tensor(rt, dtype=torch.float32))
+    q.put((rank, t.numpy(), b.numpy(), torch.cat(parts).numpy(), torch.cat(cparts).numpy()))
     dist.barrier()
     dist.destroy_process_group()
 
@@ -63,10 +70,12 @@ def test_lossless_ops_agree_with_gloo(world):
     X = np.stack(xs).astype(np.float64)
     bound = (world - 1) * U * np.abs(X).sum(0) * (1 + 1e-6)
     exact = np.array([math.fsum(X[:, i]) for i in range(T)])
-    for rank, red, bc, ag in got:
+    for rank, red, bc, ag, cag in got:
         assert (np.abs(red.astype(np.float64) - ours[rank].astype(np.float64)) <= 2 * bound).all()
         assert (np.abs(ours[rank].astype(np.float64) - exact) <= bound).all()
         bufs, _, _ = O.broadcast([x.copy() for x in xs], "f32", root=world - 1)
         assert np.array_equal(bufs[rank].view(np.uint32), bc.view(np.uint32))
         gbufs, _, _ = O.allgather([x.copy() for x in xs], "f32")
         assert np.array_equal(gbufs[rank].view(np.uint32), ag.view(np.uint32))
+        cbufs, _, _ = O.allgather_codec([x.copy() for x in xs], "f32", "bfp", 8)
+        assert np.array_equal(cbufs[rank].view(np.uint32), cag.view(np.uint32))
