@@ -36,9 +36,10 @@ DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
 NP_DTYPES = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}
 CODECS = {"none": 0, "bfp": 1, "sparse": 2}
 BFP_BLOCK = 128
-# Elements per ring message slice for the sparse codec: the ring streams every
-# chunk as consecutive messages of at most this many elements, each with its
-# own header and its own sparse/dense decision.
+# Sparse codec message granularity (reading S3).  slice=None (the default):
+# one message per ring chunk and hop, its format chosen from the nonzero count
+# of the whole chunk.  slice=RING_SLICE: the per-slice option, one message per
+# 256 elements, each with its own header and its own sparse/dense decision.
 RING_SLICE = 256
 
 
@@ -137,10 +138,12 @@ def _counters(N):
 # ---------------------------------------------------------------------------
 
 def ring(inputs, in_dtype="f32", out_dtype="f32", codec="none", bits=8, threshold=0.5,
-         slice=RING_SLICE, diff_prev=None, diff_base=None, average=False,
+         slice=None, diff_prev=None, diff_base=None, average=False,
          mode="allreduce", outputs=None, residual=None):
     """Two-pass ring allreduce (mode="allreduce") or its first pass alone
     (mode="reduce_scatter") over N host arrays.  Returns (outputs, sent, recv).
+    ``slice``: sparse codec only -- None for one message per chunk and hop,
+    else the elements of each per-slice message.
 
     For reduce_scatter only chunk r of outputs[r] is written; pass ``outputs``
     to control what the other chunks hold (default: zeros).  ``residual``:
@@ -167,7 +170,7 @@ def ring(inputs, in_dtype="f32", out_dtype="f32", codec="none", bits=8, threshol
     sent, recv = _counters(N)
     rc = lib().oracle_ring_ef({"allreduce": 0, "reduce_scatter": 1}[mode], N, T, _ptrs(inputs),
                               DTYPES[in_dtype], _ptrs(outputs), DTYPES[out_dtype], CODECS[codec],
-                              bits, float(threshold), slice,
+                              bits, float(threshold), int(slice or 0),
                               C.cast(dp, C.c_void_p) if dp is not None else None, db,
                               int(bool(average)), C.cast(rp, C.c_void_p) if rp is not None else None,
                               sent, recv)
@@ -213,14 +216,15 @@ def allgather(bufs, dtype="f32"):
     return bufs, np.array(sent[:], np.uint64), np.array(recv[:], np.uint64)
 
 
-def allgather_codec(bufs, dtype="f32", codec="bfp", bits=8, threshold=0.5, slice=RING_SLICE):
+def allgather_codec(bufs, dtype="f32", codec="bfp", bits=8, threshold=0.5, slice=None):
     """In-place compressed allgather (reading AG): chunk r of bufs[r] is rank
-    r's contribution; every buffer ends with decode(codes) of every chunk."""
+    r's contribution; every buffer ends with decode(codes) of every chunk.
+    ``slice`` as for ``ring``."""
     N, T = len(bufs), bufs[0].size
     _check(bufs, T, dtype)
     sent, recv = _counters(N)
     if lib().oracle_allgather_codec(N, T, _ptrs(bufs), DTYPES[dtype], CODECS[codec], bits,
-                                    float(threshold), slice, sent, recv) != 0:
+                                    float(threshold), int(slice or 0), sent, recv) != 0:
         raise ValueError("oracle_allgather_codec: bad arguments")
     return bufs, np.array(sent[:], np.uint64), np.array(recv[:], np.uint64)
 

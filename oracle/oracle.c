@@ -42,12 +42,17 @@
  *      unchanged; every rank (owner included) outputs decode(codes).
  *  S1  an element is "zero" iff its fp32 bit pattern is +0.0.
  *  S2  sparse iff nnz < (1 - threshold) * len (in double); tie -> dense.
- *  S3  ring messages are cut into slices of `slice` elements; each slice is
- *      one message: 8-byte header {fmt, nnz}, then fp32 values[nnz] and
- *      int32 slice-relative indices[nnz] ascending (sparse), or fp32[len]
- *      (dense).
- *  S4  sparse accumulate: acc[i] = acc[i] + v at listed positions; other
- *      positions keep acc[i].
+ *  S3  the sparse codec sends one message per ring chunk and hop (slice 0:
+ *      the format is chosen from the nonzero count of the whole chunk's
+ *      partial, as [P4] §2.1 analyses the sparsity of the tensor about to
+ *      be sent), or, as an option, one message per slice of `slice`
+ *      elements.  A message is an 8-byte header {fmt, nnz}, then fp32
+ *      values[nnz] and int32 indices[nnz] ascending, relative to the
+ *      message start (sparse), or fp32[len] (dense).
+ *  S4  decompress, then reduce ([P4] §2.2: receive, decompress, reduce;
+ *      §2.1: the receiver restores the nonzero values to their positions by
+ *      index): a sparse message is restored into a piece of +0.0 values,
+ *      and the receiver adds the whole restored piece, acc[i] = acc[i] + v.
  *  D1  diff: d = cur - prev (fp32); the ring runs on d.
  *  D2  epilogue: out = base + (v / N) when a base (previous result) is given
  *      and averaging is on; v / N with averaging only; v otherwise.
@@ -378,14 +383,13 @@ typedef struct {
     int kind;         /* codec */
     int bits;         /* bfp */
     double threshold; /* sparse */
-    size_t slice;     /* sparse message slice length */
+    size_t slice;     /* sparse: elements per message; 0 = one message per chunk */
 } codec_t;
 
 typedef struct {
     size_t len;     /* elements covered */
     size_t bytes;   /* wire size */
-    float *f;       /* NONE: fp32 values; SPARSE: restored values (+0 if absent) */
-    uint8_t *there; /* SPARSE: 1 where the message carries a value */
+    float *f;       /* NONE: fp32 values; SPARSE: restored values (+0.0 where none) */
     int8_t *exps;   /* BFP */
     uint8_t *mants; /* BFP */
     size_t nexps;   /* BFP: ceil(len/128) */
@@ -395,7 +399,6 @@ typedef struct {
 static void msg_free(message *m)
 {
     free(m->f);
-    free(m->there);
     free(m->exps);
     free(m->mants);
     memset(m, 0, sizeof *m);
@@ -420,30 +423,37 @@ static void msg_encode(message *m, const codec_t *cd, const float *x, size_t len
         oracle_bfp_encode(x, len, cd->bits, m->exps, m->mants);
         m->bytes = nb + mb;
     } else {
-        /* S3: one message per slice; the receiver restores each slice */
+        /* S3: the chunk's message (slice 0), or one message per slice.
+         * The sender lists the nonzero values and their indices (S1); the
+         * message is sparse iff S2 holds for its length.  The receiver's
+         * restored copy (S4) is built from what is sent: the listed values
+         * put back by index into zeros, or the dense values. */
+        const size_t step = cd->slice ? cd->slice : (len ? len : 1);
+        float *pv = xmalloc((len ? len : 1) * sizeof(float));
+        int32_t *pi = xmalloc((len ? len : 1) * sizeof(int32_t));
         m->f = xcalloc(len ? len : 1, sizeof(float));
-        m->there = xcalloc(len ? len : 1, 1);
         m->bytes = 0;
-        for (size_t lo = 0; lo < len; lo += cd->slice) {
-            size_t sl = len - lo < cd->slice ? len - lo : cd->slice;
+        for (size_t lo = 0; lo < len; lo += step) {
+            size_t sl = len - lo < step ? len - lo : step;
             size_t nnz = 0;
             for (size_t i = lo; i < lo + sl; i++)
-                nnz += is_nonzero(x[i]);
+                if (is_nonzero(x[i])) {
+                    pv[nnz] = x[i];
+                    pi[nnz] = (int32_t)(i - lo);
+                    nnz++;
+                }
             if (oracle_sparse_is_sparse(nnz, sl, cd->threshold)) {
-                for (size_t i = lo; i < lo + sl; i++)
-                    if (is_nonzero(x[i])) {
-                        m->f[i] = x[i];
-                        m->there[i] = 1;
-                    }
+                for (size_t k = 0; k < nnz; k++)
+                    m->f[lo + (size_t)pi[k]] = pv[k];
                 m->bytes += 8 + 8 * nnz;
             } else {
-                for (size_t i = lo; i < lo + sl; i++) {
+                for (size_t i = lo; i < lo + sl; i++)
                     m->f[i] = x[i];
-                    m->there[i] = 1;
-                }
                 m->bytes += 8 + 4 * sl;
             }
         }
+        free(pv);
+        free(pi);
     }
 }
 
@@ -456,10 +466,6 @@ static void msg_copy(message *dst, const message *src)
         dst->f = xmalloc(len * sizeof(float));
         memcpy(dst->f, src->f, src->len * sizeof(float));
     }
-    if (src->there) {
-        dst->there = xmalloc(len);
-        memcpy(dst->there, src->there, src->len);
-    }
     if (src->exps) {
         dst->exps = xmalloc(src->nexps ? src->nexps : 1);
         memcpy(dst->exps, src->exps, src->nexps);
@@ -470,16 +476,13 @@ static void msg_copy(message *dst, const message *src)
     }
 }
 
-/* Decoded value of element i and whether the message carries it. */
-static float msg_value(const message *m, const codec_t *cd, size_t i, int *there)
+/* Decoded value of element i of a message (sparse: its restored value,
+ * +0.0 where the message lists nothing). */
+static float msg_value(const message *m, const codec_t *cd, size_t i)
 {
-    *there = 1;
-    if (cd->kind == OR_CODEC_NONE)
-        return m->f[i];
     if (cd->kind == OR_CODEC_BFP)
         return oracle_bfp_value(bfp_code_at(m->mants, i, cd->bits), m->exps[i / OR_BFP_BLOCK],
                                 cd->bits);
-    *there = m->there[i];
     return m->f[i];
 }
 
@@ -532,9 +535,8 @@ static void msg_encode_ef(message *m, const codec_t *cd, const float *v, float *
         u[i] = v[i] + e[i];
     msg_encode(m, cd, u, n);
     for (size_t i = 0; i < n; i++) {
-        int there;
-        const float d = msg_value(m, cd, i, &there);
-        e[i] = u[i] - (there ? d : 0.0f);
+        const float d = msg_value(m, cd, i);
+        e[i] = u[i] - d;
     }
     free(u);
 }
@@ -547,8 +549,6 @@ int oracle_ring_ef(int mode, int N, size_t T, const void *const *in, int in_t, v
     if (N < 1 || (codec == OR_CODEC_BFP && bits != 8 && bits != 4) || (diff_prev && in_t != OR_F32))
         return -1;
     if (resid && codec != OR_CODEC_BFP) /* only a lossy codec has an error to feed back */
-        return -1;
-    if (codec == OR_CODEC_SPARSE && slice == 0)
         return -1;
     codec_t cd = {codec, bits, threshold, slice};
     for (int r = 0; r < N; r++)
@@ -583,10 +583,8 @@ int oracle_ring_ef(int mode, int N, size_t T, const void *const *in, int in_t, v
             size_t lo, len;
             chunk_range(T, N, c, &lo, &len);
             for (size_t i = 0; i < len; i++) {
-                int there;
-                float v = msg_value(&outbox[r], &cd, i, &there);
-                if (there) /* S4 */
-                    local[r][lo + i] = local[r][lo + i] + v;
+                float v = msg_value(&outbox[r], &cd, i);
+                local[r][lo + i] = local[r][lo + i] + v; /* S4 */
             }
         }
     }
@@ -615,9 +613,7 @@ int oracle_ring_ef(int mode, int N, size_t T, const void *const *in, int in_t, v
                 msg_encode(&held[r], &cd, local[r] + lo, len);
             if (codec != OR_CODEC_NONE)
                 for (size_t i = 0; i < len; i++) {
-                    int there;
-                    float v = msg_value(&held[r], &cd, i, &there);
-                    res[r][lo + i] = there ? v : 0.0f;
+                    res[r][lo + i] = msg_value(&held[r], &cd, i);
                 }
         }
         has[r * N + r] = 1;
@@ -637,9 +633,7 @@ int oracle_ring_ef(int mode, int N, size_t T, const void *const *in, int in_t, v
                 size_t lo, len;
                 chunk_range(T, N, c, &lo, &len);
                 for (size_t i = 0; i < len; i++) {
-                    int there;
-                    float v = msg_value(&outbox[r], &cd, i, &there);
-                    res[r][lo + i] = there ? v : 0.0f;
+                    res[r][lo + i] = msg_value(&outbox[r], &cd, i);
                 }
                 msg_copy(&held[r], &outbox[r]);
                 has[r * N + c] = 1;
@@ -729,16 +723,15 @@ int oracle_allgather(int N, size_t T, void *const *buf, int t, uint64_t *sent, u
 }
 
 /* Compressed allgather (reading AG), in place: chunk r of buf[r] is rank
- * r's contribution; codec BFP (bits 8 or 4) or sparse (threshold, slices of
- * `slice` elements).  Rank r sends at allgather step s the codes of chunk
- * (r - s + 1) mod N, so it forwards every chunk but chunk r + 1; the byte
- * counters add the message bytes. */
+ * r's contribution; codec BFP (bits 8 or 4) or sparse (threshold; one
+ * message per chunk, or per slice of `slice` elements, S3).  Rank r sends
+ * at allgather step s the codes of chunk (r - s + 1) mod N, so it forwards
+ * every chunk but chunk r + 1; the byte counters add the message bytes. */
 int oracle_allgather_codec(int N, size_t T, void *const *buf, int t, int codec, int bits,
                            double threshold, size_t slice, uint64_t *sent, uint64_t *recv)
 {
     if (N < 1 || (codec != OR_CODEC_BFP && codec != OR_CODEC_SPARSE) ||
-        (codec == OR_CODEC_BFP && bits != 8 && bits != 4) ||
-        (codec == OR_CODEC_SPARSE && slice == 0))
+        (codec == OR_CODEC_BFP && bits != 8 && bits != 4))
         return -1;
     codec_t cd = {codec, bits, threshold, slice};
     for (int r = 0; r < N; r++)
@@ -759,9 +752,7 @@ int oracle_allgather_codec(int N, size_t T, void *const *buf, int t, int codec, 
         size_t lo, len;
         chunk_range(T, N, r, &lo, &len);
         for (size_t i = 0; i < len; i++) {
-            int there;
-            float v = msg_value(&held[r], &cd, i, &there);
-            store_from_f32(buf[r], lo + i, t, there ? v : 0.0f);
+            store_from_f32(buf[r], lo + i, t, msg_value(&held[r], &cd, i));
         }
     }
     for (int s = 1; s <= N - 1; s++) {
@@ -776,9 +767,7 @@ int oracle_allgather_codec(int N, size_t T, void *const *buf, int t, int codec, 
             size_t lo, len;
             chunk_range(T, N, c, &lo, &len);
             for (size_t i = 0; i < len; i++) {
-                int there;
-                float v = msg_value(&inbox[r], &cd, i, &there);
-                store_from_f32(buf[r], lo + i, t, there ? v : 0.0f);
+                store_from_f32(buf[r], lo + i, t, msg_value(&inbox[r], &cd, i));
             }
             msg_copy(&held[r], &inbox[r]);
         }
@@ -860,11 +849,8 @@ int oracle_broadcast_codec(int N, size_t T, void *const *buf, int t, int root, i
         }
     }
     for (int r = 0; r < N; r++)
-        for (size_t i = 0; i < T; i++) {
-            int there;
-            float v = msg_value(&m, &cd, i, &there);
-            store_from_f32(buf[r], i, t, there ? v : 0.0f);
-        }
+        for (size_t i = 0; i < T; i++)
+            store_from_f32(buf[r], i, t, msg_value(&m, &cd, i));
     msg_free(&m);
     free(x);
     return 0;

@@ -62,26 +62,31 @@ def bfp_roundtrip(vals, bits):
     return out, nbytes
 
 
-def sparse_roundtrip(vals, threshold, slice_len):
-    """Returns (restored values, carried flags, wire bytes) for one message."""
-    out, there, nbytes = [], [], 0
-    for lo in range(0, len(vals), slice_len):
-        sl = vals[lo:lo + slice_len]
-        nnz = sum(1 for v in sl if nonzero(v))
-        if nnz < (1.0 - threshold) * len(sl):
-            out += [v if nonzero(v) else F(0.0) for v in sl]
-            there += [nonzero(v) for v in sl]
-            nbytes += 8 + 8 * nnz
+def sparse_roundtrip(vals, threshold, slice_len=None):
+    """Returns (restored values, wire bytes) of one chunk's message: one
+    message for the whole list (slice_len None) or one per slice_len
+    elements.  A sparse message lists (value, index) pairs; the receiver
+    puts the values back by index into zeros."""
+    out, nbytes = [], 0
+    step = slice_len or max(len(vals), 1)
+    for lo in range(0, len(vals), step):
+        sl = vals[lo:lo + step]
+        pairs = [(v, i) for i, v in enumerate(sl) if nonzero(v)]
+        if len(pairs) < (1.0 - threshold) * len(sl):
+            piece = [F(0.0)] * len(sl)
+            for v, i in pairs:
+                piece[i] = v
+            out += piece
+            nbytes += 8 + 8 * len(pairs)
         else:
             out += list(sl)
-            there += [True] * len(sl)
             nbytes += 8 + 4 * len(sl)
-    return out, there, nbytes
+    return out, nbytes
 
 
 # ---------------------------------------------------------------- ring
 
-def ring(xs, codec="none", bits=8, threshold=0.5, slice_len=256, mode="allreduce",
+def ring(xs, codec="none", bits=8, threshold=0.5, slice_len=None, mode="allreduce",
          diff_prev=None, diff_base=None, average=False, residual=None):
     """xs: list of N lists of float32 scalars.  Returns (results, sent, recv)
     where results[r] is a list with None at chunks rank r does not produce.
@@ -96,11 +101,11 @@ def ring(xs, codec="none", bits=8, threshold=0.5, slice_len=256, mode="allreduce
     sent, recv = [0] * N, [0] * N
 
     def encode(vals):
+        """(decoded values, wire bytes) of one message"""
         if codec == "none":
-            return list(vals), [True] * len(vals), 4 * len(vals)
+            return list(vals), 4 * len(vals)
         if codec == "bfp":
-            out, nb = bfp_roundtrip(vals, bits)
-            return out, [True] * len(vals), nb
+            return bfp_roundtrip(vals, bits)
         return sparse_roundtrip(vals, threshold, slice_len)
 
     def encode_at(r, lo, hi, vals):
@@ -109,7 +114,7 @@ def ring(xs, codec="none", bits=8, threshold=0.5, slice_len=256, mode="allreduce
         u = [F(v + residual[r][lo + k]) for k, v in enumerate(vals)]
         msg = encode(u)
         for k in range(hi - lo):
-            residual[r][lo + k] = F(u[k] - (msg[0][k] if msg[1][k] else F(0.0)))
+            residual[r][lo + k] = F(u[k] - msg[0][k])
         return msg
 
     for s in range(1, N):
@@ -117,14 +122,13 @@ def ring(xs, codec="none", bits=8, threshold=0.5, slice_len=256, mode="allreduce
         for r in range(N):
             lo, hi = ch[(r - s) % N]
             inbox[(r + 1) % N] = encode_at(r, lo, hi, local[r][lo:hi])
-            sent[r] += inbox[(r + 1) % N][2]
-            recv[(r + 1) % N] += inbox[(r + 1) % N][2]
+            sent[r] += inbox[(r + 1) % N][1]
+            recv[(r + 1) % N] += inbox[(r + 1) % N][1]
         for r in range(N):
             lo, hi = ch[(r - s - 1) % N]
-            vals, there, _ = inbox[r]
-            for i in range(lo, hi):
-                if there[i - lo]:
-                    local[r][i] = F(local[r][i] + vals[i - lo])
+            vals, _ = inbox[r]
+            for i in range(lo, hi):  # decompressed message added element by element
+                local[r][i] = F(local[r][i] + vals[i - lo])
 
     res = [[None] * T for _ in range(N)]
     held = [None] * N
@@ -137,19 +141,19 @@ def ring(xs, codec="none", bits=8, threshold=0.5, slice_len=256, mode="allreduce
             held[r] = encode_at(r, lo, hi, local[r][lo:hi])
             if codec != "none":
                 for i in range(lo, hi):
-                    res[r][i] = held[r][0][i - lo] if held[r][1][i - lo] else F(0.0)
+                    res[r][i] = held[r][0][i - lo]
     if mode == "allreduce":
         for s in range(1, N):
             inbox = [None] * N
             for r in range(N):
                 inbox[(r + 1) % N] = held[r]
-                sent[r] += held[r][2]
-                recv[(r + 1) % N] += held[r][2]
+                sent[r] += held[r][1]
+                recv[(r + 1) % N] += held[r][1]
             for r in range(N):
                 lo, hi = ch[(r - s) % N]
-                vals, there, _ = inbox[r]
+                vals, _ = inbox[r]
                 for i in range(lo, hi):
-                    res[r][i] = vals[i - lo] if there[i - lo] else F(0.0)
+                    res[r][i] = vals[i - lo]
                 held[r] = inbox[r]
     for r in range(N):
         for i in range(T):
@@ -235,7 +239,7 @@ def allgather(bufs, elem_bytes):
     return bufs, sent, recv
 
 
-def allgather_codec(xs, codec="bfp", bits=8, threshold=0.5, slice_len=256):
+def allgather_codec(xs, codec="bfp", bits=8, threshold=0.5, slice_len=None):
     """Compressed allgather of N lists of float32 scalars: the owner of chunk
     c encodes its own elements once, the codes travel the ring unchanged, and
     every rank (owner included) holds the decoded chunk.  Returns (results,
@@ -249,7 +253,7 @@ def allgather_codec(xs, codec="bfp", bits=8, threshold=0.5, slice_len=256):
         if codec == "bfp":
             out, nb = bfp_roundtrip(vals, bits)
         else:
-            out, _, nb = sparse_roundtrip(vals, threshold, slice_len)
+            out, nb = sparse_roundtrip(vals, threshold, slice_len)
         held.append((out, nb))
     res = [[F(v) for v in x] for x in xs]
     for r in range(N):

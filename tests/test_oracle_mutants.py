@@ -6,7 +6,9 @@ difference, wrong subnormal scaling in the fp16 conversion, error-feedback sign,
 owner without error feedback, flush tie in the codec statistics, wrong chunk or an
 owner that keeps its input in the compressed allgather, a root that keeps its input
 in the compressed broadcast, a dropped base or average in the difference epilogue,
-swapped or unsigned BFP4 nibbles, -0.0 taken for a zero); the mutated copy
+swapped or unsigned BFP4 nibbles, -0.0 taken for a zero, a chunk's sparse
+message cut into 256-element pieces, sparse values restored at the wrong
+index, a receiver that adds only nonzero message values); the mutated copy
 is compiled into a temporary directory and the pin suite is run against it in
 a child process.  The real oracle is never modified."""
 import os
@@ -33,13 +35,13 @@ MUTANTS = {
     "diff_sign": ("((const float *)in[r])[i] - diff_prev[r][i]", "diff_prev[r][i] - ((const float *)in[r])[i]", 1),
     "average_by_reciprocal": ("w = w / (float)N;", "w = w * (1.0f / (float)N);", 1),
     "f16_subnormal_scale": ("float q = nearbyintf(ldexpf(a, 24));", "float q = nearbyintf(ldexpf(a, 23));", 1),
-    "ef_residual_sign": ("e[i] = u[i] - (there ? d : 0.0f);", "e[i] = (there ? d : 0.0f) - u[i];", 1),
+    "ef_residual_sign": ("e[i] = u[i] - d;", "e[i] = d - u[i];", 1),
     "stats_flush_tie": ("if (fabsf(blk[i]) <= ldexpf(1.0f, e - 7))", "if (fabsf(blk[i]) < ldexpf(1.0f, e - 7))", 1),
     "ef_owner_skipped": ("            if (resid)\n                msg_encode_ef(&held[r]",
                          "            if (0)\n                msg_encode_ef(&held[r]", 1),
     "agc_recv_index": ("int c = mod((long)r - s, N);", "int c = mod((long)r - s + 1, N);", 4),
-    "bcc_root_keeps_input": ("    for (int r = 0; r < N; r++)\n        for (size_t i = 0; i < T; i++) {\n            int there;",
-                             "    for (int r = 0; r < N; r++)\n        for (size_t i = 0; i < T * (r != root); i++) {\n            int there;", 1),
+    "bcc_root_keeps_input": ("    for (int r = 0; r < N; r++)\n        for (size_t i = 0; i < T; i++)\n            store_from_f32(buf[r], i, t, msg_value(&m, &cd, i));",
+                             "    for (int r = 0; r < N; r++)\n        for (size_t i = 0; i < T * (r != root); i++)\n            store_from_f32(buf[r], i, t, msg_value(&m, &cd, i));", 1),
     "base_dropped": ("                if (diff_base)\n                    w = diff_base[i] + w;",
                      "                if (0)\n                    w = diff_base[i] + w;", 1),
     "average_dropped": ("                if (average)\n                    w = w / (float)N;",
@@ -49,6 +51,11 @@ MUTANTS = {
     "nibble_unsigned": ("return nib >= 8 ? nib - 16 : nib;", "return nib;", 1),
     "minus_zero_is_zero": ("    memcpy(&u, &v, 4);\n    return u != 0u;",
                            "    memcpy(&u, &v, 4);\n    return (u << 1) != 0u;", 1),
+    "sparse_chunk_cut_in_slices": ("const size_t step = cd->slice ? cd->slice : (len ? len : 1);",
+                                   "const size_t step = cd->slice ? cd->slice : 256;", 1),
+    "sparse_restored_at_wrong_index": ("m->f[lo + (size_t)pi[k]] = pv[k];", "m->f[lo + k] = pv[k];", 1),
+    "receiver_skips_zero_values": ("local[r][lo + i] = local[r][lo + i] + v; /* S4 */",
+                                   "if (is_nonzero(v)) local[r][lo + i] = local[r][lo + i] + v; /* S4 */", 1),
     "agc_owner_keeps_input": ("/* the owner's own chunk becomes the decoded codes as well */\n    for (int r = 0; r < N; r++) {",
                               "/* the owner's own chunk becomes the decoded codes as well */\n    for (int r = 0; r < 0; r++) {", 1),
 }

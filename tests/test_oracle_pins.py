@@ -291,8 +291,11 @@ def test_sparse_allgather_is_an_exact_copy(dt):
     for r in range(N):
         assert np.array_equal(out[r].view(np.uint8), ref[r].view(np.uint8))
     n = T // N
-    msg = [brute.sparse_roundtrip(list(O.to_f32(bufs[c][c * n:(c + 1) * n], dt)), 0.5, 256)[2]
+    msg = [brute.sparse_roundtrip(list(O.to_f32(bufs[c][c * n:(c + 1) * n], dt)), 0.5)[1]
            for c in range(N)]
+    # one message per chunk: 70 % zeros, so each is sparse (8 + 8 nnz bytes)
+    assert all(m == 8 + 8 * int(np.count_nonzero(O.to_f32(bufs[c][c * n:(c + 1) * n], dt).view(np.uint32)))
+               for c, m in enumerate(msg))
     assert [int(x) for x in sent] == [sum(msg) - msg[(r + 1) % N] for r in range(N)]
     assert all(int(x) < 4 * n * (N - 1) for x in sent)
 
@@ -565,16 +568,17 @@ def test_diff_encode():
 
 # --------------------------------------------------------------- compressed ring
 
-@pytest.mark.parametrize("codec,bits", [("bfp", 8), ("bfp", 4), ("sparse", 8)])
+@pytest.mark.parametrize("codec,bits,sl", [("bfp", 8, None), ("bfp", 4, None), ("sparse", 8, None),
+                                           ("sparse", 8, 8)])
 @pytest.mark.parametrize("N,T", [(1, 10), (2, 64), (3, 50), (4, 64), (4, 17)])
-def test_compressed_ring_brute_force(codec, bits, N, T):
+def test_compressed_ring_brute_force(codec, bits, sl, N, T):
     rng = np.random.default_rng(N * 1000 + T + bits)
     xs = [(rng.standard_normal(T) * 1e-3).astype(np.float32) for _ in range(N)]
     if codec == "sparse":
         for x in xs:
             x[rng.random(T) < 0.6] = 0.0
-    outs, sent, recv = O.ring(xs, codec=codec, bits=bits, slice=8)
-    ref, bs, br = brute.ring([list(x) for x in xs], codec=codec, bits=bits, slice_len=8)
+    outs, sent, recv = O.ring(xs, codec=codec, bits=bits, slice=sl)
+    ref, bs, br = brute.ring([list(x) for x in xs], codec=codec, bits=bits, slice_len=sl)
     for r in range(N):
         assert np.array_equal(bits32(outs[r]), bits32(np.array(ref[r], np.float32)))
     assert list(sent) == bs and list(recv) == br
@@ -630,41 +634,104 @@ def test_bfp_ring_error_within_per_hop_bounds():
             assert err.max() <= bound
 
 
-def test_sparse_ring_equals_lossless_ring():
-    """With no -0.0 inputs the sparse ring is lossless: its result is the
-    lossless ring's, bit for bit; its wire bytes follow the slice rule."""
-    N, T = 5, 3000
-    rng = np.random.default_rng(150)
+def _sparse_inputs(N, T, seed, zero_p=0.6, minus_zero_every=0):
+    rng = np.random.default_rng(seed)
     xs = []
     for _ in range(N):
         x = (rng.standard_normal(T) * 0.02).astype(np.float32)
-        x[rng.random(T) < 0.6] = 0.0
+        x[rng.random(T) < zero_p] = 0.0
+        if minus_zero_every:
+            x[rng.integers(0, minus_zero_every):: minus_zero_every] = -0.0
         xs.append(x)
-    sp, ssent, _ = O.ring(xs, codec="sparse", slice=256)
+    return xs
+
+
+@pytest.mark.parametrize("sl", [None, 256, 7])
+def test_sparse_ring_equals_lossless_ring(sl):
+    """The sparse codec is lossless and the receiver adds the whole restored
+    message (S4), so the sparse ring's result is the lossless ring's bit for
+    bit, -0.0 inputs included, in either message granularity."""
+    N, T = 5, 3000
+    xs = _sparse_inputs(N, T, 150, minus_zero_every=37)
+    sp, ssent, _ = O.ring(xs, codec="sparse", slice=sl)
     ls, lsent, _ = O.ring(xs)
     for r in range(N):
         assert np.array_equal(bits32(sp[r]), bits32(ls[r]))
-    _, bs, _ = brute.ring([list(x) for x in xs], codec="sparse", slice_len=256)
+    _, bs, _ = brute.ring([list(x) for x in xs], codec="sparse", slice_len=sl)
     assert list(ssent) == bs
-    # hop 1 carries density-0.4 slices in the sparse format: 8 + 8 nnz bytes
-    # each instead of 8 + 4*256, so it is cheaper than a dense hop
-    assert all(ssent < lsent + 8 * 2 * (N - 1) * 3)
 
 
-def test_sparse_ring_keeps_minus_zero_of_own_input():
-    """S4: a position the message omits keeps the receiver's own value, so a
-    -0.0 own input survives (a dense add of the omitted +0.0 would give +0.0)."""
+def test_sparse_ring_adds_the_restored_message():
+    """S4: an omitted position is restored as +0.0 and added, so a -0.0 own
+    input meets +0.0 and gives +0.0, as in the lossless ring."""
     # N = 2, T = 4: rank 1 owns chunk 1 = [2, 4) and receives it from rank 0,
-    # whose values there are +0.0, so the sparse message carries nothing
+    # whose values there are +0.0, so the sparse message lists nothing
     xs = [np.zeros(4, np.float32), np.array([0, 0, -0.0, 0], np.float32)]
-    sp, _, _ = O.ring(xs, codec="sparse", slice=4, mode="reduce_scatter")
-    ls, _, _ = O.ring(xs, mode="reduce_scatter")
-    assert struct.pack("<f", float(sp[1][2])) == struct.pack("<f", -0.0)
-    assert struct.pack("<f", float(ls[1][2])) == struct.pack("<f", 0.0)
-    ref, _, _ = brute.ring([list(x) for x in xs], codec="sparse", slice_len=4, mode="reduce_scatter")
-    assert struct.pack("<f", float(ref[1][2])) == struct.pack("<f", -0.0)
+    for sl in (None, 4):
+        sp, sent, _ = O.ring(xs, codec="sparse", slice=sl, mode="reduce_scatter")
+        assert struct.pack("<f", float(sp[1][2])) == struct.pack("<f", 0.0)
+        # each rank sends one all-zero chunk of 2: a sparse header, no pairs
+        assert list(sent) == [8, 8]
+        ref, _, _ = brute.ring([list(x) for x in xs], codec="sparse", slice_len=sl,
+                               mode="reduce_scatter")
+        assert struct.pack("<f", float(ref[1][2])) == struct.pack("<f", 0.0)
 
 
+def _per_chunk_message_bytes(xs, thr=0.5):
+    """bytes[h][c] of the message of chunk c at hop h (h = 1..N-1 the
+    reduce-scatter partials, h = N the owner's full sum), with numpy: the
+    partial of hop h is x_{c+1} + ... + x_{c+h}, added one float32 add at a
+    time in ring order; a message is 8 + 8 nnz bytes when nnz < (1 - thr)
+    len, else 8 + 4 len; an empty chunk sends nothing."""
+    N, T = len(xs), xs[0].size
+    n = -(-T // N)
+    out = np.zeros((N + 1, N), np.int64)
+    for c in range(N):
+        lo, hi = min(c * n, T), min((c + 1) * n, T)
+        if hi == lo:
+            continue
+        p = None
+        for h in range(1, N + 1):
+            x = xs[(c + h) % N][lo:hi]
+            p = x.copy() if p is None else (p + x).astype(np.float32)
+            nnz = int(np.count_nonzero(p.view(np.uint32)))
+            out[h][c] = 8 + 8 * nnz if nnz < (1.0 - thr) * (hi - lo) else 8 + 4 * (hi - lo)
+    return out
+
+
+@pytest.mark.parametrize("N,T,zero_p", [(4, 4 * 500, 0.6), (5, 3001, 0.75), (6, 6 * 90, 0.9),
+                                        (3, 2, 0.5), (8, 13, 0.3)])
+def test_sparse_ring_per_chunk_bytes_closed_form(N, T, zero_p):
+    """One message per chunk and hop (reading S3): reduce-scatter step s,
+    rank r sends chunk (r - s) mod N's hop-s partial; allgather step s, rank r
+    forwards the owner's message of chunk (r - s + 1) mod N."""
+    xs = _sparse_inputs(N, T, 160 + N, zero_p=zero_p)
+    _, sent, recv = O.ring(xs, codec="sparse")
+    B = _per_chunk_message_bytes(xs)
+    want = [sum(B[s][(r - s) % N] for s in range(1, N)) +
+            sum(B[N][(r - s + 1) % N] for s in range(1, N)) for r in range(N)]
+    assert [int(v) for v in sent] == want
+    assert [int(v) for v in recv] == [want[(r - 1) % N] for r in range(N)]
+    _, rs_sent, _ = O.ring(xs, codec="sparse", mode="reduce_scatter")
+    assert [int(v) for v in rs_sent] == [sum(B[s][(r - s) % N] for s in range(1, N))
+                                         for r in range(N)]
+
+
+def test_sparse_ring_per_chunk_decision_at_the_tie():
+    """Chunk length 8, threshold 0.5: a hop whose partial has 4 nonzeros is
+    dense (8 + 32 bytes), 3 nonzeros sparse (8 + 24); per-slice messages of 4
+    elements decide each half on its own."""
+    N, T = 2, 16
+    a = np.zeros(T, np.float32)
+    b = np.zeros(T, np.float32)
+    a[8:12] = [1, 2, 3, 4]      # chunk 1 of rank 0, sent at step 1: 4 of 8 nonzero
+    b[0:3] = [5, 6, 7]          # chunk 0 of rank 1, sent at step 1: 3 of 8 nonzero
+    _, sent, _ = O.ring([a, b], codec="sparse", mode="reduce_scatter")
+    assert [int(v) for v in sent] == [8 + 4 * 8, 8 + 8 * 3]
+    _, sent4, _ = O.ring([a, b], codec="sparse", slice=4, mode="reduce_scatter")
+    # rank 0: [1 2 3 4] dense (8 + 16) and [0 0 0 0] sparse (8); rank 1:
+    # [5 6 7 0] dense (8 + 16) and [0 0 0 0] sparse (8)
+    assert [int(v) for v in sent4] == [8 + 16 + 8, 8 + 16 + 8]
 # --------------------------------------------------------------- error feedback
 
 @pytest.mark.parametrize("bits", [8, 4])

@@ -97,6 +97,30 @@ def test_ring_allreduce_equals_brute_force(N, T, seed, codec):
 
 
 @SETTINGS
+@given(N=st.integers(1, 5), T=st.integers(1, 80), seed=st.integers(0, 2 ** 31 - 1),
+       sl=st.sampled_from([None, 1, 3, 8, 16]), zero_p=st.sampled_from([0.3, 0.6, 0.9]),
+       thr=st.sampled_from([0.0, 0.25, 0.5, 0.75]))
+def test_sparse_ring_is_the_lossless_ring_with_message_bytes(N, T, seed, sl, zero_p, thr):
+    """Sparse codes (one message per chunk, or per slice) restore every value
+    and the receiver adds the restored message, so the outputs are the
+    lossless ring's bit for bit (-0.0 included); the byte counts are the
+    brute force's."""
+    rng = np.random.default_rng(seed)
+    xs = []
+    for _ in range(N):
+        x = rng.standard_normal(T).astype(np.float32)
+        x[rng.random(T) < zero_p] = 0.0
+        x[rng.random(T) < 0.05] = -0.0
+        xs.append(x)
+    outs, sent, recv = O.ring([x.copy() for x in xs], codec="sparse", threshold=thr, slice=sl)
+    ls, _, _ = O.ring([x.copy() for x in xs])
+    _, bs, br = brute.ring([list(x) for x in xs], codec="sparse", threshold=thr, slice_len=sl)
+    for r in range(N):
+        assert np.array_equal(outs[r].view(np.uint32), ls[r].view(np.uint32))
+    assert list(sent) == bs and list(recv) == br
+
+
+@SETTINGS
 @given(N=st.integers(1, 5), T=st.integers(1, 700), seed=st.integers(0, 2 ** 31 - 1),
        bits=st.sampled_from([8, 4]))
 def test_compressed_allgather_is_each_chunks_round_trip(N, T, seed, bits):
