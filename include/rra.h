@@ -62,11 +62,17 @@ extern "C" {
 /* Elements per block-floating-point block ([cccl] §2.1: "e.g. 128"). */
 #define RRA_BFP_BLOCK 128
 /* Elements per ring message slice: the ring streams each chunk through the
- * receive slots in slices of this many elements; for the sparse codec every
- * slice is one message with its own header and its own sparse/dense choice
+ * receive slots in slices of a multiple of this many elements.  With
+ * RRA_SPARSE_PER_SLICE, every slice of this many elements is one sparse
+ * codec message with its own header and its own sparse/dense choice
  * ([cccl] §2.2: the tensor is cut into small chunks that are compressed and
  * sent one after the other). */
 #define RRA_RING_SLICE 256
+
+/* Granularity of the sparse codec's sparse/dense decision
+ * (rra_codec.sparse_granularity). */
+#define RRA_SPARSE_PER_CHUNK 0 /* one message per ring chunk and hop (default) */
+#define RRA_SPARSE_PER_SLICE 1 /* one message per RRA_RING_SLICE elements     */
 
 typedef enum {
     RRA_OK = 0,
@@ -89,7 +95,7 @@ typedef enum {
  * Codec of one reducing call ([cccl] §3.2/§3.3 configuration fields).
  *  kind                what goes on the wire (above).
  *  bits                8 or 4 (RRA_CODEC_BFP only).
- *  sparsity_threshold  RRA_CODEC_SPARSE: a slice is sent sparse iff its
+ *  sparsity_threshold  RRA_CODEC_SPARSE: a message is sent sparse iff its
  *                      sparsity (zeros / length) is strictly greater, i.e.
  *                      nnz < (1 - threshold) * length; must lie in [0, 1).
  *  diff_prev           NULL, or a host array of N device pointers to fp32
@@ -114,7 +120,19 @@ typedef enum {
  *                      other codecs lose nothing); start from zeros.  The
  *                      buffers must not overlap each other or any input,
  *                      output, diff_prev or diff_base buffer.
- * A NULL rra_codec* means {RRA_CODEC_NONE, 0, 0, NULL, NULL, 0, NULL}.
+ *  sparse_granularity  RRA_CODEC_SPARSE: RRA_SPARSE_PER_CHUNK (0, default):
+ *                      at every hop the sender's message for a chunk is one
+ *                      message, sparse or dense by the nonzero count of the
+ *                      whole chunk's partial ([cccl] §2.1: the sparsity of
+ *                      the tensor about to be sent decides).  Before the ring
+ *                      starts, a count pass over the inputs (one read of
+ *                      every input) gives the count of every (chunk, hop)
+ *                      message: each hop's partial is the ring-order sum of
+ *                      the inputs of the ranks it has passed.  Chunks of more
+ *                      than 2^31 - 1 elements are RRA_ERR_UNSUPPORTED (int32
+ *                      indices).  RRA_SPARSE_PER_SLICE (1): one message per
+ *                      RRA_RING_SLICE elements, each decided on its own.
+ * A NULL rra_codec* means {RRA_CODEC_NONE, 0, 0, NULL, NULL, 0, NULL, 0}.
  */
 typedef struct {
     rra_codec_kind kind;
@@ -124,6 +142,7 @@ typedef struct {
     const float *diff_base;
     int average;
     float *const *residual;
+    int sparse_granularity;
 } rra_codec;
 
 /* Opaque communicator: owns the device-side byte counters, the status word
@@ -138,7 +157,8 @@ typedef struct rra_comm rra_comm;
  *             library keeps no per-size buffers: receive slots live in
  *             on-chip shared memory of each launched block).
  *  out        receives the handle.
- * Allocates a few hundred bytes of device memory (counters, status).
+ * Allocates device memory for its counters and status (a few hundred
+ * bytes) and for the sparse codec's message counts (16 * nranks^2 + 8 bytes).
  * Threads: one communicator serves one host thread at a time (its launch
  * caches, counter sets and last-call record have no lock); separate
  * communicators may be driven from separate threads.  Calls on one
@@ -173,16 +193,25 @@ rra_status rra_comm_destroy(rra_comm *comm);
  * order ((x_{c+1} + x_{c+2}) + ...) + x_c exactly (fp32, round to nearest
  * even, no FMA).  Output: cast to out_t with round to nearest even, after the
  * optional average and diff_base epilogue.
- * Wire formats per slice of <= RRA_RING_SLICE elements (len elements):
+ * Wire formats of one message of len elements (NONE and BFP: a chunk's
+ * message is the concatenation of its slices' messages, so these sizes add
+ * up over any cut into slices of multiples of 128 elements):
  *  NONE   fp32[len]                                       4 len bytes
  *  BFP    int8 exps[ceil(len/128)] + mantissas            ceil(len/128) + len (8-bit)
  *                                                         or + ceil(len/2) (4-bit)
  *  SPARSE {uint32 fmt, uint32 nnz} + fp32 vals[nnz] + int32 idx[nnz]
- *         (slice-relative, ascending)  = 8 + 8 nnz bytes, or dense
- *         {fmt = 0, nnz} + fp32[len] = 8 + 4 len bytes.
+ *         (relative to the message start, ascending) = 8 + 8 nnz bytes, or
+ *         dense {fmt = 0, nnz} + fp32[len] = 8 + 4 len bytes; one message
+ *         per chunk and hop (len = the chunk's length; an empty chunk sends
+ *         nothing), or per RRA_RING_SLICE elements (sparse_granularity).
+ * A sparse receiver restores the message -- the listed values at their
+ * indices, +0.0 elsewhere -- and adds the whole restored chunk ([cccl] §2.2:
+ * receive, decompress, then reduce), so the sparse ring's result equals the
+ * lossless ring's bit for bit.
  * Errors: RRA_ERR_INVALID (NULL pointers, count 0 or > max_count, bad enums,
- * bits not 8/4, threshold outside [0,1), diff_prev with in_t != F32,
- * out overlapping diff_base), RRA_ERR_CUDA.
+ * bits not 8/4, threshold outside [0,1), a bad sparse_granularity,
+ * diff_prev with in_t != F32, out overlapping diff_base),
+ * RRA_ERR_UNSUPPORTED (see sparse_granularity), RRA_ERR_CUDA.
  */
 rra_status rra_ring_allreduce(rra_comm *comm, const void *const *in, void *const *out,
                               size_t count, rra_dtype in_t, rra_dtype out_t,
@@ -215,7 +244,9 @@ rra_status rra_allgather(rra_comm *comm, void *const *buf, size_t count, rra_dty
  * lossy one; §3.3: low-precision compression for all_gather once all_reduce
  * runs compressed).  On entry chunk r of buf[r] (dtype f32, f16 or bf16) is
  * rank r's contribution.  Its owner encodes it once -- BFP (codec->bits 8
- * or 4, lossy) or sparse values + indices (codec->sparsity_threshold;
+ * or 4, lossy) or sparse values + indices (codec->sparsity_threshold and
+ * sparse_granularity: one message per chunk, decided by the nonzero count
+ * of chunk r of buf[r], which a count pass reads first, or one per slice;
  * lossless) -- the codes travel the ring of the allgather pass unchanged
  * (N-1 steps), and every rank, the owner included, stores the decoded chunk
  * in dtype (round to nearest even), so all buffers end identical.  Sparse

@@ -32,6 +32,7 @@ CODEC_NONE, CODEC_BFP, CODEC_SPARSE = 0, 1, 2
 MAX_RANKS = 64
 BFP_BLOCK = 128
 RING_SLICE = 256
+SPARSE_PER_CHUNK, SPARSE_PER_SLICE = 0, 1
 
 _lib = None
 
@@ -45,7 +46,7 @@ class RRAError(RuntimeError):
 class _Codec(C.Structure):
     _fields_ = [("kind", C.c_int), ("bits", C.c_int), ("sparsity_threshold", C.c_float),
                 ("diff_prev", C.c_void_p), ("diff_base", C.c_void_p), ("average", C.c_int),
-                ("residual", C.c_void_p)]
+                ("residual", C.c_void_p), ("sparse_granularity", C.c_int)]
 
 
 class _Stats(C.Structure):
@@ -162,6 +163,7 @@ class Codec:
     diff_base: Optional[object] = None    # fp32 tensor (previous result)
     average: bool = False
     residual: Optional[Sequence] = None   # N fp32 tensors: error-feedback residuals (BFP)
+    granularity: str = "chunk"            # sparse: one message per "chunk" and hop, or per "slice"
 
     def _marshal(self):
         kinds = {"none": CODEC_NONE, "bfp": CODEC_BFP, "sparse": CODEC_SPARSE}
@@ -177,6 +179,7 @@ class Codec:
         if self.diff_base is not None:
             c.diff_base = _dev(self.diff_base, "diff_base")
         c.average = 1 if self.average else 0
+        c.sparse_granularity = {"chunk": SPARSE_PER_CHUNK, "slice": SPARSE_PER_SLICE}[self.granularity]
         if self.residual is not None:
             arr = _ptrs(self.residual, "residual")
             keep.append(arr)

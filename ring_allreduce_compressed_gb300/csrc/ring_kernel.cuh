@@ -203,12 +203,25 @@ template <int BITS> struct BfpGroup {
 };
 
 // ---------------------------------------------------------------- wire formats
+// What a step tells the wire codec about the message it moves (per-chunk
+// sparse codec; the other codecs ignore it): fk = 2 * ((h-1)*N + c) + f,
+// the message of chunk c at hop h and its format f (1 sparse, 0 dense,
+// decided for the whole chunk before the ring starts), and base, the
+// chunk-relative index of the slice's first element.
+struct Msg {
+    int fk;
+    int base;
+    __device__ __forceinline__ int sparse() const { return fk & 1; }
+    __device__ __forceinline__ int key() const { return fk >> 1; }
+};
+
 // A message covers one slice of TW = 256*G elements.  The kernel streams it
 // group by group (8 elements per lane, 256 per warp): a WireCodec's per-group
 // operations move one group between registers and a slot, so only 8 values
 // per lane are live at a time however large the slice is.
 //  Reg                   one lane's share of one group of a message.
 //  load / store          group gi: slot <-> Reg (allgather forwarding).
+//                        Every operation also takes the step's Msg.
 //  encode<DEC>           encode the lane's 8 fp32 values of group gi into the
 //                        slot; with DEC, v becomes what a receiver decodes.
 //                        Returns the group's wire bytes where they depend on
@@ -231,7 +244,8 @@ template <> struct WireCodec<kCodecNone> {
         float f[8];
     };
     __device__ __forceinline__ static void load(const unsigned char *slot, int gi, int lane,
-                                                unsigned char *, const RingArgs &, Reg &m)
+                                                unsigned char *, const RingArgs &, Reg &m,
+                                                const Msg &)
     {
         const float4 *p = reinterpret_cast<const float4 *>(slot + gi * kTile * 4) + 2 * lane;
         const float4 a = p[0], b = p[1];
@@ -239,7 +253,7 @@ template <> struct WireCodec<kCodecNone> {
         m.f[4] = b.x; m.f[5] = b.y; m.f[6] = b.z; m.f[7] = b.w;
     }
     __device__ __forceinline__ static void store(unsigned char *slot, int gi, int lane,
-                                                 const Reg &m, const RingArgs &)
+                                                 const Reg &m, const RingArgs &, const Msg &)
     {
         float4 *p = reinterpret_cast<float4 *>(slot + gi * kTile * 4) + 2 * lane;
         p[0] = make_float4(m.f[0], m.f[1], m.f[2], m.f[3]);
@@ -248,7 +262,7 @@ template <> struct WireCodec<kCodecNone> {
     template <bool DEC>
     __device__ __forceinline__ static uint32_t encode(float (&v)[8], unsigned char *slot, int gi,
                                                       int lane, int, const RingArgs &,
-                                                      unsigned char *)
+                                                      unsigned char *, const Msg &)
     {
         float4 *p = reinterpret_cast<float4 *>(slot + gi * kTile * 4) + 2 * lane;
         p[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -274,7 +288,7 @@ template <> struct WireCodec<kCodecNone> {
             v[i] = m.f[i];
     }
     __device__ __forceinline__ static uint32_t bytes(int V, const unsigned char *,
-                                                     const RingArgs &)
+                                                     const RingArgs &, const Msg &)
     {
         return 4u * (uint32_t)V;
     }
@@ -293,7 +307,8 @@ template <int BITS> struct CodecBfp {
         int e;
     };
     __device__ __forceinline__ static void load(const unsigned char *slot, int gi, int lane,
-                                                unsigned char *, const RingArgs &, Reg &m)
+                                                unsigned char *, const RingArgs &, Reg &m,
+                                                const Msg &)
     {
         m.e = (int)(int8_t)slot[2 * gi + (lane >> 4)];
         if constexpr (BITS == 8) {
@@ -306,7 +321,7 @@ template <int BITS> struct CodecBfp {
         }
     }
     __device__ __forceinline__ static void store(unsigned char *slot, int gi, int lane,
-                                                 const Reg &m, const RingArgs &)
+                                                 const Reg &m, const RingArgs &, const Msg &)
     {
         if ((lane & 15) == 0)
             slot[2 * gi + (lane >> 4)] = (unsigned char)(int8_t)m.e;
@@ -330,7 +345,7 @@ template <int BITS> struct CodecBfp {
     template <bool DEC>
     __device__ __forceinline__ static uint32_t encode(float (&v)[8], unsigned char *slot, int gi,
                                                       int lane, int, const RingArgs &,
-                                                      unsigned char *)
+                                                      unsigned char *, const Msg &)
     {
         Reg m;
         encode_reg(v, slot, gi, lane, m);
@@ -349,7 +364,7 @@ template <int BITS> struct CodecBfp {
         BfpGroup<BITS>::decode(m.w, m.e, v);
     }
     __device__ __forceinline__ static uint32_t bytes(int V, const unsigned char *,
-                                                     const RingArgs &)
+                                                     const RingArgs &, const Msg &)
     {
         return bfp_msg_bytes(V, BITS);
     }
@@ -418,8 +433,9 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     // the BFP8 allgather loop that writes fp16 straight from the codes and the
     // allgather loop of the sparse codec (slices of at most 4 groups); the
     // other loops stay rolled to keep the code within the instruction cache.
+    constexpr bool kSparseAny = CODEC == kCodecSparse || CODEC == kCodecSparseChunk;
     constexpr int kUnrollRS = CODEC != kCodecNone ? G : 1;
-    constexpr int kUnrollAG = CODEC == kCodecSparse ? G : 1;
+    constexpr int kUnrollAG = kSparseAny ? G : 1;
     const int N = a.N;
     const int W = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5;
@@ -428,7 +444,8 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     // BFP8 allgather steps write fp16 outputs straight from the codes
     constexpr bool kDirect16 = CODEC == kCodecBfp8;
     const Layout Lo = make_layout(N, K, D, a.slot_bytes, a.stage_bytes, W, FAST,
-                                  CODEC == kCodecSparse, kDirect16);
+                                  CODEC == kCodecSparse ? 1 : CODEC == kCodecSparseChunk ? 2 : 0,
+                                  kDirect16);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lo.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + Lo.empty);
     uint64_t *sbar = reinterpret_cast<uint64_t *>(smem + Lo.stage_bar);
@@ -436,7 +453,8 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     unsigned long long *rrecv = rsent + N;
     unsigned char *slots = smem + Lo.slots;
     unsigned char *stages = smem + Lo.stages;
-    unsigned char *scratch = smem + Lo.scratch + warp * (kTile * 4 + kTile);
+    unsigned char *scratch = smem + Lo.scratch + warp * (kTile * 4);
+    unsigned char *fmt_s = smem + Lo.fmt; // per-chunk sparse: format of message (hop, chunk)
 
     for (int i = threadIdx.x; i < N * K; i += blockDim.x) {
         mbar_init(full + i, 1);
@@ -456,6 +474,15 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     if constexpr (kDirect16)
         for (int i = threadIdx.x; i < 256; i += blockDim.x)
             reinterpret_cast<uint2 *>(smem + Lo.lut)[i] = bfp8_f16_entry(i - 128);
+    if constexpr (CODEC == kCodecSparseChunk) {
+        // the format of every message of the call, from the count pass: the
+        // message of chunk c at hop h is sparse iff nnz < (1 - threshold) * len
+        for (int i = threadIdx.x; i < a.N * a.N; i += blockDim.x) {
+            const long long c = i % a.N;
+            const long long lo = min(c * a.n, a.T), hi = min(lo + a.n, a.T);
+            fmt_s[i] = (double)a.sp_nnz[i] < a.one_minus_thr * (double)(hi - lo) ? 1 : 0;
+        }
+    }
     mbar_fence_init();
     __syncthreads();
 
@@ -544,6 +571,16 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     const bool first_item_withhold = a.withhold_rank >= 0;
     int withhold_g = 0; // step whose send is withheld in this slice (0: none)
 
+    // the message of chunk c at hop h (h = N: the owner's) in the slice at t0
+    auto msg_of = [&](int h, int c) -> Msg {
+        if constexpr (CODEC == kCodecSparseChunk) {
+            const int i = (h - 1) * N + c;
+            return Msg{2 * i + fmt_s[i], (int)t0};
+        } else {
+            return Msg{0, 0};
+        }
+    };
+
     // group gi of rank r's own input for chunk c (staged on the fast path)
     auto input_group = [&](int r, int c, int V, int gi, const unsigned char *sp,
                            float (&v)[8]) {
@@ -620,7 +657,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
             v[i] = s2.x;
             v[i + 1] = s2.y;
         }
-        C::template encode<true>(v, dslot, gi, lane, V, a, scratch);
+        C::template encode<true>(v, dslot, gi, lane, V, a, scratch, Msg{0, 0});
 #pragma unroll
         for (int i = 0; i < 8; i += 2) {
             const float2 d2 = __fadd2_rn(make_float2(u[i], u[i + 1]), make_float2(-v[i], -v[i + 1]));
@@ -634,8 +671,9 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     // edge cannot stall the ring.  Wider messages are streamed group by group
     // and their slot is freed at the end of the step (two slots per edge).
     constexpr bool kEarly = G == 1;
-    auto release_early = [&](int r, const unsigned char *rslot, uint32_t rb, Reg &m) {
-        C::load(rslot, 0, lane, scratch, a, m);
+    auto release_early = [&](int r, const unsigned char *rslot, uint32_t rb, Reg &m,
+                             const Msg &mg) {
+        C::load(rslot, 0, lane, scratch, a, m, mg);
         if (ONE)
             my_recv += rb;
         __syncwarp();
@@ -733,14 +771,16 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                 }
                 const unsigned char *sp = stages + (size_t)(r * D + stg.slot) * a.stage_bytes;
                 const unsigned char *rslot = slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
+                const Msg rmsg = g >= 2 ? msg_of(g - 1, c) : Msg{0, 0};
+                const Msg smsg = msg_of(g, c);
                 // wire bytes received and sent (data-dependent sizes are
                 // summed group by group below)
                 uint32_t rb = 0, sb = 0;
                 Reg m0;
                 if (g >= 2 && (kEarly || !C::kVarBytes)) {
-                    rb = C::bytes(V, rslot, a);
+                    rb = C::bytes(V, rslot, a, rmsg);
                     if (kEarly)
-                        release_early(r, rslot, rb, m0);
+                        release_early(r, rslot, rb, m0, rmsg);
                 }
                 if (!pre && !wait_ready(empty + dst * K + snd.slot, (uint32_t)(snd.phase ^ 1),
                                         a.timeout_ns, a.status)) {
@@ -757,19 +797,19 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                         if (kEarly) {
                             m = m0;
                         } else {
-                            C::load(rslot, gi, lane, scratch, a, m);
+                            C::load(rslot, gi, lane, scratch, a, m, rmsg);
                             if constexpr (C::kVarBytes)
-                                rb += C::group_bytes(m, V, gi);
+                                rb += C::group_bytes(m, V, gi, rmsg);
                         }
                         C::decode_add(m, v, lane, scratch);
                     }
                     if constexpr (EF)
                         encode_ef(r, c, V, gi, v, dslot);
                     else
-                        sb += C::template encode<false>(v, dslot, gi, lane, V, a, scratch);
+                        sb += C::template encode<false>(v, dslot, gi, lane, V, a, scratch, smsg);
                 }
                 if constexpr (!C::kVarBytes)
-                    sb = C::bytes(V, dslot, a);
+                    sb = C::bytes(V, dslot, a, smsg);
                 finish_step(r, g, g >= 2 && !kEarly, true, rb, sb);
                 if (ONE)
                     break;
@@ -804,11 +844,13 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
             }
             const unsigned char *sp = stages + (size_t)(r * D + stg.slot) * a.stage_bytes;
             const unsigned char *rslot = slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
-            uint32_t rb = recv && (kEarly || !C::kVarBytes) ? C::bytes(V, rslot, a) : 0u;
+            const Msg rmsg = recv ? msg_of(N - 1, r) : Msg{0, 0};
+            const Msg smsg = msg_of(N, r);
+            uint32_t rb = recv && (kEarly || !C::kVarBytes) ? C::bytes(V, rslot, a, rmsg) : 0u;
             uint32_t sb = 0;
             Reg m0;
             if (kEarly && recv)
-                release_early(r, rslot, rb, m0);
+                release_early(r, rslot, rb, m0, rmsg);
             if (!pre && send &&
                 !wait_ready(empty + dst * K + snd.slot, (uint32_t)(snd.phase ^ 1), a.timeout_ns,
                             a.status)) {
@@ -836,7 +878,7 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                         if (kEarly)
                             m = m0;
                         else
-                            C::load(rslot, gi, lane, scratch, a, m);
+                            C::load(rslot, gi, lane, scratch, a, m, rmsg);
                         C::decode_add(m, v, lane, scratch);
                         Reg w;
                         C::encode_reg(v, dslot, gi, lane, w);
@@ -862,9 +904,9 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     if (kEarly) {
                         m = m0;
                     } else {
-                        C::load(rslot, gi, lane, scratch, a, m);
+                        C::load(rslot, gi, lane, scratch, a, m, rmsg);
                         if constexpr (C::kVarBytes)
-                            rb += C::group_bytes(m, V, gi);
+                            rb += C::group_bytes(m, V, gi, rmsg);
                     }
                     C::decode_add(m, v, lane, scratch);
                 }
@@ -872,12 +914,12 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     if constexpr (EF)
                         encode_ef(r, r, V, gi, v, dslot);
                     else
-                        sb += C::template encode<true>(v, dslot, gi, lane, V, a, scratch);
+                        sb += C::template encode<true>(v, dslot, gi, lane, V, a, scratch, smsg);
                 }
                 output_group(r, r, V, gi, v);
             }
             if constexpr (!C::kVarBytes)
-                sb = C::bytes(V, dslot, a);
+                sb = C::bytes(V, dslot, a, smsg);
             finish_step(r, N, recv && !kEarly, send, rb, send ? sb : 0u);
             if (ONE)
                 break;
@@ -908,10 +950,11 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     }
                     const unsigned char *rslot =
                         slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
-                    uint32_t rb = (kEarly || !C::kVarBytes) ? C::bytes(V, rslot, a) : 0u;
+                    const Msg amsg = msg_of(N, c); // the owner's message, forwarded unchanged
+                    uint32_t rb = (kEarly || !C::kVarBytes) ? C::bytes(V, rslot, a, amsg) : 0u;
                     Reg m0;
                     if (kEarly)
-                        release_early(r, rslot, rb, m0);
+                        release_early(r, rslot, rb, m0, amsg);
                     if (!pre && fwd &&
                         !wait_ready(empty + dst * K + snd.slot, (uint32_t)(snd.phase ^ 1),
                                     a.timeout_ns, a.status)) {
@@ -933,9 +976,9 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                                 if (kEarly)
                                     m = m0;
                                 else
-                                    C::load(rslot, gi, lane, scratch, a, m);
+                                    C::load(rslot, gi, lane, scratch, a, m, amsg);
                                 if (fwd)
-                                    C::store(dslot, gi, lane, m, a);
+                                    C::store(dslot, gi, lane, m, a, amsg);
                                 uint32_t h[4];
                                 const uint2 sc = lut[m.e + 128]; // m.e is a signed byte
                                 if (sc.x != 0u) {
@@ -957,12 +1000,12 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                             if (kEarly) {
                                 m = m0;
                             } else {
-                                C::load(rslot, gi, lane, scratch, a, m);
+                                C::load(rslot, gi, lane, scratch, a, m, amsg);
                                 if constexpr (C::kVarBytes)
-                                    rb += C::group_bytes(m, V, gi);
+                                    rb += C::group_bytes(m, V, gi, amsg);
                             }
                             if (fwd)
-                                C::store(dslot, gi, lane, m, a);
+                                C::store(dslot, gi, lane, m, a, amsg);
                             float v[8];
                             C::values(m, v, lane, scratch);
                             output_group(r, c, V, gi, v);

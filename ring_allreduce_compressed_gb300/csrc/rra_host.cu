@@ -21,6 +21,7 @@ const void *ring_fn_none(int in_t, bool fast, int groups, int rmap);
 const void *ring_fn_bfp8(int in_t, bool fast, int groups, int rmap);
 const void *ring_fn_bfp4(int in_t, bool fast, int groups, int rmap);
 const void *ring_fn_sparse(int in_t, bool fast, int groups, int rmap);
+const void *ring_fn_sparse_chunk(int in_t, bool fast, int groups, int rmap);
 const void *ring_fn_bfp8_ef(int in_t, bool fast, int groups, int rmap);
 const void *ring_fn_bfp4_ef(int in_t, bool fast, int groups, int rmap);
 } // namespace rra
@@ -49,6 +50,10 @@ struct rra_comm {
     rra::Tune last{};      // shape of the last ring launch (blocks = blocks per SM)
     size_t crossover = 0;  // rra_allreduce_auto: tree below this many bytes per rank
     unsigned long long *stats = nullptr; // [4] codec statistics (inside `counters`)
+    // per-chunk sparse codec: message nonzero counts, [N*N] accumulated by
+    // the count pass, [N*N] its result, and its block ticket
+    unsigned long long *sp_acc = nullptr, *sp_out = nullptr;
+    unsigned *sp_ticket = nullptr;
     std::map<long long, int> occ; // (kernel key, smem) -> blocks per SM
 };
 
@@ -165,6 +170,8 @@ const void *ring_fn(int codec, int in_t, bool fast, int groups, int rmap, bool e
         return ring_fn_none(in_t, fast, groups, rmap);
     if (codec == kCodecSparse)
         return ring_fn_sparse(in_t, fast, groups, rmap);
+    if (codec == kCodecSparseChunk)
+        return ring_fn_sparse_chunk(in_t, fast, groups, rmap);
     if (codec == kCodecBfp8)
         return ring_fn_bfp8(in_t, fast, groups, rmap);
     return ring_fn_bfp4(in_t, fast, groups, rmap);
@@ -176,13 +183,16 @@ const void *ring_fn(int codec, int in_t, bool fast, int groups, int rmap, bool e
 int sparse_icap(int lim) { return std::max(lim - 1, 0); }
 int sparse_sub_bytes(int lim) { return align_up(16 + std::max(kTile * 4, 8 * sparse_icap(lim)), 16); }
 
-// Bytes of one mailbox slot for a slice of 256 * groups elements.
+// Bytes of one mailbox slot for a slice of 256 * groups elements.  The
+// per-chunk sparse slot: 32 header bytes, then room for 256 (value, index)
+// pairs per group (values region, then indices region).
 int slot_bytes_for(int codec, int groups, int sparse_lim)
 {
     switch (codec) {
     case kCodecNone: return kTile * 4 * groups;
     case kCodecBfp8: return 16 + kTile * groups;
     case kCodecBfp4: return 16 + kTile / 2 * groups;
+    case kCodecSparseChunk: return 32 + 2 * kTile * 4 * groups;
     default: return sparse_sub_bytes(sparse_lim) * groups;
     }
 }
@@ -205,7 +215,8 @@ bool pick_shape(rra_comm *c, const Tune &t, int N, long long n, int kc, int ies,
     // resident blocks to leave room for: about 24 warps per SM (three blocks
     // of up to 8 warps, two of 12 to 16)
     const int want = warps >= 12 ? 2 : 3;
-    const bool sparse = kc == kCodecSparse;
+    const bool sparse = kc == kCodecSparse || kc == kCodecSparseChunk;
+    const int sparse_kind = kc == kCodecSparse ? 1 : kc == kCodecSparseChunk ? 2 : 0;
     // a requested slice width is tried first on its own; passes 2 and 3 are
     // the automatic choice
     for (int pass = t.G ? 0 : 2; pass < 4; ++pass) {
@@ -229,7 +240,7 @@ bool pick_shape(rra_comm *c, const Tune &t, int N, long long n, int kc, int ies,
             // so with one slot every rank would wait for its successor
             for (int K = t.K ? t.K : 2; K >= (G == 1 ? 1 : 2); --K) {
                 const Layout L =
-                    make_layout(N, K, D, slot, stage, warps, fast, sparse, kc == kCodecBfp8);
+                    make_layout(N, K, D, slot, stage, warps, fast, sparse_kind, kc == kCodecBfp8);
                 const bool several = pass % 2 == 0; // leave room for `want` blocks per SM
                 const int need = several ? want * (L.total + 1024) : L.total;
                 const int have = several ? c->smem_per_sm : c->smem_optin;
@@ -274,7 +285,12 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     } else if (cd.kind == RRA_CODEC_SPARSE) {
         if (!(cd.sparsity_threshold >= 0.0f && cd.sparsity_threshold < 1.0f))
             return RRA_ERR_INVALID;
-        kc = kCodecSparse;
+        if (cd.sparse_granularity == RRA_SPARSE_PER_CHUNK)
+            kc = kCodecSparseChunk;
+        else if (cd.sparse_granularity == RRA_SPARSE_PER_SLICE)
+            kc = kCodecSparse;
+        else
+            return RRA_ERR_INVALID;
     } else {
         return RRA_ERR_INVALID;
     }
@@ -355,6 +371,10 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
         ++a.sp_full_lim;
     a.sp_icap = sparse_icap(a.sp_full_lim);
     a.sp_sub = sparse_sub_bytes(a.sp_full_lim);
+    // per-chunk sparse messages index a chunk with int32
+    if (kc == kCodecSparseChunk && a.n > 0x7fffffffLL)
+        return RRA_ERR_UNSUPPORTED;
+    a.sp_nnz = comm->sp_out;
     a.timeout_ns = comm->timeout_ns;
     a.status = comm->status;
     a.withhold_rank = comm->withhold_rank;
@@ -405,6 +425,8 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     a.K = sh.K;
     a.D = sh.D;
     a.slot_bytes = slot_bytes_for(kc, groups, a.sp_full_lim);
+    if (kc == kCodecSparseChunk)
+        a.sp_sub = 32 + kTile * 4 * groups; // the indices region of a slot
     a.stage_bytes = kTile * groups * (cd.diff_prev ? 8 : (int)ies);
     a.tiles = (a.n + kTile * groups - 1) / (kTile * groups);
     // every warp plays exactly one rank when N fits the block
@@ -417,9 +439,36 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     int per_sm = 0;
     const int grid = grid_for(comm, key, fn, warps, smem, a.tiles, t.blocks, &per_sm);
     comm->last = Tune{per_sm, a.K, a.D, groups};
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (kc == kCodecSparseChunk) {
+        // the count pass: the nonzero count of every message, so that each
+        // chunk's format is decided before its first slice is sent
+        SpCountArgs ca;
+        std::memset(&ca, 0, sizeof ca);
+        ca.N = N;
+        ca.h_lo = mode == kModeAllgather ? N : 1;
+        ca.h_hi = mode == kModeReduceScatter ? N - 1 : N;
+        ca.T = a.T;
+        ca.n = a.n;
+        ca.acc = comm->sp_acc;
+        ca.out = comm->sp_out;
+        ca.ticket = comm->sp_ticket;
+        for (int r = 0; r < N; ++r) {
+            ca.in[r] = in[r];
+            ca.prev[r] = a.prev[r];
+        }
+        // about eight 256-thread blocks per SM in all, each walking its
+        // chunk in 2048-element strides
+        const long long per_chunk = std::max(1LL, (a.n + 2047) / 2048);
+        ca.bpc = (int)std::min<long long>(per_chunk, std::max(1, num_sms() * 8 / N));
+        bool vec = (a.n * (long long)ies) % 16 == 0;
+        for (int r = 0; r < N; ++r)
+            vec = vec && al16(in[r]) && (!cd.diff_prev || al16(cd.diff_prev[r]));
+        if (ca.h_lo <= ca.h_hi && launch_sparse_chunk_count(ca, kin, vec, st) != cudaSuccess)
+            return RRA_ERR_CUDA;
+    }
     const int prev_set = comm->last_set;
     counter_sets(comm, &a.sent, &a.recv, &a.zero);
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (launch_ring(fn, a, grid, warps, smem, st) != cudaSuccess) {
         undo_counter_sets(comm, prev_set);
         return RRA_ERR_CUDA;
@@ -605,11 +654,24 @@ rra_status rra_comm_create(int nranks, size_t max_count, rra_dtype max_dtype, rr
         return RRA_ERR_NOMEM;
     }
     c->stats = c->counters + 4 * (size_t)nranks;
-    if (cudaMemset(c->counters, 0, cbytes) != cudaSuccess ||
+    // per-chunk sparse message counts: accumulator, result, ticket
+    const size_t nn = (size_t)nranks * (size_t)nranks;
+    const size_t sbytes = sizeof(unsigned long long) * (2 * nn + 1);
+    if (cudaMalloc(&c->sp_acc, sbytes) != cudaSuccess) {
+        cudaFree(c->counters);
+        cudaFree(c->status);
+        delete c;
+        return RRA_ERR_NOMEM;
+    }
+    c->sp_out = c->sp_acc + nn;
+    c->sp_ticket = reinterpret_cast<unsigned *>(c->sp_out + nn);
+    if (cudaMemset(c->sp_acc, 0, sbytes) != cudaSuccess ||
+        cudaMemset(c->counters, 0, cbytes) != cudaSuccess ||
         cudaMemset(c->status, 0, sizeof(unsigned)) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(c->counters);
         cudaFree(c->status);
+        cudaFree(c->sp_acc);
         delete c;
         return RRA_ERR_CUDA;
     }
@@ -624,6 +686,7 @@ rra_status rra_comm_destroy(rra_comm *comm)
     cudaDeviceSynchronize();
     cudaFree(comm->counters);
     cudaFree(comm->status);
+    cudaFree(comm->sp_acc);
     delete comm;
     return RRA_OK;
 }

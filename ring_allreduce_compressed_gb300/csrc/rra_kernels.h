@@ -11,7 +11,10 @@ namespace rra {
 constexpr int kMaxRanks = 64;
 constexpr int kMaxWarps = 16; // warps per block; ranks per warp = ceil(N / warps)
 
-enum Codec { kCodecNone = 0, kCodecBfp8 = 1, kCodecBfp4 = 2, kCodecSparse = 3 };
+// kCodecSparse: one sparse/dense message per 256-element slice;
+// kCodecSparseChunk: one message per ring chunk and hop, its format chosen
+// from the chunk's nonzero count (the count pass below).
+enum Codec { kCodecNone = 0, kCodecBfp8 = 1, kCodecBfp4 = 2, kCodecSparse = 3, kCodecSparseChunk = 4 };
 enum Mode { kModeAllreduce = 0, kModeReduceScatter = 1, kModeAllgather = 2 };
 
 // Launch shape of a ring kernel: blocks per SM, mailbox slots per edge,
@@ -44,10 +47,13 @@ struct RingArgs {
     long long T;       // elements per rank
     long long n;       // chunk length ceil(T/N)
     long long tiles;   // slices per chunk ceil(n / 256)
-    double one_minus_thr; // sparse: a slice is sparse iff nnz < one_minus_thr * len
-    int sp_full_lim;      // sparse: a full 256-element slice is sparse iff nnz < sp_full_lim
-    int sp_icap;          // sparse: most (value, index) pairs of a sparse group = lim - 1
-    int sp_sub;           // sparse: bytes of one group's sub-message in a slot
+    double one_minus_thr; // sparse: a message is sparse iff nnz < one_minus_thr * len
+    int sp_full_lim;      // per-slice sparse: a full 256-element slice is sparse iff nnz < sp_full_lim
+    int sp_icap;          // per-slice sparse: most (value, index) pairs of a sparse group = lim - 1
+    int sp_sub;           // per-slice sparse: bytes of one group's sub-message in a slot;
+                          // per-chunk sparse: byte offset of the index region in a slot
+    const unsigned long long *sp_nnz; // per-chunk sparse: nnz[(h-1)*N + c] of the message of
+                                      // chunk c at hop h (h = N: the owner's), from the count pass
     unsigned long long timeout_ns;
     unsigned long long *sent; // [N] device counters of this call
     unsigned long long *recv; // [N]
@@ -84,16 +90,36 @@ struct CopyArgs {
     void *buf[kMaxRanks];
 };
 
+// Per-chunk sparse codec: nonzero count of every message of one call.
+// Hop h = 1..N-1 carries the reduce-scatter partial x_{c+1} + ... + x_{c+h}
+// of chunk c (fp32, ring order), hop N the owner's full sum, or, for the
+// allgather alone, chunk c of buffer c.  Counts are summed into acc by
+// atomics; the last block to finish moves them to out and clears acc and
+// the ticket for the next call.
+struct SpCountArgs {
+    int N;
+    int h_lo, h_hi;  // hops counted: allreduce 1..N, reduce-scatter 1..N-1, allgather N..N
+    int bpc;         // blocks per chunk
+    long long T, n;
+    unsigned long long *acc; // [N * N], zero on entry
+    unsigned long long *out; // [N * N]
+    unsigned *ticket;        // zero on entry
+    const void *in[kMaxRanks];
+    const float *prev[kMaxRanks];
+};
+cudaError_t launch_sparse_chunk_count(const SpCountArgs &a, int in_kind, bool vec,
+                                      cudaStream_t st);
+
 // Shared-memory layout of the ring / copy kernels (host and device agree).
 struct Layout {
-    int full, empty, stage_bar, rank_state, slots, stages, scratch, lut, total;
+    int full, empty, stage_bar, rank_state, slots, stages, scratch, lut, fmt, total;
 };
 
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 __host__ __device__ inline Layout make_layout(int N, int K, int D, int slot_bytes,
                                               int stage_bytes, int warps, bool fast,
-                                              bool sparse, bool lut)
+                                              int sparse, bool lut)
 {
     Layout L;
     int off = 0;
@@ -113,10 +139,13 @@ __host__ __device__ inline Layout make_layout(int N, int K, int D, int slot_byte
     off += fast ? N * D * stage_bytes : 0;
     off = align_up(off, 16);
     L.scratch = off;
-    off += sparse ? warps * (256 * 4 + 256) : 0;
+    off += sparse ? warps * 256 * 4 : 0; // per warp: one restored 256-element group
     off = align_up(off, 16);
     L.lut = off; // BFP8: 256 entries of 8 bytes (the fp16 output table)
     off += lut ? 256 * 8 : 0;
+    off = align_up(off, 16);
+    L.fmt = off; // per-chunk sparse: format byte of every (hop, chunk) message
+    off += sparse == 2 ? N * N : 0;
     L.total = align_up(off, 128);
     return L;
 }

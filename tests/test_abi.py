@@ -5,6 +5,7 @@ code (neither imports, includes or links the other)."""
 import ctypes as C
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -119,6 +120,25 @@ def test_header_constants_match_the_binding():
     assert int(m.group(1)) << int(m.group(2)) == rra.RRA_DEFAULT_CROSSOVER
     assert int(consts["RRA_RING_SLICE"]) == rra.RING_SLICE
     assert int(consts["RRA_BFP_BLOCK"]) == rra.BFP_BLOCK
+    assert int(consts["RRA_SPARSE_PER_CHUNK"]) == rra.SPARSE_PER_CHUNK
+    assert int(consts["RRA_SPARSE_PER_SLICE"]) == rra.SPARSE_PER_SLICE
+
+
+def test_codec_struct_layout_matches_the_binding(tmp_path):
+    """Every field of rra_codec sits at the offset the ctypes binding uses."""
+    fields = [f for f, _ in rra._Codec._fields_]
+    prog = tmp_path / "layout.c"
+    prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "rra.h"\nint main(void){\n' +
+                    f'printf("%zu\\n", sizeof(rra_codec));\n' +
+                    "".join(f'printf("%zu\\n", offsetof(rra_codec, {f}));\n' for f in fields) +
+                    "return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), "-o", str(exe), str(prog)],
+                   check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert got[0] == C.sizeof(rra._Codec)
+    assert got[1:] == [getattr(rra._Codec, f).offset for f in fields]
 
 
 def _sources(folder, exts):

@@ -2,10 +2,11 @@
 bench.py times (the library chooses it from N, T and the dtypes alone).
 
 The oracle cannot redo 10^9-element rings in a test, so it computes sampled
-positions: slices of 256 elements are independent in the ring (BFP blocks and
-sparse messages never cross a slice boundary, and every element's chain
+positions: slices of 256 elements are independent in the BFP and lossless
+rings (BFP blocks never cross a slice boundary, and every element's chain
 depends only on its chunk index), so the ring over the chosen slices of every
-chunk is an exact sub-problem.  Properties that hold at any size are checked
+chunk is an exact sub-problem.  The per-chunk sparse ring is not sliceable
+(each chunk's format depends on all of it): it runs the whole oracle.  Properties that hold at any size are checked
 on the whole output: every rank bit-identical, the sparse ring equal to the
 lossless ring, closed-form byte counters."""
 import numpy as np
@@ -67,30 +68,50 @@ def test_bfp8_bucket_full_size():
 
 
 def test_sparse_n16_full_size():
-    """N=16, 64 Mi bf16 with 60% zeros, threshold 0.5, fp32 out: sampled
-    parity (values and the per-slice format decisions of the sample), equal
-    to the lossless ring everywhere."""
+    """N=16, 64 Mi bf16 with 60% zeros, threshold 0.5, fp32 out, one sparse
+    message per chunk and hop: the whole output and the byte counters
+    against the whole oracle (a per-chunk format depends on every slice of
+    the chunk, so no slice sample is an exact sub-problem), and equal to the
+    lossless ring."""
     c = W.CONFIGS["sparse_n16"]
     N, T = c["N"], c["T"]
     xs = W.sparse(N, T, seed=c["seed"])
     comm = rra.Comm(N, T, torch.bfloat16)
     outs = [torch.empty(T, dtype=torch.float32, device="cuda") for _ in range(N)]
     comm.ring_allreduce(xs, outs, rra.Codec("sparse", sparsity_threshold=0.5))
-    sparse_sent, _ = comm.get_bytes()
+    sparse_sent, sparse_recv = comm.get_bytes()
     assert comm.status() == rra.RRA_OK
-    check_sampled(xs, outs, N, T, 2, "bf16", "f32", codec="sparse", threshold=0.5)
-    all_ranks_identical(outs)
+    ref, rsent, rrecv = O.ring([host(x) for x in xs], "bf16", "f32", codec="sparse", threshold=0.5)
+    assert sparse_sent == [int(v) for v in rsent] and sparse_recv == [int(v) for v in rrecv]
+    for r in range(N):
+        assert_bits_equal(host(outs[r]), ref[r], f"rank {r}")
+    del ref
     lossless = [torch.empty(T, dtype=torch.float32, device="cuda") for _ in range(N)]
     comm.ring_allreduce(xs, lossless)
     lossless_sent, _ = comm.get_bytes()
     for r in range(N):
         assert torch.equal(outs[r].view(torch.int32), lossless[r].view(torch.int32)), r
-    # hop 1 is sent sparse (density 0.4): the sparse ring moves fewer bytes
-    # than 30 dense hops with headers would, more than 29 dense hops
+    # hop 1 (density 0.4) goes sparse, every later hop dense: 8 + 8 nnz bytes
+    # once, 8 + 4 n bytes for the other 29 messages a rank sends
     n = T // N
-    dense_hop = n * 4 + (n // 256) * 8
-    assert 29 * dense_hop < sparse_sent[0] < 30 * dense_hop
+    assert 29 * (8 + 4 * n) < sparse_sent[0] < 30 * (8 + 4 * n)
     assert lossless_sent[0] == 30 * n * 4
+    comm.close()
+
+
+def test_sparse_n16_full_size_per_slice():
+    """The per-slice option at full size: sampled slices are exact
+    sub-problems there (every slice decides on its own)."""
+    c = W.CONFIGS["sparse_n16"]
+    N, T = c["N"], c["T"]
+    xs = W.sparse(N, T, seed=c["seed"])
+    comm = rra.Comm(N, T, torch.bfloat16)
+    outs = [torch.empty(T, dtype=torch.float32, device="cuda") for _ in range(N)]
+    comm.ring_allreduce(xs, outs, rra.Codec("sparse", sparsity_threshold=0.5, granularity="slice"))
+    assert comm.status() == rra.RRA_OK
+    check_sampled(xs, outs, N, T, 2, "bf16", "f32", codec="sparse", threshold=0.5,
+                  slice=rra.RING_SLICE)
+    all_ranks_identical(outs)
     comm.close()
 
 

@@ -225,30 +225,154 @@ def test_bfp8_f16_outputs_across_exponents(in_dt, G):
 
 # ------------------------------------------------------------------ sparse
 
+SLICE_OF = {"chunk": None, "slice": rra.RING_SLICE}
+
+
+@pytest.mark.parametrize("gran", ["chunk", "slice"])
 @pytest.mark.parametrize("thr", [0.5, 0.2, 0.9])
 @pytest.mark.parametrize("in_dt", ["bf16", "f32", "f16"])
 @pytest.mark.parametrize("N,T", [(2, 1000), (5, 256 * 5 * 4), (16, 16 * 3000 + 5)])
-def test_sparse_ring(thr, in_dt, N, T):
+def test_sparse_ring(gran, thr, in_dt, N, T):
     xs = W.sparse(N, T, seed=N + T, dtype=TORCH_DT[in_dt])
     thr32 = float(np.float32(thr))
     out_dt = "f32"
-    codec = rra.Codec("sparse", sparsity_threshold=thr)
+    codec = rra.Codec("sparse", sparsity_threshold=thr, granularity=gran)
     gpu = run_ring(xs, out_dt, codec)
-    ref = oracle_ring(xs, in_dt, out_dt, codec="sparse", threshold=thr32)
-    compare(gpu, ref, f"sparse thr={thr}")
-    # lossless: equals the lossless ring bit for bit (no -0.0 in the inputs)
+    ref = oracle_ring(xs, in_dt, out_dt, codec="sparse", threshold=thr32, slice=SLICE_OF[gran])
+    compare(gpu, ref, f"sparse {gran} thr={thr}")
+    # lossless: equals the lossless ring bit for bit
     compare(run_ring(xs, out_dt), (ref[0], *oracle_ring(xs, in_dt, out_dt)[1:]), "vs lossless")
 
 
-def test_sparse_ring_all_zero_and_dense():
+@pytest.mark.parametrize("gran", ["chunk", "slice"])
+def test_sparse_ring_all_zero_and_dense(gran):
     N, T = 4, 4096
     zeros = [torch.zeros(T, device="cuda") for _ in range(N)]
-    codec = rra.Codec("sparse")
+    codec = rra.Codec("sparse", granularity=gran)
     gpu = run_ring(zeros, "f32", codec)
-    compare(gpu, oracle_ring(zeros, "f32", "f32", codec="sparse"), "zeros")
-    assert all(int(s) == 2 * (N - 1) * (T // N // 256) * 8 for s in gpu[1])  # headers only
+    compare(gpu, oracle_ring(zeros, "f32", "f32", codec="sparse", slice=SLICE_OF[gran]), "zeros")
+    msgs = 1 if gran == "chunk" else T // N // 256
+    assert all(int(s) == 2 * (N - 1) * msgs * 8 for s in gpu[1])  # headers only
     dense = rand_f32(N, T, seed=5)
-    compare(run_ring(dense, "f32", codec), oracle_ring(dense, "f32", "f32", codec="sparse"), "dense")
+    compare(run_ring(dense, "f32", codec),
+            oracle_ring(dense, "f32", "f32", codec="sparse", slice=SLICE_OF[gran]), "dense")
+
+
+def _sparse_with_minus_zero(N, T, seed, dt, p_zero=0.6):
+    xs = W.sparse(N, T, seed=seed, p_zero=p_zero, dtype=TORCH_DT[dt])
+    for r, x in enumerate(xs):
+        x[(r * 7) % 13::29] = -0.0
+    return xs
+
+
+@pytest.mark.parametrize("gran", ["chunk", "slice"])
+@pytest.mark.parametrize("in_dt", ["bf16", "f32"])
+def test_sparse_ring_minus_zero_is_lossless(gran, in_dt):
+    """The receiver adds the whole restored message, so -0.0 inputs give the
+    lossless ring's bits (a -0.0 meeting an omitted +0.0 becomes +0.0)."""
+    N, T = 6, 6 * 2048 + 30
+    xs = _sparse_with_minus_zero(N, T, 41, in_dt)
+    codec = rra.Codec("sparse", granularity=gran)
+    gpu = run_ring(xs, "f32", codec)
+    compare(gpu, oracle_ring(xs, in_dt, "f32", codec="sparse", slice=SLICE_OF[gran]), "-0.0")
+    lossless = run_ring(xs, "f32")
+    for r in range(N):
+        assert torch.equal(gpu[0][r].view(torch.int32), lossless[0][r].view(torch.int32))
+
+
+def _tie_inputs(N, T, dt, thr=0.5):
+    """Inputs whose hop-1 messages sit at the per-chunk decision's edge:
+    chunk c of rank c+1 has exactly ceil((1 - thr) n) nonzeros for even c
+    (dense, since sparse needs nnz < (1 - thr) n) and one fewer for odd c."""
+    n = -(-T // N)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234 + N)
+    xs = []
+    for r in range(N):
+        x = torch.zeros(T, device="cuda")
+        for c in range(N):
+            lo, hi = min(c * n, T), min((c + 1) * n, T)
+            if hi == lo:
+                continue
+            want = int(np.ceil((1 - thr) * (hi - lo)))
+            k = want - (c % 2) if (c + 1) % N == r else (hi - lo) // 3
+            k = max(0, min(k, hi - lo))
+            pos = torch.randperm(hi - lo, generator=g, device="cuda")[:k] + lo
+            x[pos] = torch.randn(k, generator=g, device="cuda") * 0.02 + 0.5
+        xs.append(x.to(TORCH_DT[dt]))
+    return xs
+
+
+@pytest.mark.parametrize("in_dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N,T", [(2, 2 * 4096), (5, 5 * 1000 + 3), (16, 16 * 2048 + 17)])
+def test_sparse_ring_per_chunk_decision_at_the_tie(in_dt, N, T):
+    """Per-chunk decisions on both sides of nnz = (1 - threshold) * n: values
+    and byte counters bit-exact against the oracle, allreduce and
+    reduce-scatter."""
+    xs = _tie_inputs(N, T, in_dt)
+    codec = rra.Codec("sparse", sparsity_threshold=0.5)
+    compare(run_ring(xs, "f32", codec), oracle_ring(xs, in_dt, "f32", codec="sparse"), "tie")
+    outs = [torch.full((T,), 7.0, device="cuda") for _ in range(N)]
+    ref_outs = [np.full(T, 7.0, np.float32) for _ in range(N)]
+    gpu = run_ring(xs, "f32", codec, mode="reduce_scatter", outs=outs)
+    ref = O.ring([host(x) for x in xs], in_dt, "f32", codec="sparse", mode="reduce_scatter",
+                 outputs=ref_outs)
+    compare(gpu, ref, "tie rs")
+
+
+@pytest.mark.parametrize("G,K", [(1, 1), (1, 2), (2, 2), (4, 2)])
+@pytest.mark.parametrize("N", [3, 8, 16])
+def test_sparse_ring_per_chunk_launch_shapes(G, K, N):
+    """Every slice width and mailbox depth moves the same per-chunk messages."""
+    T = N * 4096 * 3 + 8 * N
+    xs = _sparse_with_minus_zero(N, T, 50 + N, "bf16", p_zero=0.7)
+    comm = rra.Comm(N, T, torch.bfloat16)
+    comm.set_tuning(0, K, 0, G)
+    outs = [torch.empty(T, device="cuda") for _ in range(N)]
+    comm.ring_allreduce(xs, outs, rra.Codec("sparse"))
+    sent, recv = comm.get_bytes()
+    assert comm.status() == rra.RRA_OK
+    shape = comm.last_shape()
+    # 16 ranks' two-slot mailboxes of 4-group slices exceed the shared
+    # memory: the width is then reduced
+    assert shape[3] == G if not (N == 16 and G == 4) else shape[3] < G, shape
+    comm.close()
+    compare((outs, sent, recv), oracle_ring(xs, "bf16", "f32", codec="sparse"), f"G={G} K={K}")
+
+
+def test_sparse_ring_per_chunk_generic_path_and_in_place():
+    """Buffers off the 16-byte grid take the generic path (bounds-checked
+    loads, the count pass's scalar loads); in place, out = in."""
+    N, T = 5, 5 * 3001
+    base = _sparse_with_minus_zero(N, T + 1, 61, "f32")
+    xs = [b[1:] for b in base]  # 4-byte offset: no bulk copies
+    ref = oracle_ring(xs, "f32", "f32", codec="sparse")
+    compare(run_ring(xs, "f32", rra.Codec("sparse")), ref, "generic")
+    bufs = [x.clone() for x in _sparse_with_minus_zero(N, T, 62, "f32")]
+    ref = oracle_ring(bufs, "f32", "f32", codec="sparse")
+    comm = rra.Comm(N, T)
+    comm.ring_allreduce(bufs, bufs, rra.Codec("sparse"))
+    sent, recv = comm.get_bytes()
+    assert comm.status() == rra.RRA_OK
+    comm.close()
+    compare((bufs, sent, recv), ref, "in place")
+
+
+def test_sparse_ring_per_chunk_repeated_calls_and_other_ops():
+    """The count tables are reset by every call: a per-chunk sparse call
+    after other calls, and twice in a row on other data, on one comm."""
+    N, T = 8, 8 * 2048
+    comm = rra.Comm(N, T)
+    for seed in (1, 2):
+        xs = _sparse_with_minus_zero(N, T, 70 + seed, "f32", p_zero=0.3 + 0.4 * seed)
+        outs = [torch.empty(T, device="cuda") for _ in range(N)]
+        comm.ring_allreduce(xs, outs, rra.Codec("sparse"))
+        sent, recv = comm.get_bytes()
+        assert comm.status() == rra.RRA_OK
+        compare((outs, sent, recv), oracle_ring(xs, "f32", "f32", codec="sparse"), f"call {seed}")
+        comm.allgather([o.clone() for o in outs])
+        assert comm.status() == rra.RRA_OK
+    comm.close()
 
 
 # ------------------------------------------------------------------ diff / average / base
@@ -367,6 +491,22 @@ def test_allgather_codec_launch_shapes(G):
     assert comm.status() == rra.RRA_OK and comm.last_shape()[3] == G
     for q in range(N):
         assert_bits_equal(host(bufs[q]), ref[q], f"G={G} rank {q}")
+    assert comm.get_bytes() == (list(s), list(r))
+    comm.close()
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("N,T", [(3, 1000), (8, 8 * 2048 * 2 + 8 * 24), (16, 16 * 1024 * 3)])
+def test_allgather_codec_sparse_per_slice(dt, N, T):
+    """The per-slice option of the compressed allgather: one message per 256
+    elements of every owner's chunk."""
+    bufs = _allgather_inputs(N, T, dt, "sparse", seed=N * 7 + T)
+    ref, s, r = O.allgather_codec([host(b) for b in bufs], dt, "sparse", 8, slice=rra.RING_SLICE)
+    comm = rra.Comm(N, T, bufs[0].dtype)
+    comm.allgather(bufs, codec=rra.Codec("sparse", granularity="slice"))
+    assert comm.status() == rra.RRA_OK
+    for q in range(N):
+        assert_bits_equal(host(bufs[q]), ref[q], f"rank {q}")
     assert comm.get_bytes() == (list(s), list(r))
     comm.close()
 
