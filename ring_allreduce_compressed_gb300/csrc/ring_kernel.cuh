@@ -214,6 +214,13 @@ struct Msg {
     __device__ __forceinline__ int sparse() const { return fk & 1; }
     __device__ __forceinline__ int key() const { return fk >> 1; }
 };
+// A message known to be dense: a codec with both forms overloads its
+// operations on this type with dense-only code, so that steps whose
+// messages are all dense carry no sparse instructions.  The other codecs
+// take it as a Msg.
+struct DenseMsg : Msg {
+    __device__ __forceinline__ explicit DenseMsg(const Msg &m) : Msg(m) {}
+};
 
 // A message covers one slice of TW = 256*G elements.  The kernel streams it
 // group by group (8 elements per lane, 256 per warp): a WireCodec's per-group
@@ -433,9 +440,8 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     // the BFP8 allgather loop that writes fp16 straight from the codes and the
     // allgather loop of the sparse codec (slices of at most 4 groups); the
     // other loops stay rolled to keep the code within the instruction cache.
-    constexpr bool kSparseAny = CODEC == kCodecSparse || CODEC == kCodecSparseChunk;
     constexpr int kUnrollRS = CODEC != kCodecNone ? G : 1;
-    constexpr int kUnrollAG = kSparseAny ? G : 1;
+    constexpr int kUnrollAG = CODEC == kCodecSparse ? G : 1;
     const int N = a.N;
     const int W = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5;
@@ -571,6 +577,17 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
     const bool first_item_withhold = a.withhold_rank >= 0;
     int withhold_g = 0; // step whose send is withheld in this slice (0: none)
 
+    // run f(x, y) with the step's received and sent message; when both are
+    // dense, as DenseMsg (the per-chunk sparse codec's dense-only code)
+    auto with_msgs = [&](const Msg &x, const Msg &y, auto &&f) {
+        if constexpr (CODEC == kCodecSparseChunk) {
+            if (!x.sparse() && !y.sparse()) {
+                f(DenseMsg(x), DenseMsg(y));
+                return;
+            }
+        }
+        f(x, y);
+    };
     // the message of chunk c at hop h (h = N: the owner's) in the slice at t0
     auto msg_of = [&](int h, int c) -> Msg {
         if constexpr (CODEC == kCodecSparseChunk) {
@@ -777,39 +794,42 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                 // summed group by group below)
                 uint32_t rb = 0, sb = 0;
                 Reg m0;
-                if (g >= 2 && (kEarly || !C::kVarBytes)) {
-                    rb = C::bytes(V, rslot, a, rmsg);
-                    if (kEarly)
-                        release_early(r, rslot, rb, m0, rmsg);
-                }
+                if (g >= 2 && (kEarly || !C::kVarBytes))
+                    with_msgs(rmsg, smsg, [&](const auto &rm, const auto &) {
+                        rb = C::bytes(V, rslot, a, rm);
+                        if (kEarly)
+                            release_early(r, rslot, rb, m0, rm);
+                    });
                 if (!pre && !wait_ready(empty + dst * K + snd.slot, (uint32_t)(snd.phase ^ 1),
                                         a.timeout_ns, a.status)) {
                     ok = false;
                     break;
                 }
                 unsigned char *dslot = slots + (size_t)(dst * K + snd.slot) * a.slot_bytes;
+                with_msgs(rmsg, smsg, [&](const auto &rm, const auto &sm) {
 #pragma unroll kUnrollRS
-                for (int gi = 0; gi < G; ++gi) {
-                    float v[8];
-                    input_group(r, c, V, gi, sp, v);
-                    if (g >= 2) {
-                        Reg m;
-                        if (kEarly) {
-                            m = m0;
-                        } else {
-                            C::load(rslot, gi, lane, scratch, a, m, rmsg);
-                            if constexpr (C::kVarBytes)
-                                rb += C::group_bytes(m, V, gi, rmsg);
+                    for (int gi = 0; gi < G; ++gi) {
+                        float v[8];
+                        input_group(r, c, V, gi, sp, v);
+                        if (g >= 2) {
+                            Reg m;
+                            if (kEarly) {
+                                m = m0;
+                            } else {
+                                C::load(rslot, gi, lane, scratch, a, m, rm);
+                                if constexpr (C::kVarBytes)
+                                    rb += C::group_bytes(m, V, gi, rm);
+                            }
+                            C::decode_add(m, v, lane, scratch);
                         }
-                        C::decode_add(m, v, lane, scratch);
+                        if constexpr (EF)
+                            encode_ef(r, c, V, gi, v, dslot);
+                        else
+                            sb += C::template encode<false>(v, dslot, gi, lane, V, a, scratch, sm);
                     }
-                    if constexpr (EF)
-                        encode_ef(r, c, V, gi, v, dslot);
-                    else
-                        sb += C::template encode<false>(v, dslot, gi, lane, V, a, scratch, smsg);
-                }
-                if constexpr (!C::kVarBytes)
-                    sb = C::bytes(V, dslot, a, smsg);
+                    if constexpr (!C::kVarBytes)
+                        sb = C::bytes(V, dslot, a, sm);
+                });
                 finish_step(r, g, g >= 2 && !kEarly, true, rb, sb);
                 if (ONE)
                     break;
@@ -846,11 +866,14 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
             const unsigned char *rslot = slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
             const Msg rmsg = recv ? msg_of(N - 1, r) : Msg{0, 0};
             const Msg smsg = msg_of(N, r);
-            uint32_t rb = recv && (kEarly || !C::kVarBytes) ? C::bytes(V, rslot, a, rmsg) : 0u;
-            uint32_t sb = 0;
+            uint32_t rb = 0, sb = 0;
             Reg m0;
-            if (kEarly && recv)
-                release_early(r, rslot, rb, m0, rmsg);
+            if (recv && (kEarly || !C::kVarBytes))
+                with_msgs(rmsg, smsg, [&](const auto &rm, const auto &) {
+                    rb = C::bytes(V, rslot, a, rm);
+                    if (kEarly)
+                        release_early(r, rslot, rb, m0, rm);
+                });
             if (!pre && send &&
                 !wait_ready(empty + dst * K + snd.slot, (uint32_t)(snd.phase ^ 1), a.timeout_ns,
                             a.status)) {
@@ -895,29 +918,33 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     done = true;
                 }
             }
+            if (!done)
+                with_msgs(rmsg, smsg, [&](const auto &rm, const auto &sm) {
 #pragma unroll 1
-            for (int gi = 0; !done && gi < G; ++gi) {
-                float v[8];
-                input_group(r, r, V, gi, sp, v);
-                if (recv) {
-                    Reg m;
-                    if (kEarly) {
-                        m = m0;
-                    } else {
-                        C::load(rslot, gi, lane, scratch, a, m, rmsg);
-                        if constexpr (C::kVarBytes)
-                            rb += C::group_bytes(m, V, gi, rmsg);
+                    for (int gi = 0; gi < G; ++gi) {
+                        float v[8];
+                        input_group(r, r, V, gi, sp, v);
+                        if (recv) {
+                            Reg m;
+                            if (kEarly) {
+                                m = m0;
+                            } else {
+                                C::load(rslot, gi, lane, scratch, a, m, rm);
+                                if constexpr (C::kVarBytes)
+                                    rb += C::group_bytes(m, V, gi, rm);
+                            }
+                            C::decode_add(m, v, lane, scratch);
+                        }
+                        if (gather) {
+                            if constexpr (EF)
+                                encode_ef(r, r, V, gi, v, dslot);
+                            else
+                                sb += C::template encode<true>(v, dslot, gi, lane, V, a, scratch,
+                                                               sm);
+                        }
+                        output_group(r, r, V, gi, v);
                     }
-                    C::decode_add(m, v, lane, scratch);
-                }
-                if (gather) {
-                    if constexpr (EF)
-                        encode_ef(r, r, V, gi, v, dslot);
-                    else
-                        sb += C::template encode<true>(v, dslot, gi, lane, V, a, scratch, smsg);
-                }
-                output_group(r, r, V, gi, v);
-            }
+                });
             if constexpr (!C::kVarBytes)
                 sb = C::bytes(V, dslot, a, smsg);
             finish_step(r, N, recv && !kEarly, send, rb, send ? sb : 0u);
@@ -951,10 +978,14 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                     const unsigned char *rslot =
                         slots + (size_t)(r * K + rcv.slot) * a.slot_bytes;
                     const Msg amsg = msg_of(N, c); // the owner's message, forwarded unchanged
-                    uint32_t rb = (kEarly || !C::kVarBytes) ? C::bytes(V, rslot, a, amsg) : 0u;
+                    uint32_t rb = 0;
                     Reg m0;
-                    if (kEarly)
-                        release_early(r, rslot, rb, m0, amsg);
+                    if (kEarly || !C::kVarBytes)
+                        with_msgs(amsg, amsg, [&](const auto &am, const auto &) {
+                            rb = C::bytes(V, rslot, a, am);
+                            if (kEarly)
+                                release_early(r, rslot, rb, m0, am);
+                        });
                     if (!pre && fwd &&
                         !wait_ready(empty + dst * K + snd.slot, (uint32_t)(snd.phase ^ 1),
                                     a.timeout_ns, a.status)) {
@@ -993,24 +1024,25 @@ __global__ void __launch_bounds__(MODE == kRankPerWarp8 ? 8 * 32 : kMaxWarps * 3
                             done = true;
                         }
                     }
-                    if (!done) {
+                    if (!done)
+                        with_msgs(amsg, amsg, [&](const auto &am, const auto &) {
 #pragma unroll kUnrollAG
-                        for (int gi = 0; gi < G; ++gi) {
-                            Reg m;
-                            if (kEarly) {
-                                m = m0;
-                            } else {
-                                C::load(rslot, gi, lane, scratch, a, m, amsg);
-                                if constexpr (C::kVarBytes)
-                                    rb += C::group_bytes(m, V, gi, amsg);
+                            for (int gi = 0; gi < G; ++gi) {
+                                Reg m;
+                                if (kEarly) {
+                                    m = m0;
+                                } else {
+                                    C::load(rslot, gi, lane, scratch, a, m, am);
+                                    if constexpr (C::kVarBytes)
+                                        rb += C::group_bytes(m, V, gi, am);
+                                }
+                                if (fwd)
+                                    C::store(dslot, gi, lane, m, a, am);
+                                float v[8];
+                                C::values(m, v, lane, scratch);
+                                output_group(r, c, V, gi, v);
                             }
-                            if (fwd)
-                                C::store(dslot, gi, lane, m, a, amsg);
-                            float v[8];
-                            C::values(m, v, lane, scratch);
-                            output_group(r, c, V, gi, v);
-                        }
-                    }
+                        });
                     __syncwarp();
                     finish_step(r, g, !kEarly, fwd, rb, rb);
                     if (ONE)

@@ -12,6 +12,8 @@
 // (decompress, then reduce, §2.2), so P_h does not depend on the formats of
 // earlier hops, and one pass over the inputs -- each thread adding the ranks'
 // elements of one position in ring order -- gives every count.
+#include <algorithm>
+
 #include "ring_kernel.cuh"
 #include "wire_sparse.cuh"
 
@@ -26,13 +28,19 @@ constexpr int kCountWarps = kCountThreads / 32;
 // c = b / bpc; a warp takes 256 consecutive elements of the chunk at a time,
 // 8 per lane, and for each hop h adds rank (c + h) mod N's elements to its
 // running fp32 partial and counts the elements whose bits are not +0.0.
+// The raw 16-byte words of a batch of hops (16 words per lane: 16 hops of
+// 16-bit data, 8 of fp32, 4 of fp32 with a prev stream) are loaded before
+// any is used, so every lane keeps up to 16 loads in flight.
 template <int IN_KIND, bool VEC>
-__global__ void __launch_bounds__(kCountThreads)
+__global__ void __launch_bounds__(kCountThreads, 2)
     sparse_chunk_count_kernel(const __grid_constant__ SpCountArgs a)
 {
     constexpr bool PREV = IN_KIND == kF32Diff;
     constexpr int LT = PREV ? kF32 : IN_KIND;
     constexpr int es = dtype_size(LT);
+    constexpr int kWords = (es == 4 ? 2 : 1) * (PREV ? 2 : 1); // 16-byte words per hop
+    constexpr int kBatch = 16 / kWords;                         // hops per batch
+    using E = typename Elem<LT>::type;
     __shared__ unsigned long long s_cnt[kCountWarps][kMaxRanks];
     __shared__ bool s_last;
     const int N = a.N;
@@ -43,6 +51,57 @@ __global__ void __launch_bounds__(kCountThreads)
         (&s_cnt[0][0])[i] = 0ull;
     __syncthreads();
 
+    // the raw words of 8 elements of rank r at element offset off
+    auto fetch = [&](int r, long long off, uint4 (&w)[kWords]) {
+        const uint4 *src =
+            reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(a.in[r]) + off * es);
+#pragma unroll
+        for (int k = 0; k < (es == 4 ? 2 : 1); ++k)
+            w[k] = __ldg(src + k);
+        if constexpr (PREV) {
+            const uint4 *ps = reinterpret_cast<const uint4 *>(a.prev[r] + off);
+            w[2] = __ldg(ps);
+            w[3] = __ldg(ps + 1);
+        }
+    };
+    // the 8 fp32 input values (cur - prev with a prev stream) of raw words
+    auto widen = [&](const uint4 (&w)[kWords], float (&x)[8]) {
+        if constexpr (es == 4) {
+            const float *f = reinterpret_cast<const float *>(&w[0]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                x[i] = f[i];
+        } else {
+            const E *e = reinterpret_cast<const E *>(&w[0]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                x[i] = to_f32(e[i]);
+        }
+        if constexpr (PREV) {
+            const float *q = reinterpret_cast<const float *>(&w[2]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                x[i] = __fsub_rn(x[i], q[i]);
+        }
+    };
+    // the same from bounds-checked element loads (ragged end, unaligned)
+    auto load_scalar = [&](int r, long long off, int valid, float (&x)[8]) {
+        load8_scalar<LT>(reinterpret_cast<const char *>(a.in[r]) + off * es, valid, x);
+        if constexpr (PREV) {
+            float q[8];
+            load8_scalar<kF32>(a.prev[r] + off, valid, q);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                x[i] = __fsub_rn(x[i], q[i]);
+        }
+    };
+    auto rank_of = [&](int h) {
+        int r = c + h;
+        r -= r >= N ? N : 0;
+        r -= r >= N ? N : 0;
+        return r;
+    };
+
     const long long lo = min((long long)c * a.n, a.T);
     const long long len = min(lo + a.n, a.T) - lo;
     const long long wstride = (long long)a.bpc * kCountWarps * kTile;
@@ -50,49 +109,48 @@ __global__ void __launch_bounds__(kCountThreads)
         const long long e = w0 + 8 * lane; // chunk-relative first element of this lane
         const int valid = (int)min(max(len - e, 0LL), 8LL);
         const long long off = lo + e;
+        const bool vec = VEC && valid == 8;
         float p[8];
-#pragma unroll 4
-        for (int h = a.h_lo; h <= a.h_hi; ++h) {
-            int r = c + h;
-            r -= r >= N ? N : 0;
-            r -= r >= N ? N : 0;
-            float x[8];
-            const char *src = reinterpret_cast<const char *>(a.in[r]) + off * es;
-            if (VEC && valid == 8)
-                load8_vec<LT>(src, x);
-            else
-                load8_scalar<LT>(src, valid, x);
-            if constexpr (PREV) {
-                float q[8];
-                if (VEC && valid == 8)
-                    load8_vec<kF32>(a.prev[r] + off, q);
+        for (int h0 = a.h_lo; h0 <= a.h_hi; h0 += kBatch) {
+            uint4 w[kBatch][kWords];
+            if (vec) {
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j)
+                    if (h0 + j <= a.h_hi)
+                        fetch(rank_of(h0 + j), off, w[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int h = h0 + j;
+                if (h > a.h_hi)
+                    break;
+                float x[8];
+                if (vec)
+                    widen(w[j], x);
                 else
-                    load8_scalar<kF32>(a.prev[r] + off, valid, q);
+                    load_scalar(rank_of(h), off, valid, x);
+                if (h == a.h_lo) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    x[i] = __fsub_rn(x[i], q[i]);
-            }
-            if (h == a.h_lo) {
+                    for (int i = 0; i < 8; ++i)
+                        p[i] = x[i];
+                } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    p[i] = x[i];
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; i += 2) {
-                    const float2 s2 =
-                        __fadd2_rn(make_float2(x[i], x[i + 1]), make_float2(p[i], p[i + 1]));
-                    p[i] = s2.x;
-                    p[i + 1] = s2.y;
+                    for (int i = 0; i < 8; i += 2) {
+                        const float2 s2 = __fadd2_rn(make_float2(x[i], x[i + 1]),
+                                                     make_float2(p[i], p[i + 1]));
+                        p[i] = s2.x;
+                        p[i + 1] = s2.y;
+                    }
                 }
-            }
-            // positions past the chunk's end hold +0.0 on both sides
-            unsigned nz = 0;
+                // positions past the chunk's end hold +0.0 on both sides
+                unsigned nz = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                nz += __float_as_uint(p[i]) != 0u ? 1u : 0u;
-            const unsigned wc = __reduce_add_sync(kFull, nz);
-            if (lane == 0)
-                s_cnt[warp][h - a.h_lo] += wc;
+                for (int i = 0; i < 8; ++i)
+                    nz += __float_as_uint(p[i]) != 0u ? 1u : 0u;
+                const unsigned wc = __reduce_add_sync(kFull, nz);
+                if (lane == 0)
+                    s_cnt[warp][h - a.h_lo] += wc;
+            }
         }
     }
     __syncthreads();
@@ -129,7 +187,9 @@ template <int IN_KIND> const void *count_fn(bool vec)
 
 } // namespace
 
-cudaError_t launch_sparse_chunk_count(const SpCountArgs &a, int in_kind, bool vec,
+// One wave of resident blocks, split evenly over the chunks (at least one
+// block per chunk, at most one per 2048 elements of a chunk).
+cudaError_t launch_sparse_chunk_count(const SpCountArgs &args, int in_kind, bool vec,
                                       cudaStream_t st)
 {
     const void *fn = nullptr;
@@ -140,8 +200,18 @@ cudaError_t launch_sparse_chunk_count(const SpCountArgs &a, int in_kind, bool ve
     case kF32Diff: fn = count_fn<kF32Diff>(vec); break;
     default: return cudaErrorInvalidValue;
     }
-    void *args[] = {const_cast<SpCountArgs *>(&a)};
-    return cudaLaunchKernel(fn, dim3(a.N * a.bpc), dim3(kCountThreads), args, 0, st);
+    // resident blocks per SM of each variant, asked once
+    static int occ_cache[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int &occ = occ_cache[in_kind * 2 + (vec ? 1 : 0)];
+    if (occ < 1 &&
+        (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kCountThreads, 0) != cudaSuccess ||
+         occ < 1))
+        occ = 1;
+    SpCountArgs a = args;
+    const long long per_chunk = (a.n + kCountWarps * kTile - 1) / (kCountWarps * kTile);
+    a.bpc = (int)std::max(1LL, std::min(per_chunk, (long long)num_sms() * occ / a.N));
+    void *p[] = {&a};
+    return cudaLaunchKernel(fn, dim3(a.N * a.bpc), dim3(kCountThreads), p, 0, st);
 }
 
 const void *ring_fn_sparse_chunk(int in_t, bool fast, int groups, int mode)

@@ -54,6 +54,11 @@ struct rra_comm {
     // the count pass, [N*N] its result, and its block ticket
     unsigned long long *sp_acc = nullptr, *sp_out = nullptr;
     unsigned *sp_ticket = nullptr;
+    // per-chunk sparse codec: spill area for the pairs of a group beyond the
+    // 128 a slot holds; no launch needs more than the slots of all resident
+    // blocks, i.e. the shared memory of every SM
+    unsigned char *sp_spill = nullptr;
+    size_t sp_spill_bytes = 0;
     std::map<long long, int> occ; // (kernel key, smem) -> blocks per SM
 };
 
@@ -184,15 +189,16 @@ int sparse_icap(int lim) { return std::max(lim - 1, 0); }
 int sparse_sub_bytes(int lim) { return align_up(16 + std::max(kTile * 4, 8 * sparse_icap(lim)), 16); }
 
 // Bytes of one mailbox slot for a slice of 256 * groups elements.  The
-// per-chunk sparse slot: 32 header bytes, then room for 256 (value, index)
-// pairs per group (values region, then indices region).
+// per-chunk sparse slot: 32 header bytes, then a 1024-byte region per group
+// (256 fp32 values, or 128 (value, index) pairs; more pairs spill to global
+// memory).
 int slot_bytes_for(int codec, int groups, int sparse_lim)
 {
     switch (codec) {
     case kCodecNone: return kTile * 4 * groups;
     case kCodecBfp8: return 16 + kTile * groups;
     case kCodecBfp4: return 16 + kTile / 2 * groups;
-    case kCodecSparseChunk: return 32 + 2 * kTile * 4 * groups;
+    case kCodecSparseChunk: return 32 + kTile * 4 * groups;
     default: return sparse_sub_bytes(sparse_lim) * groups;
     }
 }
@@ -425,9 +431,12 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
     a.K = sh.K;
     a.D = sh.D;
     a.slot_bytes = slot_bytes_for(kc, groups, a.sp_full_lim);
-    if (kc == kCodecSparseChunk)
-        a.sp_sub = 32 + kTile * 4 * groups; // the indices region of a slot
     a.stage_bytes = kTile * groups * (cd.diff_prev ? 8 : (int)ies);
+    a.sp_spill = comm->sp_spill;
+    a.slots_off = make_layout(N, a.K, a.D, a.slot_bytes, a.stage_bytes, warps, fast,
+                              kc == kCodecSparse ? 1 : kc == kCodecSparseChunk ? 2 : 0,
+                              kc == kCodecBfp8)
+                      .slots;
     a.tiles = (a.n + kTile * groups - 1) / (kTile * groups);
     // every warp plays exactly one rank when N fits the block
     const int rmap = warps != N ? kRanksShared : (warps <= 8 ? kRankPerWarp8 : kRankPerWarp16);
@@ -438,6 +447,9 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
                           (fast ? 100 : 0) + rmap * 10 + groups;
     int per_sm = 0;
     const int grid = grid_for(comm, key, fn, warps, smem, a.tiles, t.blocks, &per_sm);
+    if (kc == kCodecSparseChunk &&
+        (size_t)grid * N * a.K * (size_t)(a.slot_bytes - 32) > comm->sp_spill_bytes)
+        return RRA_ERR_UNSUPPORTED; // cannot happen: the slots of all blocks fit the SMs
     comm->last = Tune{per_sm, a.K, a.D, groups};
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (kc == kCodecSparseChunk) {
@@ -457,10 +469,6 @@ rra_status ring_common(rra_comm *comm, int mode, const void *const *in, void *co
             ca.in[r] = in[r];
             ca.prev[r] = a.prev[r];
         }
-        // about eight 256-thread blocks per SM in all, each walking its
-        // chunk in 2048-element strides
-        const long long per_chunk = std::max(1LL, (a.n + 2047) / 2048);
-        ca.bpc = (int)std::min<long long>(per_chunk, std::max(1, num_sms() * 8 / N));
         bool vec = (a.n * (long long)ies) % 16 == 0;
         for (int r = 0; r < N; ++r)
             vec = vec && al16(in[r]) && (!cd.diff_prev || al16(cd.diff_prev[r]));
@@ -665,6 +673,14 @@ rra_status rra_comm_create(int nranks, size_t max_count, rra_dtype max_dtype, rr
     }
     c->sp_out = c->sp_acc + nn;
     c->sp_ticket = reinterpret_cast<unsigned *>(c->sp_out + nn);
+    c->sp_spill_bytes = (size_t)num_sms() * (size_t)c->smem_per_sm;
+    if (cudaMalloc(&c->sp_spill, c->sp_spill_bytes) != cudaSuccess) {
+        cudaFree(c->counters);
+        cudaFree(c->status);
+        cudaFree(c->sp_acc);
+        delete c;
+        return RRA_ERR_NOMEM;
+    }
     if (cudaMemset(c->sp_acc, 0, sbytes) != cudaSuccess ||
         cudaMemset(c->counters, 0, cbytes) != cudaSuccess ||
         cudaMemset(c->status, 0, sizeof(unsigned)) != cudaSuccess ||
@@ -672,6 +688,7 @@ rra_status rra_comm_create(int nranks, size_t max_count, rra_dtype max_dtype, rr
         cudaFree(c->counters);
         cudaFree(c->status);
         cudaFree(c->sp_acc);
+        cudaFree(c->sp_spill);
         delete c;
         return RRA_ERR_CUDA;
     }
@@ -687,6 +704,7 @@ rra_status rra_comm_destroy(rra_comm *comm)
     cudaFree(comm->counters);
     cudaFree(comm->status);
     cudaFree(comm->sp_acc);
+    cudaFree(comm->sp_spill);
     delete comm;
     return RRA_OK;
 }

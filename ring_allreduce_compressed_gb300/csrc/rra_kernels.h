@@ -50,10 +50,12 @@ struct RingArgs {
     double one_minus_thr; // sparse: a message is sparse iff nnz < one_minus_thr * len
     int sp_full_lim;      // per-slice sparse: a full 256-element slice is sparse iff nnz < sp_full_lim
     int sp_icap;          // per-slice sparse: most (value, index) pairs of a sparse group = lim - 1
-    int sp_sub;           // per-slice sparse: bytes of one group's sub-message in a slot;
-                          // per-chunk sparse: byte offset of the index region in a slot
+    int sp_sub;           // per-slice sparse: bytes of one group's sub-message in a slot
     const unsigned long long *sp_nnz; // per-chunk sparse: nnz[(h-1)*N + c] of the message of
                                       // chunk c at hop h (h = N: the owner's), from the count pass
+    unsigned char *sp_spill; // per-chunk sparse: the pairs of a group beyond the slot's 128,
+                             // (slot_bytes - 32) bytes per (block, slot)
+    int slots_off;           // byte offset of the mailbox slots in the block's shared memory
     unsigned long long timeout_ns;
     unsigned long long *sent; // [N] device counters of this call
     unsigned long long *recv; // [N]
@@ -99,7 +101,7 @@ struct CopyArgs {
 struct SpCountArgs {
     int N;
     int h_lo, h_hi;  // hops counted: allreduce 1..N, reduce-scatter 1..N-1, allgather N..N
-    int bpc;         // blocks per chunk
+    int bpc;         // blocks per chunk (set by the launcher)
     long long T, n;
     unsigned long long *acc; // [N * N], zero on entry
     unsigned long long *out; // [N * N]

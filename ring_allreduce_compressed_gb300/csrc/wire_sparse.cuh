@@ -235,33 +235,41 @@ template <> struct WireCodec<kCodecSparse> {
 //          indices int32 and relative to the chunk start.
 // The chunk's first slice also carries the message header {fmt, nnz}.
 // Slot layout (G groups of 256): bytes 0..8 the header {fmt, nnz} (first
-// slice only), bytes 16 + 4*gi the pair count of sparse group gi, fp32
-// values of group gi from 32 + 1024*gi, int32 indices of a sparse group gi
-// from a.sp_sub + 1024*gi (a.sp_sub = 32 + 1024*G).  A sparse group may list
-// up to all 256 of its elements (the decision is the chunk's, not the
-// group's), so each group has room for 256 pairs.  The pair counts in the
-// slot only frame the piece on chip; the receiver could read them off the
-// ascending indices, and they are not wire bytes.
+// slice only), bytes 16 + 4*gi the pair count of a sparse group gi, and the
+// 1024-byte region of group gi from 32 + 1024*gi: 256 fp32 values (dense),
+// or up to 128 pairs, values from byte 0 and indices from byte 512 of the
+// region (sparse).  A sparse chunk has fewer nonzeros than half its
+// elements, but one group of it may have more: pairs 128..255 of a group go
+// to the same layout in the slot's spill area in global memory
+// (a.sp_spill), which is written and read only then.  The pair counts only
+// frame the piece on chip; the receiver could read them off the ascending
+// indices, and they are not wire bytes.
 template <> struct WireCodec<kCodecSparseChunk> {
     static constexpr bool kVarBytes = true;
     static constexpr int kHdr = 32;
+    static constexpr int kRegion = kTile * 4;  // bytes of one group's region
+    static constexpr int kCap = kTile / 2;     // pairs of a group held in the slot
     struct Reg {
         uint32_t cnt; // pairs of a sparse group
         float f[8];   // restored values
     };
-    __device__ __forceinline__ static float *vals(const unsigned char *slot, int gi)
+    __device__ __forceinline__ static unsigned char *region(const unsigned char *slot, int gi)
     {
-        return reinterpret_cast<float *>(const_cast<unsigned char *>(slot) + kHdr + gi * kTile * 4);
-    }
-    __device__ __forceinline__ static int *idxs(const unsigned char *slot, int gi,
-                                                const RingArgs &a)
-    {
-        return reinterpret_cast<int *>(const_cast<unsigned char *>(slot) + a.sp_sub +
-                                       gi * kTile * 4);
+        return const_cast<unsigned char *>(slot) + kHdr + gi * kRegion;
     }
     __device__ __forceinline__ static uint32_t *counts(const unsigned char *slot)
     {
         return reinterpret_cast<uint32_t *>(const_cast<unsigned char *>(slot) + 16);
+    }
+    // group gi's spill region of this slot (rare path: a group of more than
+    // 128 nonzeros in a sparse chunk)
+    __device__ __forceinline__ static unsigned char *spill(const unsigned char *slot, int gi,
+                                                           const RingArgs &a)
+    {
+        extern __shared__ __align__(128) unsigned char smem[];
+        const long long si = (slot - (smem + a.slots_off)) / a.slot_bytes;
+        return a.sp_spill + ((long long)blockIdx.x * a.N * a.K + si) * (a.slot_bytes - kHdr) +
+               gi * kRegion;
     }
     __device__ __forceinline__ static int group_len(int V, int gi)
     {
@@ -295,42 +303,84 @@ template <> struct WireCodec<kCodecSparseChunk> {
                                                     const Msg &mg)
     {
         const int Vg = group_len(V, gi);
-        if (header_bytes(V, gi, mg) && lane == 0)
+        unsigned char *rg = region(slot, gi);
+        const uint32_t hb = header_bytes(V, gi, mg);
+        if (hb && lane == 0)
             *reinterpret_cast<uint2 *>(slot) =
                 make_uint2((uint32_t)mg.sparse(), (uint32_t)a.sp_nnz[mg.key()]);
         if (!mg.sparse()) {
-            float4 *p = reinterpret_cast<float4 *>(vals(slot, gi)) + 2 * lane;
+            float4 *p = reinterpret_cast<float4 *>(rg) + 2 * lane;
             p[0] = make_float4(v[0], v[1], v[2], v[3]);
             p[1] = make_float4(v[4], v[5], v[6], v[7]);
-            return header_bytes(V, gi, mg) + 4u * (uint32_t)Vg;
+            return hb + 4u * (uint32_t)Vg;
         }
         const uint32_t nzm = SparseWarp::nonzero_mask(v, lane, Vg);
         const int cnt = __popc(nzm);
         const int incl = SparseWarp::incl_scan(lane, cnt);
-        SparseWarp::write_pairs(vals(slot, gi), idxs(slot, gi, a), incl - cnt, lane,
-                                mg.base + gi * kTile, v, nzm);
         const int total = __shfl_sync(kFull, incl, 31);
+        const int ix0 = mg.base + gi * kTile;
+        if (total <= kCap) {
+            SparseWarp::write_pairs(reinterpret_cast<float *>(rg),
+                                    reinterpret_cast<int *>(rg + kRegion / 2), incl - cnt, lane,
+                                    ix0, v, nzm);
+        } else {
+            unsigned char *sp = spill(slot, gi, a);
+            int pos = incl - cnt;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if ((nzm >> i) & 1u) {
+                    unsigned char *b = pos < kCap ? rg : sp;
+                    const int k = pos < kCap ? pos : pos - kCap;
+                    reinterpret_cast<float *>(b)[k] = v[i];
+                    reinterpret_cast<int *>(b + kRegion / 2)[k] = ix0 + 8 * lane + i;
+                    ++pos;
+                }
+        }
         if (lane == 0)
             counts(slot)[gi] = (uint32_t)total;
-        return header_bytes(V, gi, mg) + 8u * (uint32_t)total;
+        return hb + 8u * (uint32_t)total;
     }
     __device__ __forceinline__ static void load(const unsigned char *slot, int gi, int lane,
                                                 unsigned char *scratch, const RingArgs &a,
                                                 Reg &m, const Msg &mg)
     {
+        const unsigned char *rg = region(slot, gi);
         if (!mg.sparse()) {
-            const float4 *p = reinterpret_cast<const float4 *>(vals(slot, gi)) + 2 * lane;
+            const float4 *p = reinterpret_cast<const float4 *>(rg) + 2 * lane;
             const float4 x = p[0], y = p[1];
             m.f[0] = x.x; m.f[1] = x.y; m.f[2] = x.z; m.f[3] = x.w;
             m.f[4] = y.x; m.f[5] = y.y; m.f[6] = y.z; m.f[7] = y.w;
             m.cnt = 0;
             return;
         }
-        m.cnt = min(counts(slot)[gi], (uint32_t)kTile);
-        SparseWarp::restore(vals(slot, gi), idxs(slot, gi, a), (int)m.cnt, mg.base + gi * kTile,
-                            lane, scratch, m.f);
+        // decompress: zeros, then every listed value at its index
+        const int cnt = (int)min(counts(slot)[gi], (uint32_t)kTile);
+        m.cnt = (uint32_t)cnt;
+        const int ix0 = mg.base + gi * kTile;
+        float *sval = reinterpret_cast<float *>(scratch);
+        float4 *mine = reinterpret_cast<float4 *>(sval) + 2 * lane;
+        mine[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        mine[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        __syncwarp();
+        const float *vs = reinterpret_cast<const float *>(rg);
+        const int *is = reinterpret_cast<const int *>(rg + kRegion / 2);
+        for (int k = lane; k < min(cnt, kCap); k += 32)
+            sval[(is[k] - ix0) & (kTile - 1)] = vs[k]; // in range for any slot contents
+        if (cnt > kCap) {
+            const unsigned char *sp = spill(slot, gi, a);
+            const float *vo = reinterpret_cast<const float *>(sp);
+            const int *io = reinterpret_cast<const int *>(sp + kRegion / 2);
+            for (int k = lane; k < cnt - kCap; k += 32)
+                sval[(io[k] - ix0) & (kTile - 1)] = vo[k];
+        }
+        __syncwarp();
+        const float4 x = mine[0], y = mine[1];
+        m.f[0] = x.x; m.f[1] = x.y; m.f[2] = x.z; m.f[3] = x.w;
+        m.f[4] = y.x; m.f[5] = y.y; m.f[6] = y.z; m.f[7] = y.w;
+        __syncwarp();
     }
-    // forward the owner's piece unchanged (allgather pass)
+    // forward the owner's piece unchanged (allgather pass): its restored
+    // values list exactly the same nonzeros
     __device__ __forceinline__ static void store(unsigned char *slot, int gi, int lane,
                                                  const Reg &m, const RingArgs &a, const Msg &mg)
     {
@@ -341,6 +391,53 @@ template <> struct WireCodec<kCodecSparseChunk> {
     __device__ __forceinline__ static uint32_t encode(float (&v)[8], unsigned char *slot, int gi,
                                                       int lane, int V, const RingArgs &a,
                                                       unsigned char *, const Msg &mg)
+    {
+        return emit(slot, gi, lane, v, V, a, mg);
+    }
+
+    // ---- the same operations for a step whose messages are all dense
+    __device__ __forceinline__ static uint32_t bytes(int V, const unsigned char *,
+                                                     const RingArgs &, const DenseMsg &mg)
+    {
+        return header_bytes(V, 0, mg) + 4u * (uint32_t)V;
+    }
+    __device__ __forceinline__ static uint32_t group_bytes(const Reg &, int V, int gi,
+                                                           const DenseMsg &mg)
+    {
+        return header_bytes(V, gi, mg) + 4u * (uint32_t)group_len(V, gi);
+    }
+    __device__ __forceinline__ static uint32_t emit(unsigned char *slot, int gi, int lane,
+                                                    const float (&v)[8], int V, const RingArgs &a,
+                                                    const DenseMsg &mg)
+    {
+        const uint32_t hb = header_bytes(V, gi, mg);
+        if (hb && lane == 0)
+            *reinterpret_cast<uint2 *>(slot) = make_uint2(0u, (uint32_t)a.sp_nnz[mg.key()]);
+        float4 *p = reinterpret_cast<float4 *>(region(slot, gi)) + 2 * lane;
+        p[0] = make_float4(v[0], v[1], v[2], v[3]);
+        p[1] = make_float4(v[4], v[5], v[6], v[7]);
+        return hb + 4u * (uint32_t)group_len(V, gi);
+    }
+    __device__ __forceinline__ static void load(const unsigned char *slot, int gi, int lane,
+                                                unsigned char *, const RingArgs &, Reg &m,
+                                                const DenseMsg &)
+    {
+        const float4 *p = reinterpret_cast<const float4 *>(region(slot, gi)) + 2 * lane;
+        const float4 x = p[0], y = p[1];
+        m.f[0] = x.x; m.f[1] = x.y; m.f[2] = x.z; m.f[3] = x.w;
+        m.f[4] = y.x; m.f[5] = y.y; m.f[6] = y.z; m.f[7] = y.w;
+        m.cnt = 0;
+    }
+    __device__ __forceinline__ static void store(unsigned char *slot, int gi, int lane,
+                                                 const Reg &m, const RingArgs &a,
+                                                 const DenseMsg &mg)
+    {
+        emit(slot, gi, lane, m.f, kTile * (gi + 1), a, mg);
+    }
+    template <bool DEC>
+    __device__ __forceinline__ static uint32_t encode(float (&v)[8], unsigned char *slot, int gi,
+                                                      int lane, int V, const RingArgs &a,
+                                                      unsigned char *, const DenseMsg &mg)
     {
         return emit(slot, gi, lane, v, V, a, mg);
     }

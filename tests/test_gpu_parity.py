@@ -320,6 +320,36 @@ def test_sparse_ring_per_chunk_decision_at_the_tie(in_dt, N, T):
     compare(gpu, ref, "tie rs")
 
 
+@pytest.mark.parametrize("G", [1, 2, 4])
+def test_sparse_ring_per_chunk_clustered_nonzeros(G):
+    """A chunk can be sparse overall while some of its 256-element groups are
+    dense: their pairs beyond the 128 a slot holds take the spill path.  Every
+    chunk here has its nonzeros packed at its start (a fifth of it), so whole
+    groups are fully nonzero in sparse messages."""
+    N, T = 8, 8 * 4096 * 2
+    n = T // N
+    g = torch.Generator(device="cuda")
+    g.manual_seed(99)
+    xs = []
+    for r in range(N):
+        x = torch.zeros(T, device="cuda")
+        for c in range(N):
+            k = n // 5 + 37 * r
+            x[c * n: c * n + k] = torch.randn(k, generator=g, device="cuda") + 3.0
+        xs.append(x)
+    comm = rra.Comm(N, T)
+    comm.set_tuning(0, 0, 0, G)
+    outs = [torch.empty(T, device="cuda") for _ in range(N)]
+    comm.ring_allreduce(xs, outs, rra.Codec("sparse"))
+    sent, recv = comm.get_bytes()
+    assert comm.status() == rra.RRA_OK
+    comm.close()
+    ref = oracle_ring(xs, "f32", "f32", codec="sparse")
+    compare((outs, sent, recv), ref, f"clustered G={G}")
+    # every hop's partial keeps the packed prefix: all messages sparse
+    assert all(int(v) < 2 * (N - 1) * (8 + 4 * n) * 0.5 for v in sent)
+
+
 @pytest.mark.parametrize("G,K", [(1, 1), (1, 2), (2, 2), (4, 2)])
 @pytest.mark.parametrize("N", [3, 8, 16])
 def test_sparse_ring_per_chunk_launch_shapes(G, K, N):
@@ -333,9 +363,7 @@ def test_sparse_ring_per_chunk_launch_shapes(G, K, N):
     sent, recv = comm.get_bytes()
     assert comm.status() == rra.RRA_OK
     shape = comm.last_shape()
-    # 16 ranks' two-slot mailboxes of 4-group slices exceed the shared
-    # memory: the width is then reduced
-    assert shape[3] == G if not (N == 16 and G == 4) else shape[3] < G, shape
+    assert shape[3] == G, shape
     comm.close()
     compare((outs, sent, recv), oracle_ring(xs, "bf16", "f32", codec="sparse"), f"G={G} K={K}")
 
