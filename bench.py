@@ -159,7 +159,7 @@ RING_KERNEL_COMMON = ("ring_kernel.cuh", "rra_device.cuh", "rra_kernels.h")
 RING_KERNEL_SOURCES = {
     "bfp8_bucket": ("ring_bfp8.cu", "ring_bfp8_ef.cu"),
     "diloco_n8": ("ring_bfp4.cu", "ring_bfp4_ef.cu"),
-    "sparse_n16": ("ring_sparse.cu", "wire_sparse.cuh"),
+    "sparse_n16": ("ring_sparse_chunk.cu", "wire_sparse.cuh"),
     "bfp8_allgather": ("ring_bfp8.cu",),
     "bfp8_broadcast": ("coll_kernels.cu",),
     "lossless_n4": ("ring_none.cu",),
@@ -195,7 +195,7 @@ def traffic_from_profile(config: str):
         return None, "summary incomplete"
     if m_sha.group(1) != kernel_sources_sha(config):
         return None, "kernel changed since the ncu capture"
-    return int(m_tr.group(1)), path
+    return int(m_tr.group(1)), os.path.relpath(path, ROOT)
 
 
 # ---------------------------------------------------------------- workloads
@@ -252,7 +252,8 @@ class Workload:
             self.out_dtype = torch.float32
             self.codec_name = "sparse"
             self.desc = ("sparse-format ring allreduce: N=16 x 64 Mi bf16, zero w.p. 0.6 else "
-                         "N(0,0.02^2), seed 2, threshold 0.5 per 256-element slice, fp32 out")
+                         "N(0,0.02^2), seed 2, threshold 0.5, one message per ring chunk and "
+                         "hop (values + int32 indices, or dense fp32), fp32 out")
         elif name == "diloco_n8":
             self.inputs, self.prev = W.diloco(self.N, self.T, seed=c["seed"], device=device)
             self.out_dtype = torch.float32
@@ -303,6 +304,16 @@ class Workload:
             self.compulsory = self.N * (n * ies + self.T * oes)
         if name == "bfp8_broadcast":  # the root reads its buffer, every rank writes its own
             self.compulsory = self.T * ies + self.N * self.T * oes
+        # algorithmic bytes of one step: the compulsory traffic, plus, for the
+        # per-chunk sparse ring, the count pass that reads every input once
+        # more before the ring starts (one step = two kernels)
+        self.alg_bytes = self.compulsory
+        self.kernels = "ring_kernel"
+        self.launches_per_step = 1
+        if name == "sparse_n16":
+            self.alg_bytes += self.N * self.T * ies
+            self.kernels = "sparse_chunk_count_kernel + ring_kernel"
+            self.launches_per_step = 2
 
     def step(self, stream=None):
         if self.name == "bfp8_allgather":
@@ -403,8 +414,11 @@ def cpu_baseline(wl: Workload, budget_s: float = 20.0):
                           "seconds": dt_all, "split": "contiguous slice groups, one thread each"},
             "sample": ("the full workload" if full else
                        f"first {slices} of {-(-n // 256)} 256-element slices of every chunk "
-                       f"({slices * 256 * wl.N} of {wl.T} elements per rank; slices are "
-                       "independent, so the sample is an exact sub-problem)")}
+                       f"({slices * 256 * wl.N} of {wl.T} elements per rank; " +
+                       ("run as its own N-rank problem: one sparse message per chunk of the "
+                        "sample, so the same work per element as the whole)"
+                        if wl.codec_name == "sparse" else
+                        "slices are independent, so the sample is an exact sub-problem)"))}
 
 
 # ---------------------------------------------------------------- arms
@@ -421,8 +435,26 @@ def run_rra(args, world, rank, local):
     assert wl.comm.status() == rra.RRA_OK
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
+    # The K timed steps are one CUDA graph of K back-to-back calls, so the
+    # host's per-call cost (argument marshalling, launch) stays outside the
+    # device timeline; the same calls made eagerly, one event pair per step,
+    # are timed afterwards for comparison.
+    graph = None
+    if not args.eager:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            gs = torch.cuda.Stream()
+            gs.wait_stream(stream)
+            with torch.cuda.stream(gs):
+                with torch.cuda.graph(graph, stream=gs):
+                    for _ in range(K):
+                        wl.step()
+            stream.wait_stream(gs)
+            graph.replay()  # one untimed replay: the graph's own warm-up
+            torch.cuda.synchronize()
+            assert wl.comm.status() == rra.RRA_OK
+        except RuntimeError:
+            graph = None
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
@@ -430,21 +462,39 @@ def run_rra(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     t_start.record(stream)
-    for k in range(K):
-        ev[k][0].record(stream)
-        wl.step()
-        ev[k][1].record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for k in range(K):
+            wl.step()
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
     status = wl.comm.status()
     total_ms = t_start.elapsed_time(t_end)
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    kern_ms = sum(step_ms) / K
-    kern_ms_median = max_over_ranks(world, statistics.median(step_ms))
     ms_step = max_over_ranks(world, total_ms / K)
-    kern_ms = max_over_ranks(world, kern_ms)
+    # per-step device time (the step's kernels back to back): from the graph,
+    # the timed region over K; eagerly, one event pair per step
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    for k in range(K):
+        ev[k][0].record(stream)
+        wl.step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    eager = {"ms_mean": statistics.mean(step_ms), "ms_median": statistics.median(step_ms),
+             "note": "the same steps launched one by one from Python, one event pair each "
+                     "(includes any wait for the host's launch)"}
+    graph_used = graph is not None
+    if graph_used:
+        kern_ms = ms_step
+        kern_ms_median = ms_step
+        del graph
+    else:
+        kern_ms = max_over_ranks(world, sum(step_ms) / K)
+        kern_ms_median = max_over_ranks(world, statistics.median(step_ms))
 
     value = whole_job_gbs(world, wl.payload, ms_step)
 
@@ -479,7 +529,7 @@ def run_rra(args, world, rank, local):
                    "replays": reps, "note": "median over CUDA-graph replays of back-to-back "
                    "calls; excludes the host launch cost that the per-step events include"}
     peak, peak_src = hbm_peak()
-    achieved = wl.compulsory / (kern_ms * 1e-3) / 1e9
+    achieved = wl.alg_bytes / (kern_ms * 1e-3) / 1e9
     traffic, traffic_src = traffic_from_profile(args.config)
 
     # end to end: pinned host inputs in, results out, through the public API.
@@ -565,25 +615,31 @@ def run_rra(args, world, rank, local):
                    "in_dtype": DT_NAME[wl.in_dtype], "out_dtype": DT_NAME[wl.out_dtype],
                    "codec": wl.codec_name, "parallelism": f"replicas x{world}",
                    "l2": wl.l2_note()},
-        "hbm_pct": 100.0 * achieved / peak,
+        "hbm_pct": 100.0 * wl.compulsory / (kern_ms * 1e-3) / 1e9 / peak,
         "busbw": value * 2 * (wl.N - 1) / wl.N,
         "bytes_sent_per_rank": sent[0],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": KERNEL_OF.get(args.config, "ring_kernel"), "kernel_ms": kern_ms,
-                     "bytes_per_launch": wl.compulsory,
+                     "kernel": KERNEL_OF.get(args.config, wl.kernels), "kernel_ms": kern_ms,
+                     "bytes_per_launch": wl.alg_bytes,
                      "kernel_ms_median": kern_ms_median,
+                     "timing": ("CUDA graph of the K timed calls: kernel_ms = timed region / K"
+                                if graph_used else "eager: one event pair per step"),
+                     "frac_compulsory": wl.compulsory / (kern_ms * 1e-3) / 1e9 / peak,
                      # the slot-materialised model: every wire byte written to a
                      # slot and read back once, beside the compulsory bytes (the
                      # slots live in shared memory here, so this can exceed 1)
                      "bytes_alg_slots": wl.compulsory + 2 * sum(sent),
                      "frac_alg_slots": (wl.compulsory + 2 * sum(sent)) / (kern_ms * 1e-3) / 1e9 / peak,
-                     "bytes_model": "compulsory: N*T*(in+out) (+ diff prev and base)",
+                     "bytes_model": ("compulsory: N*T*(in+out) (+ diff prev and base)" +
+                                     ("; + N*T*in for the count pass" if wl.alg_bytes > wl.compulsory
+                                      else "")),
                      "peak_source": peak_src, "traffic_source": traffic_src},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "latency": latency,
-        "gpu_launches": K,
+        "eager": eager,
+        "gpu_launches": K * wl.launches_per_step,
         "clocks": clk,
         "status": rra.status_string(status),
     }
@@ -897,6 +953,8 @@ def main():
                          "ncu captures, reported with its own T (not the metric's workload)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the K steps launched one by one instead of as one CUDA graph")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=60.0)
     ap.add_argument("--jsonl", default=None)

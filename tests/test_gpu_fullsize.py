@@ -121,6 +121,7 @@ def test_diloco_n8_full_size():
     always among the sampled slices)."""
     c = W.CONFIGS["diloco_n8"]
     N, T = c["N"], c["T"]
+    torch.cuda.empty_cache()  # blocks cached by earlier tests count as free
     free, _ = torch.cuda.mem_get_info()
     if free < 110 * 2 ** 30:
         pytest.skip("needs ~110 GB of device memory")
@@ -152,6 +153,7 @@ def test_diloco_n8_full_size():
 def test_sweep_extremes_ring_and_tree(N, T):
     """Message-size sweep corners: 1 KiB and 1 GiB per rank, N up to 64,
     lossless fp32, ring and tree, in place."""
+    torch.cuda.empty_cache()
     free, _ = torch.cuda.mem_get_info()
     if free < N * T * 4 * 1.3 + 2 ** 30:
         pytest.skip("not enough device memory")

@@ -588,12 +588,10 @@ def test_allgather_codec_argument_errors():
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("N", [1, 2, 3, 5, 8, 13, 64])
-@pytest.mark.parametrize("root", [0, 2])
+@pytest.mark.parametrize("N,root", [(N, root) for N in (1, 2, 3, 5, 8, 13, 64) for root in (0, 2)
+                                    if root < N])
 @pytest.mark.parametrize("T", [777, 8192])
 def test_broadcast(dt, N, root, T):
-    if root >= N:
-        pytest.skip("root outside the group")
     bufs = cast(rand_f32(N, T, seed=N * 3 + root), dt)
     ref, s, r = O.broadcast([host(b) for b in bufs], dt, root)
     comm = rra.Comm(N, T, bufs[0].dtype)
