@@ -712,7 +712,7 @@ def run_codecs(args, world, rank):
     if rank != 0:
         return
     peak, peak_src = hbm_peak()
-    n = 1 << 28
+    n = args.codec_n
     g = torch.Generator(device="cuda")
     g.manual_seed(6)
     x16 = (torch.randn(n, generator=g, device="cuda") * 1e-3).half()
@@ -953,6 +953,8 @@ def main():
                          "ncu captures, reported with its own T (not the metric's workload)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--codec-n", type=int, default=1 << 28,
+                    help="--codecs: elements per codec call (a smaller case for ncu captures)")
     ap.add_argument("--eager", action="store_true",
                     help="time the K steps launched one by one instead of as one CUDA graph")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

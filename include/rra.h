@@ -330,8 +330,11 @@ rra_status rra_bfp_decode(const int8_t *exps, const uint8_t *mants, size_t n, in
  *  vals   device, n elements of dtype capacity.  Sparse: the nnz nonzero
  *         values in index order.  Dense: a copy of x.
  *  idx    device, n int32 capacity.  Sparse: the nnz indices, ascending.
- * Sparse iff nnz < (1 - threshold) * n (evaluated in double).
- * Uses scratch (one uint32 per 4096 elements) from a workspace per device
+ * Sparse iff nnz < (1 - threshold) * n (evaluated in double).  Three
+ * passes: a count per 4096-element tile, an exclusive scan of the counts,
+ * and an emit pass that writes each tile's nonzeros at its offset (or copies
+ * x when the message is dense; idx is then left as it was).
+ * Uses scratch (one uint32 per 4096 elements, one per 4096 tiles) from a workspace per device
  * and stream that the library allocates with cudaMalloc on the first call
  * that needs more than it holds (so that first call must not be made during
  * stream capture).  Encodes on different streams may overlap: each stream
@@ -342,24 +345,28 @@ rra_status rra_sparse_encode(const void *x, size_t n, rra_dtype dtype, float thr
                              uint32_t *hdr, void *vals, int32_t *idx, void *stream);
 
 /* Largest n that rra_sparse_encode_noalloc accepts: its fixed scratch holds
- * one 32-bit count per 4096 elements, 65536 counts (256 KiB). */
+ * one 32-bit count per 4096 elements and one total per 4096 counts. */
 #define RRA_NOALLOC_MAX_COUNT (65536ull * 4096ull)
 
 /*
  * rra_sparse_encode for callers that cannot allocate device memory (the
  * pages have no counterpart; it is a deployment variant of the sparse
- * encoder).  Same arguments, output and errors as rra_sparse_encode, except:
+ * encoder).  Such callers are processes whose device memory is handed out by
+ * their own allocator or budgeted up front, latency-critical loops that
+ * cannot take an allocation's implicit device synchronisation, and libraries
+ * that must not call the CUDA allocator behind their host framework's back.
+ * Same arguments, output and errors as rra_sparse_encode, except:
  *  - it never allocates: no cudaMalloc, cudaFree or allocating library call.
- *    Its scratch is a fixed array inside the library (256 KiB of device
- *    memory on every GPU that loads the library, held until the process
- *    exits).  This suits callers that may not allocate: code recorded into a
- *    CUDA graph while capturing, latency-critical loops, processes whose
- *    device memory is owned by their own allocator or budgeted up front.
+ *    Its scratch is a fixed array inside the library (about 256 KiB of
+ *    device memory on every GPU that loads the library, held until the
+ *    process exits).
  *  - n may not exceed RRA_NOALLOC_MAX_COUNT (2^28 elements); larger n returns
  *    RRA_ERR_INVALID without doing anything (use rra_sparse_encode then).
  *  - the first call on a device looks up the scratch array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before starting any stream capture.
+ *    (cudaGetSymbolAddress) with that device current, and keeps it for the
+ *    rest of the process; after cudaDeviceReset the function must not be
+ *    called again.  Make the first call on each device before starting any
+ *    stream capture.
  *  - all calls share the one scratch array, and each call overwrites the
  *    part it uses before reading it, so no clearing is needed between calls;
  *    calls that overlap on the GPU (different streams without ordering

@@ -224,36 +224,30 @@ __global__ void __launch_bounds__(kThreads) sparse_count_kernel(const void *__re
     }
 }
 
-// Single block of 1024 threads: exclusive scan of the tile counts in place,
-// header {sparse?, nnz}.  Each thread owns a contiguous run of counts, read
-// in batches of 8 independent loads; the runs' totals are scanned with warp
-// shuffles and one shared-memory pass over the 32 warp totals.
-__global__ void __launch_bounds__(1024) sparse_scan_kernel(uint32_t *counts, long long tiles,
-                                                           long long n, double one_minus_thr,
-                                                           uint32_t *hdr)
+// Exclusive prefix of the tile counts, in place, in segments of kSegTiles
+// tiles: block s scans segment s (every thread four consecutive counts, one
+// 16-byte load; warp shuffles; one shared-memory pass over the warp totals)
+// and writes the segment's total to seg[s].  A tile's offset in the output is
+// then its in-segment prefix plus the totals of the segments before it.
+constexpr int kSegTiles = 4096;
+constexpr int kScanThreads = kSegTiles / 4;
+
+__global__ void __launch_bounds__(kScanThreads) sparse_segscan_kernel(uint32_t *counts,
+                                                                      long long tiles,
+                                                                      uint32_t *seg)
 {
-    __shared__ unsigned long long wsum[32];
+    __shared__ uint32_t wsum[kScanThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const long long per = (tiles + 1023) / 1024;
-    const long long lo = min(tiles, (long long)threadIdx.x * per);
-    const long long hi = min(tiles, lo + per);
-    unsigned long long s = 0;
-    long long i = lo;
-    for (; i + 8 <= hi; i += 8) {
-        uint32_t v[8];
+    const long long t0 = (long long)blockIdx.x * kSegTiles + 4LL * threadIdx.x;
+    uint32_t v[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            v[j] = counts[i + j];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            s += v[j];
-    }
-    for (; i < hi; ++i)
-        s += counts[i];
-    unsigned long long incl = s;
+    for (int j = 0; j < 4; ++j)
+        v[j] = t0 + j < tiles ? counts[t0 + j] : 0u;
+    const uint32_t s = v[0] + v[1] + v[2] + v[3];
+    uint32_t incl = s;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long t = __shfl_up_sync(kFull, incl, o);
+        const uint32_t t = __shfl_up_sync(kFull, incl, o);
         if (lane >= o)
             incl += t;
     }
@@ -261,128 +255,206 @@ __global__ void __launch_bounds__(1024) sparse_scan_kernel(uint32_t *counts, lon
         wsum[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        unsigned long long w = wsum[lane];
+        uint32_t w = wsum[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long t = __shfl_up_sync(kFull, w, o);
+            const uint32_t t = __shfl_up_sync(kFull, w, o);
             if (lane >= o)
                 w += t;
         }
         wsum[lane] = w; // inclusive totals of warps 0..lane
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned long long total = wsum[31];
-        hdr[0] = (double)total < one_minus_thr * (double)n ? 1u : 0u;
-        hdr[1] = (uint32_t)total;
-    }
-    unsigned long long run = (warp > 0 ? wsum[warp - 1] : 0ull) + incl - s;
-    i = lo;
-    for (; i + 8 <= hi; i += 8) {
-        uint32_t v[8];
+    uint32_t run = (warp > 0 ? wsum[warp - 1] : 0u) + incl - s;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            v[j] = counts[i + j];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            counts[i + j] = (uint32_t)run;
+    for (int j = 0; j < 4; ++j)
+        if (t0 + j < tiles) {
+            counts[t0 + j] = run;
             run += v[j];
         }
-    }
-    for (; i < hi; ++i) {
-        const uint32_t v = counts[i];
-        counts[i] = (uint32_t)run;
-        run += v;
-    }
+    if (threadIdx.x == 0)
+        seg[blockIdx.x] = wsum[kScanThreads / 32 - 1];
 }
 
+// Exclusive prefix of a thread's count c (0..8) over the lanes of its warp,
+// and the warp's total, from four ballots of the count's bits.
+__device__ __forceinline__ uint32_t warp_prefix8(uint32_t c, int lane, uint32_t &total)
+{
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t before = 0;
+    total = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t m = __ballot_sync(kFull, (c >> b) & 1u);
+        before += (uint32_t)__popc(m & lt) << b;
+        total += (uint32_t)__popc(m) << b;
+    }
+    return before;
+}
+
+// Emit pass: every tile's nonzero values and indices at its offset (the
+// tile's in-segment prefix plus the totals of the segments before it), or,
+// for a dense message, a bit copy of x.  The format is decided from the
+// total of all segments, which every block adds up for itself; block 0
+// writes the header.  Inside a tile the compacted run is staged in shared
+// memory (positions from warp ballots and a block prefix over the warp
+// totals) and leaves in consecutive, coalesced stores, two elements per
+// thread and store.  A 16-bit value and its index in the tile share one
+// staged word.  The next tile's input is loaded before the current tile's
+// run is written, so its latency overlaps the stores.
 template <int IN_T>
-__global__ void __launch_bounds__(kThreads) sparse_emit_kernel(const void *__restrict__ x, long long n,
+__global__ void __launch_bounds__(kThreads, 6) sparse_emit_kernel(const void *__restrict__ x, long long n,
                                                                const uint32_t *__restrict__ offsets,
-                                                               const uint32_t *__restrict__ hdr,
+                                                               const uint32_t *__restrict__ seg,
+                                                               long long nseg, double lim,
+                                                               uint32_t *__restrict__ hdr,
                                                                void *__restrict__ vals,
-                                                               int32_t *__restrict__ idx, int vec)
+                                                               int32_t *__restrict__ idx, int vec,
+                                                               int pairs)
 {
     using E = typename Elem<IN_T>::type;
     constexpr int es = dtype_size(IN_T);
-    __shared__ uint32_t wsum[kThreads / 32];
-    __shared__ uint32_t sval[kSpTile]; // bits of the compacted values of one tile
-    __shared__ uint16_t sidx[kSpTile]; // their positions in the tile
-    const bool sparse = hdr[0] != 0u;
+    constexpr bool W16 = es == 2;
+    constexpr int kWarps = kThreads / 32;
+    __shared__ uint32_t wsum[2 * kWarps];  // warp totals, then their exclusive prefixes
+    __shared__ uint32_t swd[kSpTile];      // 16-bit: value | index << 16; fp32: value bits
+    __shared__ uint16_t sidx[W16 ? 1 : kSpTile]; // fp32: the index in the tile
+    __shared__ unsigned long long s_total;
+    __shared__ uint32_t s_local;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const long long tiles = (n + kSpTile - 1) / kSpTile;
-    for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
-        if (!sparse) {
-            // dense fallback: vals = x (bit copy)
+    if (warp == 0) { // the total of all segments
+        unsigned long long t = 0;
+        for (long long i = lane; i < nseg; i += 32)
+            t += seg[i];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const long long e0 = t * kSpTile + (long long)h * 2048 + 8 * threadIdx.x;
-                const int vl = (int)max(0LL, min(8LL, n - e0));
-                const char *src = reinterpret_cast<const char *>(x) + e0 * es;
-                char *dst = reinterpret_cast<char *>(vals) + e0 * es;
-                if (vec && vl == 8) {
+        for (int o = 16; o >= 1; o >>= 1)
+            t += __shfl_xor_sync(kFull, t, o);
+        if (lane == 0)
+            s_total = t;
+    }
+    __syncthreads();
+    const unsigned long long total = s_total;
+    const bool sparse = (double)total < lim;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        hdr[0] = sparse ? 1u : 0u;
+        hdr[1] = (uint32_t)total;
+    }
+    if (!sparse) { // dense message: vals = x, bit for bit
+        const long long groups = (n + 7) / 8;
+        for (long long gi = blockIdx.x * (long long)kThreads + threadIdx.x; gi < groups;
+             gi += (long long)gridDim.x * kThreads) {
+            const long long e0 = gi * 8;
+            const int vl = (int)min(8LL, n - e0);
+            const char *src = reinterpret_cast<const char *>(x) + e0 * es;
+            char *dst = reinterpret_cast<char *>(vals) + e0 * es;
+            if (vec && vl == 8) {
 #pragma unroll
-                    for (int b = 0; b < es / 2; ++b)
-                        reinterpret_cast<uint4 *>(dst)[b] = reinterpret_cast<const uint4 *>(src)[b];
-                } else {
-                    for (int i = 0; i < vl; ++i)
-                        reinterpret_cast<E *>(dst)[i] = reinterpret_cast<const E *>(src)[i];
-                }
+                for (int b = 0; b < es / 2; ++b)
+                    reinterpret_cast<uint4 *>(dst)[b] = reinterpret_cast<const uint4 *>(src)[b];
+            } else {
+                for (int i = 0; i < vl; ++i)
+                    reinterpret_cast<E *>(dst)[i] = reinterpret_cast<const E *>(src)[i];
             }
-            continue;
         }
-        // compacted values and indices of the tile, staged so that they
-        // leave in consecutive, coalesced stores
-        uint32_t bits[2][8], msk[2];
+        return;
+    }
+    uint32_t bits[2][8], msk[2];
+    uint32_t off_next = 0; // the next tile's offset within its segment
+    auto load_tile = [&](long long t) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const long long e0 = t * kSpTile + (long long)h * 2048 + 8 * threadIdx.x;
             msk[h] = nz_mask8_bits<IN_T>(x, n, e0, vec, bits[h]);
         }
-        // order of elements in the tile: half h, thread, element -> the
-        // compacted order must follow it, so scan half 0 fully before half 1
-        uint32_t local = 0; // compacted elements of the tile before this half
+        off_next = offsets[t];
+    };
+    long long t = blockIdx.x;
+    if (t < tiles)
+        load_tile(t);
+    for (; t < tiles; t += gridDim.x) {
+        // positions in the tile's compacted run: half 0 (every thread) before
+        // half 1, a thread's 8 elements in order within each half
+        uint32_t before[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const uint32_t c = __popc(msk[h]);
-            uint32_t incl = c;
+            uint32_t wt;
+            before[h] = warp_prefix8(__popc(msk[h]), lane, wt);
+            if (lane == 0)
+                wsum[h * kWarps + warp] = wt;
+        }
+        __syncthreads();
+        if (warp == 0) { // exclusive prefix over (half, warp), and the tile's total
+            const uint32_t v = lane < 2 * kWarps ? wsum[lane] : 0u;
+            uint32_t incl = v;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
+            for (int o = 1; o < 2 * kWarps; o <<= 1) {
                 const uint32_t y = __shfl_up_sync(kFull, incl, o);
                 if (lane >= o)
                     incl += y;
             }
-            if (lane == 31)
-                wsum[warp] = incl;
-            __syncthreads();
-            uint32_t before = 0, total = 0;
-            for (int w = 0; w < kThreads / 32; ++w) {
-                const uint32_t s = wsum[w];
-                if (w < warp)
-                    before += s;
-                total += s;
-            }
-            uint32_t pos = local + before + incl - c;
-            const int e0 = h * 2048 + 8 * (int)threadIdx.x; // within the tile
+            if (lane < 2 * kWarps)
+                wsum[lane] = incl - v;
+            if (lane == 2 * kWarps - 1)
+                s_local = incl;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t q = wsum[h * kWarps + warp] + before[h];
+            const uint32_t e0 = h * 2048 + 8 * threadIdx.x; // within the tile
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 if ((msk[h] >> i) & 1u) {
-                    sval[pos] = bits[h][i]; // the input's own bits
-                    sidx[pos] = (uint16_t)(e0 + i);
-                    ++pos;
+                    if constexpr (W16) {
+                        swd[q] = bits[h][i] | ((e0 + i) << 16); // value bits | index
+                    } else {
+                        swd[q] = bits[h][i];
+                        sidx[q] = (uint16_t)(e0 + i);
+                    }
+                    ++q;
                 }
-            local += total;
-            __syncthreads(); // wsum is reused by the next half
         }
-        // the tile's compacted run, written with consecutive threads
-        const uint32_t base = offsets[t];
-        const long long t0 = t * kSpTile;
-        for (uint32_t k = threadIdx.x; k < local; k += kThreads) {
-            if constexpr (IN_T == kF32)
-                reinterpret_cast<uint32_t *>(vals)[base + k] = sval[k];
-            else
-                reinterpret_cast<uint16_t *>(vals)[base + k] = (uint16_t)sval[k];
-            idx[base + k] = (int32_t)(t0 + sidx[k]);
+        const uint32_t local = s_local;
+        __syncthreads();
+        uint32_t base = off_next;
+        const uint32_t tseg = (uint32_t)(t / kSegTiles);
+        for (uint32_t s2 = 0; s2 < tseg; ++s2)
+            base += seg[s2];
+        // the next tile's input, in flight while this tile's run is written
+        const long long tn = t + gridDim.x;
+        if (tn < tiles)
+            load_tile(tn);
+        const int32_t t0 = (int32_t)(t * kSpTile);
+        int32_t *ip = idx + base;
+        if constexpr (W16) {
+            uint16_t *vp = reinterpret_cast<uint16_t *>(vals) + base;
+            if (pairs && (base & 1u) == 0u) { // pairs: a 4-byte value and an 8-byte index store
+                for (uint32_t k = 2 * threadIdx.x; k < local; k += 2 * kThreads) {
+                    const uint32_t a = swd[k];
+                    if (k + 1 < local) {
+                        const uint32_t b = swd[k + 1];
+                        *reinterpret_cast<uint32_t *>(vp + k) = (a & 0xffffu) | (b << 16);
+                        *reinterpret_cast<int2 *>(ip + k) =
+                            make_int2(t0 + (int32_t)(a >> 16), t0 + (int32_t)(b >> 16));
+                    } else {
+                        vp[k] = (uint16_t)a;
+                        ip[k] = t0 + (int32_t)(a >> 16);
+                    }
+                }
+            } else {
+                for (uint32_t k = threadIdx.x; k < local; k += kThreads) {
+                    const uint32_t a = swd[k];
+                    vp[k] = (uint16_t)a;
+                    ip[k] = t0 + (int32_t)(a >> 16);
+                }
+            }
+        } else {
+            uint32_t *vp = reinterpret_cast<uint32_t *>(vals) + base;
+            for (uint32_t k = threadIdx.x; k < local; k += kThreads) {
+                vp[k] = swd[k];
+                ip[k] = t0 + (int32_t)sidx[k];
+            }
         }
         __syncthreads(); // the staging arrays are reused by the next tile
     }
@@ -667,20 +739,34 @@ cudaError_t launch_bfp_decode(const int8_t *exps, const uint8_t *mants, long lon
     return cudaGetLastError();
 }
 
-long long sparse_encode_scratch_words(long long n) { return (n + kSpTile - 1) / kSpTile; }
+// Scratch: one count (then offset) per 4096-element tile, then one total per
+// segment of 4096 tiles.
+long long sparse_encode_scratch_words(long long n)
+{
+    const long long tiles = (n + kSpTile - 1) / kSpTile;
+    return tiles + (tiles + kSegTiles - 1) / kSegTiles;
+}
 
 cudaError_t launch_sparse_encode(const void *x, long long n, int dtype, double one_minus_thr,
                                  uint32_t *hdr, void *vals, int32_t *idx, uint32_t *scratch,
                                  cudaStream_t st)
 {
-    const long long tiles = sparse_encode_scratch_words(n);
+    const long long tiles = (n + kSpTile - 1) / kSpTile;
+    const long long nseg = (tiles + kSegTiles - 1) / kSegTiles;
+    uint32_t *seg = scratch + tiles;
+    const double lim = one_minus_thr * (double)n; // sparse iff nnz < lim
     const int vec = aligned16(x) && aligned16(vals) ? 1 : 0;
     const int grid = grid_for(tiles, 1);
+    const int egrid = grid;
+    // pairs of 16-bit values and of indices leave in one store each
+    const int pairs = (reinterpret_cast<uintptr_t>(vals) & 3u) == 0 &&
+                      (reinterpret_cast<uintptr_t>(idx) & 7u) == 0;
 #define RRA_SP(T)                                                                              \
     do {                                                                                       \
         sparse_count_kernel<T><<<grid, kThreads, 0, st>>>(x, n, scratch, vec);                 \
-        sparse_scan_kernel<<<1, 1024, 0, st>>>(scratch, tiles, n, one_minus_thr, hdr);         \
-        sparse_emit_kernel<T><<<grid, kThreads, 0, st>>>(x, n, scratch, hdr, vals, idx, vec);  \
+        sparse_segscan_kernel<<<(unsigned)nseg, kScanThreads, 0, st>>>(scratch, tiles, seg);   \
+        sparse_emit_kernel<T><<<egrid, kThreads, 0, st>>>(x, n, scratch, seg, nseg, lim, hdr,  \
+                                                          vals, idx, vec, pairs);              \
     } while (0)
     if (dtype == kF32) RRA_SP(kF32);
     else if (dtype == kF16) RRA_SP(kF16);

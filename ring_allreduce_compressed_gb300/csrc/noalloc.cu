@@ -1,17 +1,16 @@
 // noalloc.cu -- rra_sparse_encode_noalloc: the sparse encoder for callers
 // that cannot allocate device memory.
 //
-// rra_sparse_encode needs scratch (one 32-bit count per 4096-element tile)
-// and takes it from a per-device workspace that grows with cudaMalloc.  Some
-// callers cannot allow that: code that runs while a CUDA graph is being
-// captured (cudaMalloc is not permitted then), latency-critical loops where
-// an allocation's implicit device synchronisation is not acceptable,
-// processes whose device memory is handed out by their own allocator or
-// budgeted up front, and libraries that must not call into the CUDA
-// allocator behind their host framework's back.  This entry point uses a
-// fixed scratch array that lives in the library image instead: a file-scope
-// __device__ array of kNoallocScratchWords words (256 KiB), present on every
-// GPU that loads the library until the process exits.
+// rra_sparse_encode needs scratch (one 32-bit count per 4096-element tile,
+// and one total per 4096 tiles) and takes it from a per-device workspace that
+// grows with cudaMalloc.  Some callers cannot allow that: processes whose
+// device memory is handed out by their own allocator or budgeted up front,
+// latency-critical loops in which an allocation's implicit device
+// synchronisation is not acceptable, and libraries that must not call into
+// the CUDA allocator behind their host framework's back.  This entry point
+// uses a fixed scratch array that lives in the library image instead: a
+// file-scope __device__ array of kNoallocScratchWords words (about 256 KiB),
+// present on every GPU that loads the library until the process exits.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -22,10 +21,9 @@
 
 namespace {
 
-constexpr long long kNoallocScratchWords = 65536; // one word per 4096-element tile
-constexpr long long kTileElems = 4096;
-static_assert(kNoallocScratchWords * kTileElems == (long long)RRA_NOALLOC_MAX_COUNT,
-              "header limit must match the scratch array");
+// one word per 4096-element tile of the largest input, then one per 4096 tiles
+constexpr long long kNoallocTiles = (long long)RRA_NOALLOC_MAX_COUNT / 4096;
+constexpr long long kNoallocScratchWords = kNoallocTiles + (kNoallocTiles + 4095) / 4096;
 
 // The scratch itself.  In host code this name is only a host-side stand-in,
 // not a device address: the address a kernel may use comes from
@@ -37,7 +35,9 @@ std::mutex g_mu;
 uint32_t *g_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up once
-// per device with that device current.
+// per device, on the first call with that device current.  The address
+// stays valid for the life of the device's primary context; after a
+// cudaDeviceReset the entry point must not be called again in this process.
 cudaError_t scratch_for_current_device(uint32_t **out)
 {
     int dev = 0;
@@ -68,13 +68,14 @@ extern "C" rra_status rra_sparse_encode_noalloc(const void *x, size_t n, rra_dty
         !(dtype == RRA_F32 || dtype == RRA_F16 || dtype == RRA_BF16) ||
         !(threshold >= 0.0f && threshold < 1.0f))
         return RRA_ERR_INVALID;
-    if (n > (size_t)RRA_NOALLOC_MAX_COUNT)
+    if (n > (size_t)RRA_NOALLOC_MAX_COUNT ||
+        rra::sparse_encode_scratch_words((long long)n) > kNoallocScratchWords)
         return RRA_ERR_INVALID; // beyond the fixed scratch: use rra_sparse_encode
     uint32_t *scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess)
         return RRA_ERR_CUDA;
-    // every word the count pass writes is read only after it was written in
-    // the same call, so nothing needs clearing between calls
+    // every word the count and scan passes write is read only after it was
+    // written in the same call, so nothing needs clearing between calls
     return rra::launch_sparse_encode(x, (long long)n, dtype, 1.0 - (double)threshold, hdr, vals,
                                      idx, scratch,
                                      reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
