@@ -751,11 +751,11 @@ def run_codecs(args, world, rank):
     ]
     out = []
     for name, fn, nbytes in cases:
-        for _ in range(3):
+        for _ in range(args.op_warmup):
             fn()
         torch.cuda.synchronize()
         times = []
-        for _ in range(10):
+        for _ in range(args.op_reps):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record()
@@ -774,6 +774,55 @@ def run_codecs(args, world, rank):
         with open(args.jsonl, "a") as f:
             for line in out:
                 f.write(json.dumps(line) + "\n")
+
+
+def run_kernels(args, world, rank):
+    """One op per library kernel that the ring workloads do not cover -- the
+    plain allgather, broadcast and tree allreduce, and the codec statistics --
+    on N=8 ranks of --kernels-T fp32 elements (default 16 Mi: 512 MB in all,
+    above the 129 MB L2), each called --op-warmup times untimed and then
+    --op-reps times, timed with CUDA events (median), against its algorithmic
+    bytes.  Also the command the ncu summaries of these kernels are captured
+    from."""
+    import ring_allreduce_compressed_gb300 as rra
+    rra.build()
+    if rank != 0:
+        return
+    peak, peak_src = hbm_peak()
+    N, T = 8, args.kernels_T
+    bufs = W.uniform(N, T, seed=4)
+    comm = rra.Comm(N, T)
+    n = -(-T // N)
+    cases = [
+        # each rank reads its own chunk once and writes the N-1 others
+        ("allgather_kernel", lambda: comm.allgather(bufs), 4 * N * n + 4 * (N - 1) * n * N),
+        # the root's buffer read once, every other buffer written once
+        ("broadcast_kernel", lambda: comm.broadcast(bufs, root=0), 4 * T + 4 * (N - 1) * T),
+        # every buffer read and written once
+        ("tree_kernel", lambda: comm.tree_allreduce(bufs), 8 * N * T),
+        # every buffer read once
+        ("codec_stats_kernel", lambda: comm.codec_stats(bufs), 4 * N * T),
+    ]
+    for name, fn, nbytes in cases:
+        for _ in range(args.op_warmup):
+            fn()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(args.op_reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b) * 1e3)
+        assert comm.status() == rra.RRA_OK
+        us = statistics.median(times)
+        line = {"kernel_bench": True, "kernel": name, "N": N, "T": T, "us": us,
+                "bytes": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9,
+                "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peak, "peak_source": peak_src}
+        print(json.dumps(line), flush=True)
+    comm.close()
 
 
 def run_sweep(args, world, rank):
@@ -953,6 +1002,14 @@ def main():
                          "ncu captures, reported with its own T (not the metric's workload)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernels", action="store_true",
+                    help="one timed call of each collective kernel the workloads do not "
+                         "cover (plain allgather, broadcast, tree; codec statistics)")
+    ap.add_argument("--kernels-T", type=int, default=16 << 20)
+    ap.add_argument("--op-warmup", type=int, default=3,
+                    help="--codecs / --kernels: untimed calls of each op before its timed ones")
+    ap.add_argument("--op-reps", type=int, default=10,
+                    help="--codecs / --kernels: timed calls of each op (median reported)")
     ap.add_argument("--codec-n", type=int, default=1 << 28,
                     help="--codecs: elements per codec call (a smaller case for ncu captures)")
     ap.add_argument("--eager", action="store_true",
@@ -981,6 +1038,8 @@ def main():
         run_sweep(args, world, rank)
     elif args.codecs:
         run_codecs(args, world, rank)
+    elif args.kernels:
+        run_kernels(args, world, rank)
     elif args.impl == "reference":
         run_reference(args, world, rank)
     else:

@@ -263,7 +263,8 @@ rra_status rra_allgather_codec(rra_comm *comm, void *const *buf, size_t count, r
  * Broadcast from rank "root" over a binomial tree of depth ceil(log2 N)
  * ([ring] table: T bytes per receiving rank, log2(N) tree).  At level
  * k = 0..ceil(log2 N)-1 every relative rank q < 2^k with q + 2^k < N sends
- * its whole buffer to q + 2^k (relative rank q = (r - root) mod N).  In
+ * its whole buffer to q + 2^k (relative rank q = (r - root) mod N).  Each
+ * edge is copied by its receiver, from the parent's copy of the slice.  In
  * place, bit-exact copies.  Errors: RRA_ERR_INVALID (root outside 0..N-1,
  * ...), RRA_ERR_CUDA.
  */
@@ -564,12 +565,15 @@ rra_status rra_codec_advise_op(rra_comm *comm, int op, int root, const void *con
 /* Test-only fault injection: in the next collective call, simulated rank
  * "rank" does not publish the message it sends at ring step "step" (1-based,
  * counted over both passes; the compressed allgather sends first at step N,
- * the owner's) -- or, in the plain broadcast or the tree, at level "step"
- * (1-based); in the compressed broadcast, where a rank publishes once for
- * all its children, any step >= 1 -- for the first slice each block
- * handles, so its receiver's wait runs out
- * and the call ends with RRA_ERR_TIMEOUT.  rank < 0 disables.  The setting
- * applies to one call only. */
+ * the owner's), for the first slice each block handles, so its receiver's
+ * wait runs out and the call ends with RRA_ERR_TIMEOUT.  In the broadcasts
+ * and the tree, where a rank publishes each slice once for every rank that
+ * reads it: the plain broadcast withholds the rank's publish when it has a
+ * child at tree level "step" (1-based); the tree withholds a rank's reduced
+ * partial at step = its sending level + 1 (the position of its lowest set
+ * bit, plus one), and its broadcast publish at step = L + 1 + a level at
+ * which it has a child (L = ceil(log2 N)); the compressed broadcast at any
+ * step >= 1.  rank < 0 disables.  The setting applies to one call only. */
 rra_status rra_debug_withhold(rra_comm *comm, int rank, int step);
 
 /* Human-readable name of a status code (static string). */

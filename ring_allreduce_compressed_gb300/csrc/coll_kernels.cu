@@ -332,6 +332,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) allgather_kernel(const __gr
 }
 
 // ---------------------------------------------------------------- broadcast
+// Pull model: every edge of the binomial tree is copied by its receiver.  A
+// rank with children holds the slice in its own slot: the root copies it
+// there from its stage (or its buffer on the generic path), every other such
+// rank from its parent's slot; every non-root rank stores it into its
+// buffer.  A slot is freed once all of its rank's children have copied it
+// (its "empty" mbarrier counts them).  A warp plays its ranks in increasing
+// relative rank, so a parent it plays always publishes before a child it
+// plays waits for it.
 template <int ES, bool FAST, int G, bool ONE>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) broadcast_kernel(const __grid_constant__ CopyArgs a)
 {
@@ -339,25 +347,27 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) broadcast_kernel(const __gr
     constexpr int TW = kTile * G;
     const int N = a.N, W = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int K = a.K, D = a.D;
-    // edge q (the slot FIFO of rank q) receives from q's parent; one stager
-    const CollSmem s = coll_carve(smem, a, N, 1, FAST);
-    coll_init(s, a, N, 1, FAST);
-    const long long T = a.T;
-    const int rstride = ONE ? N : W;
-    const int tiles = (int)a.tiles;
     const int root = a.root;
     int L = 0;
     while ((1 << L) < N)
         ++L;
-    // last level at which relative rank q forwards (-1: never)
-    auto last_send = [&](int q) -> int {
-        const int k0 = q > 0 ? 32 - __clz(q) : 0;
-        int last = -1;
-        for (int k = k0; k < L; ++k)
-            if (q + (1 << k) < N)
-                last = k;
-        return last;
+    // relative rank q: parent q - 2^floor(log2 q); children q + 2^k for every
+    // k with 2^k > q and q + 2^k < N
+    auto children = [&](int q) -> int {
+        int c = 0;
+        for (int k = q > 0 ? 32 - __clz(q) : 0; k < L; ++k)
+            c += q + (1 << k) < N ? 1 : 0;
+        return c;
     };
+    auto rel = [&](int r) -> int {
+        const int q = r - root;
+        return q < 0 ? q + N : q;
+    };
+    // slot FIFO of rank r, freed by its children; one stager (the root)
+    const CollSmem s = coll_carve(smem, a, N, 1, FAST);
+    coll_init(s, a, N, 1, FAST, [&](int r) { return max(children(rel(r)), 1); });
+    const long long T = a.T;
+    const int tiles = (int)a.tiles;
     const bool root_warp = root % W == warp;
     int cur_item = blockIdx.x, inflight = 0;
     auto issue = [&](int d) { // lane 0 of the root's warp
@@ -381,6 +391,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) broadcast_kernel(const __gr
         }
         __syncwarp();
     }
+    // the level at which relative rank q's withheld publish is checked: a
+    // rank publishes once for all its children, so the fault-injection step
+    // (a 1-based level) withholds it when q has a child at that level
+    const int wlevel = a.withhold_step - 1;
     Bytes<ONE> by;
     Fifo e{0, 0}, stg{0, 0};
     bool ok = true;
@@ -389,80 +403,77 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) broadcast_kernel(const __gr
         const bool first = item == (int)blockIdx.x;
         const int V = clamp_len(T - t0, TW);
         const unsigned long long mb = (unsigned long long)V * ES;
-        if (FAST && root_warp &&
-            !(ok = wait_ready(s.sbar + stg.slot, (uint32_t)stg.phase, a.timeout_ns, a.status)))
-            break;
-        const unsigned char *root_src =
-            FAST ? s.stages + (size_t)stg.slot * a.stage_bytes
-                 : reinterpret_cast<const unsigned char *>(a.buf[root]) + t0 * ES;
-        for (int k = 0; ok && k < L; ++k) {
-            // senders at level k: relative q < 2^k with q + 2^k < N
-            for (int r = warp; r < N; r += rstride) {
-                int q = r - root;
-                q += q < 0 ? N : 0;
-                if (!(q < (1 << k) && q + (1 << k) < N))
-                    continue;
-                int child = r + (1 << k);
-                child -= child >= N ? N : 0;
-                if (!(ok = wait_ready(s.empty + child * K + e.slot, (uint32_t)(e.phase ^ 1),
-                                      a.timeout_ns, a.status)))
-                    break;
-                const unsigned char *src =
-                    q == 0 ? root_src : s.slots + (size_t)(r * K + e.slot) * a.slot_bytes;
-                unsigned char *dslot = s.slots + (size_t)(child * K + e.slot) * a.slot_bytes;
-                const bool global_src = !FAST && q == 0;
-#pragma unroll 1
-                for (int gi = 0; gi < G; ++gi) {
-                    const int el = gi * kTile + 8 * lane;
-                    if (gi * kTile >= V)
-                        break;
-                    Vec8<ES> v;
-                    if (global_src)
-                        v.load_elems(src + (size_t)el * ES, min(max(V - el, 0), 8));
-                    else
-                        v.load(src + (size_t)el * ES);
-                    v.store(dslot + (size_t)el * ES);
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    if (!(first && r == a.withhold_rank && k + 1 == a.withhold_step))
-                        mbar_arrive(s.full + child * K + e.slot);
-                    by.add_sent(s, r, mb);
-                    if (q > 0 && k == last_send(q)) // done forwarding: free the slot
-                        mbar_arrive(s.empty + r * K + e.slot);
-                }
-            }
-            if (!ok)
+        for (int q = ONE ? rel(warp) : 0; ok && q < N; q += ONE ? N : 1) {
+            int r = q + root;
+            r -= r >= N ? N : 0;
+            if (!ONE && r % W != warp)
+                continue;
+            const int nch = children(q);
+            unsigned char *own = s.slots + (size_t)(r * K + e.slot) * a.slot_bytes;
+            char *mine = reinterpret_cast<char *>(a.buf[r]) + t0 * ES;
+            // a rank with children first waits until they have all copied the
+            // message that last used this slot
+            if (nch > 0 && !(ok = wait_ready(s.empty + r * K + e.slot, (uint32_t)(e.phase ^ 1),
+                                             a.timeout_ns, a.status)))
                 break;
-            // receivers at level k: relative q in [2^k, 2^(k+1))
-            for (int r = warp; r < N; r += rstride) {
-                int q = r - root;
-                q += q < 0 ? N : 0;
-                if (!(q >= (1 << k) && q < (2 << k)))
-                    continue;
-                if (!(ok = wait_ready(s.full + r * K + e.slot, (uint32_t)e.phase, a.timeout_ns,
+            int p = 0; // absolute rank of the parent
+            if (q == 0) {
+                if (FAST && !(ok = wait_ready(s.sbar + stg.slot, (uint32_t)stg.phase,
+                                              a.timeout_ns, a.status)))
+                    break;
+                if (nch > 0) {
+                    const unsigned char *src =
+                        FAST ? s.stages + (size_t)stg.slot * a.stage_bytes
+                             : reinterpret_cast<const unsigned char *>(a.buf[root]) + t0 * ES;
+#pragma unroll 1
+                    for (int gi = 0; gi < G; ++gi) {
+                        if (gi * kTile >= V)
+                            break;
+                        const int el = gi * kTile + 8 * lane;
+                        Vec8<ES> v;
+                        if (FAST)
+                            v.load(src + (size_t)el * ES);
+                        else
+                            v.load_elems(src + (size_t)el * ES, min(max(V - el, 0), 8));
+                        v.store(own + (size_t)el * ES);
+                    }
+                }
+            } else {
+                p = q - (1 << (31 - __clz(q))) + root;
+                p -= p >= N ? N : 0;
+                if (!(ok = wait_ready(s.full + p * K + e.slot, (uint32_t)e.phase, a.timeout_ns,
                                       a.status)))
                     break;
-                const unsigned char *rslot = s.slots + (size_t)(r * K + e.slot) * a.slot_bytes;
-                char *mine = reinterpret_cast<char *>(a.buf[r]) + t0 * ES;
+                const unsigned char *pslot = s.slots + (size_t)(p * K + e.slot) * a.slot_bytes;
 #pragma unroll 1
-                for (int gi = 0; gi < G; ++gi) {
-                    const int el = gi * kTile + 8 * lane;
+                for (int gi = 0; gi < G; ++gi) { // copy the parent's slice
                     if (gi * kTile >= V)
                         break;
+                    const int el = gi * kTile + 8 * lane;
                     const int vl = min(max(V - el, 0), 8);
                     Vec8<ES> v;
-                    v.load(rslot + (size_t)el * ES);
+                    v.load(pslot + (size_t)el * ES);
+                    if (nch > 0)
+                        v.store(own + (size_t)el * ES);
                     if (FAST && vl == 8)
                         v.store(mine + (size_t)el * ES);
                     else
                         v.store_elems(mine + (size_t)el * ES, vl);
                 }
-                __syncwarp();
-                if (lane == 0) {
+            }
+            __syncwarp();
+            if (lane == 0) {
+                if (q > 0) {
+                    mbar_arrive(s.empty + p * K + e.slot); // done with the parent's slot
                     by.add_recv(s, r, mb);
-                    if (last_send(q) < 0) // a leaf frees its slot at once
-                        mbar_arrive(s.empty + r * K + e.slot);
+                }
+                if (nch > 0) {
+                    const bool withheld = first && r == a.withhold_rank && wlevel >= 0 &&
+                                          wlevel < L && q < (1 << wlevel) &&
+                                          q + (1 << wlevel) < N;
+                    if (!withheld)
+                        mbar_arrive(s.full + r * K + e.slot);
+                    by.add_sent(s, r, mb * (unsigned long long)nch);
                 }
             }
         }
@@ -712,25 +723,53 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 }
 
 // ---------------------------------------------------------------- tree allreduce
+// Pull model on the ranks' own stages (no slots): every rank stages its slice
+// (its fp32 partial) and accumulates in it.
+//  reduce     at level k, rank r with r mod 2^(k+1) = 0 and r + 2^k < N waits
+//             until rank r + 2^k's partial is final and adds it, from that
+//             rank's stage, into its own (receiver's partial + sender's,
+//             round to nearest even: the binomial order).  A rank's partial
+//             is final once it has received at every level below its own
+//             sending level (the lowest set bit of r); it then publishes it
+//             ("reduce-full").
+//  broadcast  rank 0's stage holds the sum.  Every other rank waits for its
+//             parent's "broadcast-full" (parent: r with its highest set bit
+//             cleared), copies the parent's stage into its own (if it has
+//             children) and into its buffer, then publishes.
+// A stage is refilled once every rank that reads it -- the reduce parent and
+// the broadcast children -- has arrived on its "empty" barrier.  Barriers per
+// (rank, stage): full[r] reduce-full, full[N + r] broadcast-full, empty[r].
+// A warp walks its ranks downwards in the reduce (children first) and
+// upwards in the broadcast (parents first), so it never waits on a rank it
+// plays later.
 template <bool FAST, int G, bool ONE>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) tree_kernel(const __grid_constant__ CopyArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int TW = kTile * G;
     const int N = a.N, W = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int K = a.K, D = a.D;
-    // edge q: reduce messages from child q to its parent; edge N + q:
-    // broadcast messages into rank q.  Every rank stages (and accumulates in)
-    // its own slice; the generic path has one stage that it fills itself.
-    const CollSmem s = coll_carve(smem, a, 2 * N, N, true);
-    coll_init(s, a, 2 * N, N, FAST);
-    const long long T = a.T;
-    const int rstride = ONE ? N : W;
-    const int tiles = (int)a.tiles;
+    const int D = a.D; // stages per rank; the barrier FIFOs have D positions (a.K == D)
     int L = 0;
     while ((1 << L) < N)
         ++L;
+    auto bc_children = [&](int r) -> int { // children in the broadcast from rank 0
+        int c = 0;
+        for (int k = r > 0 ? 32 - __clz(r) : 0; k < L; ++k)
+            c += r + (1 << k) < N ? 1 : 0;
+        return c;
+    };
+    // readers of rank r's stage: its reduce parent, its broadcast children
+    auto readers = [&](int r) -> int { return (r > 0 ? 1 : 0) + bc_children(r); };
+    const CollSmem s = coll_carve(smem, a, 2 * N, N, true);
+    coll_init(s, a, 2 * N, N, FAST,
+              [&](int edge) { return edge < N ? max(readers(edge), 1) : 1; });
+    const long long T = a.T;
+    const int rstride = ONE ? N : W;
+    const int tiles = (int)a.tiles;
     int cur_item = blockIdx.x, inflight = 0;
+    auto stage_of = [&](int r, int d) -> float * {
+        return reinterpret_cast<float *>(s.stages + (size_t)(r * D + d) * a.stage_bytes);
+    };
     auto issue = [&](int r, int d) { // lane 0
         const long long t0 = (long long)cur_item * TW;
         const uint32_t bytes = (uint32_t)clamp_len(T - t0, TW) * 4;
@@ -740,8 +779,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) tree_kernel(const __grid_co
             return;
         }
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(s.stages + (size_t)(r * D + d) * a.stage_bytes,
-                 reinterpret_cast<const float *>(a.buf[r]) + t0, bytes, bar);
+        bulk_g2s(stage_of(r, d), reinterpret_cast<const float *>(a.buf[r]) + t0, bytes, bar);
     };
     if constexpr (FAST) {
         while (inflight < D && cur_item < tiles) {
@@ -753,26 +791,30 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) tree_kernel(const __grid_co
         }
         __syncwarp();
     }
+    // the last rank this warp plays (the reduce walks them downwards)
+    const int r_last = warp + ((N - 1 - warp) / rstride) * rstride;
     Bytes<ONE> by;
-    Fifo e{0, 0}, stg{0, 0};
+    Fifo stg{0, 0};
     bool ok = true;
-    auto acc_of = [&](int r) -> float * {
-        return reinterpret_cast<float *>(s.stages + (size_t)(r * D + stg.slot) * a.stage_bytes);
-    };
     for (int item = blockIdx.x; ok && item < tiles; item += gridDim.x) {
         const long long t0 = (long long)item * TW;
         const bool first = item == (int)blockIdx.x;
         const int V = clamp_len(T - t0, TW);
         const int ng = (V + kTile - 1) / kTile;
         const unsigned long long mb = 4ull * (unsigned long long)V;
-        // every rank's slice in its accumulator
-        for (int r = warp; r < N; r += rstride) {
+        const int d = stg.slot;
+        const uint32_t ph = (uint32_t)stg.phase;
+        // ---- binomial reduce to rank 0, children before parents
+        for (int r = r_last; ok && r >= warp; r -= rstride) {
+            float *acc = stage_of(r, d);
             if (FAST) {
-                if (!(ok = wait_ready(s.sbar + r * D + stg.slot, (uint32_t)stg.phase,
-                                      a.timeout_ns, a.status)))
+                if (!(ok = wait_ready(s.sbar + r * D + d, ph, a.timeout_ns, a.status)))
                     break;
             } else {
-                float *acc = acc_of(r);
+                // the one stage's last readers must be done before it is refilled
+                if (!first && !(ok = wait_ready(s.empty + r * D + d, ph ^ 1u, a.timeout_ns,
+                                                a.status)))
+                    break;
                 const float *src = reinterpret_cast<const float *>(a.buf[r]) + t0;
 #pragma unroll 1
                 for (int gi = 0; gi < ng; ++gi) {
@@ -784,47 +826,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) tree_kernel(const __grid_co
                 }
                 __syncwarp();
             }
-        }
-        if (!ok)
-            break;
-        // copy rank r's accumulator into the slot FIFO of edge `edge`
-        auto send = [&](int r, int edge, int step) -> bool {
-            if (!wait_ready(s.empty + edge * K + e.slot, (uint32_t)(e.phase ^ 1), a.timeout_ns,
-                            a.status))
-                return false;
-            const float *acc = acc_of(r);
-            float *dst = reinterpret_cast<float *>(s.slots + (size_t)(edge * K + e.slot) * a.slot_bytes);
-#pragma unroll 1
-            for (int gi = 0; gi < ng; ++gi) {
-                const int el = gi * kTile + 8 * lane;
-                reinterpret_cast<float4 *>(dst + el)[0] = reinterpret_cast<const float4 *>(acc + el)[0];
-                reinterpret_cast<float4 *>(dst + el)[1] = reinterpret_cast<const float4 *>(acc + el)[1];
-            }
-            __syncwarp();
-            if (lane == 0) {
-                if (!(first && r == a.withhold_rank && step == a.withhold_step))
-                    mbar_arrive(s.full + edge * K + e.slot);
-                by.add_sent(s, r, mb);
-            }
-            return true;
-        };
-        // ---- binomial reduce to rank 0
-        for (int k = 0; ok && k < L; ++k) {
-            for (int r = warp; r < N; r += rstride) // senders first
-                if ((r & ((2 << k) - 1)) == (1 << k) && !(ok = send(r, r, k + 1)))
-                    break;
-            if (!ok)
-                break;
-            for (int r = warp; r < N; r += rstride) { // then receivers: acc_r + acc_child
-                if ((r & ((2 << k) - 1)) != 0 || r + (1 << k) >= N)
-                    continue;
+            const int klast = r == 0 ? L : __ffs(r) - 1; // r receives at levels below this
+            for (int k = 0; k < klast; ++k) {
                 const int child = r + (1 << k);
-                if (!(ok = wait_ready(s.full + child * K + e.slot, (uint32_t)e.phase,
-                                      a.timeout_ns, a.status)))
+                if (child >= N)
                     break;
-                float *acc = acc_of(r);
-                const float *msg =
-                    reinterpret_cast<const float *>(s.slots + (size_t)(child * K + e.slot) * a.slot_bytes);
+                if (!(ok = wait_ready(s.full + child * D + d, ph, a.timeout_ns, a.status)))
+                    break;
+                const float *msg = stage_of(child, d);
 #pragma unroll 1
                 for (int gi = 0; gi < ng; ++gi) {
                     const int el = gi * kTile + 8 * lane;
@@ -839,81 +848,99 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) tree_kernel(const __grid_co
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(s.empty + child * K + e.slot);
+                    mbar_arrive(s.empty + child * D + d); // done reading the child's stage
                     by.add_recv(s, r, mb);
                 }
+            }
+            if (!ok)
+                break;
+            if (r > 0 && lane == 0) { // the partial is final: publish it
+                if (!(first && r == a.withhold_rank && a.withhold_step == klast + 1))
+                    mbar_arrive(s.full + r * D + d);
+                by.add_sent(s, r, mb);
             }
         }
         if (!ok)
             break;
-        // ---- rank 0 holds the sum: its output, then the binomial broadcast
-        auto store_out = [&](int r) {
-            const float *acc = acc_of(r);
+        // ---- binomial broadcast of rank 0's sum, parents before children
+        for (int r = warp; ok && r < N; r += rstride) {
+            float *acc = stage_of(r, d);
             float *out = reinterpret_cast<float *>(a.buf[r]) + t0;
-#pragma unroll 1
-            for (int gi = 0; gi < ng; ++gi) {
-                const int el = gi * kTile + 8 * lane;
-                float x[8];
-                load8_vec<kF32>(acc + el, x);
-                store8(out + el, kF32, x, min(max(V - el, 0), 8), FAST);
-            }
-        };
-        if (warp == 0)
-            store_out(0);
-        for (int k = 0; ok && k < L; ++k) {
-            for (int r = warp; r < N; r += rstride) // senders: r < 2^k
-                if (r < (1 << k) && r + (1 << k) < N && !(ok = send(r, N + r + (1 << k), L + k + 1)))
+            const int nch = bc_children(r);
+            if (r > 0) {
+                const int p = r - (1 << (31 - __clz(r)));
+                if (!(ok = wait_ready(s.full + (N + p) * D + d, ph, a.timeout_ns, a.status)))
                     break;
-            if (!ok)
-                break;
-            for (int r = warp; r < N; r += rstride) { // receivers: r in [2^k, 2^(k+1))
-                if (!(r >= (1 << k) && r < (2 << k)))
-                    continue;
-                if (!(ok = wait_ready(s.full + (N + r) * K + e.slot, (uint32_t)e.phase,
-                                      a.timeout_ns, a.status)))
-                    break;
-                float *acc = acc_of(r);
-                const float *msg =
-                    reinterpret_cast<const float *>(s.slots + (size_t)((N + r) * K + e.slot) * a.slot_bytes);
+                const float *src = stage_of(p, d);
 #pragma unroll 1
                 for (int gi = 0; gi < ng; ++gi) {
                     const int el = gi * kTile + 8 * lane;
-                    reinterpret_cast<float4 *>(acc + el)[0] = reinterpret_cast<const float4 *>(msg + el)[0];
-                    reinterpret_cast<float4 *>(acc + el)[1] = reinterpret_cast<const float4 *>(msg + el)[1];
+                    float x[8];
+                    load8_vec<kF32>(src + el, x);
+                    if (nch > 0) {
+                        reinterpret_cast<float4 *>(acc + el)[0] = make_float4(x[0], x[1], x[2], x[3]);
+                        reinterpret_cast<float4 *>(acc + el)[1] = make_float4(x[4], x[5], x[6], x[7]);
+                    }
+                    store8(out + el, kF32, x, min(max(V - el, 0), 8), FAST);
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(s.empty + (N + r) * K + e.slot);
+                    mbar_arrive(s.empty + p * D + d); // done reading the parent's stage
                     by.add_recv(s, r, mb);
                 }
-                store_out(r);
+            } else {
+#pragma unroll 1
+                for (int gi = 0; gi < ng; ++gi) {
+                    const int el = gi * kTile + 8 * lane;
+                    float x[8];
+                    load8_vec<kF32>(acc + el, x);
+                    store8(out + el, kF32, x, min(max(V - el, 0), 8), FAST);
+                }
+                __syncwarp();
+            }
+            if (lane == 0) {
+                if (nch > 0) {
+                    // fault injection: the broadcast levels are steps L+1..2L;
+                    // a rank publishes once, withheld when it has a child at
+                    // the withheld level
+                    const int wl = a.withhold_step - L - 1;
+                    const bool withheld = first && r == a.withhold_rank && wl >= 0 && wl < L &&
+                                          r < (1 << wl) && r + (1 << wl) < N;
+                    if (!withheld)
+                        mbar_arrive(s.full + (N + r) * D + d);
+                    by.add_sent(s, r, mb * (unsigned long long)nch);
+                }
+                if (readers(r) == 0) // N = 1: nobody else frees the stage
+                    mbar_arrive(s.empty + r * D + d);
             }
         }
         if (!ok)
             break;
-        if (FAST) { // every rank is done with its accumulator: refill the stage
+        if (FAST) {
+            // refill this item's stages once their readers are done with them
             __syncwarp();
             if (inflight == D && cur_item < tiles) {
+                for (int r = warp; ok && r < N; r += rstride)
+                    ok = wait_ready(s.empty + r * D + d, ph, a.timeout_ns, a.status);
+                if (!ok)
+                    break;
                 if (lane == 0)
                     for (int r = warp; r < N; r += rstride)
-                        issue(r, stg.slot);
+                        issue(r, d);
                 cur_item += gridDim.x;
             } else {
                 --inflight;
             }
-            stg.advance(D);
-        } else {
-            __syncwarp();
         }
-        e.advance(K);
+        stg.advance(D);
     }
     if constexpr (FAST) {
         __syncwarp();
         for (int r = warp; r < N; r += W) {
-            Fifo d = stg;
+            Fifo dd = stg;
             for (int i = 0; i < inflight; ++i) {
-                drain_phase(s.sbar + r * D + d.slot, (uint32_t)d.phase, a.timeout_ns);
-                d.advance(D);
+                drain_phase(s.sbar + r * D + dd.slot, (uint32_t)dd.phase, a.timeout_ns);
+                dd.advance(D);
             }
         }
     }

@@ -528,9 +528,11 @@ rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count
     }
     const int warps = warps_for(N);
     const bool one = warps == N;
-    // allgather: ring edges, every rank stages its chunk; broadcast: one edge
-    // into each rank, the root stages; tree: a reduce and a broadcast edge into
-    // each rank, every rank stages (and accumulates in) its slice
+    // allgather: ring edges, every rank stages its chunk; broadcast: a slot
+    // FIFO per rank (each edge copied by its receiver), the root stages; tree:
+    // no slots, every rank stages (and accumulates in) its slice, which its
+    // reduce parent and broadcast children read; a reduce-ready and a
+    // broadcast-ready barrier per rank and stage
     const int edges = which == 2 ? 2 * N : N;
     const int stagers = which == 1 ? 1 : N;
     const long long range = which == 0 ? a.n : a.T; // elements per rank walked in slices
@@ -548,16 +550,19 @@ rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count
             if (!comm->tune.G && g > 1 && (range + (long long)kTile * g - 1) / ((long long)kTile * g) < sms)
                 continue;
             const int bytes = kTile * g * (int)es;
-            const int slot = bits ? 16 + kTile * g * bits / 8 : bytes; // BFP: codes
+            const int slot = which == 2 ? 0 : bits ? 16 + kTile * g * bits / 8 : bytes; // BFP: codes
             bool found = false;
             for (int K = comm->tune.K ? comm->tune.K : 2; K >= (which == 0 ? 2 : 1) && !found; --K)
-                for (int D = fast ? (comm->tune.D ? comm->tune.D : 2) : 1; D >= 1 && !found; --D) {
+                for (int D = fast ? (comm->tune.D ? comm->tune.D : (which == 2 ? 3 : 2)) : 1;
+                     D >= 1 && !found; --D) {
+                    // the tree's barrier FIFOs follow its stages
+                    const int KK = which == 2 ? D : K;
                     const CollLayout L =
-                        coll_layout(N, edges, K, stagers, D, slot, bytes, fast || which == 2);
+                        coll_layout(N, edges, KK, stagers, D, slot, bytes, fast || which == 2);
                     if (per_sm * (L.total + 1024) <= comm->smem_per_sm &&
                         L.total <= comm->smem_optin) {
                         G = g;
-                        a.K = K;
+                        a.K = KK;
                         a.D = D;
                         smem = L.total;
                         found = true;
@@ -572,6 +577,8 @@ rra_status copy_common(rra_comm *comm, int which, void *const *buf, size_t count
     a.slot_bytes = a.stage_bytes = kTile * G * (int)es;
     if (bits)
         a.slot_bytes = 16 + kTile * G * bits / 8;
+    if (which == 2)
+        a.slot_bytes = 0;
     a.tiles = (range + (long long)kTile * G - 1) / ((long long)kTile * G);
     const void *fn = bits ? bcast_bfp_fn(bits, G, fast, one) : coll_fn(which, (int)es, G, fast, one);
     if (!fn)
