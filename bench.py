@@ -155,7 +155,7 @@ def hbm_peak():
 
 # The files each workload's ring kernel is compiled from (host-side launch
 # code excluded): a change to another codec's files leaves its summary valid.
-RING_KERNEL_COMMON = ("ring_kernel.cuh", "rra_device.cuh", "rra_kernels.h")
+RING_KERNEL_COMMON = ("ring_kernel.cuh", "bfp_group.cuh", "rra_device.cuh", "rra_kernels.h")
 RING_KERNEL_SOURCES = {
     "bfp8_bucket": ("ring_bfp8.cu", "ring_bfp8_ef.cu"),
     "diloco_n8": ("ring_bfp4.cu", "ring_bfp4_ef.cu"),

@@ -21,7 +21,7 @@ LIB = os.path.join(LIBDIR, "librra.so")
 
 SOURCES = ["rra_host.cu", "ring_none.cu", "ring_bfp8.cu", "ring_bfp4.cu", "ring_bfp8_ef.cu", "ring_bfp4_ef.cu", "ring_sparse.cu", "ring_sparse_chunk.cu", "coll_kernels.cu",
            "codec_kernels.cu", "noalloc.cu"]
-HEADERS = ["rra_device.cuh", "rra_kernels.h", "ring_kernel.cuh", "wire_sparse.cuh"]
+HEADERS = ["rra_device.cuh", "rra_kernels.h", "bfp_group.cuh", "ring_kernel.cuh", "wire_sparse.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", INCLUDE, "-I", CSRC]

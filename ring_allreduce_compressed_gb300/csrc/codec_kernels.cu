@@ -4,6 +4,7 @@
 // the sparsity exceeds a threshold; difference against the previous round).
 // All of them are HBM-bound streams: 128-bit loads and stores where the
 // buffers allow, grid-stride loops over warp-sized tiles.
+#include "bfp_group.cuh"
 #include "rra_device.cuh"
 #include "rra_kernels.h"
 #include <algorithm>
@@ -61,21 +62,25 @@ __global__ void __launch_bounds__(kThreads) bfp_encode_kernel(const void *__rest
             load8_vec<IN_T>(src, v);
         else
             load8_scalar<IN_T>(src, vl, v);
-        const int e = bfp_exponent(halfwarp_absmax(v));
-        int m[8];
-        bfp_codes<BITS>(v, e, m);
+        // the ring's encoder (half-warp maximum by warp reductions, codes
+        // from one fma each) gives offset codes m + 2^(bits-1); flipping the
+        // top bit of every code gives the two's complement this API stores
+        int e;
+        uint32_t w[2];
+        BfpGroup<BITS>::encode(v, e, w);
         const long long blk = (t * kTile + 128 * (lane >> 4)) / kBlock;
         if ((lane & 15) == 0 && blk * kBlock < n)
             exps[blk] = (int8_t)e;
         if constexpr (BITS == 8) {
+            const uint2 c2 = make_uint2(w[0] ^ 0x80808080u, w[1] ^ 0x80808080u);
             if (vec && vl == 8) {
-                *reinterpret_cast<uint2 *>(mants + e0) = pack8(m);
+                *reinterpret_cast<uint2 *>(mants + e0) = c2;
             } else {
                 for (int i = 0; i < vl; ++i)
-                    mants[e0 + i] = (uint8_t)(int8_t)m[i];
+                    mants[e0 + i] = (uint8_t)(((i < 4 ? c2.x : c2.y) >> (8 * (i & 3))) & 0xffu);
             }
         } else {
-            const uint32_t u = pack4(m);
+            const uint32_t u = w[0] ^ 0x88888888u;
             if (vec && vl == 8) {
                 *reinterpret_cast<uint32_t *>(mants + e0 / 2) = u;
             } else {
@@ -96,44 +101,49 @@ __global__ void __launch_bounds__(kThreads) bfp_decode_kernel(const int8_t *__re
     const int lane = threadIdx.x & 31;
     const long long warps = (long long)gridDim.x * (kThreads / 32);
     const long long tiles = (n + kTile - 1) / kTile;
+    // two's complement codes -> the offset codes m + 2^(bits-1) the ring's
+    // decoder reads (flip the top bit of every code)
+    constexpr uint32_t kFlip = BITS == 8 ? 0x80808080u : 0x88888888u;
     for (long long t = blockIdx.x * (long long)(kThreads / 32) + (threadIdx.x >> 5); t < tiles;
          t += warps) {
         const long long e0 = t * kTile + 8 * lane;
         const int vl = (int)max(0LL, min(8LL, n - e0));
         if (vl == 0)
             continue;
-        const int e = exps[e0 / kBlock];
-        int m[8];
+        const int e = __ldg(exps + e0 / kBlock);
+        uint32_t w[2] = {0u, 0u};
         if constexpr (BITS == 8) {
             if (vec && vl == 8) {
-                unpack8(*reinterpret_cast<const uint2 *>(mants + e0), m);
+                const uint2 u = __ldg(reinterpret_cast<const uint2 *>(mants + e0));
+                w[0] = u.x;
+                w[1] = u.y;
             } else {
-                for (int i = 0; i < 8; ++i)
-                    m[i] = i < vl ? (int)(int8_t)mants[e0 + i] : 0;
+                for (int i = 0; i < vl; ++i)
+                    w[i >> 2] |= (uint32_t)mants[e0 + i] << (8 * (i & 3));
             }
         } else {
-            uint32_t u = 0;
             if (vec && vl == 8) {
-                u = *reinterpret_cast<const uint32_t *>(mants + e0 / 2);
+                w[0] = __ldg(reinterpret_cast<const uint32_t *>(mants + e0 / 2));
             } else {
                 for (int b = 0; b < (vl + 1) / 2; ++b)
-                    u |= (uint32_t)mants[e0 / 2 + b] << (8 * b);
+                    w[0] |= (uint32_t)mants[e0 / 2 + b] << (8 * b);
             }
-            unpack4(u, m);
         }
+        // positions past n decode code 0 (flipped to the offset code of 0)
+        w[0] ^= kFlip;
+        w[1] ^= kFlip;
+        // every m * 2^(e-q) is an exact float (|m| < 2^7, e - q >= -132), so
+        // the fused decode-and-add rounds once, like decoding then adding
         float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            v[i] = bfp_value<BITS>(m[i], e);
         if (accumulate) {
             float o[8];
             if (vec && vl == 8)
                 load8_vec<kF32>(out + e0, o);
             else
                 load8_scalar<kF32>(out + e0, vl, o);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                v[i] = __fadd_rn(o[i], v[i]);
+            BfpGroup<BITS>::decode_add(w, e, o, v);
+        } else {
+            BfpGroup<BITS>::decode(w, e, v);
         }
         store8(out + e0, kF32, v, vl, vec != 0);
     }
@@ -621,6 +631,9 @@ __global__ void __launch_bounds__(kThreads) diff_kernel(const float *cur, const 
 // first hop encodes them.  A nonzero element (fp32 bits not +0.0) is flushed
 // by a BFP code of q = bits - 2 fraction bits when it rounds to code 0, that
 // is when |x| <= 2^(e - q - 1) for the block exponent e.
+// Grid: blockIdx.y = r * N + c (rank r, chunk c); the blocks along x stride
+// over the chunk's 128-element blocks, a warp at a time, so no index needs a
+// division.
 
 // 2^k as an fp32 value for k in [-149, 127] (subnormal below -126).
 __device__ __forceinline__ float pow2_exact(int k)
@@ -628,57 +641,69 @@ __device__ __forceinline__ float pow2_exact(int k)
     return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(1 << (k + 149));
 }
 
+// 4 elements of dtype IN_T at p widened to fp32; the first `valid` are read
+// (vec: all 4 present and p aligned to 4 elements)
 template <int IN_T>
-__global__ void __launch_bounds__(kThreads) codec_stats_kernel(const __grid_constant__ StatsArgs a)
+__device__ __forceinline__ void load4(const void *p, int valid, bool vec, float v[4])
 {
+    using E = typename Elem<IN_T>::type;
+    if (vec && valid == 4) {
+        if constexpr (IN_T == kF32) {
+            const float4 x = __ldg(reinterpret_cast<const float4 *>(p));
+            v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+        } else {
+            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+            const E *e = reinterpret_cast<const E *>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v[i] = to_f32(e[i]);
+        }
+        return;
+    }
+    const E *e = reinterpret_cast<const E *>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        v[i] = i < valid ? to_f32(e[i]) : 0.0f;
+}
+
+template <int IN_T>
+__global__ void __launch_bounds__(kThreads) codec_stats_kernel(const __grid_constant__ StatsArgs a,
+                                                               int vec)
+{
+    constexpr int es = dtype_size(IN_T);
     const int lane = threadIdx.x & 31;
-    const long long nb = (a.n + kBlock - 1) / kBlock; // blocks of a full chunk
-    const long long total = (long long)a.N * a.N * nb;
-    const long long wid = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    const int r = (int)(blockIdx.y / (unsigned)a.N), c = (int)(blockIdx.y % (unsigned)a.N);
+    const long long lo = min(a.T, (long long)c * a.n), hi = min(a.T, lo + a.n);
+    const char *base = reinterpret_cast<const char *>(a.in[r]);
     uint32_t cnt_nz = 0, cnt_f4 = 0, cnt_f8 = 0;
-    unsigned long long cnt_el = 0;
-    for (long long g = wid; g < total; g += nw) {
-        const int r = (int)(g / ((long long)a.N * nb));
-        const long long rem = g - (long long)r * a.N * nb;
-        const int c = (int)(rem / nb);
-        const long long b = rem - (long long)c * nb;
-        const long long lo = min(a.T, (long long)c * a.n), hi = min(a.T, lo + a.n);
-        const long long e0 = lo + b * kBlock;
-        if (e0 >= hi)
-            continue; // a short chunk has fewer blocks
-        const long long e1 = min(hi, e0 + kBlock);
+    const long long step = (long long)gridDim.x * (kThreads / 32) * kBlock;
+    for (long long e0 = lo + ((long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kBlock;
+         e0 < hi; e0 += step) {
+        const int len = (int)min((long long)kBlock, hi - e0);
+        const int valid = min(max(len - 4 * lane, 0), 4);
         float v[4];
+        load4<IN_T>(base + (e0 + 4 * lane) * es, valid, vec != 0, v);
         unsigned mx = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const long long e = e0 + lane * 4 + i;
-            v[i] = e < e1 ? to_f32(reinterpret_cast<const typename Elem<IN_T>::type *>(a.in[r])[e])
-                          : 0.0f;
+        for (int i = 0; i < 4; ++i)
             mx = max(mx, __float_as_uint(v[i]) & 0x7fffffffu);
-        }
         mx = __reduce_max_sync(kFull, mx);
         const int e = max((int)(mx >> 23), 1) - 127;
         const float t4 = pow2_exact(e - 3), t8 = pow2_exact(e - 7);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            if (e0 + lane * 4 + i >= e1)
-                continue;
-            if (__float_as_uint(v[i]) == 0u)
-                continue;
-            ++cnt_nz;
-            cnt_f4 += fabsf(v[i]) <= t4 ? 1u : 0u;
-            cnt_f8 += fabsf(v[i]) <= t8 ? 1u : 0u;
+            // absent positions read +0.0: never counted
+            const bool nz = __float_as_uint(v[i]) != 0u;
+            const float m = fabsf(v[i]);
+            cnt_nz += nz ? 1u : 0u;
+            cnt_f4 += nz && m <= t4 ? 1u : 0u;
+            cnt_f8 += nz && m <= t8 ? 1u : 0u;
         }
-        if (lane == 0)
-            cnt_el += (unsigned long long)(e1 - e0);
     }
     cnt_nz = __reduce_add_sync(kFull, cnt_nz);
     cnt_f4 = __reduce_add_sync(kFull, cnt_f4);
     cnt_f8 = __reduce_add_sync(kFull, cnt_f8);
     if (lane == 0) {
-        if (cnt_el)
-            atomicAdd(a.stats + 0, cnt_el);
         if (cnt_nz)
             atomicAdd(a.stats + 1, (unsigned long long)cnt_nz);
         if (cnt_f4)
@@ -686,6 +711,9 @@ __global__ void __launch_bounds__(kThreads) codec_stats_kernel(const __grid_cons
         if (cnt_f8)
             atomicAdd(a.stats + 3, (unsigned long long)cnt_f8);
     }
+    // the element count: one thread per (rank, chunk)
+    if (blockIdx.x == 0 && threadIdx.x == 0 && hi > lo)
+        atomicAdd(a.stats + 0, (unsigned long long)(hi - lo));
 }
 
 } // namespace
@@ -694,15 +722,21 @@ __global__ void __launch_bounds__(kThreads) codec_stats_kernel(const __grid_cons
 
 cudaError_t launch_codec_stats(const StatsArgs &a, int dtype, cudaStream_t st)
 {
+    // y: (rank, chunk); x: enough blocks of 8 warps for about 16 blocks per SM
     const long long nb = (a.n + kBlock - 1) / kBlock;
-    const long long warps = (long long)a.N * a.N * nb;
-    const int grid = grid_for((warps + kThreads / 32 - 1) / (kThreads / 32), kThreads / 32);
+    const long long per_chunk = (nb + kThreads / 32 - 1) / (kThreads / 32);
+    const long long want = std::max(1LL, (long long)num_sms() * 16 / ((long long)a.N * a.N));
+    const dim3 grid((unsigned)std::max(1LL, std::min(per_chunk, want)), (unsigned)(a.N * a.N));
+    const int es = dtype == kF32 ? 4 : 2;
+    int vec = (a.n * es) % 16 == 0 ? 1 : 0; // 4-element runs aligned in every chunk
+    for (int r = 0; r < a.N; ++r)
+        vec = vec && aligned16(a.in[r]);
     if (dtype == kF32)
-        codec_stats_kernel<kF32><<<grid, kThreads, 0, st>>>(a);
+        codec_stats_kernel<kF32><<<grid, kThreads, 0, st>>>(a, vec);
     else if (dtype == kF16)
-        codec_stats_kernel<kF16><<<grid, kThreads, 0, st>>>(a);
+        codec_stats_kernel<kF16><<<grid, kThreads, 0, st>>>(a, vec);
     else
-        codec_stats_kernel<kBF16><<<grid, kThreads, 0, st>>>(a);
+        codec_stats_kernel<kBF16><<<grid, kThreads, 0, st>>>(a, vec);
     return cudaGetLastError();
 }
 

@@ -297,97 +297,6 @@ __device__ __forceinline__ void store8_full(void *p, int out_t, const float v[8]
 
 // ---------------------------------------------------------------- BFP
 
-// 2^k as an fp32 value, for k in [-149, 127] (subnormal below -126).
-__device__ __forceinline__ float pow2i(int k)
-{
-    return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(1 << (k + 149));
-}
-
-// Block exponent from the bits of the block maximum |x| (>= 0): the unbiased
-// exponent of a normal number is floor(log2); zero and subnormal maxima
-// (biased exponent 0) give the clamp value -126.
-__device__ __forceinline__ int bfp_exponent(float amax)
-{
-    const int biased = (__float_as_int(amax) >> 23) & 0xff;
-    return max(biased, 1) - 127;
-}
-
-// x * 2^k, exact whenever the product is a normal number (k <= 132 here; the
-// factor is split so that no intermediate power of two overflows).  A
-// product in the subnormal range may be rounded, but it is then below 2^-126
-// and rounds to the integer 0 either way.
-__device__ __forceinline__ float scale_pow2(float x, int k)
-{
-    if (k > 127)
-        return __fmul_rn(__fmul_rn(x, pow2i(k - 64)), pow2i(64));
-    return __fmul_rn(x, pow2i(k));
-}
-
-// Maximum |v| over the 16 lanes of this lane's half-warp.
-__device__ __forceinline__ float halfwarp_absmax(const float v[8])
-{
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        m = fmaxf(m, fabsf(v[i]));
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1)
-        m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    return m;
-}
-
-// Integer codes of this lane's 8 elements for block exponent e.
-template <int BITS> __device__ __forceinline__ void bfp_codes(const float v[8], int e, int m[8])
-{
-    constexpr int q = BITS - 2;
-    constexpr int M = (1 << (BITS - 1)) - 1;
-    const int k = q - e;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        int c = __float2int_rn(scale_pow2(v[i], k));
-        m[i] = min(max(c, -M), M);
-    }
-}
-
-template <int BITS> __device__ __forceinline__ float bfp_value(int m, int e)
-{
-    return __fmul_rn(__int2float_rn(m), pow2i(e - (BITS - 2)));
-}
-
-// Pack / unpack the lane's 8 codes: 8-bit -> uint2 (byte i = element i),
-// 4-bit -> uint32 (nibble i = element i: element 2j low, 2j+1 high).
-__device__ __forceinline__ uint2 pack8(const int m[8])
-{
-    uint2 u;
-    u.x = (m[0] & 0xff) | ((m[1] & 0xff) << 8) | ((m[2] & 0xff) << 16) | ((uint32_t)(m[3] & 0xff) << 24);
-    u.y = (m[4] & 0xff) | ((m[5] & 0xff) << 8) | ((m[6] & 0xff) << 16) | ((uint32_t)(m[7] & 0xff) << 24);
-    return u;
-}
-__device__ __forceinline__ void unpack8(uint2 u, int m[8])
-{
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        m[i] = (int)(int8_t)((u.x >> (8 * i)) & 0xff);
-        m[i + 4] = (int)(int8_t)((u.y >> (8 * i)) & 0xff);
-    }
-}
-__device__ __forceinline__ uint32_t pack4(const int m[8])
-{
-    uint32_t u = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        u |= (uint32_t)(m[i] & 0xf) << (4 * i);
-    return u;
-}
-__device__ __forceinline__ void unpack4(uint32_t u, int m[8])
-{
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        int nib = (u >> (4 * i)) & 0xf;
-        m[i] = nib >= 8 ? nib - 16 : nib;
-    }
-}
-
 // Wire bytes of one BFP message covering len elements.
 __host__ __device__ __forceinline__ uint32_t bfp_msg_bytes(int len, int bits)
 {
