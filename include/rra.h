@@ -332,13 +332,14 @@ rra_status rra_bfp_decode(const int8_t *exps, const uint8_t *mants, size_t n, in
  *         values in index order.  Dense: a copy of x.
  *  idx    device, n int32 capacity.  Sparse: the nnz indices, ascending.
  * Sparse iff nnz < (1 - threshold) * n (evaluated in double).  Three
- * passes: a count per 4096-element tile, an exclusive scan of the counts,
- * and an emit pass that writes each tile's nonzeros at its offset (or copies
+ * passes: a count per 1024-element chunk, an exclusive scan of the counts,
+ * and an emit pass that writes each chunk's nonzeros at its offset (or copies
  * x when the message is dense; idx is then left as it was).
- * Uses scratch (one uint32 per 4096 elements, one per 4096 tiles) from a workspace per device
- * and stream that the library allocates with cudaMalloc on the first call
- * that needs more than it holds (so that first call must not be made during
- * stream capture).  Encodes on different streams may overlap: each stream
+ * Uses scratch (one uint32 per 1024 elements, one per 4096 chunks, and a
+ * ticket word) from a workspace per device and stream that the library
+ * allocates with cudaMalloc and clears on the first call that needs more
+ * than it holds (so that first call must not be made during stream
+ * capture).  Encodes on different streams may overlap: each stream
  * has its own workspace.  Errors: RRA_ERR_INVALID, RRA_ERR_NOMEM,
  * RRA_ERR_CUDA.
  */
@@ -346,7 +347,7 @@ rra_status rra_sparse_encode(const void *x, size_t n, rra_dtype dtype, float thr
                              uint32_t *hdr, void *vals, int32_t *idx, void *stream);
 
 /* Largest n that rra_sparse_encode_noalloc accepts: its fixed scratch holds
- * one 32-bit count per 4096 elements and one total per 4096 counts. */
+ * one 32-bit count per 1024 elements and one total per 4096 counts. */
 #define RRA_NOALLOC_MAX_COUNT (65536ull * 4096ull)
 
 /*
@@ -358,20 +359,22 @@ rra_status rra_sparse_encode(const void *x, size_t n, rra_dtype dtype, float thr
  * that must not call the CUDA allocator behind their host framework's back.
  * Same arguments, output and errors as rra_sparse_encode, except:
  *  - it never allocates: no cudaMalloc, cudaFree or allocating library call.
- *    Its scratch is a fixed array inside the library (about 256 KiB of
+ *    Its scratch is a fixed array inside the library (about 1 MiB of
  *    device memory on every GPU that loads the library, held until the
  *    process exits).
  *  - n may not exceed RRA_NOALLOC_MAX_COUNT (2^28 elements); larger n returns
  *    RRA_ERR_INVALID without doing anything (use rra_sparse_encode then).
  *  - the first call on a device looks up the scratch array's device address
- *    (cudaGetSymbolAddress) with that device current, and keeps it for the
- *    rest of the process; after cudaDeviceReset the function must not be
- *    called again.  Make the first call on each device before starting any
- *    stream capture.
- *  - all calls share the one scratch array, and each call overwrites the
- *    part it uses before reading it, so no clearing is needed between calls;
- *    calls that overlap on the GPU (different streams without ordering
- *    between them) race on the scratch and give undefined results.
+ *    (cudaGetSymbolAddress) with that device current, keeps it for the rest
+ *    of the process, and clears the array on the call's stream (one ticket
+ *    word of the scan must start at zero); after cudaDeviceReset the
+ *    function must not be called again.  Make the first call on each device
+ *    before starting any stream capture.
+ *  - all calls on a device share the one scratch array.  Each call writes
+ *    every count it reads before reading it and leaves the ticket at zero
+ *    again, so no clearing is needed between calls; calls that overlap on
+ *    the GPU (different streams without ordering between them) race on the
+ *    scratch and give undefined results.
  */
 rra_status rra_sparse_encode_noalloc(const void *x, size_t n, rra_dtype dtype, float threshold,
                                      uint32_t *hdr, void *vals, int32_t *idx, void *stream);

@@ -392,7 +392,9 @@ def sparse_encode(x, threshold: float, hdr, vals, idx, stream=None):
 def sparse_encode_noalloc(x, threshold: float, hdr, vals, idx, stream=None):
     """rra_sparse_encode_noalloc: the sparse encoder without any device
     allocation (fixed in-library scratch; n <= RRA_NOALLOC_MAX_COUNT), for
-    callers that cannot allocate, e.g. while a CUDA graph is being captured."""
+    callers that cannot allocate: processes whose device memory belongs to
+    their own allocator or a fixed budget, latency-critical loops, libraries
+    that must not call the CUDA allocator behind their framework's back."""
     _check(lib().rra_sparse_encode_noalloc(_dev(x, "x"), x.numel(), _dtype_code(x.dtype),
                                            threshold, _dev(hdr, "hdr"), _dev(vals, "vals"),
                                            _dev(idx, "idx"), _stream(stream)),

@@ -150,207 +150,233 @@ __global__ void __launch_bounds__(kThreads) bfp_decode_kernel(const int8_t *__re
 }
 
 // ---------------------------------------------------------------- sparse encode
-// Tile of 4096 elements per block: 256 threads x 16 elements (two groups of
-// 8 consecutive elements per thread).  Pass 1 counts the tile's nonzeros;
-// pass 2 (one block) turns the counts into exclusive offsets, decides the
-// format and writes the header; pass 3 writes the values and indices: a
-// thread's slot comes from a warp ballot/popc prefix and a block prefix sum
-// over the warps; the tile's compacted run is staged in shared memory and
-// leaves in consecutive stores at the tile's offset.
-constexpr int kSpTile = 4096;
+// Three passes over chunks of 1024 elements ([cccl] §2.1's values +
+// indices), each chunk handled by one warp, no block-wide step anywhere:
+//   count  the nonzeros of every chunk;
+//   scan   their exclusive prefix (segments of 4096 chunks; the last
+//          segment to finish scans the segments' totals, whose sum decides
+//          the format and goes into the header);
+//   emit   every chunk's nonzero values and indices at its offset, or, for
+//          a dense message, a bit copy of x.
+// Lane L holds the chunk's 16-byte words L, 32 + L, 64 + L, ... (8 16-bit
+// or 4 fp32 elements each).  The chunk's run (word by word, lanes and
+// elements in order: ascending indices) is staged in the warp's own part of
+// shared memory -- a 16-bit value and its index in the chunk share one word
+// -- and leaves in 16-byte index stores and 8-byte (16-bit values) or
+// 16-byte (fp32) value stores aligned to the output.
+constexpr int kSpChunk = 1024;  // elements per chunk
+constexpr int kSegChunks = 4096; // chunks per scan segment
+constexpr int kScanThreads = kSegChunks / 4;
 
-// Nonzero mask of the 8 elements at e0 (bit i: element e0+i is not +0.0),
-// from the elements' own bits, which are also returned (a 16-bit element
-// zero-extended): an fp16 or bf16 element widens to +0.0 exactly when its 16
-// bits are zero, so no conversion is needed.
-template <int IN_T>
-__device__ __forceinline__ uint32_t nz_mask8_bits(const void *x, long long n, long long e0,
-                                                  int vec, uint32_t w[8])
+template <int IN_T> struct SpChunk {
+    static constexpr int es = dtype_size(IN_T);
+    static constexpr int epw = 16 / es;             // elements per 16-byte word
+    static constexpr int words = kSpChunk / epw / 32; // 16-byte words per lane (4 or 8)
+};
+
+// Bit 15 set iff the low 16 bits of w are nonzero, bit 31 iff the high 16
+// bits are; no other bit set.  (w & 0x7fff) + 0x7fff carries into bit 15
+// exactly when the low 15 bits are not all zero, and cannot carry further.
+__device__ __forceinline__ uint32_t nz16(uint32_t w)
 {
-    const int vl = (int)max(0LL, min(8LL, n - e0));
-    if constexpr (IN_T == kF32) {
-        const uint32_t *p = reinterpret_cast<const uint32_t *>(x) + e0;
-        if (vec && vl == 8) {
-            const uint4 a = reinterpret_cast<const uint4 *>(p)[0];
-            const uint4 b = reinterpret_cast<const uint4 *>(p)[1];
-            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-            w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                w[i] = i < vl ? p[i] : 0u;
-        }
-    } else {
-        const uint16_t *p = reinterpret_cast<const uint16_t *>(x) + e0;
-        if (vec && vl == 8) {
-            const uint4 a = *reinterpret_cast<const uint4 *>(p);
-            const uint32_t h[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                w[2 * i] = h[i] & 0xffffu;
-                w[2 * i + 1] = h[i] >> 16;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                w[i] = i < vl ? (uint32_t)p[i] : 0u;
-        }
-    }
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        m |= (w[i] != 0u ? 1u : 0u) << i;
-    return m;
+    return (((w & 0x7fff7fffu) + 0x7fff7fffu) | w) & 0x80008000u;
 }
 
+__device__ __forceinline__ uint32_t u4_at(const uint4 &q, int k)
+{
+    return k == 0 ? q.x : k == 1 ? q.y : k == 2 ? q.z : q.w;
+}
+
+// Nonzero mask of one 16-byte word of dtype IN_T (bit i: element i).  An
+// element is zero iff its bits are all zero (+0.0 in every dtype).
+template <int IN_T> __device__ __forceinline__ uint32_t word_mask(const uint4 &q)
+{
+    if constexpr (dtype_size(IN_T) == 2) {
+        // the top bits of bytes 1 and 3 of nz16 flag the two elements of a
+        // 32-bit word; gather them into the top bits of four bytes and
+        // collect those (the four products land on distinct bits)
+        const uint32_t u0 = __byte_perm(nz16(q.x), nz16(q.y), 0x7531);
+        const uint32_t u1 = __byte_perm(nz16(q.z), nz16(q.w), 0x7531);
+        return ((u0 * 0x00204081u) >> 28) | (((u1 * 0x00204081u) >> 28) << 4);
+    } else {
+        return (q.x != 0u ? 1u : 0u) | (q.y != 0u ? 2u : 0u) | (q.z != 0u ? 4u : 0u) |
+               (q.w != 0u ? 8u : 0u);
+    }
+}
+
+// Number of nonzero elements of one 16-byte word of dtype IN_T.
+template <int IN_T> __device__ __forceinline__ uint32_t word_count(const uint4 &q)
+{
+    if constexpr (dtype_size(IN_T) == 2)
+        return (uint32_t)__popc(nz16(q.x) | (nz16(q.y) >> 1) | (nz16(q.z) >> 2) |
+                                (nz16(q.w) >> 3));
+    else
+        return (q.x != 0u ? 1u : 0u) + (q.y != 0u ? 1u : 0u) + (q.z != 0u ? 1u : 0u) +
+               (q.w != 0u ? 1u : 0u);
+}
+
+// This lane's words of chunk c (zero past n): one 16-byte load each when the
+// chunk is whole and x aligned, else element loads.
+template <int IN_T>
+__device__ __forceinline__ void load_chunk(const void *x, long long n, long long c, int lane,
+                                           int vec, uint4 (&q)[SpChunk<IN_T>::words])
+{
+    constexpr int es = SpChunk<IN_T>::es, EPW = SpChunk<IN_T>::epw, W = SpChunk<IN_T>::words;
+    const long long base = c * kSpChunk;
+    if (vec && base + kSpChunk <= n) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(x) +
+                                                           base * es);
+#pragma unroll
+        for (int j = 0; j < W; ++j)
+            q[j] = __ldcs(src + 32 * j + lane);
+    } else {
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            const long long e0 = base + (long long)(32 * j + lane) * EPW;
+            for (int i = 0; i < EPW; ++i)
+                if (e0 + i < n) {
+                    if constexpr (es == 2)
+                        w[i >> 1] |= (uint32_t)reinterpret_cast<const uint16_t *>(x)[e0 + i]
+                                     << (16 * (i & 1));
+                    else
+                        w[i] = reinterpret_cast<const uint32_t *>(x)[e0 + i];
+                }
+            q[j] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// Pass 1: counts[c] = nonzeros of chunk c.  Warps stride over the chunks;
+// the next chunk's words are loaded before this one is counted.
 template <int IN_T>
 __global__ void __launch_bounds__(kThreads) sparse_count_kernel(const void *__restrict__ x,
-                                                                long long n, uint32_t *counts,
+                                                                long long n, long long chunks,
+                                                                uint32_t *__restrict__ counts,
                                                                 int vec)
 {
-    __shared__ uint32_t wsum[kThreads / 32];
-    const long long tiles = (n + kSpTile - 1) / kSpTile;
-    for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
-        uint32_t c = 0;
+    constexpr int W = SpChunk<IN_T>::words;
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (kThreads / 32);
+    long long c = blockIdx.x * (long long)(kThreads / 32) + (threadIdx.x >> 5);
+    uint4 q[W];
+    if (c < chunks)
+        load_chunk<IN_T>(x, n, c, lane, vec, q);
+    for (; c < chunks; c += warps) {
+        uint32_t k = 0;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t w[8];
-            const long long e0 = t * kSpTile + (long long)h * 2048 + 8 * threadIdx.x;
-            c += __popc(nz_mask8_bits<IN_T>(x, n, e0, vec, w));
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1)
-            c += __shfl_xor_sync(kFull, c, o);
-        if ((threadIdx.x & 31) == 0)
-            wsum[threadIdx.x >> 5] = c;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            uint32_t s = 0;
-            for (int w = 0; w < kThreads / 32; ++w)
-                s += wsum[w];
-            counts[t] = s;
-        }
-        __syncthreads();
+        for (int j = 0; j < W; ++j)
+            k += word_count<IN_T>(q[j]);
+        if (c + warps < chunks)
+            load_chunk<IN_T>(x, n, c + warps, lane, vec, q);
+        k = __reduce_add_sync(kFull, k);
+        if (lane == 0)
+            counts[c] = k;
     }
 }
 
-// Exclusive prefix of the tile counts, in place, in segments of kSegTiles
-// tiles: block s scans segment s (every thread four consecutive counts, one
-// 16-byte load; warp shuffles; one shared-memory pass over the warp totals)
-// and writes the segment's total to seg[s].  A tile's offset in the output is
-// then its in-segment prefix plus the totals of the segments before it.
-constexpr int kSegTiles = 4096;
-constexpr int kScanThreads = kSegTiles / 4;
-
-__global__ void __launch_bounds__(kScanThreads) sparse_segscan_kernel(uint32_t *counts,
-                                                                      long long tiles,
-                                                                      uint32_t *seg)
+// Pass 2: exclusive prefix of the chunk counts, in place, in segments of
+// kSegChunks chunks: block s scans segment s (every thread four consecutive
+// counts; warp shuffles; one shared-memory pass over the warp totals) and
+// writes the segment's total to seg[s].  The block that finishes last (a
+// ticket) turns the segment totals into their exclusive prefix, in place,
+// writes the header -- the total nnz and the format, sparse iff nnz < lim --
+// and resets the ticket for the next call.
+__global__ void __launch_bounds__(kScanThreads) sparse_scan_kernel(uint32_t *counts,
+                                                                   long long chunks,
+                                                                   uint32_t *seg,
+                                                                   uint32_t *ticket, double lim,
+                                                                   uint32_t *hdr)
 {
     __shared__ uint32_t wsum[kScanThreads / 32];
+    __shared__ bool s_last;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const long long t0 = (long long)blockIdx.x * kSegTiles + 4LL * threadIdx.x;
+    // inclusive scan of v over the block; *all: the block's total
+    auto block_scan = [&](uint32_t v, uint32_t *all) {
+        uint32_t incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o)
+                incl += t;
+        }
+        if (lane == 31)
+            wsum[warp] = incl;
+        __syncthreads();
+        uint32_t before = 0, tot = 0;
+#pragma unroll
+        for (int w = 0; w < kScanThreads / 32; ++w) {
+            const uint32_t y = wsum[w];
+            before += w < warp ? y : 0u;
+            tot += y;
+        }
+        __syncthreads(); // (wsum is reused by the next scan)
+        *all = tot;
+        return before + incl;
+    };
+    const long long t0 = (long long)blockIdx.x * kSegChunks + 4LL * threadIdx.x;
     uint32_t v[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-        v[j] = t0 + j < tiles ? counts[t0 + j] : 0u;
+        v[j] = t0 + j < chunks ? counts[t0 + j] : 0u;
     const uint32_t s = v[0] + v[1] + v[2] + v[3];
-    uint32_t incl = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o)
-            incl += t;
-    }
-    if (lane == 31)
-        wsum[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        uint32_t w = wsum[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(kFull, w, o);
-            if (lane >= o)
-                w += t;
-        }
-        wsum[lane] = w; // inclusive totals of warps 0..lane
-    }
-    __syncthreads();
-    uint32_t run = (warp > 0 ? wsum[warp - 1] : 0u) + incl - s;
+    uint32_t total;
+    uint32_t run = block_scan(s, &total) - s;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-        if (t0 + j < tiles) {
+        if (t0 + j < chunks) {
             counts[t0 + j] = run;
             run += v[j];
         }
-    if (threadIdx.x == 0)
-        seg[blockIdx.x] = wsum[kScanThreads / 32 - 1];
-}
-
-// Exclusive prefix of a thread's count c (0..8) over the lanes of its warp,
-// and the warp's total, from four ballots of the count's bits.
-__device__ __forceinline__ uint32_t warp_prefix8(uint32_t c, int lane, uint32_t &total)
-{
-    const uint32_t lt = (1u << lane) - 1u;
-    uint32_t before = 0;
-    total = 0;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const uint32_t m = __ballot_sync(kFull, (c >> b) & 1u);
-        before += (uint32_t)__popc(m & lt) << b;
-        total += (uint32_t)__popc(m) << b;
-    }
-    return before;
-}
-
-// Emit pass: every tile's nonzero values and indices at its offset (the
-// tile's in-segment prefix plus the totals of the segments before it), or,
-// for a dense message, a bit copy of x.  The format is decided from the
-// total of all segments, which every block adds up for itself; block 0
-// writes the header.  Inside a tile the compacted run is staged in shared
-// memory (positions from warp ballots and a block prefix over the warp
-// totals) and leaves in consecutive, coalesced stores, two elements per
-// thread and store.  A 16-bit value and its index in the tile share one
-// staged word.  The next tile's input is loaded before the current tile's
-// run is written, so its latency overlaps the stores.
-template <int IN_T>
-__global__ void __launch_bounds__(kThreads, 6) sparse_emit_kernel(const void *__restrict__ x, long long n,
-                                                               const uint32_t *__restrict__ offsets,
-                                                               const uint32_t *__restrict__ seg,
-                                                               long long nseg, double lim,
-                                                               uint32_t *__restrict__ hdr,
-                                                               void *__restrict__ vals,
-                                                               int32_t *__restrict__ idx, int vec,
-                                                               int pairs)
-{
-    using E = typename Elem<IN_T>::type;
-    constexpr int es = dtype_size(IN_T);
-    constexpr bool W16 = es == 2;
-    constexpr int kWarps = kThreads / 32;
-    __shared__ uint32_t wsum[2 * kWarps];  // warp totals, then their exclusive prefixes
-    __shared__ uint32_t swd[kSpTile];      // 16-bit: value | index << 16; fp32: value bits
-    __shared__ uint16_t sidx[W16 ? 1 : kSpTile]; // fp32: the index in the tile
-    __shared__ unsigned long long s_total;
-    __shared__ uint32_t s_local;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const long long tiles = (n + kSpTile - 1) / kSpTile;
-    if (warp == 0) { // the total of all segments
-        unsigned long long t = 0;
-        for (long long i = lane; i < nseg; i += 32)
-            t += seg[i];
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1)
-            t += __shfl_xor_sync(kFull, t, o);
-        if (lane == 0)
-            s_total = t;
+    if (threadIdx.x == 0) {
+        seg[blockIdx.x] = total;
+        __threadfence();
+        s_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
     }
     __syncthreads();
-    const unsigned long long total = s_total;
-    const bool sparse = (double)total < lim;
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        hdr[0] = sparse ? 1u : 0u;
-        hdr[1] = (uint32_t)total;
+    if (!s_last)
+        return;
+    __threadfence();
+    const long long nseg = gridDim.x;
+    uint32_t carry = 0;
+    for (long long b0 = 0; b0 < nseg; b0 += kScanThreads) {
+        const long long i = b0 + threadIdx.x;
+        const uint32_t y = i < nseg ? __ldcg(seg + i) : 0u;
+        uint32_t all;
+        const uint32_t incl = block_scan(y, &all);
+        if (i < nseg)
+            seg[i] = carry + incl - y;
+        carry += all;
     }
-    if (!sparse) { // dense message: vals = x, bit for bit
+    if (threadIdx.x == 0) {
+        hdr[0] = (double)carry < lim ? 1u : 0u;
+        hdr[1] = carry;
+        *ticket = 0u;
+    }
+}
+
+// Pass 3: every chunk's run at its offset (counts[c] + seg[c / kSegChunks]),
+// or, when the header says dense, vals = x bit for bit.  The next chunk's
+// words are loaded once this chunk is staged, so that their latency
+// overlaps the stores.
+template <int IN_T>
+__global__ void __launch_bounds__(kThreads, 4) sparse_emit_kernel(
+    const void *__restrict__ x, long long n, long long chunks, const uint32_t *__restrict__ offs,
+    const uint32_t *__restrict__ segbase, const uint32_t *__restrict__ hdr, void *__restrict__ vals,
+    int32_t *__restrict__ idx, int vec, int quads)
+{
+    using E = typename Elem<IN_T>::type;
+    constexpr int es = SpChunk<IN_T>::es, EPW = SpChunk<IN_T>::epw, W = SpChunk<IN_T>::words;
+    constexpr bool W16 = es == 2;
+    constexpr int kWarps = kThreads / 32;
+    // the staged run, 3 slots of room in front: slot k of the run sits at
+    // position k + (ob & 3), so that a 4-aligned output group is one
+    // 16-byte shared-memory word
+    constexpr int kStage = kSpChunk + 4;
+    __shared__ __align__(16) uint32_t swd[kWarps][kStage]; // 16-bit: value | index << 16; fp32: value
+    __shared__ __align__(8) uint16_t sidx[W16 ? 1 : kWarps][W16 ? 4 : kStage]; // fp32: index in the chunk
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (hdr[0] == 0u) { // dense message: vals = x, bit for bit
         const long long groups = (n + 7) / 8;
         for (long long gi = blockIdx.x * (long long)kThreads + threadIdx.x; gi < groups;
              gi += (long long)gridDim.x * kThreads) {
@@ -361,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 6) sparse_emit_kernel(const void *__
             if (vec && vl == 8) {
 #pragma unroll
                 for (int b = 0; b < es / 2; ++b)
-                    reinterpret_cast<uint4 *>(dst)[b] = reinterpret_cast<const uint4 *>(src)[b];
+                    reinterpret_cast<uint4 *>(dst)[b] = __ldcs(reinterpret_cast<const uint4 *>(src) + b);
             } else {
                 for (int i = 0; i < vl; ++i)
                     reinterpret_cast<E *>(dst)[i] = reinterpret_cast<const E *>(src)[i];
@@ -369,108 +395,112 @@ __global__ void __launch_bounds__(kThreads, 6) sparse_emit_kernel(const void *__
         }
         return;
     }
-    uint32_t bits[2][8], msk[2];
-    uint32_t off_next = 0; // the next tile's offset within its segment
-    auto load_tile = [&](long long t) {
+    uint32_t *wsd = swd[warp];
+    uint16_t *wsi = sidx[W16 ? 0 : warp];
+    const long long warps = (long long)gridDim.x * kWarps;
+    long long c = blockIdx.x * (long long)kWarps + warp;
+    uint4 q[W];
+    if (c < chunks)
+        load_chunk<IN_T>(x, n, c, lane, vec, q);
+    for (; c < chunks; c += warps) {
+        const uint32_t ob = offs[c] + segbase[c / kSegChunks]; // the run's first output position
+        const uint32_t sh = ob & 3u;
+        // this lane's masks (word j at bits j*EPW..) and slots
+        uint32_t msk = 0, cw[W];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const long long e0 = t * kSpTile + (long long)h * 2048 + 8 * threadIdx.x;
-            msk[h] = nz_mask8_bits<IN_T>(x, n, e0, vec, bits[h]);
+        for (int j = 0; j < W; ++j) {
+            const uint32_t m = word_mask<IN_T>(q[j]);
+            msk |= m << (j * EPW);
+            cw[j] = (uint32_t)__popc(m);
         }
-        off_next = offsets[t];
-    };
-    long long t = blockIdx.x;
-    if (t < tiles)
-        load_tile(t);
-    for (; t < tiles; t += gridDim.x) {
-        // positions in the tile's compacted run: half 0 (every thread) before
-        // half 1, a thread's 8 elements in order within each half
-        uint32_t before[2];
+        uint32_t slot[W];
+        uint32_t run = sh; // the staging positions of the words before word j
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t wt;
-            before[h] = warp_prefix8(__popc(msk[h]), lane, wt);
-            if (lane == 0)
-                wsum[h * kWarps + warp] = wt;
-        }
-        __syncthreads();
-        if (warp == 0) { // exclusive prefix over (half, warp), and the tile's total
-            const uint32_t v = lane < 2 * kWarps ? wsum[lane] : 0u;
-            uint32_t incl = v;
+        for (int j = 0; j < W; j += 2) {
+            const uint32_t c2 = cw[j] | (cw[j + 1] << 16);
+            uint32_t i2 = c2;
 #pragma unroll
-            for (int o = 1; o < 2 * kWarps; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(kFull, incl, o);
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, i2, o);
                 if (lane >= o)
-                    incl += y;
+                    i2 += y;
             }
-            if (lane < 2 * kWarps)
-                wsum[lane] = incl - v;
-            if (lane == 2 * kWarps - 1)
-                s_local = incl;
+            const uint32_t t2 = __shfl_sync(kFull, i2, 31), e2 = i2 - c2;
+            slot[j] = run + (e2 & 0xffffu);
+            run += t2 & 0xffffu;
+            slot[j + 1] = run + (e2 >> 16);
+            run += t2 >> 16;
         }
-        __syncthreads();
+        const uint32_t len = run - sh; // the chunk's nonzeros
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t q = wsum[h * kWarps + warp] + before[h];
-            const uint32_t e0 = h * 2048 + 8 * threadIdx.x; // within the tile
+        for (int j = 0; j < W; ++j) {
+            const uint32_t ib = (uint32_t)((32 * j + lane) * EPW);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if ((msk[h] >> i) & 1u) {
+            for (int i = 0; i < EPW; ++i)
+                if ((msk >> (j * EPW + i)) & 1u) {
                     if constexpr (W16) {
-                        swd[q] = bits[h][i] | ((e0 + i) << 16); // value bits | index
+                        const uint32_t v = (u4_at(q[j], i >> 1) >> (16 * (i & 1))) & 0xffffu;
+                        wsd[slot[j]] = v | ((ib + i) << 16);
                     } else {
-                        swd[q] = bits[h][i];
-                        sidx[q] = (uint16_t)(e0 + i);
+                        wsd[slot[j]] = u4_at(q[j], i);
+                        wsi[slot[j]] = (uint16_t)(ib + i);
                     }
-                    ++q;
+                    ++slot[j];
                 }
         }
-        const uint32_t local = s_local;
-        __syncthreads();
-        uint32_t base = off_next;
-        const uint32_t tseg = (uint32_t)(t / kSegTiles);
-        for (uint32_t s2 = 0; s2 < tseg; ++s2)
-            base += seg[s2];
-        // the next tile's input, in flight while this tile's run is written
-        const long long tn = t + gridDim.x;
-        if (tn < tiles)
-            load_tile(tn);
-        const int32_t t0 = (int32_t)(t * kSpTile);
-        int32_t *ip = idx + base;
-        if constexpr (W16) {
-            uint16_t *vp = reinterpret_cast<uint16_t *>(vals) + base;
-            if (pairs && (base & 1u) == 0u) { // pairs: a 4-byte value and an 8-byte index store
-                for (uint32_t k = 2 * threadIdx.x; k < local; k += 2 * kThreads) {
-                    const uint32_t a = swd[k];
-                    if (k + 1 < local) {
-                        const uint32_t b = swd[k + 1];
-                        *reinterpret_cast<uint32_t *>(vp + k) = (a & 0xffffu) | (b << 16);
-                        *reinterpret_cast<int2 *>(ip + k) =
-                            make_int2(t0 + (int32_t)(a >> 16), t0 + (int32_t)(b >> 16));
-                    } else {
-                        vp[k] = (uint16_t)a;
-                        ip[k] = t0 + (int32_t)(a >> 16);
-                    }
-                }
+        __syncwarp();
+        if (c + warps < chunks)
+            load_chunk<IN_T>(x, n, c + warps, lane, vec, q);
+        // the run in 4-aligned groups; group g covers output positions
+        // (ob & ~3) + 4g .., staged at positions 4g ..
+        const int32_t t0 = (int32_t)(c * kSpChunk);
+        const uint32_t ngr = (sh + len + 3u) >> 2;
+        const long long obase = (long long)(ob - sh);
+        for (uint32_t g = lane; g < ngr; g += 32) {
+            const int k0 = (int)(4u * g) - (int)sh; // run position of the group's first slot
+            const uint4 s4 = reinterpret_cast<const uint4 *>(wsd)[g];
+            const uint32_t w4[4] = {s4.x, s4.y, s4.z, s4.w};
+            int32_t i4[4];
+            if constexpr (W16) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    i4[u] = t0 + (int32_t)(w4[u] >> 16);
             } else {
-                for (uint32_t k = threadIdx.x; k < local; k += kThreads) {
-                    const uint32_t a = swd[k];
-                    vp[k] = (uint16_t)a;
-                    ip[k] = t0 + (int32_t)(a >> 16);
+                const uint2 x2 = reinterpret_cast<const uint2 *>(wsi)[g];
+                i4[0] = t0 + (int32_t)(x2.x & 0xffffu);
+                i4[1] = t0 + (int32_t)(x2.x >> 16);
+                i4[2] = t0 + (int32_t)(x2.y & 0xffffu);
+                i4[3] = t0 + (int32_t)(x2.y >> 16);
+            }
+            const long long o = obase + 4LL * g;
+            if (quads && k0 >= 0 && k0 + 4 <= (int)len) {
+                *reinterpret_cast<int4 *>(idx + o) = make_int4(i4[0], i4[1], i4[2], i4[3]);
+                if constexpr (W16)
+                    *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(vals) + o) =
+                        make_uint2(__byte_perm(w4[0], w4[1], 0x5410), __byte_perm(w4[2], w4[3], 0x5410));
+                else
+                    *reinterpret_cast<uint4 *>(reinterpret_cast<uint32_t *>(vals) + o) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int k = k0 + u;
+                    if (k >= 0 && k < (int)len) {
+                        idx[o + u] = i4[u];
+                        if constexpr (W16)
+                            reinterpret_cast<uint16_t *>(vals)[o + u] = (uint16_t)w4[u];
+                        else
+                            reinterpret_cast<uint32_t *>(vals)[o + u] = w4[u];
+                    }
                 }
             }
-        } else {
-            uint32_t *vp = reinterpret_cast<uint32_t *>(vals) + base;
-            for (uint32_t k = threadIdx.x; k < local; k += kThreads) {
-                vp[k] = swd[k];
-                ip[k] = t0 + (int32_t)sidx[k];
-            }
         }
-        __syncthreads(); // the staging arrays are reused by the next tile
+        __syncwarp(); // (the staging area is reused by the next chunk)
     }
 }
 
 // ---------------------------------------------------------------- sparse decode
+constexpr int kSpTile = 4096; // elements per decoder tile
 // Dense message: a streaming copy (or add) of the values into acc.
 template <int IN_T>
 __global__ void __launch_bounds__(kThreads) sparse_dense_kernel(const uint32_t *__restrict__ hdr,
@@ -773,34 +803,55 @@ cudaError_t launch_bfp_decode(const int8_t *exps, const uint8_t *mants, long lon
     return cudaGetLastError();
 }
 
-// Scratch: one count (then offset) per 4096-element tile, then one total per
-// segment of 4096 tiles.
+// Scratch: the scan's ticket (word 0, at a fixed place whatever n is: it
+// must read zero when every call starts; the scan's last block resets it),
+// from word 8 one count (then offset) per 1024-element chunk, then one total
+// (then base) per segment of 4096 chunks.
+constexpr long long kSpHeadWords = 8;
 long long sparse_encode_scratch_words(long long n)
 {
-    const long long tiles = (n + kSpTile - 1) / kSpTile;
-    return tiles + (tiles + kSegTiles - 1) / kSegTiles;
+    const long long chunks = (n + kSpChunk - 1) / kSpChunk;
+    return kSpHeadWords + chunks + (chunks + kSegChunks - 1) / kSegChunks;
+}
+
+// Resident blocks per SM of a kernel, asked once per kernel.
+template <typename K> int blocks_per_sm(K kernel)
+{
+    static int occ = 0;
+    if (occ < 1 &&
+        (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess ||
+         occ < 1))
+        occ = 1;
+    return occ;
 }
 
 cudaError_t launch_sparse_encode(const void *x, long long n, int dtype, double one_minus_thr,
                                  uint32_t *hdr, void *vals, int32_t *idx, uint32_t *scratch,
                                  cudaStream_t st)
 {
-    const long long tiles = (n + kSpTile - 1) / kSpTile;
-    const long long nseg = (tiles + kSegTiles - 1) / kSegTiles;
-    uint32_t *seg = scratch + tiles;
+    const long long chunks = (n + kSpChunk - 1) / kSpChunk;
+    const long long nseg = (chunks + kSegChunks - 1) / kSegChunks;
+    uint32_t *ticket = scratch;
+    uint32_t *counts = scratch + kSpHeadWords;
+    uint32_t *seg = counts + chunks;
     const double lim = one_minus_thr * (double)n; // sparse iff nnz < lim
     const int vec = aligned16(x) && aligned16(vals) ? 1 : 0;
-    const int grid = grid_for(tiles, 1);
-    const int egrid = grid;
-    // pairs of 16-bit values and of indices leave in one store each
-    const int pairs = (reinterpret_cast<uintptr_t>(vals) & 3u) == 0 &&
-                      (reinterpret_cast<uintptr_t>(idx) & 7u) == 0;
+    const int es = dtype == kF32 ? 4 : 2;
+    // 4-element groups of the run leave in one index and one value store
+    const int quads = (reinterpret_cast<uintptr_t>(idx) & 15u) == 0 &&
+                      (reinterpret_cast<uintptr_t>(vals) & (uintptr_t)(4 * es - 1)) == 0;
+    const long long wblocks = (chunks + kThreads / 32 - 1) / (kThreads / 32); // a warp per chunk
 #define RRA_SP(T)                                                                              \
     do {                                                                                       \
-        sparse_count_kernel<T><<<grid, kThreads, 0, st>>>(x, n, scratch, vec);                 \
-        sparse_segscan_kernel<<<(unsigned)nseg, kScanThreads, 0, st>>>(scratch, tiles, seg);   \
-        sparse_emit_kernel<T><<<egrid, kThreads, 0, st>>>(x, n, scratch, seg, nseg, lim, hdr,  \
-                                                          vals, idx, vec, pairs);              \
+        const int cg = (int)std::max(1LL, std::min(wblocks, (long long)num_sms() *             \
+                                                     blocks_per_sm(sparse_count_kernel<T>)));  \
+        const int eg = (int)std::max(1LL, std::min(wblocks, (long long)num_sms() *             \
+                                                     blocks_per_sm(sparse_emit_kernel<T>)));   \
+        sparse_count_kernel<T><<<cg, kThreads, 0, st>>>(x, n, chunks, counts, vec);            \
+        sparse_scan_kernel<<<(unsigned)nseg, kScanThreads, 0, st>>>(counts, chunks, seg,       \
+                                                                   ticket, lim, hdr);          \
+        sparse_emit_kernel<T><<<eg, kThreads, 0, st>>>(x, n, chunks, counts, seg, hdr, vals,   \
+                                                       idx, vec, quads);                       \
     } while (0)
     if (dtype == kF32) RRA_SP(kF32);
     else if (dtype == kF16) RRA_SP(kF16);

@@ -1,15 +1,15 @@
 // noalloc.cu -- rra_sparse_encode_noalloc: the sparse encoder for callers
 // that cannot allocate device memory.
 //
-// rra_sparse_encode needs scratch (one 32-bit count per 4096-element tile,
-// and one total per 4096 tiles) and takes it from a per-device workspace that
+// rra_sparse_encode needs scratch (one 32-bit count per 1024-element chunk,
+// and one total per 4096 chunks) and takes it from a per-device workspace that
 // grows with cudaMalloc.  Some callers cannot allow that: processes whose
 // device memory is handed out by their own allocator or budgeted up front,
 // latency-critical loops in which an allocation's implicit device
 // synchronisation is not acceptable, and libraries that must not call into
 // the CUDA allocator behind their host framework's back.  This entry point
 // uses a fixed scratch array that lives in the library image instead: a
-// file-scope __device__ array of kNoallocScratchWords words (about 256 KiB),
+// file-scope __device__ array of kNoallocScratchWords words (about 1 MiB),
 // present on every GPU that loads the library until the process exits.
 #include <cuda_runtime.h>
 
@@ -21,9 +21,10 @@
 
 namespace {
 
-// one word per 4096-element tile of the largest input, then one per 4096 tiles
-constexpr long long kNoallocTiles = (long long)RRA_NOALLOC_MAX_COUNT / 4096;
-constexpr long long kNoallocScratchWords = kNoallocTiles + (kNoallocTiles + 4095) / 4096;
+// eight words (the scan's ticket), one word per 1024-element chunk of the
+// largest input, then one per 4096 chunks
+constexpr long long kNoallocChunks = (long long)RRA_NOALLOC_MAX_COUNT / 1024;
+constexpr long long kNoallocScratchWords = 8 + kNoallocChunks + (kNoallocChunks + 4095) / 4096;
 
 // The scratch itself.  In host code this name is only a host-side stand-in,
 // not a device address: the address a kernel may use comes from
@@ -35,10 +36,12 @@ std::mutex g_mu;
 uint32_t *g_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up once
-// per device, on the first call with that device current.  The address
-// stays valid for the life of the device's primary context; after a
-// cudaDeviceReset the entry point must not be called again in this process.
-cudaError_t scratch_for_current_device(uint32_t **out)
+// per device, on the first call with that device current; that call also
+// clears the array on its stream (the scan's ticket word must start at zero;
+// the encoder resets it after every call).  The address stays valid for the
+// life of the device's primary context; after a cudaDeviceReset the entry
+// point must not be called again in this process.
+cudaError_t scratch_for_current_device(uint32_t **out, cudaStream_t st)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -50,6 +53,9 @@ cudaError_t scratch_for_current_device(uint32_t **out)
     if (!g_ptr[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess)
+            return e;
+        e = cudaMemsetAsync(p, 0, sizeof(g_noalloc_scratch), st);
         if (e != cudaSuccess)
             return e;
         g_ptr[dev] = static_cast<uint32_t *>(p);
@@ -72,10 +78,12 @@ extern "C" rra_status rra_sparse_encode_noalloc(const void *x, size_t n, rra_dty
         rra::sparse_encode_scratch_words((long long)n) > kNoallocScratchWords)
         return RRA_ERR_INVALID; // beyond the fixed scratch: use rra_sparse_encode
     uint32_t *scratch = nullptr;
-    if (scratch_for_current_device(&scratch) != cudaSuccess)
+    if (scratch_for_current_device(&scratch, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
         return RRA_ERR_CUDA;
-    // every word the count and scan passes write is read only after it was
-    // written in the same call, so nothing needs clearing between calls
+    // every count and segment word is written in a call before that call
+    // reads it, and the scan's ticket is back at zero when a call ends, so
+    // nothing needs clearing between calls
     return rra::launch_sparse_encode(x, (long long)n, dtype, 1.0 - (double)threshold, hdr, vals,
                                      idx, scratch,
                                      reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess

@@ -758,6 +758,48 @@ def test_sparse_codec_many_tiles(dt, offset):
     assert float(store[0]) == 3.0 or offset == 0
 
 
+def _encode_and_check(x, dt, thr, stream=None):
+    n = x.numel()
+    hdr = torch.zeros(2, dtype=torch.int32, device="cuda")
+    vals = torch.zeros(n, dtype=x.dtype, device="cuda")
+    idx = torch.full((n,), -1, dtype=torch.int32, device="cuda")
+    rra.sparse_encode(x, thr, hdr, vals, idx, stream=stream)
+    torch.cuda.synchronize()
+    rh, rv, ri = O.sparse_encode(host(x), dt, float(np.float32(thr)))
+    assert list(host(hdr).view(np.uint32)) == list(rh)
+    k = int(rh[1]) if rh[0] else n
+    assert np.array_equal(bitsof_any(host(vals)[:k]), bitsof_any(rv))
+    if rh[0]:
+        assert np.array_equal(host(idx)[:k], ri)
+    return int(rh[0])
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32", "f16"])
+@pytest.mark.parametrize("dense_frac,thr", [(0.6, 0.5), (0.97, 0.5), (0.2, 0.9), (0.45, 0.5)])
+def test_sparse_encode_dense_prefix_inputs(dt, dense_frac, thr):
+    """Nonzeros only in a leading part of x, zeros after it: the format
+    follows the total count alone, and a dense message copies the zeros
+    too.  (0.45, 0.5) stays sparse."""
+    n = 40 * 4096 + 1234
+    x = W.sparse(1, n, seed=int(dense_frac * 100), p_zero=0.0, dtype=TORCH_DT[dt])[0]
+    x[int(dense_frac * n):] = 0
+    fmt = _encode_and_check(x, dt, thr)
+    assert fmt == (1 if dense_frac < 1 - thr else 0)
+
+
+def test_sparse_encode_calls_in_a_row():
+    """Encodes of different sizes and dtypes on one stream, sharing the
+    stream's scratch: larger and smaller chunk counts in turn, so that a
+    count or offset left by an earlier call would show."""
+    cases = [((1 << 22) + 17, 0.6, "bf16"), (70_001, 0.7, "f32"), ((1 << 22) + 17, 0.3, "bf16"),
+             (5_000_000, 0.8, "f16"), (4096, 0.5, "f32"), ((1 << 22) + 17, 0.6, "bf16")]
+    fmts = set()
+    for i, (n, pz, dt) in enumerate(cases):
+        x = W.sparse(1, n, seed=200 + i, p_zero=pz, dtype=TORCH_DT[dt])[0]
+        fmts.add(_encode_and_check(x, dt, 0.5))
+    assert fmts == {0, 1}
+
+
 def test_sparse_codec_concurrent_streams():
     """Encodes and decodes queued on two streams without ordering between
     them: each stream has its own scratch, so both results match the oracle."""
