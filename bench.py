@@ -435,6 +435,18 @@ def run_rra(args, world, rank, local):
     assert wl.comm.status() == rra.RRA_OK
 
     K = args.steps
+    if K is None:
+        # about one second of timed work: the step time from a few more
+        # untimed steps, the same K on every rank
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(3):
+            wl.step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_step = max_over_ranks(world, e0.elapsed_time(e1) / 3) * 1e-3
+        K = int(max(20, min(10000, round(1.0 / max(t_step, 1e-7)))))
+        args.steps = K
     # The K timed steps are one CUDA graph of K back-to-back calls, so the
     # host's per-call cost (argument marshalling, launch) stays outside the
     # device timeline; the same calls made eagerly, one event pair per step,
@@ -654,6 +666,8 @@ def run_reference(args, world, rank):
     """The oracle timed on the host cores, one bounded sample per step."""
     if rank != 0:
         return
+    if args.steps is None:
+        args.steps = 20
     wl = Workload(args.config, use_lib=False, ef=args.ef)
     n = wl.T // wl.N
     hosts = [host_copy(x) for x in wl.inputs]
@@ -988,7 +1002,9 @@ def run_drift(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about one second of timed work, 20 to 10000 "
+                         "steps; the reference arm: 20)")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["rra", "reference"], default="rra")
     ap.add_argument("--config", choices=CONFIG_NAMES, default="bfp8_bucket")

@@ -28,18 +28,19 @@ constexpr int kCountWarps = kCountThreads / 32;
 // c = b / bpc; a warp takes 256 consecutive elements of the chunk at a time,
 // 8 per lane, and for each hop h adds rank (c + h) mod N's elements to its
 // running fp32 partial and counts the elements whose bits are not +0.0.
-// The raw 16-byte words of a batch of hops (16 words per lane: 16 hops of
-// 16-bit data, 8 of fp32, 4 of fp32 with a prev stream) are loaded before
-// any is used, so every lane keeps up to 16 loads in flight.
+// The raw 16-byte words of a batch of hops (8 words per lane: 8 hops of
+// 16-bit data, 4 of fp32, 2 of fp32 with a prev stream) are loaded before
+// any is used, so every lane keeps up to 8 loads in flight (and three
+// blocks fit an SM).
 template <int IN_KIND, bool VEC>
-__global__ void __launch_bounds__(kCountThreads, 2)
+__global__ void __launch_bounds__(kCountThreads, 3)
     sparse_chunk_count_kernel(const __grid_constant__ SpCountArgs a)
 {
     constexpr bool PREV = IN_KIND == kF32Diff;
     constexpr int LT = PREV ? kF32 : IN_KIND;
     constexpr int es = dtype_size(LT);
     constexpr int kWords = (es == 4 ? 2 : 1) * (PREV ? 2 : 1); // 16-byte words per hop
-    constexpr int kBatch = 16 / kWords;                         // hops per batch
+    constexpr int kBatch = 8 / kWords;                          // hops per batch
     using E = typename Elem<LT>::type;
     __shared__ unsigned long long s_cnt[kCountWarps][kMaxRanks];
     __shared__ bool s_last;
