@@ -471,9 +471,14 @@ rra_status rra_autotune(rra_comm *comm, const void *const *in, void *const *out,
 /* Size-based choice between ring and tree ([ring] section "真实世界中的生产模式":
  * pick ring or tree by message size, from measurement; section "练习": add
  * the tree variant, switch by size and measure the crossover).  The default
- * crossover is the one measured on GB300 for N = 2..64: the ring is never
- * slower than the tree from 4 MiB per rank on. */
-#define RRA_DEFAULT_CROSSOVER (4ull << 20)
+ * crossover follows the measurement on GB300 (lossless fp32 in place, 1 KiB
+ * to 1 GiB per rank): for N = 2 and 4 the ring is never slower from 256 MiB
+ * per rank on (RRA_DEFAULT_CROSSOVER); for N = 8, 16 and 64 the tree was the
+ * faster at every measured size, so from N = 5 on the default sends every
+ * message up to 1 GiB per rank to the tree (RRA_DEFAULT_CROSSOVER_WIDE, one
+ * byte above the largest size measured). */
+#define RRA_DEFAULT_CROSSOVER (256ull << 20)
+#define RRA_DEFAULT_CROSSOVER_WIDE ((1ull << 30) + 1)
 #define RRA_ALGO_RING 0
 #define RRA_ALGO_TREE 1
 
@@ -486,8 +491,9 @@ rra_status rra_autotune(rra_comm *comm, const void *const *in, void *const *out,
 rra_status rra_allreduce_auto(rra_comm *comm, void *const *buf, size_t count, rra_dtype dtype,
                               void *stream, int *algorithm);
 
-/* Crossover of rra_allreduce_auto in bytes per rank (0 restores
- * RRA_DEFAULT_CROSSOVER).  Errors: RRA_ERR_INVALID for NULL. */
+/* Crossover of rra_allreduce_auto in bytes per rank (0 restores the
+ * default: RRA_DEFAULT_CROSSOVER for N <= 4, RRA_DEFAULT_CROSSOVER_WIDE
+ * otherwise).  Errors: RRA_ERR_INVALID for NULL. */
 rra_status rra_set_crossover(rra_comm *comm, size_t bytes_per_rank);
 rra_status rra_get_crossover(rra_comm *comm, size_t *bytes_per_rank);
 

@@ -26,7 +26,13 @@ RRA_OK, RRA_ERR_INVALID, RRA_ERR_UNSUPPORTED, RRA_ERR_CUDA, RRA_ERR_TIMEOUT, RRA
 RRA_ALGO_RING, RRA_ALGO_TREE = 0, 1
 # operations for the operator-aware codec choice (rra_codec_*_op)
 RRA_OP_ALLREDUCE, RRA_OP_ALLGATHER, RRA_OP_BROADCAST = 0, 1, 2
-RRA_DEFAULT_CROSSOVER = 4 << 20
+RRA_DEFAULT_CROSSOVER = 256 << 20          # N <= 4
+RRA_DEFAULT_CROSSOVER_WIDE = (1 << 30) + 1  # N >= 5
+
+
+def default_crossover(N: int) -> int:
+    """rra_allreduce_auto's crossover for N ranks until one is set or measured."""
+    return RRA_DEFAULT_CROSSOVER if N <= 4 else RRA_DEFAULT_CROSSOVER_WIDE
 RRA_F32, RRA_F16, RRA_BF16 = 0, 1, 2
 CODEC_NONE, CODEC_BFP, CODEC_SPARSE = 0, 1, 2
 MAX_RANKS = 64

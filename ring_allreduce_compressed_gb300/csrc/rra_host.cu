@@ -1039,11 +1039,22 @@ rra_status rra_set_crossover(rra_comm *comm, size_t bytes_per_rank)
     return RRA_OK;
 }
 
+namespace {
+// The communicator's crossover: the one set or measured, else the default
+// for its rank count.
+size_t crossover_of(const rra_comm *comm)
+{
+    if (comm->crossover)
+        return comm->crossover;
+    return comm->N <= 4 ? (size_t)RRA_DEFAULT_CROSSOVER : (size_t)RRA_DEFAULT_CROSSOVER_WIDE;
+}
+} // namespace
+
 rra_status rra_get_crossover(rra_comm *comm, size_t *bytes_per_rank)
 {
     if (!comm || !bytes_per_rank)
         return RRA_ERR_INVALID;
-    *bytes_per_rank = comm->crossover ? comm->crossover : RRA_DEFAULT_CROSSOVER;
+    *bytes_per_rank = crossover_of(comm);
     return RRA_OK;
 }
 
@@ -1052,7 +1063,7 @@ rra_status rra_allreduce_auto(rra_comm *comm, void *const *buf, size_t count, rr
 {
     if (!comm || !buf || !valid_dtype(dtype))
         return RRA_ERR_INVALID;
-    const size_t cross = comm->crossover ? comm->crossover : RRA_DEFAULT_CROSSOVER;
+    const size_t cross = crossover_of(comm);
     // the tree sums fp32 only; other dtypes always take the ring
     const bool tree = dtype == RRA_F32 && count * esize(dtype) < cross;
     if (algorithm)

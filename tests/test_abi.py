@@ -118,6 +118,8 @@ def test_header_constants_match_the_binding():
         assert int(consts[name]) == getattr(rra, name)
     m = re.search(r"#define RRA_DEFAULT_CROSSOVER \((\d+)ull << (\d+)\)", text)
     assert int(m.group(1)) << int(m.group(2)) == rra.RRA_DEFAULT_CROSSOVER
+    m = re.search(r"#define RRA_DEFAULT_CROSSOVER_WIDE \(\(1ull << (\d+)\) \+ 1\)", text)
+    assert (1 << int(m.group(1))) + 1 == rra.RRA_DEFAULT_CROSSOVER_WIDE
     assert int(consts["RRA_RING_SLICE"]) == rra.RING_SLICE
     assert int(consts["RRA_BFP_BLOCK"]) == rra.BFP_BLOCK
     assert int(consts["RRA_SPARSE_PER_CHUNK"]) == rra.SPARSE_PER_CHUNK

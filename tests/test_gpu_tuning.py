@@ -73,9 +73,13 @@ def test_autotune_other_key_is_untouched():
 
 @pytest.mark.parametrize("N", [2, 5, 8])
 def test_allreduce_auto_follows_the_crossover(N):
-    T_small, T_large = 1000, (rra.RRA_DEFAULT_CROSSOVER // 4) + 24
+    # the default for N (256 MiB per rank up to N = 4, above 1 GiB from
+    # N = 5), then a 4 MiB crossover set by the caller
+    T_small, T_large = 1000, (4 << 20) // 4 + 24
     comm = rra.Comm(N, T_large)
-    assert comm.crossover() == rra.RRA_DEFAULT_CROSSOVER
+    assert comm.crossover() == rra.default_crossover(N)
+    comm.set_crossover(4 << 20)
+    assert comm.crossover() == 4 << 20
     for T, algo in [(T_small, rra.RRA_ALGO_TREE), (T_large, rra.RRA_ALGO_RING)]:
         xs = rand_f32(N, T, seed=N + T)
         bufs = [x.clone() for x in xs]
@@ -96,7 +100,7 @@ def test_allreduce_auto_follows_the_crossover(N):
     assert comm.allreduce_auto(h) == rra.RRA_ALGO_RING
     assert comm.status() == rra.RRA_OK
     comm.set_crossover(0)
-    assert comm.crossover() == rra.RRA_DEFAULT_CROSSOVER
+    assert comm.crossover() == rra.default_crossover(N)
     comm.close()
 
 
