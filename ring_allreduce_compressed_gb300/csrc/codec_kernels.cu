@@ -596,6 +596,10 @@ __global__ void __launch_bounds__(kThreads) sparse_tile_starts_kernel(
     }
 }
 
+// Pairs of a tile each thread holds in registers (the rest, if a tile lists
+// more than kThreads * kFillPairs values, are read in a second loop).
+constexpr int kFillPairs = 8;
+
 template <int IN_T>
 __global__ void __launch_bounds__(kThreads) sparse_fill_kernel(const uint32_t *__restrict__ hdr,
                                                                const void *__restrict__ vals,
@@ -609,29 +613,59 @@ __global__ void __launch_bounds__(kThreads) sparse_fill_kernel(const uint32_t *_
     if (hdr[0] == 0u || accumulate)
         return;
     const long long tiles = (n + kSpTile - 1) / kSpTile;
-    for (long long t = blockIdx.x; t < tiles; t += gridDim.x) {
+    // The tile's listed (index, value) pairs k = kb + tid + kThreads*j are read
+    // into registers one tile ahead: the next tile's loads are in flight
+    // while this tile is written out.  The tile buffer is +0.0 between tiles:
+    // each thread zeroes the words it has just written out.
+    int32_t pi[kFillPairs];
+    float pv[kFillPairs];
+    long long kb = 0, ke = 0;
+    auto fetch = [&](long long t) {
+        kb = start[t];
+        ke = start[t + 1];
+#pragma unroll
+        for (int j = 0; j < kFillPairs; ++j) {
+            const long long k = kb + threadIdx.x + (long long)kThreads * j;
+            pi[j] = k < ke ? idx[k] : -1;
+            pv[j] = k < ke ? to_f32(reinterpret_cast<const E *>(vals)[k]) : 0.0f;
+        }
+    };
+    for (int i = threadIdx.x; i < kSpTile; i += kThreads)
+        tile[i] = 0.0f;
+    long long t = blockIdx.x;
+    if (t < tiles)
+        fetch(t);
+    __syncthreads();
+    for (; t < tiles; t += gridDim.x) {
         const long long t0 = t * kSpTile, t1 = min(n, t0 + kSpTile);
-        for (int i = threadIdx.x; i < kSpTile; i += kThreads)
-            tile[i] = 0.0f;
-        __syncthreads();
-        const long long kb = start[t], ke = start[t + 1];
-#pragma unroll 4
-        for (long long k = kb + threadIdx.x; k < ke; k += kThreads) {
+        // scatter the pairs (an index outside the tile is never written)
+#pragma unroll
+        for (int j = 0; j < kFillPairs; ++j)
+            if (pi[j] >= t0 && pi[j] < t1)
+                tile[pi[j] - t0] = pv[j];
+        for (long long k = kb + threadIdx.x + (long long)kThreads * kFillPairs; k < ke;
+             k += kThreads) {
             const long long i = idx[k];
             if (i >= t0 && i < t1)
                 tile[i - t0] = to_f32(reinterpret_cast<const E *>(vals)[k]);
         }
         __syncthreads();
+        if (t + gridDim.x < tiles)
+            fetch(t + gridDim.x);
         const int len = (int)(t1 - t0);
         if (vec && len == kSpTile) {
             float4 *dst = reinterpret_cast<float4 *>(acc + t0);
-            for (int j = threadIdx.x; j < kSpTile / 4; j += kThreads)
+            for (int j = threadIdx.x; j < kSpTile / 4; j += kThreads) {
                 dst[j] = reinterpret_cast<const float4 *>(tile)[j];
+                reinterpret_cast<float4 *>(tile)[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
         } else {
             for (int j = threadIdx.x; j < len; j += kThreads)
                 acc[t0 + j] = tile[j];
+            for (int j = threadIdx.x; j < kSpTile; j += kThreads)
+                tile[j] = 0.0f;
         }
-        __syncthreads(); // the tile is rebuilt for the next position
+        __syncthreads(); // the tile is +0.0 again before the next scatter
     }
 }
 

@@ -787,6 +787,40 @@ def test_sparse_encode_dense_prefix_inputs(dt, dense_frac, thr):
     assert fmt == (1 if dense_frac < 1 - thr else 0)
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("off", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (0, 2, 2), (3, 3, 3)])
+def test_sparse_encode_misaligned_buffers(dt, off):
+    """x, vals and idx starting off their 16-byte alignment (element offsets
+    1..3): the encoder falls back to element loads and to single-element
+    stores of the run; the result is the same bits."""
+    n = 5 * 1024 + 77
+    ox, ov, oi = off
+    big = W.sparse(1, n + ox, seed=ox + 10 * ov + 100 * oi, p_zero=0.6, dtype=TORCH_DT[dt])[0]
+    x = big[ox:]
+    hdr = torch.zeros(2, dtype=torch.int32, device="cuda")
+    vstore = torch.zeros(n + ov, dtype=TORCH_DT[dt], device="cuda")
+    istore = torch.full((n + oi,), -1, dtype=torch.int32, device="cuda")
+    vals, idx = vstore[ov:], istore[oi:]
+    rra.sparse_encode(x, 0.5, hdr, vals, idx)
+    rh, rv, ri = O.sparse_encode(host(x), dt, 0.5)
+    assert list(host(hdr).view(np.uint32)) == list(rh) and rh[0] == 1
+    k = int(rh[1])
+    assert np.array_equal(bitsof_any(host(vals)[:k]), bitsof_any(rv))
+    assert np.array_equal(host(idx)[:k], ri)
+    # nothing written before the views
+    assert all(int(v) == 0 for v in host(vstore[:ov]).view(np.uint16 if dt == "bf16" else np.uint32))
+    assert all(int(v) == -1 for v in host(istore[:oi]))
+
+
+@pytest.mark.parametrize("n", [1023, 1024, 1025, 4096 * 1024, 4096 * 1024 + 1])
+def test_sparse_encode_chunk_and_segment_edges(n):
+    """Sizes at the encoder's 1024-element chunk and 4096-chunk segment
+    boundaries, sparse and dense."""
+    for pz, fmt in ((0.7, 1), (0.2, 0)):
+        x = W.sparse(1, n, seed=n % 97 + int(10 * pz), p_zero=pz, dtype=torch.bfloat16)[0]
+        assert _encode_and_check(x, "bf16", 0.5) == fmt
+
+
 def test_sparse_encode_calls_in_a_row():
     """Encodes of different sizes and dtypes on one stream, sharing the
     stream's scratch: larger and smaller chunk counts in turn, so that a
