@@ -766,28 +766,40 @@ __global__ void __launch_bounds__(kThreads) codec_stats_kernel(const __grid_cons
     const long long lo = min(a.T, (long long)c * a.n), hi = min(a.T, lo + a.n);
     const char *base = reinterpret_cast<const char *>(a.in[r]);
     uint32_t cnt_nz = 0, cnt_f4 = 0, cnt_f8 = 0;
+    // kStatsU blocks per warp and iteration, all loaded before any is
+    // reduced, so that every lane keeps kStatsU loads in flight
+    constexpr int kStatsU = 4;
     const long long step = (long long)gridDim.x * (kThreads / 32) * kBlock;
     for (long long e0 = lo + ((long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kBlock;
-         e0 < hi; e0 += step) {
-        const int len = (int)min((long long)kBlock, hi - e0);
-        const int valid = min(max(len - 4 * lane, 0), 4);
-        float v[4];
-        load4<IN_T>(base + (e0 + 4 * lane) * es, valid, vec != 0, v);
-        unsigned mx = 0;
+         e0 < hi; e0 += kStatsU * step) {
+        float v[kStatsU][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            mx = max(mx, __float_as_uint(v[i]) & 0x7fffffffu);
-        mx = __reduce_max_sync(kFull, mx);
-        const int e = max((int)(mx >> 23), 1) - 127;
-        const float t4 = pow2_exact(e - 3), t8 = pow2_exact(e - 7);
+        for (int u = 0; u < kStatsU; ++u) {
+            const long long eu = e0 + u * step;
+            const int len = (int)min((long long)kBlock, max(hi - eu, 0LL));
+            const int valid = min(max(len - 4 * lane, 0), 4);
+            load4<IN_T>(base + (eu + 4 * lane) * es, valid, vec != 0, v[u]);
+        }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            // absent positions read +0.0: never counted
-            const bool nz = __float_as_uint(v[i]) != 0u;
-            const float m = fabsf(v[i]);
-            cnt_nz += nz ? 1u : 0u;
-            cnt_f4 += nz && m <= t4 ? 1u : 0u;
-            cnt_f8 += nz && m <= t8 ? 1u : 0u;
+        for (int u = 0; u < kStatsU; ++u) {
+            if (e0 + u * step >= hi) // (warp-uniform)
+                break;
+            unsigned mx = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                mx = max(mx, __float_as_uint(v[u][i]) & 0x7fffffffu);
+            mx = __reduce_max_sync(kFull, mx);
+            const int e = max((int)(mx >> 23), 1) - 127;
+            const float t4 = pow2_exact(e - 3), t8 = pow2_exact(e - 7);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                // absent positions read +0.0: never counted
+                const bool nz = __float_as_uint(v[u][i]) != 0u;
+                const float m = fabsf(v[u][i]);
+                cnt_nz += nz ? 1u : 0u;
+                cnt_f4 += nz && m <= t4 ? 1u : 0u;
+                cnt_f8 += nz && m <= t8 ? 1u : 0u;
+            }
         }
     }
     cnt_nz = __reduce_add_sync(kFull, cnt_nz);

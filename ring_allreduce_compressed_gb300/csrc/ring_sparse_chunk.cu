@@ -27,12 +27,15 @@ constexpr int kCountWarps = kCountThreads / 32;
 // Nonzero counts of every message (see SpCountArgs).  Block b works on chunk
 // c = b / bpc; a warp takes 256 consecutive elements of the chunk at a time,
 // 8 per lane, and for each hop h adds rank (c + h) mod N's elements to its
-// running fp32 partial and counts the elements whose bits are not +0.0.
+// running fp32 partial and counts the elements whose bits are not +0.0
+// (per lane in registers with at most 16 hops, else per warp and position).
 // The raw 16-byte words of a batch of hops (8 words per lane: 8 hops of
 // 16-bit data, 4 of fp32, 2 of fp32 with a prev stream) are loaded before
 // any is used, so every lane keeps up to 8 loads in flight (and three
 // blocks fit an SM).
-template <int IN_KIND, bool VEC>
+// NH16: at most 16 hops (N <= 16); each lane then keeps its counts of every
+// hop in registers and reduces them over the warp once, at the end.
+template <int IN_KIND, bool VEC, bool NH16>
 __global__ void __launch_bounds__(kCountThreads, 3)
     sparse_chunk_count_kernel(const __grid_constant__ SpCountArgs a)
 {
@@ -106,6 +109,63 @@ __global__ void __launch_bounds__(kCountThreads, 3)
     const long long lo = min((long long)c * a.n, a.T);
     const long long len = min(lo + a.n, a.T) - lo;
     const long long wstride = (long long)a.bpc * kCountWarps * kTile;
+    if constexpr (NH16) {
+        uint32_t cnt[16];
+#pragma unroll
+        for (int hh = 0; hh < 16; ++hh)
+            cnt[hh] = 0u;
+        for (long long w0 = ((long long)sub * kCountWarps + warp) * kTile; w0 < len; w0 += wstride) {
+            const long long e = w0 + 8 * lane;
+            const int valid = (int)min(max(len - e, 0LL), 8LL);
+            const long long off = lo + e;
+            const bool vec = VEC && valid == 8;
+            float p[8];
+#pragma unroll
+            for (int b = 0; b < 16 / kBatch; ++b) {
+                uint4 w[kBatch][kWords];
+                if (vec) {
+#pragma unroll
+                    for (int j = 0; j < kBatch; ++j)
+                        if (b * kBatch + j < nh)
+                            fetch(rank_of(a.h_lo + b * kBatch + j), off, w[j]);
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int hh = b * kBatch + j;
+                    if (hh < nh) {
+                        float x[8];
+                        if (vec)
+                            widen(w[j], x);
+                        else
+                            load_scalar(rank_of(a.h_lo + hh), off, valid, x);
+                        if (hh == 0) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                p[i] = x[i];
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 8; i += 2) {
+                                const float2 s2 = __fadd2_rn(make_float2(x[i], x[i + 1]),
+                                                             make_float2(p[i], p[i + 1]));
+                                p[i] = s2.x;
+                                p[i + 1] = s2.y;
+                            }
+                        }
+                        // positions past the chunk's end hold +0.0 on both sides
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            cnt[hh] += __float_as_uint(p[i]) != 0u ? 1u : 0u;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < 16; ++hh) {
+            const unsigned wc = __reduce_add_sync(kFull, cnt[hh]);
+            if (lane == 0 && hh < nh)
+                s_cnt[warp][hh] += wc;
+        }
+    } else
     for (long long w0 = ((long long)sub * kCountWarps + warp) * kTile; w0 < len; w0 += wstride) {
         const long long e = w0 + 8 * lane; // chunk-relative first element of this lane
         const int valid = (int)min(max(len - e, 0LL), 8LL);
@@ -180,10 +240,13 @@ __global__ void __launch_bounds__(kCountThreads, 3)
     }
 }
 
-template <int IN_KIND> const void *count_fn(bool vec)
+template <int IN_KIND> const void *count_fn(bool vec, bool nh16)
 {
-    return vec ? (const void *)sparse_chunk_count_kernel<IN_KIND, true>
-               : (const void *)sparse_chunk_count_kernel<IN_KIND, false>;
+    if (nh16)
+        return vec ? (const void *)sparse_chunk_count_kernel<IN_KIND, true, true>
+                   : (const void *)sparse_chunk_count_kernel<IN_KIND, false, true>;
+    return vec ? (const void *)sparse_chunk_count_kernel<IN_KIND, true, false>
+               : (const void *)sparse_chunk_count_kernel<IN_KIND, false, false>;
 }
 
 } // namespace
@@ -194,16 +257,17 @@ cudaError_t launch_sparse_chunk_count(const SpCountArgs &args, int in_kind, bool
                                       cudaStream_t st)
 {
     const void *fn = nullptr;
+    const bool nh16 = args.h_hi - args.h_lo + 1 <= 16;
     switch (in_kind) {
-    case kF32: fn = count_fn<kF32>(vec); break;
-    case kF16: fn = count_fn<kF16>(vec); break;
-    case kBF16: fn = count_fn<kBF16>(vec); break;
-    case kF32Diff: fn = count_fn<kF32Diff>(vec); break;
+    case kF32: fn = count_fn<kF32>(vec, nh16); break;
+    case kF16: fn = count_fn<kF16>(vec, nh16); break;
+    case kBF16: fn = count_fn<kBF16>(vec, nh16); break;
+    case kF32Diff: fn = count_fn<kF32Diff>(vec, nh16); break;
     default: return cudaErrorInvalidValue;
     }
     // resident blocks per SM of each variant, asked once
-    static int occ_cache[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    int &occ = occ_cache[in_kind * 2 + (vec ? 1 : 0)];
+    static int occ_cache[16] = {};
+    int &occ = occ_cache[in_kind * 4 + (vec ? 2 : 0) + (nh16 ? 1 : 0)];
     if (occ < 1 &&
         (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kCountThreads, 0) != cudaSuccess ||
          occ < 1))
