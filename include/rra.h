@@ -335,11 +335,10 @@ rra_status rra_bfp_decode(const int8_t *exps, const uint8_t *mants, size_t n, in
  * passes: a count per 1024-element chunk, an exclusive scan of the counts,
  * and an emit pass that writes each chunk's nonzeros at its offset (or copies
  * x when the message is dense; idx is then left as it was).
- * Uses scratch (one uint32 per 1024 elements, one per 4096 chunks, and a
- * ticket word) from a workspace per device and stream that the library
- * allocates with cudaMalloc and clears on the first call that needs more
- * than it holds (so that first call must not be made during stream
- * capture).  Encodes on different streams may overlap: each stream
+ * Uses scratch (one uint32 per 1024 elements, one per 4096 chunks) from a
+ * workspace per device and stream that the library allocates with
+ * cudaMalloc on the first call that needs more than it holds (so that first
+ * call must not be made during stream capture).  Encodes on different streams may overlap: each stream
  * has its own workspace.  Errors: RRA_ERR_INVALID, RRA_ERR_NOMEM,
  * RRA_ERR_CUDA.
  */
@@ -365,16 +364,15 @@ rra_status rra_sparse_encode(const void *x, size_t n, rra_dtype dtype, float thr
  *  - n may not exceed RRA_NOALLOC_MAX_COUNT (2^28 elements); larger n returns
  *    RRA_ERR_INVALID without doing anything (use rra_sparse_encode then).
  *  - the first call on a device looks up the scratch array's device address
- *    (cudaGetSymbolAddress) with that device current, keeps it for the rest
- *    of the process, and clears the array on the call's stream (one ticket
- *    word of the scan must start at zero); after cudaDeviceReset the
- *    function must not be called again.  Make the first call on each device
- *    before starting any stream capture.
- *  - all calls on a device share the one scratch array.  Each call writes
- *    every count it reads before reading it and leaves the ticket at zero
- *    again, so no clearing is needed between calls; calls that overlap on
- *    the GPU (different streams without ordering between them) race on the
- *    scratch and give undefined results.
+ *    (cudaGetSymbolAddress) with that device current, and keeps it for the
+ *    rest of the process; after cudaDeviceReset the function must not be
+ *    called again.  Make the first call on each device before starting any
+ *    stream capture.
+ *  - all calls on a device share the one scratch array.  A call writes
+ *    every scratch word it reads before reading it, so nothing needs
+ *    clearing, before the first call or between calls; calls that overlap
+ *    on the GPU (different streams without ordering between them) race on
+ *    the scratch and give undefined results for those calls.
  */
 rra_status rra_sparse_encode_noalloc(const void *x, size_t n, rra_dtype dtype, float threshold,
                                      uint32_t *hdr, void *vals, int32_t *idx, void *stream);

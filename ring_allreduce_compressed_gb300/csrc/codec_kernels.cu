@@ -179,9 +179,9 @@ __global__ void __launch_bounds__(kThreads) bfp_decode_kernel(const int8_t *__re
 // Three passes over chunks of 1024 elements ([cccl] §2.1's values +
 // indices), each chunk handled by one warp, no block-wide step anywhere:
 //   count  the nonzeros of every chunk;
-//   scan   their exclusive prefix (segments of 4096 chunks; the last
-//          segment to finish scans the segments' totals, whose sum decides
-//          the format and goes into the header);
+//   scan   their exclusive prefix (segments of 4096 chunks, then the
+//          segments' own prefix, whose total decides the format and goes
+//          into the header);
 //   emit   every chunk's nonzero values and indices at its offset, or, for
 //          a dense message, a bit copy of x.
 // Lane L holds the chunk's 16-byte words L, 32 + L, 64 + L, ... (8 16-bit
@@ -301,45 +301,43 @@ __global__ void __launch_bounds__(kThreads) sparse_count_kernel(const void *__re
     }
 }
 
-// Pass 2: exclusive prefix of the chunk counts, in place, in segments of
+// Pass 2a: exclusive prefix of the chunk counts, in place, in segments of
 // kSegChunks chunks: block s scans segment s (every thread four consecutive
 // counts; warp shuffles; one shared-memory pass over the warp totals) and
-// writes the segment's total to seg[s].  The block that finishes last (a
-// ticket) turns the segment totals into their exclusive prefix, in place,
-// writes the header -- the total nnz and the format, sparse iff nnz < lim --
-// and resets the ticket for the next call.
-__global__ void __launch_bounds__(kScanThreads) sparse_scan_kernel(uint32_t *counts,
-                                                                   long long chunks,
-                                                                   uint32_t *seg,
-                                                                   uint32_t *ticket, double lim,
-                                                                   uint32_t *hdr)
+// writes the segment's total to seg[s].
+// Pass 2b (one block): the segments' exclusive prefix, in place, and the
+// header: the total nnz and the format (sparse iff nnz < lim).
+// Inclusive scan of v over a block of kScanThreads threads; *all: the total.
+__device__ __forceinline__ uint32_t scan_block(uint32_t v, uint32_t *wsum, uint32_t *all)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o)
+            incl += t;
+    }
+    if (lane == 31)
+        wsum[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kScanThreads / 32; ++w) {
+        const uint32_t y = wsum[w];
+        before += w < warp ? y : 0u;
+        tot += y;
+    }
+    __syncthreads(); // (wsum is reused by the next scan)
+    *all = tot;
+    return before + incl;
+}
+
+__global__ void __launch_bounds__(kScanThreads) sparse_segscan_kernel(uint32_t *counts,
+                                                                      long long chunks,
+                                                                      uint32_t *seg)
 {
     __shared__ uint32_t wsum[kScanThreads / 32];
-    __shared__ bool s_last;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // inclusive scan of v over the block; *all: the block's total
-    auto block_scan = [&](uint32_t v, uint32_t *all) {
-        uint32_t incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o)
-                incl += t;
-        }
-        if (lane == 31)
-            wsum[warp] = incl;
-        __syncthreads();
-        uint32_t before = 0, tot = 0;
-#pragma unroll
-        for (int w = 0; w < kScanThreads / 32; ++w) {
-            const uint32_t y = wsum[w];
-            before += w < warp ? y : 0u;
-            tot += y;
-        }
-        __syncthreads(); // (wsum is reused by the next scan)
-        *all = tot;
-        return before + incl;
-    };
     const long long t0 = (long long)blockIdx.x * kSegChunks + 4LL * threadIdx.x;
     uint32_t v[4];
 #pragma unroll
@@ -347,29 +345,27 @@ __global__ void __launch_bounds__(kScanThreads) sparse_scan_kernel(uint32_t *cou
         v[j] = t0 + j < chunks ? counts[t0 + j] : 0u;
     const uint32_t s = v[0] + v[1] + v[2] + v[3];
     uint32_t total;
-    uint32_t run = block_scan(s, &total) - s;
+    uint32_t run = scan_block(s, wsum, &total) - s;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
         if (t0 + j < chunks) {
             counts[t0 + j] = run;
             run += v[j];
         }
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0)
         seg[blockIdx.x] = total;
-        __threadfence();
-        s_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!s_last)
-        return;
-    __threadfence();
-    const long long nseg = gridDim.x;
+}
+
+__global__ void __launch_bounds__(kScanThreads) sparse_segbase_kernel(uint32_t *seg, long long nseg,
+                                                                      double lim, uint32_t *hdr)
+{
+    __shared__ uint32_t wsum[kScanThreads / 32];
     uint32_t carry = 0;
     for (long long b0 = 0; b0 < nseg; b0 += kScanThreads) {
         const long long i = b0 + threadIdx.x;
-        const uint32_t y = i < nseg ? __ldcg(seg + i) : 0u;
+        const uint32_t y = i < nseg ? seg[i] : 0u;
         uint32_t all;
-        const uint32_t incl = block_scan(y, &all);
+        const uint32_t incl = scan_block(y, wsum, &all);
         if (i < nseg)
             seg[i] = carry + incl - y;
         carry += all;
@@ -377,7 +373,6 @@ __global__ void __launch_bounds__(kScanThreads) sparse_scan_kernel(uint32_t *cou
     if (threadIdx.x == 0) {
         hdr[0] = (double)carry < lim ? 1u : 0u;
         hdr[1] = carry;
-        *ticket = 0u;
     }
 }
 
@@ -875,15 +870,13 @@ cudaError_t launch_bfp_decode(const int8_t *exps, const uint8_t *mants, long lon
     return cudaGetLastError();
 }
 
-// Scratch: the scan's ticket (word 0, at a fixed place whatever n is: it
-// must read zero when every call starts; the scan's last block resets it),
-// from word 8 one count (then offset) per 1024-element chunk, then one total
-// (then base) per segment of 4096 chunks.
-constexpr long long kSpHeadWords = 8;
+// Scratch: one count (then offset) per 1024-element chunk, then one total
+// (then base) per segment of 4096 chunks.  Every word is written by a call
+// before that call reads it: nothing needs clearing, before or between calls.
 long long sparse_encode_scratch_words(long long n)
 {
     const long long chunks = (n + kSpChunk - 1) / kSpChunk;
-    return kSpHeadWords + chunks + (chunks + kSegChunks - 1) / kSegChunks;
+    return chunks + (chunks + kSegChunks - 1) / kSegChunks;
 }
 
 // Resident blocks per SM of a kernel, asked once per kernel.
@@ -903,8 +896,7 @@ cudaError_t launch_sparse_encode(const void *x, long long n, int dtype, double o
 {
     const long long chunks = (n + kSpChunk - 1) / kSpChunk;
     const long long nseg = (chunks + kSegChunks - 1) / kSegChunks;
-    uint32_t *ticket = scratch;
-    uint32_t *counts = scratch + kSpHeadWords;
+    uint32_t *counts = scratch;
     uint32_t *seg = counts + chunks;
     const double lim = one_minus_thr * (double)n; // sparse iff nnz < lim
     const int vec = aligned16(x) && aligned16(vals) ? 1 : 0;
@@ -920,8 +912,8 @@ cudaError_t launch_sparse_encode(const void *x, long long n, int dtype, double o
         const int eg = (int)std::max(1LL, std::min(wblocks, (long long)num_sms() *             \
                                                      blocks_per_sm(sparse_emit_kernel<T>)));   \
         sparse_count_kernel<T><<<cg, kThreads, 0, st>>>(x, n, chunks, counts, vec);            \
-        sparse_scan_kernel<<<(unsigned)nseg, kScanThreads, 0, st>>>(counts, chunks, seg,       \
-                                                                   ticket, lim, hdr);          \
+        sparse_segscan_kernel<<<(unsigned)nseg, kScanThreads, 0, st>>>(counts, chunks, seg);   \
+        sparse_segbase_kernel<<<1, kScanThreads, 0, st>>>(seg, nseg, lim, hdr);                \
         sparse_emit_kernel<T><<<eg, kThreads, 0, st>>>(x, n, chunks, counts, seg, hdr, vals,   \
                                                        idx, vec, quads);                       \
     } while (0)

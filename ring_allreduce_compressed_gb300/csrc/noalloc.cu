@@ -21,10 +21,10 @@
 
 namespace {
 
-// eight words (the scan's ticket), one word per 1024-element chunk of the
-// largest input, then one per 4096 chunks
+// one word per 1024-element chunk of the largest input, then one per 4096
+// chunks
 constexpr long long kNoallocChunks = (long long)RRA_NOALLOC_MAX_COUNT / 1024;
-constexpr long long kNoallocScratchWords = 8 + kNoallocChunks + (kNoallocChunks + 4095) / 4096;
+constexpr long long kNoallocScratchWords = kNoallocChunks + (kNoallocChunks + 4095) / 4096;
 
 // The scratch itself.  In host code this name is only a host-side stand-in,
 // not a device address: the address a kernel may use comes from
@@ -36,12 +36,10 @@ std::mutex g_mu;
 uint32_t *g_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up once
-// per device, on the first call with that device current; that call also
-// clears the array on its stream (the scan's ticket word must start at zero;
-// the encoder resets it after every call).  The address stays valid for the
-// life of the device's primary context; after a cudaDeviceReset the entry
-// point must not be called again in this process.
-cudaError_t scratch_for_current_device(uint32_t **out, cudaStream_t st)
+// per device, on the first call with that device current.  The address
+// stays valid for the life of the device's primary context; after a
+// cudaDeviceReset the entry point must not be called again in this process.
+cudaError_t scratch_for_current_device(uint32_t **out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -53,9 +51,6 @@ cudaError_t scratch_for_current_device(uint32_t **out, cudaStream_t st)
     if (!g_ptr[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess)
-            return e;
-        e = cudaMemsetAsync(p, 0, sizeof(g_noalloc_scratch), st);
         if (e != cudaSuccess)
             return e;
         g_ptr[dev] = static_cast<uint32_t *>(p);
@@ -78,12 +73,10 @@ extern "C" rra_status rra_sparse_encode_noalloc(const void *x, size_t n, rra_dty
         rra::sparse_encode_scratch_words((long long)n) > kNoallocScratchWords)
         return RRA_ERR_INVALID; // beyond the fixed scratch: use rra_sparse_encode
     uint32_t *scratch = nullptr;
-    if (scratch_for_current_device(&scratch, reinterpret_cast<cudaStream_t>(stream)) !=
-        cudaSuccess)
+    if (scratch_for_current_device(&scratch) != cudaSuccess)
         return RRA_ERR_CUDA;
     // every count and segment word is written in a call before that call
-    // reads it, and the scan's ticket is back at zero when a call ends, so
-    // nothing needs clearing between calls
+    // reads it, so nothing needs clearing, before or between calls
     return rra::launch_sparse_encode(x, (long long)n, dtype, 1.0 - (double)threshold, hdr, vals,
                                      idx, scratch,
                                      reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess

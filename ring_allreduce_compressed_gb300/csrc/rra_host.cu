@@ -825,12 +825,6 @@ rra_status rra_sparse_encode(const void *x, size_t n, rra_dtype dtype, float thr
             ws.first = nullptr;
             return RRA_ERR_NOMEM;
         }
-        // the encoder's ticket word starts at zero (the encoder resets it)
-        if (cudaMemsetAsync(ws.first, 0, (size_t)want * sizeof(uint32_t), st) != cudaSuccess) {
-            cudaFree(ws.first);
-            ws.first = nullptr;
-            return RRA_ERR_CUDA;
-        }
         ws.second = want;
     }
     return launch_sparse_encode(x, (long long)n, dtype, 1.0 - (double)threshold, hdr, vals, idx,

@@ -202,8 +202,7 @@ cudaError_t launch_bfp_encode(const void *x, long long n, int dtype, int bits, i
 cudaError_t launch_bfp_decode(const int8_t *exps, const uint8_t *mants, long long n, int bits,
                               float *out, int accumulate, cudaStream_t st);
 // The standalone sparse encoder.  scratch: sparse_encode_scratch_words(n)
-// 32-bit words; its first word must be zero when a call starts (it is zero
-// again when the call ends), the rest needs no clearing.
+// 32-bit words, needing no clearing (a call writes every word it reads).
 cudaError_t launch_sparse_encode(const void *x, long long n, int dtype, double one_minus_thr,
                                  uint32_t *hdr, void *vals, int32_t *idx, uint32_t *scratch,
                                  cudaStream_t st);
