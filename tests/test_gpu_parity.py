@@ -368,6 +368,27 @@ def test_sparse_ring_per_chunk_launch_shapes(G, K, N):
     compare((outs, sent, recv), oracle_ring(xs, "bf16", "f32", codec="sparse"), f"G={G} K={K}")
 
 
+@pytest.mark.parametrize("N", [17, 20, 33])
+@pytest.mark.parametrize("kind", ["bf16", "diff"])
+def test_sparse_ring_per_chunk_many_ranks(N, kind):
+    """More than 16 ranks: warps play several ranks each, and the count pass
+    takes its path for more than 16 hops (per-position warp sums); with a
+    diff stream the counts are of the fp32 differences."""
+    T = N * 2048 + 3 * N + 1
+    if kind == "bf16":
+        xs = _sparse_with_minus_zero(N, T, 80 + N, "bf16", p_zero=0.7)
+        compare(run_ring(xs, "f32", rra.Codec("sparse")),
+                oracle_ring(xs, "bf16", "f32", codec="sparse"), f"N={N}")
+    else:
+        cur, prev = W.diloco(N, T, seed=N)
+        for q in range(N):  # unchanged positions: zero differences
+            cur[q][: T // 2] = prev[q][: T // 2]
+        codec = rra.Codec("sparse", diff_prev=prev, average=True)
+        ref = O.ring([host(c) for c in cur], codec="sparse", diff_prev=[host(p) for p in prev],
+                     average=True)
+        compare(run_ring(cur, "f32", codec), ref, f"diff N={N}")
+
+
 def test_sparse_ring_per_chunk_generic_path_and_in_place():
     """Buffers off the 16-byte grid take the generic path (bounds-checked
     loads, the count pass's scalar loads); in place, out = in."""
