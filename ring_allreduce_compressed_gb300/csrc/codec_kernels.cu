@@ -419,11 +419,14 @@ __global__ void __launch_bounds__(kThreads, 4) sparse_emit_kernel(
     uint32_t *wsd = swd[warp];
     uint16_t *wsi = sidx[W16 ? 0 : warp];
     const long long warps = (long long)gridDim.x * kWarps;
-    long long c = blockIdx.x * (long long)kWarps + warp;
+    // chunks are taken from the last one down: the count pass streamed x from
+    // the first chunk up, so the chunks it read last may still be in L2
+    long long i = blockIdx.x * (long long)kWarps + warp;
     uint4 q[W];
-    if (c < chunks)
-        load_chunk<IN_T>(x, n, c, lane, vec, q);
-    for (; c < chunks; c += warps) {
+    if (i < chunks)
+        load_chunk<IN_T>(x, n, chunks - 1 - i, lane, vec, q);
+    for (; i < chunks; i += warps) {
+        const long long c = chunks - 1 - i;
         const uint32_t ob = offs[c] + segbase[c / kSegChunks]; // the run's first output position
         const uint32_t sh = ob & 3u;
         // this lane's masks (word j at bits j*EPW..) and slots
@@ -470,8 +473,8 @@ __global__ void __launch_bounds__(kThreads, 4) sparse_emit_kernel(
                 }
         }
         __syncwarp();
-        if (c + warps < chunks)
-            load_chunk<IN_T>(x, n, c + warps, lane, vec, q);
+        if (i + warps < chunks)
+            load_chunk<IN_T>(x, n, chunks - 1 - (i + warps), lane, vec, q);
         // the run in 4-aligned groups; group g covers output positions
         // (ob & ~3) + 4g .., staged at positions 4g ..
         const int32_t t0 = (int32_t)(c * kSpChunk);
