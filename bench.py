@@ -717,10 +717,10 @@ def run_reference(args, world, rank):
 # ---------------------------------------------------------------- ring vs tree sweep
 
 def run_codecs(args, world, rank):
-    """The standalone codec entry points on 2^28 elements, each timed with CUDA
-    events (median of 10 after 3 warm-ups) against its compulsory bytes: the
-    input read once and the output written once (the sparse encoder reads its
-    input twice: a count pass and an emit pass)."""
+    """The standalone codec entry points on 2^28 elements, each timed on the
+    device (time_op: 10 calls in a CUDA graph after 3 warm-ups) against its
+    compulsory bytes: the input read once and the output written once (the
+    sparse encoder reads its input twice: a count pass and an emit pass)."""
     import ring_allreduce_compressed_gb300 as rra
     rra.build()
     if rank != 0:
@@ -765,20 +765,8 @@ def run_codecs(args, world, rank):
     ]
     out = []
     for name, fn, nbytes in cases:
-        for _ in range(args.op_warmup):
-            fn()
-        torch.cuda.synchronize()
-        times = []
-        for _ in range(args.op_reps):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            b.synchronize()
-            times.append(a.elapsed_time(b) * 1e3)
-        us = statistics.median(times)
-        line = {"codec_bench": True, "op": name, "n": n, "us": us, "bytes": nbytes,
+        us, how = time_op(fn, args.op_warmup, args.op_reps)
+        line = {"codec_bench": True, "op": name, "n": n, "us": us, "timing": how, "bytes": nbytes,
                 "gbs": nbytes / (us * 1e-6) / 1e9,
                 "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peak, "peak_source": peak_src,
                 "sparse_format": "sparse" if fmt else "dense", "nnz": nnz}
@@ -790,13 +778,55 @@ def run_codecs(args, world, rank):
                 f.write(json.dumps(line) + "\n")
 
 
+def time_op(fn, warmup: int, reps: int):
+    """Device time of one call of fn in microseconds, and how it was taken:
+    the reps calls captured back to back in a CUDA graph on a side stream
+    (after the warm-up calls on that stream), the graph replayed once as its
+    own warm-up and once timed; ops that cannot be captured (a synchronous
+    read-back) are timed call by call with CUDA events (median)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            fn()
+    torch.cuda.synchronize()
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(reps):
+                    fn()
+        g.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b) * 1e3 / reps, "CUDA graph of the timed calls"
+    except RuntimeError:
+        torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b) * 1e3)
+    return statistics.median(times), "CUDA events per call (median)"
+
+
 def run_kernels(args, world, rank):
     """One op per library kernel that the ring workloads do not cover -- the
     plain allgather, broadcast and tree allreduce, and the codec statistics --
     on N=8 ranks of --kernels-T fp32 elements (default 16 Mi: 512 MB in all,
     above the 129 MB L2), each called --op-warmup times untimed and then
-    --op-reps times, timed with CUDA events (median), against its algorithmic
-    bytes.  Also the command the ncu summaries of these kernels are captured
+    --op-reps times, timed by time_op (a CUDA graph of the calls; the codec
+    statistics, which read their counts back to the host, call by call), against
+    its algorithmic bytes.  Also the command the ncu summaries of these kernels are captured
     from."""
     import ring_allreduce_compressed_gb300 as rra
     rra.build()
@@ -818,21 +848,9 @@ def run_kernels(args, world, rank):
         ("codec_stats_kernel", lambda: comm.codec_stats(bufs), 4 * N * T),
     ]
     for name, fn, nbytes in cases:
-        for _ in range(args.op_warmup):
-            fn()
-        torch.cuda.synchronize()
-        times = []
-        for _ in range(args.op_reps):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            b.synchronize()
-            times.append(a.elapsed_time(b) * 1e3)
+        us, how = time_op(fn, args.op_warmup, args.op_reps)
         assert comm.status() == rra.RRA_OK
-        us = statistics.median(times)
-        line = {"kernel_bench": True, "kernel": name, "N": N, "T": T, "us": us,
+        line = {"kernel_bench": True, "kernel": name, "N": N, "T": T, "us": us, "timing": how,
                 "bytes": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9,
                 "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peak, "peak_source": peak_src}
         print(json.dumps(line), flush=True)
