@@ -615,6 +615,9 @@ def run_rra(args, world, rank, local):
                             "results come down",
                "result_matches_device_run": ok}
 
+    others = None
+    if args.config == CONFIG_NAMES[0] and args.scale == 1 and not args.ef and args.other_configs:
+        others = run_other_configs(world, local, args.other_configs)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, budget_s=args.cpu_budget)
@@ -652,6 +655,7 @@ def run_rra(args, world, rank, local):
         "latency": latency,
         "eager": eager,
         "gpu_launches": K * wl.launches_per_step,
+        "other_configs": others,
         "clocks": clk,
         "status": rra.status_string(status),
     }
@@ -660,6 +664,63 @@ def run_rra(args, world, rank, local):
         if args.jsonl:
             with open(args.jsonl, "a") as f:
                 f.write(json.dumps(line) + "\n")
+
+
+def run_other_configs(world: int, local: int, seconds: float):
+    """Every other workload of the metric, each timed like the headline line:
+    3 untimed steps, then K back-to-back steps as one CUDA graph (K for about
+    `seconds` of timed work), one untimed replay and one timed replay, with
+    the GPU's clocks sampled over the timed replays.  The workloads are built
+    and freed one at a time (the DiLoCo one holds about 100 GB)."""
+    import ring_allreduce_compressed_gb300 as rra
+    peak, _ = hbm_peak()
+    res = {}
+    for name in CONFIG_NAMES[1:]:
+        wl = Workload(name)
+        stream = torch.cuda.current_stream()
+        for _ in range(3):
+            wl.step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(3):
+            wl.step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_step = max_over_ranks(world, e0.elapsed_time(e1) / 3) * 1e-3
+        K = int(max(10, min(2000, round(seconds / max(t_step, 1e-7)))))
+        graph = torch.cuda.CUDAGraph()
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            with torch.cuda.graph(graph, stream=gs):
+                for _ in range(K):
+                    wl.step()
+        stream.wait_stream(gs)
+        graph.replay()
+        torch.cuda.synchronize()
+        clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+        time.sleep(0.15)
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        clk = clocks.stop()
+        ms = max_over_ranks(world, a.elapsed_time(b) / K)
+        status = wl.comm.status()
+        res[name] = {
+            "workload": wl.desc, "N": wl.N, "T": wl.T, "codec": wl.codec_name,
+            "value": whole_job_gbs(world, wl.payload, ms), "unit": "GB/s",
+            "ms_per_step": ms, "steps": K, "kernels": KERNEL_OF.get(name, wl.kernels),
+            "bytes_per_step": wl.alg_bytes,
+            "frac": wl.alg_bytes / (ms * 1e-3) / 1e9 / peak,
+            "frac_compulsory": wl.compulsory / (ms * 1e-3) / 1e9 / peak,
+            "l2": wl.l2_note(), "clocks": clk, "status": rra.status_string(status)}
+        del graph, wl
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_reference(args, world, rank):
@@ -1036,6 +1097,9 @@ def main():
                          "ncu captures, reported with its own T (not the metric's workload)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--other-configs", type=float, default=0.3, metavar="SECONDS",
+                    help="the default line also times every other workload for about this "
+                         "many seconds each (0: skip)")
     ap.add_argument("--kernels", action="store_true",
                     help="one timed call of each collective kernel the workloads do not "
                          "cover (plain allgather, broadcast, tree; codec statistics)")

@@ -241,20 +241,46 @@ template <int IN_T> __device__ __forceinline__ uint32_t word_count(const uint4 &
                (q.w != 0u ? 1u : 0u);
 }
 
+// The count pass reads x once more than the output needs.  It keeps its
+// last 64 MB of x (half the 129 MB L2) with the evict-last priority, and the
+// emit pass, which takes the chunks from the last one down, reads them from
+// L2 first; every other read of x is a streaming (evict-first) load.
+constexpr long long kKeepBytes = 64ll << 20;
+
+// One 16-byte global load with the L2 evict-last policy.
+__device__ __forceinline__ uint4 ld_keep(const uint4 *p)
+{
+    uint64_t pol;
+    uint4 r;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p), "l"(pol));
+    return r;
+}
+
 // This lane's words of chunk c (zero past n): one 16-byte load each when the
-// chunk is whole and x aligned, else element loads.
+// chunk is whole and x aligned (kept in L2 with keep set), else element
+// loads.
 template <int IN_T>
 __device__ __forceinline__ void load_chunk(const void *x, long long n, long long c, int lane,
-                                           int vec, uint4 (&q)[SpChunk<IN_T>::words])
+                                           int vec, uint4 (&q)[SpChunk<IN_T>::words],
+                                           bool keep = false)
 {
     constexpr int es = SpChunk<IN_T>::es, EPW = SpChunk<IN_T>::epw, W = SpChunk<IN_T>::words;
     const long long base = c * kSpChunk;
     if (vec && base + kSpChunk <= n) {
         const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(x) +
                                                            base * es);
+        if (keep) {
 #pragma unroll
-        for (int j = 0; j < W; ++j)
-            q[j] = __ldcs(src + 32 * j + lane);
+            for (int j = 0; j < W; ++j)
+                q[j] = ld_keep(src + 32 * j + lane);
+        } else {
+#pragma unroll
+            for (int j = 0; j < W; ++j)
+                q[j] = __ldcs(src + 32 * j + lane);
+        }
     } else {
 #pragma unroll
         for (int j = 0; j < W; ++j) {
@@ -274,7 +300,8 @@ __device__ __forceinline__ void load_chunk(const void *x, long long n, long long
 }
 
 // Pass 1: counts[c] = nonzeros of chunk c.  Warps stride over the chunks;
-// the next chunk's words are loaded before this one is counted.
+// the next chunk's words are loaded before this one is counted.  The chunks
+// of the last kKeepBytes of x stay in L2 for the emit pass.
 template <int IN_T>
 __global__ void __launch_bounds__(kThreads) sparse_count_kernel(const void *__restrict__ x,
                                                                 long long n, long long chunks,
@@ -285,16 +312,17 @@ __global__ void __launch_bounds__(kThreads) sparse_count_kernel(const void *__re
     const int lane = threadIdx.x & 31;
     const long long warps = (long long)gridDim.x * (kThreads / 32);
     long long c = blockIdx.x * (long long)(kThreads / 32) + (threadIdx.x >> 5);
+    const long long keep_from = chunks - kKeepBytes / (kSpChunk * SpChunk<IN_T>::es);
     uint4 q[W];
     if (c < chunks)
-        load_chunk<IN_T>(x, n, c, lane, vec, q);
+        load_chunk<IN_T>(x, n, c, lane, vec, q, c >= keep_from);
     for (; c < chunks; c += warps) {
         uint32_t k = 0;
 #pragma unroll
         for (int j = 0; j < W; ++j)
             k += word_count<IN_T>(q[j]);
         if (c + warps < chunks)
-            load_chunk<IN_T>(x, n, c + warps, lane, vec, q);
+            load_chunk<IN_T>(x, n, c + warps, lane, vec, q, c + warps >= keep_from);
         k = __reduce_add_sync(kFull, k);
         if (lane == 0)
             counts[c] = k;
@@ -419,8 +447,8 @@ __global__ void __launch_bounds__(kThreads, 4) sparse_emit_kernel(
     uint32_t *wsd = swd[warp];
     uint16_t *wsi = sidx[W16 ? 0 : warp];
     const long long warps = (long long)gridDim.x * kWarps;
-    // chunks are taken from the last one down: the count pass streamed x from
-    // the first chunk up, so the chunks it read last may still be in L2
+    // chunks are taken from the last one down: the count pass kept its last
+    // kKeepBytes of x in L2, and these loads (evict-first) are their last use
     long long i = blockIdx.x * (long long)kWarps + warp;
     uint4 q[W];
     if (i < chunks)
