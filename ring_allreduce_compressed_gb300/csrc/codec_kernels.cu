@@ -553,17 +553,13 @@ __global__ void __launch_bounds__(kThreads, 4) sparse_emit_kernel(
 
 // ---------------------------------------------------------------- sparse decode
 constexpr int kSpTile = 4096; // elements per decoder tile
-// Dense message: a streaming copy (or add) of the values into acc.
+// Dense message: a streaming copy (or add) of the values into acc, the
+// whole grid striding over groups of 8 elements.
 template <int IN_T>
-__global__ void __launch_bounds__(kThreads) sparse_dense_kernel(const uint32_t *__restrict__ hdr,
-                                                                const void *__restrict__ vals,
-                                                                long long n, float *__restrict__ acc,
-                                                                int accumulate, int vec)
+__device__ __forceinline__ void dense_restore(const void *vals, long long n, float *acc,
+                                              int accumulate, int vec)
 {
     constexpr int es = dtype_size(IN_T);
-    const bool sparse = hdr[0] != 0u;
-    if (sparse) // sparse_fill_kernel or sparse_scatter_kernel restores it
-        return;
     const long long groups = (n + 7) / 8;
     for (long long gi = blockIdx.x * (long long)kThreads + threadIdx.x; gi < groups;
          gi += (long long)gridDim.x * kThreads) {
@@ -589,18 +585,37 @@ __global__ void __launch_bounds__(kThreads) sparse_dense_kernel(const uint32_t *
     }
 }
 
-// Sparse message, accumulate == 0: one pass over acc in 4096-element tiles.
-// First the position in the (ascending) index list where each tile starts,
-// one binary search per tile; then every tile is built in shared memory
-// (+0.0, then its values, read with consecutive threads) and written once.
-// An index outside its tile (out of order, or outside [0, n)) is never
-// written.
-__global__ void __launch_bounds__(kThreads) sparse_tile_starts_kernel(
-    const uint32_t *__restrict__ hdr, const int32_t *__restrict__ idx, long long n,
-    uint32_t *__restrict__ start, int accumulate)
+// accumulate == 1: a dense message is added by the whole grid; a sparse one
+// is left to sparse_scatter_kernel.
+template <int IN_T>
+__global__ void __launch_bounds__(kThreads) sparse_dense_kernel(const uint32_t *__restrict__ hdr,
+                                                                const void *__restrict__ vals,
+                                                                long long n, float *__restrict__ acc,
+                                                                int vec)
 {
-    if (hdr[0] == 0u || accumulate)
+    if (hdr[0] != 0u)
         return;
+    dense_restore<IN_T>(vals, n, acc, 1, vec);
+}
+
+// accumulate == 0, in one pass over acc in 4096-element tiles.  This kernel:
+// a dense message is copied by the whole grid; for a sparse one, the
+// position in the (ascending) index list where each tile starts, one binary
+// search per tile and thread.  Then sparse_fill_kernel builds every tile of
+// a sparse message in shared memory (+0.0, then its values, read with
+// consecutive threads) and writes it once.  An index outside its tile (out
+// of order, or outside [0, n)) is never written.
+template <int IN_T>
+__global__ void __launch_bounds__(kThreads) sparse_prep_kernel(const uint32_t *__restrict__ hdr,
+                                                               const void *__restrict__ vals,
+                                                               const int32_t *__restrict__ idx,
+                                                               long long n, float *__restrict__ acc,
+                                                               uint32_t *__restrict__ start, int vec)
+{
+    if (hdr[0] == 0u) {
+        dense_restore<IN_T>(vals, n, acc, 0, vec);
+        return;
+    }
     const long long nnz = min((long long)hdr[1], n); // a header never lists more than n
     const long long tiles = (n + kSpTile - 1) / kSpTile;
     for (long long t = blockIdx.x * (long long)kThreads + threadIdx.x; t <= tiles;
@@ -631,12 +646,11 @@ __global__ void __launch_bounds__(kThreads) sparse_fill_kernel(const uint32_t *_
                                                                const void *__restrict__ vals,
                                                                const int32_t *__restrict__ idx,
                                                                const uint32_t *__restrict__ start,
-                                                               long long n, float *acc,
-                                                               int accumulate, int vec)
+                                                               long long n, float *acc, int vec)
 {
     using E = typename Elem<IN_T>::type;
     __shared__ __align__(16) float tile[kSpTile];
-    if (hdr[0] == 0u || accumulate)
+    if (hdr[0] == 0u)
         return;
     const long long tiles = (n + kSpTile - 1) / kSpTile;
     // The tile's listed (index, value) pairs k = kb + tid + kThreads*j are read
@@ -695,16 +709,16 @@ __global__ void __launch_bounds__(kThreads) sparse_fill_kernel(const uint32_t *_
     }
 }
 
-// Sparse message, accumulate != 0: acc[i] += v at the listed positions.
+// accumulate == 1, sparse message: acc[i] += v at the listed positions
+// (a dense one is added by sparse_dense_kernel).
 template <int IN_T>
 __global__ void __launch_bounds__(kThreads) sparse_scatter_kernel(const uint32_t *__restrict__ hdr,
                                                                   const void *__restrict__ vals,
                                                                   const int32_t *__restrict__ idx,
-                                                                  long long n, float *acc,
-                                                                  int accumulate)
+                                                                  long long n, float *acc)
 {
     using E = typename Elem<IN_T>::type;
-    if (hdr[0] == 0u || !accumulate)
+    if (hdr[0] == 0u)
         return;
     const long long nnz = min((long long)hdr[1], n); // a header never lists more than n
     for (long long k = blockIdx.x * (long long)kThreads + threadIdx.x; k < nnz;
@@ -713,7 +727,7 @@ __global__ void __launch_bounds__(kThreads) sparse_scatter_kernel(const uint32_t
         if (i < 0 || i >= n)
             continue; // malformed index: skip rather than write out of bounds
         const float v = to_f32(reinterpret_cast<const E *>(vals)[k]);
-        acc[i] = accumulate ? __fadd_rn(acc[i], v) : v;
+        acc[i] = __fadd_rn(acc[i], v);
     }
 }
 
@@ -990,18 +1004,22 @@ cudaError_t launch_sparse_decode(const uint32_t *hdr, const void *vals, const in
     }
     uint32_t *const scratch = ws.first;
     const int vec = aligned16(vals) && aligned16(acc) ? 1 : 0;
+    // the dense stream's grid; its threads also cover the tiles + 1 starts
+    const long long tiles = (n + kSpTile - 1) / kSpTile;
     const int g1 = grid_for((n + 7) / 8, kThreads);
     const int g2 = num_sms() * 4;
-    const long long tiles = (n + kSpTile - 1) / kSpTile;
-    const int gs = (int)std::min<long long>((tiles + 1 + kThreads - 1) / kThreads, 65535);
     const int gf = (int)std::min<long long>(tiles, (long long)num_sms() * 8);
+    // the format is in the device header, so each path launches both of its
+    // kernels and the one that does not apply returns at once
 #define RRA_SD(T)                                                                                  \
     do {                                                                                           \
-        sparse_dense_kernel<T><<<g1, kThreads, 0, st>>>(hdr, vals, n, acc, accumulate, vec);       \
-        sparse_tile_starts_kernel<<<gs, kThreads, 0, st>>>(hdr, idx, n, scratch, accumulate);      \
-        sparse_fill_kernel<T><<<gf, kThreads, 0, st>>>(hdr, vals, idx, scratch, n, acc,            \
-                                                       accumulate, vec);                           \
-        sparse_scatter_kernel<T><<<g2, kThreads, 0, st>>>(hdr, vals, idx, n, acc, accumulate);     \
+        if (accumulate) {                                                                          \
+            sparse_dense_kernel<T><<<g1, kThreads, 0, st>>>(hdr, vals, n, acc, vec);               \
+            sparse_scatter_kernel<T><<<g2, kThreads, 0, st>>>(hdr, vals, idx, n, acc);             \
+        } else {                                                                                   \
+            sparse_prep_kernel<T><<<g1, kThreads, 0, st>>>(hdr, vals, idx, n, acc, scratch, vec);  \
+            sparse_fill_kernel<T><<<gf, kThreads, 0, st>>>(hdr, vals, idx, scratch, n, acc, vec);  \
+        }                                                                                          \
     } while (0)
     if (dtype == kF32) RRA_SD(kF32);
     else if (dtype == kF16) RRA_SD(kF16);

@@ -666,6 +666,32 @@ def test_broadcast_codec_slice_widths_and_blocks(G):
     comm.close()
 
 
+@pytest.mark.parametrize("G", [0, 1, 2, 4])
+def test_broadcast_codec_f16_outputs_across_exponents(G):
+    """fp16 buffers of a BFP8 broadcast for block exponents from below the
+    fp16 subnormals to near the fp16 maximum, full slices and a ragged tail:
+    every rank (the root included) holds the decoded value rounded once to
+    fp16, the oracle's bits."""
+    N, T, root = 8, 4096 * 5 + 8 * 40 + 3, 2
+    g = torch.Generator(device="cuda")
+    g.manual_seed(90 + G)
+    lo, hi = -30, 13
+    nb = -(-T // 128)
+    j = (torch.arange(nb, device="cuda") * 5) % (hi - lo + 1) + lo
+    scale = torch.pow(2.0, j.float()).repeat_interleave(128)[:T]
+    bufs = [(torch.randn(T, generator=g, device="cuda") * scale).half() for _ in range(N)]
+    ref, s, r = O.broadcast_codec([host(b) for b in bufs], "f16", root, 8)
+    comm = rra.Comm(N, T, torch.float16)
+    if G:
+        comm.set_tuning(0, 0, 0, G)
+    comm.broadcast(bufs, root=root, codec=rra.Codec("bfp", bits=8))
+    assert comm.status() == rra.RRA_OK
+    for q in range(N):
+        assert_bits_equal(host(bufs[q]), ref[q], f"G={G} rank {q}")
+    assert comm.get_bytes() == (list(s), list(r))
+    comm.close()
+
+
 def test_broadcast_codec_misaligned_takes_generic_path():
     N, T, root = 4, 5000, 1
     store = cast(rand_f32(N, T + 1, seed=4, scale=1e-2), "f16")
