@@ -471,10 +471,11 @@ rra_status rra_autotune(rra_comm *comm, const void *const *in, void *const *out,
  * the tree variant, switch by size and measure the crossover).  The default
  * crossover follows the measurement on GB300 (lossless fp32 in place, 1 KiB
  * to 1 GiB per rank): for N = 2 and 4 the ring is never slower from 256 MiB
- * per rank on (RRA_DEFAULT_CROSSOVER); for N = 8, 16 and 64 the tree was the
- * faster at every measured size, so from N = 5 on the default sends every
- * message up to 1 GiB per rank to the tree (RRA_DEFAULT_CROSSOVER_WIDE, one
- * byte above the largest size measured). */
+ * per rank on (RRA_DEFAULT_CROSSOVER); for N = 8 and 64 the tree was the
+ * faster at every measured size, and for N = 16 the ring led by 2 % from 256
+ * MiB per rank, so from N = 5 on the default sends every message up to 1 GiB
+ * per rank to the tree (RRA_DEFAULT_CROSSOVER_WIDE, one byte above the
+ * largest size measured). */
 #define RRA_DEFAULT_CROSSOVER (256ull << 20)
 #define RRA_DEFAULT_CROSSOVER_WIDE ((1ull << 30) + 1)
 #define RRA_ALGO_RING 0

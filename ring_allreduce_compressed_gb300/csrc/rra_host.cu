@@ -223,6 +223,25 @@ bool pick_shape(rra_comm *c, const Tune &t, int N, long long n, int kc, int ies,
     const int want = warps >= 12 ? 2 : 3;
     const bool sparse = kc == kCodecSparse || kc == kCodecSparseChunk;
     const int sparse_kind = kc == kCodecSparse ? 1 : kc == kCodecSparseChunk ? 2 : 0;
+    // Lossless rings of 12 or more ranks (a launch-shape sweep at N = 12,
+    // 16, 32 and 64 found this 5-19 % faster than the rule below): two slots
+    // per edge and one stage; as many blocks as give 16 resident warps per
+    // SM (one block of 16 warps, two of 12 to 15), then the widest slice that
+    // fits them.
+    if (kc == kCodecNone && fast && warps >= 12 && !t.G && !t.K && !t.D) {
+        const int nb = warps >= 16 ? 1 : 2;
+        for (int G : {8, 4, 2, 1}) {
+            if (G > 1 && (n + (long long)kTile * G - 1) / ((long long)kTile * G) < sms)
+                continue;
+            const int slot = slot_bytes_for(kc, G, sparse_lim);
+            const int stage = kTile * G * (diff ? 8 : ies);
+            const Layout L = make_layout(N, 2, 1, slot, stage, warps, true, 0, false);
+            if (nb * (L.total + 1024) <= c->smem_per_sm && L.total <= c->smem_optin) {
+                *out = LaunchShape{G, 2, 1, L.total, true};
+                return true;
+            }
+        }
+    }
     // a requested slice width is tried first on its own; passes 2 and 3 are
     // the automatic choice
     for (int pass = t.G ? 0 : 2; pass < 4; ++pass) {
