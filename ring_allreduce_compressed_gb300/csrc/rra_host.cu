@@ -224,11 +224,16 @@ bool pick_shape(rra_comm *c, const Tune &t, int N, long long n, int kc, int ies,
     const bool sparse = kc == kCodecSparse || kc == kCodecSparseChunk;
     const int sparse_kind = kc == kCodecSparse ? 1 : kc == kCodecSparseChunk ? 2 : 0;
     // Lossless rings of 12 or more ranks (a launch-shape sweep at N = 12,
-    // 16, 32 and 64 found this 5-19 % faster than the rule below): two slots
-    // per edge and one stage; as many blocks as give 16 resident warps per
-    // SM (one block of 16 warps, two of 12 to 15), then the widest slice that
-    // fits them.
-    if (kc == kCodecNone && fast && warps >= 12 && !t.G && !t.K && !t.D) {
+    // 16, 32 and 64 found this 5-19 % faster than the rule below at N = 16 to
+    // 64 and as fast at N = 12): two slots per edge and one stage; as many
+    // blocks as give 16 resident warps per SM (one block of 16 warps, two of
+    // 12 to 15), then the widest slice that fits them and leaves every SM a
+    // slice position.  BFP rings of more ranks than warps keep the rule
+    // below: a variant of this one that also accepts one slice position per
+    // two SMs was 9-30 % faster at 4 Mi elements per rank and N = 32 and 64,
+    // but 7-8 % slower at N = 24 and at 16 Mi elements per rank, N = 32.
+    const bool wide = kc == kCodecNone && warps >= 12;
+    if (wide && fast && !t.G && !t.K && !t.D) {
         const int nb = warps >= 16 ? 1 : 2;
         for (int G : {8, 4, 2, 1}) {
             if (G > 1 && (n + (long long)kTile * G - 1) / ((long long)kTile * G) < sms)
