@@ -803,6 +803,18 @@ def run_codecs(args, world, rank):
     vals = torch.empty(n, dtype=torch.bfloat16, device="cuda")
     idx = torch.empty(n, dtype=torch.int32, device="cuda")
     rra.sparse_encode(xb, 0.5, hdr, vals, idx)
+    # a dense message (45 % zeros is below the threshold) for the dense path
+    # of the accumulating decoder
+    xd = torch.randn(n, generator=g, device="cuda")
+    xd[torch.rand(n, generator=g, device="cuda") < 0.45] = 0.0
+    xd = xd.bfloat16()
+    hdr_d = torch.empty(2, dtype=torch.int32, device="cuda")
+    vals_d = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    rra.sparse_encode(xd, 0.5, hdr_d, vals_d, idx)
+    del xd
+    torch.cuda.synchronize()
+    assert int(hdr_d[0]) == 0
+    rra.sparse_encode(xb, 0.5, hdr, vals, idx)  # idx again holds xb's indices
     torch.cuda.synchronize()
     fmt, nnz = [int(v) for v in hdr.cpu()]
     cur = torch.randn(n, generator=g, device="cuda")
@@ -822,15 +834,22 @@ def run_codecs(args, world, rank):
          2 * n + (6 * nnz if fmt else 2 * n)),
         ("sparse_decode -> f32", lambda: rra.sparse_decode(hdr, vals, idx, n, out32),
          (6 * nnz if fmt else 2 * n) + 4 * n),
+        # the listed values and indices read, acc read and written at each
+        ("sparse_decode accumulate f32", lambda: rra.sparse_decode(hdr, vals, idx, n, out32, True),
+         14 * nnz if fmt else 10 * n),
+        ("sparse_decode accumulate f32, dense message",
+         lambda: rra.sparse_decode(hdr_d, vals_d, idx, n, out32, True), 10 * n,
+         {"sparse_format": "dense", "nnz": n}),
         ("diff_encode f32", lambda: rra.diff_encode(cur, prev, diff), 12 * n),
     ]
     out = []
-    for name, fn, nbytes in cases:
+    for name, fn, nbytes, *extra in cases:
         us, how = time_op(fn, args.op_warmup, args.op_reps)
         line = {"codec_bench": True, "op": name, "n": n, "us": us, "timing": how, "bytes": nbytes,
                 "gbs": nbytes / (us * 1e-6) / 1e9,
                 "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peak, "peak_source": peak_src,
                 "sparse_format": "sparse" if fmt else "dense", "nnz": nnz}
+        line.update(*extra)
         out.append(line)
         print(json.dumps(line), flush=True)
     if args.jsonl:
@@ -908,7 +927,7 @@ def run_kernels(args, world, rank):
         # every buffer read once
         ("codec_stats_kernel", lambda: comm.codec_stats(bufs), 4 * N * T),
     ]
-    for name, fn, nbytes in cases:
+    for name, fn, nbytes, *extra in cases:
         us, how = time_op(fn, args.op_warmup, args.op_reps)
         assert comm.status() == rra.RRA_OK
         line = {"kernel_bench": True, "kernel": name, "N": N, "T": T, "us": us, "timing": how,

@@ -380,8 +380,8 @@ rra_status rra_sparse_encode_noalloc(const void *x, size_t n, rra_dtype dtype, f
 /*
  * Sparse decode into fp32 acc[0..n) (hdr, vals, idx as written by
  * rra_sparse_encode: indices ascending; the format is read on the device).
- * A sparse message without accumulation is restored in one pass over acc,
- * 4096 elements at a time, using a scratch of n/4096 + 1 words per device
+ * A sparse message is restored (or added) in one pass over acc, 4096
+ * elements at a time, using a scratch of n/4096 + 1 words per device
  * and stream that the library allocates on first use and grows as needed
  * (so the first call on a stream, or the first with a larger n, must not be
  * made during stream capture; decodes on different streams may overlap);

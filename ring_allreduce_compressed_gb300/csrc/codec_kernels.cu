@@ -585,35 +585,24 @@ __device__ __forceinline__ void dense_restore(const void *vals, long long n, flo
     }
 }
 
-// accumulate == 1: a dense message is added by the whole grid; a sparse one
-// is left to sparse_scatter_kernel.
-template <int IN_T>
-__global__ void __launch_bounds__(kThreads) sparse_dense_kernel(const uint32_t *__restrict__ hdr,
-                                                                const void *__restrict__ vals,
-                                                                long long n, float *__restrict__ acc,
-                                                                int vec)
-{
-    if (hdr[0] != 0u)
-        return;
-    dense_restore<IN_T>(vals, n, acc, 1, vec);
-}
-
-// accumulate == 0, in one pass over acc in 4096-element tiles.  This kernel:
-// a dense message is copied by the whole grid; for a sparse one, the
-// position in the (ascending) index list where each tile starts, one binary
-// search per tile and thread.  Then sparse_fill_kernel builds every tile of
-// a sparse message in shared memory (+0.0, then its values, read with
+// The decode is two kernels, one pass over acc in 4096-element tiles.  This
+// one: a dense message is copied (or added) by the whole grid; for a sparse
+// one, the position in the (ascending) index list where each tile starts,
+// one binary search per tile and thread.  Then sparse_fill_kernel builds
+// every tile of a sparse message in shared memory (+0.0, or acc's values
+// when accumulating, then the listed values set or added, read with
 // consecutive threads) and writes it once.  An index outside its tile (out
-// of order, or outside [0, n)) is never written.
+// of order, or outside [0, n)) is never used.
 template <int IN_T>
 __global__ void __launch_bounds__(kThreads) sparse_prep_kernel(const uint32_t *__restrict__ hdr,
                                                                const void *__restrict__ vals,
                                                                const int32_t *__restrict__ idx,
                                                                long long n, float *__restrict__ acc,
-                                                               uint32_t *__restrict__ start, int vec)
+                                                               uint32_t *__restrict__ start,
+                                                               int accumulate, int vec)
 {
     if (hdr[0] == 0u) {
-        dense_restore<IN_T>(vals, n, acc, 0, vec);
+        dense_restore<IN_T>(vals, n, acc, accumulate, vec);
         return;
     }
     const long long nnz = min((long long)hdr[1], n); // a header never lists more than n
@@ -646,7 +635,8 @@ __global__ void __launch_bounds__(kThreads) sparse_fill_kernel(const uint32_t *_
                                                                const void *__restrict__ vals,
                                                                const int32_t *__restrict__ idx,
                                                                const uint32_t *__restrict__ start,
-                                                               long long n, float *acc, int vec)
+                                                               long long n, float *acc,
+                                                               int accumulate, int vec)
 {
     using E = typename Elem<IN_T>::type;
     __shared__ __align__(16) float tile[kSpTile];
@@ -655,8 +645,10 @@ __global__ void __launch_bounds__(kThreads) sparse_fill_kernel(const uint32_t *_
     const long long tiles = (n + kSpTile - 1) / kSpTile;
     // The tile's listed (index, value) pairs k = kb + tid + kThreads*j are read
     // into registers one tile ahead: the next tile's loads are in flight
-    // while this tile is written out.  The tile buffer is +0.0 between tiles:
-    // each thread zeroes the words it has just written out.
+    // while this tile is written out.  Between tiles the buffer holds the
+    // next tile's base: +0.0 (each thread zeroes the words it has just
+    // written out) or, accumulating, acc's values (each thread loads the
+    // words of the next tile that it will write out itself).
     int32_t pi[kFillPairs];
     float pv[kFillPairs];
     long long kb = 0, ke = 0;
@@ -670,64 +662,71 @@ __global__ void __launch_bounds__(kThreads) sparse_fill_kernel(const uint32_t *_
             pv[j] = k < ke ? to_f32(reinterpret_cast<const E *>(vals)[k]) : 0.0f;
         }
     };
-    for (int i = threadIdx.x; i < kSpTile; i += kThreads)
-        tile[i] = 0.0f;
+    // this thread's words of tile t's base: acc's values accumulating, else +0.0
+    auto load_base = [&](long long t) {
+        const long long t0 = t * kSpTile;
+        const int len = (int)(min(n, t0 + kSpTile) - t0);
+        if (!accumulate) {
+            for (int i = threadIdx.x; i < kSpTile; i += kThreads)
+                tile[i] = 0.0f;
+        } else if (vec && len == kSpTile) {
+            const float4 *src = reinterpret_cast<const float4 *>(acc + t0);
+            for (int j = threadIdx.x; j < kSpTile / 4; j += kThreads)
+                reinterpret_cast<float4 *>(tile)[j] = src[j];
+        } else {
+            for (int j = threadIdx.x; j < len; j += kThreads)
+                tile[j] = acc[t0 + j];
+        }
+    };
     long long t = blockIdx.x;
-    if (t < tiles)
+    if (t < tiles) {
         fetch(t);
+        load_base(t);
+    }
     __syncthreads();
     for (; t < tiles; t += gridDim.x) {
         const long long t0 = t * kSpTile, t1 = min(n, t0 + kSpTile);
-        // scatter the pairs (an index outside the tile is never written)
+        // set or add the pairs (an index outside the tile is never used);
+        // the indices of one message are distinct, so no two threads touch
+        // one word
 #pragma unroll
         for (int j = 0; j < kFillPairs; ++j)
             if (pi[j] >= t0 && pi[j] < t1)
-                tile[pi[j] - t0] = pv[j];
+                tile[pi[j] - t0] = accumulate ? __fadd_rn(tile[pi[j] - t0], pv[j]) : pv[j];
         for (long long k = kb + threadIdx.x + (long long)kThreads * kFillPairs; k < ke;
              k += kThreads) {
             const long long i = idx[k];
-            if (i >= t0 && i < t1)
-                tile[i - t0] = to_f32(reinterpret_cast<const E *>(vals)[k]);
+            if (i >= t0 && i < t1) {
+                const float v = to_f32(reinterpret_cast<const E *>(vals)[k]);
+                tile[i - t0] = accumulate ? __fadd_rn(tile[i - t0], v) : v;
+            }
         }
         __syncthreads();
-        if (t + gridDim.x < tiles)
-            fetch(t + gridDim.x);
+        const long long tn = t + gridDim.x;
+        if (tn < tiles)
+            fetch(tn);
         const int len = (int)(t1 - t0);
-        if (vec && len == kSpTile) {
+        const long long tn0 = tn * kSpTile;
+        const bool next_full = tn < tiles && tn0 + kSpTile <= n;
+        if (vec && len == kSpTile && (!accumulate || tn >= tiles || next_full)) {
+            // every thread moves the same float4 words out and in
             float4 *dst = reinterpret_cast<float4 *>(acc + t0);
             for (int j = threadIdx.x; j < kSpTile / 4; j += kThreads) {
                 dst[j] = reinterpret_cast<const float4 *>(tile)[j];
-                reinterpret_cast<float4 *>(tile)[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                reinterpret_cast<float4 *>(tile)[j] =
+                    !accumulate ? make_float4(0.0f, 0.0f, 0.0f, 0.0f)
+                    : tn < tiles ? reinterpret_cast<const float4 *>(acc + tn0)[j]
+                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
         } else {
             for (int j = threadIdx.x; j < len; j += kThreads)
                 acc[t0 + j] = tile[j];
-            for (int j = threadIdx.x; j < kSpTile; j += kThreads)
-                tile[j] = 0.0f;
+            if (tn < tiles) {
+                __syncthreads(); // the element loop above maps threads differently
+                load_base(tn);
+            }
         }
-        __syncthreads(); // the tile is +0.0 again before the next scatter
-    }
-}
-
-// accumulate == 1, sparse message: acc[i] += v at the listed positions
-// (a dense one is added by sparse_dense_kernel).
-template <int IN_T>
-__global__ void __launch_bounds__(kThreads) sparse_scatter_kernel(const uint32_t *__restrict__ hdr,
-                                                                  const void *__restrict__ vals,
-                                                                  const int32_t *__restrict__ idx,
-                                                                  long long n, float *acc)
-{
-    using E = typename Elem<IN_T>::type;
-    if (hdr[0] == 0u)
-        return;
-    const long long nnz = min((long long)hdr[1], n); // a header never lists more than n
-    for (long long k = blockIdx.x * (long long)kThreads + threadIdx.x; k < nnz;
-         k += (long long)gridDim.x * kThreads) {
-        const long long i = idx[k];
-        if (i < 0 || i >= n)
-            continue; // malformed index: skip rather than write out of bounds
-        const float v = to_f32(reinterpret_cast<const E *>(vals)[k]);
-        acc[i] = __fadd_rn(acc[i], v);
+        __syncthreads(); // the tile holds the next base before the next scatter
     }
 }
 
@@ -1007,19 +1006,15 @@ cudaError_t launch_sparse_decode(const uint32_t *hdr, const void *vals, const in
     // the dense stream's grid; its threads also cover the tiles + 1 starts
     const long long tiles = (n + kSpTile - 1) / kSpTile;
     const int g1 = grid_for((n + 7) / 8, kThreads);
-    const int g2 = num_sms() * 4;
     const int gf = (int)std::min<long long>(tiles, (long long)num_sms() * 8);
-    // the format is in the device header, so each path launches both of its
-    // kernels and the one that does not apply returns at once
+    // the format is in the device header: for a dense message the first
+    // kernel does all the work and the fill returns at once
 #define RRA_SD(T)                                                                                  \
     do {                                                                                           \
-        if (accumulate) {                                                                          \
-            sparse_dense_kernel<T><<<g1, kThreads, 0, st>>>(hdr, vals, n, acc, vec);               \
-            sparse_scatter_kernel<T><<<g2, kThreads, 0, st>>>(hdr, vals, idx, n, acc);             \
-        } else {                                                                                   \
-            sparse_prep_kernel<T><<<g1, kThreads, 0, st>>>(hdr, vals, idx, n, acc, scratch, vec);  \
-            sparse_fill_kernel<T><<<gf, kThreads, 0, st>>>(hdr, vals, idx, scratch, n, acc, vec);  \
-        }                                                                                          \
+        sparse_prep_kernel<T><<<g1, kThreads, 0, st>>>(hdr, vals, idx, n, acc, scratch,            \
+                                                       accumulate ? 1 : 0, vec);                   \
+        sparse_fill_kernel<T><<<gf, kThreads, 0, st>>>(hdr, vals, idx, scratch, n, acc,            \
+                                                       accumulate ? 1 : 0, vec);                   \
     } while (0)
     if (dtype == kF32) RRA_SD(kF32);
     else if (dtype == kF16) RRA_SD(kF16);

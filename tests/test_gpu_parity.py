@@ -803,6 +803,15 @@ def test_sparse_codec_many_tiles(dt, offset):
     rra.sparse_decode(hdr, vals, idx, n, acc)
     assert_bits_equal(host(acc), O.sparse_decode(rh, rv, ri, n, dt), "decode")
     assert float(store[0]) == 3.0 or offset == 0
+    # accumulating, tile by tile, onto a base with no zeros (the last tile is
+    # ragged, so the whole-tile and element paths both run)
+    base = torch.randn(n, generator=torch.Generator(device="cuda").manual_seed(5), device="cuda")
+    acc.copy_(base)
+    rra.sparse_decode(hdr, vals, idx, n, acc, accumulate=True)
+    ra = host(base).copy()
+    O.sparse_decode(rh, rv, ri, n, dt, acc=ra, accumulate=True)
+    assert_bits_equal(host(acc), ra, "decode accumulate")
+    assert float(store[0]) == 3.0 or offset == 0
 
 
 def _encode_and_check(x, dt, thr, stream=None):
