@@ -366,8 +366,7 @@ rra_status rra_sparse_encode(const void *x, size_t n, rra_dtype dtype, float thr
  *  - the first call on a device looks up the scratch array's device address
  *    (cudaGetSymbolAddress) with that device current, and keeps it for the
  *    rest of the process; after cudaDeviceReset the function must not be
- *    called again.  Make the first call on each device before starting any
- *    stream capture.
+ *    called again.
  *  - all calls on a device share the one scratch array.  A call writes
  *    every scratch word it reads before reading it, so nothing needs
  *    clearing, before the first call or between calls; calls that overlap
