@@ -109,6 +109,26 @@ def test_lossless_ring_shapes(N, T):
     compare(run_ring(xs, "f32"), oracle_ring(xs, "f32", "f32"), f"N={N} T={T}")
 
 
+@pytest.mark.parametrize("N,n,G", [(12, 152 * 512, 2), (16, 152 * 1024, 4), (32, 152 * 512, 2)])
+def test_lossless_wide_default_shape(N, n, G):
+    """Lossless rings of 12 or more ranks on the staged path take two slots
+    per edge, one stage and the widest slice that leaves every SM a slice
+    position and fits 16 resident warps per SM (one block of 16 warps, two
+    of 12); bit-exact in ring order."""
+    T = N * n
+    xs = rand_f32(N, T, seed=N + G)
+    comm = rra.Comm(N, T)
+    outs = [torch.empty_like(x) for x in xs]
+    comm.ring_allreduce(xs, outs)
+    assert comm.status() == rra.RRA_OK
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert comm.last_shape()[1:] == (2, 1, G)
+    sent, recv = comm.get_bytes()
+    comm.close()
+    compare((outs, np.array(sent, np.uint64), np.array(recv, np.uint64)),
+            oracle_ring(xs, "f32", "f32"), f"N={N} wide default")
+
+
 @pytest.mark.parametrize("in_dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("out_dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("T", [4096 * 3, 5003])
