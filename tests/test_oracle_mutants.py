@@ -8,7 +8,10 @@ owner that keeps its input in the compressed allgather, a root that keeps its in
 in the compressed broadcast, a dropped base or average in the difference epilogue,
 swapped or unsigned BFP4 nibbles, -0.0 taken for a zero, a chunk's sparse
 message cut into 256-element pieces, sparse values restored at the wrong
-index, a receiver that adds only nonzero message values); the mutated copy
+index, a receiver that adds only nonzero message values, standalone decoders
+that overwrite instead of adding or keep acc where they should clear it, a
+shifted sparse index, a broadcast that ignores its root, a swapped standalone
+difference); the mutated copy
 is compiled into a temporary directory and the pin suite is run against it in
 a child process.  The real oracle is never modified."""
 import os
@@ -56,6 +59,14 @@ MUTANTS = {
     "sparse_restored_at_wrong_index": ("m->f[lo + (size_t)pi[k]] = pv[k];", "m->f[lo + k] = pv[k];", 1),
     "receiver_skips_zero_values": ("local[r][lo + i] = local[r][lo + i] + v; /* S4 */",
                                    "if (is_nonzero(v)) local[r][lo + i] = local[r][lo + i] + v; /* S4 */", 1),
+    "bfp_decode_accumulate_overwrites": ("out[i] = accumulate ? out[i] + v : v;", "out[i] = v;", 1),
+    "sparse_dense_accumulate_overwrites": ("acc[i] = accumulate ? acc[i] + v : v;", "acc[i] = v;", 1),
+    "sparse_listed_accumulate_overwrites": ("acc[i] = accumulate ? acc[i] + v : v;", "acc[i] = v;", 2),
+    "sparse_decode_keeps_acc": ("    if (!accumulate)\n        for (size_t i = 0; i < n; i++)\n            acc[i] = 0.0f;",
+                                "    if (0)\n        for (size_t i = 0; i < n; i++)\n            acc[i] = 0.0f;", 1),
+    "sparse_encode_index_shift": ("idx[k] = (int32_t)i;", "idx[k] = (int32_t)(i + 1);", 1),
+    "broadcast_ignores_root": ("int src = (q + root) % N, dst = (qd + root) % N;", "int src = q, dst = qd;", 1),
+    "diff_encode_swapped": ("diff[i] = cur[i] - prev[i];", "diff[i] = prev[i] - cur[i];", 1),
     "agc_owner_keeps_input": ("/* the owner's own chunk becomes the decoded codes as well */\n    for (int r = 0; r < N; r++) {",
                               "/* the owner's own chunk becomes the decoded codes as well */\n    for (int r = 0; r < 0; r++) {", 1),
 }

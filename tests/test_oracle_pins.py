@@ -553,6 +553,29 @@ def test_sparse_keeps_input_dtype(dt):
     assert list(acc) == [1, 1, 2.5, 1, -1.25, 1, 1, 1, 1, 4.0]
 
 
+def test_sparse_decode_overwrites_or_adds_by_hand():
+    """Without accumulation the restored message replaces acc (+0.0 where a
+    sparse message lists nothing); with it every carried value is added: a
+    sparse message adds at its listed positions only, a dense one everywhere
+    (the values below are exact in fp32, so the sums are by hand)."""
+    garbage = np.full(6, 7.0, np.float32)
+    # sparse: two values listed at 1 and 4
+    hdr = np.array([1, 2], np.uint32)
+    vals = np.array([0.5, -3.0], np.float32)
+    idx = np.array([1, 4], np.int32)
+    got = O.sparse_decode(hdr, vals, idx, 6, acc=garbage.copy())
+    assert list(got) == [0.0, 0.5, 0.0, 0.0, -3.0, 0.0]
+    got = O.sparse_decode(hdr, vals, idx, 6, acc=garbage.copy(), accumulate=True)
+    assert list(got) == [7.0, 7.5, 7.0, 7.0, 4.0, 7.0]
+    # dense: all six values
+    hdr = np.array([0, 6], np.uint32)
+    vals = np.array([1.0, 0.0, -2.0, 0.25, 0.0, 3.0], np.float32)
+    got = O.sparse_decode(hdr, vals, np.zeros(0, np.int32), 6, acc=garbage.copy())
+    assert list(got) == [1.0, 0.0, -2.0, 0.25, 0.0, 3.0]
+    got = O.sparse_decode(hdr, vals, np.zeros(0, np.int32), 6, acc=garbage.copy(), accumulate=True)
+    assert list(got) == [8.0, 7.0, 5.0, 7.25, 7.0, 10.0]
+
+
 # --------------------------------------------------------------- diff
 
 def test_diff_encode():
