@@ -11,7 +11,8 @@ message cut into 256-element pieces, sparse values restored at the wrong
 index, a receiver that adds only nonzero message values, standalone decoders
 that overwrite instead of adding or keep acc where they should clear it, a
 shifted sparse index, a broadcast that ignores its root, a swapped standalone
-difference); the mutated copy
+difference, either chunk index of the plain allgather, chunks of floor(T/N)
+elements, a tree that counts half its bytes); the mutated copy
 is compiled into a temporary directory and the pin suite is run against it in
 a child process.  The real oracle is never modified."""
 import os
@@ -67,6 +68,10 @@ MUTANTS = {
     "sparse_encode_index_shift": ("idx[k] = (int32_t)i;", "idx[k] = (int32_t)(i + 1);", 1),
     "broadcast_ignores_root": ("int src = (q + root) % N, dst = (qd + root) % N;", "int src = q, dst = qd;", 1),
     "diff_encode_swapped": ("diff[i] = cur[i] - prev[i];", "diff[i] = prev[i] - cur[i];", 1),
+    "plain_ag_send_index": ("int c = mod((long)r - s + 1, N);", "int c = mod((long)r - s, N);", 1),
+    "plain_ag_recv_index": ("int c = mod((long)r - s, N);", "int c = mod((long)r - s + 1, N);", 3),
+    "chunk_len_floor": ("size_t n = (T + (size_t)N - 1) / (size_t)N; /* R3 */", "size_t n = T / (size_t)N; /* R3 */", 1),
+    "tree_bytes_halved": ("            sent[src] += 4 * T;", "            sent[src] += 2 * T;", 1),
     "agc_owner_keeps_input": ("/* the owner's own chunk becomes the decoded codes as well */\n    for (int r = 0; r < N; r++) {",
                               "/* the owner's own chunk becomes the decoded codes as well */\n    for (int r = 0; r < 0; r++) {", 1),
 }
