@@ -755,44 +755,19 @@ __global__ void __launch_bounds__(kThreads) diff_kernel(const float *cur, const 
 }
 
 // ---------------------------------------------------------------- codec statistics
-// One warp per 128-element BFP block (4 elements a lane).  Blocks are cut
-// from the start of each ring chunk of every rank's buffer, as the ring's
-// first hop encodes them.  A nonzero element (fp32 bits not +0.0) is flushed
-// by a BFP code of q = bits - 2 fraction bits when it rounds to code 0, that
-// is when |x| <= 2^(e - q - 1) for the block exponent e.
+// One warp per 256-element tile: two 128-element BFP blocks, one per
+// half-warp, 8 elements a lane.  Blocks are cut from the start of each ring
+// chunk of every rank's buffer, as the ring's first hop encodes them.  A
+// nonzero element (fp32 bits not +0.0) is flushed by a BFP code of q =
+// bits - 2 fraction bits when it rounds to code 0, that is when
+// |x| <= 2^(e - q - 1) for the block exponent e.
 // Grid: blockIdx.y = r * N + c (rank r, chunk c); the blocks along x stride
-// over the chunk's 128-element blocks, a warp at a time, so no index needs a
-// division.
+// over the chunk's tiles, a warp at a time, so no index needs a division.
 
 // 2^k as an fp32 value for k in [-149, 127] (subnormal below -126).
 __device__ __forceinline__ float pow2_exact(int k)
 {
     return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(1 << (k + 149));
-}
-
-// 4 elements of dtype IN_T at p widened to fp32; the first `valid` are read
-// (vec: all 4 present and p aligned to 4 elements)
-template <int IN_T>
-__device__ __forceinline__ void load4(const void *p, int valid, bool vec, float v[4])
-{
-    using E = typename Elem<IN_T>::type;
-    if (vec && valid == 4) {
-        if constexpr (IN_T == kF32) {
-            const float4 x = __ldg(reinterpret_cast<const float4 *>(p));
-            v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-        } else {
-            const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
-            const E *e = reinterpret_cast<const E *>(&u);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                v[i] = to_f32(e[i]);
-        }
-        return;
-    }
-    const E *e = reinterpret_cast<const E *>(p);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        v[i] = i < valid ? to_f32(e[i]) : 0.0f;
 }
 
 template <int IN_T>
@@ -803,38 +778,47 @@ __global__ void __launch_bounds__(kThreads) codec_stats_kernel(const __grid_cons
     const int lane = threadIdx.x & 31;
     const int r = (int)(blockIdx.y / (unsigned)a.N), c = (int)(blockIdx.y % (unsigned)a.N);
     const long long lo = min(a.T, (long long)c * a.n), hi = min(a.T, lo + a.n);
-    const char *base = reinterpret_cast<const char *>(a.in[r]);
+    const long long len = hi - lo;
+    const char *base = reinterpret_cast<const char *>(a.in[r]) + lo * es;
     uint32_t cnt_nz = 0, cnt_f4 = 0, cnt_f8 = 0;
-    // kStatsU blocks per warp and iteration, all loaded before any is
-    // reduced, so that every lane keeps kStatsU loads in flight
-    constexpr int kStatsU = 4;
-    const long long step = (long long)gridDim.x * (kThreads / 32) * kBlock;
-    for (long long e0 = lo + ((long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kBlock;
-         e0 < hi; e0 += kStatsU * step) {
-        float v[kStatsU][4];
+    // kStatsU tiles per warp and iteration, all loaded before any is
+    // counted, so that every lane keeps kStatsU loads in flight
+    constexpr int kStatsU = 2;
+    const long long step = (long long)gridDim.x * (kThreads / 32) * kTile;
+    for (long long w0 = ((long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kTile;
+         w0 < len; w0 += kStatsU * step) {
+        float v[kStatsU][8];
 #pragma unroll
         for (int u = 0; u < kStatsU; ++u) {
-            const long long eu = e0 + u * step;
-            const int len = (int)min((long long)kBlock, max(hi - eu, 0LL));
-            const int valid = min(max(len - 4 * lane, 0), 4);
-            load4<IN_T>(base + (eu + 4 * lane) * es, valid, vec != 0, v[u]);
+            const long long e = w0 + u * step + 8 * lane; // chunk-relative
+            const int valid = (int)min(max(len - e, 0LL), 8LL);
+            if (vec && valid == 8)
+                load8_vec<IN_T>(base + e * es, v[u]);
+            else
+                load8_scalar<IN_T>(base + e * es, valid, v[u]); // +0.0 past the end
         }
 #pragma unroll
         for (int u = 0; u < kStatsU; ++u) {
-            if (e0 + u * step >= hi) // (warp-uniform)
+            if (w0 + u * step >= len) // (warp-uniform)
                 break;
+            // the half-warp's block maximum: non-negative floats order like
+            // their bit patterns
             unsigned mx = 0;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i)
                 mx = max(mx, __float_as_uint(v[u][i]) & 0x7fffffffu);
-            mx = __reduce_max_sync(kFull, mx);
-            const int e = max((int)(mx >> 23), 1) - 127;
-            const float t4 = pow2_exact(e - 3), t8 = pow2_exact(e - 7);
+            const unsigned m_lo = __reduce_max_sync(kFull, lane < 16 ? mx : 0u);
+            const unsigned m_hi = __reduce_max_sync(kFull, lane < 16 ? 0u : mx);
+            const int e = max((int)((lane < 16 ? m_lo : m_hi) >> 23), 1) - 127;
+            // |x| <= 2^k as bit patterns (both non-negative)
+            const unsigned t4 = __float_as_uint(pow2_exact(e - 3));
+            const unsigned t8 = __float_as_uint(pow2_exact(e - 7));
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 // absent positions read +0.0: never counted
-                const bool nz = __float_as_uint(v[u][i]) != 0u;
-                const float m = fabsf(v[u][i]);
+                const unsigned b = __float_as_uint(v[u][i]);
+                const unsigned m = b & 0x7fffffffu;
+                const bool nz = b != 0u;
                 cnt_nz += nz ? 1u : 0u;
                 cnt_f4 += nz && m <= t4 ? 1u : 0u;
                 cnt_f8 += nz && m <= t8 ? 1u : 0u;
@@ -864,12 +848,12 @@ __global__ void __launch_bounds__(kThreads) codec_stats_kernel(const __grid_cons
 cudaError_t launch_codec_stats(const StatsArgs &a, int dtype, cudaStream_t st)
 {
     // y: (rank, chunk); x: enough blocks of 8 warps for about 16 blocks per SM
-    const long long nb = (a.n + kBlock - 1) / kBlock;
-    const long long per_chunk = (nb + kThreads / 32 - 1) / (kThreads / 32);
+    const long long nt = (a.n + kTile - 1) / kTile; // 256-element tiles per chunk
+    const long long per_chunk = (nt + kThreads / 32 - 1) / (kThreads / 32);
     const long long want = std::max(1LL, (long long)num_sms() * 16 / ((long long)a.N * a.N));
     const dim3 grid((unsigned)std::max(1LL, std::min(per_chunk, want)), (unsigned)(a.N * a.N));
     const int es = dtype == kF32 ? 4 : 2;
-    int vec = (a.n * es) % 16 == 0 ? 1 : 0; // 4-element runs aligned in every chunk
+    int vec = (a.n * es) % 16 == 0 ? 1 : 0; // 8-element runs aligned in every chunk
     for (int r = 0; r < a.N; ++r)
         vec = vec && aligned16(a.in[r]);
     if (dtype == kF32)
